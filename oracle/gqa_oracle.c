@@ -1,0 +1,547 @@
+/*
+ * gqa_oracle.c -- plain, slow, fp64 CPU oracle for the forward pass of a
+ * grouped-query attention layer whose head_dim is set independently of
+ * hidden / num_heads (Qwen3-style attention).
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only the test suite, the smoke check and the
+ * benchmark's CPU-baseline leg load this file.  The product (the CUDA
+ * library) neither links nor calls it, and this file shares no code, header
+ * or table with it.
+ *
+ * Conventions
+ *   - Every tensor input is bf16 (IEEE binary32 with the low 16 bits
+ *     dropped), passed as uint16_t bit patterns, and widened to double
+ *     exactly.  All arithmetic is double; nothing is rounded in between.
+ *   - Loops follow the definitions in the order the pages state them; the
+ *     only liberty taken is running independent output rows on OpenMP
+ *     threads, which does not change any single row's arithmetic.
+ *   - Sources are cited as: page title, section.
+ *       [NeoX]  "Support explicit attention head_dim independent of
+ *                hidden_size / num_attention_heads" (GPT-NeoX issue 1434)
+ *       [T07]   "Tutorial 07: Multi-Head and Grouped-Query Attention (Full Layer)"
+ *       [Knob]  "num_heads Is Not a Capacity Knob"
+ *       [Part]  "Attention head partitions: keep each head's dependencies intact"
+ *
+ * Readings taken where the pages are silent (each is pinned by a test in
+ * tests/test_oracle_pins.py, and listed with its reason in the design notes):
+ *   R1 fused weight row order: all Q heads, then all K heads, then all V heads
+ *      ([NeoX] "Fused QKV projection": the fused output is
+ *      query_hidden_size + 2*kv_hidden_size; [NeoX] "Checkpoint conversion"
+ *      gives q_proj/k_proj/v_proj as separate [out, hidden] matrices).
+ *   R2 query head j uses KV head g = j / (Hq/Hkv) (contiguous groups;
+ *      [NeoX] "Qwen3-0.6B example": each KV head serves 2 query heads).
+ *   R3 RMSNorm(v) = v * w / sqrt(mean(v^2) + eps), mean over head_dim.
+ *   R4 RoPE pairs element i with element i + d/2 ("rotate half"), angle
+ *      pos * theta^(-2i/d), applied to Q and K only ([T07] §3-§4).
+ *   R5 causal: query at position t sees keys u <= t, the diagonal included.
+ *   R6 out = x + o_proj(attn) ([NeoX] "Qwen3-0.6B example": residual addition).
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#define ORACLE_OK 0
+#define ORACLE_EARG (-1)
+#define ORACLE_ENOMEM (-2)
+
+/* bf16 bit pattern -> double.  Exact: a bf16 value is a binary32 value. */
+static double bf(uint16_t h)
+{
+    uint32_t u = ((uint32_t)h) << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+static void set_threads(int nthreads)
+{
+#ifdef _OPENMP
+    if (nthreads > 0) omp_set_num_threads(nthreads);
+#else
+    (void)nthreads;
+#endif
+}
+
+/* ------------------------------------------------------------------------ */
+/* Shape and cost arithmetic ([NeoX] "Proposed implementation",
+ * [Knob] "Why the cost does not move", "Where the invariance breaks").     */
+/* ------------------------------------------------------------------------ */
+
+/* Effective head width: explicit value, else hidden // heads
+ * ([NeoX] "Proposed configuration behavior").  Returns -1 when it has to be
+ * derived and hidden is not divisible by heads. */
+long oracle_effective_head_dim(long hidden, long heads, long head_dim_or_0)
+{
+    if (head_dim_or_0 > 0) return head_dim_or_0;
+    if (heads <= 0 || hidden % heads != 0) return -1;
+    return hidden / heads;
+}
+
+/* Widths of the projections ([NeoX] "Proposed implementation", "Fused QKV
+ * projection", "Output projection"):
+ *   out[0] = query_hidden = Hq*d, out[1] = kv_hidden = Hkv*d,
+ *   out[2] = fused QKV output width = Hq*d + 2*Hkv*d,
+ *   out[3] = o_proj input width = Hq*d, out[4] = o_proj output = hidden. */
+void oracle_widths(long hidden, long Hq, long Hkv, long d, long *out)
+{
+    out[0] = Hq * d;
+    out[1] = Hkv * d;
+    out[2] = Hq * d + 2 * Hkv * d;
+    out[3] = Hq * d;
+    out[4] = hidden;
+}
+
+/* Weight count of q_proj, k_proj, v_proj and o_proj
+ * ([Knob] "Why the cost does not move": 4*d_model^2 when d = d_model/h;
+ * "Where the invariance breaks": more when d is pinned). */
+long long oracle_attn_param_count(long hidden, long Hq, long Hkv, long d)
+{
+    long long h = hidden;
+    return h * (long long)(Hq * d) + 2 * h * (long long)(Hkv * d) + (long long)(Hq * d) * h;
+}
+
+/* Projection multiply-accumulates per token: every weight is used once per
+ * token ([Knob] "Why the cost does not move", the 1,048,576 at d_model 512). */
+long long oracle_proj_macs_per_token(long hidden, long Hq, long Hkv, long d)
+{
+    return oracle_attn_param_count(hidden, Hq, Hkv, d);
+}
+
+/* Score + value multiply-accumulates per query token over n keys: each
+ * query head does n*d for the scores and n*d for the value average
+ * ([Knob] "Why the cost does not move": 2*n*h*d_k). */
+long long oracle_score_value_macs_per_token(long n, long Hq, long d)
+{
+    return 2LL * n * Hq * d;
+}
+
+/* ------------------------------------------------------------------------ */
+/* The steps of the layer, one function each.                                */
+/* ------------------------------------------------------------------------ */
+
+/* y[n] = sum_k xrow[k] * W[n][k]  for n in [n0, n0+nn): one row of x @ W^T
+ * (W stored [out, in]: [NeoX] "Checkpoint conversion"; [T07] §4 step 1,
+ * "Each projection is a linear layer: x @ W^T"). */
+static void linear_row(const uint16_t *xrow, const uint16_t *W, long n0, long nn,
+                       long K, double *y)
+{
+    for (long n = 0; n < nn; ++n) {
+        const uint16_t *w = W + (n0 + n) * K;
+        double s = 0.0;
+        for (long k = 0; k < K; ++k) s += bf(xrow[k]) * bf(w[k]);
+        y[n] = s;
+    }
+}
+
+/* RMSNorm over one head vector of length d, in place (reading R3):
+ * v <- v * w / sqrt(mean(v^2) + eps)   ([T07] §3 "QK-Norm"). */
+static void rmsnorm_head(double *v, long d, const uint16_t *w, double eps)
+{
+    double ms = 0.0;
+    for (long i = 0; i < d; ++i) ms += v[i] * v[i];
+    ms /= (double)d;
+    double r = 1.0 / sqrt(ms + eps);
+    for (long i = 0; i < d; ++i) v[i] = v[i] * r * bf(w[i]);
+}
+
+/* RoPE on one head vector at position pos, in place (reading R4):
+ * for i < d/2, angle f = pos * theta^(-2i/d),
+ *   (v[i], v[i+d/2]) <- (v[i] cos f - v[i+d/2] sin f, v[i+d/2] cos f + v[i] sin f)
+ * ([T07] §4 "Set up RoPE" from (head_dim, max_position, rope_theta);
+ *  [NeoX] "Scaling and RoPE": built from the effective head_dim). */
+static void rope_head(double *v, long d, double pos, double theta)
+{
+    long half = d / 2;
+    for (long i = 0; i < half; ++i) {
+        double f = pos * pow(theta, -2.0 * (double)i / (double)d);
+        double c = cos(f), s = sin(f);
+        double a = v[i], b = v[i + half];
+        v[i] = a * c - b * s;
+        v[i + half] = b * c + a * s;
+    }
+}
+
+/* Exported single-row helpers so the pins can test each step alone. */
+int oracle_rmsnorm_rows(const double *in, long nrows, long d, const uint16_t *w,
+                        double eps, double *out)
+{
+    if (!in || !out || !w || nrows < 0 || d <= 0) return ORACLE_EARG;
+    for (long r = 0; r < nrows; ++r) {
+        memcpy(out + r * d, in + r * d, (size_t)d * sizeof(double));
+        rmsnorm_head(out + r * d, d, w, eps);
+    }
+    return ORACLE_OK;
+}
+
+int oracle_rope_rows(const double *in, long nrows, long d, const double *pos,
+                     double theta, double *out)
+{
+    if (!in || !out || !pos || nrows < 0 || d <= 0 || (d & 1)) return ORACLE_EARG;
+    for (long r = 0; r < nrows; ++r) {
+        memcpy(out + r * d, in + r * d, (size_t)d * sizeof(double));
+        rope_head(out + r * d, d, pos[r], theta);
+    }
+    return ORACLE_OK;
+}
+
+int oracle_linear(const uint16_t *x, const uint16_t *W, long M, long N, long K,
+                  double *y, int nthreads)
+{
+    if (!x || !W || !y || M < 0 || N <= 0 || K <= 0) return ORACLE_EARG;
+    set_threads(nthreads);
+#pragma omp parallel for schedule(dynamic, 1)
+    for (long m = 0; m < M; ++m) linear_row(x + m * K, W, 0, N, K, y + m * N);
+    return ORACLE_OK;
+}
+
+/* One query row of grouped-query attention ([T07] §4 step 6, computed in
+ * full precision; [NeoX] "Scaling and RoPE": scale head_dim^-0.5;
+ * [Part]: every query head sees all permitted keys of its KV group):
+ *   s_u = <q, k_u> / sqrt(d) for the visible keys u in [0, n_vis),
+ *   o   = sum_u softmax(s)_u v_u.
+ * kget/vget address key u of the group; q and o have length d.
+ * The maximum is subtracted before exp, which leaves softmax unchanged. */
+typedef struct {
+    const uint16_t *kb;   /* bf16 keys, row stride d, or NULL */
+    const uint16_t *vb;
+    const double *kd;     /* double keys (used for keys >= n_bf16), or NULL */
+    const double *vd;
+    long n_bf16;          /* keys [0, n_bf16) come from kb/vb, the rest from kd/vd */
+} kv_src;
+
+static double key_at(const kv_src *s, long u, long c, long d)
+{
+    return (u < s->n_bf16) ? bf(s->kb[u * d + c]) : s->kd[(u - s->n_bf16) * d + c];
+}
+static double val_at(const kv_src *s, long u, long c, long d)
+{
+    return (u < s->n_bf16) ? bf(s->vb[u * d + c]) : s->vd[(u - s->n_bf16) * d + c];
+}
+
+static int attend_row(const double *q, const kv_src *src, long n_vis, long d, double *o)
+{
+    double *s = (double *)malloc((size_t)(n_vis > 0 ? n_vis : 1) * sizeof(double));
+    if (!s) return ORACLE_ENOMEM;
+    double scale = 1.0 / sqrt((double)d);
+    double mx = -INFINITY;
+    for (long u = 0; u < n_vis; ++u) {
+        double dot = 0.0;
+        for (long c = 0; c < d; ++c) dot += q[c] * key_at(src, u, c, d);
+        s[u] = dot * scale;
+        if (s[u] > mx) mx = s[u];
+    }
+    double den = 0.0;
+    for (long u = 0; u < n_vis; ++u) {
+        s[u] = exp(s[u] - mx);
+        den += s[u];
+    }
+    for (long c = 0; c < d; ++c) o[c] = 0.0;
+    for (long u = 0; u < n_vis; ++u) {
+        double p = s[u] / den;
+        for (long c = 0; c < d; ++c) o[c] += p * val_at(src, u, c, d);
+    }
+    free(s);
+    return ORACLE_OK;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Stage 1: QKV projection + QK-norm + RoPE, for every token.               */
+/* ------------------------------------------------------------------------ */
+
+/* q_out [B,Hq,S,d], k_out/v_out [B,Hkv,S,d] (head-major, [T07] §4 step 4).
+ * q_norm_w/k_norm_w both NULL means no QK-norm.  Positions are 0..S-1. */
+int oracle_qkv_stage(const uint16_t *x, const uint16_t *Wqkv,
+                     const uint16_t *q_norm_w, const uint16_t *k_norm_w,
+                     double rope_theta, double eps,
+                     long B, long S, long hidden, long Hq, long Hkv, long d,
+                     double *q_out, double *k_out, double *v_out, int nthreads)
+{
+    if (!x || !Wqkv || !q_out || !k_out || !v_out) return ORACLE_EARG;
+    if (B <= 0 || S <= 0 || hidden <= 0 || Hq <= 0 || Hkv <= 0 || d <= 0 || (d & 1)) return ORACLE_EARG;
+    if ((q_norm_w == NULL) != (k_norm_w == NULL)) return ORACLE_EARG;
+    long NQ = Hq * d, NKV = Hkv * d, N = NQ + 2 * NKV;
+    int err = ORACLE_OK;
+    set_threads(nthreads);
+#pragma omp parallel for schedule(dynamic, 1)
+    for (long m = 0; m < B * S; ++m) {
+        long b = m / S, t = m % S;
+        double *row = (double *)malloc((size_t)N * sizeof(double));
+        if (!row) { err = ORACLE_ENOMEM; continue; }
+        /* step 1: fused projection, rows of Wqkv = [W_q; W_k; W_v] (R1) */
+        linear_row(x + m * hidden, Wqkv, 0, N, hidden, row);
+        for (long j = 0; j < Hq; ++j) {
+            double *v = row + j * d;
+            if (q_norm_w) rmsnorm_head(v, d, q_norm_w, eps);   /* step 2 */
+            rope_head(v, d, (double)t, rope_theta);             /* step 3 */
+            memcpy(q_out + ((b * Hq + j) * S + t) * d, v, (size_t)d * sizeof(double));
+        }
+        for (long g = 0; g < Hkv; ++g) {
+            double *v = row + NQ + g * d;
+            if (k_norm_w) rmsnorm_head(v, d, k_norm_w, eps);
+            rope_head(v, d, (double)t, rope_theta);
+            memcpy(k_out + ((b * Hkv + g) * S + t) * d, v, (size_t)d * sizeof(double));
+            memcpy(v_out + ((b * Hkv + g) * S + t) * d, row + NQ + NKV + g * d,
+                   (size_t)d * sizeof(double));
+        }
+        free(row);
+    }
+    return err;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Stage 2: causal grouped-query attention over bf16 Q/K/V.                 */
+/* ------------------------------------------------------------------------ */
+
+/* Q [B,Hq,S,d], K/V [B,Hkv,S,d] bf16.  attn [n_sel, Hq*d] for the selected
+ * tokens sel[i] = b*S + t (flattened, [T07] §4 step 7 "(batch, seq,
+ * heads*head_dim)"; [NeoX] "Attention output flattening").  sel == NULL
+ * means every token in order (n_sel must then be B*S). */
+int oracle_attention_stage(const uint16_t *Q, const uint16_t *K, const uint16_t *V,
+                           long B, long S, long Hq, long Hkv, long d, int causal,
+                           const long *sel, long n_sel, double *attn, int nthreads)
+{
+    if (!Q || !K || !V || !attn) return ORACLE_EARG;
+    if (B <= 0 || S <= 0 || Hq <= 0 || Hkv <= 0 || d <= 0 || Hq % Hkv) return ORACLE_EARG;
+    if (!sel && n_sel != B * S) return ORACLE_EARG;
+    long G = Hq / Hkv;
+    int err = ORACLE_OK;
+    set_threads(nthreads);
+#pragma omp parallel for collapse(2) schedule(dynamic, 1)
+    for (long i = 0; i < n_sel; ++i) {
+        for (long j = 0; j < Hq; ++j) {
+            long m = sel ? sel[i] : i;
+            long b = m / S, t = m % S;
+            long g = j / G;                                   /* R2 */
+            double q[1024];
+            if (d > 1024) { err = ORACLE_EARG; continue; }
+            for (long c = 0; c < d; ++c) q[c] = bf(Q[((b * Hq + j) * S + t) * d + c]);
+            kv_src src = {K + (b * Hkv + g) * S * d, V + (b * Hkv + g) * S * d, NULL, NULL, S};
+            long n_vis = causal ? t + 1 : S;                  /* R5 */
+            int e = attend_row(q, &src, n_vis, d, attn + i * Hq * d + j * d);
+            if (e) err = e;
+        }
+    }
+    return err;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Stage 3: o_proj + residual.                                               */
+/* ------------------------------------------------------------------------ */
+
+/* out[i] = x[m] + attn[m] @ Wo^T for the selected tokens m = sel[i]
+ * ([NeoX] "Output projection", "Qwen3-0.6B example" residual addition, R6).
+ * attn [M, Hq*d] bf16, Wo [hidden, Hq*d] bf16, x [M, hidden] bf16. */
+int oracle_oproj_stage(const uint16_t *attn, const uint16_t *Wo, const uint16_t *x,
+                       long M, long hidden, long QW, const long *sel, long n_sel,
+                       double *out, int nthreads)
+{
+    if (!attn || !Wo || !x || !out || M <= 0 || hidden <= 0 || QW <= 0) return ORACLE_EARG;
+    if (!sel && n_sel != M) return ORACLE_EARG;
+    set_threads(nthreads);
+#pragma omp parallel for schedule(dynamic, 1)
+    for (long i = 0; i < n_sel; ++i) {
+        long m = sel ? sel[i] : i;
+        linear_row(attn + m * QW, Wo, 0, hidden, QW, out + i * hidden);
+        for (long n = 0; n < hidden; ++n) out[i * hidden + n] += bf(x[m * hidden + n]);
+    }
+    return ORACLE_OK;
+}
+
+/* ------------------------------------------------------------------------ */
+/* The whole layer, prefill.                                                 */
+/* ------------------------------------------------------------------------ */
+
+/* Keys and values for all tokens (they are needed by every later query),
+ * then Q, attention and o_proj for the selected tokens only.  With
+ * sel == NULL every token is computed.  Any of q_sel [n_sel,Hq,d],
+ * attn_sel [n_sel,Hq*d], k_all/v_all [B,Hkv,S,d] may be NULL.
+ * out_sel [n_sel, hidden] is required. */
+int oracle_forward(const uint16_t *x, const uint16_t *Wqkv, const uint16_t *Wo,
+                   const uint16_t *q_norm_w, const uint16_t *k_norm_w,
+                   double rope_theta, double eps,
+                   long B, long S, long hidden, long Hq, long Hkv, long d, int causal,
+                   const long *sel, long n_sel,
+                   double *q_sel, double *attn_sel, double *out_sel,
+                   double *k_all, double *v_all, int nthreads)
+{
+    if (!x || !Wqkv || !Wo || !out_sel) return ORACLE_EARG;
+    if (B <= 0 || S <= 0 || hidden <= 0 || Hq <= 0 || Hkv <= 0 || d <= 0 || (d & 1)) return ORACLE_EARG;
+    if (Hq % Hkv || d > 1024) return ORACLE_EARG;
+    if ((q_norm_w == NULL) != (k_norm_w == NULL)) return ORACLE_EARG;
+    if (!sel && n_sel != B * S) return ORACLE_EARG;
+    long NQ = Hq * d, NKV = Hkv * d, G = Hq / Hkv;
+    int err = ORACLE_OK;
+    set_threads(nthreads);
+
+    double *Kd = k_all, *Vd = v_all;
+    if (!Kd) Kd = (double *)malloc((size_t)(B * Hkv * S * d) * sizeof(double));
+    if (!Vd) Vd = (double *)malloc((size_t)(B * Hkv * S * d) * sizeof(double));
+    if (!Kd || !Vd) { err = ORACLE_ENOMEM; goto done; }
+
+    /* keys and values of every token: projection rows [NQ, NQ+2*NKV) */
+#pragma omp parallel for schedule(dynamic, 1)
+    for (long m = 0; m < B * S; ++m) {
+        long b = m / S, t = m % S;
+        double *row = (double *)malloc((size_t)(2 * NKV) * sizeof(double));
+        if (!row) { err = ORACLE_ENOMEM; continue; }
+        linear_row(x + m * hidden, Wqkv, NQ, 2 * NKV, hidden, row);
+        for (long g = 0; g < Hkv; ++g) {
+            double *k = row + g * d;
+            if (k_norm_w) rmsnorm_head(k, d, k_norm_w, eps);
+            rope_head(k, d, (double)t, rope_theta);
+            memcpy(Kd + ((b * Hkv + g) * S + t) * d, k, (size_t)d * sizeof(double));
+            memcpy(Vd + ((b * Hkv + g) * S + t) * d, row + NKV + g * d, (size_t)d * sizeof(double));
+        }
+        free(row);
+    }
+
+    /* queries, attention and o_proj of the selected tokens */
+#pragma omp parallel for schedule(dynamic, 1)
+    for (long i = 0; i < n_sel; ++i) {
+        long m = sel ? sel[i] : i;
+        long b = m / S, t = m % S;
+        double *qrow = (double *)malloc((size_t)NQ * sizeof(double));
+        double *arow = (double *)malloc((size_t)NQ * sizeof(double));
+        if (!qrow || !arow) { err = ORACLE_ENOMEM; free(qrow); free(arow); continue; }
+        linear_row(x + m * hidden, Wqkv, 0, NQ, hidden, qrow);
+        for (long j = 0; j < Hq; ++j) {
+            double *q = qrow + j * d;
+            if (q_norm_w) rmsnorm_head(q, d, q_norm_w, eps);
+            rope_head(q, d, (double)t, rope_theta);
+            long g = j / G;
+            kv_src src = {NULL, NULL, Kd + (b * Hkv + g) * S * d, Vd + (b * Hkv + g) * S * d, 0};
+            long n_vis = causal ? t + 1 : S;
+            int e = attend_row(q, &src, n_vis, d, arow + j * d);
+            if (e) err = e;
+        }
+        if (q_sel) memcpy(q_sel + i * NQ, qrow, (size_t)NQ * sizeof(double));
+        if (attn_sel) memcpy(attn_sel + i * NQ, arow, (size_t)NQ * sizeof(double));
+        /* o_proj: out = x + attn @ Wo^T, attn kept in double here */
+        for (long n = 0; n < hidden; ++n) {
+            const uint16_t *w = Wo + n * NQ;
+            double s = 0.0;
+            for (long k = 0; k < NQ; ++k) s += arow[k] * bf(w[k]);
+            out_sel[i * hidden + n] = bf(x[m * hidden + n]) + s;
+        }
+        free(qrow);
+        free(arow);
+    }
+done:
+    if (Kd && Kd != k_all) free(Kd);
+    if (Vd && Vd != v_all) free(Vd);
+    return err;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Decode: one new token per sequence over a KV cache.                       */
+/* ------------------------------------------------------------------------ */
+
+/* Attention of one query token per sequence over keys [0, kv_len[b]) of a
+ * bf16 cache laid out [B, Hkv, Lmax, d] ([T07] §4 step 5: the cache returns
+ * the full history).  q [B,Hq,d] bf16; attn [B, Hq*d]. */
+int oracle_decode_attention_stage(const uint16_t *q, const uint16_t *k_cache,
+                                  const uint16_t *v_cache, const int *kv_len,
+                                  long B, long Hq, long Hkv, long d, long Lmax,
+                                  double *attn, int nthreads)
+{
+    if (!q || !k_cache || !v_cache || !kv_len || !attn) return ORACLE_EARG;
+    if (B <= 0 || Hq <= 0 || Hkv <= 0 || d <= 0 || d > 1024 || Hq % Hkv || Lmax <= 0) return ORACLE_EARG;
+    for (long b = 0; b < B; ++b)
+        if (kv_len[b] <= 0 || kv_len[b] > Lmax) return ORACLE_EARG;
+    long G = Hq / Hkv;
+    int err = ORACLE_OK;
+    set_threads(nthreads);
+#pragma omp parallel for collapse(2) schedule(dynamic, 1)
+    for (long b = 0; b < B; ++b) {
+        for (long j = 0; j < Hq; ++j) {
+            long g = j / G;
+            double qv[1024];
+            for (long c = 0; c < d; ++c) qv[c] = bf(q[(b * Hq + j) * d + c]);
+            kv_src src = {k_cache + (b * Hkv + g) * Lmax * d, v_cache + (b * Hkv + g) * Lmax * d,
+                          NULL, NULL, kv_len[b]};
+            int e = attend_row(qv, &src, kv_len[b], d, attn + b * Hq * d + j * d);
+            if (e) err = e;
+        }
+    }
+    return err;
+}
+
+/* The whole decode step ([T07] §4 steps 1-7 with L = 1): for each sequence
+ * b the new token sits at position p = cache_len[b]; its Q/K are normed and
+ * rotated at p; its K/V join the cached entries [0, p) (read from the bf16
+ * cache, which this function does not modify) and the query attends to all
+ * p+1 keys.  x [B, hidden]; out [B, hidden].  Optional outputs:
+ * q_new [B,Hq,d], k_new/v_new [B,Hkv,d], attn [B,Hq*d]. */
+int oracle_decode(const uint16_t *x, const uint16_t *Wqkv, const uint16_t *Wo,
+                  const uint16_t *q_norm_w, const uint16_t *k_norm_w,
+                  double rope_theta, double eps,
+                  long B, long hidden, long Hq, long Hkv, long d,
+                  const uint16_t *k_cache, const uint16_t *v_cache, const int *cache_len,
+                  long Lmax, double *out, double *q_new, double *k_new, double *v_new,
+                  double *attn_out, int nthreads)
+{
+    if (!x || !Wqkv || !Wo || !k_cache || !v_cache || !cache_len || !out) return ORACLE_EARG;
+    if (B <= 0 || hidden <= 0 || Hq <= 0 || Hkv <= 0 || d <= 0 || (d & 1) || d > 1024) return ORACLE_EARG;
+    if (Hq % Hkv) return ORACLE_EARG;
+    if ((q_norm_w == NULL) != (k_norm_w == NULL)) return ORACLE_EARG;
+    for (long b = 0; b < B; ++b)
+        if (cache_len[b] < 0 || cache_len[b] + 1 > Lmax) return ORACLE_EARG;
+    long NQ = Hq * d, NKV = Hkv * d, N = NQ + 2 * NKV, G = Hq / Hkv;
+    int err = ORACLE_OK;
+    set_threads(nthreads);
+    double *rows = (double *)malloc((size_t)(B * N) * sizeof(double));
+    double *arows = (double *)malloc((size_t)(B * NQ) * sizeof(double));
+    if (!rows || !arows) { free(rows); free(arows); return ORACLE_ENOMEM; }
+
+#pragma omp parallel for schedule(dynamic, 1)
+    for (long b = 0; b < B; ++b) {
+        double *row = rows + b * N;
+        double p = (double)cache_len[b];
+        linear_row(x + b * hidden, Wqkv, 0, N, hidden, row);
+        for (long j = 0; j < Hq; ++j) {
+            if (q_norm_w) rmsnorm_head(row + j * d, d, q_norm_w, eps);
+            rope_head(row + j * d, d, p, rope_theta);
+        }
+        for (long g = 0; g < Hkv; ++g) {
+            if (k_norm_w) rmsnorm_head(row + NQ + g * d, d, k_norm_w, eps);
+            rope_head(row + NQ + g * d, d, p, rope_theta);
+        }
+    }
+
+#pragma omp parallel for collapse(2) schedule(dynamic, 1)
+    for (long b = 0; b < B; ++b) {
+        for (long j = 0; j < Hq; ++j) {
+            long g = j / G;
+            const double *row = rows + b * N;
+            kv_src src = {k_cache + (b * Hkv + g) * Lmax * d, v_cache + (b * Hkv + g) * Lmax * d,
+                          row + NQ + g * d, row + NQ + NKV + g * d, cache_len[b]};
+            int e = attend_row(row + j * d, &src, cache_len[b] + 1, d, arows + b * NQ + j * d);
+            if (e) err = e;
+        }
+    }
+
+#pragma omp parallel for schedule(dynamic, 1)
+    for (long b = 0; b < B; ++b) {
+        for (long n = 0; n < hidden; ++n) {
+            const uint16_t *w = Wo + n * NQ;
+            double s = 0.0;
+            for (long k = 0; k < NQ; ++k) s += arows[b * NQ + k] * bf(w[k]);
+            out[b * hidden + n] = bf(x[b * hidden + n]) + s;
+        }
+    }
+
+    for (long b = 0; b < B; ++b) {
+        const double *row = rows + b * N;
+        if (q_new) memcpy(q_new + b * NQ, row, (size_t)NQ * sizeof(double));
+        if (k_new) memcpy(k_new + b * NKV, row + NQ, (size_t)NKV * sizeof(double));
+        if (v_new) memcpy(v_new + b * NKV, row + NQ + NKV, (size_t)NKV * sizeof(double));
+        if (attn_out) memcpy(attn_out + b * NQ, arows + b * NQ, (size_t)NQ * sizeof(double));
+    }
+    free(rows);
+    free(arows);
+    return err;
+}

@@ -1,0 +1,454 @@
+"""Pins of the fp64 CPU oracle against what the pages and mathematics fix.
+
+Each test ties one step of the oracle to something other than the oracle:
+numbers printed on the pages (tests/golden/*.txt, each line cited), closed
+forms worked out by hand, invariants of the mathematics, and special cases that
+reduce to a library routine evaluated independently (torch in float64 on the
+CPU).  The cases are chosen so that a plausible slip (a dropped term, a wrong
+sign or index, a transposed operand, an off-by-one in the mask, a wrong head
+map) fails at least one of them.
+
+Sources cited by title and section:
+  [NeoX]  "Support explicit attention head_dim independent of hidden_size / num_attention_heads"
+  [T07]   "Tutorial 07: Multi-Head and Grouped-Query Attention (Full Layer)"
+  [Knob]  "num_heads Is Not a Capacity Knob"
+  [Part]  "Attention head partitions: keep each head's dependencies intact"
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+import torch.nn.functional as F
+
+import oracle
+from conftest import golden_rows
+from transformer_gqa_attention_qkv_gb300.inputs import LayerConfig, make_layer_inputs
+
+T = 4  # oracle threads in these tests
+
+
+def bf16(a):
+    return torch.as_tensor(np.asarray(a, dtype=np.float32)).to(torch.bfloat16)
+
+
+def f64(t):
+    return t.float().double()
+
+
+# ----------------------------------------------------------------- geometry / cost
+
+def test_geometry_matches_pages():
+    """[NeoX] "Qwen3-0.6B example", "Current GPT-NeoX limitation"; [T07] §2; [Knob] §"Where the invariance breaks"."""
+    for name, hidden, heads, kvh, hd, *want in golden_rows("geometry.txt"):
+        hidden, heads = int(hidden), int(heads)
+        kvh = int(kvh) if kvh != "-" else heads
+        d = oracle.effective_head_dim(hidden, heads, int(hd) or None)
+        w = oracle.widths(hidden, heads, kvh, d)
+        got = [w["query_hidden"], w["kv_hidden"], w["qkv_out"], w["o_in"], w["o_out"]]
+        for g, e in zip(got, want):
+            if e != "-":
+                assert g == int(e), (name, got, want)
+
+
+def test_derived_head_dim_quotients():
+    """[NeoX] opening: hidden/heads is 64, 80, 80 while the configs set 128."""
+    for name, hidden, heads, explicit, quotient in golden_rows("quotients.txt"):
+        assert oracle.effective_head_dim(int(hidden), int(heads)) == int(quotient)
+        assert oracle.effective_head_dim(int(hidden), int(heads), int(explicit)) == int(explicit)
+    # divisibility only matters when deriving ([NeoX] "Proposed configuration behavior")
+    assert oracle.effective_head_dim(1000, 3) == -1
+    assert oracle.effective_head_dim(1000, 3, 128) == 128
+
+
+def test_capacity_knob_counts():
+    """[Knob]: 4*d_model^2 weights for every h, pinned-128 counts, 2*n*d_model MACs."""
+    for kind, dm, h, hd, n, val in golden_rows("capacity_knob_counts.txt"):
+        dm, h, hd, val = int(dm), int(h), int(hd), int(val)
+        if kind == "params":
+            assert oracle.attn_param_count(dm, h, h, hd) == val
+        elif kind == "proj_macs":
+            assert oracle.proj_macs_per_token(dm, h, h, hd) == val
+        else:
+            assert oracle.score_value_macs_per_token(int(n), h, hd) == val
+
+
+# ----------------------------------------------------------------- projection
+
+def test_linear_orientation_is_x_times_w_transpose():
+    """W is stored [out, in] and y = x @ W^T ([NeoX] "Checkpoint conversion";
+    [T07] §4 step 1).  Unit rows of x pick out columns of W^T, i.e. rows of W."""
+    rng = np.random.default_rng(0)
+    K, N = 5, 3
+    W = bf16(rng.integers(-8, 8, size=(N, K)))
+    x = bf16(np.eye(K))
+    y = oracle.linear(x, W, threads=T)
+    assert y.shape == (K, N)
+    np.testing.assert_array_equal(y, f64(W).numpy().T)
+
+
+# ----------------------------------------------------------------- QK-norm
+
+def test_rmsnorm_closed_forms():
+    """Reading R3: v*w/sqrt(mean(v^2)+eps) over head_dim ([T07] §3)."""
+    ones = bf16([1, 1, 1, 1])
+    out = oracle.rmsnorm_rows(np.array([[3.0, 4.0, 0.0, 0.0]]), ones, 0.0)
+    np.testing.assert_allclose(out, [[1.2, 1.6, 0.0, 0.0]], rtol=0, atol=1e-15)
+    w = bf16([2.0, 0.5, 1.0, 1.0])
+    out = oracle.rmsnorm_rows(np.array([[3.0, 4.0, 0.0, 0.0]]), w, 0.0)
+    np.testing.assert_allclose(out, [[2.4, 0.8, 0.0, 0.0]], rtol=0, atol=1e-15)
+    # eps sits inside the square root: mean(1)=1, eps=3 -> 1/2
+    out = oracle.rmsnorm_rows(np.array([[1.0, 1.0, 1.0, 1.0]]), ones, 3.0)
+    np.testing.assert_allclose(out, [[0.5] * 4], rtol=0, atol=1e-15)
+
+
+def test_rmsnorm_invariant_and_library():
+    """With unit weights the normed row has rms sqrt(ms/(ms+eps)); and the
+    step equals torch.nn.functional.rms_norm evaluated in float64."""
+    rng = np.random.default_rng(1)
+    rows = rng.standard_normal((7, 128)) * 3.0
+    eps = 1e-2
+    out = oracle.rmsnorm_rows(rows, bf16(np.ones(128)), eps)
+    ms = (rows ** 2).mean(1)
+    np.testing.assert_allclose(np.sqrt((out ** 2).mean(1)), np.sqrt(ms / (ms + eps)), rtol=1e-13)
+    w = bf16(1.0 + 0.1 * rng.standard_normal(128))
+    ref = F.rms_norm(torch.from_numpy(rows), (128,), weight=f64(w), eps=eps).numpy()
+    np.testing.assert_allclose(oracle.rmsnorm_rows(rows, w, eps), ref, rtol=1e-13, atol=1e-14)
+
+
+# ----------------------------------------------------------------- RoPE
+
+def test_rope_closed_forms():
+    """Reading R4: pair (i, i+d/2), angle pos*theta^(-2i/d) ([T07] §4 RoPE)."""
+    # d=2: one pair, frequency 1: (1,0) at position p -> (cos p, sin p)
+    for p in (0.0, 1.0, 2.5, 100.0):
+        out = oracle.rope_rows(np.array([[1.0, 0.0]]), [p], 10000.0)
+        np.testing.assert_allclose(out, [[math.cos(p), math.sin(p)]], atol=1e-14)
+    # d=4, theta=100: frequencies (1, 0.1).  e_1 at position 10 turns by 1 rad in
+    # the (1,3) plane; e_0 turns by 10 rad in the (0,2) plane.
+    out = oracle.rope_rows(np.array([[0.0, 1.0, 0.0, 0.0], [1.0, 0.0, 0.0, 0.0]]), [10.0, 10.0], 100.0)
+    np.testing.assert_allclose(out[0], [0.0, math.cos(1.0), 0.0, math.sin(1.0)], atol=1e-14)
+    np.testing.assert_allclose(out[1], [math.cos(10.0), 0.0, math.sin(10.0), 0.0], atol=1e-14)
+
+
+def test_rope_invariants():
+    """Identity at position 0, norm preserving, and <R_m q, R_n k> depends only on m-n."""
+    rng = np.random.default_rng(2)
+    d = 128
+    v = rng.standard_normal((3, d))
+    np.testing.assert_allclose(oracle.rope_rows(v, [0.0] * 3, 1e6), v, atol=0)
+    r = oracle.rope_rows(v, [5.0, 77.0, 16383.0], 1e6)
+    np.testing.assert_allclose(np.linalg.norm(r, axis=1), np.linalg.norm(v, axis=1), rtol=1e-13)
+    q, k = rng.standard_normal((1, d)), rng.standard_normal((1, d))
+    dots = []
+    for shift in (0.0, 13.0, 4000.0):
+        rq = oracle.rope_rows(q, [20.0 + shift], 1e4)
+        rk = oracle.rope_rows(k, [7.0 + shift], 1e4)
+        dots.append(float((rq @ rk.T).item()))
+    np.testing.assert_allclose(dots, dots[0], rtol=1e-10)
+
+
+def test_rope_equals_complex_rotation():
+    """Rotate-half RoPE is multiplication of z_i = v_i + i*v_{i+d/2} by
+    exp(i*pos*theta^(-2i/d)), evaluated with torch complex128."""
+    rng = np.random.default_rng(3)
+    d, theta = 64, 1e4
+    v = rng.standard_normal((5, d))
+    pos = np.array([0.0, 1.0, 9.0, 300.0, 8192.0])
+    out = oracle.rope_rows(v, pos, theta)
+    half = d // 2
+    z = torch.complex(torch.from_numpy(v[:, :half]), torch.from_numpy(v[:, half:]))
+    freq = theta ** (-2.0 * torch.arange(half, dtype=torch.float64) / d)
+    ang = torch.from_numpy(pos)[:, None] * freq[None, :]
+    zr = z * torch.polar(torch.ones_like(ang), ang)
+    ref = torch.cat([zr.real, zr.imag], dim=1).numpy()
+    np.testing.assert_allclose(out, ref, rtol=1e-12, atol=1e-12)
+
+
+# ----------------------------------------------------------------- attention
+
+def _att(Q, K, V, causal=True, sel=None):
+    B, Hq, S, d = Q.shape
+    Hkv = K.shape[1]
+    return oracle.attention_stage(Q, K, V, B, S, Hq, Hkv, d, causal=causal, sel=sel, threads=T)
+
+
+def test_attention_two_keys_closed_form():
+    """Scale head_dim^-0.5 ([NeoX] "Scaling and RoPE"; [T07] §4).  d=4, query
+    (2,0,0,0), keys 0 and (1,0,0,0): scores 0 and 1, so row 1 weights are
+    1/(1+e) and e/(1+e); row 0 sees only key 0 (causal, diagonal included)."""
+    Q = bf16(np.zeros((1, 1, 2, 4))); Q[0, 0, 1, 0] = 2.0
+    K = bf16(np.zeros((1, 1, 2, 4))); K[0, 0, 1, 0] = 1.0
+    V = bf16(np.zeros((1, 1, 2, 4)))
+    V[0, 0, 0] = bf16([4.0, 0.0, 0.0, 8.0]); V[0, 0, 1] = bf16([0.0, 4.0, 0.0, 0.0])
+    out = _att(Q, K, V)
+    e = math.e
+    np.testing.assert_allclose(out[0], [4.0, 0.0, 0.0, 8.0], atol=1e-15)
+    np.testing.assert_allclose(out[1], [4 / (1 + e), 4 * e / (1 + e), 0.0, 8 / (1 + e)], rtol=1e-14)
+    # without the mask row 0 sees both keys with score 0: the plain mean
+    out = _att(Q, K, V, causal=False)
+    np.testing.assert_allclose(out[0], [2.0, 2.0, 0.0, 4.0], atol=1e-15)
+
+
+def test_attention_equal_keys_gives_prefix_mean():
+    """All keys equal: softmax is uniform over the visible prefix, so row t is
+    the mean of V[0..t]; row 0 is V[0] exactly."""
+    rng = np.random.default_rng(4)
+    S, d = 37, 8
+    Q = bf16(rng.standard_normal((1, 1, S, d)))
+    K = bf16(np.tile(rng.standard_normal((1, 1, 1, d)), (1, 1, S, 1)))
+    V = bf16(rng.standard_normal((1, 1, S, d)))
+    out = _att(Q, K, V)
+    v = f64(V)[0, 0].numpy()
+    ref = np.cumsum(v, axis=0) / np.arange(1, S + 1)[:, None]
+    np.testing.assert_allclose(out, ref, rtol=1e-12, atol=1e-13)
+    np.testing.assert_array_equal(out[0], v[0])
+
+
+def test_attention_group_map_markers():
+    """Reading R2: query head j reads KV head j // (Hq/Hkv) ([NeoX] "Qwen3-0.6B
+    example": each KV head serves 2 query heads; [Part]: preserve the mapping
+    from global query heads to their KV group).  Each KV head's values are a
+    distinct constant marker, so each query head must return its group's marker."""
+    rng = np.random.default_rng(5)
+    B, S, Hq, Hkv, d = 2, 9, 8, 2, 4
+    markers = np.arange(1, B * Hkv * d + 1, dtype=np.float32).reshape(B, Hkv, 1, d)
+    V = bf16(np.tile(markers, (1, 1, S, 1)))
+    Q = bf16(rng.standard_normal((B, Hq, S, d)))
+    K = bf16(rng.standard_normal((B, Hkv, S, d)))
+    out = _att(Q, K, V).reshape(B, S, Hq, d)
+    for j in range(Hq):
+        for b in range(B):
+            np.testing.assert_allclose(out[b, :, j], np.broadcast_to(markers[b, j // 4, 0], (S, d)),
+                                       rtol=1e-14)
+
+
+def test_attention_equals_library_sdpa():
+    """Special case that reduces to a library routine: the attention step equals
+    torch's scaled_dot_product_attention in float64 with each KV head repeated
+    for its contiguous group, causal and non-causal, with a ragged length."""
+    rng = np.random.default_rng(6)
+    B, S, Hq, Hkv, d = 2, 45, 6, 2, 16
+    Q = bf16(rng.standard_normal((B, Hq, S, d)) * 2)
+    K = bf16(rng.standard_normal((B, Hkv, S, d)) * 2)
+    V = bf16(rng.standard_normal((B, Hkv, S, d)))
+    G = Hq // Hkv
+    for causal in (True, False):
+        ref = F.scaled_dot_product_attention(f64(Q), f64(K).repeat_interleave(G, 1),
+                                             f64(V).repeat_interleave(G, 1), is_causal=causal)
+        ref = ref.transpose(1, 2).reshape(B * S, Hq * d).numpy()
+        np.testing.assert_allclose(_att(Q, K, V, causal=causal), ref, rtol=1e-11, atol=1e-12)
+    # the row-sampled path returns exactly the selected rows
+    sel = [0, 3, 44, 45, 89]
+    np.testing.assert_array_equal(_att(Q, K, V, sel=sel), _att(Q, K, V)[sel])
+
+
+def test_attention_no_future_leak():
+    """[Part]: a causal test with a nontrivial length.  A huge value planted in V
+    at position 50 must leave rows < 50 untouched and move rows >= 50."""
+    rng = np.random.default_rng(7)
+    S, d = 130, 8
+    Q = bf16(rng.standard_normal((1, 2, S, d)))
+    K = bf16(rng.standard_normal((1, 1, S, d)))
+    V = bf16(rng.standard_normal((1, 1, S, d)))
+    base = _att(Q, K, V)
+    V2 = V.clone(); V2[0, 0, 50] = 1e4
+    spiked = _att(Q, K, V2)
+    np.testing.assert_array_equal(spiked[:50], base[:50])
+    assert np.all(np.abs(spiked[50:] - base[50:]).max(axis=1) > 1e-3)
+
+
+# ----------------------------------------------------------------- whole layer
+
+def _tiny(qk_norm=True, **kw):
+    cfg = LayerConfig("tiny", B=2, S=19, hidden=24, Hq=4, Hkv=2, head_dim=8, qk_norm=qk_norm,
+                      rope_theta=1e4, eps=1e-6)
+    return cfg.with_(**kw) if kw else cfg
+
+
+def _fwd(cfg, t, **kw):
+    return oracle.forward(t["x"], t["Wqkv"], t["Wo"], t["q_norm_w"], t["k_norm_w"], cfg.rope_theta,
+                          cfg.eps, cfg.B, cfg.S, cfg.hidden, cfg.Hq, cfg.Hkv, cfg.head_dim,
+                          causal=cfg.causal, threads=T, **kw)
+
+
+def test_forward_equals_library_composition():
+    """The whole layer ([T07] §4 steps 1-7, residual as in [NeoX] "Qwen3-0.6B
+    example") equals a float64 composition of torch library routines:
+    F.linear, F.rms_norm, complex-multiplication RoPE, scaled_dot_product_attention."""
+    for qk in (True, False):
+        cfg = _tiny(qk_norm=qk)
+        t = make_layer_inputs(cfg, seed=11, w_std=0.3)
+        B, S, h, Hq, Hkv, d = cfg.B, cfg.S, cfg.hidden, cfg.Hq, cfg.Hkv, cfg.head_dim
+        x, W, Wo = f64(t["x"]), f64(t["Wqkv"]), f64(t["Wo"])
+        q = F.linear(x, W[:Hq * d]).view(B, S, Hq, d)
+        k = F.linear(x, W[Hq * d:(Hq + Hkv) * d]).view(B, S, Hkv, d)
+        v = F.linear(x, W[(Hq + Hkv) * d:]).view(B, S, Hkv, d)
+        if qk:
+            q = F.rms_norm(q, (d,), weight=f64(t["q_norm_w"]), eps=cfg.eps)
+            k = F.rms_norm(k, (d,), weight=f64(t["k_norm_w"]), eps=cfg.eps)
+
+        def rope(a):
+            half = d // 2
+            z = torch.complex(a[..., :half], a[..., half:])
+            ang = torch.arange(S, dtype=torch.float64)[:, None] * \
+                cfg.rope_theta ** (-2.0 * torch.arange(half, dtype=torch.float64) / d)
+            z = z * torch.polar(torch.ones_like(ang), ang)[None, :, None, :]
+            return torch.cat([z.real, z.imag], -1)
+
+        q, k = rope(q).transpose(1, 2), rope(k).transpose(1, 2)
+        v = v.transpose(1, 2)
+        a = F.scaled_dot_product_attention(q, k.repeat_interleave(Hq // Hkv, 1),
+                                           v.repeat_interleave(Hq // Hkv, 1), is_causal=True)
+        a = a.transpose(1, 2).reshape(B, S, Hq * d)
+        ref = (x + F.linear(a, Wo)).reshape(B * S, h).numpy()
+        got = _fwd(cfg, t, want_stages=True)
+        np.testing.assert_allclose(got["out"], ref, rtol=1e-11, atol=1e-11)
+        np.testing.assert_allclose(got["attn"], a.reshape(B * S, -1).numpy(), rtol=1e-11, atol=1e-11)
+        np.testing.assert_allclose(got["k"], k.numpy(), rtol=1e-11, atol=1e-11)
+
+
+def test_forward_stages_agree_with_stage_functions():
+    """oracle.forward and the three stage functions compute the same layer, and
+    the row-sampled forward returns exactly the selected rows."""
+    cfg = _tiny()
+    t = make_layer_inputs(cfg, seed=12, w_std=0.3)
+    full = _fwd(cfg, t, want_stages=True)
+    q, k, v = oracle.qkv_stage(t["x"], t["Wqkv"], t["q_norm_w"], t["k_norm_w"], cfg.rope_theta,
+                               cfg.eps, cfg.B, cfg.S, cfg.hidden, cfg.Hq, cfg.Hkv, cfg.head_dim,
+                               threads=T)
+    np.testing.assert_allclose(full["k"], k, rtol=1e-13, atol=1e-14)
+    np.testing.assert_allclose(full["q"], q.transpose(0, 2, 1, 3).reshape(-1, cfg.Hq, cfg.head_dim),
+                               rtol=1e-13, atol=1e-14)
+    sel = [0, 5, 18, 19, 37]
+    part = _fwd(cfg, t, sel=sel)
+    np.testing.assert_allclose(part, full["out"][sel], rtol=0, atol=0)
+
+
+def test_forward_head_sum_decomposition():
+    """[Knob] "Why the cost does not move": the layer is the sum over heads of
+    head_i @ W_O_i, so zeroing all of W_O but head j's slice keeps exactly
+    head j's term, and the terms add up to the full output minus x."""
+    cfg = _tiny()
+    t = make_layer_inputs(cfg, seed=13, w_std=0.3)
+    d = cfg.head_dim
+    full = _fwd(cfg, t) - f64(t["x"]).reshape(-1, cfg.hidden).numpy()
+    total = np.zeros_like(full)
+    for j in range(cfg.Hq):
+        t2 = dict(t)
+        wo = torch.zeros_like(t["Wo"]); wo[:, j * d:(j + 1) * d] = t["Wo"][:, j * d:(j + 1) * d]
+        t2["Wo"] = wo
+        term = _fwd(cfg, t2) - f64(t["x"]).reshape(-1, cfg.hidden).numpy()
+        assert np.abs(term).max() > 1e-3
+        total += term
+    np.testing.assert_allclose(total, full, rtol=1e-11, atol=1e-12)
+    # Wo = 0 leaves the residual alone
+    t3 = dict(t); t3["Wo"] = torch.zeros_like(t["Wo"])
+    np.testing.assert_array_equal(_fwd(cfg, t3), f64(t["x"]).reshape(-1, cfg.hidden).numpy())
+
+
+def test_forward_permutation_tests():
+    """[Part]: distinguishable heads so a permutation cannot hide.  Permuting the
+    query heads inside a KV group (their Wqkv rows and the matching Wo columns)
+    leaves the output unchanged; permuting only the Q rows permutes attn by head;
+    swapping two KV groups together with their query heads changes nothing."""
+    cfg = _tiny()
+    t = make_layer_inputs(cfg, seed=14, w_std=0.3)
+    d, Hq, Hkv = cfg.head_dim, cfg.Hq, cfg.Hkv
+    base = _fwd(cfg, t, want_stages=True)
+
+    def permuted(qperm, gperm):
+        rows = [np.arange(qperm[j] * d, qperm[j] * d + d) for j in range(Hq)]
+        rows += [Hq * d + np.arange(gperm[g] * d, gperm[g] * d + d) for g in range(Hkv)]
+        rows += [(Hq + Hkv) * d + np.arange(gperm[g] * d, gperm[g] * d + d) for g in range(Hkv)]
+        W = t["Wqkv"][torch.from_numpy(np.concatenate(rows))]
+        cols = np.concatenate([np.arange(qperm[j] * d, qperm[j] * d + d) for j in range(Hq)])
+        Wo = t["Wo"][:, torch.from_numpy(cols)]
+        return W, Wo
+
+    # within-group swap of heads 0 and 1 (both in group 0)
+    W, Wo = permuted([1, 0, 2, 3], [0, 1])
+    t2 = dict(t, Wqkv=W, Wo=Wo)
+    got = _fwd(cfg, t2, want_stages=True)
+    np.testing.assert_allclose(got["out"], base["out"], rtol=1e-12, atol=1e-13)
+    a = got["attn"].reshape(-1, Hq, d)
+    np.testing.assert_allclose(a[:, [1, 0, 2, 3]], base["attn"].reshape(-1, Hq, d), rtol=1e-12, atol=1e-13)
+    # swap the two KV groups and carry their query heads along
+    W, Wo = permuted([2, 3, 0, 1], [1, 0])
+    got = _fwd(cfg, dict(t, Wqkv=W, Wo=Wo))
+    np.testing.assert_allclose(got, base["out"], rtol=1e-12, atol=1e-13)
+    # a cross-group swap of query heads alone is NOT a symmetry: it must change attn
+    W, _ = permuted([2, 1, 0, 3], [0, 1])
+    got = _fwd(cfg, dict(t, Wqkv=W), want_stages=True)
+    a = got["attn"].reshape(-1, Hq, d)
+    assert np.abs(a[:, 0] - base["attn"].reshape(-1, Hq, d)[:, 2]).max() > 1e-3
+
+
+def test_forward_value_only_weights():
+    """Reading R1 (fused rows Q, then K, then V): with the Q and K blocks zero
+    every score is 0, the softmax is uniform over the prefix, and attn is the
+    prefix mean of V = x @ W_v^T, whatever RoPE and QK-norm do to zeros."""
+    cfg = _tiny(qk_norm=False)
+    t = make_layer_inputs(cfg, seed=15, w_std=0.3)
+    d, Hq, Hkv = cfg.head_dim, cfg.Hq, cfg.Hkv
+    W = t["Wqkv"].clone(); W[:(Hq + Hkv) * d] = 0
+    got = _fwd(cfg, dict(t, Wqkv=W), want_stages=True)
+    v = (f64(t["x"]) @ f64(W[(Hq + Hkv) * d:]).T).numpy().reshape(cfg.B, cfg.S, Hkv, d)
+    pm = np.cumsum(v, axis=1) / np.arange(1, cfg.S + 1)[None, :, None, None]
+    ref = np.repeat(pm, Hq // Hkv, axis=2).reshape(cfg.B * cfg.S, Hq * d)
+    np.testing.assert_allclose(got["attn"], ref, rtol=1e-12, atol=1e-13)
+
+
+# ----------------------------------------------------------------- decode
+
+def test_decode_matches_prefill_last_token():
+    """[T07] §4 step 5 (the cache returns the whole history) and the RoPE
+    offset: decoding token S-1 over a cache holding the prefill's keys and
+    values of tokens 0..S-2 reproduces the prefill's last row.  The cached
+    entries are bf16-rounded, so agreement is to bf16 accuracy; a wrong
+    position or a dropped new key misses by far more."""
+    cfg = _tiny(S=23, B=3)
+    t = make_layer_inputs(cfg, seed=16, w_std=0.3)
+    B, S, d, Hq, Hkv = cfg.B, cfg.S, cfg.head_dim, cfg.Hq, cfg.Hkv
+    pre = _fwd(cfg, t, want_stages=True)
+    Lmax = S + 5
+    kc = torch.zeros((B, Hkv, Lmax, d), dtype=torch.bfloat16); vc = torch.zeros_like(kc)
+    kc[:, :, :S - 1] = torch.from_numpy(pre["k"][:, :, :S - 1]).to(torch.bfloat16)
+    vc[:, :, :S - 1] = torch.from_numpy(pre["v"][:, :, :S - 1]).to(torch.bfloat16)
+    dec = oracle.decode(t["x"][:, S - 1], t["Wqkv"], t["Wo"], t["q_norm_w"], t["k_norm_w"],
+                        cfg.rope_theta, cfg.eps, B, cfg.hidden, Hq, Hkv, d, kc, vc,
+                        [S - 1] * B, Lmax, threads=T)
+    last = pre["out"].reshape(B, S, -1)[:, S - 1]
+    np.testing.assert_allclose(dec["out"], last, rtol=0, atol=2e-2 * np.abs(last).max())
+    np.testing.assert_allclose(dec["k"], pre["k"][:, :, S - 1], rtol=1e-12, atol=1e-13)
+    # a decode at the wrong position (S instead of S-1) must disagree clearly
+    wrong = oracle.decode(t["x"][:, S - 1], t["Wqkv"], t["Wo"], t["q_norm_w"], t["k_norm_w"],
+                          cfg.rope_theta, cfg.eps, B, cfg.hidden, Hq, Hkv, d, kc, vc,
+                          [S] * B, Lmax, threads=T)
+    assert np.abs(wrong["k"] - pre["k"][:, :, S - 1]).max() > 1e-2
+
+
+def test_decode_attention_stage_matches_prefill_rows():
+    """Decode attention of the new token over keys [0, L) equals the prefill
+    attention row L-1 computed from the same bf16 Q/K/V."""
+    rng = np.random.default_rng(17)
+    B, S, Hq, Hkv, d = 2, 31, 4, 2, 16
+    Q = bf16(rng.standard_normal((B, Hq, S, d)))
+    K = bf16(rng.standard_normal((B, Hkv, S, d)))
+    V = bf16(rng.standard_normal((B, Hkv, S, d)))
+    lens = [S, 17]
+    q = torch.stack([Q[b, :, lens[b] - 1] for b in range(B)])
+    got = oracle.decode_attention_stage(q, K, V, lens, B, Hq, Hkv, d, S, threads=T)
+    full = _att(Q, K, V).reshape(B, S, -1)
+    for b in range(B):
+        np.testing.assert_allclose(got[b], full[b, lens[b] - 1], rtol=1e-13, atol=1e-14)
+
+
+def test_oracle_rejects_bad_arguments():
+    with pytest.raises(RuntimeError):
+        oracle.rope_rows(np.zeros((1, 3)), [0.0], 1e4)     # odd head_dim
+    rng = np.random.default_rng(0)
+    Q = bf16(rng.standard_normal((1, 3, 4, 8)))
+    K = bf16(rng.standard_normal((1, 2, 4, 8)))
+    with pytest.raises(RuntimeError):
+        oracle.attention_stage(Q, K, K, 1, 4, 3, 2, 8)     # Hq % Hkv != 0
