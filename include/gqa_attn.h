@@ -1,0 +1,215 @@
+/*
+ * gqa_attn.h -- C ABI of the GB300 (sm_103a) grouped-query attention layer.
+ *
+ * The layer: a fused QKV projection hidden -> (Hq + 2*Hkv)*head_dim,
+ * per-head RMSNorm of Q and K (QK-norm), RoPE on Q and K, causal
+ * grouped-query attention softmax(Q K^T / sqrt(head_dim)) V where every KV
+ * head serves Hq/Hkv query heads, and an output projection Hq*head_dim ->
+ * hidden followed by the residual add.  head_dim is an explicit argument,
+ * independent of hidden / Hq.
+ *
+ * Sources (page title, section):
+ *   [NeoX] "Support explicit attention head_dim independent of hidden_size /
+ *          num_attention_heads": "Background" (projection shapes), "Fused QKV
+ *          projection", "Attention output flattening", "Output projection",
+ *          "Scaling and RoPE", "Checkpoint conversion" (weight shapes),
+ *          "Qwen3-0.6B example" (residual addition, 2 query heads per KV head).
+ *   [T07]  "Tutorial 07: Multi-Head and Grouped-Query Attention (Full Layer)":
+ *          §3 QK-Norm, §4 the complete layer (steps 1-7), §6 reshape flow.
+ *   [Knob] "num_heads Is Not a Capacity Knob": "Why the cost does not move"
+ *          (weight and multiply-accumulate counts), "Where the invariance
+ *          breaks" (head_dim is a kernel tile dimension).
+ *
+ * Conventions for every entry point
+ *   - Tensors are bf16, passed as pointers to their 16-bit patterns
+ *     (gqa_bf16), dense row-major with the shapes given per argument.  Unless
+ *     a comment says "host", a pointer is a DEVICE pointer of the current CUDA
+ *     device.  The caller owns all memory; the library never frees or keeps
+ *     a caller pointer past the call.
+ *   - Weights are stored [out_features, in_features] and applied as x @ W^T
+ *     ([NeoX] "Checkpoint conversion").  Wqkv stacks, by rows, W_q
+ *     [Hq*d, hidden], then W_k [Hkv*d, hidden], then W_v [Hkv*d, hidden].
+ *   - Query head j attends with KV head j / (Hq/Hkv).
+ *   - RMSNorm(v) = v * w / sqrt(mean(v^2) + eps) over head_dim.  RoPE pairs
+ *     element i with i + head_dim/2 at angle pos * theta^(-2i/head_dim).
+ *   - `stream` is a cudaStream_t passed as void* (NULL: the legacy default
+ *     stream).  Work is enqueued asynchronously; the function returns after
+ *     validation and launch.  Outputs are valid once the stream reaches them.
+ *   - Status: GQA_OK (0) or a negative GQA_ERR_* code.  Arguments are
+ *     validated before anything is launched; a rejected call launches nothing
+ *     and writes nothing.  gqa_last_error() returns a message for the last
+ *     failing call on the calling thread.
+ *   - Supported shapes: head_dim in {64, 128}; hidden a multiple of 8;
+ *     Hq a multiple of Hkv.  Other head_dim values return
+ *     GQA_ERR_UNSUPPORTED, naming the dimension ([Knob] "Where the
+ *     invariance breaks": head_dim is a tile dimension of the fused kernels).
+ *   - Device-side waits are bounded.  A wait that runs out records
+ *     GQA_ERR_TIMEOUT in a per-device error word that gqa_check_device_error()
+ *     reports; the kernel then returns without hanging the GPU.
+ */
+#ifndef GQA_ATTN_H
+#define GQA_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t gqa_bf16; /* bit pattern of one bf16 value */
+
+#define GQA_OK 0
+#define GQA_ERR_ARG (-1)         /* null/aliasing pointer, bad size, bad combination */
+#define GQA_ERR_UNSUPPORTED (-2) /* valid layer, shape outside what the kernels tile */
+#define GQA_ERR_CUDA (-3)        /* a CUDA runtime call failed (message has details) */
+#define GQA_ERR_TIMEOUT (-4)     /* a bounded device wait gave up */
+#define GQA_ERR_WORKSPACE (-5)   /* workspace missing or smaller than required */
+
+/* ------------------------------------------------------------------ prefill */
+
+/* Bytes of device workspace gqa_attn_forward_ex needs: Q [B,Hq,S,d],
+ * K and V [B,Hkv,S,d] and attn [B,S,Hq*d], bf16, each 256-byte aligned.
+ * Returns 0 for invalid sizes. */
+size_t gqa_attn_workspace_size(int B, int S, int hidden, int Hq, int Hkv, int head_dim);
+
+/* The whole layer forward ([T07] §4 steps 1-7; [NeoX] "Qwen3-0.6B example"):
+ *   x        [B, S, hidden]
+ *   Wqkv     [(Hq + 2*Hkv)*head_dim, hidden]   rows W_q; W_k; W_v
+ *   Wo       [hidden, Hq*head_dim]
+ *   q_norm_w [head_dim] or NULL; k_norm_w [head_dim] or NULL -- both NULL
+ *            (no QK-norm) or both non-NULL, else GQA_ERR_ARG
+ *   rope_theta > 0, eps >= 0; positions are 0..S-1 in every sequence
+ *   causal   1: query t sees keys u <= t; 0: every key of its sequence
+ *   out      [B, S, hidden] = x + o_proj(attn); must not overlap x or the
+ *            weights (GQA_ERR_ARG)
+ *   workspace: device memory of at least gqa_attn_workspace_size(...) bytes,
+ *            256-byte aligned, not overlapping any argument; contents on exit
+ *            are the intermediate Q, K, V and attn.
+ * Stages run in order on `stream`: QKV projection (+ QK-norm + RoPE),
+ * attention, o_proj (+ residual). */
+int gqa_attn_forward_ex(const gqa_bf16 *x, const gqa_bf16 *Wqkv, const gqa_bf16 *Wo,
+                        const gqa_bf16 *q_norm_w, const gqa_bf16 *k_norm_w,
+                        float rope_theta, float eps,
+                        int B, int S, int hidden, int Hq, int Hkv, int head_dim, int causal,
+                        gqa_bf16 *out, void *workspace, size_t workspace_bytes, void *stream);
+
+/* Same as gqa_attn_forward_ex on the legacy default stream with a workspace
+ * the library allocates on first use and grows on demand (kept until exit).
+ * Calls that overlap on the device share that workspace: serialise them. */
+int gqa_attn_forward(const gqa_bf16 *x, const gqa_bf16 *Wqkv, const gqa_bf16 *Wo,
+                     const gqa_bf16 *q_norm_w, const gqa_bf16 *k_norm_w,
+                     float rope_theta, float eps,
+                     int B, int S, int hidden, int Hq, int Hkv, int head_dim, int causal,
+                     gqa_bf16 *out);
+
+/* Stage 1 alone: qkv = x @ Wqkv^T, then QK-norm and RoPE at positions
+ * 0..S-1, written head-major ([T07] §4 steps 1-4):
+ *   q_out [B, Hq, S, head_dim], k_out and v_out [B, Hkv, S, head_dim]. */
+int gqa_qkv_proj(const gqa_bf16 *x, const gqa_bf16 *Wqkv,
+                 const gqa_bf16 *q_norm_w, const gqa_bf16 *k_norm_w,
+                 float rope_theta, float eps,
+                 int B, int S, int hidden, int Hq, int Hkv, int head_dim,
+                 gqa_bf16 *q_out, gqa_bf16 *k_out, gqa_bf16 *v_out, void *stream);
+
+/* Stage 2 alone: grouped-query attention with scale head_dim^-0.5, fp32
+ * softmax and accumulation ([T07] §4 step 6; [NeoX] "Scaling and RoPE"):
+ *   q [B, Hq, S, head_dim], k and v [B, Hkv, S, head_dim]
+ *   attn_out [B, S, Hq*head_dim] ([NeoX] "Attention output flattening"). */
+int gqa_attention(const gqa_bf16 *q, const gqa_bf16 *k, const gqa_bf16 *v,
+                  int B, int S, int Hq, int Hkv, int head_dim, int causal,
+                  gqa_bf16 *attn_out, void *stream);
+
+/* Stage 3 alone: out = x + attn @ Wo^T ([NeoX] "Output projection"):
+ *   attn [M, q_width], Wo [hidden, q_width], x and out [M, hidden];
+ *   q_width and hidden multiples of 8; out must not overlap x. */
+int gqa_oproj_residual(const gqa_bf16 *attn, const gqa_bf16 *Wo, const gqa_bf16 *x,
+                       int M, int hidden, int q_width, gqa_bf16 *out, void *stream);
+
+/* ------------------------------------------------------------------- decode */
+
+/* Bytes of device workspace gqa_attn_decode needs (Q of the new tokens,
+ * attn, and the split-KV partial results).  Returns 0 for invalid sizes. */
+size_t gqa_attn_decode_workspace_size(int B, int hidden, int Hq, int Hkv, int head_dim, int Lmax);
+
+/* One decode step: one new token per sequence over a KV cache ([T07] §4
+ * with L = 1; step 5 "update and fetch" of the cache).
+ *   x          [B, hidden], the new tokens
+ *   k_cache, v_cache [B, Hkv, Lmax, head_dim]: entries [0, cache_len[b]) hold
+ *              the normed and rotated keys / the values of earlier tokens;
+ *              this call writes the new token's K and V at slot cache_len[b]
+ *   cache_len  device int32 [B]: tokens already cached; the new token's
+ *              position and slot.  Must satisfy 0 <= cache_len[b] < Lmax
+ *              (device-side values are not checked on the host; out-of-range
+ *              rows are skipped and reported as GQA_ERR_ARG through
+ *              gqa_check_device_error).  Not modified: the caller advances it.
+ *   out        [B, hidden] = x + o_proj(attn over keys 0..cache_len[b])
+ *   workspace  at least gqa_attn_decode_workspace_size(...) bytes. */
+int gqa_attn_decode(const gqa_bf16 *x, const gqa_bf16 *Wqkv, const gqa_bf16 *Wo,
+                    const gqa_bf16 *q_norm_w, const gqa_bf16 *k_norm_w,
+                    float rope_theta, float eps,
+                    int B, int hidden, int Hq, int Hkv, int head_dim,
+                    gqa_bf16 *k_cache, gqa_bf16 *v_cache, const int *cache_len, int Lmax,
+                    gqa_bf16 *out, void *workspace, size_t workspace_bytes, void *stream);
+
+/* Decode stage 1 alone: projection + QK-norm + RoPE at position
+ * cache_len[b]; q_out [B, Hq, head_dim]; K and V written into the caches at
+ * slot cache_len[b]. */
+int gqa_decode_qkv(const gqa_bf16 *x, const gqa_bf16 *Wqkv,
+                   const gqa_bf16 *q_norm_w, const gqa_bf16 *k_norm_w,
+                   float rope_theta, float eps,
+                   int B, int hidden, int Hq, int Hkv, int head_dim,
+                   gqa_bf16 *k_cache, gqa_bf16 *v_cache, const int *cache_len, int Lmax,
+                   gqa_bf16 *q_out, void *stream);
+
+/* Bytes of workspace gqa_decode_attention needs for its split partials. */
+size_t gqa_decode_attention_workspace_size(int B, int Hq, int Hkv, int head_dim, int Lmax);
+
+/* Decode stage 2 alone: split-KV attention of one query per sequence,
+ * q [B, Hq, head_dim], over keys [0, kv_len[b]) of the caches
+ * [B, Hkv, Lmax, head_dim]; kv_len device int32 [B], 1 <= kv_len[b] <= Lmax.
+ * attn_out [B, Hq*head_dim]. */
+int gqa_decode_attention(const gqa_bf16 *q, const gqa_bf16 *k_cache, const gqa_bf16 *v_cache,
+                         const int *kv_len, int B, int Hq, int Hkv, int head_dim, int Lmax,
+                         gqa_bf16 *attn_out, void *workspace, size_t workspace_bytes,
+                         void *stream);
+
+/* ------------------------------------------------------------ accounting */
+
+/* Algorithmic cost of one prefill forward, all pointers host, any may be NULL
+ * ([Knob] "Why the cost does not move"):
+ *   weights          q/k/v/o projection weights = hidden*(Hq+2Hkv)*d + Hq*d*hidden
+ *   proj_macs_per_token = weights (each weight used once per token)
+ *   attn_macs        score + value multiply-accumulates over the whole batch:
+ *                    2*d per (query head, query, visible key); causal counts
+ *                    the S(S+1)/2 visible pairs per sequence
+ *   flops            2*(B*S*proj_macs_per_token + attn_macs)
+ * Returns GQA_ERR_ARG for non-positive sizes. */
+int gqa_attn_cost(int B, int S, int hidden, int Hq, int Hkv, int head_dim, int causal,
+                  long long *weights, long long *proj_macs_per_token,
+                  long long *attn_macs, long long *flops);
+
+/* ------------------------------------------------------------- diagnostics */
+
+/* Message for the last nonzero status returned on the calling thread. */
+const char *gqa_last_error(void);
+
+/* Synchronises the current device, then reads and clears its device error
+ * word.  Returns GQA_OK, GQA_ERR_TIMEOUT (a bounded wait gave up),
+ * GQA_ERR_ARG (a device-side index check failed) or GQA_ERR_CUDA. */
+int gqa_check_device_error(void);
+
+/* Watchdog self-test: launches one kernel whose mbarrier wait can never
+ * complete, with a wait limit of limit_ms milliseconds (1..5000), waits for
+ * it, and returns what the kernel reported: GQA_ERR_TIMEOUT when the bounded
+ * wait works.  The device stays usable afterwards. */
+int gqa_selftest_bounded_wait(int limit_ms);
+
+/* Number of kernels the last successful host call enqueued (for launch
+ * accounting in benchmarks). */
+int gqa_last_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* GQA_ATTN_H */

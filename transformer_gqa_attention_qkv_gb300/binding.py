@@ -1,0 +1,223 @@
+"""ctypes binding of ``libgqa_attn.so`` (declared in ``include/gqa_attn.h``).
+
+Argument marshalling only: every function takes torch tensors on the current
+CUDA device, checks dtype/contiguity, and passes raw pointers, sizes and the
+current torch stream to the C entry point of the same name.  Every step of the
+computation runs in the library's CUDA kernels; there is no fallback.  If the
+library has not been built, the first call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libgqa_attn.so")
+
+GQA_OK = 0
+GQA_ERR_ARG = -1
+GQA_ERR_UNSUPPORTED = -2
+GQA_ERR_CUDA = -3
+GQA_ERR_TIMEOUT = -4
+GQA_ERR_WORKSPACE = -5
+
+# every symbol include/gqa_attn.h declares
+EXPORTS = (
+    "gqa_attn_workspace_size", "gqa_attn_forward_ex", "gqa_attn_forward", "gqa_qkv_proj",
+    "gqa_attention", "gqa_oproj_residual", "gqa_attn_decode_workspace_size", "gqa_attn_decode",
+    "gqa_decode_qkv", "gqa_decode_attention_workspace_size", "gqa_decode_attention",
+    "gqa_attn_cost", "gqa_last_error", "gqa_check_device_error", "gqa_selftest_bounded_wait",
+    "gqa_last_launch_count",
+)
+
+
+class GqaError(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__(f"{msg} (status {code})")
+        self.code = code
+
+
+_lib = None
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+_F = ctypes.c_float
+_Z = ctypes.c_size_t
+_LLP = ctypes.POINTER(ctypes.c_longlong)
+
+
+def lib():
+    """Load the library once; raise if it is missing (no fallback exists)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(f"{LIB_PATH} is missing: build it with "
+                           "`python -m transformer_gqa_attention_qkv_gb300.build`")
+    L = ctypes.CDLL(LIB_PATH)
+    sig = {
+        "gqa_attn_workspace_size": (_Z, [_I] * 6),
+        "gqa_attn_forward_ex": (_I, [_P] * 5 + [_F, _F] + [_I] * 7 + [_P, _P, _Z, _P]),
+        "gqa_attn_forward": (_I, [_P] * 5 + [_F, _F] + [_I] * 7 + [_P]),
+        "gqa_qkv_proj": (_I, [_P] * 4 + [_F, _F] + [_I] * 6 + [_P] * 4),
+        "gqa_attention": (_I, [_P] * 3 + [_I] * 6 + [_P, _P]),
+        "gqa_oproj_residual": (_I, [_P] * 3 + [_I] * 3 + [_P, _P]),
+        "gqa_attn_decode_workspace_size": (_Z, [_I] * 6),
+        "gqa_attn_decode": (_I, [_P] * 5 + [_F, _F] + [_I] * 5 + [_P, _P, _P, _I, _P, _P, _Z, _P]),
+        "gqa_decode_qkv": (_I, [_P] * 4 + [_F, _F] + [_I] * 5 + [_P, _P, _P, _I, _P, _P]),
+        "gqa_decode_attention_workspace_size": (_Z, [_I] * 5),
+        "gqa_decode_attention": (_I, [_P] * 4 + [_I] * 5 + [_P, _P, _Z, _P]),
+        "gqa_attn_cost": (_I, [_I] * 7 + [_LLP] * 4),
+        "gqa_last_error": (ctypes.c_char_p, []),
+        "gqa_check_device_error": (_I, []),
+        "gqa_selftest_bounded_wait": (_I, [_I]),
+        "gqa_last_launch_count": (_I, []),
+    }
+    for name, (res, args) in sig.items():
+        fn = getattr(L, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = L
+    return L
+
+
+def _check(rc: int):
+    if rc != GQA_OK:
+        msg = lib().gqa_last_error().decode(errors="replace")
+        raise GqaError(rc, msg)
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor):
+        raise TypeError("expected a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError("tensor must be on a CUDA device")
+    if not t.is_contiguous():
+        raise ValueError("tensor must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _bf16(t):
+    if t is not None and t.dtype != torch.bfloat16:
+        raise TypeError(f"expected bfloat16, got {t.dtype}")
+    return _ptr(t)
+
+
+def _i32(t):
+    if t.dtype != torch.int32:
+        raise TypeError(f"expected int32, got {t.dtype}")
+    return _ptr(t)
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+# ------------------------------------------------------------------- prefill
+
+def gqa_attn_workspace_size(B, S, hidden, Hq, Hkv, head_dim) -> int:
+    return int(lib().gqa_attn_workspace_size(B, S, hidden, Hq, Hkv, head_dim))
+
+
+def gqa_attn_forward_ex(x, Wqkv, Wo, q_norm_w, k_norm_w, rope_theta, eps, B, S, hidden, Hq, Hkv,
+                        head_dim, causal, out, workspace, stream=None):
+    _check(lib().gqa_attn_forward_ex(_bf16(x), _bf16(Wqkv), _bf16(Wo), _bf16(q_norm_w), _bf16(k_norm_w),
+                                     rope_theta, eps, B, S, hidden, Hq, Hkv, head_dim, int(causal),
+                                     _bf16(out), _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                     _stream(stream)))
+    return out
+
+
+def gqa_attn_forward(x, Wqkv, Wo, q_norm_w, k_norm_w, rope_theta, eps, B, S, hidden, Hq, Hkv,
+                     head_dim, causal, out):
+    """Runs on the legacy default stream with the library's own workspace."""
+    _check(lib().gqa_attn_forward(_bf16(x), _bf16(Wqkv), _bf16(Wo), _bf16(q_norm_w), _bf16(k_norm_w),
+                                  rope_theta, eps, B, S, hidden, Hq, Hkv, head_dim, int(causal), _bf16(out)))
+    return out
+
+
+def gqa_qkv_proj(x, Wqkv, q_norm_w, k_norm_w, rope_theta, eps, B, S, hidden, Hq, Hkv, head_dim,
+                 q_out, k_out, v_out, stream=None):
+    _check(lib().gqa_qkv_proj(_bf16(x), _bf16(Wqkv), _bf16(q_norm_w), _bf16(k_norm_w), rope_theta, eps,
+                              B, S, hidden, Hq, Hkv, head_dim, _bf16(q_out), _bf16(k_out), _bf16(v_out),
+                              _stream(stream)))
+
+
+def gqa_attention(q, k, v, B, S, Hq, Hkv, head_dim, causal, attn_out, stream=None):
+    _check(lib().gqa_attention(_bf16(q), _bf16(k), _bf16(v), B, S, Hq, Hkv, head_dim, int(causal),
+                               _bf16(attn_out), _stream(stream)))
+
+
+def gqa_oproj_residual(attn, Wo, x, M, hidden, q_width, out, stream=None):
+    _check(lib().gqa_oproj_residual(_bf16(attn), _bf16(Wo), _bf16(x), M, hidden, q_width, _bf16(out),
+                                    _stream(stream)))
+
+
+# -------------------------------------------------------------------- decode
+
+def gqa_attn_decode_workspace_size(B, hidden, Hq, Hkv, head_dim, Lmax) -> int:
+    return int(lib().gqa_attn_decode_workspace_size(B, hidden, Hq, Hkv, head_dim, Lmax))
+
+
+def gqa_attn_decode(x, Wqkv, Wo, q_norm_w, k_norm_w, rope_theta, eps, B, hidden, Hq, Hkv, head_dim,
+                    k_cache, v_cache, cache_len, Lmax, out, workspace, stream=None):
+    _check(lib().gqa_attn_decode(_bf16(x), _bf16(Wqkv), _bf16(Wo), _bf16(q_norm_w), _bf16(k_norm_w),
+                                 rope_theta, eps, B, hidden, Hq, Hkv, head_dim, _bf16(k_cache),
+                                 _bf16(v_cache), _i32(cache_len), Lmax, _bf16(out), _ptr(workspace),
+                                 workspace.numel() * workspace.element_size(), _stream(stream)))
+    return out
+
+
+def gqa_decode_qkv(x, Wqkv, q_norm_w, k_norm_w, rope_theta, eps, B, hidden, Hq, Hkv, head_dim,
+                   k_cache, v_cache, cache_len, Lmax, q_out, stream=None):
+    _check(lib().gqa_decode_qkv(_bf16(x), _bf16(Wqkv), _bf16(q_norm_w), _bf16(k_norm_w), rope_theta, eps,
+                                B, hidden, Hq, Hkv, head_dim, _bf16(k_cache), _bf16(v_cache),
+                                _i32(cache_len), Lmax, _bf16(q_out), _stream(stream)))
+
+
+def gqa_decode_attention_workspace_size(B, Hq, Hkv, head_dim, Lmax) -> int:
+    return int(lib().gqa_decode_attention_workspace_size(B, Hq, Hkv, head_dim, Lmax))
+
+
+def gqa_decode_attention(q, k_cache, v_cache, kv_len, B, Hq, Hkv, head_dim, Lmax, attn_out, workspace,
+                         stream=None):
+    _check(lib().gqa_decode_attention(_bf16(q), _bf16(k_cache), _bf16(v_cache), _i32(kv_len), B, Hq, Hkv,
+                                      head_dim, Lmax, _bf16(attn_out), _ptr(workspace),
+                                      workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+# ---------------------------------------------------------------- accounting
+
+def gqa_attn_cost(B, S, hidden, Hq, Hkv, head_dim, causal=True) -> dict:
+    vals = [ctypes.c_longlong() for _ in range(4)]
+    _check(lib().gqa_attn_cost(B, S, hidden, Hq, Hkv, head_dim, int(causal), *[ctypes.byref(v) for v in vals]))
+    return {"weights": vals[0].value, "proj_macs_per_token": vals[1].value,
+            "attn_macs": vals[2].value, "flops": vals[3].value}
+
+
+def gqa_last_error() -> str:
+    return lib().gqa_last_error().decode(errors="replace")
+
+
+def gqa_check_device_error() -> int:
+    return int(lib().gqa_check_device_error())
+
+
+def gqa_selftest_bounded_wait(limit_ms: int) -> int:
+    return int(lib().gqa_selftest_bounded_wait(limit_ms))
+
+
+def gqa_last_launch_count() -> int:
+    return int(lib().gqa_last_launch_count())
+
+
+# --------------------------------------------------------- tensor helpers
+
+def new_workspace(nbytes: int, device=None) -> torch.Tensor:
+    """A uint8 device buffer (torch allocations are 256-byte aligned)."""
+    return torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=device or "cuda")

@@ -1,0 +1,597 @@
+// api.cu -- the C ABI declared in include/gqa_attn.h: argument validation,
+// per-device state (error word, RoPE tables, default workspace), tensor-map
+// encoding, and the launch sequences of the prefill forward and decode step.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <math.h>
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <mutex>
+#include <vector>
+
+#include "../../include/gqa_attn.h"
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace gqa {
+
+// ------------------------------------------------------------ error state
+
+static thread_local char g_msg[512] = "";
+static thread_local int g_launches = 0;
+
+static int fail(int code, const char *fmt, ...)
+{
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_msg, sizeof g_msg, fmt, ap);
+    va_end(ap);
+    return code;
+}
+
+static int cuda_fail(cudaError_t e, const char *what)
+{
+    return fail(GQA_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+// -------------------------------------------------------- tensor-map encoder
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn get_encoder()
+{
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+CUresult encode_tmap(CUtensorMap *map, const void *base, int rank, const uint64_t *dims, const uint64_t *strides_bytes,
+                     const uint32_t *box, bool swizzle128)
+{
+    EncodeTiledFn fn = get_encoder();
+    if (!fn) return CUDA_ERROR_NOT_INITIALIZED;
+    cuuint64_t d[5], s[4];
+    cuuint32_t b[5], es[5];
+    for (int i = 0; i < rank; ++i) {
+        d[i] = dims[i];
+        b[i] = box[i];
+        es[i] = 1;
+        if (i + 1 < rank) s[i] = strides_bytes[i];
+    }
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, const_cast<void *>(base), d, s, b, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+}
+
+// --------------------------------------------------------- per-device state
+
+struct RopeTable {
+    double theta;
+    int d;
+    int rows;
+    float2 *dev;
+};
+
+struct DeviceState {
+    bool init = false;
+    int num_sms = 0;
+    unsigned *err = nullptr;             // device error word
+    std::vector<RopeTable> ropes;        // kept until exit (kernels may still read old ones)
+    void *ws = nullptr;                  // default workspace of gqa_attn_forward
+    size_t ws_bytes = 0;
+};
+
+static std::mutex g_mu;
+static DeviceState g_dev[64];
+
+static int device_state(DeviceState **out)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= 64) return fail(GQA_ERR_CUDA, "device index %d out of range", dev);
+    DeviceState &st = g_dev[dev];
+    if (!st.init) {
+        int major = 0, minor = 0;
+        cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+        if (major != 10 || minor != 3)
+            return fail(GQA_ERR_UNSUPPORTED, "device %d is sm_%d%d; this library is built for sm_103a", dev, major,
+                        minor);
+        e = cudaDeviceGetAttribute(&st.num_sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
+        e = cudaMalloc(&st.err, 256);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaMalloc(error word)");
+        e = cudaMemset(st.err, 0, 256);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaMemset(error word)");
+        if (!get_encoder()) return fail(GQA_ERR_CUDA, "cuTensorMapEncodeTiled entry point unavailable");
+        st.init = true;
+    }
+    *out = &st;
+    return GQA_OK;
+}
+
+// cos/sin(pos * theta^(-2i/d)) for pos < rows, i < d/2, computed in double on
+// the host and stored as fp32 (cos, sin) pairs.  Angles reach ~1.6e4 rad, where
+// an fp32 angle would already be off by ~1e-3 rad.
+static int rope_table(DeviceState &st, double theta, int d, int rows, const float2 **out)
+{
+    for (const RopeTable &t : st.ropes)
+        if (t.theta == theta && t.d == d && t.rows >= rows) {
+            *out = t.dev;
+            return GQA_OK;
+        }
+    int cap = 4096;
+    while (cap < rows) cap *= 2;
+    std::vector<float2> host((size_t)cap * (d / 2));
+    for (int p = 0; p < cap; ++p)
+        for (int i = 0; i < d / 2; ++i) {
+            const double f = (double)p * pow(theta, -2.0 * i / d);
+            host[(size_t)p * (d / 2) + i] = make_float2((float)cos(f), (float)sin(f));
+        }
+    float2 *dev = nullptr;
+    cudaError_t e = cudaMalloc(&dev, host.size() * sizeof(float2));
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMalloc(rope table)");
+    e = cudaMemcpy(dev, host.data(), host.size() * sizeof(float2), cudaMemcpyHostToDevice);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpy(rope table)");
+    st.ropes.push_back({theta, d, cap, dev});
+    *out = dev;
+    return GQA_OK;
+}
+
+// ------------------------------------------------------------- validation
+
+static bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
+
+static bool overlap(const void *a, size_t na, const void *b, size_t nb)
+{
+    const uintptr_t x = (uintptr_t)a, y = (uintptr_t)b;
+    return x < y + nb && y < x + na;
+}
+
+static int check_layer(int B, int S, int hidden, int Hq, int Hkv, int d, const void *qn, const void *kn)
+{
+    if (B <= 0 || S <= 0 || hidden <= 0 || Hq <= 0 || Hkv <= 0 || d <= 0)
+        return fail(GQA_ERR_ARG, "sizes must be positive (B=%d S=%d hidden=%d Hq=%d Hkv=%d head_dim=%d)", B, S, hidden,
+                    Hq, Hkv, d);
+    if (Hq % Hkv) return fail(GQA_ERR_ARG, "Hq=%d is not a multiple of Hkv=%d", Hq, Hkv);
+    if (d & 1) return fail(GQA_ERR_ARG, "head_dim=%d is odd; RoPE pairs need an even head_dim", d);
+    if ((qn == nullptr) != (kn == nullptr))
+        return fail(GQA_ERR_ARG, "q_norm_w and k_norm_w must both be given or both be NULL");
+    if (d != 64 && d != 128) return fail(GQA_ERR_UNSUPPORTED, "unsupported head_dim: %d (supported: 64, 128)", d);
+    if (hidden % 8) return fail(GQA_ERR_UNSUPPORTED, "unsupported hidden: %d (must be a multiple of 8)", hidden);
+    if ((long long)B * S > (1LL << 30) || (long long)(Hq + 2 * Hkv) * d > (1 << 20) || hidden > (1 << 20))
+        return fail(GQA_ERR_UNSUPPORTED, "problem too large");
+    return GQA_OK;
+}
+
+static int check_group_pow2(int Hq, int Hkv)
+{
+    const int G = Hq / Hkv;
+    if ((G & (G - 1)) || G > 128)
+        return fail(GQA_ERR_UNSUPPORTED, "unsupported group size Hq/Hkv=%d (a power of two up to 128)", G);
+    return GQA_OK;
+}
+
+static size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+struct FwdLayout {
+    size_t q, k, v, attn, total;
+};
+
+static FwdLayout fwd_layout(int B, int S, int Hq, int Hkv, int d)
+{
+    FwdLayout L;
+    const size_t tok = (size_t)B * S;
+    L.q = 0;
+    L.k = L.q + align256(tok * Hq * d * 2);
+    L.v = L.k + align256(tok * Hkv * d * 2);
+    L.attn = L.v + align256(tok * Hkv * d * 2);
+    L.total = L.attn + align256(tok * Hq * d * 2);
+    return L;
+}
+
+// ------------------------------------------------------------ stage runners
+
+static int run_qkv(DeviceState &st, const gqa_bf16 *x, const gqa_bf16 *Wqkv, const gqa_bf16 *qn, const gqa_bf16 *kn,
+                   float theta, float eps, int B, int S, int hidden, int Hq, int Hkv, int d, const int *pos_dev,
+                   int q_seq, int kv_seq, int rope_rows, gqa_bf16 *q_out, gqa_bf16 *k_out, gqa_bf16 *v_out,
+                   cudaStream_t stream)
+{
+    const float2 *rope = nullptr;
+    int rc;
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        rc = rope_table(st, (double)theta, d, rope_rows, &rope);
+    }
+    if (rc) return rc;
+    GemmProblem p{x, Wqkv, pos_dev ? B : B * S, (Hq + 2 * Hkv) * d, hidden};
+    QkvEpilogue e{};
+    e.Hq = Hq;
+    e.Hkv = Hkv;
+    e.d = d;
+    e.S = S;
+    e.pos_dev = pos_dev;
+    e.q_seq = q_seq;
+    e.kv_seq = kv_seq;
+    e.q_norm_w = qn;
+    e.k_norm_w = kn;
+    e.eps = eps;
+    e.rope = rope;
+    e.rope_rows = rope_rows;
+    e.q_out = q_out;
+    e.k_out = k_out;
+    e.v_out = v_out;
+    cudaError_t ce = launch_gemm_qkv(p, e, st.err, st.num_sms, stream);
+    if (ce != cudaSuccess) return cuda_fail(ce, "QKV projection launch");
+    ++g_launches;
+    return GQA_OK;
+}
+
+static int run_attention(DeviceState &st, const gqa_bf16 *q, const gqa_bf16 *k, const gqa_bf16 *v, int B, int S,
+                         int Hq, int Hkv, int d, int causal, gqa_bf16 *out, cudaStream_t stream)
+{
+    AttentionProblem p{q, k, v, out, B, S, Hq, Hkv, d, causal ? 1 : 0};
+    cudaError_t ce = launch_attention(p, st.err, st.num_sms, stream);
+    if (ce != cudaSuccess) return cuda_fail(ce, "attention launch");
+    ++g_launches;
+    return GQA_OK;
+}
+
+static int run_oproj(DeviceState &st, const gqa_bf16 *attn, const gqa_bf16 *Wo, const gqa_bf16 *x, int M, int hidden,
+                     int qw, gqa_bf16 *out, cudaStream_t stream)
+{
+    GemmProblem p{attn, Wo, M, hidden, qw};
+    ResidualEpilogue e{x, out};
+    cudaError_t ce = launch_gemm_residual(p, e, st.err, st.num_sms, stream);
+    if (ce != cudaSuccess) return cuda_fail(ce, "o_proj launch");
+    ++g_launches;
+    return GQA_OK;
+}
+
+static int run_decode_attn(DeviceState &st, const gqa_bf16 *q, const gqa_bf16 *kc, const gqa_bf16 *vc,
+                           const int *len, int bias, int B, int Hq, int Hkv, int d, int Lmax, gqa_bf16 *out,
+                           float *partials, int splits, cudaStream_t stream)
+{
+    DecodeAttentionProblem p{};
+    p.q = q;
+    p.k_cache = kc;
+    p.v_cache = vc;
+    p.len = len;
+    p.len_bias = bias;
+    p.out = out;
+    p.B = B;
+    p.Hq = Hq;
+    p.Hkv = Hkv;
+    p.d = d;
+    p.Lmax = Lmax;
+    p.partials = partials;
+    p.splits = splits;
+    cudaError_t ce = launch_decode_attention(p, st.err, stream);
+    if (ce != cudaSuccess) return cuda_fail(ce, "decode attention launch");
+    g_launches += 2;
+    return GQA_OK;
+}
+
+}  // namespace gqa
+
+using namespace gqa;
+
+// =================================================================== C ABI
+
+extern "C" {
+
+const char *gqa_last_error(void) { return g_msg; }
+
+int gqa_last_launch_count(void) { return g_launches; }
+
+size_t gqa_attn_workspace_size(int B, int S, int hidden, int Hq, int Hkv, int head_dim)
+{
+    if (B <= 0 || S <= 0 || hidden <= 0 || Hq <= 0 || Hkv <= 0 || head_dim <= 0) return 0;
+    return fwd_layout(B, S, Hq, Hkv, head_dim).total;
+}
+
+int gqa_qkv_proj(const gqa_bf16 *x, const gqa_bf16 *Wqkv, const gqa_bf16 *q_norm_w, const gqa_bf16 *k_norm_w,
+                 float rope_theta, float eps, int B, int S, int hidden, int Hq, int Hkv, int head_dim, gqa_bf16 *q_out,
+                 gqa_bf16 *k_out, gqa_bf16 *v_out, void *stream)
+{
+    g_launches = 0;
+    int rc = check_layer(B, S, hidden, Hq, Hkv, head_dim, q_norm_w, k_norm_w);
+    if (rc) return rc;
+    if (!x || !Wqkv || !q_out || !k_out || !v_out) return fail(GQA_ERR_ARG, "null tensor pointer");
+    if (!aligned16(x) || !aligned16(Wqkv) || !aligned16(q_out) || !aligned16(k_out) || !aligned16(v_out))
+        return fail(GQA_ERR_ARG, "tensor pointers must be 16-byte aligned");
+    if (!(rope_theta > 0.0f) || !(eps >= 0.0f)) return fail(GQA_ERR_ARG, "rope_theta must be > 0 and eps >= 0");
+    DeviceState *st;
+    if ((rc = device_state(&st))) return rc;
+    return run_qkv(*st, x, Wqkv, q_norm_w, k_norm_w, rope_theta, eps, B, S, hidden, Hq, Hkv, head_dim, nullptr, S, S,
+                   S, q_out, k_out, v_out, (cudaStream_t)stream);
+}
+
+int gqa_attention(const gqa_bf16 *q, const gqa_bf16 *k, const gqa_bf16 *v, int B, int S, int Hq, int Hkv,
+                  int head_dim, int causal, gqa_bf16 *attn_out, void *stream)
+{
+    g_launches = 0;
+    int rc = check_layer(B, S, 8, Hq, Hkv, head_dim, nullptr, nullptr);
+    if (rc) return rc;
+    if ((rc = check_group_pow2(Hq, Hkv))) return rc;
+    if (!q || !k || !v || !attn_out) return fail(GQA_ERR_ARG, "null tensor pointer");
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(attn_out))
+        return fail(GQA_ERR_ARG, "tensor pointers must be 16-byte aligned");
+    DeviceState *st;
+    if ((rc = device_state(&st))) return rc;
+    return run_attention(*st, q, k, v, B, S, Hq, Hkv, head_dim, causal, attn_out, (cudaStream_t)stream);
+}
+
+int gqa_oproj_residual(const gqa_bf16 *attn, const gqa_bf16 *Wo, const gqa_bf16 *x, int M, int hidden, int q_width,
+                       gqa_bf16 *out, void *stream)
+{
+    g_launches = 0;
+    if (M <= 0 || hidden <= 0 || q_width <= 0) return fail(GQA_ERR_ARG, "sizes must be positive");
+    if (hidden % 8 || q_width % 8) return fail(GQA_ERR_UNSUPPORTED, "hidden and q_width must be multiples of 8");
+    if (!attn || !Wo || !x || !out) return fail(GQA_ERR_ARG, "null tensor pointer");
+    if (!aligned16(attn) || !aligned16(Wo) || !aligned16(x) || !aligned16(out))
+        return fail(GQA_ERR_ARG, "tensor pointers must be 16-byte aligned");
+    if (overlap(out, (size_t)M * hidden * 2, x, (size_t)M * hidden * 2))
+        return fail(GQA_ERR_ARG, "out must not overlap x");
+    DeviceState *st;
+    int rc;
+    if ((rc = device_state(&st))) return rc;
+    return run_oproj(*st, attn, Wo, x, M, hidden, q_width, out, (cudaStream_t)stream);
+}
+
+int gqa_attn_forward_ex(const gqa_bf16 *x, const gqa_bf16 *Wqkv, const gqa_bf16 *Wo, const gqa_bf16 *q_norm_w,
+                        const gqa_bf16 *k_norm_w, float rope_theta, float eps, int B, int S, int hidden, int Hq,
+                        int Hkv, int head_dim, int causal, gqa_bf16 *out, void *workspace, size_t workspace_bytes,
+                        void *stream)
+{
+    g_launches = 0;
+    int rc = check_layer(B, S, hidden, Hq, Hkv, head_dim, q_norm_w, k_norm_w);
+    if (rc) return rc;
+    if ((rc = check_group_pow2(Hq, Hkv))) return rc;
+    if (!x || !Wqkv || !Wo || !out) return fail(GQA_ERR_ARG, "null tensor pointer");
+    if (!aligned16(x) || !aligned16(Wqkv) || !aligned16(Wo) || !aligned16(out))
+        return fail(GQA_ERR_ARG, "tensor pointers must be 16-byte aligned");
+    if (!(rope_theta > 0.0f) || !(eps >= 0.0f)) return fail(GQA_ERR_ARG, "rope_theta must be > 0 and eps >= 0");
+    const size_t nx = (size_t)B * S * hidden * 2;
+    const size_t nw = (size_t)(Hq + 2 * Hkv) * head_dim * hidden * 2, no = (size_t)hidden * Hq * head_dim * 2;
+    if (overlap(out, nx, x, nx) || overlap(out, nx, Wqkv, nw) || overlap(out, nx, Wo, no))
+        return fail(GQA_ERR_ARG, "out must not overlap x or the weights");
+    const FwdLayout L = fwd_layout(B, S, Hq, Hkv, head_dim);
+    if (!workspace || workspace_bytes < L.total)
+        return fail(GQA_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", L.total,
+                    workspace ? workspace_bytes : (size_t)0);
+    if (((uintptr_t)workspace & 255u) != 0) return fail(GQA_ERR_ARG, "workspace must be 256-byte aligned");
+    if (overlap(workspace, L.total, out, nx) || overlap(workspace, L.total, x, nx))
+        return fail(GQA_ERR_ARG, "workspace must not overlap the arguments");
+    DeviceState *st;
+    if ((rc = device_state(&st))) return rc;
+    uint8_t *ws = (uint8_t *)workspace;
+    gqa_bf16 *q = (gqa_bf16 *)(ws + L.q), *k = (gqa_bf16 *)(ws + L.k), *v = (gqa_bf16 *)(ws + L.v);
+    gqa_bf16 *attn = (gqa_bf16 *)(ws + L.attn);
+    cudaStream_t s = (cudaStream_t)stream;
+    if ((rc = run_qkv(*st, x, Wqkv, q_norm_w, k_norm_w, rope_theta, eps, B, S, hidden, Hq, Hkv, head_dim, nullptr, S,
+                      S, S, q, k, v, s)))
+        return rc;
+    if ((rc = run_attention(*st, q, k, v, B, S, Hq, Hkv, head_dim, causal, attn, s))) return rc;
+    return run_oproj(*st, attn, Wo, x, B * S, hidden, Hq * head_dim, out, s);
+}
+
+int gqa_attn_forward(const gqa_bf16 *x, const gqa_bf16 *Wqkv, const gqa_bf16 *Wo, const gqa_bf16 *q_norm_w,
+                     const gqa_bf16 *k_norm_w, float rope_theta, float eps, int B, int S, int hidden, int Hq, int Hkv,
+                     int head_dim, int causal, gqa_bf16 *out)
+{
+    g_launches = 0;
+    int rc = check_layer(B, S, hidden, Hq, Hkv, head_dim, q_norm_w, k_norm_w);
+    if (rc) return rc;
+    DeviceState *st;
+    if ((rc = device_state(&st))) return rc;
+    const size_t need = fwd_layout(B, S, Hq, Hkv, head_dim).total;
+    void *ws;
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        if (st->ws_bytes < need) {
+            if (st->ws) {
+                cudaError_t e = cudaDeviceSynchronize();
+                if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
+                cudaFree(st->ws);
+                st->ws = nullptr;
+                st->ws_bytes = 0;
+            }
+            cudaError_t e = cudaMalloc(&st->ws, need);
+            if (e != cudaSuccess) return cuda_fail(e, "cudaMalloc(workspace)");
+            st->ws_bytes = need;
+        }
+        ws = st->ws;
+    }
+    return gqa_attn_forward_ex(x, Wqkv, Wo, q_norm_w, k_norm_w, rope_theta, eps, B, S, hidden, Hq, Hkv, head_dim,
+                               causal, out, ws, need, nullptr);
+}
+
+// ------------------------------------------------------------------ decode
+
+static size_t decode_layout(int B, int Hq, int Hkv, int d, int Lmax, int num_sms, size_t *off_attn,
+                            size_t *off_part, int *splits)
+{
+    const int sp = decode_choose_splits(B, Hkv, Lmax, num_sms);
+    const size_t q = align256((size_t)B * Hq * d * 2);
+    const size_t a = align256((size_t)B * Hq * d * 2);
+    const size_t p = align256(decode_partials_floats(B, Hq, sp, d) * 4);
+    if (off_attn) *off_attn = q;
+    if (off_part) *off_part = q + a;
+    if (splits) *splits = sp;
+    return q + a + p;
+}
+
+static int num_sms_current()
+{
+    int dev = 0, n = 148;
+    if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    return n > 0 ? n : 148;
+}
+
+size_t gqa_decode_attention_workspace_size(int B, int Hq, int Hkv, int head_dim, int Lmax)
+{
+    if (B <= 0 || Hq <= 0 || Hkv <= 0 || head_dim <= 0 || Lmax <= 0) return 0;
+    const int sp = decode_choose_splits(B, Hkv, Lmax, num_sms_current());
+    return align256(decode_partials_floats(B, Hq, sp, head_dim) * 4);
+}
+
+size_t gqa_attn_decode_workspace_size(int B, int hidden, int Hq, int Hkv, int head_dim, int Lmax)
+{
+    if (B <= 0 || hidden <= 0 || Hq <= 0 || Hkv <= 0 || head_dim <= 0 || Lmax <= 0) return 0;
+    return decode_layout(B, Hq, Hkv, head_dim, Lmax, num_sms_current(), nullptr, nullptr, nullptr);
+}
+
+static int check_decode(int B, int hidden, int Hq, int Hkv, int d, int Lmax, const void *qn, const void *kn)
+{
+    int rc = check_layer(B, 1, hidden, Hq, Hkv, d, qn, kn);
+    if (rc) return rc;
+    if (Lmax <= 0) return fail(GQA_ERR_ARG, "Lmax must be positive");
+    const int G = Hq / Hkv;
+    if (G != 1 && G != 2 && G != 4 && G != 8)
+        return fail(GQA_ERR_UNSUPPORTED, "unsupported decode group size Hq/Hkv=%d (supported: 1, 2, 4, 8)", G);
+    if ((long long)B * Hkv * Lmax * d > (1LL << 40)) return fail(GQA_ERR_UNSUPPORTED, "cache too large");
+    return GQA_OK;
+}
+
+int gqa_decode_qkv(const gqa_bf16 *x, const gqa_bf16 *Wqkv, const gqa_bf16 *q_norm_w, const gqa_bf16 *k_norm_w,
+                   float rope_theta, float eps, int B, int hidden, int Hq, int Hkv, int head_dim, gqa_bf16 *k_cache,
+                   gqa_bf16 *v_cache, const int *cache_len, int Lmax, gqa_bf16 *q_out, void *stream)
+{
+    g_launches = 0;
+    int rc = check_decode(B, hidden, Hq, Hkv, head_dim, Lmax, q_norm_w, k_norm_w);
+    if (rc) return rc;
+    if (!x || !Wqkv || !k_cache || !v_cache || !cache_len || !q_out) return fail(GQA_ERR_ARG, "null pointer");
+    if (!aligned16(x) || !aligned16(Wqkv) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(q_out))
+        return fail(GQA_ERR_ARG, "tensor pointers must be 16-byte aligned");
+    if (!(rope_theta > 0.0f) || !(eps >= 0.0f)) return fail(GQA_ERR_ARG, "rope_theta must be > 0 and eps >= 0");
+    DeviceState *st;
+    if ((rc = device_state(&st))) return rc;
+    return run_qkv(*st, x, Wqkv, q_norm_w, k_norm_w, rope_theta, eps, B, 1, hidden, Hq, Hkv, head_dim, cache_len, 1,
+                   Lmax, Lmax, q_out, k_cache, v_cache, (cudaStream_t)stream);
+}
+
+int gqa_decode_attention(const gqa_bf16 *q, const gqa_bf16 *k_cache, const gqa_bf16 *v_cache, const int *kv_len,
+                         int B, int Hq, int Hkv, int head_dim, int Lmax, gqa_bf16 *attn_out, void *workspace,
+                         size_t workspace_bytes, void *stream)
+{
+    g_launches = 0;
+    int rc = check_decode(B, 8, Hq, Hkv, head_dim, Lmax, nullptr, nullptr);
+    if (rc) return rc;
+    if (!q || !k_cache || !v_cache || !kv_len || !attn_out) return fail(GQA_ERR_ARG, "null pointer");
+    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(attn_out))
+        return fail(GQA_ERR_ARG, "tensor pointers must be 16-byte aligned");
+    DeviceState *st;
+    if ((rc = device_state(&st))) return rc;
+    const int sp = decode_choose_splits(B, Hkv, Lmax, st->num_sms);
+    const size_t need = align256(decode_partials_floats(B, Hq, sp, head_dim) * 4);
+    if (!workspace || workspace_bytes < need)
+        return fail(GQA_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", need,
+                    workspace ? workspace_bytes : (size_t)0);
+    if (!aligned16(workspace)) return fail(GQA_ERR_ARG, "workspace must be 16-byte aligned");
+    return run_decode_attn(*st, q, k_cache, v_cache, kv_len, 0, B, Hq, Hkv, head_dim, Lmax, attn_out,
+                           (float *)workspace, sp, (cudaStream_t)stream);
+}
+
+int gqa_attn_decode(const gqa_bf16 *x, const gqa_bf16 *Wqkv, const gqa_bf16 *Wo, const gqa_bf16 *q_norm_w,
+                    const gqa_bf16 *k_norm_w, float rope_theta, float eps, int B, int hidden, int Hq, int Hkv,
+                    int head_dim, gqa_bf16 *k_cache, gqa_bf16 *v_cache, const int *cache_len, int Lmax,
+                    gqa_bf16 *out, void *workspace, size_t workspace_bytes, void *stream)
+{
+    g_launches = 0;
+    int rc = check_decode(B, hidden, Hq, Hkv, head_dim, Lmax, q_norm_w, k_norm_w);
+    if (rc) return rc;
+    if (!x || !Wqkv || !Wo || !k_cache || !v_cache || !cache_len || !out) return fail(GQA_ERR_ARG, "null pointer");
+    if (!aligned16(x) || !aligned16(Wqkv) || !aligned16(Wo) || !aligned16(k_cache) || !aligned16(v_cache) ||
+        !aligned16(out))
+        return fail(GQA_ERR_ARG, "tensor pointers must be 16-byte aligned");
+    if (!(rope_theta > 0.0f) || !(eps >= 0.0f)) return fail(GQA_ERR_ARG, "rope_theta must be > 0 and eps >= 0");
+    if (overlap(out, (size_t)B * hidden * 2, x, (size_t)B * hidden * 2))
+        return fail(GQA_ERR_ARG, "out must not overlap x");
+    DeviceState *st;
+    if ((rc = device_state(&st))) return rc;
+    size_t off_attn, off_part;
+    int sp;
+    const size_t need = decode_layout(B, Hq, Hkv, head_dim, Lmax, st->num_sms, &off_attn, &off_part, &sp);
+    if (!workspace || workspace_bytes < need)
+        return fail(GQA_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", need,
+                    workspace ? workspace_bytes : (size_t)0);
+    if (((uintptr_t)workspace & 255u) != 0) return fail(GQA_ERR_ARG, "workspace must be 256-byte aligned");
+    uint8_t *ws = (uint8_t *)workspace;
+    gqa_bf16 *q = (gqa_bf16 *)ws, *attn = (gqa_bf16 *)(ws + off_attn);
+    float *part = (float *)(ws + off_part);
+    cudaStream_t s = (cudaStream_t)stream;
+    if ((rc = run_qkv(*st, x, Wqkv, q_norm_w, k_norm_w, rope_theta, eps, B, 1, hidden, Hq, Hkv, head_dim, cache_len, 1,
+                      Lmax, Lmax, q, k_cache, v_cache, s)))
+        return rc;
+    if ((rc = run_decode_attn(*st, q, k_cache, v_cache, cache_len, 1, B, Hq, Hkv, head_dim, Lmax, attn, part, sp, s)))
+        return rc;
+    return run_oproj(*st, attn, Wo, x, B, hidden, Hq * head_dim, out, s);
+}
+
+// ---------------------------------------------------------------- accounting
+
+int gqa_attn_cost(int B, int S, int hidden, int Hq, int Hkv, int head_dim, int causal, long long *weights,
+                  long long *proj_macs_per_token, long long *attn_macs, long long *flops)
+{
+    if (B <= 0 || S <= 0 || hidden <= 0 || Hq <= 0 || Hkv <= 0 || head_dim <= 0)
+        return fail(GQA_ERR_ARG, "sizes must be positive");
+    const long long h = hidden, d = head_dim;
+    const long long w = h * (Hq + 2LL * Hkv) * d + (long long)Hq * d * h;
+    const long long pairs = causal ? (long long)S * (S + 1) / 2 : (long long)S * S;
+    const long long am = 2LL * d * Hq * pairs * B;
+    if (weights) *weights = w;
+    if (proj_macs_per_token) *proj_macs_per_token = w;
+    if (attn_macs) *attn_macs = am;
+    if (flops) *flops = 2LL * ((long long)B * S * w + am);
+    return GQA_OK;
+}
+
+// --------------------------------------------------------------- diagnostics
+
+int gqa_check_device_error(void)
+{
+    DeviceState *st;
+    int rc = device_state(&st);
+    if (rc) return rc;
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
+    unsigned word = 0;
+    e = cudaMemcpy(&word, st->err, sizeof word, cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpy(error word)");
+    if (word) {
+        e = cudaMemset(st->err, 0, sizeof word);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaMemset(error word)");
+    }
+    if (word & kErrTimeout) return fail(GQA_ERR_TIMEOUT, "a bounded device wait gave up (error word 0x%x)", word);
+    if (word & kErrIndex) return fail(GQA_ERR_ARG, "a device-side index check failed (error word 0x%x)", word);
+    return GQA_OK;
+}
+
+int gqa_selftest_bounded_wait(int limit_ms)
+{
+    if (limit_ms < 1 || limit_ms > 5000) return fail(GQA_ERR_ARG, "limit_ms must be in [1, 5000]");
+    DeviceState *st;
+    int rc = device_state(&st);
+    if (rc) return rc;
+    if ((rc = gqa_check_device_error())) return rc;  // start from a clean word
+    cudaError_t e = launch_selftest_wait(st->err, (unsigned long long)limit_ms * 1000000ull, nullptr);
+    if (e != cudaSuccess) return cuda_fail(e, "self-test launch");
+    return gqa_check_device_error();
+}
+
+}  // extern "C"

@@ -1,0 +1,416 @@
+// gemm.cu -- persistent tcgen05 GEMM for the two projections of the layer.
+//
+//   QKV projection ([NeoX] "Fused QKV projection": hidden -> Hq*d + 2*Hkv*d)
+//   with per-head RMSNorm of Q and K ([T07] §3 "QK-Norm") and RoPE on Q and K
+//   ([T07] §4 step 3) fused into the epilogue, written head-major
+//   ([T07] §4 step 4, (batch, heads, seq, head_dim)).
+//
+//   o_proj ([NeoX] "Output projection": Hq*d -> hidden) with the residual add
+//   ([NeoX] "Qwen3-0.6B example", residual addition) fused into the epilogue.
+//
+// Structure (one CTA per SM, persistent over output tiles):
+//   warp 0      TMA producer: A/B k-slices into a STAGES-deep shared ring
+//   warp 1      MMA issuer: tcgen05.mma 128 x BN x 16 into a TMEM accumulator;
+//               two accumulators so tile i's epilogue overlaps tile i+1's loop
+//   warps 2..5  epilogue: tcgen05.ld (one thread = one output row), fused
+//               math, 16-byte global stores
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace gqa {
+
+namespace {
+
+constexpr int BM = 128;
+constexpr int BK = 64;  // one 128-byte swizzle row of bf16
+constexpr int kThreads = 192;
+
+enum { EPI_QKV = 0, EPI_RESIDUAL = 1 };
+
+struct GemmParams {
+    int M, N, K;
+    int num_m, num_n, num_k, num_tiles;
+    unsigned *err;
+    QkvEpilogue qkv;
+    ResidualEpilogue res;
+};
+
+template <int BN, int STAGES>
+struct Smem {
+    static constexpr int A_BYTES = BM * BK * 2;
+    static constexpr int B_BYTES = BN * BK * 2;
+    static constexpr int RING = STAGES * (A_BYTES + B_BYTES);
+    static constexpr int BARS = RING;                       // 2*STAGES + 5 mbarriers
+    static constexpr int TMEM_SLOT = BARS + (2 * STAGES + 5) * 8;
+    static constexpr int NORM = (TMEM_SLOT + 16 + 15) & ~15;  // 2 x 128 floats
+    static constexpr int TOTAL = NORM + 2 * 128 * 4;
+    static constexpr int ALLOC = TOTAL + 1024;               // slack for 1024-byte alignment
+};
+
+// Grouped rasterisation: walk 8 M-blocks per N-block so that concurrently
+// running CTAs share A rows and B rows in L2.
+DEVI void tile_coords(int tile, int num_m, int num_n, int &mb, int &nb)
+{
+    constexpr int GM = 8;
+    const int per_group = GM * num_n;
+    const int grp = tile / per_group;
+    const int first = grp * GM;
+    const int gm = min(num_m - first, GM);
+    const int local = tile - grp * per_group;
+    mb = first + local % gm;
+    nb = local / gm;
+}
+
+DEVI void store_row_bf16(uint16_t *dst, const float *v, int n)  // n multiple of 8, dst 16B aligned
+{
+    uint4 *d4 = reinterpret_cast<uint4 *>(dst);
+#pragma unroll
+    for (int i = 0; i < n / 8; ++i) {
+        uint4 w;
+        w.x = pack_bf16(v[8 * i + 0], v[8 * i + 1]);
+        w.y = pack_bf16(v[8 * i + 2], v[8 * i + 3]);
+        w.z = pack_bf16(v[8 * i + 4], v[8 * i + 5]);
+        w.w = pack_bf16(v[8 * i + 6], v[8 * i + 7]);
+        d4[i] = w;
+    }
+}
+
+// Epilogue of one QKV tile row: BN columns = BN/D whole heads.
+template <int BN, int D>
+DEVI void epilogue_qkv(const GemmParams &P, uint32_t tcol, int m, int n0, bool row_ok, const float *s_norm)
+{
+    const QkvEpilogue &e = P.qkv;
+    const int HqD = e.Hq * D, HkvD = e.Hkv * D;
+    int b = 0, pos = 0, q_slot = 0, kv_slot = 0;
+    if (row_ok) {
+        if (e.pos_dev) {
+            b = m;
+            pos = e.pos_dev[m];
+            kv_slot = pos;
+        } else {
+            b = m / e.S;
+            pos = m - b * e.S;
+            q_slot = kv_slot = pos;
+        }
+        if (pos < 0 || pos >= e.rope_rows || kv_slot >= e.kv_seq) {
+            atomicOr(P.err, kErrIndex);
+            row_ok = false;
+        }
+    }
+    const bool has_norm = e.q_norm_w != nullptr;
+#pragma unroll 1
+    for (int h = 0; h < BN / D; ++h) {
+        const int n = n0 + h * D;
+        if (n >= P.N) break;  // uniform across the warp
+        const uint32_t col = tcol + h * D;
+        int kind, head;
+        if (n < HqD) {
+            kind = 0;
+            head = n / D;
+        } else if (n < HqD + HkvD) {
+            kind = 1;
+            head = (n - HqD) / D;
+        } else {
+            kind = 2;
+            head = (n - HqD - HkvD) / D;
+        }
+        uint16_t *dst;
+        if (kind == 0)
+            dst = e.q_out + ((size_t)(b * e.Hq + head) * e.q_seq + q_slot) * D;
+        else
+            dst = (kind == 1 ? e.k_out : e.v_out) + ((size_t)(b * e.Hkv + head) * e.kv_seq + kv_slot) * D;
+
+        if (kind == 2) {  // V: no norm, no rotation
+#pragma unroll 1
+            for (int c = 0; c < D; c += 32) {
+                uint32_t r[32];
+                tmem_ld32(col + c, r);
+                float v[32];
+#pragma unroll
+                for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+                if (row_ok) store_row_bf16(dst + c, v, 32);
+            }
+            continue;
+        }
+        float rinv = 1.0f;
+        if (has_norm) {
+            float ss = 0.0f;
+#pragma unroll 1
+            for (int c = 0; c < D; c += 32) {
+                uint32_t r[32];
+                tmem_ld32(col + c, r);
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    const float f = __uint_as_float(r[i]);
+                    ss = fmaf(f, f, ss);
+                }
+            }
+            rinv = 1.0f / sqrtf(ss * (1.0f / D) + e.eps);
+        }
+        const float *w = s_norm + (kind == 0 ? 0 : 128);
+        const float2 *cs = e.rope + (size_t)(row_ok ? pos : 0) * (D / 2);
+#pragma unroll 1
+        for (int c = 0; c < D / 2; c += 32) {
+            uint32_t r1[32], r2[32];
+            tmem_ld32(col + c, r1);
+            tmem_ld32(col + c + D / 2, r2);
+            float y1[32], y2[32];
+#pragma unroll
+            for (int i = 0; i < 32; i += 2) {
+                const float4 t = __ldg(reinterpret_cast<const float4 *>(cs + c + i));  // (cos, sin) x 2
+#pragma unroll
+                for (int k = 0; k < 2; ++k) {
+                    const float co = k ? t.z : t.x, si = k ? t.w : t.y;
+                    float x1 = __uint_as_float(r1[i + k]) * rinv;
+                    float x2 = __uint_as_float(r2[i + k]) * rinv;
+                    if (has_norm) {
+                        x1 *= w[c + i + k];
+                        x2 *= w[c + i + k + D / 2];
+                    }
+                    y1[i + k] = x1 * co - x2 * si;
+                    y2[i + k] = x2 * co + x1 * si;
+                }
+            }
+            if (row_ok) {
+                store_row_bf16(dst + c, y1, 32);
+                store_row_bf16(dst + c + D / 2, y2, 32);
+            }
+        }
+    }
+}
+
+template <int BN>
+DEVI void epilogue_residual(const GemmParams &P, uint32_t tcol, int m, int n0, bool row_ok)
+{
+    const ResidualEpilogue &e = P.res;
+#pragma unroll 1
+    for (int c = 0; c < BN; c += 32) {
+        const int n = n0 + c;
+        if (n >= P.N) break;  // uniform across the warp
+        uint32_t r[32];
+        tmem_ld32(tcol + c, r);
+        if (!row_ok) continue;
+        const size_t off = (size_t)m * P.N + n;
+        const uint4 *src = reinterpret_cast<const uint4 *>(e.resid + off);
+        uint4 *dst = reinterpret_cast<uint4 *>(e.out + off);
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+            if (n + 8 * v >= P.N) break;
+            const uint4 x = src[v];
+            const uint32_t xs[4] = {x.x, x.y, x.z, x.w};
+            uint32_t o[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+                o[k] = pack_bf16(__uint_as_float(r[8 * v + 2 * k]) + bf16lo(xs[k]),
+                                 __uint_as_float(r[8 * v + 2 * k + 1]) + bf16hi(xs[k]));
+            dst[v] = make_uint4(o[0], o[1], o[2], o[3]);
+        }
+    }
+}
+
+template <int BN, int STAGES, int EPI, int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const GemmParams P)
+{
+    using L = Smem<BN, STAGES>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t *sA = smem;
+    uint8_t *sB = smem + STAGES * L::A_BYTES;
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + L::BARS);
+    uint64_t *empty = full + STAGES;
+    uint64_t *tfull = empty + STAGES;
+    uint64_t *tempty = tfull + 2;
+    uint64_t *drain = tempty + 2;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::TMEM_SLOT);
+    float *s_norm = reinterpret_cast<float *>(smem + L::NORM);
+
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    unsigned *err = P.err;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(full + s, 1);
+            mbar_init(empty + s, 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(tfull + a, 1);
+            mbar_init(tempty + a, 4);
+        }
+        mbar_init(drain, 1);
+        fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tmA);
+        tma_prefetch_desc(&tmB);
+    }
+    if (warp == 1) tmem_alloc(tmem_slot, 2 * BN);
+    if (EPI == EPI_QKV && warp >= 2 && P.qkv.q_norm_w) {
+        for (int i = threadIdx.x - 64; i < D; i += 128) {
+            s_norm[i] = __uint_as_float((uint32_t)P.qkv.q_norm_w[i] << 16);
+            s_norm[128 + i] = __uint_as_float((uint32_t)P.qkv.k_norm_w[i] << 16);
+        }
+    }
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            int it = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; ok && tile < P.num_tiles; tile += gridDim.x) {
+                int mb, nb;
+                tile_coords(tile, P.num_m, P.num_n, mb, nb);
+                for (int kb = 0; kb < P.num_k; ++kb, ++it) {
+                    const int s = it % STAGES;
+                    const uint32_t ph = (it / STAGES) & 1;
+                    if (!mbar_wait(empty + s, ph ^ 1, err)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(full + s, L::A_BYTES + L::B_BYTES);
+                    tma_load_2d(sA + s * L::A_BYTES, &tmA, kb * BK, mb * BM, full + s);
+                    tma_load_2d(sB + s * L::B_BYTES, &tmB, kb * BK, nb * BN, full + s);
+                }
+            }
+            // every issued copy has landed before the CTA may exit
+            for (int j = max(0, it - STAGES); j < it; ++j) mbar_wait(full + j % STAGES, (j / STAGES) & 1, err);
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            constexpr uint32_t idesc = idesc_bf16_f32(BM, BN, 0, 0);
+            int it = 0, use = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; ok && tile < P.num_tiles; tile += gridDim.x, ++use) {
+                const int acc = use & 1;
+                if (!mbar_wait(tempty + acc, ((use >> 1) & 1) ^ 1, err)) break;
+                tc_fence_after();
+                const uint32_t d_tmem = tmem + acc * BN;
+                for (int kb = 0; kb < P.num_k; ++kb, ++it) {
+                    const int s = it % STAGES;
+                    if (!mbar_wait(full + s, (it / STAGES) & 1, err)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a0 = smem_u32(sA + s * L::A_BYTES);
+                    const uint32_t b0 = smem_u32(sB + s * L::B_BYTES);
+#pragma unroll
+                    for (int k = 0; k < BK / 16; ++k)
+                        umma_bf16_ss(d_tmem, sw128_desc(a0 + 32 * k, 16, 1024), sw128_desc(b0 + 32 * k, 16, 1024),
+                                     idesc, (kb | k) != 0);
+                    umma_commit(empty + s);  // frees the stage once these MMAs have read it
+                }
+                if (!ok) break;
+                umma_commit(tfull + acc);  // accumulator ready for the epilogue
+            }
+            umma_commit(drain);
+            mbar_wait(drain, 0, err);
+        }
+    } else {
+        const int quarter = warp & 3;  // TMEM lanes this warp may access
+        const int row = quarter * 32 + lane;
+        int use = 0;
+        for (int tile = blockIdx.x; tile < P.num_tiles; tile += gridDim.x, ++use) {
+            int mb, nb;
+            tile_coords(tile, P.num_m, P.num_n, mb, nb);
+            const int acc = use & 1;
+            if (!mbar_wait(tfull + acc, (use >> 1) & 1, err)) break;
+            tc_fence_after();
+            const uint32_t tcol = tmem + ((uint32_t)(quarter * 32) << 16) + acc * BN;
+            const int m = mb * BM + row;
+            const bool row_ok = m < P.M;
+            if constexpr (EPI == EPI_QKV)
+                epilogue_qkv<BN, D>(P, tcol, m, nb * BN, row_ok, s_norm);
+            else
+                epilogue_residual<BN>(P, tcol, m, nb * BN, row_ok);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(tempty + acc);
+        }
+    }
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 2 * BN);
+    }
+}
+
+template <int BN, int STAGES, int EPI, int D>
+cudaError_t run(const GemmProblem &p, const GemmParams &params, int num_sms, cudaStream_t stream)
+{
+    using L = Smem<BN, STAGES>;
+    CUtensorMap ta, tb;
+    const uint64_t dA[2] = {(uint64_t)p.K, (uint64_t)p.M}, sA[1] = {(uint64_t)p.K * 2};
+    const uint64_t dB[2] = {(uint64_t)p.K, (uint64_t)p.N}, sB[1] = {(uint64_t)p.K * 2};
+    const uint32_t bA[2] = {BK, BM}, bB[2] = {BK, BN};
+    if (encode_tmap(&ta, p.A, 2, dA, sA, bA, true) != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    if (encode_tmap(&tb, p.B, 2, dB, sB, bB, true) != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    auto kern = gemm_kernel<BN, STAGES, EPI, D>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC);
+    if (e != cudaSuccess) return e;
+    const int grid = params.num_tiles < num_sms ? params.num_tiles : num_sms;
+    kern<<<grid, kThreads, L::ALLOC, stream>>>(ta, tb, params);
+    return cudaGetLastError();
+}
+
+GemmParams make_params(const GemmProblem &p, int BN, unsigned *err)
+{
+    GemmParams g{};
+    g.M = p.M;
+    g.N = p.N;
+    g.K = p.K;
+    g.num_m = (p.M + BM - 1) / BM;
+    g.num_n = (p.N + BN - 1) / BN;
+    g.num_k = (p.K + BK - 1) / BK;
+    g.num_tiles = g.num_m * g.num_n;
+    g.err = err;
+    return g;
+}
+
+}  // namespace
+
+cudaError_t launch_gemm_qkv(const GemmProblem &p, const QkvEpilogue &e, unsigned *err, int num_sms,
+                            cudaStream_t stream)
+{
+    // Decode-sized problems (one M block) use narrower tiles so more SMs
+    // stream the weight matrix.
+    const bool small_m = p.M <= BM;
+    if (e.d == 128) {
+        if (small_m) {
+            GemmParams g = make_params(p, 128, err);
+            g.qkv = e;
+            return run<128, 6, EPI_QKV, 128>(p, g, num_sms, stream);
+        }
+        GemmParams g = make_params(p, 256, err);
+        g.qkv = e;
+        return run<256, 4, EPI_QKV, 128>(p, g, num_sms, stream);
+    }
+    if (e.d == 64) {
+        if (small_m) {
+            GemmParams g = make_params(p, 64, err);
+            g.qkv = e;
+            return run<64, 8, EPI_QKV, 64>(p, g, num_sms, stream);
+        }
+        GemmParams g = make_params(p, 256, err);
+        g.qkv = e;
+        return run<256, 4, EPI_QKV, 64>(p, g, num_sms, stream);
+    }
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_gemm_residual(const GemmProblem &p, const ResidualEpilogue &e, unsigned *err, int num_sms,
+                                 cudaStream_t stream)
+{
+    if (p.M <= BM) {
+        GemmParams g = make_params(p, 64, err);
+        g.res = e;
+        return run<64, 8, EPI_RESIDUAL, 0>(p, g, num_sms, stream);
+    }
+    GemmParams g = make_params(p, 256, err);
+    g.res = e;
+    return run<256, 4, EPI_RESIDUAL, 0>(p, g, num_sms, stream);
+}
+
+}  // namespace gqa

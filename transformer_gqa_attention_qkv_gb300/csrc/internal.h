@@ -1,0 +1,83 @@
+// internal.h -- host-side declarations shared by the library's translation
+// units (launchers and their argument blocks).  Not part of the public ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace gqa {
+
+// ---------------------------------------------------------------- GEMM core
+// C[M, N] = A[M, K] @ B[N, K]^T on tcgen05, A and B bf16 row-major (K
+// contiguous), fp32 accumulation in TMEM, with one of two fused epilogues.
+
+// Epilogue "qkv": the N columns are Hq query heads, then Hkv key heads, then
+// Hkv value heads, each d wide.  Q and K heads are RMS-normed (optional) and
+// rotated (RoPE) at the row's position; results are written head-major.
+struct QkvEpilogue {
+    int Hq, Hkv, d;
+    int S;                 // prefill: tokens per sequence (row m = b*S + t)
+    const int *pos_dev;    // decode: row m = b, position = slot = pos_dev[b]; NULL for prefill
+    int q_seq;             // sequence extent of q_out (S, or 1 for decode)
+    int kv_seq;            // sequence extent of k_out / v_out (S, or Lmax for decode)
+    const uint16_t *q_norm_w, *k_norm_w;  // [d] bf16, or both NULL
+    float eps;
+    const float2 *rope;    // [rope_rows][d/2] (cos, sin)
+    int rope_rows;
+    uint16_t *q_out, *k_out, *v_out;
+};
+
+// Epilogue "residual": out[m, n] = acc[m, n] + resid[m, n] (bf16, [M, N]).
+struct ResidualEpilogue {
+    const uint16_t *resid;
+    uint16_t *out;
+};
+
+struct GemmProblem {
+    const void *A;  // [M, K] bf16
+    const void *B;  // [N, K] bf16
+    int M, N, K;
+};
+
+// Launchers return a cudaError_t (cudaSuccess when enqueued).
+cudaError_t launch_gemm_qkv(const GemmProblem &p, const QkvEpilogue &e, unsigned *err, int num_sms,
+                            cudaStream_t stream);
+cudaError_t launch_gemm_residual(const GemmProblem &p, const ResidualEpilogue &e, unsigned *err, int num_sms,
+                                 cudaStream_t stream);
+
+// ------------------------------------------------------- prefill attention
+struct AttentionProblem {
+    const uint16_t *q;  // [B, Hq, S, d]
+    const uint16_t *k;  // [B, Hkv, S, d]
+    const uint16_t *v;  // [B, Hkv, S, d]
+    uint16_t *out;      // [B, S, Hq*d]
+    int B, S, Hq, Hkv, d, causal;
+};
+cudaError_t launch_attention(const AttentionProblem &p, unsigned *err, int num_sms, cudaStream_t stream);
+
+// -------------------------------------------------------- decode attention
+struct DecodeAttentionProblem {
+    const uint16_t *q;        // [B, Hq, d]
+    const uint16_t *k_cache;  // [B, Hkv, Lmax, d]
+    const uint16_t *v_cache;
+    const int *len;           // device [B]; keys attended = len[b] + len_bias
+    int len_bias;
+    uint16_t *out;            // [B, Hq*d]
+    int B, Hq, Hkv, d, Lmax;
+    float *partials;          // split partials (see decode_partials_floats)
+    int splits;               // number of key splits per (b, kv head)
+};
+int decode_choose_splits(int B, int Hkv, int Lmax, int num_sms);
+size_t decode_partials_floats(int B, int Hq, int splits, int d);
+cudaError_t launch_decode_attention(const DecodeAttentionProblem &p, unsigned *err, cudaStream_t stream);
+
+// --------------------------------------------------------------- self test
+cudaError_t launch_selftest_wait(unsigned *err, unsigned long long limit_ns, cudaStream_t stream);
+
+// Tensor-map encoder (driver entry point, resolved once).
+CUresult encode_tmap(CUtensorMap *map, const void *base, int rank, const uint64_t *dims,
+                     const uint64_t *strides_bytes, const uint32_t *box, bool swizzle128);
+
+}  // namespace gqa
