@@ -65,12 +65,24 @@ typedef uint16_t gqa_bf16; /* bit pattern of one bf16 value */
 #define GQA_ERR_CUDA (-3)        /* a CUDA runtime call failed (message has details) */
 #define GQA_ERR_TIMEOUT (-4)     /* a bounded device wait gave up */
 #define GQA_ERR_WORKSPACE (-5)   /* workspace missing or smaller than required */
+#define GQA_ERR_RANGE (-6)       /* reported by gqa_check_device_error: a prefill Q/K/V value
+                                    beyond +-65504 was clamped to the binary16 range */
+
+typedef uint16_t gqa_f16; /* bit pattern of one IEEE binary16 value */
 
 /* ------------------------------------------------------------------ prefill */
 
 /* Bytes of device workspace gqa_attn_forward_ex needs: Q [B,Hq,S,d],
- * K and V [B,Hkv,S,d] and attn [B,S,Hq*d], bf16, each 256-byte aligned.
- * Returns 0 for invalid sizes. */
+ * K and V [B,Hkv,S,d] (binary16) and attn [B,S,Hq*d] (bf16), each 256-byte
+ * aligned.  Returns 0 for invalid sizes.
+ *
+ * Why binary16 for Q, K and V: the attention step computes in fp32 from them
+ * ([T07] §4 step 6 casts the 16-bit projections to float32).  binary16 keeps 3
+ * more mantissa bits than bf16, so storing them costs the scores and outputs
+ * an 8x smaller rounding error at the same bandwidth and tensor-core rate.
+ * QK-norm bounds every Q and K row by sqrt(head_dim) * max|w|; a value beyond
+ * the binary16 range (possible only for V, or without QK-norm, at magnitudes
+ * above 65504) is clamped and reported as GQA_ERR_RANGE. */
 size_t gqa_attn_workspace_size(int B, int S, int hidden, int Hq, int Hkv, int head_dim);
 
 /* The whole layer forward ([T07] §4 steps 1-7; [NeoX] "Qwen3-0.6B example"):
@@ -104,19 +116,20 @@ int gqa_attn_forward(const gqa_bf16 *x, const gqa_bf16 *Wqkv, const gqa_bf16 *Wo
                      gqa_bf16 *out);
 
 /* Stage 1 alone: qkv = x @ Wqkv^T, then QK-norm and RoPE at positions
- * 0..S-1, written head-major ([T07] §4 steps 1-4):
+ * 0..S-1, written head-major ([T07] §4 steps 1-4), as binary16:
  *   q_out [B, Hq, S, head_dim], k_out and v_out [B, Hkv, S, head_dim]. */
 int gqa_qkv_proj(const gqa_bf16 *x, const gqa_bf16 *Wqkv,
                  const gqa_bf16 *q_norm_w, const gqa_bf16 *k_norm_w,
                  float rope_theta, float eps,
                  int B, int S, int hidden, int Hq, int Hkv, int head_dim,
-                 gqa_bf16 *q_out, gqa_bf16 *k_out, gqa_bf16 *v_out, void *stream);
+                 gqa_f16 *q_out, gqa_f16 *k_out, gqa_f16 *v_out, void *stream);
 
 /* Stage 2 alone: grouped-query attention with scale head_dim^-0.5, fp32
  * softmax and accumulation ([T07] §4 step 6; [NeoX] "Scaling and RoPE"):
- *   q [B, Hq, S, head_dim], k and v [B, Hkv, S, head_dim]
- *   attn_out [B, S, Hq*head_dim] ([NeoX] "Attention output flattening"). */
-int gqa_attention(const gqa_bf16 *q, const gqa_bf16 *k, const gqa_bf16 *v,
+ *   q [B, Hq, S, head_dim], k and v [B, Hkv, S, head_dim], binary16
+ *   attn_out [B, S, Hq*head_dim], bf16 ([NeoX] "Attention output flattening").
+ * Supported group sizes Hq/Hkv: powers of two up to 128. */
+int gqa_attention(const gqa_f16 *q, const gqa_f16 *k, const gqa_f16 *v,
                   int B, int S, int Hq, int Hkv, int head_dim, int causal,
                   gqa_bf16 *attn_out, void *stream);
 

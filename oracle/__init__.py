@@ -67,8 +67,10 @@ def _load():
     lib.oracle_qkv_stage.argtypes = [_u16p, _u16p, _u16p, _u16p, _D, _D,
                                      _L, _L, _L, _L, _L, _L, _f64p, _f64p, _f64p, _I]
     lib.oracle_attention_stage.restype = _I
-    lib.oracle_attention_stage.argtypes = [_u16p, _u16p, _u16p, _L, _L, _L, _L, _L, _I,
+    lib.oracle_attention_stage.argtypes = [_u16p, _u16p, _u16p, _I, _L, _L, _L, _L, _L, _I,
                                            _i64p, _L, _f64p, _I]
+    lib.oracle_f16_to_double.restype = None
+    lib.oracle_f16_to_double.argtypes = [_u16p, _L, _f64p]
     lib.oracle_oproj_stage.restype = _I
     lib.oracle_oproj_stage.argtypes = [_u16p, _u16p, _u16p, _L, _L, _L, _i64p, _L, _f64p, _I]
     lib.oracle_forward.restype = _I
@@ -95,16 +97,22 @@ def default_threads() -> int:
 
 # ---------------------------------------------------------------- marshalling
 
-def _bits(t):
-    """bf16 torch tensor or uint16 numpy array -> contiguous uint16 numpy array."""
+def _bits(t, allow_f16=False):
+    """bf16 (or, where allowed, float16) torch tensor, or uint16 numpy array
+    -> contiguous uint16 numpy array of the 16-bit patterns."""
     if t is None:
         return None
     if isinstance(t, np.ndarray):
         assert t.dtype == np.uint16
         return np.ascontiguousarray(t)
     import torch
-    assert t.dtype == torch.bfloat16, t.dtype
+    assert t.dtype == torch.bfloat16 or (allow_f16 and t.dtype == torch.float16), t.dtype
     return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def _is_f16(t):
+    import torch
+    return isinstance(t, torch.Tensor) and t.dtype == torch.float16
 
 
 def _p16(a):
@@ -192,12 +200,22 @@ def qkv_stage(x, Wqkv, q_norm_w, k_norm_w, rope_theta, eps, B, S, hidden, Hq, Hk
     return q, k, v
 
 
+def f16_to_double(bits: np.ndarray) -> np.ndarray:
+    """IEEE binary16 bit patterns -> float64 (exact)."""
+    b = np.ascontiguousarray(bits, dtype=np.uint16).reshape(-1)
+    out = np.empty(b.shape[0])
+    _load().oracle_f16_to_double(_p16(b), b.shape[0], _pf(out))
+    return out.reshape(np.shape(bits))
+
+
 def attention_stage(Q, K, V, B, S, Hq, Hkv, d, causal=True, sel=None, threads=None):
-    """attn [n_sel, Hq*d] from bf16 Q [B,Hq,S,d], K/V [B,Hkv,S,d]."""
+    """attn [n_sel, Hq*d] from Q [B,Hq,S,d], K/V [B,Hkv,S,d], all bf16 or all float16."""
     s, n = _sel(sel, B * S)
     out = np.empty((n, Hq * d))
-    qb, kb, vb = _bits(Q), _bits(K), _bits(V)
-    _check(_load().oracle_attention_stage(_p16(qb), _p16(kb), _p16(vb), B, S, Hq, Hkv, d,
+    f16 = _is_f16(Q)
+    assert _is_f16(K) == f16 and _is_f16(V) == f16, "Q, K and V must share one 16-bit format"
+    qb, kb, vb = _bits(Q, True), _bits(K, True), _bits(V, True)
+    _check(_load().oracle_attention_stage(_p16(qb), _p16(kb), _p16(vb), int(f16), B, S, Hq, Hkv, d,
                                           int(causal), None if s is None else s.ctypes.data_as(_i64p),
                                           n, _pf(out), threads or default_threads()),
            "attention_stage")

@@ -57,6 +57,26 @@ static double bf(uint16_t h)
     return (double)f;
 }
 
+/* IEEE binary16 bit pattern -> double, exact (subnormals, infinities, NaN). */
+static double h16(uint16_t h)
+{
+    int sign = (h >> 15) & 1, e = (h >> 10) & 31, m = h & 1023;
+    double v;
+    if (e == 0) v = ldexp((double)m, -24);
+    else if (e == 31) v = m ? NAN : INFINITY;
+    else v = ldexp((double)(1024 + m), e - 25);
+    return sign ? -v : v;
+}
+
+/* 16-bit pattern of either format -> double. */
+static double w16(uint16_t h, int f16) { return f16 ? h16(h) : bf(h); }
+
+/* Exported for the pin against numpy's float16 conversion. */
+void oracle_f16_to_double(const uint16_t *h, long n, double *out)
+{
+    for (long i = 0; i < n; ++i) out[i] = h16(h[i]);
+}
+
 static void set_threads(int nthreads)
 {
 #ifdef _OPENMP
@@ -206,20 +226,21 @@ int oracle_linear(const uint16_t *x, const uint16_t *W, long M, long N, long K,
  * kget/vget address key u of the group; q and o have length d.
  * The maximum is subtracted before exp, which leaves softmax unchanged. */
 typedef struct {
-    const uint16_t *kb;   /* bf16 keys, row stride d, or NULL */
+    const uint16_t *kb;   /* 16-bit keys, row stride d, or NULL */
     const uint16_t *vb;
     const double *kd;     /* double keys (used for keys >= n_bf16), or NULL */
     const double *vd;
     long n_bf16;          /* keys [0, n_bf16) come from kb/vb, the rest from kd/vd */
+    int f16;              /* kb/vb hold binary16 (1) or bf16 (0) patterns */
 } kv_src;
 
 static double key_at(const kv_src *s, long u, long c, long d)
 {
-    return (u < s->n_bf16) ? bf(s->kb[u * d + c]) : s->kd[(u - s->n_bf16) * d + c];
+    return (u < s->n_bf16) ? w16(s->kb[u * d + c], s->f16) : s->kd[(u - s->n_bf16) * d + c];
 }
 static double val_at(const kv_src *s, long u, long c, long d)
 {
-    return (u < s->n_bf16) ? bf(s->vb[u * d + c]) : s->vd[(u - s->n_bf16) * d + c];
+    return (u < s->n_bf16) ? w16(s->vb[u * d + c], s->f16) : s->vd[(u - s->n_bf16) * d + c];
 }
 
 static int attend_row(const double *q, const kv_src *src, long n_vis, long d, double *o)
@@ -293,14 +314,15 @@ int oracle_qkv_stage(const uint16_t *x, const uint16_t *Wqkv,
 }
 
 /* ------------------------------------------------------------------------ */
-/* Stage 2: causal grouped-query attention over bf16 Q/K/V.                 */
+/* Stage 2: causal grouped-query attention over 16-bit Q/K/V.               */
 /* ------------------------------------------------------------------------ */
 
-/* Q [B,Hq,S,d], K/V [B,Hkv,S,d] bf16.  attn [n_sel, Hq*d] for the selected
+/* Q [B,Hq,S,d], K/V [B,Hkv,S,d], all bf16 (in_f16 = 0) or all IEEE binary16
+ * (in_f16 = 1); either is widened to double exactly.  attn [n_sel, Hq*d] for the selected
  * tokens sel[i] = b*S + t (flattened, [T07] §4 step 7 "(batch, seq,
  * heads*head_dim)"; [NeoX] "Attention output flattening").  sel == NULL
  * means every token in order (n_sel must then be B*S). */
-int oracle_attention_stage(const uint16_t *Q, const uint16_t *K, const uint16_t *V,
+int oracle_attention_stage(const uint16_t *Q, const uint16_t *K, const uint16_t *V, int in_f16,
                            long B, long S, long Hq, long Hkv, long d, int causal,
                            const long *sel, long n_sel, double *attn, int nthreads)
 {
@@ -318,8 +340,8 @@ int oracle_attention_stage(const uint16_t *Q, const uint16_t *K, const uint16_t 
             long g = j / G;                                   /* R2 */
             double q[1024];
             if (d > 1024) { err = ORACLE_EARG; continue; }
-            for (long c = 0; c < d; ++c) q[c] = bf(Q[((b * Hq + j) * S + t) * d + c]);
-            kv_src src = {K + (b * Hkv + g) * S * d, V + (b * Hkv + g) * S * d, NULL, NULL, S};
+            for (long c = 0; c < d; ++c) q[c] = w16(Q[((b * Hq + j) * S + t) * d + c], in_f16);
+            kv_src src = {K + (b * Hkv + g) * S * d, V + (b * Hkv + g) * S * d, NULL, NULL, S, in_f16};
             long n_vis = causal ? t + 1 : S;                  /* R5 */
             int e = attend_row(q, &src, n_vis, d, attn + i * Hq * d + j * d);
             if (e) err = e;
@@ -413,7 +435,7 @@ int oracle_forward(const uint16_t *x, const uint16_t *Wqkv, const uint16_t *Wo,
             if (q_norm_w) rmsnorm_head(q, d, q_norm_w, eps);
             rope_head(q, d, (double)t, rope_theta);
             long g = j / G;
-            kv_src src = {NULL, NULL, Kd + (b * Hkv + g) * S * d, Vd + (b * Hkv + g) * S * d, 0};
+            kv_src src = {NULL, NULL, Kd + (b * Hkv + g) * S * d, Vd + (b * Hkv + g) * S * d, 0, 0};
             long n_vis = causal ? t + 1 : S;
             int e = attend_row(q, &src, n_vis, d, arow + j * d);
             if (e) err = e;
@@ -462,7 +484,7 @@ int oracle_decode_attention_stage(const uint16_t *q, const uint16_t *k_cache,
             double qv[1024];
             for (long c = 0; c < d; ++c) qv[c] = bf(q[(b * Hq + j) * d + c]);
             kv_src src = {k_cache + (b * Hkv + g) * Lmax * d, v_cache + (b * Hkv + g) * Lmax * d,
-                          NULL, NULL, kv_len[b]};
+                          NULL, NULL, kv_len[b], 0};
             int e = attend_row(qv, &src, kv_len[b], d, attn + b * Hq * d + j * d);
             if (e) err = e;
         }
@@ -518,7 +540,7 @@ int oracle_decode(const uint16_t *x, const uint16_t *Wqkv, const uint16_t *Wo,
             long g = j / G;
             const double *row = rows + b * N;
             kv_src src = {k_cache + (b * Hkv + g) * Lmax * d, v_cache + (b * Hkv + g) * Lmax * d,
-                          row + NQ + g * d, row + NQ + NKV + g * d, cache_len[b]};
+                          row + NQ + g * d, row + NQ + NKV + g * d, cache_len[b], 0};
             int e = attend_row(row + j * d, &src, cache_len[b] + 1, d, arows + b * NQ + j * d);
             if (e) err = e;
         }

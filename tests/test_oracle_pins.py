@@ -243,6 +243,31 @@ def test_attention_equals_library_sdpa():
     np.testing.assert_array_equal(_att(Q, K, V, sel=sel), _att(Q, K, V)[sel])
 
 
+def test_f16_widening_matches_numpy():
+    """The oracle's binary16 decoder agrees with numpy's float16 on all 65536
+    bit patterns (normals, subnormals, zeros, infinities, NaN)."""
+    bits = np.arange(65536, dtype=np.uint16)
+    got = oracle.f16_to_double(bits)
+    ref = bits.view(np.float16).astype(np.float64)
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], ref[~nan])
+
+
+def test_attention_f16_inputs_equal_library_sdpa():
+    """The attention step on binary16 Q/K/V equals torch's SDPA on the same
+    values widened to float64."""
+    rng = np.random.default_rng(8)
+    B, S, Hq, Hkv, d = 1, 70, 4, 2, 32
+    Q = torch.from_numpy(rng.standard_normal((B, Hq, S, d)) * 2).half()
+    K = torch.from_numpy(rng.standard_normal((B, Hkv, S, d)) * 2).half()
+    V = torch.from_numpy(rng.standard_normal((B, Hkv, S, d))).half()
+    ref = F.scaled_dot_product_attention(Q.double(), K.double().repeat_interleave(2, 1),
+                                         V.double().repeat_interleave(2, 1), is_causal=True)
+    ref = ref.transpose(1, 2).reshape(B * S, Hq * d).numpy()
+    np.testing.assert_allclose(_att(Q, K, V), ref, rtol=1e-11, atol=1e-12)
+
+
 def test_attention_no_future_leak():
     """[Part]: a causal test with a nontrivial length.  A huge value planted in V
     at position 50 must leave rows < 50 untouched and move rows >= 50."""

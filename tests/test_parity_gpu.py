@@ -31,6 +31,11 @@ def bf16_randn(shape, gen, std=1.0):
     return (torch.randn(*shape, generator=gen) * std).to(torch.bfloat16)
 
 
+def f16_randn(shape, gen, std=1.0):
+    """Q/K/V of the attention stage are binary16 (see include/gqa_attn.h)."""
+    return (torch.randn(*shape, generator=gen) * std).to(torch.float16)
+
+
 # ----------------------------------------------------------------- stage 1
 
 QKV_CASES = [
@@ -47,8 +52,8 @@ QKV_CASES = [
 def test_qkv_projection_stage(B, S, hidden, Hq, Hkv, d, qk):
     cfg = LayerConfig("t", B, S, hidden, Hq, Hkv, d, qk, 1e4 if d == 64 else 1e6)
     t = make_layer_inputs(cfg, seed=100 + S, w_std=0.05)
-    q = torch.empty((B, Hq, S, d), dtype=torch.bfloat16, device=DEV)
-    k = torch.empty((B, Hkv, S, d), dtype=torch.bfloat16, device=DEV)
+    q = torch.empty((B, Hq, S, d), dtype=torch.float16, device=DEV)
+    k = torch.empty((B, Hkv, S, d), dtype=torch.float16, device=DEV)
     v = torch.empty_like(k)
     gq.gqa_qkv_proj(dev(t["x"]), dev(t["Wqkv"]), dev(t["q_norm_w"]), dev(t["k_norm_w"]), cfg.rope_theta,
                     cfg.eps, B, S, hidden, Hq, Hkv, d, q, k, v)
@@ -80,9 +85,9 @@ ATTN_CASES = [
 @pytest.mark.parametrize("B,S,Hq,Hkv,d,causal", ATTN_CASES)
 def test_attention_stage(B, S, Hq, Hkv, d, causal):
     g = torch.Generator().manual_seed(200 + S)
-    Q = bf16_randn((B, Hq, S, d), g, 1.5)
-    K = bf16_randn((B, Hkv, S, d), g, 1.5)
-    V = bf16_randn((B, Hkv, S, d), g)
+    Q = f16_randn((B, Hq, S, d), g, 1.5)
+    K = f16_randn((B, Hkv, S, d), g, 1.5)
+    V = f16_randn((B, Hkv, S, d), g)
     out = torch.empty((B, S, Hq * d), dtype=torch.bfloat16, device=DEV)
     gq.gqa_attention(dev(Q), dev(K), dev(V), B, S, Hq, Hkv, d, causal, out)
     torch.cuda.synchronize()
@@ -97,14 +102,14 @@ def test_attention_group_map_markers_gpu():
     B, S, Hq, Hkv, d = 2, 200, 16, 4, 128
     g = torch.Generator().manual_seed(5)
     markers = torch.arange(1, B * Hkv * d + 1, dtype=torch.float32).reshape(B, Hkv, 1, d) / (B * Hkv * d)
-    V = markers.expand(B, Hkv, S, d).contiguous().to(torch.bfloat16)
-    Q = bf16_randn((B, Hq, S, d), g)
-    K = bf16_randn((B, Hkv, S, d), g)
+    V = markers.expand(B, Hkv, S, d).contiguous().to(torch.float16)
+    Q = f16_randn((B, Hq, S, d), g)
+    K = f16_randn((B, Hkv, S, d), g)
     out = torch.empty((B, S, Hq * d), dtype=torch.bfloat16, device=DEV)
     gq.gqa_attention(dev(Q), dev(K), dev(V), B, S, Hq, Hkv, d, True, out)
     torch.cuda.synchronize()
     o = to64(out).reshape(B, S, Hq, d)
-    mk = to64(markers.to(torch.bfloat16))
+    mk = to64(markers.to(torch.float16))
     for j in range(Hq):
         np.testing.assert_allclose(o[:, :, j], np.broadcast_to(mk[:, j // (Hq // Hkv)], (B, S, d)),
                                    rtol=1e-2, atol=0)
@@ -115,9 +120,9 @@ def test_attention_no_future_leak_gpu():
     bit-identical and changes every later row."""
     B, S, Hq, Hkv, d = 1, 1000, 8, 2, 128
     g = torch.Generator().manual_seed(6)
-    Q = bf16_randn((B, Hq, S, d), g)
-    K = bf16_randn((B, Hkv, S, d), g)
-    V = bf16_randn((B, Hkv, S, d), g)
+    Q = f16_randn((B, Hq, S, d), g)
+    K = f16_randn((B, Hkv, S, d), g)
+    V = f16_randn((B, Hkv, S, d), g)
     outs = []
     for spike in (False, True):
         V2 = V.clone()
@@ -181,16 +186,19 @@ def ws_views(cfg, ws):
     d = cfg.head_dim
     sizes = [tok * cfg.Hq * d * 2, tok * cfg.Hkv * d * 2, tok * cfg.Hkv * d * 2, tok * cfg.Hq * d * 2]
     offs = np.cumsum([0] + [al(s) for s in sizes])
-    views = [ws[offs[i]:offs[i] + sizes[i]].view(torch.bfloat16) for i in range(4)]
+    dts = [torch.float16, torch.float16, torch.float16, torch.bfloat16]
+    views = [ws[offs[i]:offs[i] + sizes[i]].view(dts[i]) for i in range(4)]
     return (views[0].view(cfg.B, cfg.Hq, cfg.S, d), views[1].view(cfg.B, cfg.Hkv, cfg.S, d),
             views[2].view(cfg.B, cfg.Hkv, cfg.S, d), views[3].view(cfg.B * cfg.S, cfg.Hq * d))
 
 
 REDUCED = [
-    # name, overrides of the workload geometry (reduced length), weight std
+    # name, overrides of the workload geometry (reduced length), Wqkv std
     ("qwen3_0p6b", {}, 0.02),
     ("vaswani_mha", {"B": 2, "S": 512}, 0.02),
-    ("vaswani_mha", {"B": 2, "S": 300}, 0.1),   # larger weights: a peaked softmax
+    # larger Q/K weights: a peaked softmax (Wo stays at 0.02, so the output's
+    # bf16 rounding floor stays below the tolerance)
+    ("vaswani_mha", {"B": 2, "S": 300}, 0.1),
     ("qwen3_4b", {"B": 1, "S": 1024}, 0.02),
     ("qwen3_32b", {"B": 1, "S": 640}, 0.02),
 ]
@@ -199,7 +207,7 @@ REDUCED = [
 @pytest.mark.parametrize("name,over,w_std", REDUCED)
 def test_forward_reduced_workloads(name, over, w_std):
     cfg = PREFILL_CONFIGS[name].with_(**over)
-    t = make_layer_inputs(cfg, seed=SEEDS[name], w_std=w_std)
+    t = make_layer_inputs(cfg, seed=SEEDS[name], w_std=w_std, wo_std=0.02)
     out, ws = run_forward(cfg, t)
     ref = oracle.forward(t["x"], t["Wqkv"], t["Wo"], t["q_norm_w"], t["k_norm_w"], cfg.rope_theta, cfg.eps,
                          cfg.B, cfg.S, cfg.hidden, cfg.Hq, cfg.Hkv, cfg.head_dim, causal=cfg.causal,
@@ -230,6 +238,28 @@ def test_forward_full_workloads_sampled(name):
     # K and V of every token (the oracle has them all)
     assert_parity("K", to64(k), ref["k"])
     assert_parity("V", to64(v), ref["v"])
+
+
+def test_range_guard_reports_clamped_values():
+    """Q/K/V are stored as binary16: a value beyond +-65504 (here V from huge
+    value weights) is clamped and reported as GQA_ERR_RANGE; normal inputs are
+    not flagged."""
+    cfg = LayerConfig("t", 1, 64, 256, 2, 1, 64, True, 1e4)
+    t = make_layer_inputs(cfg, seed=3)
+    W = t["Wqkv"].clone()
+    W[3 * 64:] = 3000.0  # V rows: |v| ~ 3000 * |sum(x)| >> 65504
+    q = torch.empty((1, 2, 64, 64), dtype=torch.float16, device=DEV)
+    k = torch.empty((1, 1, 64, 64), dtype=torch.float16, device=DEV)
+    v = torch.empty_like(k)
+    gq.gqa_qkv_proj(dev(t["x"]), dev(W), dev(t["q_norm_w"]), dev(t["k_norm_w"]), cfg.rope_theta, cfg.eps,
+                    1, 64, 256, 2, 1, 64, q, k, v)
+    torch.cuda.synchronize()
+    assert gq.gqa_check_device_error() == gq.GQA_ERR_RANGE
+    assert torch.isfinite(v.float()).all() and v.float().abs().max() == 65504.0
+    gq.gqa_qkv_proj(dev(t["x"]), dev(t["Wqkv"]), dev(t["q_norm_w"]), dev(t["k_norm_w"]), cfg.rope_theta,
+                    cfg.eps, 1, 64, 256, 2, 1, 64, q, k, v)
+    torch.cuda.synchronize()
+    assert gq.gqa_check_device_error() == gq.GQA_OK
 
 
 def test_forward_default_stream_entry_point():

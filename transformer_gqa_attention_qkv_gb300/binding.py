@@ -22,6 +22,7 @@ GQA_ERR_UNSUPPORTED = -2
 GQA_ERR_CUDA = -3
 GQA_ERR_TIMEOUT = -4
 GQA_ERR_WORKSPACE = -5
+GQA_ERR_RANGE = -6
 
 # every symbol include/gqa_attn.h declares
 EXPORTS = (
@@ -106,6 +107,12 @@ def _bf16(t):
     return _ptr(t)
 
 
+def _f16(t):
+    if t is not None and t.dtype != torch.float16:
+        raise TypeError(f"expected float16, got {t.dtype}")
+    return _ptr(t)
+
+
 def _i32(t):
     if t.dtype != torch.int32:
         raise TypeError(f"expected int32, got {t.dtype}")
@@ -143,13 +150,15 @@ def gqa_attn_forward(x, Wqkv, Wo, q_norm_w, k_norm_w, rope_theta, eps, B, S, hid
 
 def gqa_qkv_proj(x, Wqkv, q_norm_w, k_norm_w, rope_theta, eps, B, S, hidden, Hq, Hkv, head_dim,
                  q_out, k_out, v_out, stream=None):
+    """q_out/k_out/v_out are float16 (binary16) tensors."""
     _check(lib().gqa_qkv_proj(_bf16(x), _bf16(Wqkv), _bf16(q_norm_w), _bf16(k_norm_w), rope_theta, eps,
-                              B, S, hidden, Hq, Hkv, head_dim, _bf16(q_out), _bf16(k_out), _bf16(v_out),
+                              B, S, hidden, Hq, Hkv, head_dim, _f16(q_out), _f16(k_out), _f16(v_out),
                               _stream(stream)))
 
 
 def gqa_attention(q, k, v, B, S, Hq, Hkv, head_dim, causal, attn_out, stream=None):
-    _check(lib().gqa_attention(_bf16(q), _bf16(k), _bf16(v), B, S, Hq, Hkv, head_dim, int(causal),
+    """q/k/v are float16 (binary16) tensors; attn_out is bfloat16."""
+    _check(lib().gqa_attention(_f16(q), _f16(k), _f16(v), B, S, Hq, Hkv, head_dim, int(causal),
                                _bf16(attn_out), _stream(stream)))
 
 

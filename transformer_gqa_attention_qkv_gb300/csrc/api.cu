@@ -208,8 +208,8 @@ static FwdLayout fwd_layout(int B, int S, int Hq, int Hkv, int d)
 
 static int run_qkv(DeviceState &st, const gqa_bf16 *x, const gqa_bf16 *Wqkv, const gqa_bf16 *qn, const gqa_bf16 *kn,
                    float theta, float eps, int B, int S, int hidden, int Hq, int Hkv, int d, const int *pos_dev,
-                   int q_seq, int kv_seq, int rope_rows, gqa_bf16 *q_out, gqa_bf16 *k_out, gqa_bf16 *v_out,
-                   cudaStream_t stream)
+                   int q_seq, int kv_seq, int rope_rows, int f16_out, gqa_bf16 *q_out, gqa_bf16 *k_out,
+                   gqa_bf16 *v_out, cudaStream_t stream)
 {
     const float2 *rope = nullptr;
     int rc;
@@ -232,6 +232,7 @@ static int run_qkv(DeviceState &st, const gqa_bf16 *x, const gqa_bf16 *Wqkv, con
     e.eps = eps;
     e.rope = rope;
     e.rope_rows = rope_rows;
+    e.f16_out = f16_out;
     e.q_out = q_out;
     e.k_out = k_out;
     e.v_out = v_out;
@@ -305,8 +306,8 @@ size_t gqa_attn_workspace_size(int B, int S, int hidden, int Hq, int Hkv, int he
 }
 
 int gqa_qkv_proj(const gqa_bf16 *x, const gqa_bf16 *Wqkv, const gqa_bf16 *q_norm_w, const gqa_bf16 *k_norm_w,
-                 float rope_theta, float eps, int B, int S, int hidden, int Hq, int Hkv, int head_dim, gqa_bf16 *q_out,
-                 gqa_bf16 *k_out, gqa_bf16 *v_out, void *stream)
+                 float rope_theta, float eps, int B, int S, int hidden, int Hq, int Hkv, int head_dim, gqa_f16 *q_out,
+                 gqa_f16 *k_out, gqa_f16 *v_out, void *stream)
 {
     g_launches = 0;
     int rc = check_layer(B, S, hidden, Hq, Hkv, head_dim, q_norm_w, k_norm_w);
@@ -318,10 +319,10 @@ int gqa_qkv_proj(const gqa_bf16 *x, const gqa_bf16 *Wqkv, const gqa_bf16 *q_norm
     DeviceState *st;
     if ((rc = device_state(&st))) return rc;
     return run_qkv(*st, x, Wqkv, q_norm_w, k_norm_w, rope_theta, eps, B, S, hidden, Hq, Hkv, head_dim, nullptr, S, S,
-                   S, q_out, k_out, v_out, (cudaStream_t)stream);
+                   S, 1, q_out, k_out, v_out, (cudaStream_t)stream);
 }
 
-int gqa_attention(const gqa_bf16 *q, const gqa_bf16 *k, const gqa_bf16 *v, int B, int S, int Hq, int Hkv,
+int gqa_attention(const gqa_f16 *q, const gqa_f16 *k, const gqa_f16 *v, int B, int S, int Hq, int Hkv,
                   int head_dim, int causal, gqa_bf16 *attn_out, void *stream)
 {
     g_launches = 0;
@@ -384,7 +385,7 @@ int gqa_attn_forward_ex(const gqa_bf16 *x, const gqa_bf16 *Wqkv, const gqa_bf16 
     gqa_bf16 *attn = (gqa_bf16 *)(ws + L.attn);
     cudaStream_t s = (cudaStream_t)stream;
     if ((rc = run_qkv(*st, x, Wqkv, q_norm_w, k_norm_w, rope_theta, eps, B, S, hidden, Hq, Hkv, head_dim, nullptr, S,
-                      S, S, q, k, v, s)))
+                      S, S, 1, q, k, v, s)))
         return rc;
     if ((rc = run_attention(*st, q, k, v, B, S, Hq, Hkv, head_dim, causal, attn, s))) return rc;
     return run_oproj(*st, attn, Wo, x, B * S, hidden, Hq * head_dim, out, s);
@@ -482,7 +483,7 @@ int gqa_decode_qkv(const gqa_bf16 *x, const gqa_bf16 *Wqkv, const gqa_bf16 *q_no
     DeviceState *st;
     if ((rc = device_state(&st))) return rc;
     return run_qkv(*st, x, Wqkv, q_norm_w, k_norm_w, rope_theta, eps, B, 1, hidden, Hq, Hkv, head_dim, cache_len, 1,
-                   Lmax, Lmax, q_out, k_cache, v_cache, (cudaStream_t)stream);
+                   Lmax, Lmax, 0, q_out, k_cache, v_cache, (cudaStream_t)stream);
 }
 
 int gqa_decode_attention(const gqa_bf16 *q, const gqa_bf16 *k_cache, const gqa_bf16 *v_cache, const int *kv_len,
@@ -536,7 +537,7 @@ int gqa_attn_decode(const gqa_bf16 *x, const gqa_bf16 *Wqkv, const gqa_bf16 *Wo,
     float *part = (float *)(ws + off_part);
     cudaStream_t s = (cudaStream_t)stream;
     if ((rc = run_qkv(*st, x, Wqkv, q_norm_w, k_norm_w, rope_theta, eps, B, 1, hidden, Hq, Hkv, head_dim, cache_len, 1,
-                      Lmax, Lmax, q, k_cache, v_cache, s)))
+                      Lmax, Lmax, 0, q, k_cache, v_cache, s)))
         return rc;
     if ((rc = run_decode_attn(*st, q, k_cache, v_cache, cache_len, 1, B, Hq, Hkv, head_dim, Lmax, attn, part, sp, s)))
         return rc;
@@ -579,6 +580,8 @@ int gqa_check_device_error(void)
     }
     if (word & kErrTimeout) return fail(GQA_ERR_TIMEOUT, "a bounded device wait gave up (error word 0x%x)", word);
     if (word & kErrIndex) return fail(GQA_ERR_ARG, "a device-side index check failed (error word 0x%x)", word);
+    if (word & kErrRange)
+        return fail(GQA_ERR_RANGE, "a Q/K/V value beyond the binary16 range was clamped (error word 0x%x)", word);
     return GQA_OK;
 }
 

@@ -15,9 +15,13 @@
 //   warp 1      MMA: S = Q K^T (TMEM), then O += P V (TMEM)
 //   warps 2..5  softmax: one thread per row (tcgen05.ld 32x32b gives a thread
 //               a whole row, so row max and row sum need no shuffles); online
-//               softmax in fp32 with exp2; P to shared memory as bf16;
+//               softmax in fp32 with exp2; P to shared memory as binary16;
 //               O rescaled in TMEM only when the running max grows by more
 //               than 2^8; final O / l written as bf16.
+//
+// Q, K and V arrive as binary16: with QK-norm their rows are bounded by
+// sqrt(d) * max|w|, and binary16 keeps 3 more mantissa bits than bf16, which
+// halves the rounding error that storage adds to the scores and outputs.
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -39,7 +43,7 @@ struct AttnParams {
 
 template <int D>
 struct ASmem {
-    static constexpr int CHUNK = kRows * 128;             // 128 rows x 64 bf16 = 16 KB
+    static constexpr int CHUNK = kRows * 128;             // 128 rows x 64 16-bit = 16 KB
     static constexpr int NCH = D / 64;                    // d chunks per row
     static constexpr int Q = 0;
     static constexpr int K = Q + NCH * CHUNK;             // 2 stages
@@ -127,8 +131,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp == 1) {
         if (lane == 0) {
-            constexpr uint32_t idesc_s = idesc_bf16_f32(kRows, kKeys, 0, 0);  // Q, K both K-major (over d)
-            constexpr uint32_t idesc_o = idesc_bf16_f32(kRows, D, 0, 1);      // P K-major, V MN-major (d contiguous)
+            constexpr uint32_t idesc_s = idesc_f16_f32(kRows, kKeys, 0, 0);  // Q, K: binary16, K-major (over d)
+            constexpr uint32_t idesc_o = idesc_f16_f32(kRows, D, 0, 1);      // P K-major, V MN-major (d contiguous)
             const uint32_t sQ = smem_u32(smem + L::Q);
             const uint32_t sP = smem_u32(smem + L::P);
             auto issue_s = [&](int j) {
@@ -138,7 +142,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int c = 0; c < L::NCH; ++c)
 #pragma unroll
                     for (int k = 0; k < 4; ++k)
-                        umma_bf16_ss(tS, sw128_desc(sQ + c * L::CHUNK + 32 * k, 16, 1024),
+                        umma_f16_ss(tS, sw128_desc(sQ + c * L::CHUNK + 32 * k, 16, 1024),
                                      sw128_desc(sK + c * L::CHUNK + 32 * k, 16, 1024), idesc_s, (c | k) != 0);
                 umma_commit(s_full);
             };
@@ -161,7 +165,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t sV = smem_u32(smem + L::V + s * L::NCH * L::CHUNK);
 #pragma unroll
                 for (int k = 0; k < kKeys / 16; ++k)
-                    umma_bf16_ss(tO, sw128_desc(sP + (k >> 2) * L::CHUNK + 32 * (k & 3), 16, 1024),
+                    umma_f16_ss(tO, sw128_desc(sP + (k >> 2) * L::CHUNK + 32 * (k & 3), 16, 1024),
                                  sw128_desc(sV + k * 16 * 128, L::CHUNK, 1024), idesc_o, (j | k) != 0);
                 umma_commit(o_done);
                 umma_commit(kv_empty + s);
@@ -216,7 +220,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const float p0 = ex2(fmaf(sv[c], P.scale_log2, -m_use));
                 const float p1 = ex2(fmaf(sv[c + 1], P.scale_log2, -m_use));
                 rs += p0 + p1;
-                pk[c / 2] = pack_bf16(p0, p1);
+                pk[c / 2] = pack_f16(p0, p1);  // p <= 2^8: inside the binary16 range
             }
             l_i = l_i * alpha + rs;
             m_i = m_new;

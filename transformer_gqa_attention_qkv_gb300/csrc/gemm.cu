@@ -61,17 +61,28 @@ DEVI void tile_coords(int tile, int num_m, int num_n, int &mb, int &nb)
     nb = local / gm;
 }
 
-DEVI void store_row_bf16(uint16_t *dst, const float *v, int n)  // n multiple of 8, dst 16B aligned
+// 32 values of one row -> 16-bit storage (bf16, or binary16 clamped to its
+// finite range; *clamped is set when a value had to be clamped).  dst is
+// 16-byte aligned.
+DEVI void store32(uint16_t *dst, const float *v, bool f16, bool &clamped)
 {
     uint4 *d4 = reinterpret_cast<uint4 *>(dst);
+    if (f16) {
+        float c[32];
 #pragma unroll
-    for (int i = 0; i < n / 8; ++i) {
-        uint4 w;
-        w.x = pack_bf16(v[8 * i + 0], v[8 * i + 1]);
-        w.y = pack_bf16(v[8 * i + 2], v[8 * i + 3]);
-        w.z = pack_bf16(v[8 * i + 4], v[8 * i + 5]);
-        w.w = pack_bf16(v[8 * i + 6], v[8 * i + 7]);
-        d4[i] = w;
+        for (int i = 0; i < 32; ++i) {
+            c[i] = fminf(fmaxf(v[i], -kHalfMax), kHalfMax);
+            clamped |= !(c[i] == v[i]);
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            d4[i] = make_uint4(pack_f16(c[8 * i + 0], c[8 * i + 1]), pack_f16(c[8 * i + 2], c[8 * i + 3]),
+                               pack_f16(c[8 * i + 4], c[8 * i + 5]), pack_f16(c[8 * i + 6], c[8 * i + 7]));
+    } else {
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            d4[i] = make_uint4(pack_bf16(v[8 * i + 0], v[8 * i + 1]), pack_bf16(v[8 * i + 2], v[8 * i + 3]),
+                               pack_bf16(v[8 * i + 4], v[8 * i + 5]), pack_bf16(v[8 * i + 6], v[8 * i + 7]));
     }
 }
 
@@ -98,6 +109,8 @@ DEVI void epilogue_qkv(const GemmParams &P, uint32_t tcol, int m, int n0, bool r
         }
     }
     const bool has_norm = e.q_norm_w != nullptr;
+    const bool f16 = e.f16_out != 0;
+    bool clamped = false;
 #pragma unroll 1
     for (int h = 0; h < BN / D; ++h) {
         const int n = n0 + h * D;
@@ -128,7 +141,7 @@ DEVI void epilogue_qkv(const GemmParams &P, uint32_t tcol, int m, int n0, bool r
                 float v[32];
 #pragma unroll
                 for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
-                if (row_ok) store_row_bf16(dst + c, v, 32);
+                if (row_ok) store32(dst + c, v, f16, clamped);
             }
             continue;
         }
@@ -172,11 +185,12 @@ DEVI void epilogue_qkv(const GemmParams &P, uint32_t tcol, int m, int n0, bool r
                 }
             }
             if (row_ok) {
-                store_row_bf16(dst + c, y1, 32);
-                store_row_bf16(dst + c + D / 2, y2, 32);
+                store32(dst + c, y1, f16, clamped);
+                store32(dst + c + D / 2, y2, f16, clamped);
             }
         }
     }
+    if (clamped) atomicOr(P.err, kErrRange);
 }
 
 template <int BN>
@@ -298,7 +312,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint32_t b0 = smem_u32(sB + s * L::B_BYTES);
 #pragma unroll
                     for (int k = 0; k < BK / 16; ++k)
-                        umma_bf16_ss(d_tmem, sw128_desc(a0 + 32 * k, 16, 1024), sw128_desc(b0 + 32 * k, 16, 1024),
+                        umma_f16_ss(d_tmem, sw128_desc(a0 + 32 * k, 16, 1024), sw128_desc(b0 + 32 * k, 16, 1024),
                                      idesc, (kb | k) != 0);
                     umma_commit(empty + s);  // frees the stage once these MMAs have read it
                 }

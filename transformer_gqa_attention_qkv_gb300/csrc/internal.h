@@ -26,6 +26,7 @@ struct QkvEpilogue {
     float eps;
     const float2 *rope;    // [rope_rows][d/2] (cos, sin)
     int rope_rows;
+    int f16_out;           // 1: Q/K/V stored as binary16 (clamped, flagged); 0: bf16
     uint16_t *q_out, *k_out, *v_out;
 };
 

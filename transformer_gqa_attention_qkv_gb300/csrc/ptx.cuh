@@ -6,6 +6,7 @@
 
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <stdint.h>
 
 #define DEVI __device__ __forceinline__
@@ -16,6 +17,7 @@ namespace gqa {
 enum : unsigned {
     kErrTimeout = 1u,  // a bounded wait gave up
     kErrIndex = 2u,    // a device-side index check failed (e.g. cache slot out of range)
+    kErrRange = 4u,    // a value beyond the binary16 range was clamped
 };
 
 // Default limit of a bounded wait: 1 s of %globaltimer.  Every legitimate
@@ -139,17 +141,26 @@ DEVI uint64_t sw128_desc(uint32_t saddr, uint32_t lbo_bytes, uint32_t sbo_bytes)
     return d;
 }
 
-// Instruction descriptor of tcgen05.mma kind::f16: bf16 A and B, fp32 D,
-// M x N tile, each operand K-major (0) or MN-major (1).
-__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, int a_mn_major, int b_mn_major)
+// Instruction descriptor of tcgen05.mma kind::f16 with fp32 D: A and B both
+// bf16 (ab_fmt 1) or both binary16 (ab_fmt 0), M x N tile, each operand
+// K-major (0) or MN-major (1).
+__host__ __device__ constexpr uint32_t idesc_f32acc(int M, int N, int a_mn_major, int b_mn_major, uint32_t ab_fmt)
 {
     return (1u << 4)                        // D format f32
-           | (1u << 7)                      // A format bf16
-           | (1u << 10)                     // B format bf16
+           | (ab_fmt << 7)                  // A format
+           | (ab_fmt << 10)                 // B format
            | ((uint32_t)a_mn_major << 15)   // A major
            | ((uint32_t)b_mn_major << 16)   // B major
            | ((uint32_t)(N >> 3) << 17)     // N / 8
            | ((uint32_t)(M >> 4) << 24);    // M / 16
+}
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, int a_mn_major, int b_mn_major)
+{
+    return idesc_f32acc(M, N, a_mn_major, b_mn_major, 1u);
+}
+__host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N, int a_mn_major, int b_mn_major)
+{
+    return idesc_f32acc(M, N, a_mn_major, b_mn_major, 0u);
 }
 
 // Whole warp: allocate ncols TMEM columns (power of two >= 32); the base
@@ -166,8 +177,9 @@ DEVI void tmem_dealloc(uint32_t taddr, uint32_t ncols)
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
 }
 
-// D[tmem] (+)= A[smem desc] * B[smem desc]^T  (one thread issues)
-DEVI void umma_bf16_ss(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t accumulate)
+// D[tmem] (+)= A[smem desc] * B[smem desc]^T, kind::f16 (bf16 or binary16
+// operands as the instruction descriptor says); one thread issues.
+DEVI void umma_f16_ss(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t accumulate)
 {
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
@@ -244,6 +256,15 @@ DEVI uint32_t pack_bf16(float lo, float hi)
     __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t *>(&h);
 }
+
+// Two floats -> packed binary16x2 (round to nearest even), lo in the low half.
+DEVI uint32_t pack_f16(float lo, float hi)
+{
+    __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&h);
+}
+
+constexpr float kHalfMax = 65504.0f;  // largest finite binary16
 
 DEVI float ex2(float x)
 {

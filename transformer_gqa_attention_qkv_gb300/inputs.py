@@ -93,16 +93,17 @@ def _gen(seed: int, device) -> torch.Generator:
 
 
 def make_layer_inputs(cfg: LayerConfig, seed: int, *, w_std: float = 0.02,
-                      x_std: float = 1.0, norm_std: float = 0.1,
+                      x_std: float = 1.0, norm_std: float = 0.1, wo_std: float | None = None,
                       device: str = "cpu") -> dict:
     """bf16 tensors x [B,S,hidden], Wqkv [(Hq+2Hkv)d, hidden] (rows: W_q, W_k,
-    W_v), Wo [hidden, Hq d], q_norm_w / k_norm_w [d] (None without QK-norm)."""
+    W_v), Wo [hidden, Hq d], q_norm_w / k_norm_w [d] (None without QK-norm).
+    wo_std defaults to w_std."""
     g = _gen(seed, device)
     d = cfg.head_dim
     n_qkv = (cfg.Hq + 2 * cfg.Hkv) * d
     x = _normal((cfg.B, cfg.S, cfg.hidden), g, x_std, device=device)
     wqkv = _normal((n_qkv, cfg.hidden), g, w_std, device=device)
-    wo = _normal((cfg.hidden, cfg.Hq * d), g, w_std, device=device)
+    wo = _normal((cfg.hidden, cfg.Hq * d), g, w_std if wo_std is None else wo_std, device=device)
     if cfg.qk_norm:
         qn = _normal((d,), g, norm_std, 1.0, device=device)
         kn = _normal((d,), g, norm_std, 1.0, device=device)
