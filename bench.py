@@ -1,0 +1,464 @@
+#!/usr/bin/env python3
+"""Benchmark of the GQA attention layer forward on GB300.
+
+Default workload: the Qwen3-32B-shaped prefill layer (B=1, S=16384, hidden
+5120, 64 query heads, 8 KV heads, head_dim 128, QK-norm, RoPE theta 1e6,
+causal), bf16 inputs resident in HBM.  One step = one full layer forward
+(QKV projection + QK-norm + RoPE, causal GQA attention, o_proj + residual)
+through gqa_attn_forward_ex.  Metric: algorithmic TFLOP/s (2*M*N*K per
+projection, 4*d per visible (query head, query, key) pair) and its fraction of
+the measured dense bf16 peak.  The same line carries the decode step
+(Qwen3-8B shape, 64 sequences x 8192 cached tokens) in GB/s of algorithmic
+bytes against the measured HBM bandwidth.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+--impl reference times the plain fp64 CPU oracle on the host cores (there is
+no other implementation of this layer to compare against), on a bounded
+sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "attn-layer fwd TFLOP/s & % bf16 peak (prefill); decode GB/s & % HBM peak"
+L2_BYTES = 129 * 1024 * 1024
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+# ------------------------------------------------------------------ helpers
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return p, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def prefill_flops(cfg):
+    d = cfg.head_dim
+    M = cfg.B * cfg.S
+    qkv = 2 * M * (cfg.Hq + 2 * cfg.Hkv) * d * cfg.hidden
+    pairs = cfg.S * (cfg.S + 1) // 2 if cfg.causal else cfg.S * cfg.S
+    attn = 4 * cfg.B * cfg.Hq * d * pairs
+    oproj = 2 * M * cfg.hidden * cfg.Hq * d
+    return {"qkv": qkv, "attn": attn, "oproj": oproj, "total": qkv + attn + oproj}
+
+
+def decode_bytes(cfg):
+    """Algorithmic bytes of one decode step: each cached K/V entry read once
+    (plus the new one), weights read once, x/out, q and the appended K/V."""
+    d, B = cfg.head_dim, cfg.B
+    kv_read = 2 * B * cfg.Hkv * (cfg.cache_len + 1) * d * 2
+    weights = ((cfg.Hq + 2 * cfg.Hkv) * d * cfg.hidden + cfg.hidden * cfg.Hq * d) * 2
+    act = 2 * B * cfg.hidden * 2 + 2 * B * cfg.Hkv * d * 2
+    return {"kv_read": kv_read, "weights": weights, "act": act, "total": kv_read + weights + act}
+
+
+def source_hash(*rel):
+    h = hashlib.sha256()
+    for r in rel:
+        with open(os.path.join(ROOT, r), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(name, src_files):
+    """dram bytes per launch recorded under profiles/ for a kernel, or None if
+    the kernel's sources changed since the capture."""
+    path = os.path.join(ROOT, "profiles", f"{name}.traffic.txt")
+    try:
+        kv = {}
+        with open(path) as f:
+            for line in f:
+                if ":" in line and not line.startswith("#"):
+                    k, v = line.split(":", 1)
+                    kv[k.strip()] = v.strip()
+        if kv.get("source_sha") != source_hash(*src_files):
+            return None
+        return int(float(kv["dram_bytes_per_launch"]))
+    except (OSError, KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples every 200 ms while running."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        self.out = ""
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+
+    def summary(self):
+        rows = []
+        for line in (self.out or "").splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                rows.append((float(parts[0]), float(parts[1]), parts[4:8]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for _, _, fl in rows for i, v in enumerate(fl) if v.lower() == "active"})
+        loaded = [r[0] for r in rows if r[0] > 0.5 * r[1]] or [r[0] for r in rows]
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ---------------------------------------------------------------- CPU oracle
+
+def cpu_oracle_sample(cfg, tokens, seed):
+    """Time the fp64 oracle on the first `tokens` positions of one sequence of
+    the workload (all heads, all three stages).  Returns (flop/s, seconds,
+    threads, description)."""
+    import oracle
+    from transformer_gqa_attention_qkv_gb300.inputs import make_layer_inputs
+    sub = cfg.with_(B=1, S=tokens)
+    t = make_layer_inputs(sub, seed=seed)
+    threads = oracle.default_threads()
+    oracle.build()
+    t0 = time.perf_counter()
+    oracle.forward(t["x"], t["Wqkv"], t["Wo"], t["q_norm_w"], t["k_norm_w"], sub.rope_theta, sub.eps,
+                   sub.B, sub.S, sub.hidden, sub.Hq, sub.Hkv, sub.head_dim, causal=sub.causal, threads=threads)
+    dt = time.perf_counter() - t0
+    fl = prefill_flops(sub)["total"]
+    desc = (f"fp64 oracle, full layer on the first {tokens} tokens of one sequence of {cfg.name} "
+            f"(all {cfg.Hq} query heads; {fl / 1e9:.1f} GFLOP algorithmic)")
+    return fl / dt, dt, threads, desc
+
+
+# --------------------------------------------------------------- distributed
+
+def dist_setup(n_gpus):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if os.environ.get("BENCH_BACKEND", "nccl") == "nccl" else "gloo"
+        dist.init_process_group(backend=backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def reduce_max(value, world, device=None):
+    """max over ranks of a float (the slowest rank defines the job's time)."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def reduce_sum(value, world, device=None):
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+# --------------------------------------------------------------- our arm
+
+def run_ours(args, world, rank, local):
+    import torch
+
+    from transformer_gqa_attention_qkv_gb300 import binding as gq
+    from transformer_gqa_attention_qkv_gb300.inputs import (DECODE_CONFIGS, PREFILL_CONFIGS, SEEDS,
+                                                            make_decode_inputs, make_layer_inputs)
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream()
+    peaks, peak_src = load_peaks()
+    cfg = PREFILL_CONFIGS[args.workload]
+    fl = prefill_flops(cfg)
+
+    # ---- prefill inputs (generated on the device, seeded; larger than L2)
+    t = make_layer_inputs(cfg, seed=SEEDS[cfg.name] + 7919 * rank, device=str(dev))
+    out = torch.empty_like(t["x"])
+    ws = gq.new_workspace(gq.gqa_attn_workspace_size(cfg.B, cfg.S, cfg.hidden, cfg.Hq, cfg.Hkv,
+                                                     cfg.head_dim), dev)
+    flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev)
+
+    def fwd():
+        gq.gqa_attn_forward_ex(t["x"], t["Wqkv"], t["Wo"], t["q_norm_w"], t["k_norm_w"], cfg.rope_theta,
+                               cfg.eps, cfg.B, cfg.S, cfg.hidden, cfg.Hq, cfg.Hkv, cfg.head_dim, cfg.causal,
+                               out, ws, stream)
+
+    for _ in range(args.warmup):
+        fwd()
+    torch.cuda.synchronize()
+    if gq.gqa_check_device_error() != 0:
+        raise RuntimeError("device error during warm-up: " + gq.gqa_last_error())
+
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    launches = 0
+    with ClockSampler(local) as clk:
+        barrier(world)
+        torch.cuda.synchronize()
+        wall0 = time.perf_counter()
+        for i in range(args.steps):
+            flush.zero_()  # evict L2 between steps (outside the events)
+            ev[i][0].record(stream)
+            fwd()
+            launches += gq.gqa_last_launch_count()
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+        wall = time.perf_counter() - wall0
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    ms = statistics.mean(step_ms)
+    ms_job = reduce_max(ms, world, dev)
+    value = reduce_sum(fl["total"], world, dev) / (ms_job * 1e-3) / 1e12
+
+    # ---- per-kernel durations (same kernels, launched stage by stage, events between)
+    d = cfg.head_dim
+    q = ws[:cfg.B * cfg.Hq * cfg.S * d * 2].view(torch.float16)
+    k = torch.empty((cfg.B, cfg.Hkv, cfg.S, d), dtype=torch.float16, device=dev)
+    v = torch.empty_like(k)
+    attn = torch.empty((cfg.B * cfg.S, cfg.Hq * d), dtype=torch.bfloat16, device=dev)
+    stage_ms = {"qkv": [], "attn": [], "oproj": []}
+    for i in range(args.warmup + args.steps):
+        e = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+        flush.zero_()
+        e[0].record(stream)
+        gq.gqa_qkv_proj(t["x"], t["Wqkv"], t["q_norm_w"], t["k_norm_w"], cfg.rope_theta, cfg.eps, cfg.B, cfg.S,
+                        cfg.hidden, cfg.Hq, cfg.Hkv, d, q, k, v, stream)
+        e[1].record(stream)
+        gq.gqa_attention(q, k, v, cfg.B, cfg.S, cfg.Hq, cfg.Hkv, d, cfg.causal, attn, stream)
+        e[2].record(stream)
+        gq.gqa_oproj_residual(attn, t["Wo"], t["x"], cfg.B * cfg.S, cfg.hidden, cfg.Hq * d, out, stream)
+        e[3].record(stream)
+        torch.cuda.synchronize()
+        if i >= args.warmup:
+            stage_ms["qkv"].append(e[0].elapsed_time(e[1]))
+            stage_ms["attn"].append(e[1].elapsed_time(e[2]))
+            stage_ms["oproj"].append(e[2].elapsed_time(e[3]))
+    kern = {s: statistics.mean(v_) for s, v_ in stage_ms.items()}
+    dom = max(("qkv", "attn", "oproj"), key=lambda s: kern[s])
+    peak_tf = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    dom_src = {"attn": ["transformer_gqa_attention_qkv_gb300/csrc/attention.cu"],
+               "qkv": ["transformer_gqa_attention_qkv_gb300/csrc/gemm.cu"],
+               "oproj": ["transformer_gqa_attention_qkv_gb300/csrc/gemm.cu"]}[dom]
+    achieved = fl[dom] / (kern[dom] * 1e-3) / 1e12
+    roofline = {"bound": "tensor", "kernel": dom, "achieved": round(achieved, 1), "peak": peak_tf,
+                "unit": "TFLOP/s", "frac": round(achieved / peak_tf, 4),
+                "peak_source": f"{peak_src} bf16 dense (burst); binary16 and bf16 share the dense rate",
+                "traffic": recorded_traffic(f"{dom}_{cfg.name}", dom_src),
+                "kernel_ms": {s: round(x, 4) for s, x in kern.items()},
+                "kernel_tflops": {s: round(fl[s] / (kern[s] * 1e-3) / 1e12, 1) for s in kern}}
+    del q, k, v, attn
+
+    # ---- e2e: host (pinned) x in, host out back, inside the timed region
+    x_host = t["x"].cpu().pin_memory()
+    out_host = torch.empty_like(x_host).pin_memory()
+    x_dev = torch.empty_like(t["x"])
+
+    def fwd_e2e():
+        x_dev.copy_(x_host, non_blocking=True)
+        gq.gqa_attn_forward_ex(x_dev, t["Wqkv"], t["Wo"], t["q_norm_w"], t["k_norm_w"], cfg.rope_theta,
+                               cfg.eps, cfg.B, cfg.S, cfg.hidden, cfg.Hq, cfg.Hkv, cfg.head_dim, cfg.causal,
+                               out, ws, stream)
+        out_host.copy_(out, non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        fwd_e2e()
+    torch.cuda.synchronize()
+    barrier(world)
+    ee = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    for i in range(args.steps):
+        flush.zero_()
+        ee[i][0].record(stream)
+        fwd_e2e()
+        ee[i][1].record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    e2e_ms = reduce_max(statistics.mean(a.elapsed_time(b) for a, b in ee), world, dev)
+    e2e = {"value": round(reduce_sum(fl["total"], world, dev) / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+           "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": x_host.numel() * 2,
+           "d2h_bytes_per_step": out_host.numel() * 2}
+    del t, out, ws, x_host, out_host, x_dev
+    torch.cuda.empty_cache()
+
+    # ---- decode step
+    dc = DECODE_CONFIGS["qwen3_8b_decode"]
+    db = decode_bytes(dc)
+    dt_ = make_decode_inputs(dc, seed=SEEDS[dc.name] + 7919 * rank, device=str(dev))
+    dout = torch.empty_like(dt_["x"])
+    dws = gq.new_workspace(gq.gqa_attn_decode_workspace_size(dc.B, dc.hidden, dc.Hq, dc.Hkv, dc.head_dim,
+                                                             dc.lmax), dev)
+
+    def dec():
+        gq.gqa_attn_decode(dt_["x"], dt_["Wqkv"], dt_["Wo"], dt_["q_norm_w"], dt_["k_norm_w"], dc.rope_theta,
+                           dc.eps, dc.B, dc.hidden, dc.Hq, dc.Hkv, dc.head_dim, dt_["k_cache"], dt_["v_cache"],
+                           dt_["cache_len"], dc.lmax, dout, dws, stream)
+
+    for _ in range(args.warmup):
+        dec()
+    torch.cuda.synchronize()
+    dev_ = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    barrier(world)
+    for i in range(args.steps):
+        flush.zero_()
+        dev_[i][0].record(stream)
+        dec()
+        launches += gq.gqa_last_launch_count()
+        dev_[i][1].record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    dms = reduce_max(statistics.mean(a.elapsed_time(b) for a, b in dev_), world, dev)
+    # decode attention kernel alone (split + combine), for its roofline
+    qd = torch.empty((dc.B, dc.Hq, dc.head_dim), dtype=torch.bfloat16, device=dev)
+    ad = torch.empty((dc.B, dc.Hq * dc.head_dim), dtype=torch.bfloat16, device=dev)
+    kl = (dt_["cache_len"] + 1).to(torch.int32)
+    aws = gq.new_workspace(gq.gqa_decode_attention_workspace_size(dc.B, dc.Hq, dc.Hkv, dc.head_dim, dc.lmax),
+                           dev)
+    ams = []
+    for i in range(args.warmup + args.steps):
+        a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        flush.zero_()
+        a0.record(stream)
+        gq.gqa_decode_attention(qd, dt_["k_cache"], dt_["v_cache"], kl, dc.B, dc.Hq, dc.Hkv, dc.head_dim,
+                                dc.lmax, ad, aws, stream)
+        a1.record(stream)
+        torch.cuda.synchronize()
+        if i >= args.warmup:
+            ams.append(a0.elapsed_time(a1))
+    ams_ = statistics.mean(ams)
+    hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    attn_bytes = db["kv_read"] + dc.B * dc.Hq * dc.head_dim * 2 * 2
+    dec_ach = attn_bytes / (ams_ * 1e-3) / 1e9
+    decode = {"workload": dc.name, "value": round(reduce_sum(db["total"], world, dev) / (dms * 1e-3) / 1e9, 1),
+              "unit": "GB/s", "ms_per_step": round(dms, 4), "frac_of_hbm": round(db["total"] / (dms * 1e-3) / 1e9 / hbm, 4),
+              "bytes_per_step": db["total"],
+              "roofline": {"bound": "hbm", "kernel": "decode_attention", "achieved": round(dec_ach, 1),
+                           "peak": hbm, "unit": "GB/s", "frac": round(dec_ach / hbm, 4),
+                           "peak_source": f"{peak_src} copy bandwidth",
+                           "traffic": recorded_traffic("decode_attention_" + dc.name,
+                                                       ["transformer_gqa_attention_qkv_gb300/csrc/decode.cu"]),
+                           "kernel_ms": round(ams_, 4)}}
+    del dt_, dout, dws
+
+    # ---- CPU baseline (rank 0, N=1 only)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu:
+        fls, secs, threads, desc = cpu_oracle_sample(cfg, args.cpu_tokens, SEEDS[cfg.name])
+        cpu = {"value": round(fls / 1e12, 6), "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+               "sample": desc, "seconds": round(secs, 2)}
+
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_job, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16 in/out, binary16 Q/K/V/P, fp32 accumulate", "data": "synthetic",
+        "frac_of_peak": round(value / world / peak_tf, 4),
+        "config": {"workload": cfg.name, "B": cfg.B, "S": cfg.S, "hidden": cfg.hidden, "Hq": cfg.Hq,
+                   "Hkv": cfg.Hkv, "head_dim": cfg.head_dim, "qk_norm": cfg.qk_norm, "rope_theta": cfg.rope_theta,
+                   "causal": cfg.causal, "flops_per_step": fl["total"], "parallelism": f"replicas x{world}",
+                   "l2": "flushed between steps (2x L2 buffer written outside the timed events)"},
+        "roofline": roofline, "decode": decode, "e2e": e2e, "cpu_baseline": cpu,
+        "gpu_launches": launches, "wall_s": round(wall, 3), "clocks": clk.summary(),
+        "step_ms": [round(x, 4) for x in step_ms],
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------- reference arm
+
+def run_reference(args, world, rank):
+    """The fp64 CPU oracle, as it stands, on the host cores; each step is a
+    bounded sample (a prefix of one sequence) of the same workload."""
+    if rank != 0:
+        return
+    from transformer_gqa_attention_qkv_gb300.inputs import PREFILL_CONFIGS, SEEDS
+    cfg = PREFILL_CONFIGS[args.workload]
+    for _ in range(args.warmup):
+        cpu_oracle_sample(cfg, args.ref_tokens, SEEDS[cfg.name])
+    rates, secs = [], []
+    for _ in range(args.steps):
+        r, s, threads, desc = cpu_oracle_sample(cfg, args.ref_tokens, SEEDS[cfg.name])
+        rates.append(r)
+        secs.append(s)
+    value = statistics.mean(rates) / 1e12
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * statistics.mean(secs), 1),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": cfg.name, "B": cfg.B, "S": cfg.S, "hidden": cfg.hidden, "Hq": cfg.Hq,
+                       "Hkv": cfg.Hkv, "head_dim": cfg.head_dim, "parallelism": "host cores"},
+            "cpu_baseline": {"kind": "oracle", "cores": threads, "sample": desc, "value": round(value, 6),
+                             "unit": "TFLOP/s"},
+            "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="qwen3_32b")
+    ap.add_argument("--cpu-tokens", type=int, default=512, help="tokens of the CPU-baseline sample")
+    ap.add_argument("--ref-tokens", type=int, default=256, help="tokens per reference-arm step")
+    ap.add_argument("--no-cpu", action="store_true")
+    args = ap.parse_args(argv)
+    world, rank, local = dist_setup(args.gpus)
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+    else:
+        run_ours(args, world, rank, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
