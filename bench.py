@@ -108,7 +108,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "100"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
@@ -241,19 +241,21 @@ def run_ours(args, world, rank, local):
 
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     launches = 0
-    with ClockSampler(local) as clk:
-        barrier(world)
-        torch.cuda.synchronize()
-        wall0 = time.perf_counter()
-        for i in range(args.steps):
-            flush.zero_()  # evict L2 between steps (outside the events)
-            ev[i][0].record(stream)
-            fwd()
-            launches += gq.gqa_last_launch_count()
-            ev[i][1].record(stream)
-        torch.cuda.synchronize()
-        barrier(world)
-        wall = time.perf_counter() - wall0
+    # clocks are sampled from here to the end of the last timed loop (decode)
+    clk = ClockSampler(local).__enter__()
+    time.sleep(0.25)
+    barrier(world)
+    torch.cuda.synchronize()
+    wall0 = time.perf_counter()
+    for i in range(args.steps):
+        flush.zero_()  # evict L2 between steps (outside the events)
+        ev[i][0].record(stream)
+        fwd()
+        launches += gq.gqa_last_launch_count()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    wall = time.perf_counter() - wall0
     step_ms = [a.elapsed_time(b) for a, b in ev]
     ms = statistics.mean(step_ms)
     ms_job = reduce_max(ms, world, dev)
@@ -355,6 +357,7 @@ def run_ours(args, world, rank, local):
     torch.cuda.synchronize()
     barrier(world)
     dms = reduce_max(statistics.mean(a.elapsed_time(b) for a, b in dev_), world, dev)
+    clk.__exit__(None, None, None)
     # decode attention kernel alone (split + combine), for its roofline
     qd = torch.empty((dc.B, dc.Hq, dc.head_dim), dtype=torch.bfloat16, device=dev)
     ad = torch.empty((dc.B, dc.Hq * dc.head_dim), dtype=torch.bfloat16, device=dev)
@@ -439,19 +442,83 @@ def run_reference(args, world, rank):
     print(json.dumps(line), flush=True)
 
 
+def run_stage(args, local):
+    """Launch one stage alone, warmup + steps times, and print its mean time.
+    Used for profiler captures of a single kernel (not a benchmark line)."""
+    import torch
+
+    from transformer_gqa_attention_qkv_gb300 import binding as gq
+    from transformer_gqa_attention_qkv_gb300.inputs import (DECODE_CONFIGS, PREFILL_CONFIGS, SEEDS,
+                                                            make_decode_inputs, make_layer_inputs)
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream()
+    if args.stage == "decode_attn":
+        dc = DECODE_CONFIGS["qwen3_8b_decode"]
+        t = make_decode_inputs(dc, seed=SEEDS[dc.name], device=str(dev))
+        q = torch.randn((dc.B, dc.Hq, dc.head_dim), device=dev).to(torch.bfloat16)
+        a = torch.empty((dc.B, dc.Hq * dc.head_dim), dtype=torch.bfloat16, device=dev)
+        kl = (t["cache_len"] + 1).to(torch.int32)
+        ws = gq.new_workspace(gq.gqa_decode_attention_workspace_size(dc.B, dc.Hq, dc.Hkv, dc.head_dim, dc.lmax), dev)
+
+        def go():
+            gq.gqa_decode_attention(q, t["k_cache"], t["v_cache"], kl, dc.B, dc.Hq, dc.Hkv, dc.head_dim, dc.lmax,
+                                    a, ws, stream)
+        name = dc.name
+    else:
+        cfg = PREFILL_CONFIGS[args.workload]
+        t = make_layer_inputs(cfg, seed=SEEDS[cfg.name], device=str(dev))
+        d = cfg.head_dim
+        q = torch.empty((cfg.B, cfg.Hq, cfg.S, d), dtype=torch.float16, device=dev)
+        k = torch.empty((cfg.B, cfg.Hkv, cfg.S, d), dtype=torch.float16, device=dev)
+        v = torch.empty_like(k)
+        attn = torch.empty((cfg.B * cfg.S, cfg.Hq * d), dtype=torch.bfloat16, device=dev)
+        out = torch.empty_like(t["x"])
+        gq.gqa_qkv_proj(t["x"], t["Wqkv"], t["q_norm_w"], t["k_norm_w"], cfg.rope_theta, cfg.eps, cfg.B, cfg.S,
+                        cfg.hidden, cfg.Hq, cfg.Hkv, d, q, k, v, stream)
+        gq.gqa_attention(q, k, v, cfg.B, cfg.S, cfg.Hq, cfg.Hkv, d, cfg.causal, attn, stream)
+
+        def go():
+            if args.stage == "qkv":
+                gq.gqa_qkv_proj(t["x"], t["Wqkv"], t["q_norm_w"], t["k_norm_w"], cfg.rope_theta, cfg.eps, cfg.B,
+                                cfg.S, cfg.hidden, cfg.Hq, cfg.Hkv, d, q, k, v, stream)
+            elif args.stage == "attn":
+                gq.gqa_attention(q, k, v, cfg.B, cfg.S, cfg.Hq, cfg.Hkv, d, cfg.causal, attn, stream)
+            else:
+                gq.gqa_oproj_residual(attn, t["Wo"], t["x"], cfg.B * cfg.S, cfg.hidden, cfg.Hq * d, out, stream)
+        name = cfg.name
+    torch.cuda.synchronize()
+    ms = []
+    for i in range(args.warmup + args.steps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        go()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        if i >= args.warmup:
+            ms.append(e0.elapsed_time(e1))
+    if gq.gqa_check_device_error() != 0:
+        raise RuntimeError(gq.gqa_last_error())
+    print(json.dumps({"stage": args.stage, "workload": name, "ms": round(statistics.mean(ms), 4) if ms else None}))
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="qwen3_32b")
     ap.add_argument("--cpu-tokens", type=int, default=512, help="tokens of the CPU-baseline sample")
     ap.add_argument("--ref-tokens", type=int, default=256, help="tokens per reference-arm step")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--stage", choices=["qkv", "attn", "oproj", "decode_attn"], default=None,
+                    help="launch one stage alone (for profiler captures); prints its time, no benchmark line")
     args = ap.parse_args(argv)
     world, rank, local = dist_setup(args.gpus)
-    if args.impl == "reference":
+    if args.stage:
+        run_stage(args, local)
+    elif args.impl == "reference":
         run_reference(args, world, rank)
     else:
         run_ours(args, world, rank, local)

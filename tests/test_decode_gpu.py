@@ -79,7 +79,7 @@ def test_decode_attention_stage(B, Hq, Hkv, d, Lmax, lens):
     assert_parity("decode attn", to64(out), ref)
 
 
-def run_decode(cfg, t, cache_len=None):
+def run_decode(cfg, t, cache_len=None, want_attn=False):
     kc, vc = dev(t["k_cache"]), dev(t["v_cache"])
     cl = dev(t["cache_len"] if cache_len is None else cache_len)
     out = torch.empty((cfg.B, cfg.hidden), dtype=torch.bfloat16, device=DEV)
@@ -90,7 +90,13 @@ def run_decode(cfg, t, cache_len=None):
                        cfg.lmax, out, ws)
     torch.cuda.synchronize()
     assert gq.gqa_check_device_error() == 0
-    return out
+    if not want_attn:
+        return out
+    # workspace layout: q [B,Hq,d] bf16, then attn [B,Hq*d] bf16, each 256-byte aligned
+    n = cfg.B * cfg.Hq * cfg.head_dim * 2
+    off = (n + 255) // 256 * 256
+    attn = ws[off:off + n].view(torch.bfloat16).view(cfg.B, cfg.Hq * cfg.head_dim)
+    return out, attn
 
 
 def test_decode_step_reduced_ragged():
@@ -109,9 +115,11 @@ def test_decode_step_full_workload():
     launch configuration the benchmark times; full oracle."""
     cfg = DECODE_CONFIGS["qwen3_8b_decode"]
     t = make_decode_inputs(cfg, seed=SEEDS["qwen3_8b_decode"])
-    out = run_decode(cfg, t)
+    out, attn = run_decode(cfg, t, want_attn=True)
     ref = oracle.decode(t["x"], t["Wqkv"], t["Wo"], t["q_norm_w"], t["k_norm_w"], cfg.rope_theta, cfg.eps,
                         cfg.B, cfg.hidden, cfg.Hq, cfg.Hkv, cfg.head_dim, t["k_cache"], t["v_cache"],
                         t["cache_len"], cfg.lmax)
     assert_parity("decode out", to64(out), ref["out"])
-    assert_parity("decode out - x", to64(out) - to64(t["x"]), ref["out"] - to64(t["x"]), 2e-2, 1e-2)
+    # the attention output itself: the o_proj term (~1e-2) sits below the bf16
+    # resolution of out (|x| ~ 1), so out alone cannot show an error in it
+    assert_parity("decode attn", to64(attn), ref["attn"])
