@@ -187,6 +187,30 @@ int gqa_decode_attention(const gqa_bf16 *q, const gqa_bf16 *k_cache, const gqa_b
                          gqa_bf16 *attn_out, void *workspace, size_t workspace_bytes,
                          void *stream);
 
+/* The same decode attention as gqa_decode_attention, for callers that cannot
+ * allocate device memory: no workspace argument, and the call itself performs
+ * no allocation.  It is meant for hosts that give a kernel only its input and
+ * output buffers (plugin or custom-op interfaces without a workspace hook) and
+ * for serving loops whose device memory is owned entirely by another
+ * allocator.  The pages have no counterpart for this entry point; it exists
+ * only for those callers.
+ *   Scratch: a fixed 16 MiB array of fp32 split partials compiled into the
+ *   library (kept on every GPU that loads the library until the process
+ *   exits).  Sizes whose partials for a single split exceed it
+ *   (B*Hq*(head_dim+2) > 4194304 floats) return GQA_ERR_UNSUPPORTED; larger
+ *   problems may use fewer splits than gqa_decode_attention does, so results
+ *   agree to rounding, not bit for bit.
+ *   Sharing: every call uses the same array and leaves its last partials in
+ *   it; calls that overlap on the GPU race and give wrong results, so order
+ *   them (one stream, or events).
+ *   Set-up: the first call on a device looks up the array's device address
+ *   with that device current; make that first call before any stream capture.
+ * Arguments as for gqa_decode_attention; device-side length errors are not
+ * reported (those sequences get zero rows). */
+int gqa_decode_attention_noalloc(const gqa_bf16 *q, const gqa_bf16 *k_cache, const gqa_bf16 *v_cache,
+                                 const int *kv_len, int B, int Hq, int Hkv, int head_dim, int Lmax,
+                                 gqa_bf16 *attn_out, void *stream);
+
 /* ------------------------------------------------------------ accounting */
 
 /* Algorithmic cost of one prefill forward, all pointers host, any may be NULL

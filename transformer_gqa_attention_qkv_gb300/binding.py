@@ -30,7 +30,7 @@ EXPORTS = (
     "gqa_attention", "gqa_oproj_residual", "gqa_attn_decode_workspace_size", "gqa_attn_decode",
     "gqa_decode_qkv", "gqa_decode_attention_workspace_size", "gqa_decode_attention",
     "gqa_attn_cost", "gqa_last_error", "gqa_check_device_error", "gqa_selftest_bounded_wait",
-    "gqa_last_launch_count",
+    "gqa_last_launch_count", "gqa_decode_attention_noalloc",
 )
 
 
@@ -74,6 +74,7 @@ def lib():
         "gqa_check_device_error": (_I, []),
         "gqa_selftest_bounded_wait": (_I, [_I]),
         "gqa_last_launch_count": (_I, []),
+        "gqa_decode_attention_noalloc": (_I, [_P] * 4 + [_I] * 5 + [_P, _P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(L, name)
@@ -198,6 +199,15 @@ def gqa_decode_attention(q, k_cache, v_cache, kv_len, B, Hq, Hkv, head_dim, Lmax
     _check(lib().gqa_decode_attention(_bf16(q), _bf16(k_cache), _bf16(v_cache), _i32(kv_len), B, Hq, Hkv,
                                       head_dim, Lmax, _bf16(attn_out), _ptr(workspace),
                                       workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def gqa_decode_attention_noalloc(q, k_cache, v_cache, kv_len, B, Hq, Hkv, head_dim, Lmax, attn_out,
+                                 stream=None):
+    """Decode attention without a workspace, for callers that cannot allocate
+    device memory: the split partials live in a fixed array inside the
+    library.  Calls that overlap on the GPU race on that array."""
+    _check(lib().gqa_decode_attention_noalloc(_bf16(q), _bf16(k_cache), _bf16(v_cache), _i32(kv_len), B, Hq,
+                                              Hkv, head_dim, Lmax, _bf16(attn_out), _stream(stream)))
 
 
 # ---------------------------------------------------------------- accounting

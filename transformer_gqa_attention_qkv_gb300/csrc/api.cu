@@ -32,6 +32,8 @@ static int fail(int code, const char *fmt, ...)
     return code;
 }
 
+void record_error_message(const char *msg) { snprintf(g_msg, sizeof g_msg, "%s", msg); }
+
 static int cuda_fail(cudaError_t e, const char *what)
 {
     return fail(GQA_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));

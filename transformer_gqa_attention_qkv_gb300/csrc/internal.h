@@ -77,6 +77,9 @@ cudaError_t launch_decode_attention(const DecodeAttentionProblem &p, unsigned *e
 // --------------------------------------------------------------- self test
 cudaError_t launch_selftest_wait(unsigned *err, unsigned long long limit_ns, cudaStream_t stream);
 
+// Sets the message gqa_last_error() returns on the calling thread.
+void record_error_message(const char *msg);
+
 // Tensor-map encoder (driver entry point, resolved once).
 CUresult encode_tmap(CUtensorMap *map, const void *base, int rank, const uint64_t *dims,
                      const uint64_t *strides_bytes, const uint32_t *box, bool swizzle128);
