@@ -359,7 +359,7 @@ def run_ours(args, world, rank, local):
     dms = reduce_max(statistics.mean(a.elapsed_time(b) for a, b in dev_), world, dev)
     clk.__exit__(None, None, None)
     # decode attention kernel alone (split + combine), for its roofline
-    qd = torch.empty((dc.B, dc.Hq, dc.head_dim), dtype=torch.bfloat16, device=dev)
+    qd = torch.zeros((dc.B, dc.Hq, dc.head_dim), dtype=torch.float16, device=dev)
     ad = torch.empty((dc.B, dc.Hq * dc.head_dim), dtype=torch.bfloat16, device=dev)
     kl = (dt_["cache_len"] + 1).to(torch.int32)
     aws = gq.new_workspace(gq.gqa_decode_attention_workspace_size(dc.B, dc.Hq, dc.Hkv, dc.head_dim, dc.lmax),
@@ -456,7 +456,7 @@ def run_stage(args, local):
     if args.stage == "decode_attn":
         dc = DECODE_CONFIGS["qwen3_8b_decode"]
         t = make_decode_inputs(dc, seed=SEEDS[dc.name], device=str(dev))
-        q = torch.randn((dc.B, dc.Hq, dc.head_dim), device=dev).to(torch.bfloat16)
+        q = torch.randn((dc.B, dc.Hq, dc.head_dim), device=dev).to(torch.float16)
         a = torch.empty((dc.B, dc.Hq * dc.head_dim), dtype=torch.bfloat16, device=dev)
         kl = (t["cache_len"] + 1).to(torch.int32)
         ws = gq.new_workspace(gq.gqa_decode_attention_workspace_size(dc.B, dc.Hq, dc.Hkv, dc.head_dim, dc.lmax), dev)

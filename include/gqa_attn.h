@@ -166,23 +166,24 @@ int gqa_attn_decode(const gqa_bf16 *x, const gqa_bf16 *Wqkv, const gqa_bf16 *Wo,
                     gqa_bf16 *out, void *workspace, size_t workspace_bytes, void *stream);
 
 /* Decode stage 1 alone: projection + QK-norm + RoPE at position
- * cache_len[b]; q_out [B, Hq, head_dim]; K and V written into the caches at
+ * cache_len[b]; q_out [B, Hq, head_dim] as binary16 (see
+ * gqa_attn_workspace_size for why); K and V written as bf16 into the caches at
  * slot cache_len[b]. */
 int gqa_decode_qkv(const gqa_bf16 *x, const gqa_bf16 *Wqkv,
                    const gqa_bf16 *q_norm_w, const gqa_bf16 *k_norm_w,
                    float rope_theta, float eps,
                    int B, int hidden, int Hq, int Hkv, int head_dim,
                    gqa_bf16 *k_cache, gqa_bf16 *v_cache, const int *cache_len, int Lmax,
-                   gqa_bf16 *q_out, void *stream);
+                   gqa_f16 *q_out, void *stream);
 
 /* Bytes of workspace gqa_decode_attention needs for its split partials. */
 size_t gqa_decode_attention_workspace_size(int B, int Hq, int Hkv, int head_dim, int Lmax);
 
 /* Decode stage 2 alone: split-KV attention of one query per sequence,
- * q [B, Hq, head_dim], over keys [0, kv_len[b]) of the caches
+ * q [B, Hq, head_dim] binary16, over keys [0, kv_len[b]) of the bf16 caches
  * [B, Hkv, Lmax, head_dim]; kv_len device int32 [B], 1 <= kv_len[b] <= Lmax.
- * attn_out [B, Hq*head_dim]. */
-int gqa_decode_attention(const gqa_bf16 *q, const gqa_bf16 *k_cache, const gqa_bf16 *v_cache,
+ * attn_out [B, Hq*head_dim] bf16. */
+int gqa_decode_attention(const gqa_f16 *q, const gqa_bf16 *k_cache, const gqa_bf16 *v_cache,
                          const int *kv_len, int B, int Hq, int Hkv, int head_dim, int Lmax,
                          gqa_bf16 *attn_out, void *workspace, size_t workspace_bytes,
                          void *stream);
@@ -207,7 +208,7 @@ int gqa_decode_attention(const gqa_bf16 *q, const gqa_bf16 *k_cache, const gqa_b
  *   with that device current; make that first call before any stream capture.
  * Arguments as for gqa_decode_attention; device-side length errors are not
  * reported (those sequences get zero rows). */
-int gqa_decode_attention_noalloc(const gqa_bf16 *q, const gqa_bf16 *k_cache, const gqa_bf16 *v_cache,
+int gqa_decode_attention_noalloc(const gqa_f16 *q, const gqa_bf16 *k_cache, const gqa_bf16 *v_cache,
                                  const int *kv_len, int B, int Hq, int Hkv, int head_dim, int Lmax,
                                  gqa_bf16 *attn_out, void *stream);
 

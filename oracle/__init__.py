@@ -78,7 +78,7 @@ def _load():
                                    _L, _L, _L, _L, _L, _L, _I, _i64p, _L,
                                    _f64p, _f64p, _f64p, _f64p, _f64p, _I]
     lib.oracle_decode_attention_stage.restype = _I
-    lib.oracle_decode_attention_stage.argtypes = [_u16p, _u16p, _u16p, _i32p,
+    lib.oracle_decode_attention_stage.argtypes = [_u16p, _I, _u16p, _u16p, _i32p,
                                                   _L, _L, _L, _L, _L, _f64p, _I]
     lib.oracle_decode.restype = _I
     lib.oracle_decode.argtypes = [_u16p, _u16p, _u16p, _u16p, _u16p, _D, _D,
@@ -255,11 +255,12 @@ def forward(x, Wqkv, Wo, q_norm_w, k_norm_w, rope_theta, eps, B, S, hidden, Hq, 
 
 
 def decode_attention_stage(q, k_cache, v_cache, kv_len, B, Hq, Hkv, d, Lmax, threads=None):
-    """attn [B, Hq*d] of bf16 q [B,Hq,d] over keys [0, kv_len[b]) of the caches."""
+    """attn [B, Hq*d] of q [B,Hq,d] (bf16 or float16) over keys [0, kv_len[b])
+    of the bf16 caches."""
     out = np.empty((B, Hq * d))
     kl = np.ascontiguousarray(np.asarray(kv_len, dtype=np.int32))
-    qb, kb, vb = _bits(q), _bits(k_cache), _bits(v_cache)
-    _check(_load().oracle_decode_attention_stage(_p16(qb), _p16(kb), _p16(vb),
+    qb, kb, vb = _bits(q, True), _bits(k_cache), _bits(v_cache)
+    _check(_load().oracle_decode_attention_stage(_p16(qb), int(_is_f16(q)), _p16(kb), _p16(vb),
                                                  kl.ctypes.data_as(_i32p), B, Hq, Hkv, d, Lmax,
                                                  _pf(out), threads or default_threads()),
            "decode_attention_stage")

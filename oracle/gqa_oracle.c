@@ -464,8 +464,9 @@ done:
 
 /* Attention of one query token per sequence over keys [0, kv_len[b]) of a
  * bf16 cache laid out [B, Hkv, Lmax, d] ([T07] §4 step 5: the cache returns
- * the full history).  q [B,Hq,d] bf16; attn [B, Hq*d]. */
-int oracle_decode_attention_stage(const uint16_t *q, const uint16_t *k_cache,
+ * the full history).  q [B,Hq,d] bf16 (q_f16 = 0) or binary16 (q_f16 = 1),
+ * widened exactly; attn [B, Hq*d]. */
+int oracle_decode_attention_stage(const uint16_t *q, int q_f16, const uint16_t *k_cache,
                                   const uint16_t *v_cache, const int *kv_len,
                                   long B, long Hq, long Hkv, long d, long Lmax,
                                   double *attn, int nthreads)
@@ -482,7 +483,7 @@ int oracle_decode_attention_stage(const uint16_t *q, const uint16_t *k_cache,
         for (long j = 0; j < Hq; ++j) {
             long g = j / G;
             double qv[1024];
-            for (long c = 0; c < d; ++c) qv[c] = bf(q[(b * Hq + j) * d + c]);
+            for (long c = 0; c < d; ++c) qv[c] = w16(q[(b * Hq + j) * d + c], q_f16);
             kv_src src = {k_cache + (b * Hkv + g) * Lmax * d, v_cache + (b * Hkv + g) * Lmax * d,
                           NULL, NULL, kv_len[b], 0};
             int e = attend_row(qv, &src, kv_len[b], d, attn + b * Hq * d + j * d);

@@ -38,7 +38,7 @@ def test_decode_qkv_stage_and_append(B, L, hidden, Hq, Hkv, d, qk):
     # ragged positions: sequence b holds L - b*5 tokens (at least 0)
     cl = torch.tensor([max(0, L - 5 * b) for b in range(B)], dtype=torch.int32)
     kc, vc = dev(t["k_cache"]), dev(t["v_cache"])
-    q = torch.empty((B, Hq, d), dtype=torch.bfloat16, device=DEV)
+    q = torch.empty((B, Hq, d), dtype=torch.float16, device=DEV)  # q of the new tokens is binary16
     gq.gqa_decode_qkv(dev(t["x"]), dev(t["Wqkv"]), dev(t["q_norm_w"]), dev(t["k_norm_w"]), cfg.rope_theta,
                       cfg.eps, B, hidden, Hq, Hkv, d, kc, vc, dev(cl), cfg.lmax, q)
     torch.cuda.synchronize()
@@ -66,7 +66,7 @@ def test_decode_qkv_stage_and_append(B, L, hidden, Hq, Hkv, d, qk):
 ])
 def test_decode_attention_stage(B, Hq, Hkv, d, Lmax, lens):
     g = torch.Generator().manual_seed(500 + Lmax)
-    q = bf16_randn((B, Hq, d), g, 1.5)
+    q = (torch.randn((B, Hq, d), generator=g) * 1.5).to(torch.float16)
     kc = bf16_randn((B, Hkv, Lmax, d), g)
     vc = bf16_randn((B, Hkv, Lmax, d), g)
     kl = torch.tensor(lens, dtype=torch.int32)

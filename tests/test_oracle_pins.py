@@ -469,6 +469,24 @@ def test_decode_attention_stage_matches_prefill_rows():
         np.testing.assert_allclose(got[b], full[b, lens[b] - 1], rtol=1e-13, atol=1e-14)
 
 
+def test_decode_attention_f16_query_equals_library_sdpa():
+    """Decode attention with a binary16 query over bf16 caches equals torch's
+    SDPA (float64) of the widened values over each sequence's prefix."""
+    rng = np.random.default_rng(18)
+    B, Hq, Hkv, d, Lmax = 3, 8, 2, 32, 40
+    q = torch.from_numpy(rng.standard_normal((B, Hq, d)) * 1.5).half()
+    kc = bf16(rng.standard_normal((B, Hkv, Lmax, d)))
+    vc = bf16(rng.standard_normal((B, Hkv, Lmax, d)))
+    lens = [40, 1, 17]
+    got = oracle.decode_attention_stage(q, kc, vc, lens, B, Hq, Hkv, d, Lmax, threads=T)
+    for b in range(B):
+        L = lens[b]
+        k = f64(kc[b, :, :L]).repeat_interleave(Hq // Hkv, 0)
+        v = f64(vc[b, :, :L]).repeat_interleave(Hq // Hkv, 0)
+        ref = F.scaled_dot_product_attention(q[b].double()[:, None], k, v)[:, 0].reshape(-1).numpy()
+        np.testing.assert_allclose(got[b], ref, rtol=1e-11, atol=1e-12)
+
+
 def test_oracle_rejects_bad_arguments():
     with pytest.raises(RuntimeError):
         oracle.rope_rows(np.zeros((1, 3)), [0.0], 1e4)     # odd head_dim

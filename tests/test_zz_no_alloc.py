@@ -41,7 +41,7 @@ def _noalloc_via_cabi(q, kc, vc, kl, B, Hq, Hkv, d, Lmax):
 def test_noalloc_matches_workspace_entry_point_twice(B, Hq, Hkv, d, Lmax):
     g = torch.Generator(device="cuda").manual_seed(900 + B)
     for call in range(2):
-        q = (torch.randn((B, Hq, d), generator=g, device="cuda") * 1.5).to(torch.bfloat16)
+        q = (torch.randn((B, Hq, d), generator=g, device="cuda") * 1.5).to(torch.float16)
         kc = torch.randn((B, Hkv, Lmax, d), generator=g, device="cuda").to(torch.bfloat16)
         vc = torch.randn((B, Hkv, Lmax, d), generator=g, device="cuda").to(torch.bfloat16)
         # ragged lengths that differ between the two calls

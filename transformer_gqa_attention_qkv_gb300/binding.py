@@ -187,7 +187,7 @@ def gqa_decode_qkv(x, Wqkv, q_norm_w, k_norm_w, rope_theta, eps, B, hidden, Hq, 
                    k_cache, v_cache, cache_len, Lmax, q_out, stream=None):
     _check(lib().gqa_decode_qkv(_bf16(x), _bf16(Wqkv), _bf16(q_norm_w), _bf16(k_norm_w), rope_theta, eps,
                                 B, hidden, Hq, Hkv, head_dim, _bf16(k_cache), _bf16(v_cache),
-                                _i32(cache_len), Lmax, _bf16(q_out), _stream(stream)))
+                                _i32(cache_len), Lmax, _f16(q_out), _stream(stream)))
 
 
 def gqa_decode_attention_workspace_size(B, Hq, Hkv, head_dim, Lmax) -> int:
@@ -196,7 +196,7 @@ def gqa_decode_attention_workspace_size(B, Hq, Hkv, head_dim, Lmax) -> int:
 
 def gqa_decode_attention(q, k_cache, v_cache, kv_len, B, Hq, Hkv, head_dim, Lmax, attn_out, workspace,
                          stream=None):
-    _check(lib().gqa_decode_attention(_bf16(q), _bf16(k_cache), _bf16(v_cache), _i32(kv_len), B, Hq, Hkv,
+    _check(lib().gqa_decode_attention(_f16(q), _bf16(k_cache), _bf16(v_cache), _i32(kv_len), B, Hq, Hkv,
                                       head_dim, Lmax, _bf16(attn_out), _ptr(workspace),
                                       workspace.numel() * workspace.element_size(), _stream(stream)))
 
@@ -206,7 +206,7 @@ def gqa_decode_attention_noalloc(q, k_cache, v_cache, kv_len, B, Hq, Hkv, head_d
     """Decode attention without a workspace, for callers that cannot allocate
     device memory: the split partials live in a fixed array inside the
     library.  Calls that overlap on the GPU race on that array."""
-    _check(lib().gqa_decode_attention_noalloc(_bf16(q), _bf16(k_cache), _bf16(v_cache), _i32(kv_len), B, Hq,
+    _check(lib().gqa_decode_attention_noalloc(_f16(q), _bf16(k_cache), _bf16(v_cache), _i32(kv_len), B, Hq,
                                               Hkv, head_dim, Lmax, _bf16(attn_out), _stream(stream)))
 
 

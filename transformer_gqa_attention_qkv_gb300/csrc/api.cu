@@ -210,7 +210,7 @@ static FwdLayout fwd_layout(int B, int S, int Hq, int Hkv, int d)
 
 static int run_qkv(DeviceState &st, const gqa_bf16 *x, const gqa_bf16 *Wqkv, const gqa_bf16 *qn, const gqa_bf16 *kn,
                    float theta, float eps, int B, int S, int hidden, int Hq, int Hkv, int d, const int *pos_dev,
-                   int q_seq, int kv_seq, int rope_rows, int f16_out, gqa_bf16 *q_out, gqa_bf16 *k_out,
+                   int q_seq, int kv_seq, int rope_rows, int kv_f16, gqa_bf16 *q_out, gqa_bf16 *k_out,
                    gqa_bf16 *v_out, cudaStream_t stream)
 {
     const float2 *rope = nullptr;
@@ -234,7 +234,8 @@ static int run_qkv(DeviceState &st, const gqa_bf16 *x, const gqa_bf16 *Wqkv, con
     e.eps = eps;
     e.rope = rope;
     e.rope_rows = rope_rows;
-    e.f16_out = f16_out;
+    e.q_f16 = 1;         // Q is always binary16 (bounded by QK-norm; fp32 math reads it)
+    e.kv_f16 = kv_f16;   // prefill: binary16 workspace; decode: the bf16 cache
     e.q_out = q_out;
     e.k_out = k_out;
     e.v_out = v_out;
@@ -473,7 +474,7 @@ static int check_decode(int B, int hidden, int Hq, int Hkv, int d, int Lmax, con
 
 int gqa_decode_qkv(const gqa_bf16 *x, const gqa_bf16 *Wqkv, const gqa_bf16 *q_norm_w, const gqa_bf16 *k_norm_w,
                    float rope_theta, float eps, int B, int hidden, int Hq, int Hkv, int head_dim, gqa_bf16 *k_cache,
-                   gqa_bf16 *v_cache, const int *cache_len, int Lmax, gqa_bf16 *q_out, void *stream)
+                   gqa_bf16 *v_cache, const int *cache_len, int Lmax, gqa_f16 *q_out, void *stream)
 {
     g_launches = 0;
     int rc = check_decode(B, hidden, Hq, Hkv, head_dim, Lmax, q_norm_w, k_norm_w);
@@ -488,7 +489,7 @@ int gqa_decode_qkv(const gqa_bf16 *x, const gqa_bf16 *Wqkv, const gqa_bf16 *q_no
                    Lmax, Lmax, 0, q_out, k_cache, v_cache, (cudaStream_t)stream);
 }
 
-int gqa_decode_attention(const gqa_bf16 *q, const gqa_bf16 *k_cache, const gqa_bf16 *v_cache, const int *kv_len,
+int gqa_decode_attention(const gqa_f16 *q, const gqa_bf16 *k_cache, const gqa_bf16 *v_cache, const int *kv_len,
                          int B, int Hq, int Hkv, int head_dim, int Lmax, gqa_bf16 *attn_out, void *workspace,
                          size_t workspace_bytes, void *stream)
 {
@@ -535,7 +536,8 @@ int gqa_attn_decode(const gqa_bf16 *x, const gqa_bf16 *Wqkv, const gqa_bf16 *Wo,
                     workspace ? workspace_bytes : (size_t)0);
     if (((uintptr_t)workspace & 255u) != 0) return fail(GQA_ERR_ARG, "workspace must be 256-byte aligned");
     uint8_t *ws = (uint8_t *)workspace;
-    gqa_bf16 *q = (gqa_bf16 *)ws, *attn = (gqa_bf16 *)(ws + off_attn);
+    gqa_f16 *q = (gqa_f16 *)ws;  // binary16 q of the new tokens
+    gqa_bf16 *attn = (gqa_bf16 *)(ws + off_attn);
     float *part = (float *)(ws + off_part);
     cudaStream_t s = (cudaStream_t)stream;
     if ((rc = run_qkv(*st, x, Wqkv, q_norm_w, k_norm_w, rope_theta, eps, B, 1, hidden, Hq, Hkv, head_dim, cache_len, 1,

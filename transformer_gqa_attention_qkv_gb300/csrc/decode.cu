@@ -71,9 +71,10 @@ __global__ void __launch_bounds__(kWarps * 32)
         const uint4 v = *reinterpret_cast<const uint4 *>(P.q + ((size_t)(b * P.Hq + g * G + h) * D + dl * 8));
         const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            q[h][2 * k] = bf16lo(w[k]) * scale_log2;
-            q[h][2 * k + 1] = bf16hi(w[k]) * scale_log2;
+        for (int k = 0; k < 4; ++k) {  // q is binary16
+            const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&w[k]));
+            q[h][2 * k] = f.x * scale_log2;
+            q[h][2 * k + 1] = f.y * scale_log2;
         }
     }
     float m[G], l[G], o[G][8];

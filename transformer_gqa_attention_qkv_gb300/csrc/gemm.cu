@@ -109,7 +109,6 @@ DEVI void epilogue_qkv(const GemmParams &P, uint32_t tcol, int m, int n0, bool r
         }
     }
     const bool has_norm = e.q_norm_w != nullptr;
-    const bool f16 = e.f16_out != 0;
     bool clamped = false;
 #pragma unroll 1
     for (int h = 0; h < BN / D; ++h) {
@@ -132,6 +131,7 @@ DEVI void epilogue_qkv(const GemmParams &P, uint32_t tcol, int m, int n0, bool r
             dst = e.q_out + ((size_t)(b * e.Hq + head) * e.q_seq + q_slot) * D;
         else
             dst = (kind == 1 ? e.k_out : e.v_out) + ((size_t)(b * e.Hkv + head) * e.kv_seq + kv_slot) * D;
+        const bool f16 = (kind == 0 ? e.q_f16 : e.kv_f16) != 0;
 
         if (kind == 2) {  // V: no norm, no rotation
 #pragma unroll 1

@@ -26,7 +26,8 @@ struct QkvEpilogue {
     float eps;
     const float2 *rope;    // [rope_rows][d/2] (cos, sin)
     int rope_rows;
-    int f16_out;           // 1: Q/K/V stored as binary16 (clamped, flagged); 0: bf16
+    int q_f16;             // 1: Q stored as binary16 (clamped, flagged); 0: bf16
+    int kv_f16;            // 1: K and V stored as binary16 (clamped, flagged); 0: bf16
     uint16_t *q_out, *k_out, *v_out;
 };
 
@@ -60,7 +61,7 @@ cudaError_t launch_attention(const AttentionProblem &p, unsigned *err, int num_s
 
 // -------------------------------------------------------- decode attention
 struct DecodeAttentionProblem {
-    const uint16_t *q;        // [B, Hq, d]
+    const uint16_t *q;        // [B, Hq, d] binary16
     const uint16_t *k_cache;  // [B, Hkv, Lmax, d]
     const uint16_t *v_cache;
     const int *len;           // device [B]; keys attended = len[b] + len_bias

@@ -82,7 +82,7 @@ int noalloc_setup(NoAllocDevice **out)
 
 using namespace gqa;
 
-extern "C" int gqa_decode_attention_noalloc(const gqa_bf16 *q, const gqa_bf16 *k_cache, const gqa_bf16 *v_cache,
+extern "C" int gqa_decode_attention_noalloc(const gqa_f16 *q, const gqa_bf16 *k_cache, const gqa_bf16 *v_cache,
                                             const int *kv_len, int B, int Hq, int Hkv, int head_dim, int Lmax,
                                             gqa_bf16 *attn_out, void *stream)
 {
