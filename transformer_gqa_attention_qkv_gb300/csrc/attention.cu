@@ -5,23 +5,32 @@
 // ([T07] §4 step 6 in fp32; [NeoX] "Scaling and RoPE" scale head_dim^-0.5;
 //  [NeoX] "Attention output flattening": output width Hq*d).
 //
-// One CTA handles one (sequence b, KV head g, block of R = 128/G positions)
-// work item.  The G query heads of the group are packed into the MMA's M
-// dimension: row r of the 128-row tile is head g*G + r/R at position
-// t0 + r%R.  Each K/V tile (128 keys) is therefore brought into shared memory
-// once by TMA and used by every query head of the group in a single MMA.
+// Work item: (sequence b, KV head g, block of 2R positions), R = 128/G.  The G
+// query heads of the group are packed into the MMA's M dimension: row r of a
+// 128-row tile is head g*G + r/R at position t0 + r%R.  A CTA owns two such
+// tiles (positions t0.., t0+R..); every K/V tile of 128 keys is brought into
+// shared memory once by TMA and used by all G heads of both tiles.
 //
-//   warp 0      TMA: Q tile once, then K and V tiles into a 2-deep ring
-//   warp 1      MMA: S = Q K^T (TMEM), then O += P V (TMEM)
-//   warps 2..5  softmax: one thread per row (tcgen05.ld 32x32b gives a thread
-//               a whole row, so row max and row sum need no shuffles); online
-//               softmax in fp32 with exp2; P to shared memory as binary16;
-//               O rescaled in TMEM only when the running max grows by more
-//               than 2^8; final O / l written as bf16.
+//   warp 0      TMA: both Q tiles once, then K and V tiles into a ring
+//   warp 1      MMA: per key tile j, for tile i = 0, 1:
+//                 O_i += P_i(j) V(j)  (P read from TMEM),  S_i(j+1) = Q_i K(j+1)^T
+//   warps 2..5  softmax of tile 0, warps 6..9 softmax of tile 1 (one thread per
+//               row; tcgen05.ld 32x32b gives a thread a whole row, so the row
+//               max and sum need no shuffles).  While one warpgroup runs its
+//               softmax, the tensor core works on the other tile.
+//
+// TMEM (512 columns): tile i holds S_i in columns [256i, 256i+128) and O_i in
+// [256i+128, 256i+128+d).  P_i (binary16, two per column) is written over the
+// first 64 columns of S_i and consumed from there by the PV MMA; MMAs issued by
+// one thread run in order, so S_i(j+1) overwrites P_i(j) only after PV_i(j).
+//
+// Online softmax in fp32 with exp2 and the scale folded into log2 units.  O is
+// rescaled in TMEM only when a row's running max grows by more than 2^8; P
+// stays <= 2^8 in between, and the final O / l is exact either way.
 //
 // Q, K and V arrive as binary16: with QK-norm their rows are bounded by
 // sqrt(d) * max|w|, and binary16 keeps 3 more mantissa bits than bf16, which
-// halves the rounding error that storage adds to the scores and outputs.
+// cuts the rounding error that storage adds to scores and outputs.
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -31,7 +40,8 @@ namespace {
 
 constexpr int kRows = 128;      // MMA M: packed query rows per tile
 constexpr int kKeys = 128;      // keys per K/V tile
-constexpr int kThreads = 192;
+constexpr int kTiles = 2;       // query tiles per CTA
+constexpr int kThreads = 320;   // 2 + 2 x 4 warps
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O only past a 256x growth
 
 struct AttnParams {
@@ -44,13 +54,14 @@ struct AttnParams {
 template <int D>
 struct ASmem {
     static constexpr int CHUNK = kRows * 128;             // 128 rows x 64 16-bit = 16 KB
-    static constexpr int NCH = D / 64;                    // d chunks per row
+    static constexpr int NCH = D / 64;                    // 64-wide d chunks
+    static constexpr int STAGES = D == 128 ? 2 : 3;       // K/V ring depth (also keeps 1 CTA per SM)
     static constexpr int Q = 0;
-    static constexpr int K = Q + NCH * CHUNK;             // 2 stages
-    static constexpr int V = K + 2 * NCH * CHUNK;         // 2 stages
-    static constexpr int P = V + 2 * NCH * CHUNK;         // 2 key chunks
-    static constexpr int BARS = P + 2 * CHUNK;
-    static constexpr int NBARS = 1 + 2 + 2 + 2 + 3 + 1;   // q, k[2], v[2], kv_empty[2], s, p, o, drain
+    static constexpr int K = Q + kTiles * NCH * CHUNK;
+    static constexpr int V = K + STAGES * NCH * CHUNK;
+    static constexpr int BARS = V + STAGES * NCH * CHUNK;
+    // q_full, k_full[S], v_full[S], kv_empty[S], s_full[2], p_full[2], o_done[2], drain
+    static constexpr int NBARS = 1 + 3 * STAGES + 2 + 2 + 2 + 1;
     static constexpr int TMEM_SLOT = BARS + NBARS * 8;
     static constexpr int TOTAL = TMEM_SLOT + 16;
     static constexpr int ALLOC = TOTAL + 1024;
@@ -62,17 +73,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const __grid_constant__ CUtensorMap tmV, const AttnParams P)
 {
     using L = ASmem<D>;
+    constexpr int ST = L::STAGES;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::BARS);
     uint64_t *q_full = bars;
     uint64_t *k_full = bars + 1;
-    uint64_t *v_full = bars + 3;
-    uint64_t *kv_empty = bars + 5;
-    uint64_t *s_full = bars + 7;
-    uint64_t *p_full = bars + 8;
-    uint64_t *o_done = bars + 9;
-    uint64_t *drain = bars + 10;
+    uint64_t *v_full = k_full + ST;
+    uint64_t *kv_empty = v_full + ST;
+    uint64_t *s_full = kv_empty + ST;
+    uint64_t *p_full = s_full + 2;
+    uint64_t *o_done = p_full + 2;
+    uint64_t *drain = o_done + 2;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::TMEM_SLOT);
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -83,13 +95,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int bh = item % (P.B * P.Hkv);
     const int qblk = P.n_qblk - 1 - item / (P.B * P.Hkv);
     const int b = bh / P.Hkv, g = bh % P.Hkv;
-    const int t0 = qblk * P.R;
-    const int t_last = min(t0 + P.R, P.S) - 1;
+    const int t0 = qblk * kTiles * P.R;
+    const int t_last = min(t0 + kTiles * P.R, P.S) - 1;
     const int n_kv = P.causal ? (t_last / kKeys + 1) : (P.S + kKeys - 1) / kKeys;
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < L::NBARS; ++i) mbar_init(bars + i, 1);
-        mbar_init(p_full, 4);
+        mbar_init(p_full, 4);  // one arrival per softmax warp
+        mbar_init(p_full + 1, 4);
         fence_mbar_init();
     }
     if (warp == 0 && lane == 0) {
@@ -97,23 +110,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_prefetch_desc(&tmK);
         tma_prefetch_desc(&tmV);
     }
-    if (warp == 1) tmem_alloc(tmem_slot, 256);
+    if (warp == 1) tmem_alloc(tmem_slot, 512);
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    const uint32_t tS = tmem;        // S: columns [0, 128)
-    const uint32_t tO = tmem + 128;  // O: columns [128, 128 + D)
 
     if (warp == 0) {
         if (lane == 0) {
-            const uint32_t q_bytes = L::NCH * 64 * 2 * P.R * P.G;
+            const uint32_t q_bytes = kTiles * L::NCH * 64 * 2 * P.R * P.G;
             mbar_arrive_expect_tx(q_full, q_bytes);
-            for (int c = 0; c < L::NCH; ++c)
-                tma_load_3d(smem + L::Q + c * L::CHUNK, &tmQ, c * 64, t0, b * P.Hq + g * P.G, q_full);
+            for (int i = 0; i < kTiles; ++i)
+                for (int c = 0; c < L::NCH; ++c)
+                    tma_load_3d(smem + L::Q + (i * L::NCH + c) * L::CHUNK, &tmQ, c * 64, t0 + i * P.R,
+                                b * P.Hq + g * P.G, q_full);
             int j = 0;
             for (; j < n_kv; ++j) {
-                const int s = j & 1;
-                if (!mbar_wait(kv_empty + s, ((j >> 1) & 1) ^ 1, err)) break;
+                const int s = j % ST;
+                if (!mbar_wait(kv_empty + s, ((j / ST) & 1) ^ 1, err)) break;
                 mbar_arrive_expect_tx(k_full + s, L::NCH * L::CHUNK);
                 for (int c = 0; c < L::NCH; ++c)
                     tma_load_3d(smem + L::K + (s * L::NCH + c) * L::CHUNK, &tmK, c * 64, j * kKeys, b * P.Hkv + g,
@@ -123,136 +136,150 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tma_load_3d(smem + L::V + (s * L::NCH + c) * L::CHUNK, &tmV, c * 64, j * kKeys, b * P.Hkv + g,
                                 v_full + s);
             }
+            // every issued copy has landed before the CTA may exit
             mbar_wait(q_full, 0, err);
-            for (int i = max(0, j - 2); i < j; ++i) {
-                mbar_wait(k_full + (i & 1), (i >> 1) & 1, err);
-                mbar_wait(v_full + (i & 1), (i >> 1) & 1, err);
+            for (int i = max(0, j - ST); i < j; ++i) {
+                mbar_wait(k_full + i % ST, (i / ST) & 1, err);
+                mbar_wait(v_full + i % ST, (i / ST) & 1, err);
             }
         }
     } else if (warp == 1) {
         if (lane == 0) {
-            constexpr uint32_t idesc_s = idesc_f16_f32(kRows, kKeys, 0, 0);  // Q, K: binary16, K-major (over d)
-            constexpr uint32_t idesc_o = idesc_f16_f32(kRows, D, 0, 1);      // P K-major, V MN-major (d contiguous)
-            const uint32_t sQ = smem_u32(smem + L::Q);
-            const uint32_t sP = smem_u32(smem + L::P);
-            auto issue_s = [&](int j) {
-                const int s = j & 1;
-                const uint32_t sK = smem_u32(smem + L::K + s * L::NCH * L::CHUNK);
+            constexpr uint32_t idesc_s = idesc_f16_f32(kRows, kKeys, 0, 0);  // Q, K: K-major over d
+            constexpr uint32_t idesc_o = idesc_f16_f32(kRows, D, 0, 1);      // P (TMEM), V MN-major (d contiguous)
+            auto issue_s = [&](int i, int j) {  // S_i = Q_i K(j)^T
+                const uint32_t sQ = smem_u32(smem + L::Q + i * L::NCH * L::CHUNK);
+                const uint32_t sK = smem_u32(smem + L::K + (j % ST) * L::NCH * L::CHUNK);
 #pragma unroll
                 for (int c = 0; c < L::NCH; ++c)
 #pragma unroll
                     for (int k = 0; k < 4; ++k)
-                        umma_f16_ss(tS, sw128_desc(sQ + c * L::CHUNK + 32 * k, 16, 1024),
-                                     sw128_desc(sK + c * L::CHUNK + 32 * k, 16, 1024), idesc_s, (c | k) != 0);
-                umma_commit(s_full);
+                        umma_f16_ss(tmem + 256 * i, sw128_desc(sQ + c * L::CHUNK + 32 * k, 16, 1024),
+                                    sw128_desc(sK + c * L::CHUNK + 32 * k, 16, 1024), idesc_s, (c | k) != 0);
+                umma_commit(s_full + i);
             };
             bool ok = mbar_wait(q_full, 0, err) && mbar_wait(k_full, 0, err);
             if (ok) {
                 tc_fence_after();
-                issue_s(0);
+                issue_s(0, 0);
+                issue_s(1, 0);
             }
             for (int j = 0; ok && j < n_kv; ++j) {
-                const int s = j & 1;
-                if (!mbar_wait(p_full, j & 1, err)) break;
-                tc_fence_after();
-                if (j + 1 < n_kv) {
-                    if (!mbar_wait(k_full + ((j + 1) & 1), ((j + 1) >> 1) & 1, err)) break;
-                    tc_fence_after();
-                    issue_s(j + 1);
-                }
-                if (!mbar_wait(v_full + s, (j >> 1) & 1, err)) break;
-                tc_fence_after();
+                const int s = j % ST;
                 const uint32_t sV = smem_u32(smem + L::V + s * L::NCH * L::CHUNK);
+                for (int i = 0; i < kTiles; ++i) {
+                    if (!mbar_wait(p_full + i, j & 1, err)) {
+                        ok = false;
+                        break;
+                    }
+                    if (i == 0 && !mbar_wait(v_full + s, (j / ST) & 1, err)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t tS = tmem + 256 * i, tO = tS + 128;
 #pragma unroll
-                for (int k = 0; k < kKeys / 16; ++k)
-                    umma_f16_ss(tO, sw128_desc(sP + (k >> 2) * L::CHUNK + 32 * (k & 3), 16, 1024),
-                                 sw128_desc(sV + k * 16 * 128, L::CHUNK, 1024), idesc_o, (j | k) != 0);
-                umma_commit(o_done);
-                umma_commit(kv_empty + s);
+                    for (int k = 0; k < kKeys / 16; ++k)  // 16 keys = 8 packed TMEM columns of P
+                        umma_f16_ts(tO, tS + 8 * k, sw128_desc(sV + k * 16 * 128, L::CHUNK, 1024), idesc_o,
+                                    (j | k) != 0);
+                    if (i == kTiles - 1) umma_commit(kv_empty + s);
+                    if (j + 1 < n_kv) {
+                        if (i == 0) {
+                            if (!mbar_wait(k_full + (j + 1) % ST, ((j + 1) / ST) & 1, err)) {
+                                ok = false;
+                                break;
+                            }
+                            tc_fence_after();
+                        }
+                        issue_s(i, j + 1);
+                    } else {
+                        umma_commit(o_done + i);
+                    }
+                }
             }
             umma_commit(drain);
             mbar_wait(drain, 0, err);
         }
     } else {
-        const int quarter = warp & 3;
-        const int r = quarter * 32 + lane;  // tile row = TMEM lane
+        const int wg = (warp - 2) >> 2;   // which query tile
+        const int quarter = warp & 3;     // TMEM lanes this warp may access
+        const int r = quarter * 32 + lane;
         const int hl = r / P.R, tl = r - hl * P.R;
         const bool in_pack = hl < P.G;
-        const int t = t0 + tl;
+        const int t = t0 + wg * P.R + tl;
         const bool row_ok = in_pack && t < P.S;
-        const int t_vis = in_pack ? t : -1;  // last visible key for a causal row
+        // keys u <= lim are visible to this row
+        const int lim = !in_pack ? -1 : (P.causal ? min(t, P.S - 1) : P.S - 1);
         const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
-        uint8_t *prow = smem + L::P + r * 128;
+        const uint32_t tS = tmem + 256 * wg + lane_off, tO = tS + 128;
+        const float sl = P.scale_log2;
         float m_i = -INFINITY, l_i = 0.0f;
 
         for (int j = 0; j < n_kv; ++j) {
-            if (!mbar_wait(s_full, j & 1, err)) break;
+            if (!mbar_wait(s_full + wg, j & 1, err)) break;
             tc_fence_after();
-            float sv[kKeys];
-#pragma unroll
-            for (int c = 0; c < kKeys; c += 32) {
-                uint32_t rr[32];
-                tmem_ld32(tS + lane_off + c, rr);
-#pragma unroll
-                for (int i = 0; i < 32; ++i) sv[c + i] = __uint_as_float(rr[i]);
-            }
             const int u0 = j * kKeys;
-            const int lim = P.causal ? min(t_vis, P.S - 1) : (in_pack ? P.S - 1 : -1);  // keys u <= lim visible
+            const bool partial = u0 + kKeys - 1 > lim;
+            // pass 1: row max
             float mx = -INFINITY;
-            if (u0 + kKeys - 1 > lim) {
 #pragma unroll
-                for (int c = 0; c < kKeys; ++c)
-                    if (u0 + c > lim) sv[c] = -INFINITY;
+            for (int c = 0; c < 4; ++c) {
+                uint32_t v[32];
+                tmem_ld32(tS + 32 * c, v);
+                if (partial) {
+#pragma unroll
+                    for (int e = 0; e < 32; ++e)
+                        if (u0 + 32 * c + e <= lim) mx = fmaxf(mx, __uint_as_float(v[e]));
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) mx = fmaxf(mx, __uint_as_float(v[e]));
+                }
             }
-#pragma unroll
-            for (int c = 0; c < kKeys; ++c) mx = fmaxf(mx, sv[c]);
-            const float m_cand = fmaxf(m_i, mx * P.scale_log2);
+            const float m_cand = fmaxf(m_i, mx * sl);
             float m_new = m_i, alpha = 1.0f;
             if (m_cand > m_i + kRescaleThreshold) {
                 m_new = m_cand;
                 alpha = ex2(m_i - m_new);  // 0 on the first tile
             }
             const float m_use = (m_new == -INFINITY) ? 0.0f : m_new;
+            // pass 2: p = 2^(s*scale - m), row sum, P as binary16 over the first 64 columns
             float rs = 0.0f;
-            uint32_t pk[kKeys / 2];
 #pragma unroll
-            for (int c = 0; c < kKeys; c += 2) {
-                const float p0 = ex2(fmaf(sv[c], P.scale_log2, -m_use));
-                const float p1 = ex2(fmaf(sv[c + 1], P.scale_log2, -m_use));
-                rs += p0 + p1;
-                pk[c / 2] = pack_f16(p0, p1);  // p <= 2^8: inside the binary16 range
+            for (int c = 0; c < 4; ++c) {
+                uint32_t v[32], pk[16];
+                tmem_ld32(tS + 32 * c, v);
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                    float p0 = ex2(fmaf(__uint_as_float(v[2 * e]), sl, -m_use));
+                    float p1 = ex2(fmaf(__uint_as_float(v[2 * e + 1]), sl, -m_use));
+                    if (partial) {
+                        if (u0 + 32 * c + 2 * e > lim) p0 = 0.0f;
+                        if (u0 + 32 * c + 2 * e + 1 > lim) p1 = 0.0f;
+                    }
+                    rs += p0 + p1;
+                    pk[e] = pack_f16(p0, p1);
+                }
+                tmem_st16_nowait(tS + 16 * c, pk);  // columns already read in this pass
             }
+            tmem_st_wait();
             l_i = l_i * alpha + rs;
             m_i = m_new;
-            // PV(j-1) must be done before P is overwritten and before O is rescaled
-            if (j > 0) {
-                if (!mbar_wait(o_done, (j - 1) & 1, err)) break;
-                tc_fence_after();
-            }
-#pragma unroll
-            for (int kc = 0; kc < 2; ++kc)
-#pragma unroll
-                for (int gi = 0; gi < 8; ++gi) {
-                    const int q16 = kc * 32 + gi * 4;
-                    *reinterpret_cast<uint4 *>(prow + kc * L::CHUNK + ((gi ^ (r & 7)) << 4)) =
-                        make_uint4(pk[q16], pk[q16 + 1], pk[q16 + 2], pk[q16 + 3]);
-                }
+            // O_i(j-1) is complete: S_i(j) was issued after PV_i(j-1)
             if (j > 0 && __any_sync(0xffffffffu, alpha != 1.0f)) {
 #pragma unroll 1
                 for (int c = 0; c < D; c += 32) {
                     uint32_t o[32];
-                    tmem_ld32(tO + lane_off + c, o);
+                    tmem_ld32(tO + c, o);
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-                    tmem_st32(tO + lane_off + c, o);
+                    for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+                    tmem_st32(tO + c, o);
                 }
             }
-            fence_proxy_async_smem();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(p_full);
+            if (lane == 0) mbar_arrive(p_full + wg);
         }
-        if (mbar_wait(o_done, (n_kv - 1) & 1, err)) {
+        if (mbar_wait(o_done + wg, 0, err)) {
             tc_fence_after();
             const float inv_l = (l_i > 0.0f) ? 1.0f / l_i : 0.0f;
             const int head = g * P.G + hl;
@@ -260,7 +287,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll 1
             for (int c = 0; c < D; c += 32) {
                 uint32_t o[32];
-                tmem_ld32(tO + lane_off + c, o);
+                tmem_ld32(tO + c, o);
                 if (row_ok) {
                     uint4 *d4 = reinterpret_cast<uint4 *>(dst + c);
 #pragma unroll
@@ -279,7 +306,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc(tmem, 256);
+        tmem_dealloc(tmem, 512);
     }
 }
 
@@ -307,7 +334,7 @@ cudaError_t run_attn(const AttentionProblem &p, unsigned *err, cudaStream_t stre
     a.Hkv = p.Hkv;
     a.G = G;
     a.R = R;
-    a.n_qblk = (p.S + R - 1) / R;
+    a.n_qblk = (p.S + kTiles * R - 1) / (kTiles * R);
     a.causal = p.causal;
     a.num_items = p.B * p.Hkv * a.n_qblk;
     a.scale_log2 = 1.4426950408889634f / sqrtf((float)D);
