@@ -270,6 +270,37 @@ DEVI void tmem_st32(uint32_t taddr, const uint32_t (&r)[32])
         : "memory");
 }
 
+// ----------------------------------------------------- warp-level MMA (mma.sync)
+
+// Four 8x8 16-bit matrices from shared memory; lane i gives the address of row
+// i%8 of matrix i/8; lane t receives (row t/4, columns 2(t%4), 2(t%4)+1) of
+// each matrix (transposed matrices with .trans).
+DEVI void ldsm_x4(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2, uint32_t &r3)
+{
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr)
+                 : "memory");
+}
+DEVI void ldsm_x4_trans(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2, uint32_t &r3)
+{
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr)
+                 : "memory");
+}
+
+// D = A(16x16, row) * B(16x8, col) + C, bf16 inputs, fp32 accumulators.
+DEVI void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
+                         uint32_t b1)
+{
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
 // ------------------------------------------------------------------- misc
 
 DEVI float bf16lo(uint32_t v) { return __uint_as_float(v << 16); }
