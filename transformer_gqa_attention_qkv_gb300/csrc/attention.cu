@@ -219,22 +219,22 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!mbar_wait(s_full + wg, j & 1, err)) break;
             tc_fence_after();
             const int u0 = j * kKeys;
-            const bool partial = u0 + kKeys - 1 > lim;
-            // pass 1: row max
-            float mx = -INFINITY;
+            // the whole S row in registers (one TMEM load, one wait)
+            uint32_t v[kKeys];
+            tmem_ld128(tS, v);
+            if (u0 + kKeys - 1 > lim) {  // diagonal or ragged tile: mask keys past lim
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                uint32_t v[32];
-                tmem_ld32(tS + 32 * c, v);
-                if (partial) {
-#pragma unroll
-                    for (int e = 0; e < 32; ++e)
-                        if (u0 + 32 * c + e <= lim) mx = fmaxf(mx, __uint_as_float(v[e]));
-                } else {
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) mx = fmaxf(mx, __uint_as_float(v[e]));
-                }
+                for (int e = 0; e < kKeys; ++e)
+                    if (u0 + e > lim) v[e] = __float_as_uint(-INFINITY);
             }
+            // row max: four independent chains of three-input max
+            float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+            for (int e = 0; e < kKeys; e += 8)
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                    mx4[k] = fmax3(mx4[k], __uint_as_float(v[e + 2 * k]), __uint_as_float(v[e + 2 * k + 1]));
+            const float mx = fmaxf(fmax3(mx4[0], mx4[1], mx4[2]), mx4[3]);
             const float m_cand = fmaxf(m_i, mx * sl);
             float m_new = m_i, alpha = 1.0f;
             if (m_cand > m_i + kRescaleThreshold) {
@@ -242,26 +242,26 @@ __global__ void __launch_bounds__(kThreads, 1)
                 alpha = ex2(m_i - m_new);  // 0 on the first tile
             }
             const float m_use = (m_new == -INFINITY) ? 0.0f : m_new;
-            // pass 2: p = 2^(s*scale - m), row sum, P as binary16 over the first 64 columns
-            float rs = 0.0f;
+            // p = 2^(s*scale - m) (masked keys give 2^-inf = 0), row sum, and P as
+            // binary16 over the first 64 columns of S (already read)
+            const float2 sl2 = make_float2(sl, sl), nm2 = make_float2(-m_use, -m_use);
+            float2 rs2[2] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f)};
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
-                uint32_t v[32], pk[16];
-                tmem_ld32(tS + 32 * c, v);
+                uint32_t pk[16];
 #pragma unroll
                 for (int e = 0; e < 16; ++e) {
-                    float p0 = ex2(fmaf(__uint_as_float(v[2 * e]), sl, -m_use));
-                    float p1 = ex2(fmaf(__uint_as_float(v[2 * e + 1]), sl, -m_use));
-                    if (partial) {
-                        if (u0 + 32 * c + 2 * e > lim) p0 = 0.0f;
-                        if (u0 + 32 * c + 2 * e + 1 > lim) p1 = 0.0f;
-                    }
-                    rs += p0 + p1;
-                    pk[e] = pack_f16(p0, p1);
+                    const float2 x = __ffma2_rn(
+                        make_float2(__uint_as_float(v[32 * c + 2 * e]), __uint_as_float(v[32 * c + 2 * e + 1])), sl2,
+                        nm2);
+                    const float2 p = make_float2(ex2(x.x), ex2(x.y));
+                    rs2[e & 1] = __fadd2_rn(rs2[e & 1], p);
+                    pk[e] = pack_f16(p.x, p.y);
                 }
-                tmem_st16_nowait(tS + 16 * c, pk);  // columns already read in this pass
+                tmem_st16_nowait(tS + 16 * c, pk);
             }
             tmem_st_wait();
+            const float rs = (rs2[0].x + rs2[0].y) + (rs2[1].x + rs2[1].y);
             l_i = l_i * alpha + rs;
             m_i = m_new;
             // O_i(j-1) is complete: S_i(j) was issued after PV_i(j-1)

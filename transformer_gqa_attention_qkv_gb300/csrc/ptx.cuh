@@ -242,6 +242,38 @@ DEVI void tmem_ld32(uint32_t taddr, uint32_t (&r)[32])
         : "memory");
 }
 
+// TMEM -> registers, 32 lanes x 32 bits, 128 consecutive columns (a whole
+// 128-wide row per thread) in one instruction, then wait.
+#define GQA_R8(i) "=r"(r[i]), "=r"(r[i + 1]), "=r"(r[i + 2]), "=r"(r[i + 3]), "=r"(r[i + 4]), "=r"(r[i + 5]), \
+                  "=r"(r[i + 6]), "=r"(r[i + 7])
+DEVI void tmem_ld128(uint32_t taddr, uint32_t (&r)[128])
+{
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x128.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,"
+        "%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,"
+        "%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63,"
+        "%64,%65,%66,%67,%68,%69,%70,%71,%72,%73,%74,%75,%76,%77,%78,%79,"
+        "%80,%81,%82,%83,%84,%85,%86,%87,%88,%89,%90,%91,%92,%93,%94,%95,"
+        "%96,%97,%98,%99,%100,%101,%102,%103,%104,%105,%106,%107,%108,%109,%110,%111,"
+        "%112,%113,%114,%115,%116,%117,%118,%119,%120,%121,%122,%123,%124,%125,%126,%127}, [%128];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : GQA_R8(0), GQA_R8(8), GQA_R8(16), GQA_R8(24), GQA_R8(32), GQA_R8(40), GQA_R8(48), GQA_R8(56),
+          GQA_R8(64), GQA_R8(72), GQA_R8(80), GQA_R8(88), GQA_R8(96), GQA_R8(104), GQA_R8(112), GQA_R8(120)
+        : "r"(taddr)
+        : "memory");
+}
+#undef GQA_R8
+
+// max of three floats in one instruction (sm_100+)
+DEVI float fmax3(float a, float b, float c)
+{
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
 // registers -> TMEM, 32 lanes x 32 bits, 16 consecutive columns (no wait).
 DEVI void tmem_st16_nowait(uint32_t taddr, const uint32_t (&r)[16])
 {
