@@ -30,6 +30,7 @@ enum { EPI_QKV = 0, EPI_RESIDUAL = 1 };
 struct GemmParams {
     int M, N, K;
     int num_m, num_n, num_k, num_tiles;
+    int group_m;  // M-blocks per raster group
     unsigned *err;
     QkvEpilogue qkv;
     ResidualEpilogue res;
@@ -47,11 +48,13 @@ struct Smem {
     static constexpr int ALLOC = TOTAL + 1024;               // slack for 1024-byte alignment
 };
 
-// Grouped rasterisation: walk 8 M-blocks per N-block so that concurrently
-// running CTAs share A rows and B rows in L2.
-DEVI void tile_coords(int tile, int num_m, int num_n, int &mb, int &nb)
+// Grouped rasterisation: walk GM M-blocks per N-block so that concurrently
+// running CTAs share A rows and B rows in L2.  The A panels of a group stay in
+// L2 while the group sweeps all N-blocks, and each B panel is read from DRAM
+// once per group (GM = 32 for the QKV projection, 16 for o_proj, whose A
+// panels are longer; both measured best at the Qwen3-32B shape).
+DEVI void tile_coords(int tile, int num_m, int num_n, int GM, int &mb, int &nb)
 {
-    constexpr int GM = 8;
     const int per_group = GM * num_n;
     const int grp = tile / per_group;
     const int first = grp * GM;
@@ -275,7 +278,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool ok = true;
             for (int tile = blockIdx.x; ok && tile < P.num_tiles; tile += gridDim.x) {
                 int mb, nb;
-                tile_coords(tile, P.num_m, P.num_n, mb, nb);
+                tile_coords(tile, P.num_m, P.num_n, P.group_m, mb, nb);
                 for (int kb = 0; kb < P.num_k; ++kb, ++it) {
                     const int s = it % STAGES;
                     const uint32_t ph = (it / STAGES) & 1;
@@ -328,7 +331,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         int use = 0;
         for (int tile = blockIdx.x; tile < P.num_tiles; tile += gridDim.x, ++use) {
             int mb, nb;
-            tile_coords(tile, P.num_m, P.num_n, mb, nb);
+            tile_coords(tile, P.num_m, P.num_n, P.group_m, mb, nb);
             const int acc = use & 1;
             if (!mbar_wait(tfull + acc, (use >> 1) & 1, err)) break;
             tc_fence_after();
@@ -380,6 +383,7 @@ GemmParams make_params(const GemmProblem &p, int BN, unsigned *err)
     g.num_k = (p.K + BK - 1) / BK;
     g.num_tiles = g.num_m * g.num_n;
     g.err = err;
+    g.group_m = 32;
     return g;
 }
 
@@ -424,6 +428,7 @@ cudaError_t launch_gemm_residual(const GemmProblem &p, const ResidualEpilogue &e
     }
     GemmParams g = make_params(p, 256, err);
     g.res = e;
+    g.group_m = 16;  // o_proj's A panels are twice as long (K = Hq*d): half the group
     return run<256, 4, EPI_RESIDUAL, 0>(p, g, num_sms, stream);
 }
 
