@@ -32,6 +32,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "attn-layer fwd TFLOP/s & % bf16 peak (prefill); decode GB/s & % HBM peak"
+CSRC = "transformer_gqa_attention_qkv_gb300/csrc/"
 L2_BYTES = 129 * 1024 * 1024
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
@@ -287,9 +288,9 @@ def run_ours(args, world, rank, local):
     kern = {s: statistics.mean(v_) for s, v_ in stage_ms.items()}
     dom = max(("qkv", "attn", "oproj"), key=lambda s: kern[s])
     peak_tf = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
-    dom_src = {"attn": ["transformer_gqa_attention_qkv_gb300/csrc/attention.cu"],
-               "qkv": ["transformer_gqa_attention_qkv_gb300/csrc/gemm.cu"],
-               "oproj": ["transformer_gqa_attention_qkv_gb300/csrc/gemm.cu"]}[dom]
+    dom_src = {"attn": [CSRC + "attention.cu", CSRC + "ptx.cuh"],
+               "qkv": [CSRC + "gemm.cu", CSRC + "ptx.cuh"],
+               "oproj": [CSRC + "gemm.cu", CSRC + "ptx.cuh"]}[dom]
     achieved = fl[dom] / (kern[dom] * 1e-3) / 1e12
     roofline = {"bound": "tensor", "kernel": dom, "achieved": round(achieved, 1), "peak": peak_tf,
                 "unit": "TFLOP/s", "frac": round(achieved / peak_tf, 4),
@@ -386,7 +387,7 @@ def run_ours(args, world, rank, local):
                            "peak": hbm, "unit": "GB/s", "frac": round(dec_ach / hbm, 4),
                            "peak_source": f"{peak_src} copy bandwidth",
                            "traffic": recorded_traffic("decode_attention_" + dc.name,
-                                                       ["transformer_gqa_attention_qkv_gb300/csrc/decode.cu"]),
+                                                       [CSRC + "decode.cu", CSRC + "ptx.cuh"]),
                            "kernel_ms": round(ams_, 4)}}
     del dt_, dout, dws
 
@@ -509,7 +510,7 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="qwen3_32b")
-    ap.add_argument("--cpu-tokens", type=int, default=512, help="tokens of the CPU-baseline sample")
+    ap.add_argument("--cpu-tokens", type=int, default=2048, help="tokens of the CPU-baseline sample")
     ap.add_argument("--ref-tokens", type=int, default=256, help="tokens per reference-arm step")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--stage", choices=["qkv", "attn", "oproj", "decode_attn"], default=None,
