@@ -80,6 +80,10 @@ def _load():
     lib.oracle_decode_attention_stage.restype = _I
     lib.oracle_decode_attention_stage.argtypes = [_u16p, _I, _u16p, _u16p, _i32p,
                                                   _L, _L, _L, _L, _L, _f64p, _I]
+    lib.oracle_prefill_cached.restype = _I
+    lib.oracle_prefill_cached.argtypes = [_u16p, _u16p, _u16p, _u16p, _u16p, _D, _D,
+                                          _L, _L, _L, _L, _L, _L, _I, _u16p, _u16p, _i32p, _L,
+                                          _f64p, _f64p, _f64p, _f64p, _I]
     lib.oracle_decode.restype = _I
     lib.oracle_decode.argtypes = [_u16p, _u16p, _u16p, _u16p, _u16p, _D, _D,
                                   _L, _L, _L, _L, _L, _u16p, _u16p, _i32p, _L,
@@ -265,6 +269,23 @@ def decode_attention_stage(q, k_cache, v_cache, kv_len, B, Hq, Hkv, d, Lmax, thr
                                                  _pf(out), threads or default_threads()),
            "decode_attention_stage")
     return out
+
+
+def prefill_cached(x, Wqkv, Wo, q_norm_w, k_norm_w, rope_theta, eps, B, S, hidden, Hq, Hkv, d,
+                   k_cache, v_cache, p0, Lmax, causal=True, threads=None):
+    """S new tokens per sequence at positions p0[b].. after p0[b] cached ones.
+    Returns dict out [B*S, hidden], k/v [B,Hkv,S,d] (the new tokens'), attn
+    [B*S, Hq*d]; the caches are read, not modified."""
+    out = np.empty((B * S, hidden)); kn_ = np.empty((B, Hkv, S, d)); vn_ = np.empty((B, Hkv, S, d))
+    a = np.empty((B * S, Hq * d))
+    p = np.ascontiguousarray(np.asarray(p0, dtype=np.int32))
+    xb, wb, ob, qn, kn = _bits(x), _bits(Wqkv), _bits(Wo), _bits(q_norm_w), _bits(k_norm_w)
+    kb, vb = _bits(k_cache), _bits(v_cache)
+    _check(_load().oracle_prefill_cached(_p16(xb), _p16(wb), _p16(ob), _p16(qn), _p16(kn), rope_theta, eps,
+                                         B, S, hidden, Hq, Hkv, d, int(causal), _p16(kb), _p16(vb),
+                                         p.ctypes.data_as(_i32p), Lmax, _pf(out), _pf(kn_), _pf(vn_), _pf(a),
+                                         threads or default_threads()), "prefill_cached")
+    return {"out": out, "k": kn_, "v": vn_, "attn": a}
 
 
 def decode(x, Wqkv, Wo, q_norm_w, k_norm_w, rope_theta, eps, B, hidden, Hq, Hkv, d,

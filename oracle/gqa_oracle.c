@@ -568,3 +568,93 @@ int oracle_decode(const uint16_t *x, const uint16_t *Wqkv, const uint16_t *Wo,
     free(arows);
     return err;
 }
+
+/* ------------------------------------------------------------------------ */
+/* Prefill into a KV cache: S new tokens per sequence after p0[b] cached.     */
+/* ------------------------------------------------------------------------ */
+
+/* The layer for S new tokens of each sequence b at positions p0[b] .. p0[b]+S-1
+ * ([T07] §4: RoPE at the position offsets, step 5 the cache returns the whole
+ * history; [Part]: position encodings and masks use the same global token
+ * positions).  Keys and values [0, p0[b]) come from the bf16 caches
+ * [B, Hkv, Lmax, d] (not modified here); the new tokens' keys and values are
+ * computed in double.  Query t attends to keys u <= p0[b] + t (causal) or to
+ * all p0[b] + S keys.  x [B, S, hidden]; out [B, S, hidden].  Optional:
+ * k_new/v_new [B, Hkv, S, d] and attn [B, S, Hq*d].  With p0 = 0 this is the
+ * plain prefill; with S = 1 it is the decode step. */
+int oracle_prefill_cached(const uint16_t *x, const uint16_t *Wqkv, const uint16_t *Wo,
+                          const uint16_t *q_norm_w, const uint16_t *k_norm_w,
+                          double rope_theta, double eps,
+                          long B, long S, long hidden, long Hq, long Hkv, long d, int causal,
+                          const uint16_t *k_cache, const uint16_t *v_cache, const int *p0,
+                          long Lmax, double *out, double *k_new, double *v_new, double *attn_out,
+                          int nthreads)
+{
+    if (!x || !Wqkv || !Wo || !k_cache || !v_cache || !p0 || !out) return ORACLE_EARG;
+    if (B <= 0 || S <= 0 || hidden <= 0 || Hq <= 0 || Hkv <= 0 || d <= 0 || (d & 1) || d > 1024) return ORACLE_EARG;
+    if (Hq % Hkv) return ORACLE_EARG;
+    if ((q_norm_w == NULL) != (k_norm_w == NULL)) return ORACLE_EARG;
+    for (long b = 0; b < B; ++b)
+        if (p0[b] < 0 || p0[b] + S > Lmax) return ORACLE_EARG;
+    long NQ = Hq * d, NKV = Hkv * d, N = NQ + 2 * NKV, G = Hq / Hkv;
+    int err = ORACLE_OK;
+    set_threads(nthreads);
+    double *rows = (double *)malloc((size_t)(B * S * N) * sizeof(double));
+    double *Kn = (double *)malloc((size_t)(B * Hkv * S * d) * sizeof(double));
+    double *Vn = (double *)malloc((size_t)(B * Hkv * S * d) * sizeof(double));
+    double *arows = (double *)malloc((size_t)(B * S * NQ) * sizeof(double));
+    if (!rows || !Kn || !Vn || !arows) { err = ORACLE_ENOMEM; goto done; }
+
+    /* steps 1-3 for every new token, at its global position */
+#pragma omp parallel for schedule(dynamic, 1)
+    for (long m = 0; m < B * S; ++m) {
+        long b = m / S, t = m % S;
+        double pos = (double)(p0[b] + t);
+        double *row = rows + m * N;
+        linear_row(x + m * hidden, Wqkv, 0, N, hidden, row);
+        for (long j = 0; j < Hq; ++j) {
+            if (q_norm_w) rmsnorm_head(row + j * d, d, q_norm_w, eps);
+            rope_head(row + j * d, d, pos, rope_theta);
+        }
+        for (long g = 0; g < Hkv; ++g) {
+            double *k = row + NQ + g * d;
+            if (k_norm_w) rmsnorm_head(k, d, k_norm_w, eps);
+            rope_head(k, d, pos, rope_theta);
+            memcpy(Kn + ((b * Hkv + g) * S + t) * d, k, (size_t)d * sizeof(double));
+            memcpy(Vn + ((b * Hkv + g) * S + t) * d, row + NQ + NKV + g * d, (size_t)d * sizeof(double));
+        }
+    }
+
+    /* step 6: cached keys [0, p0) then the new ones */
+#pragma omp parallel for collapse(2) schedule(dynamic, 1)
+    for (long m = 0; m < B * S; ++m) {
+        for (long j = 0; j < Hq; ++j) {
+            long b = m / S, t = m % S, g = j / G;
+            kv_src src = {k_cache + (b * Hkv + g) * Lmax * d, v_cache + (b * Hkv + g) * Lmax * d,
+                          Kn + (b * Hkv + g) * S * d, Vn + (b * Hkv + g) * S * d, p0[b], 0};
+            long n_vis = causal ? p0[b] + t + 1 : p0[b] + S;
+            int e = attend_row(rows + m * N + j * d, &src, n_vis, d, arows + m * NQ + j * d);
+            if (e) err = e;
+        }
+    }
+
+    /* step 7: o_proj and the residual */
+#pragma omp parallel for schedule(dynamic, 1)
+    for (long m = 0; m < B * S; ++m) {
+        for (long n = 0; n < hidden; ++n) {
+            const uint16_t *w = Wo + n * NQ;
+            double s = 0.0;
+            for (long k = 0; k < NQ; ++k) s += arows[m * NQ + k] * bf(w[k]);
+            out[m * hidden + n] = bf(x[m * hidden + n]) + s;
+        }
+    }
+    if (k_new) memcpy(k_new, Kn, (size_t)(B * Hkv * S * d) * sizeof(double));
+    if (v_new) memcpy(v_new, Vn, (size_t)(B * Hkv * S * d) * sizeof(double));
+    if (attn_out) memcpy(attn_out, arows, (size_t)(B * S * NQ) * sizeof(double));
+done:
+    free(rows);
+    free(Kn);
+    free(Vn);
+    free(arows);
+    return err;
+}

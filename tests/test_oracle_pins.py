@@ -487,6 +487,65 @@ def test_decode_attention_f16_query_equals_library_sdpa():
         np.testing.assert_allclose(got[b], ref, rtol=1e-11, atol=1e-12)
 
 
+def _empty_cache(B, Hkv, Lmax, d):
+    return torch.zeros((B, Hkv, Lmax, d), dtype=torch.bfloat16), torch.zeros((B, Hkv, Lmax, d), dtype=torch.bfloat16)
+
+
+def test_prefill_cached_at_offset_zero_is_the_plain_prefill():
+    """With nothing cached (p0 = 0) the cached prefill is the plain layer."""
+    cfg = _tiny(S=21)
+    t = make_layer_inputs(cfg, seed=19, w_std=0.3)
+    kc, vc = _empty_cache(cfg.B, cfg.Hkv, 32, cfg.head_dim)
+    got = oracle.prefill_cached(t["x"], t["Wqkv"], t["Wo"], t["q_norm_w"], t["k_norm_w"], cfg.rope_theta, cfg.eps,
+                                cfg.B, cfg.S, cfg.hidden, cfg.Hq, cfg.Hkv, cfg.head_dim, kc, vc, [0] * cfg.B, 32,
+                                threads=T)
+    ref = _fwd(cfg, t, want_stages=True)
+    np.testing.assert_allclose(got["out"], ref["out"], rtol=1e-13, atol=1e-13)
+    np.testing.assert_allclose(got["k"], ref["k"], rtol=1e-13, atol=1e-13)
+    np.testing.assert_allclose(got["attn"], ref["attn"], rtol=1e-13, atol=1e-13)
+
+
+def test_prefill_cached_single_token_is_the_decode_step():
+    """One new token per sequence is exactly the decode step."""
+    cfg = _tiny(S=1, B=3)
+    t = make_layer_inputs(cfg, seed=20, w_std=0.3)
+    rng = np.random.default_rng(20)
+    Lmax = 40
+    kc = bf16(rng.standard_normal((cfg.B, cfg.Hkv, Lmax, cfg.head_dim)))
+    vc = bf16(rng.standard_normal((cfg.B, cfg.Hkv, Lmax, cfg.head_dim)))
+    p0 = [5, 0, 39]
+    got = oracle.prefill_cached(t["x"], t["Wqkv"], t["Wo"], t["q_norm_w"], t["k_norm_w"], cfg.rope_theta, cfg.eps,
+                                cfg.B, 1, cfg.hidden, cfg.Hq, cfg.Hkv, cfg.head_dim, kc, vc, p0, Lmax, threads=T)
+    dec = oracle.decode(t["x"][:, 0], t["Wqkv"], t["Wo"], t["q_norm_w"], t["k_norm_w"], cfg.rope_theta, cfg.eps,
+                        cfg.B, cfg.hidden, cfg.Hq, cfg.Hkv, cfg.head_dim, kc, vc, p0, Lmax, threads=T)
+    np.testing.assert_allclose(got["out"], dec["out"], rtol=1e-13, atol=1e-13)
+    np.testing.assert_allclose(got["k"][:, :, 0], dec["k"], rtol=1e-13, atol=1e-13)
+
+
+def test_prefill_in_two_chunks_matches_one_prefill():
+    """Chunked prefill: the first S1 tokens prefilled, their keys/values cached
+    (bf16), then the next S2 tokens at offset S1 reproduce the one-shot
+    prefill's last S2 rows to bf16 accuracy ([Part]: global positions)."""
+    cfg = _tiny(S=30, B=2)
+    t = make_layer_inputs(cfg, seed=21, w_std=0.3)
+    S1, S2, Lmax = 17, 13, 32
+    full = _fwd(cfg, t, want_stages=True)
+    kc, vc = _empty_cache(cfg.B, cfg.Hkv, Lmax, cfg.head_dim)
+    kc[:, :, :S1] = torch.from_numpy(full["k"][:, :, :S1]).to(torch.bfloat16)
+    vc[:, :, :S1] = torch.from_numpy(full["v"][:, :, :S1]).to(torch.bfloat16)
+    got = oracle.prefill_cached(t["x"][:, S1:].contiguous(), t["Wqkv"], t["Wo"], t["q_norm_w"], t["k_norm_w"],
+                                cfg.rope_theta, cfg.eps, cfg.B, S2, cfg.hidden, cfg.Hq, cfg.Hkv, cfg.head_dim,
+                                kc, vc, [S1] * cfg.B, Lmax, threads=T)
+    ref = full["out"].reshape(cfg.B, cfg.S, -1)[:, S1:].reshape(-1, cfg.hidden)
+    np.testing.assert_allclose(got["out"], ref, rtol=0, atol=2e-2 * np.abs(ref).max())
+    np.testing.assert_allclose(got["k"], full["k"][:, :, S1:], rtol=1e-12, atol=1e-13)
+    # the wrong offset is caught
+    bad = oracle.prefill_cached(t["x"][:, S1:].contiguous(), t["Wqkv"], t["Wo"], t["q_norm_w"], t["k_norm_w"],
+                                cfg.rope_theta, cfg.eps, cfg.B, S2, cfg.hidden, cfg.Hq, cfg.Hkv, cfg.head_dim,
+                                kc, vc, [S1 - 1] * cfg.B, Lmax, threads=T)
+    assert np.abs(bad["k"] - full["k"][:, :, S1:]).max() > 1e-2
+
+
 def test_oracle_rejects_bad_arguments():
     with pytest.raises(RuntimeError):
         oracle.rope_rows(np.zeros((1, 3)), [0.0], 1e4)     # odd head_dim
