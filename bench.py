@@ -391,6 +391,48 @@ def run_ours(args, world, rank, local):
                            "kernel_ms": round(ams_, 4)}}
     del dt_, dout, dws
 
+    # ---- chunked prefill: the last 2048 tokens of a 16384-token Qwen3-32B context
+    chunk = None
+    if not args.no_chunk:
+        cc = cfg.with_(S=2048)
+        p0, Lmax = 14336, 16384
+        ct = make_layer_inputs(cc, seed=SEEDS[cfg.name] + 17 + 7919 * rank, device=str(dev))
+        gen = torch.Generator(device=dev)
+        gen.manual_seed(SEEDS[cfg.name] + 18)
+        kc = torch.randn((1, cc.Hkv, Lmax, cc.head_dim), generator=gen, device=dev).to(torch.bfloat16)
+        vc = torch.randn((1, cc.Hkv, Lmax, cc.head_dim), generator=gen, device=dev).to(torch.bfloat16)
+        cl = torch.full((1,), p0, dtype=torch.int32, device=dev)
+        cout = torch.empty_like(ct["x"])
+        cws = gq.new_workspace(gq.gqa_attn_prefill_cached_workspace_size(1, cc.S, cc.Hq, cc.head_dim), dev)
+        cf = {"qkv": 2 * cc.S * (cc.Hq + 2 * cc.Hkv) * cc.head_dim * cc.hidden,
+              "attn": 4 * cc.Hq * cc.head_dim * (cc.S * p0 + cc.S * (cc.S + 1) // 2),
+              "oproj": 2 * cc.S * cc.hidden * cc.Hq * cc.head_dim}
+        cf["total"] = sum(cf.values())
+
+        def chunk_step():
+            gq.gqa_attn_prefill_cached(ct["x"], ct["Wqkv"], ct["Wo"], ct["q_norm_w"], ct["k_norm_w"], cc.rope_theta,
+                                       cc.eps, 1, cc.S, cc.hidden, cc.Hq, cc.Hkv, cc.head_dim, True, kc, vc, cl,
+                                       Lmax, cout, cws, stream)
+
+        for _ in range(args.warmup):
+            chunk_step()
+        torch.cuda.synchronize()
+        cev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(args.steps)]
+        for i in range(args.steps):
+            flush.zero_()
+            cev[i][0].record(stream)
+            chunk_step()
+            launches += gq.gqa_last_launch_count()
+            cev[i][1].record(stream)
+        torch.cuda.synchronize()
+        cms = reduce_max(statistics.mean(a.elapsed_time(b) for a, b in cev), world, dev)
+        chunk = {"workload": "qwen3_32b last 2048-token chunk after 14336 cached (Lmax 16384)",
+                 "value": round(reduce_sum(cf["total"], world, dev) / (cms * 1e-3) / 1e12, 1), "unit": "TFLOP/s",
+                 "ms_per_step": round(cms, 4), "frac_of_peak": round(cf["total"] / (cms * 1e-3) / 1e12 / peak_tf, 4),
+                 "flops_per_step": cf["total"]}
+        del ct, kc, vc, cout, cws
+
     # ---- CPU baseline (rank 0, N=1 only)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
@@ -407,7 +449,7 @@ def run_ours(args, world, rank, local):
                    "Hkv": cfg.Hkv, "head_dim": cfg.head_dim, "qk_norm": cfg.qk_norm, "rope_theta": cfg.rope_theta,
                    "causal": cfg.causal, "flops_per_step": fl["total"], "parallelism": f"replicas x{world}",
                    "l2": "flushed between steps (2x L2 buffer written outside the timed events)"},
-        "roofline": roofline, "decode": decode, "e2e": e2e, "cpu_baseline": cpu,
+        "roofline": roofline, "decode": decode, "chunked_prefill": chunk, "e2e": e2e, "cpu_baseline": cpu,
         "gpu_launches": launches, "wall_s": round(wall, 3), "clocks": clk.summary(),
         "step_ms": [round(x, 4) for x in step_ms],
     }
@@ -513,6 +555,7 @@ def main(argv=None):
     ap.add_argument("--cpu-tokens", type=int, default=2048, help="tokens of the CPU-baseline sample")
     ap.add_argument("--ref-tokens", type=int, default=256, help="tokens per reference-arm step")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--no-chunk", action="store_true", help="skip the chunked-prefill measurement")
     ap.add_argument("--stage", choices=["qkv", "attn", "oproj", "decode_attn"], default=None,
                     help="launch one stage alone (for profiler captures); prints its time, no benchmark line")
     args = ap.parse_args(argv)

@@ -139,6 +139,43 @@ int gqa_attention(const gqa_f16 *q, const gqa_f16 *k, const gqa_f16 *v,
 int gqa_oproj_residual(const gqa_bf16 *attn, const gqa_bf16 *Wo, const gqa_bf16 *x,
                        int M, int hidden, int q_width, gqa_bf16 *out, void *stream);
 
+/* ---------------------------------------------------- prefill into a cache */
+
+/* Bytes of workspace gqa_attn_prefill_cached needs: Q [B,Hq,S,d] and attn
+ * [B,S,Hq*d], both bf16, 256-byte aligned. */
+size_t gqa_attn_prefill_cached_workspace_size(int B, int S, int Hq, int head_dim);
+
+/* Chunked prefill: S new tokens per sequence appended to a KV cache
+ * ([T07] §4: RoPE at the position offsets, step 5 the cache returns the
+ * whole history; [Part]: masks and positions use global token positions).
+ *   x          [B, S, hidden], the new tokens of each sequence
+ *   k_cache, v_cache [B, Hkv, Lmax, head_dim] bf16: entries [0, cache_len[b])
+ *              hold earlier tokens (normed, rotated K; V); this call writes
+ *              the new tokens' K and V at slots cache_len[b] .. cache_len[b]+S-1
+ *   cache_len  device int32 [B]: tokens already cached = the first new
+ *              token's position; needs cache_len[b] + S <= Lmax (checked on the
+ *              device: violating sequences get zero attention rows and
+ *              gqa_check_device_error reports GQA_ERR_ARG).  Not modified.
+ *   causal     1: new token t sees keys u <= cache_len[b] + t; 0: all
+ *              cache_len[b] + S keys
+ *   out        [B, S, hidden] = x + o_proj(attn)
+ * With cache_len = 0 this is the plain prefill that also fills the cache.
+ * Q meets the bf16 cache in the score MMA, so on this path Q and P are bf16
+ * (the plain prefill keeps binary16). */
+int gqa_attn_prefill_cached(const gqa_bf16 *x, const gqa_bf16 *Wqkv, const gqa_bf16 *Wo,
+                            const gqa_bf16 *q_norm_w, const gqa_bf16 *k_norm_w,
+                            float rope_theta, float eps,
+                            int B, int S, int hidden, int Hq, int Hkv, int head_dim, int causal,
+                            gqa_bf16 *k_cache, gqa_bf16 *v_cache, const int *cache_len, int Lmax,
+                            gqa_bf16 *out, void *workspace, size_t workspace_bytes, void *stream);
+
+/* Its attention stage alone: q [B, Hq, S, head_dim] bf16 (positions
+ * cache_len[b] + t) over keys [0, cache_len[b] + S) of the caches (the new
+ * tokens' keys already appended); attn_out [B, S, Hq*head_dim] bf16. */
+int gqa_attention_cached(const gqa_bf16 *q, const gqa_bf16 *k_cache, const gqa_bf16 *v_cache,
+                         const int *cache_len, int B, int S, int Hq, int Hkv, int head_dim, int Lmax,
+                         int causal, gqa_bf16 *attn_out, void *stream);
+
 /* ------------------------------------------------------------------- decode */
 
 /* Bytes of device workspace gqa_attn_decode needs (Q of the new tokens,

@@ -31,6 +31,7 @@ EXPORTS = (
     "gqa_decode_qkv", "gqa_decode_attention_workspace_size", "gqa_decode_attention",
     "gqa_attn_cost", "gqa_last_error", "gqa_check_device_error", "gqa_selftest_bounded_wait",
     "gqa_last_launch_count", "gqa_decode_attention_noalloc",
+    "gqa_attn_prefill_cached_workspace_size", "gqa_attn_prefill_cached", "gqa_attention_cached",
 )
 
 
@@ -75,6 +76,9 @@ def lib():
         "gqa_selftest_bounded_wait": (_I, [_I]),
         "gqa_last_launch_count": (_I, []),
         "gqa_decode_attention_noalloc": (_I, [_P] * 4 + [_I] * 5 + [_P, _P]),
+        "gqa_attn_prefill_cached_workspace_size": (_Z, [_I] * 4),
+        "gqa_attn_prefill_cached": (_I, [_P] * 5 + [_F, _F] + [_I] * 7 + [_P, _P, _P, _I, _P, _P, _Z, _P]),
+        "gqa_attention_cached": (_I, [_P] * 4 + [_I] * 7 + [_P, _P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(L, name)
@@ -166,6 +170,28 @@ def gqa_attention(q, k, v, B, S, Hq, Hkv, head_dim, causal, attn_out, stream=Non
 def gqa_oproj_residual(attn, Wo, x, M, hidden, q_width, out, stream=None):
     _check(lib().gqa_oproj_residual(_bf16(attn), _bf16(Wo), _bf16(x), M, hidden, q_width, _bf16(out),
                                     _stream(stream)))
+
+
+# ------------------------------------------------------ prefill into a cache
+
+def gqa_attn_prefill_cached_workspace_size(B, S, Hq, head_dim) -> int:
+    return int(lib().gqa_attn_prefill_cached_workspace_size(B, S, Hq, head_dim))
+
+
+def gqa_attn_prefill_cached(x, Wqkv, Wo, q_norm_w, k_norm_w, rope_theta, eps, B, S, hidden, Hq, Hkv, head_dim,
+                            causal, k_cache, v_cache, cache_len, Lmax, out, workspace, stream=None):
+    _check(lib().gqa_attn_prefill_cached(_bf16(x), _bf16(Wqkv), _bf16(Wo), _bf16(q_norm_w), _bf16(k_norm_w),
+                                         rope_theta, eps, B, S, hidden, Hq, Hkv, head_dim, int(causal),
+                                         _bf16(k_cache), _bf16(v_cache), _i32(cache_len), Lmax, _bf16(out),
+                                         _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                         _stream(stream)))
+    return out
+
+
+def gqa_attention_cached(q, k_cache, v_cache, cache_len, B, S, Hq, Hkv, head_dim, Lmax, causal, attn_out,
+                         stream=None):
+    _check(lib().gqa_attention_cached(_bf16(q), _bf16(k_cache), _bf16(v_cache), _i32(cache_len), B, S, Hq, Hkv,
+                                      head_dim, Lmax, int(causal), _bf16(attn_out), _stream(stream)))
 
 
 # -------------------------------------------------------------------- decode

@@ -210,8 +210,8 @@ static FwdLayout fwd_layout(int B, int S, int Hq, int Hkv, int d)
 
 static int run_qkv(DeviceState &st, const gqa_bf16 *x, const gqa_bf16 *Wqkv, const gqa_bf16 *qn, const gqa_bf16 *kn,
                    float theta, float eps, int B, int S, int hidden, int Hq, int Hkv, int d, const int *pos_dev,
-                   int q_seq, int kv_seq, int rope_rows, int kv_f16, gqa_bf16 *q_out, gqa_bf16 *k_out,
-                   gqa_bf16 *v_out, cudaStream_t stream)
+                   int q_seq, int kv_seq, int rope_rows, int q_f16, int kv_f16, uint16_t *q_out, uint16_t *k_out,
+                   uint16_t *v_out, cudaStream_t stream)
 {
     const float2 *rope = nullptr;
     int rc;
@@ -220,7 +220,7 @@ static int run_qkv(DeviceState &st, const gqa_bf16 *x, const gqa_bf16 *Wqkv, con
         rc = rope_table(st, (double)theta, d, rope_rows, &rope);
     }
     if (rc) return rc;
-    GemmProblem p{x, Wqkv, pos_dev ? B : B * S, (Hq + 2 * Hkv) * d, hidden};
+    GemmProblem p{x, Wqkv, B * S, (Hq + 2 * Hkv) * d, hidden};
     QkvEpilogue e{};
     e.Hq = Hq;
     e.Hkv = Hkv;
@@ -234,8 +234,8 @@ static int run_qkv(DeviceState &st, const gqa_bf16 *x, const gqa_bf16 *Wqkv, con
     e.eps = eps;
     e.rope = rope;
     e.rope_rows = rope_rows;
-    e.q_f16 = 1;         // Q is always binary16 (bounded by QK-norm; fp32 math reads it)
-    e.kv_f16 = kv_f16;   // prefill: binary16 workspace; decode: the bf16 cache
+    e.q_f16 = q_f16;     // binary16 unless Q meets a bf16 cache in the same MMA
+    e.kv_f16 = kv_f16;   // prefill: binary16 workspace; cached paths: the bf16 cache
     e.q_out = q_out;
     e.k_out = k_out;
     e.v_out = v_out;
@@ -245,10 +245,11 @@ static int run_qkv(DeviceState &st, const gqa_bf16 *x, const gqa_bf16 *Wqkv, con
     return GQA_OK;
 }
 
-static int run_attention(DeviceState &st, const gqa_bf16 *q, const gqa_bf16 *k, const gqa_bf16 *v, int B, int S,
-                         int Hq, int Hkv, int d, int causal, gqa_bf16 *out, cudaStream_t stream)
+static int run_attention(DeviceState &st, const uint16_t *q, const uint16_t *k, const uint16_t *v, int B, int S,
+                         int Hq, int Hkv, int d, int causal, gqa_bf16 *out, cudaStream_t stream, int kv_seq = 0,
+                         const int *kv_start = nullptr, int bf16_qkv = 0)
 {
-    AttentionProblem p{q, k, v, out, B, S, Hq, Hkv, d, causal ? 1 : 0};
+    AttentionProblem p{q, k, v, out, B, S, Hq, Hkv, d, causal ? 1 : 0, kv_seq > 0 ? kv_seq : S, kv_start, bf16_qkv};
     cudaError_t ce = launch_attention(p, st.err, st.num_sms, stream);
     if (ce != cudaSuccess) return cuda_fail(ce, "attention launch");
     ++g_launches;
@@ -322,7 +323,7 @@ int gqa_qkv_proj(const gqa_bf16 *x, const gqa_bf16 *Wqkv, const gqa_bf16 *q_norm
     DeviceState *st;
     if ((rc = device_state(&st))) return rc;
     return run_qkv(*st, x, Wqkv, q_norm_w, k_norm_w, rope_theta, eps, B, S, hidden, Hq, Hkv, head_dim, nullptr, S, S,
-                   S, 1, q_out, k_out, v_out, (cudaStream_t)stream);
+                   S, 1, 1, q_out, k_out, v_out, (cudaStream_t)stream);
 }
 
 int gqa_attention(const gqa_f16 *q, const gqa_f16 *k, const gqa_f16 *v, int B, int S, int Hq, int Hkv,
@@ -388,7 +389,7 @@ int gqa_attn_forward_ex(const gqa_bf16 *x, const gqa_bf16 *Wqkv, const gqa_bf16 
     gqa_bf16 *attn = (gqa_bf16 *)(ws + L.attn);
     cudaStream_t s = (cudaStream_t)stream;
     if ((rc = run_qkv(*st, x, Wqkv, q_norm_w, k_norm_w, rope_theta, eps, B, S, hidden, Hq, Hkv, head_dim, nullptr, S,
-                      S, S, 1, q, k, v, s)))
+                      S, S, 1, 1, q, k, v, s)))
         return rc;
     if ((rc = run_attention(*st, q, k, v, B, S, Hq, Hkv, head_dim, causal, attn, s))) return rc;
     return run_oproj(*st, attn, Wo, x, B * S, hidden, Hq * head_dim, out, s);
@@ -486,7 +487,7 @@ int gqa_decode_qkv(const gqa_bf16 *x, const gqa_bf16 *Wqkv, const gqa_bf16 *q_no
     DeviceState *st;
     if ((rc = device_state(&st))) return rc;
     return run_qkv(*st, x, Wqkv, q_norm_w, k_norm_w, rope_theta, eps, B, 1, hidden, Hq, Hkv, head_dim, cache_len, 1,
-                   Lmax, Lmax, 0, q_out, k_cache, v_cache, (cudaStream_t)stream);
+                   Lmax, Lmax, 1, 0, q_out, k_cache, v_cache, (cudaStream_t)stream);
 }
 
 int gqa_decode_attention(const gqa_f16 *q, const gqa_bf16 *k_cache, const gqa_bf16 *v_cache, const int *kv_len,
@@ -541,11 +542,82 @@ int gqa_attn_decode(const gqa_bf16 *x, const gqa_bf16 *Wqkv, const gqa_bf16 *Wo,
     float *part = (float *)(ws + off_part);
     cudaStream_t s = (cudaStream_t)stream;
     if ((rc = run_qkv(*st, x, Wqkv, q_norm_w, k_norm_w, rope_theta, eps, B, 1, hidden, Hq, Hkv, head_dim, cache_len, 1,
-                      Lmax, Lmax, 0, q, k_cache, v_cache, s)))
+                      Lmax, Lmax, 1, 0, q, k_cache, v_cache, s)))
         return rc;
     if ((rc = run_decode_attn(*st, q, k_cache, v_cache, cache_len, 1, B, Hq, Hkv, head_dim, Lmax, attn, part, sp, s)))
         return rc;
     return run_oproj(*st, attn, Wo, x, B, hidden, Hq * head_dim, out, s);
+}
+
+// ------------------------------------------------------ prefill into a cache
+
+size_t gqa_attn_prefill_cached_workspace_size(int B, int S, int Hq, int head_dim)
+{
+    if (B <= 0 || S <= 0 || Hq <= 0 || head_dim <= 0) return 0;
+    const size_t n = (size_t)B * S * Hq * head_dim * 2;
+    return 2 * align256(n);  // Q (bf16) and attn (bf16)
+}
+
+static int check_cached(int B, int S, int hidden, int Hq, int Hkv, int d, int Lmax, const void *qn, const void *kn)
+{
+    int rc = check_layer(B, S, hidden, Hq, Hkv, d, qn, kn);
+    if (rc) return rc;
+    if ((rc = check_group_pow2(Hq, Hkv))) return rc;
+    if (Lmax < S) return fail(GQA_ERR_ARG, "Lmax=%d is smaller than the %d new tokens", Lmax, S);
+    if ((long long)B * Hkv * Lmax * d > (1LL << 40)) return fail(GQA_ERR_UNSUPPORTED, "cache too large");
+    return GQA_OK;
+}
+
+int gqa_attention_cached(const gqa_bf16 *q, const gqa_bf16 *k_cache, const gqa_bf16 *v_cache, const int *cache_len,
+                         int B, int S, int Hq, int Hkv, int head_dim, int Lmax, int causal, gqa_bf16 *attn_out,
+                         void *stream)
+{
+    g_launches = 0;
+    int rc = check_cached(B, S, 8, Hq, Hkv, head_dim, Lmax, nullptr, nullptr);
+    if (rc) return rc;
+    if (!q || !k_cache || !v_cache || !cache_len || !attn_out) return fail(GQA_ERR_ARG, "null pointer");
+    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(attn_out))
+        return fail(GQA_ERR_ARG, "tensor pointers must be 16-byte aligned");
+    DeviceState *st;
+    if ((rc = device_state(&st))) return rc;
+    return run_attention(*st, q, k_cache, v_cache, B, S, Hq, Hkv, head_dim, causal, attn_out, (cudaStream_t)stream,
+                         Lmax, cache_len, 1);
+}
+
+int gqa_attn_prefill_cached(const gqa_bf16 *x, const gqa_bf16 *Wqkv, const gqa_bf16 *Wo, const gqa_bf16 *q_norm_w,
+                            const gqa_bf16 *k_norm_w, float rope_theta, float eps, int B, int S, int hidden, int Hq,
+                            int Hkv, int head_dim, int causal, gqa_bf16 *k_cache, gqa_bf16 *v_cache,
+                            const int *cache_len, int Lmax, gqa_bf16 *out, void *workspace, size_t workspace_bytes,
+                            void *stream)
+{
+    g_launches = 0;
+    int rc = check_cached(B, S, hidden, Hq, Hkv, head_dim, Lmax, q_norm_w, k_norm_w);
+    if (rc) return rc;
+    if (!x || !Wqkv || !Wo || !k_cache || !v_cache || !cache_len || !out) return fail(GQA_ERR_ARG, "null pointer");
+    if (!aligned16(x) || !aligned16(Wqkv) || !aligned16(Wo) || !aligned16(k_cache) || !aligned16(v_cache) ||
+        !aligned16(out))
+        return fail(GQA_ERR_ARG, "tensor pointers must be 16-byte aligned");
+    if (!(rope_theta > 0.0f) || !(eps >= 0.0f)) return fail(GQA_ERR_ARG, "rope_theta must be > 0 and eps >= 0");
+    const size_t nx = (size_t)B * S * hidden * 2;
+    if (overlap(out, nx, x, nx)) return fail(GQA_ERR_ARG, "out must not overlap x");
+    const size_t need = gqa_attn_prefill_cached_workspace_size(B, S, Hq, head_dim);
+    if (!workspace || workspace_bytes < need)
+        return fail(GQA_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", need,
+                    workspace ? workspace_bytes : (size_t)0);
+    if (((uintptr_t)workspace & 255u) != 0) return fail(GQA_ERR_ARG, "workspace must be 256-byte aligned");
+    DeviceState *st;
+    if ((rc = device_state(&st))) return rc;
+    uint8_t *ws = (uint8_t *)workspace;
+    gqa_bf16 *q = (gqa_bf16 *)ws;  // bf16: it meets the bf16 cache in the score MMA
+    gqa_bf16 *attn = (gqa_bf16 *)(ws + need / 2);
+    cudaStream_t s = (cudaStream_t)stream;
+    // K/V of the new tokens go straight into the cache at slots cache_len[b] + t
+    if ((rc = run_qkv(*st, x, Wqkv, q_norm_w, k_norm_w, rope_theta, eps, B, S, hidden, Hq, Hkv, head_dim, cache_len,
+                      S, Lmax, Lmax, 0, 0, q, k_cache, v_cache, s)))
+        return rc;
+    if ((rc = run_attention(*st, q, k_cache, v_cache, B, S, Hq, Hkv, head_dim, causal, attn, s, Lmax, cache_len, 1)))
+        return rc;
+    return run_oproj(*st, attn, Wo, x, B * S, hidden, Hq * head_dim, out, s);
 }
 
 // ---------------------------------------------------------------- accounting

@@ -46,6 +46,8 @@ constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O only past a 
 
 struct AttnParams {
     int B, S, Hq, Hkv, G, R, n_qblk, causal, num_items;
+    int kv_seq;            // sequence extent of the K/V tensors
+    const int *kv_start;   // device [B]: cached keys before the queries (NULL: none)
     float scale_log2;  // log2(e) / sqrt(d)
     uint16_t *out;
     unsigned *err;
@@ -67,7 +69,9 @@ struct ASmem {
     static constexpr int ALLOC = TOTAL + 1024;
 };
 
-template <int D>
+// D: head_dim.  BF: Q, K, V and P are bf16 (queries over a bf16 KV cache)
+// instead of binary16.
+template <int D, bool BF>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                 const __grid_constant__ CUtensorMap tmV, const AttnParams P)
@@ -97,7 +101,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int b = bh / P.Hkv, g = bh % P.Hkv;
     const int t0 = qblk * kTiles * P.R;
     const int t_last = min(t0 + kTiles * P.R, P.S) - 1;
-    const int n_kv = P.causal ? (t_last / kKeys + 1) : (P.S + kKeys - 1) / kKeys;
+    // keys [0, p0) are cached before the S queries; query t sits at position p0 + t
+    int p0 = P.kv_start ? P.kv_start[b] : 0;
+    const bool bad = p0 < 0 || p0 + P.S > P.kv_seq;
+    if (bad) {
+        if (threadIdx.x == 0) atomicOr(P.err, kErrIndex);
+        p0 = 0;
+    }
+    const int n_kv = bad ? 0 : (P.causal ? ((p0 + t_last) / kKeys + 1) : (p0 + P.S + kKeys - 1) / kKeys);
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < L::NBARS; ++i) mbar_init(bars + i, 1);
@@ -145,8 +156,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp == 1) {
         if (lane == 0) {
-            constexpr uint32_t idesc_s = idesc_f16_f32(kRows, kKeys, 0, 0);  // Q, K: K-major over d
-            constexpr uint32_t idesc_o = idesc_f16_f32(kRows, D, 0, 1);      // P (TMEM), V MN-major (d contiguous)
+            // S: Q, K K-major over d; O: P from TMEM, V MN-major (d contiguous)
+            constexpr uint32_t idesc_s = BF ? idesc_bf16_f32(kRows, kKeys, 0, 0) : idesc_f16_f32(kRows, kKeys, 0, 0);
+            constexpr uint32_t idesc_o = BF ? idesc_bf16_f32(kRows, D, 0, 1) : idesc_f16_f32(kRows, D, 0, 1);
             auto issue_s = [&](int i, int j) {  // S_i = Q_i K(j)^T
                 const uint32_t sQ = smem_u32(smem + L::Q + i * L::NCH * L::CHUNK);
                 const uint32_t sK = smem_u32(smem + L::K + (j % ST) * L::NCH * L::CHUNK);
@@ -158,7 +170,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                     sw128_desc(sK + c * L::CHUNK + 32 * k, 16, 1024), idesc_s, (c | k) != 0);
                 umma_commit(s_full + i);
             };
-            bool ok = mbar_wait(q_full, 0, err) && mbar_wait(k_full, 0, err);
+            bool ok = n_kv > 0 && mbar_wait(q_full, 0, err) && mbar_wait(k_full, 0, err);
             if (ok) {
                 tc_fence_after();
                 issue_s(0, 0);
@@ -209,7 +221,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int t = t0 + wg * P.R + tl;
         const bool row_ok = in_pack && t < P.S;
         // keys u <= lim are visible to this row
-        const int lim = !in_pack ? -1 : (P.causal ? min(t, P.S - 1) : P.S - 1);
+        const int lim = !in_pack ? -1 : (P.causal ? p0 + min(t, P.S - 1) : p0 + P.S - 1);
         const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
         const uint32_t tS = tmem + 256 * wg + lane_off, tO = tS + 128;
         const float sl = P.scale_log2;
@@ -256,7 +268,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         nm2);
                     const float2 p = make_float2(ex2(x.x), ex2(x.y));
                     rs2[e & 1] = __fadd2_rn(rs2[e & 1], p);
-                    pk[e] = pack_f16(p.x, p.y);
+                    pk[e] = BF ? pack_bf16(p.x, p.y) : pack_f16(p.x, p.y);
                 }
                 tmem_st16_nowait(tS + 16 * c, pk);
             }
@@ -279,7 +291,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(p_full + wg);
         }
-        if (mbar_wait(o_done + wg, 0, err)) {
+        if (n_kv == 0) {  // rejected offset (reported): zero rows, nothing else ran
+            if (row_ok) {
+                uint4 *d4 = reinterpret_cast<uint4 *>(P.out + ((size_t)(b * P.S + t) * P.Hq + g * P.G + hl) * D);
+                for (int c = 0; c < D / 8; ++c) d4[c] = make_uint4(0, 0, 0, 0);
+            }
+        } else if (mbar_wait(o_done + wg, 0, err)) {
             tc_fence_after();
             const float inv_l = (l_i > 0.0f) ? 1.0f / l_i : 0.0f;
             const int head = g * P.G + hl;
@@ -310,7 +327,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-template <int D>
+template <int D, bool BF>
 cudaError_t run_attn(const AttentionProblem &p, unsigned *err, cudaStream_t stream)
 {
     using L = ASmem<D>;
@@ -321,8 +338,9 @@ cudaError_t run_attn(const AttentionProblem &p, unsigned *err, cudaStream_t stre
     const uint64_t dq[3] = {(uint64_t)D, (uint64_t)p.S, (uint64_t)p.B * p.Hq};
     const uint64_t sq[2] = {(uint64_t)D * 2, (uint64_t)p.S * D * 2};
     const uint32_t bq[3] = {64, (uint32_t)R, (uint32_t)G};
-    const uint64_t dk[3] = {(uint64_t)D, (uint64_t)p.S, (uint64_t)p.B * p.Hkv};
-    const uint64_t sk[2] = {(uint64_t)D * 2, (uint64_t)p.S * D * 2};
+    // K, V viewed as [B*Hkv, kv_seq, D] (16-bit elements; the copy is type-blind)
+    const uint64_t dk[3] = {(uint64_t)D, (uint64_t)p.kv_seq, (uint64_t)p.B * p.Hkv};
+    const uint64_t sk[2] = {(uint64_t)D * 2, (uint64_t)p.kv_seq * D * 2};
     const uint32_t bk[3] = {64, (uint32_t)kKeys, 1};
     if (encode_tmap(&tq, p.q, 3, dq, sq, bq, true) != CUDA_SUCCESS) return cudaErrorInvalidValue;
     if (encode_tmap(&tk, p.k, 3, dk, sk, bk, true) != CUDA_SUCCESS) return cudaErrorInvalidValue;
@@ -338,9 +356,11 @@ cudaError_t run_attn(const AttentionProblem &p, unsigned *err, cudaStream_t stre
     a.causal = p.causal;
     a.num_items = p.B * p.Hkv * a.n_qblk;
     a.scale_log2 = 1.4426950408889634f / sqrtf((float)D);
+    a.kv_seq = p.kv_seq;
+    a.kv_start = p.kv_start;
     a.out = p.out;
     a.err = err;
-    auto kern = attn_kernel<D>;
+    auto kern = attn_kernel<D, BF>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC);
     if (e != cudaSuccess) return e;
     kern<<<a.num_items, kThreads, L::ALLOC, stream>>>(tq, tk, tv, a);
@@ -355,8 +375,13 @@ cudaError_t launch_attention(const AttentionProblem &p, unsigned *err, int num_s
     if (p.Hkv <= 0 || p.Hq % p.Hkv) return cudaErrorInvalidValue;
     const int G = p.Hq / p.Hkv;
     if (G > kRows) return cudaErrorInvalidValue;
-    if (p.d == 128) return run_attn<128>(p, err, stream);
-    if (p.d == 64) return run_attn<64>(p, err, stream);
+    if (p.bf16_qkv) {
+        if (p.d == 128) return run_attn<128, true>(p, err, stream);
+        if (p.d == 64) return run_attn<64, true>(p, err, stream);
+    } else {
+        if (p.d == 128) return run_attn<128, false>(p, err, stream);
+        if (p.d == 64) return run_attn<64, false>(p, err, stream);
+    }
     return cudaErrorInvalidValue;
 }
 

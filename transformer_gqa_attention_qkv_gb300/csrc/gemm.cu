@@ -97,9 +97,10 @@ DEVI void epilogue_qkv(const GemmParams &P, uint32_t tcol, int m, int n0, bool r
     const int HqD = e.Hq * D, HkvD = e.Hkv * D;
     int b = 0, pos = 0, q_slot = 0, kv_slot = 0;
     if (row_ok) {
-        if (e.pos_dev) {
-            b = m;
-            pos = e.pos_dev[m];
+        if (e.pos_dev) {  // new tokens after pos_dev[b] cached ones: position = slot = pos_dev[b] + t
+            b = m / e.S;
+            q_slot = m - b * e.S;
+            pos = e.pos_dev[b] + q_slot;
             kv_slot = pos;
         } else {
             b = m / e.S;

@@ -18,8 +18,8 @@ namespace gqa {
 // rotated (RoPE) at the row's position; results are written head-major.
 struct QkvEpilogue {
     int Hq, Hkv, d;
-    int S;                 // prefill: tokens per sequence (row m = b*S + t)
-    const int *pos_dev;    // decode: row m = b, position = slot = pos_dev[b]; NULL for prefill
+    int S;                 // tokens per sequence (row m = b*S + t)
+    const int *pos_dev;    // cached: position = K/V slot = pos_dev[b] + t; NULL: position t
     int q_seq;             // sequence extent of q_out (S, or 1 for decode)
     int kv_seq;            // sequence extent of k_out / v_out (S, or Lmax for decode)
     const uint16_t *q_norm_w, *k_norm_w;  // [d] bf16, or both NULL
@@ -52,10 +52,13 @@ cudaError_t launch_gemm_residual(const GemmProblem &p, const ResidualEpilogue &e
 // ------------------------------------------------------- prefill attention
 struct AttentionProblem {
     const uint16_t *q;  // [B, Hq, S, d]
-    const uint16_t *k;  // [B, Hkv, S, d]
-    const uint16_t *v;  // [B, Hkv, S, d]
+    const uint16_t *k;  // [B, Hkv, kv_seq, d]
+    const uint16_t *v;  // [B, Hkv, kv_seq, d]
     uint16_t *out;      // [B, S, Hq*d]
     int B, S, Hq, Hkv, d, causal;
+    int kv_seq;            // sequence extent of k/v (S, or Lmax for a cache)
+    const int *kv_start;   // device [B]: keys already cached before the S queries (NULL: 0)
+    int bf16_qkv;          // 1: q/k/v bf16 (P bf16); 0: binary16 (P binary16)
 };
 cudaError_t launch_attention(const AttentionProblem &p, unsigned *err, int num_sms, cudaStream_t stream);
 
