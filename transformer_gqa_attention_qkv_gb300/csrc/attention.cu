@@ -69,13 +69,16 @@ struct ASmem {
     static constexpr int ALLOC = TOTAL + 1024;
 };
 
-// D: head_dim.  BF: Q, K, V and P are bf16 (queries over a bf16 KV cache)
-// instead of binary16.
-template <int D, bool BF>
+// D: head_dim.  CACHED: the queries follow kv_start[b] cached keys of a bf16
+// KV cache, so Q, K, V and P are bf16; otherwise they are binary16 and the
+// keys are exactly the S query positions (this variant compiles without any
+// offset arithmetic).
+template <int D, bool CACHED>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                 const __grid_constant__ CUtensorMap tmV, const AttnParams P)
 {
+    constexpr bool BF = CACHED;
     using L = ASmem<D>;
     constexpr int ST = L::STAGES;
     extern __shared__ uint8_t smem_raw[];
@@ -102,11 +105,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int t0 = qblk * kTiles * P.R;
     const int t_last = min(t0 + kTiles * P.R, P.S) - 1;
     // keys [0, p0) are cached before the S queries; query t sits at position p0 + t
-    int p0 = P.kv_start ? P.kv_start[b] : 0;
-    const bool bad = p0 < 0 || p0 + P.S > P.kv_seq;
-    if (bad) {
-        if (threadIdx.x == 0) atomicOr(P.err, kErrIndex);
-        p0 = 0;
+    int p0 = 0;
+    bool bad = false;
+    if constexpr (CACHED) {
+        p0 = P.kv_start[b];
+        bad = p0 < 0 || p0 + P.S > P.kv_seq;
+        if (bad) {
+            if (threadIdx.x == 0) atomicOr(P.err, kErrIndex);
+            p0 = 0;
+        }
     }
     const int n_kv = bad ? 0 : (P.causal ? ((p0 + t_last) / kKeys + 1) : (p0 + P.S + kKeys - 1) / kKeys);
 
@@ -170,7 +177,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                     sw128_desc(sK + c * L::CHUNK + 32 * k, 16, 1024), idesc_s, (c | k) != 0);
                 umma_commit(s_full + i);
             };
-            bool ok = n_kv > 0 && mbar_wait(q_full, 0, err) && mbar_wait(k_full, 0, err);
+            bool ok = (!CACHED || n_kv > 0) && mbar_wait(q_full, 0, err) && mbar_wait(k_full, 0, err);
             if (ok) {
                 tc_fence_after();
                 issue_s(0, 0);
@@ -291,7 +298,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(p_full + wg);
         }
-        if (n_kv == 0) {  // rejected offset (reported): zero rows, nothing else ran
+        if (CACHED && n_kv == 0) {  // rejected offset (reported): zero rows, nothing else ran
             if (row_ok) {
                 uint4 *d4 = reinterpret_cast<uint4 *>(P.out + ((size_t)(b * P.S + t) * P.Hq + g * P.G + hl) * D);
                 for (int c = 0; c < D / 8; ++c) d4[c] = make_uint4(0, 0, 0, 0);
