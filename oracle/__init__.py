@@ -88,6 +88,14 @@ def _load():
     lib.oracle_decode.argtypes = [_u16p, _u16p, _u16p, _u16p, _u16p, _D, _D,
                                   _L, _L, _L, _L, _L, _u16p, _u16p, _i32p, _L,
                                   _f64p, _f64p, _f64p, _f64p, _f64p, _I]
+    # the *_rd forms take the rotary width (reading R16) after eps
+    lib.oracle_rope_rows_rd.restype = _I
+    lib.oracle_rope_rows_rd.argtypes = [_f64p, _L, _L, _L, _f64p, _D, _f64p]
+    for name in ("oracle_qkv_stage", "oracle_forward", "oracle_decode", "oracle_prefill_cached"):
+        base = getattr(lib, name).argtypes
+        f = getattr(lib, name + "_rd")
+        f.restype = _I
+        f.argtypes = base[:7] + [_L] + base[7:]
     _lib = lib
     return lib
 
@@ -173,12 +181,18 @@ def rmsnorm_rows(rows: np.ndarray, w, eps: float) -> np.ndarray:
     return out
 
 
-def rope_rows(rows: np.ndarray, pos, theta: float) -> np.ndarray:
+def _rd(rotary_dim, d):
+    return d if rotary_dim is None else int(rotary_dim)
+
+
+def rope_rows(rows: np.ndarray, pos, theta: float, rotary_dim=None) -> np.ndarray:
+    """RoPE of each row at its position; rotary_dim (default: the row
+    length) rotates only the first rotary_dim features (reading R16)."""
     rows = np.ascontiguousarray(rows, dtype=np.float64)
     n, d = rows.shape
     p = np.ascontiguousarray(np.broadcast_to(np.asarray(pos, dtype=np.float64), (n,)))
     out = np.empty_like(rows)
-    _check(_load().oracle_rope_rows(_pf(rows), n, d, _pf(p), theta, _pf(out)), "rope")
+    _check(_load().oracle_rope_rows_rd(_pf(rows), n, d, _rd(rotary_dim, d), _pf(p), theta, _pf(out)), "rope")
     return out
 
 
@@ -194,12 +208,12 @@ def linear(x, W, threads=None) -> np.ndarray:
 
 
 def qkv_stage(x, Wqkv, q_norm_w, k_norm_w, rope_theta, eps, B, S, hidden, Hq, Hkv, d,
-              threads=None):
+              threads=None, rotary_dim=None):
     """Q [B,Hq,S,d], K/V [B,Hkv,S,d] after projection, QK-norm and RoPE."""
     q = np.empty((B, Hq, S, d)); k = np.empty((B, Hkv, S, d)); v = np.empty((B, Hkv, S, d))
     xb, wb, qn, kn = _bits(x), _bits(Wqkv), _bits(q_norm_w), _bits(k_norm_w)
-    _check(_load().oracle_qkv_stage(_p16(xb), _p16(wb), _p16(qn), _p16(kn), rope_theta, eps,
-                                    B, S, hidden, Hq, Hkv, d, _pf(q), _pf(k), _pf(v),
+    _check(_load().oracle_qkv_stage_rd(_p16(xb), _p16(wb), _p16(qn), _p16(kn), rope_theta, eps,
+                                       _rd(rotary_dim, d), B, S, hidden, Hq, Hkv, d, _pf(q), _pf(k), _pf(v),
                                     threads or default_threads()), "qkv_stage")
     return q, k, v
 
@@ -238,7 +252,7 @@ def oproj_stage(attn, Wo, x, M, hidden, QW, sel=None, threads=None):
 
 
 def forward(x, Wqkv, Wo, q_norm_w, k_norm_w, rope_theta, eps, B, S, hidden, Hq, Hkv, d,
-            causal=True, sel=None, want_stages=False, threads=None):
+            causal=True, sel=None, want_stages=False, threads=None, rotary_dim=None):
     """The whole layer.  Returns out [n_sel, hidden]; with want_stages also
     q [n_sel,Hq,d], attn [n_sel,Hq*d], k/v [B,Hkv,S,d] (all float64)."""
     s, n = _sel(sel, B * S)
@@ -248,8 +262,8 @@ def forward(x, Wqkv, Wo, q_norm_w, k_norm_w, rope_theta, eps, B, S, hidden, Hq, 
     k = np.empty((B, Hkv, S, d)) if want_stages else None
     v = np.empty((B, Hkv, S, d)) if want_stages else None
     xb, wb, ob, qn, kn = _bits(x), _bits(Wqkv), _bits(Wo), _bits(q_norm_w), _bits(k_norm_w)
-    _check(_load().oracle_forward(_p16(xb), _p16(wb), _p16(ob), _p16(qn), _p16(kn), rope_theta,
-                                  eps, B, S, hidden, Hq, Hkv, d, int(causal),
+    _check(_load().oracle_forward_rd(_p16(xb), _p16(wb), _p16(ob), _p16(qn), _p16(kn), rope_theta,
+                                     eps, _rd(rotary_dim, d), B, S, hidden, Hq, Hkv, d, int(causal),
                                   None if s is None else s.ctypes.data_as(_i64p), n,
                                   _pf(q), _pf(a), _pf(out), _pf(k), _pf(v),
                                   threads or default_threads()), "forward")
@@ -272,7 +286,7 @@ def decode_attention_stage(q, k_cache, v_cache, kv_len, B, Hq, Hkv, d, Lmax, thr
 
 
 def prefill_cached(x, Wqkv, Wo, q_norm_w, k_norm_w, rope_theta, eps, B, S, hidden, Hq, Hkv, d,
-                   k_cache, v_cache, p0, Lmax, causal=True, threads=None):
+                   k_cache, v_cache, p0, Lmax, causal=True, threads=None, rotary_dim=None):
     """S new tokens per sequence at positions p0[b].. after p0[b] cached ones.
     Returns dict out [B*S, hidden], k/v [B,Hkv,S,d] (the new tokens'), attn
     [B*S, Hq*d]; the caches are read, not modified."""
@@ -281,15 +295,15 @@ def prefill_cached(x, Wqkv, Wo, q_norm_w, k_norm_w, rope_theta, eps, B, S, hidde
     p = np.ascontiguousarray(np.asarray(p0, dtype=np.int32))
     xb, wb, ob, qn, kn = _bits(x), _bits(Wqkv), _bits(Wo), _bits(q_norm_w), _bits(k_norm_w)
     kb, vb = _bits(k_cache), _bits(v_cache)
-    _check(_load().oracle_prefill_cached(_p16(xb), _p16(wb), _p16(ob), _p16(qn), _p16(kn), rope_theta, eps,
-                                         B, S, hidden, Hq, Hkv, d, int(causal), _p16(kb), _p16(vb),
+    _check(_load().oracle_prefill_cached_rd(_p16(xb), _p16(wb), _p16(ob), _p16(qn), _p16(kn), rope_theta, eps,
+                                            _rd(rotary_dim, d), B, S, hidden, Hq, Hkv, d, int(causal), _p16(kb), _p16(vb),
                                          p.ctypes.data_as(_i32p), Lmax, _pf(out), _pf(kn_), _pf(vn_), _pf(a),
                                          threads or default_threads()), "prefill_cached")
     return {"out": out, "k": kn_, "v": vn_, "attn": a}
 
 
 def decode(x, Wqkv, Wo, q_norm_w, k_norm_w, rope_theta, eps, B, hidden, Hq, Hkv, d,
-           k_cache, v_cache, cache_len, Lmax, threads=None):
+           k_cache, v_cache, cache_len, Lmax, threads=None, rotary_dim=None):
     """One decode step.  Returns dict out [B,hidden], q [B,Hq,d], k/v [B,Hkv,d]
     (the new token's), attn [B,Hq*d]; the caches are read, not modified."""
     out = np.empty((B, hidden)); q = np.empty((B, Hq, d))
@@ -297,8 +311,8 @@ def decode(x, Wqkv, Wo, q_norm_w, k_norm_w, rope_theta, eps, B, hidden, Hq, Hkv,
     cl = np.ascontiguousarray(np.asarray(cache_len, dtype=np.int32))
     xb, wb, ob, qn, kn = _bits(x), _bits(Wqkv), _bits(Wo), _bits(q_norm_w), _bits(k_norm_w)
     kb, vb = _bits(k_cache), _bits(v_cache)
-    _check(_load().oracle_decode(_p16(xb), _p16(wb), _p16(ob), _p16(qn), _p16(kn), rope_theta, eps,
-                                 B, hidden, Hq, Hkv, d, _p16(kb), _p16(vb), cl.ctypes.data_as(_i32p),
+    _check(_load().oracle_decode_rd(_p16(xb), _p16(wb), _p16(ob), _p16(qn), _p16(kn), rope_theta, eps,
+                                    _rd(rotary_dim, d), B, hidden, Hq, Hkv, d, _p16(kb), _p16(vb), cl.ctypes.data_as(_i32p),
                                  Lmax, _pf(out), _pf(q), _pf(kn_), _pf(vn_), _pf(a),
                                  threads or default_threads()), "decode")
     return {"out": out, "q": q, "k": kn_, "v": vn_, "attn": a}

@@ -35,6 +35,12 @@
  *      pos * theta^(-2i/d), applied to Q and K only ([T07] §3-§4).
  *   R5 causal: query at position t sees keys u <= t, the diagonal included.
  *   R6 out = x + o_proj(attn) ([NeoX] "Qwen3-0.6B example": residual addition).
+ *   R16 partial rotary: with rotary_dim rd (even, 0 <= rd <= d) the rotation
+ *      of R4 acts on the first rd features only, pairing i with i + rd/2 at
+ *      angle pos * theta^(-2i/rd); features [rd, d) pass unchanged; rd = d is
+ *      R4 ([NeoX] "Scaling and RoPE": RoPE is built from the effective
+ *      head_dim, subject to the rotary_pct setting and an even dimension).
+ *      The functions named *_rd take rd; the others use rd = d.
  */
 #include <math.h>
 #include <stdint.h>
@@ -168,16 +174,17 @@ static void rmsnorm_head(double *v, long d, const uint16_t *w, double eps)
     for (long i = 0; i < d; ++i) v[i] = v[i] * r * bf(w[i]);
 }
 
-/* RoPE on one head vector at position pos, in place (reading R4):
- * for i < d/2, angle f = pos * theta^(-2i/d),
- *   (v[i], v[i+d/2]) <- (v[i] cos f - v[i+d/2] sin f, v[i+d/2] cos f + v[i] sin f)
+/* RoPE on the first rd features of one head vector at position pos, in
+ * place (readings R4, R16): for i < rd/2, angle f = pos * theta^(-2i/rd),
+ *   (v[i], v[i+rd/2]) <- (v[i] cos f - v[i+rd/2] sin f, v[i+rd/2] cos f + v[i] sin f);
+ * features from rd on are not touched.
  * ([T07] §4 "Set up RoPE" from (head_dim, max_position, rope_theta);
  *  [NeoX] "Scaling and RoPE": built from the effective head_dim). */
-static void rope_head(double *v, long d, double pos, double theta)
+static void rope_head(double *v, long rd, double pos, double theta)
 {
-    long half = d / 2;
+    long half = rd / 2;
     for (long i = 0; i < half; ++i) {
-        double f = pos * pow(theta, -2.0 * (double)i / (double)d);
+        double f = pos * pow(theta, -2.0 * (double)i / (double)rd);
         double c = cos(f), s = sin(f);
         double a = v[i], b = v[i + half];
         v[i] = a * c - b * s;
@@ -197,15 +204,22 @@ int oracle_rmsnorm_rows(const double *in, long nrows, long d, const uint16_t *w,
     return ORACLE_OK;
 }
 
+int oracle_rope_rows_rd(const double *in, long nrows, long d, long rd, const double *pos,
+                        double theta, double *out)
+{
+    if (!in || !out || !pos || nrows < 0 || d <= 0 || (d & 1)) return ORACLE_EARG;
+    if (rd < 0 || rd > d || (rd & 1)) return ORACLE_EARG;
+    for (long r = 0; r < nrows; ++r) {
+        memcpy(out + r * d, in + r * d, (size_t)d * sizeof(double));
+        rope_head(out + r * d, rd, pos[r], theta);
+    }
+    return ORACLE_OK;
+}
+
 int oracle_rope_rows(const double *in, long nrows, long d, const double *pos,
                      double theta, double *out)
 {
-    if (!in || !out || !pos || nrows < 0 || d <= 0 || (d & 1)) return ORACLE_EARG;
-    for (long r = 0; r < nrows; ++r) {
-        memcpy(out + r * d, in + r * d, (size_t)d * sizeof(double));
-        rope_head(out + r * d, d, pos[r], theta);
-    }
-    return ORACLE_OK;
+    return oracle_rope_rows_rd(in, nrows, d, d, pos, theta, out);
 }
 
 int oracle_linear(const uint16_t *x, const uint16_t *W, long M, long N, long K,
@@ -275,15 +289,16 @@ static int attend_row(const double *q, const kv_src *src, long n_vis, long d, do
 
 /* q_out [B,Hq,S,d], k_out/v_out [B,Hkv,S,d] (head-major, [T07] §4 step 4).
  * q_norm_w/k_norm_w both NULL means no QK-norm.  Positions are 0..S-1. */
-int oracle_qkv_stage(const uint16_t *x, const uint16_t *Wqkv,
+int oracle_qkv_stage_rd(const uint16_t *x, const uint16_t *Wqkv,
                      const uint16_t *q_norm_w, const uint16_t *k_norm_w,
-                     double rope_theta, double eps,
+                     double rope_theta, double eps, long rd,
                      long B, long S, long hidden, long Hq, long Hkv, long d,
                      double *q_out, double *k_out, double *v_out, int nthreads)
 {
     if (!x || !Wqkv || !q_out || !k_out || !v_out) return ORACLE_EARG;
     if (B <= 0 || S <= 0 || hidden <= 0 || Hq <= 0 || Hkv <= 0 || d <= 0 || (d & 1)) return ORACLE_EARG;
     if ((q_norm_w == NULL) != (k_norm_w == NULL)) return ORACLE_EARG;
+    if (rd < 0 || rd > d || (rd & 1)) return ORACLE_EARG;
     long NQ = Hq * d, NKV = Hkv * d, N = NQ + 2 * NKV;
     int err = ORACLE_OK;
     set_threads(nthreads);
@@ -297,13 +312,13 @@ int oracle_qkv_stage(const uint16_t *x, const uint16_t *Wqkv,
         for (long j = 0; j < Hq; ++j) {
             double *v = row + j * d;
             if (q_norm_w) rmsnorm_head(v, d, q_norm_w, eps);   /* step 2 */
-            rope_head(v, d, (double)t, rope_theta);             /* step 3 */
+            rope_head(v, rd, (double)t, rope_theta);             /* step 3 */
             memcpy(q_out + ((b * Hq + j) * S + t) * d, v, (size_t)d * sizeof(double));
         }
         for (long g = 0; g < Hkv; ++g) {
             double *v = row + NQ + g * d;
             if (k_norm_w) rmsnorm_head(v, d, k_norm_w, eps);
-            rope_head(v, d, (double)t, rope_theta);
+            rope_head(v, rd, (double)t, rope_theta);
             memcpy(k_out + ((b * Hkv + g) * S + t) * d, v, (size_t)d * sizeof(double));
             memcpy(v_out + ((b * Hkv + g) * S + t) * d, row + NQ + NKV + g * d,
                    (size_t)d * sizeof(double));
@@ -382,9 +397,9 @@ int oracle_oproj_stage(const uint16_t *attn, const uint16_t *Wo, const uint16_t 
  * sel == NULL every token is computed.  Any of q_sel [n_sel,Hq,d],
  * attn_sel [n_sel,Hq*d], k_all/v_all [B,Hkv,S,d] may be NULL.
  * out_sel [n_sel, hidden] is required. */
-int oracle_forward(const uint16_t *x, const uint16_t *Wqkv, const uint16_t *Wo,
+int oracle_forward_rd(const uint16_t *x, const uint16_t *Wqkv, const uint16_t *Wo,
                    const uint16_t *q_norm_w, const uint16_t *k_norm_w,
-                   double rope_theta, double eps,
+                   double rope_theta, double eps, long rd,
                    long B, long S, long hidden, long Hq, long Hkv, long d, int causal,
                    const long *sel, long n_sel,
                    double *q_sel, double *attn_sel, double *out_sel,
@@ -394,6 +409,7 @@ int oracle_forward(const uint16_t *x, const uint16_t *Wqkv, const uint16_t *Wo,
     if (B <= 0 || S <= 0 || hidden <= 0 || Hq <= 0 || Hkv <= 0 || d <= 0 || (d & 1)) return ORACLE_EARG;
     if (Hq % Hkv || d > 1024) return ORACLE_EARG;
     if ((q_norm_w == NULL) != (k_norm_w == NULL)) return ORACLE_EARG;
+    if (rd < 0 || rd > d || (rd & 1)) return ORACLE_EARG;
     if (!sel && n_sel != B * S) return ORACLE_EARG;
     long NQ = Hq * d, NKV = Hkv * d, G = Hq / Hkv;
     int err = ORACLE_OK;
@@ -414,7 +430,7 @@ int oracle_forward(const uint16_t *x, const uint16_t *Wqkv, const uint16_t *Wo,
         for (long g = 0; g < Hkv; ++g) {
             double *k = row + g * d;
             if (k_norm_w) rmsnorm_head(k, d, k_norm_w, eps);
-            rope_head(k, d, (double)t, rope_theta);
+            rope_head(k, rd, (double)t, rope_theta);
             memcpy(Kd + ((b * Hkv + g) * S + t) * d, k, (size_t)d * sizeof(double));
             memcpy(Vd + ((b * Hkv + g) * S + t) * d, row + NKV + g * d, (size_t)d * sizeof(double));
         }
@@ -433,7 +449,7 @@ int oracle_forward(const uint16_t *x, const uint16_t *Wqkv, const uint16_t *Wo,
         for (long j = 0; j < Hq; ++j) {
             double *q = qrow + j * d;
             if (q_norm_w) rmsnorm_head(q, d, q_norm_w, eps);
-            rope_head(q, d, (double)t, rope_theta);
+            rope_head(q, rd, (double)t, rope_theta);
             long g = j / G;
             kv_src src = {NULL, NULL, Kd + (b * Hkv + g) * S * d, Vd + (b * Hkv + g) * S * d, 0, 0};
             long n_vis = causal ? t + 1 : S;
@@ -499,9 +515,9 @@ int oracle_decode_attention_stage(const uint16_t *q, int q_f16, const uint16_t *
  * cache, which this function does not modify) and the query attends to all
  * p+1 keys.  x [B, hidden]; out [B, hidden].  Optional outputs:
  * q_new [B,Hq,d], k_new/v_new [B,Hkv,d], attn [B,Hq*d]. */
-int oracle_decode(const uint16_t *x, const uint16_t *Wqkv, const uint16_t *Wo,
+int oracle_decode_rd(const uint16_t *x, const uint16_t *Wqkv, const uint16_t *Wo,
                   const uint16_t *q_norm_w, const uint16_t *k_norm_w,
-                  double rope_theta, double eps,
+                  double rope_theta, double eps, long rd,
                   long B, long hidden, long Hq, long Hkv, long d,
                   const uint16_t *k_cache, const uint16_t *v_cache, const int *cache_len,
                   long Lmax, double *out, double *q_new, double *k_new, double *v_new,
@@ -511,6 +527,7 @@ int oracle_decode(const uint16_t *x, const uint16_t *Wqkv, const uint16_t *Wo,
     if (B <= 0 || hidden <= 0 || Hq <= 0 || Hkv <= 0 || d <= 0 || (d & 1) || d > 1024) return ORACLE_EARG;
     if (Hq % Hkv) return ORACLE_EARG;
     if ((q_norm_w == NULL) != (k_norm_w == NULL)) return ORACLE_EARG;
+    if (rd < 0 || rd > d || (rd & 1)) return ORACLE_EARG;
     for (long b = 0; b < B; ++b)
         if (cache_len[b] < 0 || cache_len[b] + 1 > Lmax) return ORACLE_EARG;
     long NQ = Hq * d, NKV = Hkv * d, N = NQ + 2 * NKV, G = Hq / Hkv;
@@ -527,11 +544,11 @@ int oracle_decode(const uint16_t *x, const uint16_t *Wqkv, const uint16_t *Wo,
         linear_row(x + b * hidden, Wqkv, 0, N, hidden, row);
         for (long j = 0; j < Hq; ++j) {
             if (q_norm_w) rmsnorm_head(row + j * d, d, q_norm_w, eps);
-            rope_head(row + j * d, d, p, rope_theta);
+            rope_head(row + j * d, rd, p, rope_theta);
         }
         for (long g = 0; g < Hkv; ++g) {
             if (k_norm_w) rmsnorm_head(row + NQ + g * d, d, k_norm_w, eps);
-            rope_head(row + NQ + g * d, d, p, rope_theta);
+            rope_head(row + NQ + g * d, rd, p, rope_theta);
         }
     }
 
@@ -582,9 +599,9 @@ int oracle_decode(const uint16_t *x, const uint16_t *Wqkv, const uint16_t *Wo,
  * all p0[b] + S keys.  x [B, S, hidden]; out [B, S, hidden].  Optional:
  * k_new/v_new [B, Hkv, S, d] and attn [B, S, Hq*d].  With p0 = 0 this is the
  * plain prefill; with S = 1 it is the decode step. */
-int oracle_prefill_cached(const uint16_t *x, const uint16_t *Wqkv, const uint16_t *Wo,
+int oracle_prefill_cached_rd(const uint16_t *x, const uint16_t *Wqkv, const uint16_t *Wo,
                           const uint16_t *q_norm_w, const uint16_t *k_norm_w,
-                          double rope_theta, double eps,
+                          double rope_theta, double eps, long rd,
                           long B, long S, long hidden, long Hq, long Hkv, long d, int causal,
                           const uint16_t *k_cache, const uint16_t *v_cache, const int *p0,
                           long Lmax, double *out, double *k_new, double *v_new, double *attn_out,
@@ -594,6 +611,7 @@ int oracle_prefill_cached(const uint16_t *x, const uint16_t *Wqkv, const uint16_
     if (B <= 0 || S <= 0 || hidden <= 0 || Hq <= 0 || Hkv <= 0 || d <= 0 || (d & 1) || d > 1024) return ORACLE_EARG;
     if (Hq % Hkv) return ORACLE_EARG;
     if ((q_norm_w == NULL) != (k_norm_w == NULL)) return ORACLE_EARG;
+    if (rd < 0 || rd > d || (rd & 1)) return ORACLE_EARG;
     for (long b = 0; b < B; ++b)
         if (p0[b] < 0 || p0[b] + S > Lmax) return ORACLE_EARG;
     long NQ = Hq * d, NKV = Hkv * d, N = NQ + 2 * NKV, G = Hq / Hkv;
@@ -614,12 +632,12 @@ int oracle_prefill_cached(const uint16_t *x, const uint16_t *Wqkv, const uint16_
         linear_row(x + m * hidden, Wqkv, 0, N, hidden, row);
         for (long j = 0; j < Hq; ++j) {
             if (q_norm_w) rmsnorm_head(row + j * d, d, q_norm_w, eps);
-            rope_head(row + j * d, d, pos, rope_theta);
+            rope_head(row + j * d, rd, pos, rope_theta);
         }
         for (long g = 0; g < Hkv; ++g) {
             double *k = row + NQ + g * d;
             if (k_norm_w) rmsnorm_head(k, d, k_norm_w, eps);
-            rope_head(k, d, pos, rope_theta);
+            rope_head(k, rd, pos, rope_theta);
             memcpy(Kn + ((b * Hkv + g) * S + t) * d, k, (size_t)d * sizeof(double));
             memcpy(Vn + ((b * Hkv + g) * S + t) * d, row + NQ + NKV + g * d, (size_t)d * sizeof(double));
         }
@@ -657,4 +675,55 @@ done:
     free(Vn);
     free(arows);
     return err;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Full rotary (rd = d, reading R4): the entry points without _rd.           */
+/* ------------------------------------------------------------------------ */
+
+int oracle_qkv_stage(const uint16_t *x, const uint16_t *Wqkv,
+                     const uint16_t *q_norm_w, const uint16_t *k_norm_w,
+                     double rope_theta, double eps,
+                     long B, long S, long hidden, long Hq, long Hkv, long d,
+                     double *q_out, double *k_out, double *v_out, int nthreads)
+{
+    return oracle_qkv_stage_rd(x, Wqkv, q_norm_w, k_norm_w, rope_theta, eps, d, B, S, hidden, Hq, Hkv, d,
+                               q_out, k_out, v_out, nthreads);
+}
+
+int oracle_forward(const uint16_t *x, const uint16_t *Wqkv, const uint16_t *Wo,
+                   const uint16_t *q_norm_w, const uint16_t *k_norm_w,
+                   double rope_theta, double eps,
+                   long B, long S, long hidden, long Hq, long Hkv, long d, int causal,
+                   const long *sel, long n_sel,
+                   double *q_sel, double *attn_sel, double *out_sel,
+                   double *k_all, double *v_all, int nthreads)
+{
+    return oracle_forward_rd(x, Wqkv, Wo, q_norm_w, k_norm_w, rope_theta, eps, d, B, S, hidden, Hq, Hkv, d,
+                             causal, sel, n_sel, q_sel, attn_sel, out_sel, k_all, v_all, nthreads);
+}
+
+int oracle_decode(const uint16_t *x, const uint16_t *Wqkv, const uint16_t *Wo,
+                  const uint16_t *q_norm_w, const uint16_t *k_norm_w,
+                  double rope_theta, double eps,
+                  long B, long hidden, long Hq, long Hkv, long d,
+                  const uint16_t *k_cache, const uint16_t *v_cache, const int *cache_len,
+                  long Lmax, double *out, double *q_new, double *k_new, double *v_new,
+                  double *attn_out, int nthreads)
+{
+    return oracle_decode_rd(x, Wqkv, Wo, q_norm_w, k_norm_w, rope_theta, eps, d, B, hidden, Hq, Hkv, d,
+                            k_cache, v_cache, cache_len, Lmax, out, q_new, k_new, v_new, attn_out, nthreads);
+}
+
+int oracle_prefill_cached(const uint16_t *x, const uint16_t *Wqkv, const uint16_t *Wo,
+                          const uint16_t *q_norm_w, const uint16_t *k_norm_w,
+                          double rope_theta, double eps,
+                          long B, long S, long hidden, long Hq, long Hkv, long d, int causal,
+                          const uint16_t *k_cache, const uint16_t *v_cache, const int *p0,
+                          long Lmax, double *out, double *k_new, double *v_new, double *attn_out,
+                          int nthreads)
+{
+    return oracle_prefill_cached_rd(x, Wqkv, Wo, q_norm_w, k_norm_w, rope_theta, eps, d, B, S, hidden, Hq,
+                                    Hkv, d, causal, k_cache, v_cache, p0, Lmax, out, k_new, v_new, attn_out,
+                                    nthreads);
 }

@@ -554,3 +554,105 @@ def test_oracle_rejects_bad_arguments():
     K = bf16(rng.standard_normal((1, 2, 4, 8)))
     with pytest.raises(RuntimeError):
         oracle.attention_stage(Q, K, K, 1, 4, 3, 2, 8)     # Hq % Hkv != 0
+
+
+# ----------------------------------------------------------------- partial rotary (reading R16)
+
+def _complex_rope(a, pos, theta, rd):
+    """Rotate-half RoPE on the first rd features as complex multiplication of
+    z_i = a_i + i*a_{i+rd/2} by exp(i*pos*theta^(-2i/rd)); the rest unchanged."""
+    a = torch.as_tensor(a, dtype=torch.float64)
+    if rd == 0:
+        return a.clone()
+    half = rd // 2
+    z = torch.complex(a[..., :half], a[..., half:rd])
+    ang = torch.as_tensor(pos, dtype=torch.float64)[..., None] * \
+        theta ** (-2.0 * torch.arange(half, dtype=torch.float64) / rd)
+    z = z * torch.polar(torch.ones_like(ang), ang)
+    return torch.cat([z.real, z.imag, a[..., rd:]], dim=-1)
+
+
+def test_partial_rope_equals_complex_rotation_of_leading_features():
+    """[NeoX] "Scaling and RoPE": rotary_pct < 1 rotates only the leading
+    features, with frequencies over the rotary width; rd = d is the full
+    rotation and rd = 0 the identity."""
+    rng = np.random.default_rng(31)
+    d, theta = 64, 1e4
+    v = rng.standard_normal((6, d))
+    pos = np.array([0.0, 1.0, 7.0, 129.0, 4095.0, 8192.0])
+    for rd in (0, 16, 32, 48, 64):
+        out = oracle.rope_rows(v, pos, theta, rotary_dim=rd)
+        ref = _complex_rope(v, pos, theta, rd).numpy()
+        np.testing.assert_allclose(out, ref, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(oracle.rope_rows(v, pos, theta, rotary_dim=d), oracle.rope_rows(v, pos, theta),
+                               rtol=0, atol=0)
+    # a slip that uses d instead of rd for the frequencies is caught
+    wrong = _complex_rope(v, pos, theta ** (16 / d), 16).numpy()  # theta^(-2i/d) = (theta^(rd/d))^(-2i/rd)
+    assert np.abs(oracle.rope_rows(v, pos, theta, rotary_dim=16) - wrong).max() > 1e-3
+
+
+def test_partial_rope_invariants():
+    """The rotated part keeps its norm, the tail is untouched, and the score of
+    two rotated vectors depends only on the position difference."""
+    rng = np.random.default_rng(32)
+    d, rd, theta = 32, 8, 1e6
+    q, k = rng.standard_normal(d), rng.standard_normal(d)
+    a = oracle.rope_rows(np.stack([q] * 3), [0.0, 5.0, 1000.0], theta, rotary_dim=rd)
+    np.testing.assert_allclose(np.linalg.norm(a[:, :rd], axis=1), np.linalg.norm(q[:rd]), rtol=1e-12)
+    np.testing.assert_allclose(a[:, rd:], np.stack([q[rd:]] * 3), rtol=0, atol=0)
+    np.testing.assert_allclose(a[0], q, rtol=0, atol=1e-15)
+    dots = []
+    for m, n in ((3, 1), (10, 8), (1002, 1000)):
+        qm = oracle.rope_rows(q[None], [float(m)], theta, rotary_dim=rd)[0]
+        kn = oracle.rope_rows(k[None], [float(n)], theta, rotary_dim=rd)[0]
+        dots.append(qm @ kn)
+    np.testing.assert_allclose(dots, dots[0], rtol=1e-10)
+
+
+def test_forward_partial_rotary_equals_library_composition():
+    """The layer with rotary_dim = d/4 and d/2 equals the float64 torch
+    composition (F.linear, F.rms_norm, complex RoPE on the leading features,
+    SDPA); the cached prefill at offset 0 and the decode step of the last token
+    agree with it."""
+    for rd in (2, 4):
+        cfg = _tiny()
+        t = make_layer_inputs(cfg, seed=33, w_std=0.3)
+        B, S, h, Hq, Hkv, d = cfg.B, cfg.S, cfg.hidden, cfg.Hq, cfg.Hkv, cfg.head_dim
+        x, W, Wo = f64(t["x"]), f64(t["Wqkv"]), f64(t["Wo"])
+        q = F.linear(x, W[:Hq * d]).view(B, S, Hq, d)
+        k = F.linear(x, W[Hq * d:(Hq + Hkv) * d]).view(B, S, Hkv, d)
+        v = F.linear(x, W[(Hq + Hkv) * d:]).view(B, S, Hkv, d)
+        q = F.rms_norm(q, (d,), weight=f64(t["q_norm_w"]), eps=cfg.eps)
+        k = F.rms_norm(k, (d,), weight=f64(t["k_norm_w"]), eps=cfg.eps)
+        pos = torch.arange(S, dtype=torch.float64)[:, None]
+        q = _complex_rope(q, pos, cfg.rope_theta, rd).transpose(1, 2)
+        k = _complex_rope(k, pos, cfg.rope_theta, rd).transpose(1, 2)
+        v = v.transpose(1, 2)
+        a = F.scaled_dot_product_attention(q, k.repeat_interleave(Hq // Hkv, 1),
+                                           v.repeat_interleave(Hq // Hkv, 1), is_causal=True)
+        a = a.transpose(1, 2).reshape(B, S, Hq * d)
+        ref = (x + F.linear(a, Wo)).reshape(B * S, h).numpy()
+        got = _fwd(cfg, t, want_stages=True, rotary_dim=rd)
+        np.testing.assert_allclose(got["out"], ref, rtol=1e-11, atol=1e-11)
+        np.testing.assert_allclose(got["k"], k.numpy(), rtol=1e-11, atol=1e-11)
+        qs, ks, vs = oracle.qkv_stage(t["x"], t["Wqkv"], t["q_norm_w"], t["k_norm_w"], cfg.rope_theta, cfg.eps,
+                                      B, S, h, Hq, Hkv, d, threads=T, rotary_dim=rd)
+        np.testing.assert_allclose(qs, q.numpy(), rtol=1e-11, atol=1e-11)
+        kc, vc = _empty_cache(B, Hkv, 32, d)
+        pc = oracle.prefill_cached(t["x"], t["Wqkv"], t["Wo"], t["q_norm_w"], t["k_norm_w"], cfg.rope_theta,
+                                   cfg.eps, B, S, h, Hq, Hkv, d, kc, vc, [0] * B, 32, threads=T, rotary_dim=rd)
+        np.testing.assert_allclose(pc["out"], ref, rtol=1e-11, atol=1e-11)
+        kc[:, :, :S - 1] = torch.from_numpy(got["k"][:, :, :S - 1]).to(torch.bfloat16)
+        vc[:, :, :S - 1] = torch.from_numpy(got["v"][:, :, :S - 1]).to(torch.bfloat16)
+        dec = oracle.decode(t["x"][:, S - 1], t["Wqkv"], t["Wo"], t["q_norm_w"], t["k_norm_w"], cfg.rope_theta,
+                            cfg.eps, B, h, Hq, Hkv, d, kc, vc, [S - 1] * B, 32, threads=T, rotary_dim=rd)
+        np.testing.assert_allclose(dec["k"], got["k"][:, :, S - 1], rtol=1e-12, atol=1e-13)
+        last = got["out"].reshape(B, S, -1)[:, S - 1]
+        np.testing.assert_allclose(dec["out"], last, rtol=0, atol=2e-2 * np.abs(last).max())
+
+
+def test_partial_rotary_rejects_bad_widths():
+    v = np.zeros((1, 8))
+    for rd in (-2, 3, 10):
+        with pytest.raises(RuntimeError):
+            oracle.rope_rows(v, [0.0], 1e4, rotary_dim=rd)
