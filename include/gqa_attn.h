@@ -31,7 +31,8 @@
  *     [Hq*d, hidden], then W_k [Hkv*d, hidden], then W_v [Hkv*d, hidden].
  *   - Query head j attends with KV head j / (Hq/Hkv).
  *   - RMSNorm(v) = v * w / sqrt(mean(v^2) + eps) over head_dim.  RoPE pairs
- *     element i with i + head_dim/2 at angle pos * theta^(-2i/head_dim).
+ *     element i with i + head_dim/2 at angle pos * theta^(-2i/head_dim)
+ *     (the *_rd entry points rotate only the first rotary_dim features).
  *   - `stream` is a cudaStream_t passed as void* (NULL: the legacy default
  *     stream).  Work is enqueued asynchronously; the function returns after
  *     validation and launch.  Outputs are valid once the stream reaches them.
@@ -248,6 +249,48 @@ int gqa_decode_attention(const gqa_f16 *q, const gqa_bf16 *k_cache, const gqa_bf
 int gqa_decode_attention_noalloc(const gqa_f16 *q, const gqa_bf16 *k_cache, const gqa_bf16 *v_cache,
                                  const int *kv_len, int B, int Hq, int Hkv, int head_dim, int Lmax,
                                  gqa_bf16 *attn_out, void *stream);
+
+/* ------------------------------------------------------- partial rotary */
+
+/* The same five layer entry points with the rotary width as an argument:
+ * RoPE rotates only the first rotary_dim features of every Q and K head,
+ * pairing element i with i + rotary_dim/2 at angle
+ * pos * theta^(-2i/rotary_dim); features [rotary_dim, head_dim) are
+ * normalised but not rotated ([NeoX] "Scaling and RoPE": RoPE is built from
+ * the effective head_dim subject to the rotary_pct setting, i.e. rotary_dim =
+ * head_dim * rotary_pct, and an even width).  rotary_dim = head_dim is the
+ * plain entry point; rotary_dim = 0 applies no rotation.  rotary_dim odd,
+ * negative or above head_dim: GQA_ERR_ARG; a value other than head_dim,
+ * head_dim/2, head_dim/4 or 0: GQA_ERR_UNSUPPORTED.  Every other argument,
+ * layout, ownership rule and status is that of the function without _rd. */
+int gqa_attn_forward_rd(const gqa_bf16 *x, const gqa_bf16 *Wqkv, const gqa_bf16 *Wo,
+                        const gqa_bf16 *q_norm_w, const gqa_bf16 *k_norm_w,
+                        float rope_theta, float eps, int rotary_dim,
+                        int B, int S, int hidden, int Hq, int Hkv, int head_dim, int causal,
+                        gqa_bf16 *out, void *workspace, size_t workspace_bytes, void *stream);
+int gqa_qkv_proj_rd(const gqa_bf16 *x, const gqa_bf16 *Wqkv,
+                    const gqa_bf16 *q_norm_w, const gqa_bf16 *k_norm_w,
+                    float rope_theta, float eps, int rotary_dim,
+                    int B, int S, int hidden, int Hq, int Hkv, int head_dim,
+                    gqa_f16 *q_out, gqa_f16 *k_out, gqa_f16 *v_out, void *stream);
+int gqa_attn_prefill_cached_rd(const gqa_bf16 *x, const gqa_bf16 *Wqkv, const gqa_bf16 *Wo,
+                               const gqa_bf16 *q_norm_w, const gqa_bf16 *k_norm_w,
+                               float rope_theta, float eps, int rotary_dim,
+                               int B, int S, int hidden, int Hq, int Hkv, int head_dim, int causal,
+                               gqa_bf16 *k_cache, gqa_bf16 *v_cache, const int *cache_len, int Lmax,
+                               gqa_bf16 *out, void *workspace, size_t workspace_bytes, void *stream);
+int gqa_attn_decode_rd(const gqa_bf16 *x, const gqa_bf16 *Wqkv, const gqa_bf16 *Wo,
+                       const gqa_bf16 *q_norm_w, const gqa_bf16 *k_norm_w,
+                       float rope_theta, float eps, int rotary_dim,
+                       int B, int hidden, int Hq, int Hkv, int head_dim,
+                       gqa_bf16 *k_cache, gqa_bf16 *v_cache, const int *cache_len, int Lmax,
+                       gqa_bf16 *out, void *workspace, size_t workspace_bytes, void *stream);
+int gqa_decode_qkv_rd(const gqa_bf16 *x, const gqa_bf16 *Wqkv,
+                      const gqa_bf16 *q_norm_w, const gqa_bf16 *k_norm_w,
+                      float rope_theta, float eps, int rotary_dim,
+                      int B, int hidden, int Hq, int Hkv, int head_dim,
+                      gqa_bf16 *k_cache, gqa_bf16 *v_cache, const int *cache_len, int Lmax,
+                      gqa_f16 *q_out, void *stream);
 
 /* ------------------------------------------------------------ accounting */
 

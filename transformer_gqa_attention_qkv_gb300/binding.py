@@ -32,6 +32,8 @@ EXPORTS = (
     "gqa_attn_cost", "gqa_last_error", "gqa_check_device_error", "gqa_selftest_bounded_wait",
     "gqa_last_launch_count", "gqa_decode_attention_noalloc",
     "gqa_attn_prefill_cached_workspace_size", "gqa_attn_prefill_cached", "gqa_attention_cached",
+    "gqa_attn_forward_rd", "gqa_qkv_proj_rd", "gqa_attn_prefill_cached_rd", "gqa_attn_decode_rd",
+    "gqa_decode_qkv_rd",
 )
 
 
@@ -80,6 +82,13 @@ def lib():
         "gqa_attn_prefill_cached": (_I, [_P] * 5 + [_F, _F] + [_I] * 7 + [_P, _P, _P, _I, _P, _P, _Z, _P]),
         "gqa_attention_cached": (_I, [_P] * 4 + [_I] * 7 + [_P, _P]),
     }
+    # the *_rd forms: rotary_dim (int) right after rope_theta and eps
+    for base, name in (("gqa_attn_forward_ex", "gqa_attn_forward_rd"), ("gqa_qkv_proj", "gqa_qkv_proj_rd"),
+                       ("gqa_attn_prefill_cached", "gqa_attn_prefill_cached_rd"),
+                       ("gqa_attn_decode", "gqa_attn_decode_rd"), ("gqa_decode_qkv", "gqa_decode_qkv_rd")):
+        res, args = sig[base]
+        k = args.index(_F) + 2
+        sig[name] = (res, args[:k] + [_I] + args[k:])
     for name, (res, args) in sig.items():
         fn = getattr(L, name)
         fn.restype = res
@@ -159,6 +168,51 @@ def gqa_qkv_proj(x, Wqkv, q_norm_w, k_norm_w, rope_theta, eps, B, S, hidden, Hq,
     _check(lib().gqa_qkv_proj(_bf16(x), _bf16(Wqkv), _bf16(q_norm_w), _bf16(k_norm_w), rope_theta, eps,
                               B, S, hidden, Hq, Hkv, head_dim, _f16(q_out), _f16(k_out), _f16(v_out),
                               _stream(stream)))
+
+
+# ------------------------------------------- partial rotary (rotary_dim < head_dim)
+
+def gqa_attn_forward_rd(x, Wqkv, Wo, q_norm_w, k_norm_w, rope_theta, eps, rotary_dim, B, S, hidden, Hq, Hkv,
+                        head_dim, causal, out, workspace, stream=None):
+    _check(lib().gqa_attn_forward_rd(_bf16(x), _bf16(Wqkv), _bf16(Wo), _bf16(q_norm_w), _bf16(k_norm_w),
+                                     rope_theta, eps, rotary_dim, B, S, hidden, Hq, Hkv, head_dim, int(causal),
+                                     _bf16(out), _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                     _stream(stream)))
+    return out
+
+
+def gqa_qkv_proj_rd(x, Wqkv, q_norm_w, k_norm_w, rope_theta, eps, rotary_dim, B, S, hidden, Hq, Hkv, head_dim,
+                    q_out, k_out, v_out, stream=None):
+    _check(lib().gqa_qkv_proj_rd(_bf16(x), _bf16(Wqkv), _bf16(q_norm_w), _bf16(k_norm_w), rope_theta, eps,
+                                 rotary_dim, B, S, hidden, Hq, Hkv, head_dim, _f16(q_out), _f16(k_out),
+                                 _f16(v_out), _stream(stream)))
+
+
+def gqa_attn_prefill_cached_rd(x, Wqkv, Wo, q_norm_w, k_norm_w, rope_theta, eps, rotary_dim, B, S, hidden, Hq,
+                               Hkv, head_dim, causal, k_cache, v_cache, cache_len, Lmax, out, workspace,
+                               stream=None):
+    _check(lib().gqa_attn_prefill_cached_rd(_bf16(x), _bf16(Wqkv), _bf16(Wo), _bf16(q_norm_w), _bf16(k_norm_w),
+                                            rope_theta, eps, rotary_dim, B, S, hidden, Hq, Hkv, head_dim,
+                                            int(causal), _bf16(k_cache), _bf16(v_cache), _i32(cache_len), Lmax,
+                                            _bf16(out), _ptr(workspace),
+                                            workspace.numel() * workspace.element_size(), _stream(stream)))
+    return out
+
+
+def gqa_attn_decode_rd(x, Wqkv, Wo, q_norm_w, k_norm_w, rope_theta, eps, rotary_dim, B, hidden, Hq, Hkv,
+                       head_dim, k_cache, v_cache, cache_len, Lmax, out, workspace, stream=None):
+    _check(lib().gqa_attn_decode_rd(_bf16(x), _bf16(Wqkv), _bf16(Wo), _bf16(q_norm_w), _bf16(k_norm_w),
+                                    rope_theta, eps, rotary_dim, B, hidden, Hq, Hkv, head_dim, _bf16(k_cache),
+                                    _bf16(v_cache), _i32(cache_len), Lmax, _bf16(out), _ptr(workspace),
+                                    workspace.numel() * workspace.element_size(), _stream(stream)))
+    return out
+
+
+def gqa_decode_qkv_rd(x, Wqkv, q_norm_w, k_norm_w, rope_theta, eps, rotary_dim, B, hidden, Hq, Hkv, head_dim,
+                      k_cache, v_cache, cache_len, Lmax, q_out, stream=None):
+    _check(lib().gqa_decode_qkv_rd(_bf16(x), _bf16(Wqkv), _bf16(q_norm_w), _bf16(k_norm_w), rope_theta, eps,
+                                   rotary_dim, B, hidden, Hq, Hkv, head_dim, _bf16(k_cache), _bf16(v_cache),
+                                   _i32(cache_len), Lmax, _f16(q_out), _stream(stream)))
 
 
 def gqa_attention(q, k, v, B, S, Hq, Hkv, head_dim, causal, attn_out, stream=None):

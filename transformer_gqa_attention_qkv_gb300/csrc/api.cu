@@ -126,7 +126,7 @@ static int device_state(DeviceState **out)
     return GQA_OK;
 }
 
-// cos/sin(pos * theta^(-2i/d)) for pos < rows, i < d/2, computed in double on
+// cos/sin(pos * theta^(-2i/d)) for pos < rows, i < d/2 (d: the rotary width), computed in double on
 // the host and stored as fp32 (cos, sin) pairs.  Angles reach ~1.6e4 rad, where
 // an fp32 angle would already be off by ~1e-3 rad.
 static int rope_table(DeviceState &st, double theta, int d, int rows, const float2 **out)
@@ -188,6 +188,17 @@ static int check_group_pow2(int Hq, int Hkv)
     return GQA_OK;
 }
 
+// rotary_dim: even, in [0, head_dim]; the kernels implement d, d/2, d/4 and 0.
+static int check_rotary(int rd, int d)
+{
+    if (rd < 0 || rd > d || (rd & 1))
+        return fail(GQA_ERR_ARG, "rotary_dim=%d must be even and in [0, head_dim=%d]", rd, d);
+    if (rd != d && rd != d / 2 && rd != d / 4 && rd != 0)
+        return fail(GQA_ERR_UNSUPPORTED, "unsupported rotary_dim=%d (supported: head_dim, head_dim/2, head_dim/4, 0)",
+                    rd);
+    return GQA_OK;
+}
+
 static size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 struct FwdLayout {
@@ -209,17 +220,19 @@ static FwdLayout fwd_layout(int B, int S, int Hq, int Hkv, int d)
 // ------------------------------------------------------------ stage runners
 
 static int run_qkv(DeviceState &st, const gqa_bf16 *x, const gqa_bf16 *Wqkv, const gqa_bf16 *qn, const gqa_bf16 *kn,
-                   float theta, float eps, int B, int S, int hidden, int Hq, int Hkv, int d, const int *pos_dev,
+                   float theta, float eps, int rd, int B, int S, int hidden, int Hq, int Hkv, int d, const int *pos_dev,
                    int q_seq, int kv_seq, int rope_rows, int q_f16, int kv_f16, uint16_t *q_out, uint16_t *k_out,
                    uint16_t *v_out, cudaStream_t stream)
 {
     const float2 *rope = nullptr;
-    int rc;
-    {
-        std::lock_guard<std::mutex> lk(g_mu);
-        rc = rope_table(st, (double)theta, d, rope_rows, &rope);
+    if (rd > 0) {
+        int rc;
+        {
+            std::lock_guard<std::mutex> lk(g_mu);
+            rc = rope_table(st, (double)theta, rd, rope_rows, &rope);
+        }
+        if (rc) return rc;
     }
-    if (rc) return rc;
     GemmProblem p{x, Wqkv, B * S, (Hq + 2 * Hkv) * d, hidden};
     QkvEpilogue e{};
     e.Hq = Hq;
@@ -232,6 +245,7 @@ static int run_qkv(DeviceState &st, const gqa_bf16 *x, const gqa_bf16 *Wqkv, con
     e.q_norm_w = qn;
     e.k_norm_w = kn;
     e.eps = eps;
+    e.rd = rd;
     e.rope = rope;
     e.rope_rows = rope_rows;
     e.q_f16 = q_f16;     // binary16 unless Q meets a bf16 cache in the same MMA
@@ -309,9 +323,9 @@ size_t gqa_attn_workspace_size(int B, int S, int hidden, int Hq, int Hkv, int he
     return fwd_layout(B, S, Hq, Hkv, head_dim).total;
 }
 
-int gqa_qkv_proj(const gqa_bf16 *x, const gqa_bf16 *Wqkv, const gqa_bf16 *q_norm_w, const gqa_bf16 *k_norm_w,
-                 float rope_theta, float eps, int B, int S, int hidden, int Hq, int Hkv, int head_dim, gqa_f16 *q_out,
-                 gqa_f16 *k_out, gqa_f16 *v_out, void *stream)
+int gqa_qkv_proj_rd(const gqa_bf16 *x, const gqa_bf16 *Wqkv, const gqa_bf16 *q_norm_w, const gqa_bf16 *k_norm_w,
+                 float rope_theta, float eps, int rotary_dim, int B, int S, int hidden, int Hq, int Hkv, int head_dim,
+                 gqa_f16 *q_out, gqa_f16 *k_out, gqa_f16 *v_out, void *stream)
 {
     g_launches = 0;
     int rc = check_layer(B, S, hidden, Hq, Hkv, head_dim, q_norm_w, k_norm_w);
@@ -320,10 +334,11 @@ int gqa_qkv_proj(const gqa_bf16 *x, const gqa_bf16 *Wqkv, const gqa_bf16 *q_norm
     if (!aligned16(x) || !aligned16(Wqkv) || !aligned16(q_out) || !aligned16(k_out) || !aligned16(v_out))
         return fail(GQA_ERR_ARG, "tensor pointers must be 16-byte aligned");
     if (!(rope_theta > 0.0f) || !(eps >= 0.0f)) return fail(GQA_ERR_ARG, "rope_theta must be > 0 and eps >= 0");
+    if ((rc = check_rotary(rotary_dim, head_dim))) return rc;
     DeviceState *st;
     if ((rc = device_state(&st))) return rc;
-    return run_qkv(*st, x, Wqkv, q_norm_w, k_norm_w, rope_theta, eps, B, S, hidden, Hq, Hkv, head_dim, nullptr, S, S,
-                   S, 1, 1, q_out, k_out, v_out, (cudaStream_t)stream);
+    return run_qkv(*st, x, Wqkv, q_norm_w, k_norm_w, rope_theta, eps, rotary_dim, B, S, hidden, Hq, Hkv, head_dim,
+                   nullptr, S, S, S, 1, 1, q_out, k_out, v_out, (cudaStream_t)stream);
 }
 
 int gqa_attention(const gqa_f16 *q, const gqa_f16 *k, const gqa_f16 *v, int B, int S, int Hq, int Hkv,
@@ -358,10 +373,10 @@ int gqa_oproj_residual(const gqa_bf16 *attn, const gqa_bf16 *Wo, const gqa_bf16 
     return run_oproj(*st, attn, Wo, x, M, hidden, q_width, out, (cudaStream_t)stream);
 }
 
-int gqa_attn_forward_ex(const gqa_bf16 *x, const gqa_bf16 *Wqkv, const gqa_bf16 *Wo, const gqa_bf16 *q_norm_w,
-                        const gqa_bf16 *k_norm_w, float rope_theta, float eps, int B, int S, int hidden, int Hq,
-                        int Hkv, int head_dim, int causal, gqa_bf16 *out, void *workspace, size_t workspace_bytes,
-                        void *stream)
+int gqa_attn_forward_rd(const gqa_bf16 *x, const gqa_bf16 *Wqkv, const gqa_bf16 *Wo, const gqa_bf16 *q_norm_w,
+                        const gqa_bf16 *k_norm_w, float rope_theta, float eps, int rotary_dim, int B, int S,
+                        int hidden, int Hq, int Hkv, int head_dim, int causal, gqa_bf16 *out, void *workspace,
+                        size_t workspace_bytes, void *stream)
 {
     g_launches = 0;
     int rc = check_layer(B, S, hidden, Hq, Hkv, head_dim, q_norm_w, k_norm_w);
@@ -371,6 +386,7 @@ int gqa_attn_forward_ex(const gqa_bf16 *x, const gqa_bf16 *Wqkv, const gqa_bf16 
     if (!aligned16(x) || !aligned16(Wqkv) || !aligned16(Wo) || !aligned16(out))
         return fail(GQA_ERR_ARG, "tensor pointers must be 16-byte aligned");
     if (!(rope_theta > 0.0f) || !(eps >= 0.0f)) return fail(GQA_ERR_ARG, "rope_theta must be > 0 and eps >= 0");
+    if ((rc = check_rotary(rotary_dim, head_dim))) return rc;
     const size_t nx = (size_t)B * S * hidden * 2;
     const size_t nw = (size_t)(Hq + 2 * Hkv) * head_dim * hidden * 2, no = (size_t)hidden * Hq * head_dim * 2;
     if (overlap(out, nx, x, nx) || overlap(out, nx, Wqkv, nw) || overlap(out, nx, Wo, no))
@@ -388,8 +404,8 @@ int gqa_attn_forward_ex(const gqa_bf16 *x, const gqa_bf16 *Wqkv, const gqa_bf16 
     gqa_bf16 *q = (gqa_bf16 *)(ws + L.q), *k = (gqa_bf16 *)(ws + L.k), *v = (gqa_bf16 *)(ws + L.v);
     gqa_bf16 *attn = (gqa_bf16 *)(ws + L.attn);
     cudaStream_t s = (cudaStream_t)stream;
-    if ((rc = run_qkv(*st, x, Wqkv, q_norm_w, k_norm_w, rope_theta, eps, B, S, hidden, Hq, Hkv, head_dim, nullptr, S,
-                      S, S, 1, 1, q, k, v, s)))
+    if ((rc = run_qkv(*st, x, Wqkv, q_norm_w, k_norm_w, rope_theta, eps, rotary_dim, B, S, hidden, Hq, Hkv, head_dim,
+                      nullptr, S, S, S, 1, 1, q, k, v, s)))
         return rc;
     if ((rc = run_attention(*st, q, k, v, B, S, Hq, Hkv, head_dim, causal, attn, s))) return rc;
     return run_oproj(*st, attn, Wo, x, B * S, hidden, Hq * head_dim, out, s);
@@ -473,9 +489,9 @@ static int check_decode(int B, int hidden, int Hq, int Hkv, int d, int Lmax, con
     return GQA_OK;
 }
 
-int gqa_decode_qkv(const gqa_bf16 *x, const gqa_bf16 *Wqkv, const gqa_bf16 *q_norm_w, const gqa_bf16 *k_norm_w,
-                   float rope_theta, float eps, int B, int hidden, int Hq, int Hkv, int head_dim, gqa_bf16 *k_cache,
-                   gqa_bf16 *v_cache, const int *cache_len, int Lmax, gqa_f16 *q_out, void *stream)
+int gqa_decode_qkv_rd(const gqa_bf16 *x, const gqa_bf16 *Wqkv, const gqa_bf16 *q_norm_w, const gqa_bf16 *k_norm_w,
+                   float rope_theta, float eps, int rotary_dim, int B, int hidden, int Hq, int Hkv, int head_dim,
+                   gqa_bf16 *k_cache, gqa_bf16 *v_cache, const int *cache_len, int Lmax, gqa_f16 *q_out, void *stream)
 {
     g_launches = 0;
     int rc = check_decode(B, hidden, Hq, Hkv, head_dim, Lmax, q_norm_w, k_norm_w);
@@ -484,10 +500,11 @@ int gqa_decode_qkv(const gqa_bf16 *x, const gqa_bf16 *Wqkv, const gqa_bf16 *q_no
     if (!aligned16(x) || !aligned16(Wqkv) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(q_out))
         return fail(GQA_ERR_ARG, "tensor pointers must be 16-byte aligned");
     if (!(rope_theta > 0.0f) || !(eps >= 0.0f)) return fail(GQA_ERR_ARG, "rope_theta must be > 0 and eps >= 0");
+    if ((rc = check_rotary(rotary_dim, head_dim))) return rc;
     DeviceState *st;
     if ((rc = device_state(&st))) return rc;
-    return run_qkv(*st, x, Wqkv, q_norm_w, k_norm_w, rope_theta, eps, B, 1, hidden, Hq, Hkv, head_dim, cache_len, 1,
-                   Lmax, Lmax, 1, 0, q_out, k_cache, v_cache, (cudaStream_t)stream);
+    return run_qkv(*st, x, Wqkv, q_norm_w, k_norm_w, rope_theta, eps, rotary_dim, B, 1, hidden, Hq, Hkv, head_dim,
+                   cache_len, 1, Lmax, Lmax, 1, 0, q_out, k_cache, v_cache, (cudaStream_t)stream);
 }
 
 int gqa_decode_attention(const gqa_f16 *q, const gqa_bf16 *k_cache, const gqa_bf16 *v_cache, const int *kv_len,
@@ -512,9 +529,9 @@ int gqa_decode_attention(const gqa_f16 *q, const gqa_bf16 *k_cache, const gqa_bf
                            (float *)workspace, sp, (cudaStream_t)stream);
 }
 
-int gqa_attn_decode(const gqa_bf16 *x, const gqa_bf16 *Wqkv, const gqa_bf16 *Wo, const gqa_bf16 *q_norm_w,
-                    const gqa_bf16 *k_norm_w, float rope_theta, float eps, int B, int hidden, int Hq, int Hkv,
-                    int head_dim, gqa_bf16 *k_cache, gqa_bf16 *v_cache, const int *cache_len, int Lmax,
+int gqa_attn_decode_rd(const gqa_bf16 *x, const gqa_bf16 *Wqkv, const gqa_bf16 *Wo, const gqa_bf16 *q_norm_w,
+                    const gqa_bf16 *k_norm_w, float rope_theta, float eps, int rotary_dim, int B, int hidden, int Hq,
+                    int Hkv, int head_dim, gqa_bf16 *k_cache, gqa_bf16 *v_cache, const int *cache_len, int Lmax,
                     gqa_bf16 *out, void *workspace, size_t workspace_bytes, void *stream)
 {
     g_launches = 0;
@@ -525,6 +542,7 @@ int gqa_attn_decode(const gqa_bf16 *x, const gqa_bf16 *Wqkv, const gqa_bf16 *Wo,
         !aligned16(out))
         return fail(GQA_ERR_ARG, "tensor pointers must be 16-byte aligned");
     if (!(rope_theta > 0.0f) || !(eps >= 0.0f)) return fail(GQA_ERR_ARG, "rope_theta must be > 0 and eps >= 0");
+    if ((rc = check_rotary(rotary_dim, head_dim))) return rc;
     if (overlap(out, (size_t)B * hidden * 2, x, (size_t)B * hidden * 2))
         return fail(GQA_ERR_ARG, "out must not overlap x");
     DeviceState *st;
@@ -541,8 +559,8 @@ int gqa_attn_decode(const gqa_bf16 *x, const gqa_bf16 *Wqkv, const gqa_bf16 *Wo,
     gqa_bf16 *attn = (gqa_bf16 *)(ws + off_attn);
     float *part = (float *)(ws + off_part);
     cudaStream_t s = (cudaStream_t)stream;
-    if ((rc = run_qkv(*st, x, Wqkv, q_norm_w, k_norm_w, rope_theta, eps, B, 1, hidden, Hq, Hkv, head_dim, cache_len, 1,
-                      Lmax, Lmax, 1, 0, q, k_cache, v_cache, s)))
+    if ((rc = run_qkv(*st, x, Wqkv, q_norm_w, k_norm_w, rope_theta, eps, rotary_dim, B, 1, hidden, Hq, Hkv, head_dim,
+                      cache_len, 1, Lmax, Lmax, 1, 0, q, k_cache, v_cache, s)))
         return rc;
     if ((rc = run_decode_attn(*st, q, k_cache, v_cache, cache_len, 1, B, Hq, Hkv, head_dim, Lmax, attn, part, sp, s)))
         return rc;
@@ -584,9 +602,9 @@ int gqa_attention_cached(const gqa_bf16 *q, const gqa_bf16 *k_cache, const gqa_b
                          Lmax, cache_len, 1);
 }
 
-int gqa_attn_prefill_cached(const gqa_bf16 *x, const gqa_bf16 *Wqkv, const gqa_bf16 *Wo, const gqa_bf16 *q_norm_w,
-                            const gqa_bf16 *k_norm_w, float rope_theta, float eps, int B, int S, int hidden, int Hq,
-                            int Hkv, int head_dim, int causal, gqa_bf16 *k_cache, gqa_bf16 *v_cache,
+int gqa_attn_prefill_cached_rd(const gqa_bf16 *x, const gqa_bf16 *Wqkv, const gqa_bf16 *Wo, const gqa_bf16 *q_norm_w,
+                            const gqa_bf16 *k_norm_w, float rope_theta, float eps, int rotary_dim, int B, int S,
+                            int hidden, int Hq, int Hkv, int head_dim, int causal, gqa_bf16 *k_cache, gqa_bf16 *v_cache,
                             const int *cache_len, int Lmax, gqa_bf16 *out, void *workspace, size_t workspace_bytes,
                             void *stream)
 {
@@ -598,6 +616,7 @@ int gqa_attn_prefill_cached(const gqa_bf16 *x, const gqa_bf16 *Wqkv, const gqa_b
         !aligned16(out))
         return fail(GQA_ERR_ARG, "tensor pointers must be 16-byte aligned");
     if (!(rope_theta > 0.0f) || !(eps >= 0.0f)) return fail(GQA_ERR_ARG, "rope_theta must be > 0 and eps >= 0");
+    if ((rc = check_rotary(rotary_dim, head_dim))) return rc;
     const size_t nx = (size_t)B * S * hidden * 2;
     if (overlap(out, nx, x, nx)) return fail(GQA_ERR_ARG, "out must not overlap x");
     const size_t need = gqa_attn_prefill_cached_workspace_size(B, S, Hq, head_dim);
@@ -612,12 +631,59 @@ int gqa_attn_prefill_cached(const gqa_bf16 *x, const gqa_bf16 *Wqkv, const gqa_b
     gqa_bf16 *attn = (gqa_bf16 *)(ws + need / 2);
     cudaStream_t s = (cudaStream_t)stream;
     // K/V of the new tokens go straight into the cache at slots cache_len[b] + t
-    if ((rc = run_qkv(*st, x, Wqkv, q_norm_w, k_norm_w, rope_theta, eps, B, S, hidden, Hq, Hkv, head_dim, cache_len,
-                      S, Lmax, Lmax, 0, 0, q, k_cache, v_cache, s)))
+    if ((rc = run_qkv(*st, x, Wqkv, q_norm_w, k_norm_w, rope_theta, eps, rotary_dim, B, S, hidden, Hq, Hkv, head_dim,
+                      cache_len, S, Lmax, Lmax, 0, 0, q, k_cache, v_cache, s)))
         return rc;
     if ((rc = run_attention(*st, q, k_cache, v_cache, B, S, Hq, Hkv, head_dim, causal, attn, s, Lmax, cache_len, 1)))
         return rc;
     return run_oproj(*st, attn, Wo, x, B * S, hidden, Hq * head_dim, out, s);
+}
+
+// ------------------------------------------- full rotary (rotary_dim = head_dim)
+
+int gqa_qkv_proj(const gqa_bf16 *x, const gqa_bf16 *Wqkv, const gqa_bf16 *q_norm_w, const gqa_bf16 *k_norm_w,
+                 float rope_theta, float eps, int B, int S, int hidden, int Hq, int Hkv, int head_dim, gqa_f16 *q_out,
+                 gqa_f16 *k_out, gqa_f16 *v_out, void *stream)
+{
+    return gqa_qkv_proj_rd(x, Wqkv, q_norm_w, k_norm_w, rope_theta, eps, head_dim, B, S, hidden, Hq, Hkv, head_dim,
+                           q_out, k_out, v_out, stream);
+}
+
+int gqa_attn_forward_ex(const gqa_bf16 *x, const gqa_bf16 *Wqkv, const gqa_bf16 *Wo, const gqa_bf16 *q_norm_w,
+                        const gqa_bf16 *k_norm_w, float rope_theta, float eps, int B, int S, int hidden, int Hq,
+                        int Hkv, int head_dim, int causal, gqa_bf16 *out, void *workspace, size_t workspace_bytes,
+                        void *stream)
+{
+    return gqa_attn_forward_rd(x, Wqkv, Wo, q_norm_w, k_norm_w, rope_theta, eps, head_dim, B, S, hidden, Hq, Hkv,
+                               head_dim, causal, out, workspace, workspace_bytes, stream);
+}
+
+int gqa_decode_qkv(const gqa_bf16 *x, const gqa_bf16 *Wqkv, const gqa_bf16 *q_norm_w, const gqa_bf16 *k_norm_w,
+                   float rope_theta, float eps, int B, int hidden, int Hq, int Hkv, int head_dim, gqa_bf16 *k_cache,
+                   gqa_bf16 *v_cache, const int *cache_len, int Lmax, gqa_f16 *q_out, void *stream)
+{
+    return gqa_decode_qkv_rd(x, Wqkv, q_norm_w, k_norm_w, rope_theta, eps, head_dim, B, hidden, Hq, Hkv, head_dim,
+                             k_cache, v_cache, cache_len, Lmax, q_out, stream);
+}
+
+int gqa_attn_decode(const gqa_bf16 *x, const gqa_bf16 *Wqkv, const gqa_bf16 *Wo, const gqa_bf16 *q_norm_w,
+                    const gqa_bf16 *k_norm_w, float rope_theta, float eps, int B, int hidden, int Hq, int Hkv,
+                    int head_dim, gqa_bf16 *k_cache, gqa_bf16 *v_cache, const int *cache_len, int Lmax,
+                    gqa_bf16 *out, void *workspace, size_t workspace_bytes, void *stream)
+{
+    return gqa_attn_decode_rd(x, Wqkv, Wo, q_norm_w, k_norm_w, rope_theta, eps, head_dim, B, hidden, Hq, Hkv, head_dim,
+                              k_cache, v_cache, cache_len, Lmax, out, workspace, workspace_bytes, stream);
+}
+
+int gqa_attn_prefill_cached(const gqa_bf16 *x, const gqa_bf16 *Wqkv, const gqa_bf16 *Wo, const gqa_bf16 *q_norm_w,
+                            const gqa_bf16 *k_norm_w, float rope_theta, float eps, int B, int S, int hidden, int Hq,
+                            int Hkv, int head_dim, int causal, gqa_bf16 *k_cache, gqa_bf16 *v_cache,
+                            const int *cache_len, int Lmax, gqa_bf16 *out, void *workspace, size_t workspace_bytes,
+                            void *stream)
+{
+    return gqa_attn_prefill_cached_rd(x, Wqkv, Wo, q_norm_w, k_norm_w, rope_theta, eps, head_dim, B, S, hidden, Hq, Hkv,
+                                      head_dim, causal, k_cache, v_cache, cache_len, Lmax, out, workspace,
+                                      workspace_bytes, stream);
 }
 
 // ---------------------------------------------------------------- accounting

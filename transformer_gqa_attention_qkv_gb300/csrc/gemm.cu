@@ -89,6 +89,74 @@ DEVI void store32(uint16_t *dst, const float *v, bool f16, bool &clamped)
     }
 }
 
+// Normalised (x * rinv * w) head row of a Q or K head, rotated on its first
+// RD features (rotate-half pairs (i, i + RD/2), (cos, sin) of angle
+// pos * theta^(-2i/RD) from cs[i]) and stored; features [RD, D) are only
+// normalised.  RD is D, D/2, D/4 or 0; when RD/2 is below 32 the pairs lie
+// inside the first 32 columns and are formed in registers.
+template <int D, int RD>
+DEVI void rope_store(uint32_t col, uint16_t *dst, float rinv, bool has_norm, const float *w, const float2 *cs,
+                     bool row_ok, bool f16, bool &clamped)
+{
+    auto nrm = [&](float x, int c) { return has_norm ? x * rinv * w[c] : x * rinv; };
+    int done = 0;  // columns [0, done) are stored
+    if constexpr (RD >= 64) {
+#pragma unroll 1
+        for (int c = 0; c < RD / 2; c += 32) {
+            uint32_t r1[32], r2[32];
+            tmem_ld32(col + c, r1);
+            tmem_ld32(col + c + RD / 2, r2);
+            float y1[32], y2[32];
+#pragma unroll
+            for (int i = 0; i < 32; i += 2) {
+                const float4 t = __ldg(reinterpret_cast<const float4 *>(cs + c + i));  // (cos, sin) x 2
+#pragma unroll
+                for (int k = 0; k < 2; ++k) {
+                    const float co = k ? t.z : t.x, si = k ? t.w : t.y;
+                    const float x1 = nrm(__uint_as_float(r1[i + k]), c + i + k);
+                    const float x2 = nrm(__uint_as_float(r2[i + k]), c + i + k + RD / 2);
+                    y1[i + k] = x1 * co - x2 * si;
+                    y2[i + k] = x2 * co + x1 * si;
+                }
+            }
+            if (row_ok) {
+                store32(dst + c, y1, f16, clamped);
+                store32(dst + c + RD / 2, y2, f16, clamped);
+            }
+        }
+        done = RD;
+    } else if constexpr (RD > 0) {
+        static_assert(RD == 16 || RD == 32, "pairs inside the first 32 columns");
+        uint32_t r[32];
+        tmem_ld32(col, r);
+        float y[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) y[i] = nrm(__uint_as_float(r[i]), i);
+#pragma unroll
+        for (int i = 0; i < RD / 2; i += 2) {
+            const float4 t = __ldg(reinterpret_cast<const float4 *>(cs + i));
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+                const float co = k ? t.z : t.x, si = k ? t.w : t.y;
+                const float x1 = y[i + k], x2 = y[i + k + RD / 2];
+                y[i + k] = x1 * co - x2 * si;
+                y[i + k + RD / 2] = x2 * co + x1 * si;
+            }
+        }
+        if (row_ok) store32(dst, y, f16, clamped);
+        done = 32;
+    }
+#pragma unroll 1
+    for (int c = done; c < D; c += 32) {  // features past the rotary width
+        uint32_t r[32];
+        tmem_ld32(col + c, r);
+        float y[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) y[i] = nrm(__uint_as_float(r[i]), c + i);
+        if (row_ok) store32(dst + c, y, f16, clamped);
+    }
+}
+
 // Epilogue of one QKV tile row: BN columns = BN/D whole heads.
 template <int BN, int D>
 DEVI void epilogue_qkv(const GemmParams &P, uint32_t tcol, int m, int n0, bool row_ok, const float *s_norm)
@@ -165,34 +233,15 @@ DEVI void epilogue_qkv(const GemmParams &P, uint32_t tcol, int m, int n0, bool r
             rinv = 1.0f / sqrtf(ss * (1.0f / D) + e.eps);
         }
         const float *w = s_norm + (kind == 0 ? 0 : 128);
-        const float2 *cs = e.rope + (size_t)(row_ok ? pos : 0) * (D / 2);
-#pragma unroll 1
-        for (int c = 0; c < D / 2; c += 32) {
-            uint32_t r1[32], r2[32];
-            tmem_ld32(col + c, r1);
-            tmem_ld32(col + c + D / 2, r2);
-            float y1[32], y2[32];
-#pragma unroll
-            for (int i = 0; i < 32; i += 2) {
-                const float4 t = __ldg(reinterpret_cast<const float4 *>(cs + c + i));  // (cos, sin) x 2
-#pragma unroll
-                for (int k = 0; k < 2; ++k) {
-                    const float co = k ? t.z : t.x, si = k ? t.w : t.y;
-                    float x1 = __uint_as_float(r1[i + k]) * rinv;
-                    float x2 = __uint_as_float(r2[i + k]) * rinv;
-                    if (has_norm) {
-                        x1 *= w[c + i + k];
-                        x2 *= w[c + i + k + D / 2];
-                    }
-                    y1[i + k] = x1 * co - x2 * si;
-                    y2[i + k] = x2 * co + x1 * si;
-                }
-            }
-            if (row_ok) {
-                store32(dst + c, y1, f16, clamped);
-                store32(dst + c + D / 2, y2, f16, clamped);
-            }
-        }
+        const int p = row_ok ? pos : 0;
+        if (e.rd == D)
+            rope_store<D, D>(col, dst, rinv, has_norm, w, e.rope + (size_t)p * (D / 2), row_ok, f16, clamped);
+        else if (e.rd == D / 2)
+            rope_store<D, D / 2>(col, dst, rinv, has_norm, w, e.rope + (size_t)p * (D / 4), row_ok, f16, clamped);
+        else if (e.rd == D / 4)
+            rope_store<D, D / 4>(col, dst, rinv, has_norm, w, e.rope + (size_t)p * (D / 8), row_ok, f16, clamped);
+        else
+            rope_store<D, 0>(col, dst, rinv, has_norm, w, nullptr, row_ok, f16, clamped);
     }
     if (clamped) atomicOr(P.err, kErrRange);
 }

@@ -24,7 +24,8 @@ struct QkvEpilogue {
     int kv_seq;            // sequence extent of k_out / v_out (S, or Lmax for decode)
     const uint16_t *q_norm_w, *k_norm_w;  // [d] bf16, or both NULL
     float eps;
-    const float2 *rope;    // [rope_rows][d/2] (cos, sin)
+    int rd;                // rotary width: d, d/2, d/4 or 0 (RoPE on features [0, rd))
+    const float2 *rope;    // [rope_rows][rd/2] (cos, sin of pos * theta^(-2i/rd)); NULL when rd = 0
     int rope_rows;
     int q_f16;             // 1: Q stored as binary16 (clamped, flagged); 0: bf16
     int kv_f16;            // 1: K and V stored as binary16 (clamped, flagged); 0: bf16
