@@ -27,6 +27,7 @@ _u16p = ctypes.POINTER(ctypes.c_uint16)
 _f64p = ctypes.POINTER(ctypes.c_double)
 _i64p = ctypes.POINTER(ctypes.c_long)
 _i32p = ctypes.POINTER(ctypes.c_int)
+_u8p = ctypes.POINTER(ctypes.c_uint8)
 _L = ctypes.c_long
 _D = ctypes.c_double
 _I = ctypes.c_int
@@ -88,6 +89,18 @@ def _load():
     lib.oracle_decode.argtypes = [_u16p, _u16p, _u16p, _u16p, _u16p, _D, _D,
                                   _L, _L, _L, _L, _L, _u16p, _u16p, _i32p, _L,
                                   _f64p, _f64p, _f64p, _f64p, _f64p, _I]
+    _u8p = ctypes.POINTER(ctypes.c_uint8)
+    lib.oracle_e4m3_decode.restype = None
+    lib.oracle_e4m3_decode.argtypes = [_u8p, _L, _f64p]
+    lib.oracle_e4m3_encode.restype = None
+    lib.oracle_e4m3_encode.argtypes = [_f64p, _L, _u8p]
+    lib.oracle_decode_attention_stage_fp8.restype = _I
+    lib.oracle_decode_attention_stage_fp8.argtypes = [_u16p, _I, _u8p, _u8p, _D, _D, _i32p,
+                                                      _L, _L, _L, _L, _L, _f64p, _I]
+    lib.oracle_decode_fp8.restype = _I
+    lib.oracle_decode_fp8.argtypes = [_u16p, _u16p, _u16p, _u16p, _u16p, _D, _D,
+                                      _L, _L, _L, _L, _L, _u8p, _u8p, _D, _D, _i32p, _L,
+                                      _f64p, _f64p, _f64p, _f64p, _u8p, _u8p, _f64p, _I]
     # the *_rd forms take the rotary width (reading R16) after eps
     lib.oracle_rope_rows_rd.restype = _I
     lib.oracle_rope_rows_rd.argtypes = [_f64p, _L, _L, _L, _f64p, _D, _f64p]
@@ -316,3 +329,70 @@ def decode(x, Wqkv, Wo, q_norm_w, k_norm_w, rope_theta, eps, B, hidden, Hq, Hkv,
                                  Lmax, _pf(out), _pf(q), _pf(kn_), _pf(vn_), _pf(a),
                                  threads or default_threads()), "decode")
     return {"out": out, "q": q, "k": kn_, "v": vn_, "attn": a}
+
+
+# ------------------------------------------------------------- FP8 KV cache (reading R17)
+
+def _codes(a):
+    """uint8 E4M3 codes: a numpy uint8 array or a torch uint8 / float8_e4m3fn tensor."""
+    if isinstance(a, np.ndarray):
+        assert a.dtype == np.uint8
+        return np.ascontiguousarray(a)
+    import torch
+    t = a.detach().cpu().contiguous()
+    if t.dtype != torch.uint8:
+        t = t.view(torch.uint8)
+    return t.numpy()
+
+
+def e4m3_decode(codes) -> np.ndarray:
+    """E4M3 codes -> float64 (exact)."""
+    c = _codes(codes)
+    flat = c.reshape(-1)
+    out = np.empty(flat.shape[0])
+    _load().oracle_e4m3_decode(flat.ctypes.data_as(_u8p), flat.shape[0], _pf(out))
+    return out.reshape(c.shape)
+
+
+def e4m3_encode(x) -> np.ndarray:
+    """float64 values -> nearest E4M3 codes (ties to even, saturating at +-448)."""
+    a = np.ascontiguousarray(np.asarray(x, dtype=np.float64))
+    flat = a.reshape(-1)
+    out = np.empty(flat.shape[0], dtype=np.uint8)
+    _load().oracle_e4m3_encode(_pf(flat), flat.shape[0], out.ctypes.data_as(_u8p))
+    return out.reshape(a.shape)
+
+
+def decode_attention_stage_fp8(q, k_codes, v_codes, k_scale, v_scale, kv_len, B, Hq, Hkv, d, Lmax,
+                               threads=None):
+    """attn [B, Hq*d] of q [B,Hq,d] (bf16 or float16) over keys [0, kv_len[b])
+    of FP8 caches [B,Hkv,Lmax,d] worth code * scale."""
+    out = np.empty((B, Hq * d))
+    kl = np.ascontiguousarray(np.asarray(kv_len, dtype=np.int32))
+    qb, kb, vb = _bits(q, True), _codes(k_codes), _codes(v_codes)
+    _check(_load().oracle_decode_attention_stage_fp8(_p16(qb), int(_is_f16(q)), kb.ctypes.data_as(_u8p),
+                                                     vb.ctypes.data_as(_u8p), k_scale, v_scale,
+                                                     kl.ctypes.data_as(_i32p), B, Hq, Hkv, d, Lmax,
+                                                     _pf(out), threads or default_threads()),
+           "decode_attention_stage_fp8")
+    return out
+
+
+def decode_fp8(x, Wqkv, Wo, q_norm_w, k_norm_w, rope_theta, eps, B, hidden, Hq, Hkv, d,
+               k_codes, v_codes, k_scale, v_scale, cache_len, Lmax, threads=None):
+    """One decode step over FP8 caches.  Returns dict out [B,hidden], q
+    [B,Hq,d], k/v [B,Hkv,d] (the new token's, before quantisation), k_code /
+    v_code [B,Hkv,d] (uint8, as appended), attn [B,Hq*d]; the caches are read,
+    not modified."""
+    out = np.empty((B, hidden)); q = np.empty((B, Hq, d))
+    kn_ = np.empty((B, Hkv, d)); vn_ = np.empty((B, Hkv, d)); a = np.empty((B, Hq * d))
+    kc_ = np.empty((B, Hkv, d), dtype=np.uint8); vc_ = np.empty((B, Hkv, d), dtype=np.uint8)
+    cl = np.ascontiguousarray(np.asarray(cache_len, dtype=np.int32))
+    xb, wb, ob, qn, kn = _bits(x), _bits(Wqkv), _bits(Wo), _bits(q_norm_w), _bits(k_norm_w)
+    kb, vb = _codes(k_codes), _codes(v_codes)
+    _check(_load().oracle_decode_fp8(_p16(xb), _p16(wb), _p16(ob), _p16(qn), _p16(kn), rope_theta, eps,
+                                     B, hidden, Hq, Hkv, d, kb.ctypes.data_as(_u8p), vb.ctypes.data_as(_u8p),
+                                     k_scale, v_scale, cl.ctypes.data_as(_i32p), Lmax, _pf(out), _pf(q),
+                                     _pf(kn_), _pf(vn_), kc_.ctypes.data_as(_u8p), vc_.ctypes.data_as(_u8p),
+                                     _pf(a), threads or default_threads()), "decode_fp8")
+    return {"out": out, "q": q, "k": kn_, "v": vn_, "k_code": kc_, "v_code": vc_, "attn": a}

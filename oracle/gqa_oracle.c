@@ -41,6 +41,11 @@
  *      R4 ([NeoX] "Scaling and RoPE": RoPE is built from the effective
  *      head_dim, subject to the rotary_pct setting and an even dimension).
  *      The functions named *_rd take rd; the others use rd = d.
+ *   R17 FP8 KV cache (decode): one OCP FP8 E4M3 code per cached element times
+ *      one scale per tensor (k_scale, v_scale); a value enters as the nearest
+ *      code to value / scale, ties to even, saturating at +-448; the new
+ *      token's key and value are appended as codes and attended like the
+ *      rest ("Head Dimension" article, §5.2: FP8 for the K, V cache).
  */
 #include <math.h>
 #include <stdint.h>
@@ -244,17 +249,24 @@ typedef struct {
     const uint16_t *vb;
     const double *kd;     /* double keys (used for keys >= n_bf16), or NULL */
     const double *vd;
-    long n_bf16;          /* keys [0, n_bf16) come from kb/vb, the rest from kd/vd */
+    long n_bf16;          /* keys [0, n_bf16) come from kb/vb (or k8/v8), the rest from kd/vd */
     int f16;              /* kb/vb hold binary16 (1) or bf16 (0) patterns */
+    const uint8_t *k8;    /* FP8 E4M3 keys and values (used instead of kb/vb when k8 != NULL), */
+    const uint8_t *v8;    /* each code worth e4m3(code) * ks (keys) or * vs (values) */
+    double ks, vs;
 } kv_src;
+
+static double e4m3(uint8_t code);
 
 static double key_at(const kv_src *s, long u, long c, long d)
 {
-    return (u < s->n_bf16) ? w16(s->kb[u * d + c], s->f16) : s->kd[(u - s->n_bf16) * d + c];
+    if (u >= s->n_bf16) return s->kd[(u - s->n_bf16) * d + c];
+    return s->k8 ? e4m3(s->k8[u * d + c]) * s->ks : w16(s->kb[u * d + c], s->f16);
 }
 static double val_at(const kv_src *s, long u, long c, long d)
 {
-    return (u < s->n_bf16) ? w16(s->vb[u * d + c], s->f16) : s->vd[(u - s->n_bf16) * d + c];
+    if (u >= s->n_bf16) return s->vd[(u - s->n_bf16) * d + c];
+    return s->v8 ? e4m3(s->v8[u * d + c]) * s->vs : w16(s->vb[u * d + c], s->f16);
 }
 
 static int attend_row(const double *q, const kv_src *src, long n_vis, long d, double *o)
@@ -726,4 +738,183 @@ int oracle_prefill_cached(const uint16_t *x, const uint16_t *Wqkv, const uint16_
     return oracle_prefill_cached_rd(x, Wqkv, Wo, q_norm_w, k_norm_w, rope_theta, eps, d, B, S, hidden, Hq,
                                     Hkv, d, causal, k_cache, v_cache, p0, Lmax, out, k_new, v_new, attn_out,
                                     nthreads);
+}
+
+/* ------------------------------------------------------------------------ */
+/* FP8 KV cache for decode.                                                  */
+/* ------------------------------------------------------------------------ */
+
+/* The pages ask only for "FP8 precision for the K, V cache" ("Head Dimension"
+ * article, §5.2).  Reading R17: every cached key and value is one OCP FP8
+ * E4M3 code (1 sign bit, 4 exponent bits with bias 7, 3 mantissa bits; no
+ * infinities; exponent field 15 with mantissa 7 is NaN; largest finite 448;
+ * subnormals m * 2^-9) times one scale per tensor (k_scale for keys, v_scale
+ * for values).  A value x enters the cache as the code nearest to x / scale
+ * (ties to even mantissa), values beyond 448 in magnitude saturating to
+ * +-448. */
+
+/* E4M3 code -> double (exact). */
+static double e4m3(uint8_t code)
+{
+    int sign = code >> 7, e = (code >> 3) & 15, m = code & 7;
+    double v;
+    if (e == 15 && m == 7) return NAN;
+    if (e == 0) v = ldexp((double)m, -9);
+    else v = ldexp(1.0 + m / 8.0, e - 7);
+    return sign ? -v : v;
+}
+
+/* double -> nearest E4M3 code, ties to even, saturating at +-448. */
+static uint8_t e4m3_code(double x)
+{
+    if (isnan(x)) return 0x7F;
+    uint8_t sign = (x < 0.0 || (x == 0.0 && signbit(x))) ? 0x80 : 0;
+    double a = fabs(x);
+    if (a >= 448.0) return sign | 0x7E;
+    if (a < ldexp(1.0, -6)) {                      /* subnormal: a multiple of 2^-9 */
+        double m = nearbyint(ldexp(a, 9));          /* 0..8; 8 is the smallest normal */
+        return sign | (uint8_t)m;                   /* code 8 = exponent field 1, mantissa 0 */
+    }
+    int e;
+    frexp(a, &e);                                   /* a = f * 2^e, f in [0.5, 1) */
+    e -= 1;                                         /* a in [2^e, 2^(e+1)) */
+    double m = nearbyint((ldexp(a, -e) - 1.0) * 8.0);  /* 0..8 */
+    if (m == 8.0) {
+        m = 0.0;
+        e += 1;
+    }
+    if (e > 8 || (e == 8 && m > 6.0)) return sign | 0x7E;  /* rounded past 448 */
+    return sign | (uint8_t)(((e + 7) << 3) | (int)m);
+}
+
+void oracle_e4m3_decode(const uint8_t *code, long n, double *out)
+{
+    for (long i = 0; i < n; ++i) out[i] = e4m3(code[i]);
+}
+
+void oracle_e4m3_encode(const double *x, long n, uint8_t *code)
+{
+    for (long i = 0; i < n; ++i) code[i] = e4m3_code(x[i]);
+}
+
+/* Decode attention over keys [0, kv_len[b]) of FP8 caches [B, Hkv, Lmax, d]
+ * (reading R17).  q [B,Hq,d] bf16 or binary16 (q_f16); attn [B, Hq*d]. */
+int oracle_decode_attention_stage_fp8(const uint16_t *q, int q_f16, const uint8_t *k_cache,
+                                      const uint8_t *v_cache, double k_scale, double v_scale,
+                                      const int *kv_len, long B, long Hq, long Hkv, long d, long Lmax,
+                                      double *attn, int nthreads)
+{
+    if (!q || !k_cache || !v_cache || !kv_len || !attn) return ORACLE_EARG;
+    if (B <= 0 || Hq <= 0 || Hkv <= 0 || d <= 0 || d > 1024 || Hq % Hkv || Lmax <= 0) return ORACLE_EARG;
+    for (long b = 0; b < B; ++b)
+        if (kv_len[b] <= 0 || kv_len[b] > Lmax) return ORACLE_EARG;
+    long G = Hq / Hkv;
+    int err = ORACLE_OK;
+    set_threads(nthreads);
+#pragma omp parallel for collapse(2) schedule(dynamic, 1)
+    for (long b = 0; b < B; ++b) {
+        for (long j = 0; j < Hq; ++j) {
+            long g = j / G;
+            double qv[1024];
+            for (long c = 0; c < d; ++c) qv[c] = w16(q[(b * Hq + j) * d + c], q_f16);
+            kv_src src = {NULL, NULL, NULL, NULL, kv_len[b], 0,
+                          k_cache + (b * Hkv + g) * Lmax * d, v_cache + (b * Hkv + g) * Lmax * d,
+                          k_scale, v_scale};
+            int e = attend_row(qv, &src, kv_len[b], d, attn + b * Hq * d + j * d);
+            if (e) err = e;
+        }
+    }
+    return err;
+}
+
+/* The decode step over FP8 caches (readings R17, R4): as oracle_decode, but
+ * the cached entries [0, p) are E4M3 codes times k_scale / v_scale, and the
+ * new token's key and value enter the cache as codes (e4m3_code of k / k_scale
+ * and v / v_scale), so the query attends to their dequantised values like to
+ * every other entry.  The caches are read, not modified.  Optional outputs:
+ * q_new [B,Hq,d], k_new/v_new [B,Hkv,d] before quantisation, k_code/v_code
+ * [B,Hkv,d] the codes appended, attn [B,Hq*d]. */
+int oracle_decode_fp8(const uint16_t *x, const uint16_t *Wqkv, const uint16_t *Wo,
+                      const uint16_t *q_norm_w, const uint16_t *k_norm_w,
+                      double rope_theta, double eps,
+                      long B, long hidden, long Hq, long Hkv, long d,
+                      const uint8_t *k_cache, const uint8_t *v_cache, double k_scale, double v_scale,
+                      const int *cache_len, long Lmax, double *out, double *q_new, double *k_new,
+                      double *v_new, uint8_t *k_code, uint8_t *v_code, double *attn_out, int nthreads)
+{
+    if (!x || !Wqkv || !Wo || !k_cache || !v_cache || !cache_len || !out) return ORACLE_EARG;
+    if (B <= 0 || hidden <= 0 || Hq <= 0 || Hkv <= 0 || d <= 0 || (d & 1) || d > 1024) return ORACLE_EARG;
+    if (Hq % Hkv || !(k_scale > 0.0) || !(v_scale > 0.0)) return ORACLE_EARG;
+    if ((q_norm_w == NULL) != (k_norm_w == NULL)) return ORACLE_EARG;
+    for (long b = 0; b < B; ++b)
+        if (cache_len[b] < 0 || cache_len[b] + 1 > Lmax) return ORACLE_EARG;
+    long NQ = Hq * d, NKV = Hkv * d, N = NQ + 2 * NKV, G = Hq / Hkv;
+    int err = ORACLE_OK;
+    set_threads(nthreads);
+    double *rows = (double *)malloc((size_t)(B * N) * sizeof(double));
+    double *deq = (double *)malloc((size_t)(B * 2 * NKV) * sizeof(double));  /* new K, V dequantised */
+    uint8_t *codes = (uint8_t *)malloc((size_t)(B * 2 * NKV));
+    double *arows = (double *)malloc((size_t)(B * NQ) * sizeof(double));
+    if (!rows || !deq || !codes || !arows) { err = ORACLE_ENOMEM; goto done; }
+
+#pragma omp parallel for schedule(dynamic, 1)
+    for (long b = 0; b < B; ++b) {
+        double *row = rows + b * N;
+        double p = (double)cache_len[b];
+        linear_row(x + b * hidden, Wqkv, 0, N, hidden, row);
+        for (long j = 0; j < Hq; ++j) {
+            if (q_norm_w) rmsnorm_head(row + j * d, d, q_norm_w, eps);
+            rope_head(row + j * d, d, p, rope_theta);
+        }
+        for (long g = 0; g < Hkv; ++g) {
+            if (k_norm_w) rmsnorm_head(row + NQ + g * d, d, k_norm_w, eps);
+            rope_head(row + NQ + g * d, d, p, rope_theta);
+        }
+        /* the new K and V as they enter the cache */
+        for (long i = 0; i < NKV; ++i) {
+            uint8_t ck = e4m3_code(row[NQ + i] / k_scale), cv = e4m3_code(row[NQ + NKV + i] / v_scale);
+            codes[b * 2 * NKV + i] = ck;
+            codes[b * 2 * NKV + NKV + i] = cv;
+            deq[b * 2 * NKV + i] = e4m3(ck) * k_scale;
+            deq[b * 2 * NKV + NKV + i] = e4m3(cv) * v_scale;
+        }
+    }
+
+#pragma omp parallel for collapse(2) schedule(dynamic, 1)
+    for (long b = 0; b < B; ++b) {
+        for (long j = 0; j < Hq; ++j) {
+            long g = j / G;
+            kv_src src = {NULL, NULL, deq + b * 2 * NKV + g * d, deq + b * 2 * NKV + NKV + g * d,
+                          cache_len[b], 0, k_cache + (b * Hkv + g) * Lmax * d,
+                          v_cache + (b * Hkv + g) * Lmax * d, k_scale, v_scale};
+            int e = attend_row(rows + b * N + j * d, &src, cache_len[b] + 1, d, arows + b * NQ + j * d);
+            if (e) err = e;
+        }
+    }
+
+#pragma omp parallel for schedule(dynamic, 1)
+    for (long b = 0; b < B; ++b) {
+        for (long n = 0; n < hidden; ++n) {
+            const uint16_t *w = Wo + n * NQ;
+            double acc = 0.0;
+            for (long k = 0; k < NQ; ++k) acc += arows[b * NQ + k] * bf(w[k]);
+            out[b * hidden + n] = bf(x[b * hidden + n]) + acc;
+        }
+    }
+
+    for (long b = 0; b < B; ++b) {
+        const double *row = rows + b * N;
+        if (q_new) memcpy(q_new + b * NQ, row, (size_t)NQ * sizeof(double));
+        if (k_new) memcpy(k_new + b * NKV, row + NQ, (size_t)NKV * sizeof(double));
+        if (v_new) memcpy(v_new + b * NKV, row + NQ + NKV, (size_t)NKV * sizeof(double));
+        if (k_code) memcpy(k_code + b * NKV, codes + b * 2 * NKV, (size_t)NKV);
+        if (v_code) memcpy(v_code + b * NKV, codes + b * 2 * NKV + NKV, (size_t)NKV);
+        if (attn_out) memcpy(attn_out + b * NQ, arows + b * NQ, (size_t)NQ * sizeof(double));
+    }
+done:
+    free(rows);
+    free(deq);
+    free(codes);
+    free(arows);
+    return err;
 }

@@ -656,3 +656,91 @@ def test_partial_rotary_rejects_bad_widths():
     for rd in (-2, 3, 10):
         with pytest.raises(RuntimeError):
             oracle.rope_rows(v, [0.0], 1e4, rotary_dim=rd)
+
+
+# ----------------------------------------------------------------- FP8 KV cache (reading R17)
+
+def test_e4m3_decode_matches_library_on_every_code():
+    """All 256 E4M3 codes widen to the values torch's float8_e4m3fn gives
+    (NaN for S.1111.111, no infinities)."""
+    codes = np.arange(256, dtype=np.uint8)
+    got = oracle.e4m3_decode(codes)
+    ref = torch.from_numpy(codes).view(torch.float8_e4m3fn).double().numpy()
+    assert np.array_equal(np.isnan(got), np.isnan(ref)) and np.isnan(got).sum() == 2
+    np.testing.assert_array_equal(got[~np.isnan(got)], ref[~np.isnan(ref)])
+
+
+def test_e4m3_encode_matches_library_and_saturates():
+    """In range, the nearest code with ties to even equals torch's conversion;
+    beyond +-448 the code saturates to +-448 (closed forms)."""
+    rng = np.random.default_rng(41)
+    x = rng.standard_normal(200000) * np.exp(rng.uniform(-14.0, 6.0, 200000))
+    x = x[np.abs(x) < 448.0]
+    ref = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    np.testing.assert_array_equal(oracle.e4m3_encode(x), ref)
+    # ties: 1 + 1/16 lies halfway between 1 and 1.125 -> even mantissa (1.0);
+    # 1 + 3/16 -> 1.25; 2^-10 halfway between 0 and the smallest subnormal -> 0
+    got = oracle.e4m3_decode(oracle.e4m3_encode([1.0625, 1.1875, 2.0 ** -10, 3 * 2.0 ** -10, -1.0625]))
+    np.testing.assert_array_equal(got, [1.0, 1.25, 0.0, 2.0 ** -8, -1.0])
+    sat = oracle.e4m3_encode([448.0, 463.99, 464.0, 1e30, -1e30, float("inf")])
+    np.testing.assert_array_equal(sat, [0x7E, 0x7E, 0x7E, 0x7E, 0xFE, 0x7E])
+    assert oracle.e4m3_encode([float("nan")])[0] == 0x7F
+
+
+def test_fp8_decode_attention_equals_bf16_path_on_exact_codes():
+    """With power-of-two scales every dequantised entry is a bf16 value, so
+    attention over the FP8 cache equals attention over the bf16 cache holding
+    those values (two independent code paths of the oracle)."""
+    rng = np.random.default_rng(42)
+    B, Hq, Hkv, d, Lmax = 3, 8, 2, 32, 50
+    ks, vs = 2.0 ** -5, 2.0 ** -3
+    kc8 = rng.integers(0, 256, (B, Hkv, Lmax, d), dtype=np.uint8)
+    vc8 = rng.integers(0, 256, (B, Hkv, Lmax, d), dtype=np.uint8)
+    kc8[(kc8 & 0x7F) == 0x7F] = 0x10  # no NaN codes
+    vc8[(vc8 & 0x7F) == 0x7F] = 0x10
+    q = torch.from_numpy(rng.standard_normal((B, Hq, d))).half()
+    lens = [50, 1, 23]
+    got = oracle.decode_attention_stage_fp8(q, kc8, vc8, ks, vs, lens, B, Hq, Hkv, d, Lmax, threads=T)
+    kb = bf16(oracle.e4m3_decode(kc8) * ks)
+    vb = bf16(oracle.e4m3_decode(vc8) * vs)
+    assert np.array_equal(f64(kb).numpy(), oracle.e4m3_decode(kc8) * ks)  # exact in bf16
+    ref = oracle.decode_attention_stage(q, kb, vb, lens, B, Hq, Hkv, d, Lmax, threads=T)
+    np.testing.assert_allclose(got, ref, rtol=1e-13, atol=1e-14)
+
+
+def test_fp8_decode_step_equals_library_composition():
+    """The FP8 decode step: the appended codes are the nearest codes of the new
+    key / value over their scales, and the output is x + SDPA(q, cache with the
+    new entries, all dequantised) @ Wo^T, evaluated with torch in float64."""
+    cfg = _tiny(B=3)
+    t = make_layer_inputs(cfg, seed=43, w_std=0.3)
+    rng = np.random.default_rng(43)
+    B, h, Hq, Hkv, d = cfg.B, cfg.hidden, cfg.Hq, cfg.Hkv, cfg.head_dim
+    Lmax, ks, vs = 30, 0.05, 0.02
+    kc8 = oracle.e4m3_encode(rng.standard_normal((B, Hkv, Lmax, d)) / ks)
+    vc8 = oracle.e4m3_encode(rng.standard_normal((B, Hkv, Lmax, d)) / vs)
+    cl = [0, 7, 29]
+    x1 = t["x"][:, 0].contiguous()
+    got = oracle.decode_fp8(x1, t["Wqkv"], t["Wo"], t["q_norm_w"], t["k_norm_w"], cfg.rope_theta, cfg.eps, B, h,
+                            Hq, Hkv, d, kc8, vc8, ks, vs, cl, Lmax, threads=T)
+    np.testing.assert_array_equal(got["k_code"], oracle.e4m3_encode(got["k"] / ks))
+    np.testing.assert_array_equal(got["v_code"], oracle.e4m3_encode(got["v"] / vs))
+    # the bf16 decode computes the same q, k, v before quantisation
+    ref_bf = oracle.decode(x1, t["Wqkv"], t["Wo"], t["q_norm_w"], t["k_norm_w"], cfg.rope_theta, cfg.eps, B, h,
+                           Hq, Hkv, d, bf16(np.zeros((B, Hkv, Lmax, d))), bf16(np.zeros((B, Hkv, Lmax, d))), cl,
+                           Lmax, threads=T)
+    np.testing.assert_allclose(got["q"], ref_bf["q"], rtol=1e-13, atol=1e-14)
+    np.testing.assert_allclose(got["k"], ref_bf["k"], rtol=1e-13, atol=1e-14)
+    kd = oracle.e4m3_decode(kc8) * ks
+    vd = oracle.e4m3_decode(vc8) * vs
+    for b in range(B):
+        p = cl[b]
+        k = np.concatenate([kd[b, :, :p], (oracle.e4m3_decode(got["k_code"][b]) * ks)[:, None]], axis=1)
+        v = np.concatenate([vd[b, :, :p], (oracle.e4m3_decode(got["v_code"][b]) * vs)[:, None]], axis=1)
+        k = torch.from_numpy(k).repeat_interleave(Hq // Hkv, 0)
+        v = torch.from_numpy(v).repeat_interleave(Hq // Hkv, 0)
+        qb = torch.from_numpy(got["q"][b])[:, None]
+        a = F.scaled_dot_product_attention(qb, k, v)[:, 0].reshape(-1)
+        np.testing.assert_allclose(got["attn"][b], a.numpy(), rtol=1e-11, atol=1e-12)
+        o = f64(t["x"][b, 0]) + F.linear(a, f64(t["Wo"]))
+        np.testing.assert_allclose(got["out"][b], o.numpy(), rtol=1e-11, atol=1e-11)
