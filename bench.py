@@ -59,13 +59,14 @@ def prefill_flops(cfg):
     return {"qkv": qkv, "attn": attn, "oproj": oproj, "total": qkv + attn + oproj}
 
 
-def decode_bytes(cfg):
+def decode_bytes(cfg, kv_elem=2):
     """Algorithmic bytes of one decode step: each cached K/V entry read once
-    (plus the new one), weights read once, x/out, q and the appended K/V."""
+    (plus the new one), weights read once, x/out, q and the appended K/V.
+    kv_elem: bytes per cache element (2 bf16, 1 E4M3)."""
     d, B = cfg.head_dim, cfg.B
-    kv_read = 2 * B * cfg.Hkv * (cfg.cache_len + 1) * d * 2
+    kv_read = 2 * B * cfg.Hkv * (cfg.cache_len + 1) * d * kv_elem
     weights = ((cfg.Hq + 2 * cfg.Hkv) * d * cfg.hidden + cfg.hidden * cfg.Hq * d) * 2
-    act = 2 * B * cfg.hidden * 2 + 2 * B * cfg.Hkv * d * 2
+    act = 2 * B * cfg.hidden * 2 + 2 * B * cfg.Hkv * d * kv_elem
     return {"kv_read": kv_read, "weights": weights, "act": act, "total": kv_read + weights + act}
 
 
@@ -389,7 +390,50 @@ def run_ours(args, world, rank, local):
                            "traffic": recorded_traffic("decode_attention_" + dc.name,
                                                        [CSRC + "decode.cu", CSRC + "ptx.cuh"]),
                            "kernel_ms": round(ams_, 4)}}
-    del dt_, dout, dws
+
+    # ---- the same decode step over E4M3 caches (scale 2^-5: the N(0,1)
+    # cache entries land well inside E4M3's range)
+    f8s = 2.0 ** -5
+    kc8 = (dt_["k_cache"].float() / f8s).to(torch.float8_e4m3fn).view(torch.uint8)
+    vc8 = (dt_["v_cache"].float() / f8s).to(torch.float8_e4m3fn).view(torch.uint8)
+    del dt_["k_cache"], dt_["v_cache"]
+    db8 = decode_bytes(dc, kv_elem=1)
+
+    def dec8():
+        gq.gqa_attn_decode_fp8(dt_["x"], dt_["Wqkv"], dt_["Wo"], dt_["q_norm_w"], dt_["k_norm_w"], dc.rope_theta,
+                               dc.eps, dc.B, dc.hidden, dc.Hq, dc.Hkv, dc.head_dim, kc8, vc8, f8s, f8s,
+                               dt_["cache_len"], dc.lmax, dout, dws, stream)
+
+    def time_it(fn):
+        nonlocal launches
+        ts = []
+        for i in range(args.warmup + args.steps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            flush.zero_()
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            if i >= args.warmup:
+                ts.append(e0.elapsed_time(e1))
+                launches += gq.gqa_last_launch_count()
+        return statistics.mean(ts)
+
+    d8ms = reduce_max(time_it(dec8), world, dev)
+    a8ms = time_it(lambda: gq.gqa_decode_attention_fp8(qd, kc8, vc8, f8s, f8s, kl, dc.B, dc.Hq, dc.Hkv,
+                                                        dc.head_dim, dc.lmax, ad, aws, stream))
+    a8_bytes = db8["kv_read"] + dc.B * dc.Hq * dc.head_dim * 2 * 2
+    a8_ach = a8_bytes / (a8ms * 1e-3) / 1e9
+    decode_fp8 = {"workload": dc.name + " with E4M3 K/V caches (per-tensor scales)",
+                  "value": round(reduce_sum(db8["total"], world, dev) / (d8ms * 1e-3) / 1e9, 1), "unit": "GB/s",
+                  "ms_per_step": round(d8ms, 4), "frac_of_hbm": round(db8["total"] / (d8ms * 1e-3) / 1e9 / hbm, 4),
+                  "bytes_per_step": db8["total"], "speedup_vs_bf16_cache": round(dms / d8ms, 3),
+                  "roofline": {"bound": "hbm", "kernel": "decode_attention_fp8", "achieved": round(a8_ach, 1),
+                               "peak": hbm, "unit": "GB/s", "frac": round(a8_ach / hbm, 4),
+                               "peak_source": f"{peak_src} copy bandwidth", "kernel_ms": round(a8ms, 4)}}
+    if gq.gqa_check_device_error() != 0:
+        raise RuntimeError(gq.gqa_last_error())
+    del dt_, dout, dws, kc8, vc8
 
     # ---- chunked prefill: the last 2048 tokens of a 16384-token Qwen3-32B context
     chunk = None
@@ -449,7 +493,7 @@ def run_ours(args, world, rank, local):
                    "Hkv": cfg.Hkv, "head_dim": cfg.head_dim, "qk_norm": cfg.qk_norm, "rope_theta": cfg.rope_theta,
                    "causal": cfg.causal, "flops_per_step": fl["total"], "parallelism": f"replicas x{world}",
                    "l2": "flushed between steps (2x L2 buffer written outside the timed events)"},
-        "roofline": roofline, "decode": decode, "chunked_prefill": chunk, "e2e": e2e, "cpu_baseline": cpu,
+        "roofline": roofline, "decode": decode, "decode_fp8": decode_fp8, "chunked_prefill": chunk, "e2e": e2e, "cpu_baseline": cpu,
         "gpu_launches": launches, "wall_s": round(wall, 3), "clocks": clk.summary(),
         "step_ms": [round(x, 4) for x in step_ms],
     }
@@ -496,17 +540,25 @@ def run_stage(args, local):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     stream = torch.cuda.current_stream()
-    if args.stage == "decode_attn":
+    if args.stage in ("decode_attn", "decode_attn_fp8"):
         dc = DECODE_CONFIGS["qwen3_8b_decode"]
         t = make_decode_inputs(dc, seed=SEEDS[dc.name], device=str(dev))
         q = torch.randn((dc.B, dc.Hq, dc.head_dim), device=dev).to(torch.float16)
         a = torch.empty((dc.B, dc.Hq * dc.head_dim), dtype=torch.bfloat16, device=dev)
         kl = (t["cache_len"] + 1).to(torch.int32)
         ws = gq.new_workspace(gq.gqa_decode_attention_workspace_size(dc.B, dc.Hq, dc.Hkv, dc.head_dim, dc.lmax), dev)
+        f8s = 2.0 ** -5
+        if args.stage == "decode_attn_fp8":
+            t["k_cache"] = (t["k_cache"].float() / f8s).to(torch.float8_e4m3fn).view(torch.uint8)
+            t["v_cache"] = (t["v_cache"].float() / f8s).to(torch.float8_e4m3fn).view(torch.uint8)
 
         def go():
-            gq.gqa_decode_attention(q, t["k_cache"], t["v_cache"], kl, dc.B, dc.Hq, dc.Hkv, dc.head_dim, dc.lmax,
-                                    a, ws, stream)
+            if args.stage == "decode_attn_fp8":
+                gq.gqa_decode_attention_fp8(q, t["k_cache"], t["v_cache"], f8s, f8s, kl, dc.B, dc.Hq, dc.Hkv,
+                                            dc.head_dim, dc.lmax, a, ws, stream)
+            else:
+                gq.gqa_decode_attention(q, t["k_cache"], t["v_cache"], kl, dc.B, dc.Hq, dc.Hkv, dc.head_dim,
+                                        dc.lmax, a, ws, stream)
         name = dc.name
     else:
         cfg = PREFILL_CONFIGS[args.workload]
@@ -556,7 +608,7 @@ def main(argv=None):
     ap.add_argument("--ref-tokens", type=int, default=256, help="tokens per reference-arm step")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-chunk", action="store_true", help="skip the chunked-prefill measurement")
-    ap.add_argument("--stage", choices=["qkv", "attn", "oproj", "decode_attn"], default=None,
+    ap.add_argument("--stage", choices=["qkv", "attn", "oproj", "decode_attn", "decode_attn_fp8"], default=None,
                     help="launch one stage alone (for profiler captures); prints its time, no benchmark line")
     args = ap.parse_args(argv)
     world, rank, local = dist_setup(args.gpus)

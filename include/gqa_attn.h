@@ -250,6 +250,49 @@ int gqa_decode_attention_noalloc(const gqa_f16 *q, const gqa_bf16 *k_cache, cons
                                  const int *kv_len, int B, int Hq, int Hkv, int head_dim, int Lmax,
                                  gqa_bf16 *attn_out, void *stream);
 
+/* ------------------------------------------------ FP8 (E4M3) KV cache */
+
+/* The decode step with its caches in FP8 ("Head Dimension" article, §5.2:
+ * FP8 precision for the K, V cache).  A cache element is one OCP FP8 E4M3
+ * code (1 sign, 4 exponent bits with bias 7, 3 mantissa bits; largest finite
+ * value 448) and stands for code * k_scale (keys) or code * v_scale (values),
+ * one scale per tensor.  A new key or value is stored as the code nearest to
+ * value / scale (value / scale computed in fp32, ties to even), saturated to
+ * +-448; a saturated or NaN value sets the range flag that
+ * gqa_check_device_error() reports as GQA_ERR_RANGE.  Caches are
+ * [B, Hkv, Lmax, head_dim] codes, half the bytes of bf16 caches; everything
+ * else (arguments, workspace and its size, positions, statuses) is as for
+ * the bf16 functions of the same name without _fp8.  head_dim must be 128
+ * (else GQA_ERR_UNSUPPORTED); k_scale and v_scale must be finite and > 0
+ * (else GQA_ERR_ARG). */
+typedef uint8_t gqa_e4m3; /* one OCP FP8 E4M3 code */
+
+int gqa_attn_decode_fp8(const gqa_bf16 *x, const gqa_bf16 *Wqkv, const gqa_bf16 *Wo,
+                        const gqa_bf16 *q_norm_w, const gqa_bf16 *k_norm_w,
+                        float rope_theta, float eps,
+                        int B, int hidden, int Hq, int Hkv, int head_dim,
+                        gqa_e4m3 *k_cache, gqa_e4m3 *v_cache, float k_scale, float v_scale,
+                        const int *cache_len, int Lmax,
+                        gqa_bf16 *out, void *workspace, size_t workspace_bytes, void *stream);
+
+/* Stage alone: projection, QK-norm and RoPE of the new token, its key and
+ * value appended to the E4M3 caches at slot cache_len[b]; q_out [B, Hq,
+ * head_dim] binary16. */
+int gqa_decode_qkv_fp8(const gqa_bf16 *x, const gqa_bf16 *Wqkv,
+                       const gqa_bf16 *q_norm_w, const gqa_bf16 *k_norm_w,
+                       float rope_theta, float eps,
+                       int B, int hidden, int Hq, int Hkv, int head_dim,
+                       gqa_e4m3 *k_cache, gqa_e4m3 *v_cache, float k_scale, float v_scale,
+                       const int *cache_len, int Lmax, gqa_f16 *q_out, void *stream);
+
+/* Stage alone: split-KV attention of q [B, Hq, head_dim] (binary16) over
+ * keys [0, kv_len[b]) of the E4M3 caches; attn_out [B, Hq*head_dim] bf16;
+ * workspace of gqa_decode_attention_workspace_size(...) bytes. */
+int gqa_decode_attention_fp8(const gqa_f16 *q, const gqa_e4m3 *k_cache, const gqa_e4m3 *v_cache,
+                             float k_scale, float v_scale, const int *kv_len,
+                             int B, int Hq, int Hkv, int head_dim, int Lmax,
+                             gqa_bf16 *attn_out, void *workspace, size_t workspace_bytes, void *stream);
+
 /* ------------------------------------------------------- partial rotary */
 
 /* The same five layer entry points with the rotary width as an argument:

@@ -33,7 +33,7 @@ EXPORTS = (
     "gqa_last_launch_count", "gqa_decode_attention_noalloc",
     "gqa_attn_prefill_cached_workspace_size", "gqa_attn_prefill_cached", "gqa_attention_cached",
     "gqa_attn_forward_rd", "gqa_qkv_proj_rd", "gqa_attn_prefill_cached_rd", "gqa_attn_decode_rd",
-    "gqa_decode_qkv_rd",
+    "gqa_decode_qkv_rd", "gqa_attn_decode_fp8", "gqa_decode_qkv_fp8", "gqa_decode_attention_fp8",
 )
 
 
@@ -89,6 +89,9 @@ def lib():
         res, args = sig[base]
         k = args.index(_F) + 2
         sig[name] = (res, args[:k] + [_I] + args[k:])
+    sig["gqa_attn_decode_fp8"] = (_I, [_P] * 5 + [_F, _F] + [_I] * 5 + [_P, _P, _F, _F, _P, _I, _P, _P, _Z, _P])
+    sig["gqa_decode_qkv_fp8"] = (_I, [_P] * 4 + [_F, _F] + [_I] * 5 + [_P, _P, _F, _F, _P, _I, _P, _P])
+    sig["gqa_decode_attention_fp8"] = (_I, [_P] * 3 + [_F, _F, _P] + [_I] * 5 + [_P, _P, _Z, _P])
     for name, (res, args) in sig.items():
         fn = getattr(L, name)
         fn.restype = res
@@ -130,6 +133,13 @@ def _f16(t):
 def _i32(t):
     if t.dtype != torch.int32:
         raise TypeError(f"expected int32, got {t.dtype}")
+    return _ptr(t)
+
+
+def _u8(t):
+    """E4M3 codes: a uint8 or float8_e4m3fn tensor."""
+    if t is not None and t.dtype not in (torch.uint8, torch.float8_e4m3fn):
+        raise TypeError(f"expected uint8 or float8_e4m3fn codes, got {t.dtype}")
     return _ptr(t)
 
 
@@ -320,3 +330,29 @@ def gqa_last_launch_count() -> int:
 def new_workspace(nbytes: int, device=None) -> torch.Tensor:
     """A uint8 device buffer (torch allocations are 256-byte aligned)."""
     return torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=device or "cuda")
+
+
+# --------------------------------------------------------- FP8 (E4M3) KV cache
+
+def gqa_attn_decode_fp8(x, Wqkv, Wo, q_norm_w, k_norm_w, rope_theta, eps, B, hidden, Hq, Hkv, head_dim,
+                        k_cache, v_cache, k_scale, v_scale, cache_len, Lmax, out, workspace, stream=None):
+    """k_cache / v_cache: E4M3 codes (uint8 or float8_e4m3fn) worth code * scale."""
+    _check(lib().gqa_attn_decode_fp8(_bf16(x), _bf16(Wqkv), _bf16(Wo), _bf16(q_norm_w), _bf16(k_norm_w),
+                                     rope_theta, eps, B, hidden, Hq, Hkv, head_dim, _u8(k_cache), _u8(v_cache),
+                                     k_scale, v_scale, _i32(cache_len), Lmax, _bf16(out), _ptr(workspace),
+                                     workspace.numel() * workspace.element_size(), _stream(stream)))
+    return out
+
+
+def gqa_decode_qkv_fp8(x, Wqkv, q_norm_w, k_norm_w, rope_theta, eps, B, hidden, Hq, Hkv, head_dim,
+                       k_cache, v_cache, k_scale, v_scale, cache_len, Lmax, q_out, stream=None):
+    _check(lib().gqa_decode_qkv_fp8(_bf16(x), _bf16(Wqkv), _bf16(q_norm_w), _bf16(k_norm_w), rope_theta, eps,
+                                    B, hidden, Hq, Hkv, head_dim, _u8(k_cache), _u8(v_cache), k_scale, v_scale,
+                                    _i32(cache_len), Lmax, _f16(q_out), _stream(stream)))
+
+
+def gqa_decode_attention_fp8(q, k_cache, v_cache, k_scale, v_scale, kv_len, B, Hq, Hkv, head_dim, Lmax,
+                             attn_out, workspace, stream=None):
+    _check(lib().gqa_decode_attention_fp8(_f16(q), _u8(k_cache), _u8(v_cache), k_scale, v_scale, _i32(kv_len),
+                                          B, Hq, Hkv, head_dim, Lmax, _bf16(attn_out), _ptr(workspace),
+                                          workspace.numel() * workspace.element_size(), _stream(stream)))

@@ -61,7 +61,7 @@ static EncodeTiledFn get_encoder()
 }
 
 CUresult encode_tmap(CUtensorMap *map, const void *base, int rank, const uint64_t *dims, const uint64_t *strides_bytes,
-                     const uint32_t *box, bool swizzle128)
+                     const uint32_t *box, bool swizzle128, int elem_bytes)
 {
     EncodeTiledFn fn = get_encoder();
     if (!fn) return CUDA_ERROR_NOT_INITIALIZED;
@@ -73,7 +73,8 @@ CUresult encode_tmap(CUtensorMap *map, const void *base, int rank, const uint64_
         es[i] = 1;
         if (i + 1 < rank) s[i] = strides_bytes[i];
     }
-    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, const_cast<void *>(base), d, s, b, es,
+    const CUtensorMapDataType type = elem_bytes == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    return fn(map, type, (cuuint32_t)rank, const_cast<void *>(base), d, s, b, es,
               CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
 }
@@ -222,7 +223,7 @@ static FwdLayout fwd_layout(int B, int S, int Hq, int Hkv, int d)
 static int run_qkv(DeviceState &st, const gqa_bf16 *x, const gqa_bf16 *Wqkv, const gqa_bf16 *qn, const gqa_bf16 *kn,
                    float theta, float eps, int rd, int B, int S, int hidden, int Hq, int Hkv, int d, const int *pos_dev,
                    int q_seq, int kv_seq, int rope_rows, int q_f16, int kv_f16, uint16_t *q_out, uint16_t *k_out,
-                   uint16_t *v_out, cudaStream_t stream)
+                   uint16_t *v_out, cudaStream_t stream, int kv_fp8 = 0, float k_scale = 1.0f, float v_scale = 1.0f)
 {
     const float2 *rope = nullptr;
     if (rd > 0) {
@@ -250,6 +251,9 @@ static int run_qkv(DeviceState &st, const gqa_bf16 *x, const gqa_bf16 *Wqkv, con
     e.rope_rows = rope_rows;
     e.q_f16 = q_f16;     // binary16 unless Q meets a bf16 cache in the same MMA
     e.kv_f16 = kv_f16;   // prefill: binary16 workspace; cached paths: the bf16 cache
+    e.kv_fp8 = kv_fp8;   // decode into an E4M3 cache
+    e.k_scale = k_scale;
+    e.v_scale = v_scale;
     e.q_out = q_out;
     e.k_out = k_out;
     e.v_out = v_out;
@@ -281,14 +285,18 @@ static int run_oproj(DeviceState &st, const gqa_bf16 *attn, const gqa_bf16 *Wo, 
     return GQA_OK;
 }
 
-static int run_decode_attn(DeviceState &st, const gqa_bf16 *q, const gqa_bf16 *kc, const gqa_bf16 *vc,
+static int run_decode_attn(DeviceState &st, const gqa_bf16 *q, const void *kc, const void *vc,
                            const int *len, int bias, int B, int Hq, int Hkv, int d, int Lmax, gqa_bf16 *out,
-                           float *partials, int splits, cudaStream_t stream)
+                           float *partials, int splits, cudaStream_t stream, int fp8 = 0, float k_scale = 1.0f,
+                           float v_scale = 1.0f)
 {
     DecodeAttentionProblem p{};
     p.q = q;
     p.k_cache = kc;
     p.v_cache = vc;
+    p.fp8 = fp8;
+    p.k_scale = k_scale;
+    p.v_scale = v_scale;
     p.len = len;
     p.len_bias = bias;
     p.out = out;
@@ -637,6 +645,100 @@ int gqa_attn_prefill_cached_rd(const gqa_bf16 *x, const gqa_bf16 *Wqkv, const gq
     if ((rc = run_attention(*st, q, k_cache, v_cache, B, S, Hq, Hkv, head_dim, causal, attn, s, Lmax, cache_len, 1)))
         return rc;
     return run_oproj(*st, attn, Wo, x, B * S, hidden, Hq * head_dim, out, s);
+}
+
+// ------------------------------------------------------ FP8 (E4M3) KV cache
+
+static int check_fp8(int d, float k_scale, float v_scale)
+{
+    if (!(k_scale > 0.0f) || !(v_scale > 0.0f) || !isfinite(k_scale) || !isfinite(v_scale))
+        return fail(GQA_ERR_ARG, "k_scale and v_scale must be finite and > 0");
+    if (d != 128) return fail(GQA_ERR_UNSUPPORTED, "E4M3 caches support head_dim 128 (got %d)", d);
+    return GQA_OK;
+}
+
+int gqa_decode_attention_fp8(const gqa_f16 *q, const gqa_e4m3 *k_cache, const gqa_e4m3 *v_cache, float k_scale,
+                             float v_scale, const int *kv_len, int B, int Hq, int Hkv, int head_dim, int Lmax,
+                             gqa_bf16 *attn_out, void *workspace, size_t workspace_bytes, void *stream)
+{
+    g_launches = 0;
+    int rc = check_decode(B, 8, Hq, Hkv, head_dim, Lmax, nullptr, nullptr);
+    if (rc) return rc;
+    if ((rc = check_fp8(head_dim, k_scale, v_scale))) return rc;
+    if (!q || !k_cache || !v_cache || !kv_len || !attn_out) return fail(GQA_ERR_ARG, "null pointer");
+    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(attn_out))
+        return fail(GQA_ERR_ARG, "tensor pointers must be 16-byte aligned");
+    DeviceState *st;
+    if ((rc = device_state(&st))) return rc;
+    const int sp = decode_choose_splits(B, Hkv, Lmax, st->num_sms);
+    const size_t need = align256(decode_partials_floats(B, Hq, sp, head_dim) * 4);
+    if (!workspace || workspace_bytes < need)
+        return fail(GQA_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", need,
+                    workspace ? workspace_bytes : (size_t)0);
+    if (!aligned16(workspace)) return fail(GQA_ERR_ARG, "workspace must be 16-byte aligned");
+    return run_decode_attn(*st, q, k_cache, v_cache, kv_len, 0, B, Hq, Hkv, head_dim, Lmax, attn_out,
+                           (float *)workspace, sp, (cudaStream_t)stream, 1, k_scale, v_scale);
+}
+
+int gqa_decode_qkv_fp8(const gqa_bf16 *x, const gqa_bf16 *Wqkv, const gqa_bf16 *q_norm_w, const gqa_bf16 *k_norm_w,
+                       float rope_theta, float eps, int B, int hidden, int Hq, int Hkv, int head_dim,
+                       gqa_e4m3 *k_cache, gqa_e4m3 *v_cache, float k_scale, float v_scale, const int *cache_len,
+                       int Lmax, gqa_f16 *q_out, void *stream)
+{
+    g_launches = 0;
+    int rc = check_decode(B, hidden, Hq, Hkv, head_dim, Lmax, q_norm_w, k_norm_w);
+    if (rc) return rc;
+    if ((rc = check_fp8(head_dim, k_scale, v_scale))) return rc;
+    if (!x || !Wqkv || !k_cache || !v_cache || !cache_len || !q_out) return fail(GQA_ERR_ARG, "null pointer");
+    if (!aligned16(x) || !aligned16(Wqkv) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(q_out))
+        return fail(GQA_ERR_ARG, "tensor pointers must be 16-byte aligned");
+    if (!(rope_theta > 0.0f) || !(eps >= 0.0f)) return fail(GQA_ERR_ARG, "rope_theta must be > 0 and eps >= 0");
+    DeviceState *st;
+    if ((rc = device_state(&st))) return rc;
+    return run_qkv(*st, x, Wqkv, q_norm_w, k_norm_w, rope_theta, eps, head_dim, B, 1, hidden, Hq, Hkv, head_dim,
+                   cache_len, 1, Lmax, Lmax, 1, 0, q_out, (uint16_t *)k_cache, (uint16_t *)v_cache,
+                   (cudaStream_t)stream, 1, k_scale, v_scale);
+}
+
+int gqa_attn_decode_fp8(const gqa_bf16 *x, const gqa_bf16 *Wqkv, const gqa_bf16 *Wo, const gqa_bf16 *q_norm_w,
+                        const gqa_bf16 *k_norm_w, float rope_theta, float eps, int B, int hidden, int Hq, int Hkv,
+                        int head_dim, gqa_e4m3 *k_cache, gqa_e4m3 *v_cache, float k_scale, float v_scale,
+                        const int *cache_len, int Lmax, gqa_bf16 *out, void *workspace, size_t workspace_bytes,
+                        void *stream)
+{
+    g_launches = 0;
+    int rc = check_decode(B, hidden, Hq, Hkv, head_dim, Lmax, q_norm_w, k_norm_w);
+    if (rc) return rc;
+    if ((rc = check_fp8(head_dim, k_scale, v_scale))) return rc;
+    if (!x || !Wqkv || !Wo || !k_cache || !v_cache || !cache_len || !out) return fail(GQA_ERR_ARG, "null pointer");
+    if (!aligned16(x) || !aligned16(Wqkv) || !aligned16(Wo) || !aligned16(k_cache) || !aligned16(v_cache) ||
+        !aligned16(out))
+        return fail(GQA_ERR_ARG, "tensor pointers must be 16-byte aligned");
+    if (!(rope_theta > 0.0f) || !(eps >= 0.0f)) return fail(GQA_ERR_ARG, "rope_theta must be > 0 and eps >= 0");
+    if (overlap(out, (size_t)B * hidden * 2, x, (size_t)B * hidden * 2))
+        return fail(GQA_ERR_ARG, "out must not overlap x");
+    DeviceState *st;
+    if ((rc = device_state(&st))) return rc;
+    size_t off_attn, off_part;
+    int sp;
+    const size_t need = decode_layout(B, Hq, Hkv, head_dim, Lmax, st->num_sms, &off_attn, &off_part, &sp);
+    if (!workspace || workspace_bytes < need)
+        return fail(GQA_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", need,
+                    workspace ? workspace_bytes : (size_t)0);
+    if (((uintptr_t)workspace & 255u) != 0) return fail(GQA_ERR_ARG, "workspace must be 256-byte aligned");
+    uint8_t *ws = (uint8_t *)workspace;
+    gqa_f16 *q = (gqa_f16 *)ws;
+    gqa_bf16 *attn = (gqa_bf16 *)(ws + off_attn);
+    float *part = (float *)(ws + off_part);
+    cudaStream_t s = (cudaStream_t)stream;
+    if ((rc = run_qkv(*st, x, Wqkv, q_norm_w, k_norm_w, rope_theta, eps, head_dim, B, 1, hidden, Hq, Hkv, head_dim,
+                      cache_len, 1, Lmax, Lmax, 1, 0, q, (uint16_t *)k_cache, (uint16_t *)v_cache, s, 1, k_scale,
+                      v_scale)))
+        return rc;
+    if ((rc = run_decode_attn(*st, q, k_cache, v_cache, cache_len, 1, B, Hq, Hkv, head_dim, Lmax, attn, part, sp, s,
+                              1, k_scale, v_scale)))
+        return rc;
+    return run_oproj(*st, attn, Wo, x, B, hidden, Hq * head_dim, out, s);
 }
 
 // ------------------------------------------- full rotary (rotary_dim = head_dim)

@@ -89,14 +89,44 @@ DEVI void store32(uint16_t *dst, const float *v, bool f16, bool &clamped)
     }
 }
 
+// Storage format of one projected head row: bf16, binary16 (clamped to its
+// range and flagged), or E4M3 codes of value / scale (saturated and flagged).
+struct OutFmt {
+    int mode;     // 0 bf16, 1 binary16, 2 E4M3
+    float scale;  // E4M3 only
+};
+
+// Columns [c, c + 32) of a head row whose first element is at dst.
+DEVI void put32(void *dst, int c, const float *v, OutFmt f, bool &clamped)
+{
+    if (f.mode != 2) {
+        store32(reinterpret_cast<uint16_t *>(dst) + c, v, f.mode == 1, clamped);
+        return;
+    }
+    uint32_t w[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        float q[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            q[k] = __fdiv_rn(v[4 * i + k], f.scale);
+            clamped |= !(fabsf(q[k]) <= 448.0f);
+        }
+        w[i] = f32x2_to_e4m3x2(q[0], q[1]) | (f32x2_to_e4m3x2(q[2], q[3]) << 16);
+    }
+    uint4 *d4 = reinterpret_cast<uint4 *>(reinterpret_cast<uint8_t *>(dst) + c);
+    d4[0] = make_uint4(w[0], w[1], w[2], w[3]);
+    d4[1] = make_uint4(w[4], w[5], w[6], w[7]);
+}
+
 // Normalised (x * rinv * w) head row of a Q or K head, rotated on its first
 // RD features (rotate-half pairs (i, i + RD/2), (cos, sin) of angle
 // pos * theta^(-2i/RD) from cs[i]) and stored; features [RD, D) are only
 // normalised.  RD is D, D/2, D/4 or 0; when RD/2 is below 32 the pairs lie
 // inside the first 32 columns and are formed in registers.
 template <int D, int RD>
-DEVI void rope_store(uint32_t col, uint16_t *dst, float rinv, bool has_norm, const float *w, const float2 *cs,
-                     bool row_ok, bool f16, bool &clamped)
+DEVI void rope_store(uint32_t col, void *dst, float rinv, bool has_norm, const float *w, const float2 *cs,
+                     bool row_ok, OutFmt fmt, bool &clamped)
 {
     auto nrm = [&](float x, int c) { return has_norm ? x * rinv * w[c] : x * rinv; };
     int done = 0;  // columns [0, done) are stored
@@ -120,8 +150,8 @@ DEVI void rope_store(uint32_t col, uint16_t *dst, float rinv, bool has_norm, con
                 }
             }
             if (row_ok) {
-                store32(dst + c, y1, f16, clamped);
-                store32(dst + c + RD / 2, y2, f16, clamped);
+                put32(dst, c, y1, fmt, clamped);
+                put32(dst, c + RD / 2, y2, fmt, clamped);
             }
         }
         done = RD;
@@ -143,7 +173,7 @@ DEVI void rope_store(uint32_t col, uint16_t *dst, float rinv, bool has_norm, con
                 y[i + k + RD / 2] = x2 * co + x1 * si;
             }
         }
-        if (row_ok) store32(dst, y, f16, clamped);
+        if (row_ok) put32(dst, 0, y, fmt, clamped);
         done = 32;
     }
 #pragma unroll 1
@@ -153,7 +183,7 @@ DEVI void rope_store(uint32_t col, uint16_t *dst, float rinv, bool has_norm, con
         float y[32];
 #pragma unroll
         for (int i = 0; i < 32; ++i) y[i] = nrm(__uint_as_float(r[i]), c + i);
-        if (row_ok) store32(dst + c, y, f16, clamped);
+        if (row_ok) put32(dst, c, y, fmt, clamped);
     }
 }
 
@@ -198,12 +228,23 @@ DEVI void epilogue_qkv(const GemmParams &P, uint32_t tcol, int m, int n0, bool r
             kind = 2;
             head = (n - HqD - HkvD) / D;
         }
-        uint16_t *dst;
-        if (kind == 0)
+        // element offset of the head row; K/V rows hold 1-byte codes when kv_fp8
+        void *dst;
+        OutFmt fmt;
+        if (kind == 0) {
             dst = e.q_out + ((size_t)(b * e.Hq + head) * e.q_seq + q_slot) * D;
-        else
-            dst = (kind == 1 ? e.k_out : e.v_out) + ((size_t)(b * e.Hkv + head) * e.kv_seq + kv_slot) * D;
-        const bool f16 = (kind == 0 ? e.q_f16 : e.kv_f16) != 0;
+            fmt = {e.q_f16 ? 1 : 0, 1.0f};
+        } else {
+            const size_t off = ((size_t)(b * e.Hkv + head) * e.kv_seq + kv_slot) * D;
+            uint16_t *base = kind == 1 ? e.k_out : e.v_out;
+            if (e.kv_fp8) {
+                dst = reinterpret_cast<uint8_t *>(base) + off;
+                fmt = {2, kind == 1 ? e.k_scale : e.v_scale};
+            } else {
+                dst = base + off;
+                fmt = {e.kv_f16 ? 1 : 0, 1.0f};
+            }
+        }
 
         if (kind == 2) {  // V: no norm, no rotation
 #pragma unroll 1
@@ -213,7 +254,7 @@ DEVI void epilogue_qkv(const GemmParams &P, uint32_t tcol, int m, int n0, bool r
                 float v[32];
 #pragma unroll
                 for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
-                if (row_ok) store32(dst + c, v, f16, clamped);
+                if (row_ok) put32(dst, c, v, fmt, clamped);
             }
             continue;
         }
@@ -235,13 +276,13 @@ DEVI void epilogue_qkv(const GemmParams &P, uint32_t tcol, int m, int n0, bool r
         const float *w = s_norm + (kind == 0 ? 0 : 128);
         const int p = row_ok ? pos : 0;
         if (e.rd == D)
-            rope_store<D, D>(col, dst, rinv, has_norm, w, e.rope + (size_t)p * (D / 2), row_ok, f16, clamped);
+            rope_store<D, D>(col, dst, rinv, has_norm, w, e.rope + (size_t)p * (D / 2), row_ok, fmt, clamped);
         else if (e.rd == D / 2)
-            rope_store<D, D / 2>(col, dst, rinv, has_norm, w, e.rope + (size_t)p * (D / 4), row_ok, f16, clamped);
+            rope_store<D, D / 2>(col, dst, rinv, has_norm, w, e.rope + (size_t)p * (D / 4), row_ok, fmt, clamped);
         else if (e.rd == D / 4)
-            rope_store<D, D / 4>(col, dst, rinv, has_norm, w, e.rope + (size_t)p * (D / 8), row_ok, f16, clamped);
+            rope_store<D, D / 4>(col, dst, rinv, has_norm, w, e.rope + (size_t)p * (D / 8), row_ok, fmt, clamped);
         else
-            rope_store<D, 0>(col, dst, rinv, has_norm, w, nullptr, row_ok, f16, clamped);
+            rope_store<D, 0>(col, dst, rinv, has_norm, w, nullptr, row_ok, fmt, clamped);
     }
     if (clamped) atomicOr(P.err, kErrRange);
 }

@@ -29,6 +29,8 @@ struct QkvEpilogue {
     int rope_rows;
     int q_f16;             // 1: Q stored as binary16 (clamped, flagged); 0: bf16
     int kv_f16;            // 1: K and V stored as binary16 (clamped, flagged); 0: bf16
+    int kv_fp8;            // 1: K and V stored as E4M3 codes of value / k_scale, value / v_scale
+    float k_scale, v_scale;
     uint16_t *q_out, *k_out, *v_out;
 };
 
@@ -66,8 +68,10 @@ cudaError_t launch_attention(const AttentionProblem &p, unsigned *err, int num_s
 // -------------------------------------------------------- decode attention
 struct DecodeAttentionProblem {
     const uint16_t *q;        // [B, Hq, d] binary16
-    const uint16_t *k_cache;  // [B, Hkv, Lmax, d]
-    const uint16_t *v_cache;
+    const void *k_cache;      // [B, Hkv, Lmax, d] bf16, or E4M3 codes when fp8
+    const void *v_cache;
+    int fp8;                  // caches hold E4M3 codes worth code * k_scale / v_scale
+    float k_scale, v_scale;
     const int *len;           // device [B]; keys attended = len[b] + len_bias
     int len_bias;
     uint16_t *out;            // [B, Hq*d]
@@ -85,8 +89,9 @@ cudaError_t launch_selftest_wait(unsigned *err, unsigned long long limit_ns, cud
 // Sets the message gqa_last_error() returns on the calling thread.
 void record_error_message(const char *msg);
 
-// Tensor-map encoder (driver entry point, resolved once).
+// Tensor-map encoder (driver entry point, resolved once); elements of 2 bytes
+// (16-bit floats, copied bit for bit) or 1 byte (FP8 codes).
 CUresult encode_tmap(CUtensorMap *map, const void *base, int rank, const uint64_t *dims,
-                     const uint64_t *strides_bytes, const uint32_t *box, bool swizzle128);
+                     const uint64_t *strides_bytes, const uint32_t *box, bool swizzle128, int elem_bytes = 2);
 
 }  // namespace gqa

@@ -7,6 +7,7 @@
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+#include <cuda_fp8.h>
 #include <stdint.h>
 
 #define DEVI __device__ __forceinline__
@@ -331,6 +332,42 @@ DEVI void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, u
         "{%0,%1,%2,%3};"
         : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// D = A(16x16, row) * B(16x8, col) + C, binary16 inputs, fp32 accumulators.
+DEVI void mma_f16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
+                        uint32_t b1)
+{
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// ------------------------------------------------------------------- FP8
+
+// Two E4M3 codes (low byte first) -> binary16x2 (low half first).  Exact:
+// every E4M3 value is a binary16 value.
+DEVI uint32_t e4m3x2_to_f16x2(uint32_t two_codes)
+{
+    const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(two_codes & 0xFFFFu), __NV_E4M3);
+    return (uint32_t)h.x | ((uint32_t)h.y << 16);
+}
+
+// Two floats -> two E4M3 codes (lo in the low byte), nearest with ties to
+// even, saturating at +-448.
+DEVI uint32_t f32x2_to_e4m3x2(float lo, float hi)
+{
+    return (uint32_t)__nv_cvt_float2_to_fp8x2(make_float2(lo, hi), __NV_SATFINITE, __NV_E4M3);
+}
+
+// Byte permute: result byte i = byte sel[i] of (b:a) (a bytes 0-3, b bytes 4-7).
+DEVI uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel)
+{
+    uint32_t r;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
+    return r;
 }
 
 // ------------------------------------------------------------------- misc
