@@ -245,16 +245,24 @@ __global__ void __launch_bounds__(32 * (1 + CW), 1)
             // S[heads x 16 keys] = Q K^T
             float sc[2][4] = {{0.0f, 0.0f, 0.0f, 0.0f}, {0.0f, 0.0f, 0.0f, 0.0f}};
             if constexpr (F8) {
+                // four independent accumulators (n-tile x k-step parity) halve the MMA chains
+                float sc2[2][4] = {{0.0f, 0.0f, 0.0f, 0.0f}, {0.0f, 0.0f, 0.0f, 0.0f}};
 #pragma unroll
                 for (int kp = 0; kp < KS / 2; ++kp) {  // two k-steps (32 codes) per ldmatrix
                     uint32_t rk[4];  // (keys 0-7, k-step 2kp), (8-15, 2kp), (0-7, 2kp+1), (8-15, 2kp+1)
                     ldsm_x4(kb + swz8(f8_key, (2 * kp + f8_blk) * 16), rk[0], rk[1], rk[2], rk[3]);
+                    uint32_t bk[4][2];
 #pragma unroll
-                    for (int m = 0; m < 4; ++m) {
-                        const int ks = 2 * kp + (m >> 1);
-                        mma_f16_16816(sc[m & 1], qh[ks][0], 0u, qh[ks][1], 0u, e4m3x2_to_f16x2(rk[m]),
-                                      e4m3x2_to_f16x2(rk[m] >> 16));
-                    }
+                    for (int m = 0; m < 4; ++m) e4m3x4_to_f16x4(rk[m], bk[m][0], bk[m][1]);
+                    mma_f16_16816(sc[0], qh[2 * kp][0], 0u, qh[2 * kp][1], 0u, bk[0][0], bk[0][1]);
+                    mma_f16_16816(sc[1], qh[2 * kp][0], 0u, qh[2 * kp][1], 0u, bk[1][0], bk[1][1]);
+                    mma_f16_16816(sc2[0], qh[2 * kp + 1][0], 0u, qh[2 * kp + 1][1], 0u, bk[2][0], bk[2][1]);
+                    mma_f16_16816(sc2[1], qh[2 * kp + 1][0], 0u, qh[2 * kp + 1][1], 0u, bk[3][0], bk[3][1]);
+                }
+#pragma unroll
+                for (int n = 0; n < 2; ++n) {
+                    sc[n][0] += sc2[n][0];
+                    sc[n][1] += sc2[n][1];
                 }
             } else {
 #pragma unroll
@@ -279,7 +287,11 @@ __global__ void __launch_bounds__(32 * (1 + CW), 1)
             }
             mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
             mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-            const float m_new = fmaxf(m_run, mx);
+            // F8: the running max moves only when a score passes it by more than
+            // 2^8 (P then stays <= 2^8, exact in binary16's range), so O is
+            // rescaled rarely; bf16: every time the max grows
+            float m_new = fmaxf(m_run, mx);
+            if (F8 && !(mx > m_run + 8.0f)) m_new = m_run;
             const float m_use = (m_new == -INFINITY) ? 0.0f : m_new;
             const float alpha = ex2(m_run - m_use);
             m_run = m_new;
@@ -290,14 +302,9 @@ __global__ void __launch_bounds__(32 * (1 + CW), 1)
             // P as the A fragment of O += P V (rows 8..15 are padding), split
             // into bf16 high and low parts so P keeps ~16 mantissa bits
             uint32_t a0h = 0u, a2h = 0u, a0l = 0u, a2l = 0u;
-            if (F8 && row_valid) {  // binary16 high and low parts
-                const __half2 h01 = __floats2half2_rn(p[0], p[1]);
-                const __half2 h23 = __floats2half2_rn(p[2], p[3]);
-                const float2 f01 = __half22float2(h01), f23 = __half22float2(h23);
-                a0h = *reinterpret_cast<const uint32_t *>(&h01);
-                a2h = *reinterpret_cast<const uint32_t *>(&h23);
-                a0l = pack_f16(p[0] - f01.x, p[1] - f01.y);
-                a2l = pack_f16(p[2] - f23.x, p[3] - f23.y);
+            if (F8 && row_valid) {  // binary16 (11-bit significand), one MMA per tile
+                a0h = pack_f16(p[0], p[1]);
+                a2h = pack_f16(p[2], p[3]);
             } else if (row_valid) {
                 const __nv_bfloat162 h01 = __floats2bfloat162_rn(p[0], p[1]);
                 const __nv_bfloat162 h23 = __floats2bfloat162_rn(p[2], p[3]);
@@ -307,28 +314,28 @@ __global__ void __launch_bounds__(32 * (1 + CW), 1)
                 a0l = bf16x2_bits(p[0] - f01.x, p[1] - f01.y);
                 a2l = bf16x2_bits(p[2] - f23.x, p[3] - f23.y);
             }
+            if (!F8 || __any_sync(0xffffffffu, alpha != 1.0f)) {
 #pragma unroll
-            for (int n = 0; n < NT; ++n) {
-                o[n][0] *= alpha;
-                o[n][1] *= alpha;
+                for (int n = 0; n < NT; ++n) {
+                    o[n][0] *= alpha;
+                    o[n][1] *= alpha;
+                }
             }
             if constexpr (F8) {
 #pragma unroll
                 for (int j2 = 0; j2 < D / 32; ++j2) {  // two 16-wide d blocks per ldmatrix
                     uint32_t rv[4];  // (keys 0-7, block 2j2), (8-15, 2j2), (0-7, 2j2+1), (8-15, 2j2+1)
                     ldsm_x4_trans(vb + swz8(f8_key, (2 * j2 + f8_blk) * 16), rv[0], rv[1], rv[2], rv[3]);
+                    uint32_t bv[4][2];  // n-tiles 4 j2 .. 4 j2 + 3: (even d, odd d) of blocks 2 j2, 2 j2 + 1
 #pragma unroll
                     for (int x = 0; x < 2; ++x) {
-                        const int j = 2 * j2 + x;
                         // bytes (k c, k c+1, k+1 c, k+1 c+1) -> (k c, k+1 c | k c+1, k+1 c+1)
                         const uint32_t lo = prmt(rv[2 * x], 0u, 0x3120u), hi = prmt(rv[2 * x + 1], 0u, 0x3120u);
-                        const uint32_t be0 = e4m3x2_to_f16x2(lo), bo0 = e4m3x2_to_f16x2(lo >> 16);
-                        const uint32_t be1 = e4m3x2_to_f16x2(hi), bo1 = e4m3x2_to_f16x2(hi >> 16);
-                        mma_f16_16816(o[2 * j], a0h, 0u, a2h, 0u, be0, be1);
-                        mma_f16_16816(o[2 * j + 1], a0h, 0u, a2h, 0u, bo0, bo1);
-                        mma_f16_16816(o[2 * j], a0l, 0u, a2l, 0u, be0, be1);
-                        mma_f16_16816(o[2 * j + 1], a0l, 0u, a2l, 0u, bo0, bo1);
+                        e4m3x4_to_f16x4(lo, bv[2 * x][0], bv[2 * x + 1][0]);
+                        e4m3x4_to_f16x4(hi, bv[2 * x][1], bv[2 * x + 1][1]);
                     }
+#pragma unroll
+                    for (int n = 0; n < 4; ++n) mma_f16_16816(o[4 * j2 + n], a0h, 0u, a2h, 0u, bv[n][0], bv[n][1]);
                 }
             } else {
 #pragma unroll

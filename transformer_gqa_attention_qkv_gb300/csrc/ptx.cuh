@@ -347,12 +347,17 @@ DEVI void mma_f16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, ui
 
 // ------------------------------------------------------------------- FP8
 
-// Two E4M3 codes (low byte first) -> binary16x2 (low half first).  Exact:
-// every E4M3 value is a binary16 value.
-DEVI uint32_t e4m3x2_to_f16x2(uint32_t two_codes)
+// Four E4M3 codes (byte 0 first) -> two binary16x2 words: lo = codes 0, 1,
+// hi = codes 2, 3 (the lower code in the lower half).  Exact: every E4M3
+// value is a binary16 value.
+DEVI void e4m3x4_to_f16x4(uint32_t four_codes, uint32_t &lo, uint32_t &hi)
 {
-    const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(two_codes & 0xFFFFu), __NV_E4M3);
-    return (uint32_t)h.x | ((uint32_t)h.y << 16);
+    asm("{\n\t.reg .b16 c01, c23;\n\t"
+        "mov.b32 {c01, c23}, %2;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %0, c01;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %1, c23;\n\t}"
+        : "=r"(lo), "=r"(hi)
+        : "r"(four_codes));
 }
 
 // Two floats -> two E4M3 codes (lo in the low byte), nearest with ties to
