@@ -430,7 +430,10 @@ def run_ours(args, world, rank, local):
                   "bytes_per_step": db8["total"], "speedup_vs_bf16_cache": round(dms / d8ms, 3),
                   "roofline": {"bound": "hbm", "kernel": "decode_attention_fp8", "achieved": round(a8_ach, 1),
                                "peak": hbm, "unit": "GB/s", "frac": round(a8_ach / hbm, 4),
-                               "peak_source": f"{peak_src} copy bandwidth", "kernel_ms": round(a8ms, 4)}}
+                               "peak_source": f"{peak_src} copy bandwidth",
+                               "traffic": recorded_traffic("decode_attention_fp8_" + dc.name,
+                                                           [CSRC + "decode.cu", CSRC + "ptx.cuh"]),
+                               "kernel_ms": round(a8ms, 4)}}
     if gq.gqa_check_device_error() != 0:
         raise RuntimeError(gq.gqa_last_error())
     del dt_, dout, dws, kc8, vc8
