@@ -123,3 +123,24 @@ def test_decode_step_full_workload():
     # the attention output itself: the o_proj term (~1e-2) sits below the bf16
     # resolution of out (|x| ~ 1), so out alone cannot show an error in it
     assert_parity("decode attn", to64(attn), ref["attn"])
+
+
+@pytest.mark.parametrize("B,hidden,Hq,Hkv,d", [
+    (1, 2048, 16, 8, 128),    # M = 1
+    (128, 1024, 8, 2, 64),    # M = 128 (one full M block); head_dim 64 tiles
+    (5, 520, 4, 4, 64),       # hidden not a multiple of 64: a ragged o_proj tile
+])
+def test_decode_step_shapes(B, hidden, Hq, Hkv, d):
+    """The decode step at the edges of its projection tiling: one sequence,
+    a full 128-row M block, a ragged output width; output and attention match
+    the oracle, and a second call on the same workspace repeats the first."""
+    cfg = DecodeConfig("t", B, 40, hidden, Hq, Hkv, d, d == 128, 1e6, Lmax=48)
+    t = make_decode_inputs(cfg, seed=650 + B)
+    cl = torch.tensor([(7 * b) % 41 for b in range(B)], dtype=torch.int32)
+    out, attn = run_decode(cfg, t, cl, want_attn=True)
+    ref = oracle.decode(t["x"], t["Wqkv"], t["Wo"], t["q_norm_w"], t["k_norm_w"], cfg.rope_theta, cfg.eps,
+                        cfg.B, cfg.hidden, cfg.Hq, cfg.Hkv, cfg.head_dim, t["k_cache"], t["v_cache"], cl, cfg.lmax)
+    assert_parity("decode attn", to64(attn), ref["attn"])
+    assert_parity("decode out", to64(out), ref["out"])
+    out2, _ = run_decode(cfg, t, cl, want_attn=True)
+    assert torch.equal(out, out2)
