@@ -73,7 +73,7 @@ def fwd(L, **kw):
 
 @pytest.mark.parametrize("kw,code", [
     ({"S": 0}, -1), ({"B": -1}, -1), ({"Hq": 3}, -1), ({"d": 127}, -1), ({"qn": 0}, -1),
-    ({"d": 96}, -2), ({"d": 256}, -2), ({"hidden": 100}, -2), ({"Hq": 24, "Hkv": 8}, -2),
+    ({"d": 96}, -2), ({"d": 512}, -2), ({"d": 320}, -2), ({"hidden": 100}, -2), ({"Hq": 24, "Hkv": 8}, -2),
     ({"x": 0}, -1), ({"out": FAKE + 2}, -1), ({"out": FAKE}, -1), ({"theta": 0.0}, -1),
     ({"wsb": 100}, -5), ({"ws": 0}, -5), ({"ws": FAKE * 8 + 16}, -1),
 ])

@@ -379,6 +379,7 @@ cudaError_t run_attn(const AttentionProblem &p, unsigned *err, cudaStream_t stre
 cudaError_t launch_attention(const AttentionProblem &p, unsigned *err, int num_sms, cudaStream_t stream)
 {
     (void)num_sms;
+    if (p.d == 256) return launch_attention256(p, err, stream);
     if (p.Hkv <= 0 || p.Hq % p.Hkv) return cudaErrorInvalidValue;
     const int G = p.Hq / p.Hkv;
     if (G > kRows) return cudaErrorInvalidValue;

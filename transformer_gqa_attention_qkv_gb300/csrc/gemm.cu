@@ -43,8 +43,8 @@ struct Smem {
     static constexpr int RING = STAGES * (A_BYTES + B_BYTES);
     static constexpr int BARS = RING;                       // 2*STAGES + 5 mbarriers
     static constexpr int TMEM_SLOT = BARS + (2 * STAGES + 5) * 8;
-    static constexpr int NORM = (TMEM_SLOT + 16 + 15) & ~15;  // 2 x 128 floats
-    static constexpr int TOTAL = NORM + 2 * 128 * 4;
+    static constexpr int NORM = (TMEM_SLOT + 16 + 15) & ~15;  // q_norm_w, k_norm_w: 2 x 256 floats
+    static constexpr int TOTAL = NORM + 2 * 256 * 4;
     static constexpr int ALLOC = TOTAL + 1024;               // slack for 1024-byte alignment
 };
 
@@ -273,7 +273,7 @@ DEVI void epilogue_qkv(const GemmParams &P, uint32_t tcol, int m, int n0, bool r
             }
             rinv = 1.0f / sqrtf(ss * (1.0f / D) + e.eps);
         }
-        const float *w = s_norm + (kind == 0 ? 0 : 128);
+        const float *w = s_norm + (kind == 0 ? 0 : 256);
         const int p = row_ok ? pos : 0;
         if (e.rd == D)
             rope_store<D, D>(col, dst, rinv, has_norm, w, e.rope + (size_t)p * (D / 2), row_ok, fmt, clamped);
@@ -356,7 +356,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (EPI == EPI_QKV && warp >= 2 && P.qkv.q_norm_w) {
         for (int i = threadIdx.x - 64; i < D; i += 128) {
             s_norm[i] = __uint_as_float((uint32_t)P.qkv.q_norm_w[i] << 16);
-            s_norm[128 + i] = __uint_as_float((uint32_t)P.qkv.k_norm_w[i] << 16);
+            s_norm[256 + i] = __uint_as_float((uint32_t)P.qkv.k_norm_w[i] << 16);
         }
     }
     __syncthreads();
@@ -495,6 +495,11 @@ cudaError_t launch_gemm_qkv(const GemmProblem &p, const QkvEpilogue &e, unsigned
         GemmParams g = make_params(p, 256, err);
         g.qkv = e;
         return run<256, 4, EPI_QKV, 128>(p, g, num_sms, stream);
+    }
+    if (e.d == 256) {  // one 256-wide head per tile, also for decode-sized problems
+        GemmParams g = make_params(p, 256, err);
+        g.qkv = e;
+        return run<256, 4, EPI_QKV, 256>(p, g, num_sms, stream);
     }
     if (e.d == 64) {
         if (small_m) {

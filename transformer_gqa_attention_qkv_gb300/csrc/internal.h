@@ -64,6 +64,8 @@ struct AttentionProblem {
     int bf16_qkv;          // 1: q/k/v bf16 (P bf16); 0: binary16 (P binary16)
 };
 cudaError_t launch_attention(const AttentionProblem &p, unsigned *err, int num_sms, cudaStream_t stream);
+// head_dim 256 (called by launch_attention)
+cudaError_t launch_attention256(const AttentionProblem &p, unsigned *err, cudaStream_t stream);
 
 // -------------------------------------------------------- decode attention
 struct DecodeAttentionProblem {

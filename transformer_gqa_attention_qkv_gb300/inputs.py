@@ -68,13 +68,16 @@ PREFILL_CONFIGS = {
     "vaswani_mha": LayerConfig("vaswani_mha", 8, 2048, 512, 8, 8, 64, False, 1e4),
     "qwen3_4b": LayerConfig("qwen3_4b", 4, 4096, 2560, 32, 8, 128, True, 1e6),
     "qwen3_32b": LayerConfig("qwen3_32b", 1, 16384, 5120, 64, 8, 128, True, 1e6),
+    # head_dim 256 at the Gemma-3 example's width (hidden 640, four query heads);
+    # one KV head, batch and length are this workload's own choice
+    "gemma3_d256": LayerConfig("gemma3_d256", 4, 4096, 640, 4, 1, 256, True, 1e6),
 }
 DECODE_CONFIGS = {
     "qwen3_8b_decode": DecodeConfig("qwen3_8b_decode", 64, 8192, 4096, 32, 8, 128, True, 1e6),
 }
 # seeds: 1000 + position of the workload in the list above
 SEEDS = {"qwen3_0p6b": 1000, "vaswani_mha": 1001, "qwen3_4b": 1002,
-         "qwen3_32b": 1003, "qwen3_8b_decode": 1004}
+         "qwen3_32b": 1003, "qwen3_8b_decode": 1004, "gemma3_d256": 1005}
 
 
 def _normal(shape, gen, std, mean=0.0, device="cpu"):
