@@ -101,6 +101,12 @@ def _load():
     lib.oracle_decode_fp8.argtypes = [_u16p, _u16p, _u16p, _u16p, _u16p, _D, _D,
                                       _L, _L, _L, _L, _L, _u8p, _u8p, _D, _D, _i32p, _L,
                                       _f64p, _f64p, _f64p, _f64p, _u8p, _u8p, _f64p, _I]
+    lib.oracle_backward.restype = _I
+    lib.oracle_backward.argtypes = [_u16p, _u16p, _u16p, _u16p, _u16p, _D, _D, _L, _L, _L, _L, _L, _L, _I,
+                                    _u16p, _f64p, _f64p, _f64p, _f64p, _f64p, _f64p, _f64p, _f64p, _f64p, _I]
+    lib.oracle_attention_backward.restype = _I
+    lib.oracle_attention_backward.argtypes = [_u16p, _u16p, _u16p, _u16p, _I, _L, _L, _L, _L, _L, _I,
+                                              _f64p, _f64p, _f64p, _I]
     # the *_rd forms take the rotary width (reading R16) after eps
     lib.oracle_rope_rows_rd.restype = _I
     lib.oracle_rope_rows_rd.argtypes = [_f64p, _L, _L, _L, _f64p, _D, _f64p]
@@ -396,3 +402,43 @@ def decode_fp8(x, Wqkv, Wo, q_norm_w, k_norm_w, rope_theta, eps, B, hidden, Hq, 
                                      _pf(kn_), _pf(vn_), kc_.ctypes.data_as(_u8p), vc_.ctypes.data_as(_u8p),
                                      _pf(a), threads or default_threads()), "decode_fp8")
     return {"out": out, "q": q, "k": kn_, "v": vn_, "k_code": kc_, "v_code": vc_, "attn": a}
+
+
+# ------------------------------------------------------------- backward
+
+def backward(x, Wqkv, Wo, q_norm_w, k_norm_w, rope_theta, eps, B, S, hidden, Hq, Hkv, d, dout,
+             causal=True, want_stages=False, threads=None):
+    """Gradients of the layer given dout = dL/dout [B*S, hidden] (bf16).
+    Returns dict dx [B*S, hidden], dWqkv [(Hq+2Hkv)d, hidden], dWo [hidden,
+    Hq*d], dq_norm_w / dk_norm_w [d]; with want_stages also d_attn [B*S,
+    Hq*d] and the attention-input gradients dq [B,Hq,S,d], dk/dv [B,Hkv,S,d]."""
+    lib = _load()
+    N = (Hq + 2 * Hkv) * d
+    dx = np.empty((B * S, hidden)); dW = np.empty((N, hidden)); dWo = np.empty((hidden, Hq * d))
+    dqn = np.empty(d); dkn = np.empty(d)
+    da = np.empty((B * S, Hq * d)) if want_stages else None
+    dq = np.empty((B, Hq, S, d)) if want_stages else None
+    dk = np.empty((B, Hkv, S, d)) if want_stages else None
+    dv = np.empty((B, Hkv, S, d)) if want_stages else None
+    xb, wb, ob, qn, kn, gb = _bits(x), _bits(Wqkv), _bits(Wo), _bits(q_norm_w), _bits(k_norm_w), _bits(dout)
+    _check(lib.oracle_backward(_p16(xb), _p16(wb), _p16(ob), _p16(qn), _p16(kn), rope_theta, eps, B, S, hidden,
+                               Hq, Hkv, d, int(causal), _p16(gb), _pf(dx), _pf(dW), _pf(dWo), _pf(dqn), _pf(dkn),
+                               _pf(da), _pf(dq), _pf(dk), _pf(dv), threads or default_threads()), "backward")
+    res = {"dx": dx, "dWqkv": dW, "dWo": dWo, "dq_norm_w": dqn, "dk_norm_w": dkn}
+    if want_stages:
+        res.update({"d_attn": da, "dq": dq, "dk": dk, "dv": dv})
+    return res
+
+
+def attention_backward(Q, K, V, dO, B, S, Hq, Hkv, d, causal=True, threads=None):
+    """dq [B,Hq,S,d], dk/dv [B,Hkv,S,d] of the attention alone, from 16-bit
+    Q [B,Hq,S,d], K/V [B,Hkv,S,d], dO [B,S,Hq*d] (all bf16 or all float16)."""
+    lib = _load()
+    f16 = _is_f16(Q)
+    assert all(_is_f16(t) == f16 for t in (K, V, dO)), "Q, K, V and dO must share one 16-bit format"
+    dq = np.empty((B, Hq, S, d)); dk = np.empty((B, Hkv, S, d)); dv = np.empty((B, Hkv, S, d))
+    qb, kb, vb, gb = _bits(Q, True), _bits(K, True), _bits(V, True), _bits(dO, True)
+    _check(lib.oracle_attention_backward(_p16(qb), _p16(kb), _p16(vb), _p16(gb), int(f16), B, S, Hq, Hkv, d,
+                                         int(causal), _pf(dq), _pf(dk), _pf(dv), threads or default_threads()),
+           "attention_backward")
+    return dq, dk, dv

@@ -46,6 +46,9 @@
  *      code to value / scale, ties to even, saturating at +-448; the new
  *      token's key and value are appended as codes and attended like the
  *      rest ("Head Dimension" article, §5.2: FP8 for the K, V cache).
+ *   R19 backward: the gradients are the derivatives of the forward steps
+ *      above in reverse order (the pages print none); a KV head's K and V
+ *      gradients sum over the query heads of its group.
  */
 #include <math.h>
 #include <stdint.h>
@@ -916,5 +919,309 @@ done:
     free(deq);
     free(codes);
     free(arows);
+    return err;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Backward of the layer (gradients of a scalar loss L given dout = dL/dout). */
+/* ------------------------------------------------------------------------ */
+
+/* The pages ask for "the backward pass, including gradients into the shared
+ * KV projections" ([NeoX] "Qwen3-0.6B example": both K and V projections serve
+ * all query heads of a group; [Part]: a KV head's gradients come from every
+ * query head that reads it).  They print no backward formulas; these are the
+ * derivatives of the forward steps above, taken in reverse order:
+ *   out = x + attn Wo^T          -> d_attn = dout Wo, dWo = dout^T attn, dx = dout
+ *   o_t = sum_u p_u v_u, p = softmax(s), s_u = scale <q_t, k_u>
+ *                                 -> dv_u += p_u do_t; dp_u = <do_t, v_u>;
+ *                                    ds_u = p_u (dp_u - <do_t, o_t>);
+ *                                    dq_t = scale sum_u ds_u k_u; dk_u += scale ds_u q_t
+ *   q = RoPE(q_n)                 -> dq_n = RoPE^T(dq) (rotation by -angle)
+ *   q_n = q_pre r w, r = (mean(q_pre^2) + eps)^(-1/2)
+ *                                 -> dq_pre_i = r w_i dq_n_i - q_pre_i r^3 / d sum_k q_pre_k w_k dq_n_k
+ *                                    dw_i += q_pre_i r dq_n_i (over every Q row; k_norm_w over K rows)
+ *   qkv_pre = x Wqkv^T            -> dx += d_qkv_pre Wqkv, dWqkv = d_qkv_pre^T x
+ * K and V gradients of a KV head sum over the G query heads of its group.
+ * Full rotary (rotary_dim = d).  Outputs (all required): dx [B*S, hidden],
+ * dWqkv [(Hq+2Hkv)*d, hidden], dWo [hidden, Hq*d], dqn/dkn [d] (zeroed
+ * when there is no QK-norm).  Optional: d_attn [B*S, Hq*d] and the
+ * attention-input gradients dq [B,Hq,S,d], dk/dv [B,Hkv,S,d] (after RoPE,
+ * i.e. with respect to the attention's q, k, v). */
+
+/* inverse RoPE: rotation of the first rd features by -angle */
+static void rope_head_inv(double *v, long rd, double pos, double theta)
+{
+    long half = rd / 2;
+    for (long i = 0; i < half; ++i) {
+        double f = pos * pow(theta, -2.0 * (double)i / (double)rd);
+        double c = cos(f), s = sin(f);
+        double a = v[i], b = v[i + half];
+        v[i] = a * c + b * s;
+        v[i + half] = b * c - a * s;
+    }
+}
+
+/* RMSNorm backward of one row: y = x r w.  dx and (accumulated) dw. */
+static void rmsnorm_head_bwd(const double *x, const double *dy, long d, const uint16_t *w, double eps,
+                             double *dx, double *dw)
+{
+    double ms = 0.0;
+    for (long i = 0; i < d; ++i) ms += x[i] * x[i];
+    ms /= (double)d;
+    double r = 1.0 / sqrt(ms + eps);
+    double dot = 0.0;
+    for (long i = 0; i < d; ++i) dot += x[i] * bf(w[i]) * dy[i];
+    for (long i = 0; i < d; ++i) {
+        dx[i] = r * bf(w[i]) * dy[i] - x[i] * r * r * r / (double)d * dot;
+        dw[i] += x[i] * r * dy[i];
+    }
+}
+
+int oracle_backward(const uint16_t *x, const uint16_t *Wqkv, const uint16_t *Wo,
+                    const uint16_t *q_norm_w, const uint16_t *k_norm_w,
+                    double rope_theta, double eps,
+                    long B, long S, long hidden, long Hq, long Hkv, long d, int causal,
+                    const uint16_t *dout,
+                    double *dx, double *dWqkv, double *dWo, double *dqn, double *dkn,
+                    double *d_attn_out, double *dq_out, double *dk_out, double *dv_out, int nthreads)
+{
+    if (!x || !Wqkv || !Wo || !dout || !dx || !dWqkv || !dWo || !dqn || !dkn) return ORACLE_EARG;
+    if (B <= 0 || S <= 0 || hidden <= 0 || Hq <= 0 || Hkv <= 0 || d <= 0 || (d & 1) || d > 1024) return ORACLE_EARG;
+    if (Hq % Hkv) return ORACLE_EARG;
+    if ((q_norm_w == NULL) != (k_norm_w == NULL)) return ORACLE_EARG;
+    const long M = B * S, NQ = Hq * d, NKV = Hkv * d, N = NQ + 2 * NKV, G = Hq / Hkv;
+    const double scale = 1.0 / sqrt((double)d);
+    int err = ORACLE_OK;
+    set_threads(nthreads);
+    double *pre = (double *)malloc((size_t)(M * N) * sizeof(double));   /* qkv before norm/RoPE */
+    double *Q = (double *)malloc((size_t)(B * Hq * S * d) * sizeof(double));
+    double *K = (double *)malloc((size_t)(B * Hkv * S * d) * sizeof(double));
+    double *V = (double *)malloc((size_t)(B * Hkv * S * d) * sizeof(double));
+    double *attn = (double *)malloc((size_t)(M * NQ) * sizeof(double));
+    double *dattn = (double *)malloc((size_t)(M * NQ) * sizeof(double));
+    double *dQ = (double *)calloc((size_t)(B * Hq * S * d), sizeof(double));
+    double *dK = (double *)calloc((size_t)(B * Hkv * S * d), sizeof(double));
+    double *dV = (double *)calloc((size_t)(B * Hkv * S * d), sizeof(double));
+    double *dpre = (double *)malloc((size_t)(M * N) * sizeof(double));
+    if (!pre || !Q || !K || !V || !attn || !dattn || !dQ || !dK || !dV || !dpre) { err = ORACLE_ENOMEM; goto done; }
+
+    /* forward: projections, norm, RoPE */
+#pragma omp parallel for schedule(dynamic, 1)
+    for (long m = 0; m < M; ++m) {
+        long b = m / S, t = m % S;
+        double *row = pre + m * N;
+        linear_row(x + m * hidden, Wqkv, 0, N, hidden, row);
+        double tmp[1024];
+        for (long j = 0; j < Hq; ++j) {
+            memcpy(tmp, row + j * d, (size_t)d * sizeof(double));
+            if (q_norm_w) rmsnorm_head(tmp, d, q_norm_w, eps);
+            rope_head(tmp, d, (double)t, rope_theta);
+            memcpy(Q + ((b * Hq + j) * S + t) * d, tmp, (size_t)d * sizeof(double));
+        }
+        for (long g = 0; g < Hkv; ++g) {
+            memcpy(tmp, row + NQ + g * d, (size_t)d * sizeof(double));
+            if (k_norm_w) rmsnorm_head(tmp, d, k_norm_w, eps);
+            rope_head(tmp, d, (double)t, rope_theta);
+            memcpy(K + ((b * Hkv + g) * S + t) * d, tmp, (size_t)d * sizeof(double));
+            memcpy(V + ((b * Hkv + g) * S + t) * d, row + NQ + NKV + g * d, (size_t)d * sizeof(double));
+        }
+    }
+    /* forward attention (kept: attn rows) */
+#pragma omp parallel for collapse(2) schedule(dynamic, 1)
+    for (long m = 0; m < M; ++m)
+        for (long j = 0; j < Hq; ++j) {
+            long b = m / S, t = m % S, g = j / G;
+            kv_src src = {NULL, NULL, K + (b * Hkv + g) * S * d, V + (b * Hkv + g) * S * d, 0, 0};
+            int e = attend_row(Q + ((b * Hq + j) * S + t) * d, &src, causal ? t + 1 : S, d, attn + m * NQ + j * d);
+            if (e) err = e;
+        }
+    /* out = x + attn Wo^T:  d_attn = dout Wo;  dWo = dout^T attn */
+#pragma omp parallel for schedule(dynamic, 1)
+    for (long m = 0; m < M; ++m)
+        for (long c = 0; c < NQ; ++c) {
+            double s = 0.0;
+            for (long n = 0; n < hidden; ++n) s += bf(dout[m * hidden + n]) * bf(Wo[n * NQ + c]);
+            dattn[m * NQ + c] = s;
+        }
+#pragma omp parallel for schedule(dynamic, 1)
+    for (long n = 0; n < hidden; ++n)
+        for (long c = 0; c < NQ; ++c) {
+            double s = 0.0;
+            for (long m = 0; m < M; ++m) s += bf(dout[m * hidden + n]) * attn[m * NQ + c];
+            dWo[n * NQ + c] = s;
+        }
+    /* attention backward, one (sequence, KV head) at a time so that the
+     * K/V gradient sums over the group's query heads need no locking */
+#pragma omp parallel for collapse(2) schedule(dynamic, 1)
+    for (long b = 0; b < B; ++b)
+        for (long g = 0; g < Hkv; ++g) {
+            const double *Kg = K + (b * Hkv + g) * S * d, *Vg = V + (b * Hkv + g) * S * d;
+            double *dKg = dK + (b * Hkv + g) * S * d, *dVg = dV + (b * Hkv + g) * S * d;
+            double *p = (double *)malloc((size_t)S * sizeof(double));
+            double *dp = (double *)malloc((size_t)S * sizeof(double));
+            if (!p || !dp) { err = ORACLE_ENOMEM; free(p); free(dp); continue; }
+            for (long j = g * G; j < (g + 1) * G; ++j)
+                for (long t = 0; t < S; ++t) {
+                    const double *q = Q + ((b * Hq + j) * S + t) * d;
+                    const double *o = attn + (b * S + t) * NQ + j * d;
+                    const double *dO = dattn + (b * S + t) * NQ + j * d;
+                    double *dq = dQ + ((b * Hq + j) * S + t) * d;
+                    long n_vis = causal ? t + 1 : S;
+                    double mx = -INFINITY;
+                    for (long u = 0; u < n_vis; ++u) {
+                        double s = 0.0;
+                        for (long c = 0; c < d; ++c) s += q[c] * Kg[u * d + c];
+                        p[u] = s * scale;
+                        if (p[u] > mx) mx = p[u];
+                    }
+                    double den = 0.0;
+                    for (long u = 0; u < n_vis; ++u) { p[u] = exp(p[u] - mx); den += p[u]; }
+                    double Dt = 0.0;
+                    for (long c = 0; c < d; ++c) Dt += dO[c] * o[c];
+                    for (long u = 0; u < n_vis; ++u) {
+                        p[u] /= den;
+                        double s = 0.0;
+                        for (long c = 0; c < d; ++c) s += dO[c] * Vg[u * d + c];
+                        dp[u] = s;
+                    }
+                    for (long u = 0; u < n_vis; ++u) {
+                        double ds = p[u] * (dp[u] - Dt);
+                        for (long c = 0; c < d; ++c) {
+                            dq[c] += scale * ds * Kg[u * d + c];
+                            dKg[u * d + c] += scale * ds * q[c];
+                            dVg[u * d + c] += p[u] * dO[c];
+                        }
+                    }
+                }
+            free(p);
+            free(dp);
+        }
+    /* RoPE^T and QK-norm backward -> d_qkv_pre; norm-weight gradients */
+    for (long i = 0; i < d; ++i) { dqn[i] = 0.0; dkn[i] = 0.0; }
+    {
+        double *dqn_rows = (double *)calloc((size_t)(M * d), sizeof(double));
+        double *dkn_rows = (double *)calloc((size_t)(M * d), sizeof(double));
+        if (!dqn_rows || !dkn_rows) { free(dqn_rows); free(dkn_rows); err = ORACLE_ENOMEM; goto done; }
+#pragma omp parallel for schedule(dynamic, 1)
+        for (long m = 0; m < M; ++m) {
+            long b = m / S, t = m % S;
+            double dy[1024];
+            for (long j = 0; j < Hq; ++j) {
+                memcpy(dy, dQ + ((b * Hq + j) * S + t) * d, (size_t)d * sizeof(double));
+                rope_head_inv(dy, d, (double)t, rope_theta);
+                if (q_norm_w)
+                    rmsnorm_head_bwd(pre + m * N + j * d, dy, d, q_norm_w, eps, dpre + m * N + j * d, dqn_rows + m * d);
+                else
+                    memcpy(dpre + m * N + j * d, dy, (size_t)d * sizeof(double));
+            }
+            for (long g = 0; g < Hkv; ++g) {
+                memcpy(dy, dK + ((b * Hkv + g) * S + t) * d, (size_t)d * sizeof(double));
+                rope_head_inv(dy, d, (double)t, rope_theta);
+                if (k_norm_w)
+                    rmsnorm_head_bwd(pre + m * N + NQ + g * d, dy, d, k_norm_w, eps, dpre + m * N + NQ + g * d,
+                                     dkn_rows + m * d);
+                else
+                    memcpy(dpre + m * N + NQ + g * d, dy, (size_t)d * sizeof(double));
+                memcpy(dpre + m * N + NQ + NKV + g * d, dV + ((b * Hkv + g) * S + t) * d, (size_t)d * sizeof(double));
+            }
+        }
+        for (long m = 0; m < M; ++m)
+            for (long i = 0; i < d; ++i) { dqn[i] += dqn_rows[m * d + i]; dkn[i] += dkn_rows[m * d + i]; }
+        free(dqn_rows);
+        free(dkn_rows);
+    }
+    /* dx = dout + d_qkv_pre Wqkv;  dWqkv = d_qkv_pre^T x */
+#pragma omp parallel for schedule(dynamic, 1)
+    for (long m = 0; m < M; ++m)
+        for (long k = 0; k < hidden; ++k) {
+            double s = bf(dout[m * hidden + k]);
+            for (long n = 0; n < N; ++n) s += dpre[m * N + n] * bf(Wqkv[n * hidden + k]);
+            dx[m * hidden + k] = s;
+        }
+#pragma omp parallel for schedule(dynamic, 1)
+    for (long n = 0; n < N; ++n)
+        for (long k = 0; k < hidden; ++k) {
+            double s = 0.0;
+            for (long m = 0; m < M; ++m) s += dpre[m * N + n] * bf(x[m * hidden + k]);
+            dWqkv[n * hidden + k] = s;
+        }
+    if (d_attn_out) memcpy(d_attn_out, dattn, (size_t)(M * NQ) * sizeof(double));
+    if (dq_out) memcpy(dq_out, dQ, (size_t)(B * Hq * S * d) * sizeof(double));
+    if (dk_out) memcpy(dk_out, dK, (size_t)(B * Hkv * S * d) * sizeof(double));
+    if (dv_out) memcpy(dv_out, dV, (size_t)(B * Hkv * S * d) * sizeof(double));
+done:
+    free(pre); free(Q); free(K); free(V); free(attn); free(dattn); free(dQ); free(dK); free(dV); free(dpre);
+    return err;
+}
+
+/* Attention backward alone, from 16-bit Q [B,Hq,S,d], K/V [B,Hkv,S,d] and
+ * dO [B,S,Hq*d] (all bf16, or all binary16 with in_f16 = 1), widened exactly:
+ * dq [B,Hq,S,d], dk/dv [B,Hkv,S,d] as in oracle_backward (K/V gradients sum
+ * over the group's query heads). */
+int oracle_attention_backward(const uint16_t *Qb, const uint16_t *Kb, const uint16_t *Vb, const uint16_t *dOb,
+                              int in_f16, long B, long S, long Hq, long Hkv, long d, int causal,
+                              double *dq, double *dk, double *dv, int nthreads)
+{
+    if (!Qb || !Kb || !Vb || !dOb || !dq || !dk || !dv) return ORACLE_EARG;
+    if (B <= 0 || S <= 0 || Hq <= 0 || Hkv <= 0 || d <= 0 || d > 1024 || Hq % Hkv) return ORACLE_EARG;
+    const long G = Hq / Hkv, NQ = Hq * d;
+    const double scale = 1.0 / sqrt((double)d);
+    int err = ORACLE_OK;
+    set_threads(nthreads);
+    memset(dq, 0, (size_t)(B * Hq * S * d) * sizeof(double));
+    memset(dk, 0, (size_t)(B * Hkv * S * d) * sizeof(double));
+    memset(dv, 0, (size_t)(B * Hkv * S * d) * sizeof(double));
+#pragma omp parallel for collapse(2) schedule(dynamic, 1)
+    for (long b = 0; b < B; ++b)
+        for (long g = 0; g < Hkv; ++g) {
+            double *Kg = (double *)malloc((size_t)(S * d) * sizeof(double));
+            double *Vg = (double *)malloc((size_t)(S * d) * sizeof(double));
+            double *p = (double *)malloc((size_t)S * sizeof(double));
+            double *dp = (double *)malloc((size_t)S * sizeof(double));
+            double q[1024], o[1024], dO[1024];
+            if (!Kg || !Vg || !p || !dp) { err = ORACLE_ENOMEM; free(Kg); free(Vg); free(p); free(dp); continue; }
+            for (long i = 0; i < S * d; ++i) {
+                Kg[i] = w16(Kb[(b * Hkv + g) * S * d + i], in_f16);
+                Vg[i] = w16(Vb[(b * Hkv + g) * S * d + i], in_f16);
+            }
+            double *dKg = dk + (b * Hkv + g) * S * d, *dVg = dv + (b * Hkv + g) * S * d;
+            for (long j = g * G; j < (g + 1) * G; ++j)
+                for (long t = 0; t < S; ++t) {
+                    for (long c = 0; c < d; ++c) {
+                        q[c] = w16(Qb[((b * Hq + j) * S + t) * d + c], in_f16);
+                        dO[c] = w16(dOb[(b * S + t) * NQ + j * d + c], in_f16);
+                    }
+                    long n_vis = causal ? t + 1 : S;
+                    double mx = -INFINITY;
+                    for (long u = 0; u < n_vis; ++u) {
+                        double s = 0.0;
+                        for (long c = 0; c < d; ++c) s += q[c] * Kg[u * d + c];
+                        p[u] = s * scale;
+                        if (p[u] > mx) mx = p[u];
+                    }
+                    double den = 0.0;
+                    for (long u = 0; u < n_vis; ++u) { p[u] = exp(p[u] - mx); den += p[u]; }
+                    for (long c = 0; c < d; ++c) o[c] = 0.0;
+                    for (long u = 0; u < n_vis; ++u) {
+                        p[u] /= den;
+                        for (long c = 0; c < d; ++c) o[c] += p[u] * Vg[u * d + c];
+                    }
+                    double Dt = 0.0;
+                    for (long c = 0; c < d; ++c) Dt += dO[c] * o[c];
+                    double *dqr = dq + ((b * Hq + j) * S + t) * d;
+                    for (long u = 0; u < n_vis; ++u) {
+                        double s = 0.0;
+                        for (long c = 0; c < d; ++c) s += dO[c] * Vg[u * d + c];
+                        dp[u] = s;
+                        double ds = p[u] * (dp[u] - Dt);
+                        for (long c = 0; c < d; ++c) {
+                            dqr[c] += scale * ds * Kg[u * d + c];
+                            dKg[u * d + c] += scale * ds * q[c];
+                            dVg[u * d + c] += p[u] * dO[c];
+                        }
+                    }
+                }
+            free(Kg); free(Vg); free(p); free(dp);
+        }
     return err;
 }

@@ -744,3 +744,104 @@ def test_fp8_decode_step_equals_library_composition():
         np.testing.assert_allclose(got["attn"][b], a.numpy(), rtol=1e-11, atol=1e-12)
         o = f64(t["x"][b, 0]) + F.linear(a, f64(t["Wo"]))
         np.testing.assert_allclose(got["out"][b], o.numpy(), rtol=1e-11, atol=1e-11)
+
+
+# ----------------------------------------------------------------- backward
+
+def _torch_layer(cfg, t, causal=True, keep=None):
+    """The layer as a float64 torch composition (F.linear, F.rms_norm, complex
+    RoPE, SDPA); parameters are leaves with requires_grad.  keep (a dict)
+    receives the attention's q, k, v and attn with retained gradients."""
+    B, S, h, Hq, Hkv, d = cfg.B, cfg.S, cfg.hidden, cfg.Hq, cfg.Hkv, cfg.head_dim
+    leaves = {k: f64(v).requires_grad_(True) for k, v in t.items() if v is not None}
+    x, W, Wo = leaves["x"], leaves["Wqkv"], leaves["Wo"]
+    q = F.linear(x, W[:Hq * d]).view(B, S, Hq, d)
+    k = F.linear(x, W[Hq * d:(Hq + Hkv) * d]).view(B, S, Hkv, d)
+    v = F.linear(x, W[(Hq + Hkv) * d:]).view(B, S, Hkv, d)
+    if "q_norm_w" in leaves:
+        q = F.rms_norm(q, (d,), weight=leaves["q_norm_w"], eps=cfg.eps)
+        k = F.rms_norm(k, (d,), weight=leaves["k_norm_w"], eps=cfg.eps)
+    pos = torch.arange(S, dtype=torch.float64)[:, None]
+    q = _complex_rope(q, pos, cfg.rope_theta, d).transpose(1, 2)
+    k = _complex_rope(k, pos, cfg.rope_theta, d).transpose(1, 2)
+    v = v.transpose(1, 2)
+    if keep is not None:
+        for name, tt in (("q", q), ("k", k), ("v", v)):
+            tt.retain_grad()
+            keep[name] = tt
+    a = F.scaled_dot_product_attention(q, k.repeat_interleave(Hq // Hkv, 1), v.repeat_interleave(Hq // Hkv, 1),
+                                       is_causal=causal)
+    a = a.transpose(1, 2).reshape(B, S, Hq * d)
+    if keep is not None:
+        a.retain_grad()
+        keep["attn"] = a
+    return leaves, x + F.linear(a, Wo)
+
+
+@pytest.mark.parametrize("qk,causal", [(True, True), (False, True), (True, False)])
+def test_backward_equals_library_autograd(qk, causal):
+    """Every gradient of the layer (x, Wqkv, Wo, both norm weights, and the
+    attention's inputs/outputs) equals torch's float64 autograd through the
+    library composition; K/V gradients include the sum over a group's heads."""
+    cfg = _tiny(qk_norm=qk)
+    t = make_layer_inputs(cfg, seed=51, w_std=0.3)
+    dout = bf16(np.random.default_rng(51).standard_normal((cfg.B * cfg.S, cfg.hidden)))
+    keep = {}
+    leaves, out = _torch_layer(cfg, t, causal, keep)
+    (out.reshape(-1, cfg.hidden) * f64(dout)).sum().backward()
+    got = oracle.backward(t["x"], t["Wqkv"], t["Wo"], t["q_norm_w"], t["k_norm_w"], cfg.rope_theta, cfg.eps,
+                          cfg.B, cfg.S, cfg.hidden, cfg.Hq, cfg.Hkv, cfg.head_dim, dout, causal=causal,
+                          want_stages=True, threads=T)
+    tol = dict(rtol=1e-10, atol=1e-11)
+    np.testing.assert_allclose(got["dx"], leaves["x"].grad.reshape(-1, cfg.hidden).numpy(), **tol)
+    np.testing.assert_allclose(got["dWqkv"], leaves["Wqkv"].grad.numpy(), **tol)
+    np.testing.assert_allclose(got["dWo"], leaves["Wo"].grad.numpy(), **tol)
+    np.testing.assert_allclose(got["d_attn"], keep["attn"].grad.reshape(cfg.B * cfg.S, -1).numpy(), **tol)
+    np.testing.assert_allclose(got["dq"], keep["q"].grad.numpy(), **tol)
+    np.testing.assert_allclose(got["dk"], keep["k"].grad.numpy(), **tol)
+    np.testing.assert_allclose(got["dv"], keep["v"].grad.numpy(), **tol)
+    if qk:
+        np.testing.assert_allclose(got["dq_norm_w"], leaves["q_norm_w"].grad.numpy(), **tol)
+        np.testing.assert_allclose(got["dk_norm_w"], leaves["k_norm_w"].grad.numpy(), **tol)
+    else:
+        assert not got["dq_norm_w"].any() and not got["dk_norm_w"].any()
+
+
+def test_attention_backward_stage_equals_library_autograd():
+    """The attention backward alone (16-bit inputs widened exactly) equals
+    torch float64 autograd of SDPA with repeated KV heads."""
+    rng = np.random.default_rng(52)
+    B, S, Hq, Hkv, d = 2, 23, 6, 2, 16
+    Q = torch.from_numpy(rng.standard_normal((B, Hq, S, d))).half()
+    K = torch.from_numpy(rng.standard_normal((B, Hkv, S, d))).half()
+    V = torch.from_numpy(rng.standard_normal((B, Hkv, S, d))).half()
+    dO = torch.from_numpy(rng.standard_normal((B, S, Hq * d))).half()
+    for causal in (True, False):
+        q, k, v = (a.double().requires_grad_(True) for a in (Q, K, V))
+        a = F.scaled_dot_product_attention(q, k.repeat_interleave(Hq // Hkv, 1), v.repeat_interleave(Hq // Hkv, 1),
+                                           is_causal=causal)
+        (a.transpose(1, 2).reshape(B, S, -1) * dO.double()).sum().backward()
+        dq, dk, dv = oracle.attention_backward(Q, K, V, dO, B, S, Hq, Hkv, d, causal=causal, threads=T)
+        np.testing.assert_allclose(dq, q.grad.numpy(), rtol=1e-10, atol=1e-12)
+        np.testing.assert_allclose(dk, k.grad.numpy(), rtol=1e-10, atol=1e-12)
+        np.testing.assert_allclose(dv, v.grad.numpy(), rtol=1e-10, atol=1e-12)
+
+
+def test_attention_backward_closed_forms():
+    """A single key: the softmax is the constant 1, so dq = dk = 0 and dv = dO
+    summed over the group's heads; with dO = 0 every gradient vanishes."""
+    rng = np.random.default_rng(53)
+    B, S, Hq, Hkv, d = 1, 1, 4, 2, 8
+    Q = bf16(rng.standard_normal((B, Hq, S, d)))
+    K = bf16(rng.standard_normal((B, Hkv, S, d)))
+    V = bf16(rng.standard_normal((B, Hkv, S, d)))
+    dO = bf16(rng.standard_normal((B, S, Hq * d)))
+    dq, dk, dv = oracle.attention_backward(Q, K, V, dO, B, S, Hq, Hkv, d, threads=T)
+    assert np.abs(dq).max() < 1e-15 and np.abs(dk).max() < 1e-15
+    do = f64(dO).reshape(B, S, Hq, d).numpy()
+    np.testing.assert_allclose(dv[0, :, 0], do[0, 0].reshape(Hkv, Hq // Hkv, d).sum(1), rtol=1e-14, atol=0)
+    Z = bf16(np.zeros((1, 7, Hq * d)))
+    dq, dk, dv = oracle.attention_backward(bf16(rng.standard_normal((1, Hq, 7, d))),
+                                           bf16(rng.standard_normal((1, Hkv, 7, d))),
+                                           bf16(rng.standard_normal((1, Hkv, 7, d))), Z, 1, 7, Hq, Hkv, d, threads=T)
+    assert not dq.any() and not dk.any() and not dv.any()
