@@ -335,6 +335,43 @@ int gqa_decode_qkv_rd(const gqa_bf16 *x, const gqa_bf16 *Wqkv,
                       gqa_bf16 *k_cache, gqa_bf16 *v_cache, const int *cache_len, int Lmax,
                       gqa_f16 *q_out, void *stream);
 
+/* ---------------------------------------------------------------- backward */
+
+/* Gradients of the whole layer (the derivatives of [T07] §4 steps 1-7 in
+ * reverse order; the K and V projections receive the gradients of every
+ * query head of their group, [NeoX] "Qwen3-0.6B example", [Part]).  Given the
+ * forward's inputs and dout = dL/dout [B, S, hidden] (bf16), writes
+ *   dx        [B, S, hidden]               bf16  (dout plus the path through the projection)
+ *   dWqkv     [(Hq+2Hkv)*head_dim, hidden] fp32
+ *   dWo       [hidden, Hq*head_dim]        fp32
+ *   dq_norm_w, dk_norm_w [head_dim]        fp32  (required with QK-norm, else may be NULL)
+ * The forward is recomputed (Q, K, V, the attention's per-row log-sum-exp);
+ * the attention backward recomputes its probabilities from them.  Full
+ * rotary; head_dim 64 or 128; Hq/Hkv a power of two up to 32, else
+ * GQA_ERR_UNSUPPORTED.  dx must not overlap x or dout.  workspace: at least
+ * gqa_attn_backward_workspace_size(...) bytes, 256-byte aligned.  Enqueued on
+ * `stream`. */
+size_t gqa_attn_backward_workspace_size(int B, int S, int hidden, int Hq, int Hkv, int head_dim);
+int gqa_attn_backward(const gqa_bf16 *x, const gqa_bf16 *Wqkv, const gqa_bf16 *Wo,
+                      const gqa_bf16 *q_norm_w, const gqa_bf16 *k_norm_w,
+                      float rope_theta, float eps,
+                      int B, int S, int hidden, int Hq, int Hkv, int head_dim, int causal,
+                      const gqa_bf16 *dout, gqa_bf16 *dx, float *dWqkv, float *dWo,
+                      float *dq_norm_w, float *dk_norm_w,
+                      void *workspace, size_t workspace_bytes, void *stream);
+
+/* Stage alone: the attention backward.  q [B, Hq, S, head_dim], k and v
+ * [B, Hkv, S, head_dim], dO [B, Hq, S, head_dim] (all binary16, head-major);
+ * writes dq [B, Hq, S, head_dim] and dk, dv [B, Hkv, S, head_dim] in fp32
+ * (dk and dv summed over each group's query heads).  The forward attention
+ * is recomputed into the workspace (gqa_attention_backward_workspace_size
+ * bytes, 256-byte aligned).  Same shape limits as gqa_attn_backward. */
+size_t gqa_attention_backward_workspace_size(int B, int S, int Hq, int head_dim);
+int gqa_attention_backward(const gqa_f16 *q, const gqa_f16 *k, const gqa_f16 *v, const gqa_f16 *dO,
+                           int B, int S, int Hq, int Hkv, int head_dim, int causal,
+                           float *dq, float *dk, float *dv,
+                           void *workspace, size_t workspace_bytes, void *stream);
+
 /* ------------------------------------------------------------ accounting */
 
 /* Algorithmic cost of one prefill forward, all pointers host, any may be NULL

@@ -34,6 +34,8 @@ EXPORTS = (
     "gqa_attn_prefill_cached_workspace_size", "gqa_attn_prefill_cached", "gqa_attention_cached",
     "gqa_attn_forward_rd", "gqa_qkv_proj_rd", "gqa_attn_prefill_cached_rd", "gqa_attn_decode_rd",
     "gqa_decode_qkv_rd", "gqa_attn_decode_fp8", "gqa_decode_qkv_fp8", "gqa_decode_attention_fp8",
+    "gqa_attn_backward_workspace_size", "gqa_attn_backward", "gqa_attention_backward_workspace_size",
+    "gqa_attention_backward",
 )
 
 
@@ -92,6 +94,10 @@ def lib():
     sig["gqa_attn_decode_fp8"] = (_I, [_P] * 5 + [_F, _F] + [_I] * 5 + [_P, _P, _F, _F, _P, _I, _P, _P, _Z, _P])
     sig["gqa_decode_qkv_fp8"] = (_I, [_P] * 4 + [_F, _F] + [_I] * 5 + [_P, _P, _F, _F, _P, _I, _P, _P])
     sig["gqa_decode_attention_fp8"] = (_I, [_P] * 3 + [_F, _F, _P] + [_I] * 5 + [_P, _P, _Z, _P])
+    sig["gqa_attn_backward_workspace_size"] = (_Z, [_I] * 6)
+    sig["gqa_attn_backward"] = (_I, [_P] * 5 + [_F, _F] + [_I] * 7 + [_P] * 6 + [_P, _Z, _P])
+    sig["gqa_attention_backward_workspace_size"] = (_Z, [_I] * 4)
+    sig["gqa_attention_backward"] = (_I, [_P] * 4 + [_I] * 6 + [_P] * 3 + [_P, _Z, _P])
     for name, (res, args) in sig.items():
         fn = getattr(L, name)
         fn.restype = res
@@ -356,3 +362,35 @@ def gqa_decode_attention_fp8(q, k_cache, v_cache, k_scale, v_scale, kv_len, B, H
     _check(lib().gqa_decode_attention_fp8(_f16(q), _u8(k_cache), _u8(v_cache), k_scale, v_scale, _i32(kv_len),
                                           B, Hq, Hkv, head_dim, Lmax, _bf16(attn_out), _ptr(workspace),
                                           workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+# ----------------------------------------------------------------- backward
+
+def _f32(t):
+    if t is not None and t.dtype != torch.float32:
+        raise TypeError(f"expected float32, got {t.dtype}")
+    return _ptr(t)
+
+
+def gqa_attn_backward_workspace_size(B, S, hidden, Hq, Hkv, head_dim) -> int:
+    return int(lib().gqa_attn_backward_workspace_size(B, S, hidden, Hq, Hkv, head_dim))
+
+
+def gqa_attn_backward(x, Wqkv, Wo, q_norm_w, k_norm_w, rope_theta, eps, B, S, hidden, Hq, Hkv, head_dim, causal,
+                      dout, dx, dWqkv, dWo, dq_norm_w, dk_norm_w, workspace, stream=None):
+    """dx bf16; dWqkv, dWo, dq_norm_w, dk_norm_w float32."""
+    _check(lib().gqa_attn_backward(_bf16(x), _bf16(Wqkv), _bf16(Wo), _bf16(q_norm_w), _bf16(k_norm_w), rope_theta,
+                                   eps, B, S, hidden, Hq, Hkv, head_dim, int(causal), _bf16(dout), _bf16(dx),
+                                   _f32(dWqkv), _f32(dWo), _f32(dq_norm_w), _f32(dk_norm_w), _ptr(workspace),
+                                   workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def gqa_attention_backward_workspace_size(B, S, Hq, head_dim) -> int:
+    return int(lib().gqa_attention_backward_workspace_size(B, S, Hq, head_dim))
+
+
+def gqa_attention_backward(q, k, v, dO, B, S, Hq, Hkv, head_dim, causal, dq, dk, dv, workspace, stream=None):
+    """q, k, v, dO float16 head-major; dq, dk, dv float32."""
+    _check(lib().gqa_attention_backward(_f16(q), _f16(k), _f16(v), _f16(dO), B, S, Hq, Hkv, head_dim, int(causal),
+                                        _f32(dq), _f32(dk), _f32(dv), _ptr(workspace),
+                                        workspace.numel() * workspace.element_size(), _stream(stream)))

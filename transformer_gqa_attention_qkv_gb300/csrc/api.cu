@@ -73,7 +73,9 @@ CUresult encode_tmap(CUtensorMap *map, const void *base, int rank, const uint64_
         es[i] = 1;
         if (i + 1 < rank) s[i] = strides_bytes[i];
     }
-    const CUtensorMapDataType type = elem_bytes == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    const CUtensorMapDataType type = elem_bytes == 1   ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                                     : elem_bytes == 4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                                       : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
     return fn(map, type, (cuuint32_t)rank, const_cast<void *>(base), d, s, b, es,
               CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -224,7 +226,8 @@ static FwdLayout fwd_layout(int B, int S, int Hq, int Hkv, int d)
 static int run_qkv(DeviceState &st, const gqa_bf16 *x, const gqa_bf16 *Wqkv, const gqa_bf16 *qn, const gqa_bf16 *kn,
                    float theta, float eps, int rd, int B, int S, int hidden, int Hq, int Hkv, int d, const int *pos_dev,
                    int q_seq, int kv_seq, int rope_rows, int q_f16, int kv_f16, uint16_t *q_out, uint16_t *k_out,
-                   uint16_t *v_out, cudaStream_t stream, int kv_fp8 = 0, float k_scale = 1.0f, float v_scale = 1.0f)
+                   uint16_t *v_out, cudaStream_t stream, int kv_fp8 = 0, float k_scale = 1.0f, float v_scale = 1.0f,
+                   float *pre_out = nullptr)
 {
     const float2 *rope = nullptr;
     if (rd > 0) {
@@ -253,6 +256,7 @@ static int run_qkv(DeviceState &st, const gqa_bf16 *x, const gqa_bf16 *Wqkv, con
     e.q_f16 = q_f16;     // binary16 unless Q meets a bf16 cache in the same MMA
     e.kv_f16 = kv_f16;   // prefill: binary16 workspace; cached paths: the bf16 cache
     e.kv_fp8 = kv_fp8;   // decode into an E4M3 cache
+    e.pre_out = pre_out; // backward: the pre-norm Q/K rows
     e.k_scale = k_scale;
     e.v_scale = v_scale;
     e.q_out = q_out;
@@ -266,9 +270,10 @@ static int run_qkv(DeviceState &st, const gqa_bf16 *x, const gqa_bf16 *Wqkv, con
 
 static int run_attention(DeviceState &st, const uint16_t *q, const uint16_t *k, const uint16_t *v, int B, int S,
                          int Hq, int Hkv, int d, int causal, gqa_bf16 *out, cudaStream_t stream, int kv_seq = 0,
-                         const int *kv_start = nullptr, int bf16_qkv = 0)
+                         const int *kv_start = nullptr, int bf16_qkv = 0, float *lse = nullptr, int lse_ld = 0)
 {
-    AttentionProblem p{q, k, v, out, B, S, Hq, Hkv, d, causal ? 1 : 0, kv_seq > 0 ? kv_seq : S, kv_start, bf16_qkv};
+    AttentionProblem p{q,         k,        v,        out, B,   S,      Hq, Hkv, d, causal ? 1 : 0,
+                       kv_seq > 0 ? kv_seq : S, kv_start, bf16_qkv, lse, lse_ld};
     cudaError_t ce = launch_attention(p, st.err, st.num_sms, stream);
     if (ce != cudaSuccess) return cuda_fail(ce, "attention launch");
     ++g_launches;
@@ -449,6 +454,215 @@ int gqa_attn_forward(const gqa_bf16 *x, const gqa_bf16 *Wqkv, const gqa_bf16 *Wo
     }
     return gqa_attn_forward_ex(x, Wqkv, Wo, q_norm_w, k_norm_w, rope_theta, eps, B, S, hidden, Hq, Hkv, head_dim,
                                causal, out, ws, need, nullptr);
+}
+
+// ---------------------------------------------------------------- backward
+
+// Attention backward workspace: o (bf16 [B*S, Hq*d]), lse and D (fp32 [B*Hq, ld]).
+struct AttnBwdLayout {
+    size_t o, lse, dsum, total;
+    int ld;
+};
+
+static AttnBwdLayout attn_bwd_layout(int B, int S, int Hq, int d)
+{
+    AttnBwdLayout L;
+    L.ld = (S + 3) & ~3;
+    L.o = 0;
+    L.lse = align256((size_t)B * S * Hq * d * 2);
+    L.dsum = L.lse + align256((size_t)B * Hq * L.ld * 4);
+    L.total = L.dsum + align256((size_t)B * Hq * L.ld * 4);
+    return L;
+}
+
+static int check_backward(int B, int S, int hidden, int Hq, int Hkv, int d, const void *qn, const void *kn)
+{
+    int rc = check_layer(B, S, hidden, Hq, Hkv, d, qn, kn);
+    if (rc) return rc;
+    if ((rc = check_group_pow2(Hq, Hkv))) return rc;
+    if (d != 64 && d != 128) return fail(GQA_ERR_UNSUPPORTED, "the backward supports head_dim 64 and 128 (got %d)", d);
+    if (Hq / Hkv > 32)
+        return fail(GQA_ERR_UNSUPPORTED, "the backward supports groups of up to 32 query heads (got %d)", Hq / Hkv);
+    return GQA_OK;
+}
+
+// The attention backward from q, k, v (forward recomputed for o and lse).
+static int run_attention_bwd(DeviceState &st, const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                             const uint16_t *dO, int B, int S, int Hq, int Hkv, int d, int causal, float *dq,
+                             float *dk, float *dv, uint8_t *ws, cudaStream_t s)
+{
+    const AttnBwdLayout L = attn_bwd_layout(B, S, Hq, d);
+    gqa_bf16 *o = (gqa_bf16 *)(ws + L.o);
+    float *lse = (float *)(ws + L.lse), *dsum = (float *)(ws + L.dsum);
+    int rc = run_attention(st, q, k, v, B, S, Hq, Hkv, d, causal, o, s, 0, nullptr, 0, lse, L.ld);
+    if (rc) return rc;
+    AttnBwdProblem p{q, k, v, o, dO, lse, dsum, L.ld, dq, dk, dv, B, S, Hq, Hkv, d, causal ? 1 : 0};
+    cudaError_t ce = launch_attention_backward(p, st.err, s);
+    if (ce != cudaSuccess) return cuda_fail(ce, "attention backward launch");
+    g_launches += 3;
+    return GQA_OK;
+}
+
+size_t gqa_attention_backward_workspace_size(int B, int S, int Hq, int head_dim)
+{
+    if (B <= 0 || S <= 0 || Hq <= 0 || head_dim <= 0) return 0;
+    return attn_bwd_layout(B, S, Hq, head_dim).total;
+}
+
+int gqa_attention_backward(const gqa_f16 *q, const gqa_f16 *k, const gqa_f16 *v, const gqa_f16 *dO, int B, int S,
+                           int Hq, int Hkv, int head_dim, int causal, float *dq, float *dk, float *dv,
+                           void *workspace, size_t workspace_bytes, void *stream)
+{
+    g_launches = 0;
+    int rc = check_backward(B, S, 8, Hq, Hkv, head_dim, nullptr, nullptr);
+    if (rc) return rc;
+    if (!q || !k || !v || !dO || !dq || !dk || !dv) return fail(GQA_ERR_ARG, "null tensor pointer");
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(dO) || !aligned16(dq) || !aligned16(dk) ||
+        !aligned16(dv))
+        return fail(GQA_ERR_ARG, "tensor pointers must be 16-byte aligned");
+    const size_t need = attn_bwd_layout(B, S, Hq, head_dim).total;
+    if (!workspace || workspace_bytes < need)
+        return fail(GQA_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", need,
+                    workspace ? workspace_bytes : (size_t)0);
+    if (((uintptr_t)workspace & 255u) != 0) return fail(GQA_ERR_ARG, "workspace must be 256-byte aligned");
+    DeviceState *st;
+    if ((rc = device_state(&st))) return rc;
+    return run_attention_bwd(*st, q, k, v, dO, B, S, Hq, Hkv, head_dim, causal, dq, dk, dv, (uint8_t *)workspace,
+                             (cudaStream_t)stream);
+}
+
+// Layer backward workspace: the forward's q, k, v (binary16, head-major) and
+// pre-norm Q/K rows (fp32), dO (binary16, head-major), the attention-input
+// gradients (fp32), dqkv (bf16), then the attention backward's own part.
+struct LayerBwdLayout {
+    size_t q, k, v, pre, dO, dq, dk, dv, dqkv, norm, attn, total;
+};
+
+static LayerBwdLayout layer_bwd_layout(int B, int S, int Hq, int Hkv, int d)
+{
+    LayerBwdLayout L;
+    const size_t M = (size_t)B * S;
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        const size_t at = off;
+        off += align256(bytes);
+        return at;
+    };
+    L.q = take(M * Hq * d * 2);
+    L.k = take(M * Hkv * d * 2);
+    L.v = take(M * Hkv * d * 2);
+    L.pre = take(M * (Hq + Hkv) * d * 4);
+    L.dO = take(M * Hq * d * 2);
+    L.dq = take(M * Hq * d * 4);
+    L.dk = take(M * Hkv * d * 4);
+    L.dv = take(M * Hkv * d * 4);
+    L.dqkv = take(M * (Hq + 2 * Hkv) * d * 2);
+    L.norm = take(2 * d * 4);
+    L.attn = take(attn_bwd_layout(B, S, Hq, d).total);
+    L.total = off;
+    return L;
+}
+
+size_t gqa_attn_backward_workspace_size(int B, int S, int hidden, int Hq, int Hkv, int head_dim)
+{
+    if (B <= 0 || S <= 0 || hidden <= 0 || Hq <= 0 || Hkv <= 0 || head_dim <= 0) return 0;
+    return layer_bwd_layout(B, S, Hq, Hkv, head_dim).total;
+}
+
+int gqa_attn_backward(const gqa_bf16 *x, const gqa_bf16 *Wqkv, const gqa_bf16 *Wo, const gqa_bf16 *q_norm_w,
+                      const gqa_bf16 *k_norm_w, float rope_theta, float eps, int B, int S, int hidden, int Hq,
+                      int Hkv, int head_dim, int causal, const gqa_bf16 *dout, gqa_bf16 *dx, float *dWqkv,
+                      float *dWo, float *dq_norm_w, float *dk_norm_w, void *workspace, size_t workspace_bytes,
+                      void *stream)
+{
+    g_launches = 0;
+    int rc = check_backward(B, S, hidden, Hq, Hkv, head_dim, q_norm_w, k_norm_w);
+    if (rc) return rc;
+    if (!x || !Wqkv || !Wo || !dout || !dx || !dWqkv || !dWo) return fail(GQA_ERR_ARG, "null tensor pointer");
+    if (q_norm_w && (!dq_norm_w || !dk_norm_w))
+        return fail(GQA_ERR_ARG, "dq_norm_w and dk_norm_w are required with QK-norm");
+    if (!aligned16(x) || !aligned16(Wqkv) || !aligned16(Wo) || !aligned16(dout) || !aligned16(dx) ||
+        !aligned16(dWqkv) || !aligned16(dWo))
+        return fail(GQA_ERR_ARG, "tensor pointers must be 16-byte aligned");
+    if (!(rope_theta > 0.0f) || !(eps >= 0.0f)) return fail(GQA_ERR_ARG, "rope_theta must be > 0 and eps >= 0");
+    const size_t nx = (size_t)B * S * hidden * 2;
+    if (overlap(dx, nx, dout, nx) || overlap(dx, nx, x, nx)) return fail(GQA_ERR_ARG, "dx must not overlap x or dout");
+    const LayerBwdLayout L = layer_bwd_layout(B, S, Hq, Hkv, head_dim);
+    if (!workspace || workspace_bytes < L.total)
+        return fail(GQA_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", L.total,
+                    workspace ? workspace_bytes : (size_t)0);
+    if (((uintptr_t)workspace & 255u) != 0) return fail(GQA_ERR_ARG, "workspace must be 256-byte aligned");
+    DeviceState *st;
+    if ((rc = device_state(&st))) return rc;
+    uint8_t *ws = (uint8_t *)workspace;
+    const int d = head_dim, M = B * S, NQ = Hq * d, N = (Hq + 2 * Hkv) * d;
+    uint16_t *q = (uint16_t *)(ws + L.q), *k = (uint16_t *)(ws + L.k), *v = (uint16_t *)(ws + L.v);
+    uint16_t *dO = (uint16_t *)(ws + L.dO), *dqkv = (uint16_t *)(ws + L.dqkv);
+    float *pre = q_norm_w ? (float *)(ws + L.pre) : nullptr;
+    float *dq = (float *)(ws + L.dq), *dk = (float *)(ws + L.dk), *dv = (float *)(ws + L.dv);
+    float *dqn = dq_norm_w ? dq_norm_w : (float *)(ws + L.norm);
+    float *dkn = dk_norm_w ? dk_norm_w : (float *)(ws + L.norm) + d;
+    uint8_t *aws = ws + L.attn;
+    const gqa_bf16 *o = (const gqa_bf16 *)(aws + attn_bwd_layout(B, S, Hq, d).o);
+    cudaStream_t s = (cudaStream_t)stream;
+    // 1. the forward's Q, K, V (binary16) and pre-norm rows
+    if ((rc = run_qkv(*st, x, Wqkv, q_norm_w, k_norm_w, rope_theta, eps, d, B, S, hidden, Hq, Hkv, d, nullptr, S, S,
+                      S, 1, 1, q, k, v, s, 0, 1.0f, 1.0f, pre)))
+        return rc;
+    // 2. dO = dout Wo, head-major binary16
+    {
+        GemmProblem p{dout, Wo, M, NQ, hidden};
+        GemmOut go{};
+        go.head = HeadEpilogue{dO, S, Hq, d};
+        cudaError_t ce = launch_gemm_general(p, 0, 1, GEMM_OUT_HEAD16, go, st->err, st->num_sms, s);
+        if (ce != cudaSuccess) return cuda_fail(ce, "dO = dout Wo launch");
+        ++g_launches;
+    }
+    // 3. attention backward (forward recomputed for o and lse)
+    if ((rc = run_attention_bwd(*st, q, k, v, dO, B, S, Hq, Hkv, d, causal, dq, dk, dv, aws, s))) return rc;
+    // 4. inverse RoPE and the QK-norm gradient -> dqkv
+    {
+        const float2 *rope = nullptr;
+        {
+            std::lock_guard<std::mutex> lk(g_mu);
+            rc = rope_table(*st, (double)rope_theta, d, S, &rope);
+        }
+        if (rc) return rc;
+        cudaError_t ce = cudaMemsetAsync(dqn, 0, d * sizeof(float), s);
+        if (ce == cudaSuccess) ce = cudaMemsetAsync(dkn, 0, d * sizeof(float), s);
+        if (ce != cudaSuccess) return cuda_fail(ce, "cudaMemsetAsync(norm-weight gradients)");
+        RopeNormBwd rp{dq, dk, dv, pre, rope, q_norm_w, k_norm_w, eps, dqkv, dqn, dkn, M, S, N, Hq, Hkv, d};
+        ce = launch_rope_norm_bwd(rp, s);
+        if (ce != cudaSuccess) return cuda_fail(ce, "RoPE / QK-norm backward launch");
+        ++g_launches;
+    }
+    // 5. dx = dout + dqkv Wqkv
+    {
+        GemmProblem p{dqkv, Wqkv, M, hidden, N};
+        GemmOut go{};
+        go.res = ResidualEpilogue{dout, dx};
+        cudaError_t ce = launch_gemm_general(p, 0, 1, GEMM_OUT_RESIDUAL, go, st->err, st->num_sms, s);
+        if (ce != cudaSuccess) return cuda_fail(ce, "dx launch");
+        ++g_launches;
+    }
+    // 6. dWqkv = dqkv^T x;  7. dWo = dout^T attn
+    {
+        GemmProblem p{dqkv, x, N, hidden, M};
+        GemmOut go{};
+        go.f32 = dWqkv;
+        cudaError_t ce = launch_gemm_general(p, 1, 1, GEMM_OUT_F32, go, st->err, st->num_sms, s);
+        if (ce != cudaSuccess) return cuda_fail(ce, "dWqkv launch");
+        ++g_launches;
+    }
+    {
+        GemmProblem p{dout, o, hidden, NQ, M};
+        GemmOut go{};
+        go.f32 = dWo;
+        cudaError_t ce = launch_gemm_general(p, 1, 1, GEMM_OUT_F32, go, st->err, st->num_sms, s);
+        if (ce != cudaSuccess) return cuda_fail(ce, "dWo launch");
+        ++g_launches;
+    }
+    return GQA_OK;
 }
 
 // ------------------------------------------------------------------ decode

@@ -50,6 +50,8 @@ struct AttnParams {
     const int *kv_start;   // device [B]: cached keys before the queries (NULL: none)
     float scale_log2;  // log2(e) / sqrt(d)
     uint16_t *out;
+    float *lse;        // optional log2-sum-exp at lse[(b*Hq + head)*lse_ld + t] (plain prefill)
+    int lse_ld;
     unsigned *err;
 };
 
@@ -308,6 +310,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float inv_l = (l_i > 0.0f) ? 1.0f / l_i : 0.0f;
             const int head = g * P.G + hl;
             uint16_t *dst = P.out + ((size_t)(b * P.S + t) * P.Hq + head) * D;
+            if (!CACHED && P.lse && row_ok) P.lse[(size_t)(b * P.Hq + head) * P.lse_ld + t] = m_i + log2f(l_i);
 #pragma unroll 1
             for (int c = 0; c < D; c += 32) {
                 uint32_t o[32];
@@ -366,6 +369,8 @@ cudaError_t run_attn(const AttentionProblem &p, unsigned *err, cudaStream_t stre
     a.kv_seq = p.kv_seq;
     a.kv_start = p.kv_start;
     a.out = p.out;
+    a.lse = p.lse;
+    a.lse_ld = p.lse_ld;
     a.err = err;
     auto kern = attn_kernel<D, BF>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC);

@@ -1,0 +1,120 @@
+// backward.cu -- the elementwise part of the layer's backward: inverse RoPE
+// and the RMSNorm (QK-norm) gradient, from the attention-input gradients to
+// the gradient of the fused projection's output.
+//
+// For one Q or K head row at position t (the derivatives of [T07] §3 and §4
+// steps 2-3; rotation pairs (i, i + d/2) at angle t * theta^(-2i/d)):
+//   dn = RoPE^T(dy)                       (rotation by -angle)
+//   u = x r, r = (mean(x^2) + eps)^(-1/2)  (x: the pre-norm row of the forward)
+//   dx_i = r (w_i dn_i - u_i / d * sum_k u_k w_k dn_k),   dw_i += u_i dn_i
+// Without QK-norm dx = dn.  V rows pass unchanged.  One warp per (token,
+// head) row; lane l holds elements l, l + 32, ... (so the rotation pairs are
+// lane-local); the norm-weight gradients are summed per block in shared
+// memory and added to the global [d] vectors once per block.
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace gqa {
+
+namespace {
+
+constexpr int kWarpsPerBlock = 8;
+
+template <int D>
+__global__ void __launch_bounds__(32 * kWarpsPerBlock)
+    rope_norm_bwd_kernel(const RopeNormBwd P)
+{
+    constexpr int E = D / 32;   // elements per lane
+    __shared__ float s_dw[2][D];  // q_norm_w, k_norm_w gradients of this block
+    for (int i = threadIdx.x; i < 2 * D; i += blockDim.x) (&s_dw[0][0])[i] = 0.0f;
+    __syncthreads();
+    const int lane = threadIdx.x % 32;
+    const int NH = P.Hq + P.Hkv;
+    const long row = (long)blockIdx.x * kWarpsPerBlock + threadIdx.x / 32;  // m * NH + h
+    if (row < (long)P.M * NH) {
+        const long m = row / NH;
+        const int h = (int)(row - m * NH);
+        const int b = (int)(m / P.S), t = (int)(m - (long)b * P.S);
+        const bool isq = h < P.Hq;
+        const int head = isq ? h : h - P.Hq;
+        const float *dy = isq ? P.dq + ((size_t)(b * P.Hq + head) * P.S + t) * D
+                              : P.dk + ((size_t)(b * P.Hkv + head) * P.S + t) * D;
+        float y[E];
+#pragma unroll
+        for (int e = 0; e < E; ++e) y[e] = dy[lane + 32 * e];
+        // inverse rotation: element i = lane + 32e pairs with i + D/2 = lane + 32(e + E/2)
+        const float2 *cs = P.rope + (size_t)t * (D / 2);
+#pragma unroll
+        for (int e = 0; e < E / 2; ++e) {
+            const float2 c = cs[lane + 32 * e];
+            const float a = y[e], bb = y[e + E / 2];
+            y[e] = a * c.x + bb * c.y;
+            y[e + E / 2] = bb * c.x - a * c.y;
+        }
+        const int col = isq ? head * D : P.Hq * D + head * D;
+        uint16_t *dst = P.dqkv + (size_t)m * P.N + col;
+        if (P.pre) {
+            const uint16_t *w = isq ? P.q_norm_w : P.k_norm_w;
+            const float *x = P.pre + (size_t)m * NH * D + (size_t)h * D;
+            float xv[E], wv[E], ss = 0.0f;
+#pragma unroll
+            for (int e = 0; e < E; ++e) {
+                xv[e] = x[lane + 32 * e];
+                wv[e] = bf16lo(w[lane + 32 * e]);
+                ss = fmaf(xv[e], xv[e], ss);
+            }
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+            const float r = 1.0f / sqrtf(ss * (1.0f / D) + P.eps);
+            float dot = 0.0f;
+#pragma unroll
+            for (int e = 0; e < E; ++e) dot = fmaf(xv[e] * r * wv[e], y[e], dot);
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, off);
+#pragma unroll
+            for (int e = 0; e < E; ++e) {
+                const float u = xv[e] * r;
+                atomicAdd(&s_dw[isq ? 0 : 1][lane + 32 * e], u * y[e]);
+                y[e] = r * (wv[e] * y[e] - u * dot * (1.0f / D));
+            }
+        }
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+            const __nv_bfloat16 v = __float2bfloat16_rn(y[e]);
+            dst[lane + 32 * e] = *reinterpret_cast<const uint16_t *>(&v);
+        }
+        if (!isq) {  // the V row of the same KV head passes unchanged
+            const float *dv = P.dv + ((size_t)(b * P.Hkv + head) * P.S + t) * D;
+            uint16_t *vdst = P.dqkv + (size_t)m * P.N + (P.Hq + P.Hkv) * D + head * D;
+#pragma unroll
+            for (int e = 0; e < E; ++e) {
+                const __nv_bfloat16 v = __float2bfloat16_rn(dv[lane + 32 * e]);
+                vdst[lane + 32 * e] = *reinterpret_cast<const uint16_t *>(&v);
+            }
+        }
+    }
+    if (P.pre) {
+        __syncthreads();
+        for (int i = threadIdx.x; i < D; i += blockDim.x) {
+            atomicAdd(P.dq_norm_w + i, s_dw[0][i]);
+            atomicAdd(P.dk_norm_w + i, s_dw[1][i]);
+        }
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_rope_norm_bwd(const RopeNormBwd &p, cudaStream_t stream)
+{
+    const long rows = (long)p.M * (p.Hq + p.Hkv);
+    const unsigned grid = (unsigned)((rows + kWarpsPerBlock - 1) / kWarpsPerBlock);
+    if (p.d == 128)
+        rope_norm_bwd_kernel<128><<<grid, 32 * kWarpsPerBlock, 0, stream>>>(p);
+    else if (p.d == 64)
+        rope_norm_bwd_kernel<64><<<grid, 32 * kWarpsPerBlock, 0, stream>>>(p);
+    else
+        return cudaErrorInvalidValue;
+    return cudaGetLastError();
+}
+
+}  // namespace gqa

@@ -25,7 +25,15 @@ constexpr int BM = 128;
 constexpr int BK = 64;  // one 128-byte swizzle row of bf16
 constexpr int kThreads = 192;
 
-enum { EPI_QKV = 0, EPI_RESIDUAL = 1 };
+enum { EPI_QKV = 0, EPI_RESIDUAL = 1, EPI_F32 = 2, EPI_HEAD16 = 3 };
+
+// Operand storage: K-major (the contraction index contiguous: A [M, K], B
+// [N, K]) or MN-major (the row / column index contiguous: A stored [K, M],
+// B stored [K, N]).  MAJ bit 0: A is MN-major; bit 1: B is MN-major.  An
+// MN-major tile sits in shared memory as 64-wide column chunks of BK rows
+// (128-byte swizzle), the layout the tensor core reads with the operand's
+// major bit set.
+constexpr int kMnChunk = 64 * BK * 2;  // one 64-wide MN chunk of BK rows: 8 KB
 
 struct GemmParams {
     int M, N, K;
@@ -34,6 +42,8 @@ struct GemmParams {
     unsigned *err;
     QkvEpilogue qkv;
     ResidualEpilogue res;
+    float *f32_out;         // EPI_F32: C [M, N] fp32
+    HeadEpilogue head;      // EPI_HEAD16
 };
 
 template <int BN, int STAGES>
@@ -187,6 +197,51 @@ DEVI void rope_store(uint32_t col, void *dst, float rinv, bool has_norm, const f
     }
 }
 
+// fp32 C rows (N a multiple of 8).
+template <int BN>
+DEVI void epilogue_f32(const GemmParams &P, uint32_t tcol, int m, int n0, bool row_ok)
+{
+#pragma unroll 1
+    for (int c = 0; c < BN; c += 32) {
+        const int n = n0 + c;
+        if (n >= P.N) break;  // uniform across the warp
+        uint32_t r[32];
+        tmem_ld32(tcol + c, r);
+        if (!row_ok) continue;
+        float4 *dst = reinterpret_cast<float4 *>(P.f32_out + (size_t)m * P.N + n);
+#pragma unroll
+        for (int v = 0; v < 8; ++v) {
+            if (n + 4 * v >= P.N) break;
+            dst[v] = make_float4(__uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]),
+                                 __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3]));
+        }
+    }
+}
+
+// binary16 head-major output: column n = j*d + c of row m = b*S + t goes to
+// out[((b*H + j)*S + t)*d + c] (clamped to binary16's range and flagged).
+template <int BN>
+DEVI void epilogue_head16(const GemmParams &P, uint32_t tcol, int m, int n0, bool row_ok)
+{
+    const HeadEpilogue &e = P.head;
+    const int b = m / e.S, t = m - (m / e.S) * e.S;
+    bool clamped = false;
+#pragma unroll 1
+    for (int c = 0; c < BN; c += 32) {
+        const int n = n0 + c;
+        if (n >= P.N) break;
+        uint32_t r[32];
+        tmem_ld32(tcol + c, r);
+        if (!row_ok) continue;
+        const int j = n / e.d, cc = n - j * e.d;
+        float v[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+        store32(e.out + ((size_t)(b * e.H + j) * e.S + t) * e.d + cc, v, true, clamped);
+    }
+    if (clamped) atomicOr(P.err, kErrRange);
+}
+
 // Epilogue of one QKV tile row: BN columns = BN/D whole heads.
 template <int BN, int D>
 DEVI void epilogue_qkv(const GemmParams &P, uint32_t tcol, int m, int n0, bool row_ok, const float *s_norm)
@@ -261,6 +316,9 @@ DEVI void epilogue_qkv(const GemmParams &P, uint32_t tcol, int m, int n0, bool r
         float rinv = 1.0f;
         if (has_norm) {
             float ss = 0.0f;
+            // pre-norm Q/K rows for the backward's RMSNorm gradient: [M, (Hq+Hkv)*D] fp32
+            float *pre = e.pre_out ? e.pre_out + (size_t)m * (e.Hq + e.Hkv) * D + (kind == 0 ? head : e.Hq + head) * D
+                                   : nullptr;
 #pragma unroll 1
             for (int c = 0; c < D; c += 32) {
                 uint32_t r[32];
@@ -269,6 +327,13 @@ DEVI void epilogue_qkv(const GemmParams &P, uint32_t tcol, int m, int n0, bool r
                 for (int i = 0; i < 32; ++i) {
                     const float f = __uint_as_float(r[i]);
                     ss = fmaf(f, f, ss);
+                }
+                if (pre && row_ok) {
+                    float4 *d4 = reinterpret_cast<float4 *>(pre + c);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        d4[i] = make_float4(__uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1]),
+                                            __uint_as_float(r[4 * i + 2]), __uint_as_float(r[4 * i + 3]));
                 }
             }
             rinv = 1.0f / sqrtf(ss * (1.0f / D) + e.eps);
@@ -316,10 +381,11 @@ DEVI void epilogue_residual(const GemmParams &P, uint32_t tcol, int m, int n0, b
     }
 }
 
-template <int BN, int STAGES, int EPI, int D>
+template <int BN, int STAGES, int EPI, int D, int MAJ>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const GemmParams P)
 {
+    constexpr bool AMN = MAJ & 1, BMN = (MAJ >> 1) & 1;
     using L = Smem<BN, STAGES>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -378,8 +444,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                         break;
                     }
                     mbar_arrive_expect_tx(full + s, L::A_BYTES + L::B_BYTES);
-                    tma_load_2d(sA + s * L::A_BYTES, &tmA, kb * BK, mb * BM, full + s);
-                    tma_load_2d(sB + s * L::B_BYTES, &tmB, kb * BK, nb * BN, full + s);
+                    if constexpr (AMN) {
+                        for (int c = 0; c < BM / 64; ++c)
+                            tma_load_2d(sA + s * L::A_BYTES + c * kMnChunk, &tmA, mb * BM + c * 64, kb * BK, full + s);
+                    } else {
+                        tma_load_2d(sA + s * L::A_BYTES, &tmA, kb * BK, mb * BM, full + s);
+                    }
+                    if constexpr (BMN) {
+                        for (int c = 0; c < BN / 64; ++c)
+                            tma_load_2d(sB + s * L::B_BYTES + c * kMnChunk, &tmB, nb * BN + c * 64, kb * BK, full + s);
+                    } else {
+                        tma_load_2d(sB + s * L::B_BYTES, &tmB, kb * BK, nb * BN, full + s);
+                    }
                 }
             }
             // every issued copy has landed before the CTA may exit
@@ -387,7 +463,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp == 1) {
         if (lane == 0) {
-            constexpr uint32_t idesc = idesc_bf16_f32(BM, BN, 0, 0);
+            constexpr uint32_t idesc = idesc_bf16_f32(BM, BN, AMN ? 1 : 0, BMN ? 1 : 0);
             int it = 0, use = 0;
             bool ok = true;
             for (int tile = blockIdx.x; ok && tile < P.num_tiles; tile += gridDim.x, ++use) {
@@ -405,9 +481,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint32_t a0 = smem_u32(sA + s * L::A_BYTES);
                     const uint32_t b0 = smem_u32(sB + s * L::B_BYTES);
 #pragma unroll
-                    for (int k = 0; k < BK / 16; ++k)
-                        umma_f16_ss(d_tmem, sw128_desc(a0 + 32 * k, 16, 1024), sw128_desc(b0 + 32 * k, 16, 1024),
-                                     idesc, (kb | k) != 0);
+                    for (int k = 0; k < BK / 16; ++k) {
+                        // K-major: the next 16 K values are 32 bytes along the row; MN-major:
+                        // the next 16 K rows are 2 KB down each 64-wide chunk
+                        const uint64_t ad = AMN ? sw128_desc(a0 + k * 16 * 128, kMnChunk, 1024)
+                                                : sw128_desc(a0 + 32 * k, 16, 1024);
+                        const uint64_t bd = BMN ? sw128_desc(b0 + k * 16 * 128, kMnChunk, 1024)
+                                                : sw128_desc(b0 + 32 * k, 16, 1024);
+                        umma_f16_ss(d_tmem, ad, bd, idesc, (kb | k) != 0);
+                    }
                     umma_commit(empty + s);  // frees the stage once these MMAs have read it
                 }
                 if (!ok) break;
@@ -431,8 +513,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             const bool row_ok = m < P.M;
             if constexpr (EPI == EPI_QKV)
                 epilogue_qkv<BN, D>(P, tcol, m, nb * BN, row_ok, s_norm);
-            else
+            else if constexpr (EPI == EPI_RESIDUAL)
                 epilogue_residual<BN>(P, tcol, m, nb * BN, row_ok);
+            else if constexpr (EPI == EPI_F32)
+                epilogue_f32<BN>(P, tcol, m, nb * BN, row_ok);
+            else
+                epilogue_head16<BN>(P, tcol, m, nb * BN, row_ok);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(tempty + acc);
@@ -445,17 +531,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-template <int BN, int STAGES, int EPI, int D>
+template <int BN, int STAGES, int EPI, int D, int MAJ = 0>
 cudaError_t run(const GemmProblem &p, const GemmParams &params, int num_sms, cudaStream_t stream)
 {
     using L = Smem<BN, STAGES>;
+    constexpr bool AMN = MAJ & 1, BMN = (MAJ >> 1) & 1;
     CUtensorMap ta, tb;
-    const uint64_t dA[2] = {(uint64_t)p.K, (uint64_t)p.M}, sA[1] = {(uint64_t)p.K * 2};
-    const uint64_t dB[2] = {(uint64_t)p.K, (uint64_t)p.N}, sB[1] = {(uint64_t)p.K * 2};
-    const uint32_t bA[2] = {BK, BM}, bB[2] = {BK, BN};
+    // K-major A [M, K]: box {BK, BM}; MN-major A stored [K, M]: box {64, BK} per 64-wide chunk
+    const uint64_t dA[2] = {AMN ? (uint64_t)p.M : (uint64_t)p.K, AMN ? (uint64_t)p.K : (uint64_t)p.M};
+    const uint64_t sA[1] = {(AMN ? (uint64_t)p.M : (uint64_t)p.K) * 2};
+    const uint64_t dB[2] = {BMN ? (uint64_t)p.N : (uint64_t)p.K, BMN ? (uint64_t)p.K : (uint64_t)p.N};
+    const uint64_t sB[1] = {(BMN ? (uint64_t)p.N : (uint64_t)p.K) * 2};
+    const uint32_t bA[2] = {AMN ? 64u : (uint32_t)BK, AMN ? (uint32_t)BK : (uint32_t)BM};
+    const uint32_t bB[2] = {BMN ? 64u : (uint32_t)BK, BMN ? (uint32_t)BK : (uint32_t)BN};
     if (encode_tmap(&ta, p.A, 2, dA, sA, bA, true) != CUDA_SUCCESS) return cudaErrorInvalidValue;
     if (encode_tmap(&tb, p.B, 2, dB, sB, bB, true) != CUDA_SUCCESS) return cudaErrorInvalidValue;
-    auto kern = gemm_kernel<BN, STAGES, EPI, D>;
+    auto kern = gemm_kernel<BN, STAGES, EPI, D, MAJ>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC);
     if (e != cudaSuccess) return e;
     const int grid = params.num_tiles < num_sms ? params.num_tiles : num_sms;
@@ -526,6 +617,32 @@ cudaError_t launch_gemm_residual(const GemmProblem &p, const ResidualEpilogue &e
     g.res = e;
     g.group_m = 16;  // o_proj's A panels are twice as long (K = Hq*d): half the group
     return run<256, 4, EPI_RESIDUAL, 0>(p, g, num_sms, stream);
+}
+
+}  // namespace gqa
+
+namespace gqa {
+
+// Backward-pass products (see internal.h).
+cudaError_t launch_gemm_general(const GemmProblem &p, int a_mn, int b_mn, int epi, const GemmOut &o, unsigned *err,
+                                int num_sms, cudaStream_t stream)
+{
+    GemmParams g = make_params(p, 256, err);
+    g.f32_out = o.f32;
+    g.head = o.head;
+    g.res = o.res;
+    const int maj = (a_mn ? 1 : 0) | (b_mn ? 2 : 0);
+#define GQA_RUN(E, M_) return run<256, 4, E, 0, M_>(p, g, num_sms, stream)
+    if (epi == GEMM_OUT_F32) {
+        if (maj == 3) GQA_RUN(EPI_F32, 3);
+        if (maj == 0) GQA_RUN(EPI_F32, 0);
+    } else if (epi == GEMM_OUT_HEAD16) {
+        if (maj == 2) GQA_RUN(EPI_HEAD16, 2);
+    } else if (epi == GEMM_OUT_RESIDUAL) {
+        if (maj == 2) GQA_RUN(EPI_RESIDUAL, 2);
+    }
+#undef GQA_RUN
+    return cudaErrorInvalidValue;
 }
 
 }  // namespace gqa

@@ -31,6 +31,7 @@ struct QkvEpilogue {
     int kv_f16;            // 1: K and V stored as binary16 (clamped, flagged); 0: bf16
     int kv_fp8;            // 1: K and V stored as E4M3 codes of value / k_scale, value / v_scale
     float k_scale, v_scale;
+    float *pre_out;        // non-NULL (with QK-norm): pre-norm Q and K rows, [M, (Hq+Hkv)*d] fp32
     uint16_t *q_out, *k_out, *v_out;
 };
 
@@ -40,10 +41,26 @@ struct ResidualEpilogue {
     uint16_t *out;
 };
 
+// Epilogue "head16": C written head-major in binary16 (the attention
+// gradient dO of the backward): column j*d + c of row b*S + t goes to
+// out[((b*H + j)*S + t)*d + c].
+struct HeadEpilogue {
+    uint16_t *out;
+    int S, H, d;
+};
+
 struct GemmProblem {
-    const void *A;  // [M, K] bf16
-    const void *B;  // [N, K] bf16
+    const void *A;  // [M, K] bf16 (stored [K, M] when MN-major)
+    const void *B;  // [N, K] bf16 (stored [K, N] when MN-major)
     int M, N, K;
+};
+
+// Output of launch_gemm_general.
+enum { GEMM_OUT_F32 = 0, GEMM_OUT_HEAD16 = 1, GEMM_OUT_RESIDUAL = 2 };
+struct GemmOut {
+    float *f32;             // GEMM_OUT_F32: [M, N]
+    HeadEpilogue head;      // GEMM_OUT_HEAD16
+    ResidualEpilogue res;   // GEMM_OUT_RESIDUAL: bf16 out = C + resid
 };
 
 // Launchers return a cudaError_t (cudaSuccess when enqueued).
@@ -51,6 +68,11 @@ cudaError_t launch_gemm_qkv(const GemmProblem &p, const QkvEpilogue &e, unsigned
                             cudaStream_t stream);
 cudaError_t launch_gemm_residual(const GemmProblem &p, const ResidualEpilogue &e, unsigned *err, int num_sms,
                                  cudaStream_t stream);
+// The backward's products: A and/or B MN-major (a_mn, b_mn), 256-wide tiles.
+// Implemented: F32 with both K-major or both MN-major; HEAD16 and RESIDUAL with B
+// MN-major.  Other combinations return cudaErrorInvalidValue.
+cudaError_t launch_gemm_general(const GemmProblem &p, int a_mn, int b_mn, int epi, const GemmOut &o, unsigned *err,
+                                int num_sms, cudaStream_t stream);
 
 // ------------------------------------------------------- prefill attention
 struct AttentionProblem {
@@ -62,8 +84,41 @@ struct AttentionProblem {
     int kv_seq;            // sequence extent of k/v (S, or Lmax for a cache)
     const int *kv_start;   // device [B]: keys already cached before the S queries (NULL: 0)
     int bf16_qkv;          // 1: q/k/v bf16 (P bf16); 0: binary16 (P binary16)
+    float *lse;            // non-NULL (plain prefill only): per (b, head, t) log2-sum-exp of the
+                           // scaled scores, at lse[(b*Hq + head)*lse_ld + t]: P = 2^(s*log2(e)/sqrt(d) - lse)
+    int lse_ld;
 };
 cudaError_t launch_attention(const AttentionProblem &p, unsigned *err, int num_sms, cudaStream_t stream);
+// Backward of the attention (head_dim 64 / 128, Hq/Hkv <= 32).  q, k, v, dO
+// binary16 head-major ([B, H, S, d]); o the forward's bf16 output [B, S,
+// Hq*d]; lse the forward's log2-sum-exp and dsum a workspace, both fp32
+// [B*Hq, ld] with ld >= S, ld % 4 == 0; dq [B, Hq, S, d], dk/dv [B, Hkv, S, d]
+// fp32 (written, not accumulated).
+struct AttnBwdProblem {
+    const uint16_t *q, *k, *v, *o, *dO;
+    const float *lse;
+    float *dsum;
+    int ld;
+    float *dq, *dk, *dv;
+    int B, S, Hq, Hkv, d, causal;
+};
+cudaError_t launch_attention_backward(const AttnBwdProblem &p, unsigned *err, cudaStream_t stream);
+
+// Inverse RoPE and the QK-norm gradient (backward.cu): dq [B, Hq, S, d], dk /
+// dv [B, Hkv, S, d] fp32 -> dqkv [M, N] bf16 (N = (Hq + 2 Hkv) d, the fused
+// projection's output gradient), with the norm-weight gradients added to
+// dq_norm_w / dk_norm_w (fp32 [d], zeroed by the caller).  pre: the forward's
+// pre-norm Q and K rows [M, (Hq + Hkv) d] fp32, or NULL without QK-norm.
+struct RopeNormBwd {
+    const float *dq, *dk, *dv, *pre;
+    const float2 *rope;  // [S rows][d/2] (cos, sin)
+    const uint16_t *q_norm_w, *k_norm_w;
+    float eps;
+    uint16_t *dqkv;
+    float *dq_norm_w, *dk_norm_w;
+    int M, S, N, Hq, Hkv, d;
+};
+cudaError_t launch_rope_norm_bwd(const RopeNormBwd &p, cudaStream_t stream);
 // head_dim 256 (called by launch_attention)
 cudaError_t launch_attention256(const AttentionProblem &p, unsigned *err, cudaStream_t stream);
 
@@ -92,7 +147,7 @@ cudaError_t launch_selftest_wait(unsigned *err, unsigned long long limit_ns, cud
 void record_error_message(const char *msg);
 
 // Tensor-map encoder (driver entry point, resolved once); elements of 2 bytes
-// (16-bit floats, copied bit for bit) or 1 byte (FP8 codes).
+// (16-bit floats, copied bit for bit), 1 byte (FP8 codes) or 4 bytes (fp32).
 CUresult encode_tmap(CUtensorMap *map, const void *base, int rank, const uint64_t *dims,
                      const uint64_t *strides_bytes, const uint32_t *box, bool swizzle128, int elem_bytes = 2);
 
