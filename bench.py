@@ -516,6 +516,57 @@ def run_ours(args, world, rank, local):
             raise RuntimeError(gq.gqa_last_error())
         del wt, wout, wws, wa, L_
 
+    # ---- backward of the same layer (workload qwen3_32b): gradients of x, Wqkv, Wo and the norm weights
+    bwd = None
+    if not args.no_bwd:
+        bt = make_layer_inputs(cfg, seed=SEEDS[cfg.name] + 29 + 7919 * rank, device=str(dev))
+        gen = torch.Generator(device=dev)
+        gen.manual_seed(SEEDS[cfg.name] + 31)
+        dout = torch.randn((cfg.B * cfg.S, cfg.hidden), generator=gen, device=dev).to(torch.bfloat16)
+        d_ = cfg.head_dim
+        Nq = (cfg.Hq + 2 * cfg.Hkv) * d_
+        bdx = torch.empty_like(bt["x"])
+        bdW = torch.empty((Nq, cfg.hidden), dtype=torch.float32, device=dev)
+        bdWo = torch.empty((cfg.hidden, cfg.Hq * d_), dtype=torch.float32, device=dev)
+        bqn = torch.empty(d_, dtype=torch.float32, device=dev)
+        bkn = torch.empty(d_, dtype=torch.float32, device=dev)
+        bws = gq.new_workspace(gq.gqa_attn_backward_workspace_size(cfg.B, cfg.S, cfg.hidden, cfg.Hq, cfg.Hkv, d_),
+                               dev)
+
+        def bwd_step():
+            gq.gqa_attn_backward(bt["x"], bt["Wqkv"], bt["Wo"], bt["q_norm_w"], bt["k_norm_w"], cfg.rope_theta,
+                                 cfg.eps, cfg.B, cfg.S, cfg.hidden, cfg.Hq, cfg.Hkv, d_, cfg.causal, dout, bdx, bdW,
+                                 bdWo, bqn, bkn, bws, stream)
+
+        bms = reduce_max(time_it(bwd_step), world, dev)
+        # algorithmic: each projection twice (input and weight gradients), attention 2.5x its forward
+        bflops = 2 * (fl["qkv"] + fl["oproj"]) + 5 * fl["attn"] // 2
+        del bdW, bdWo, bws
+        # the attention backward alone (forward attention recomputed for O and lse, then D, dK/dV, dQ)
+        aq = torch.randn((cfg.B, cfg.Hq, cfg.S, d_), generator=gen, device=dev).to(torch.float16)
+        ak = torch.randn((cfg.B, cfg.Hkv, cfg.S, d_), generator=gen, device=dev).to(torch.float16)
+        av = torch.randn((cfg.B, cfg.Hkv, cfg.S, d_), generator=gen, device=dev).to(torch.float16)
+        ag = torch.randn((cfg.B, cfg.Hq, cfg.S, d_), generator=gen, device=dev).to(torch.float16)
+        adq = torch.empty((cfg.B, cfg.Hq, cfg.S, d_), dtype=torch.float32, device=dev)
+        adk = torch.empty((cfg.B, cfg.Hkv, cfg.S, d_), dtype=torch.float32, device=dev)
+        adv = torch.empty_like(adk)
+        aws = gq.new_workspace(gq.gqa_attention_backward_workspace_size(cfg.B, cfg.S, cfg.Hq, d_), dev)
+        abms = time_it(lambda: gq.gqa_attention_backward(aq, ak, av, ag, cfg.B, cfg.S, cfg.Hq, cfg.Hkv, d_,
+                                                         cfg.causal, adq, adk, adv, aws, stream))
+        bwd = {"workload": cfg.name + " backward: dx, dWqkv, dWo, dq_norm_w, dk_norm_w from dout",
+               "value": round(reduce_sum(bflops, world, dev) / (bms * 1e-3) / 1e12, 1), "unit": "TFLOP/s",
+               "ms_per_step": round(bms, 4), "frac_of_peak": round(bflops / (bms * 1e-3) / 1e12 / peak_tf, 4),
+               "flops_per_step": bflops,
+               "note": "algorithmic flops exclude the recomputed forward (Q, K, V and the attention) the time includes",
+               "attention_backward": {"ms": round(abms, 4),
+                                      "tflops": round(2.5 * fl["attn"] / (abms * 1e-3) / 1e12, 1),
+                                      "frac_of_peak": round(2.5 * fl["attn"] / (abms * 1e-3) / 1e12 / peak_tf, 4),
+                                      "note": "2.5x the forward attention flops over the time of forward recompute "
+                                              "+ D + dK/dV + dQ"}}
+        if gq.gqa_check_device_error() != 0:
+            raise RuntimeError(gq.gqa_last_error())
+        del bt, dout, bdx, aq, ak, av, ag, adq, adk, adv, aws
+
     # ---- CPU baseline (rank 0, N=1 only)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
@@ -532,7 +583,7 @@ def run_ours(args, world, rank, local):
                    "Hkv": cfg.Hkv, "head_dim": cfg.head_dim, "qk_norm": cfg.qk_norm, "rope_theta": cfg.rope_theta,
                    "causal": cfg.causal, "flops_per_step": fl["total"], "parallelism": f"replicas x{world}",
                    "l2": "flushed between steps (2x L2 buffer written outside the timed events)"},
-        "roofline": roofline, "decode": decode, "decode_fp8": decode_fp8, "chunked_prefill": chunk, "head_dim_256": wide, "e2e": e2e, "cpu_baseline": cpu,
+        "roofline": roofline, "decode": decode, "decode_fp8": decode_fp8, "chunked_prefill": chunk, "head_dim_256": wide, "backward": bwd, "e2e": e2e, "cpu_baseline": cpu,
         "gpu_launches": launches, "wall_s": round(wall, 3), "clocks": clk.summary(),
         "step_ms": [round(x, 4) for x in step_ms],
     }
@@ -611,9 +662,18 @@ def run_stage(args, local):
         gq.gqa_qkv_proj(t["x"], t["Wqkv"], t["q_norm_w"], t["k_norm_w"], cfg.rope_theta, cfg.eps, cfg.B, cfg.S,
                         cfg.hidden, cfg.Hq, cfg.Hkv, d, q, k, v, stream)
         gq.gqa_attention(q, k, v, cfg.B, cfg.S, cfg.Hq, cfg.Hkv, d, cfg.causal, attn, stream)
+        if args.stage == "attn_bwd":
+            g_ = torch.randn_like(q, dtype=torch.float32).to(torch.float16)
+            dq_ = torch.empty(q.shape, dtype=torch.float32, device=dev)
+            dk_ = torch.empty(k.shape, dtype=torch.float32, device=dev)
+            dv_ = torch.empty_like(dk_)
+            bws_ = gq.new_workspace(gq.gqa_attention_backward_workspace_size(cfg.B, cfg.S, cfg.Hq, d), dev)
 
         def go():
-            if args.stage == "qkv":
+            if args.stage == "attn_bwd":
+                gq.gqa_attention_backward(q, k, v, g_, cfg.B, cfg.S, cfg.Hq, cfg.Hkv, d, cfg.causal, dq_, dk_, dv_,
+                                          bws_, stream)
+            elif args.stage == "qkv":
                 gq.gqa_qkv_proj(t["x"], t["Wqkv"], t["q_norm_w"], t["k_norm_w"], cfg.rope_theta, cfg.eps, cfg.B,
                                 cfg.S, cfg.hidden, cfg.Hq, cfg.Hkv, d, q, k, v, stream)
             elif args.stage == "attn":
@@ -648,7 +708,8 @@ def main(argv=None):
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-chunk", action="store_true", help="skip the chunked-prefill measurement")
     ap.add_argument("--no-d256", action="store_true", help="skip the head_dim 256 measurement")
-    ap.add_argument("--stage", choices=["qkv", "attn", "oproj", "decode_attn", "decode_attn_fp8"], default=None,
+    ap.add_argument("--no-bwd", action="store_true", help="skip the backward measurement")
+    ap.add_argument("--stage", choices=["qkv", "attn", "oproj", "decode_attn", "decode_attn_fp8", "attn_bwd"], default=None,
                     help="launch one stage alone (for profiler captures); prints its time, no benchmark line")
     args = ap.parse_args(argv)
     world, rank, local = dist_setup(args.gpus)
