@@ -42,6 +42,9 @@ def f16_randn(shape, gen, std=1.0):
     (1, 200, 8, 2, 64, False),    # no mask
     (1, 1, 4, 1, 128, True),      # a single token
     (1, 640, 32, 8, 128, True),   # Qwen3-4B/8B heads
+    (1, 260, 32, 1, 128, True),   # G = 32 (4 positions per query tile)
+    (1, 256, 8, 2, 128, False),   # no mask, no ragged edge: every tile unmasked
+    (2, 1024, 8, 1, 64, True),    # many tiles per CTA (both operand rings wrap often)
 ])
 def test_attention_backward_stage(B, S, Hq, Hkv, d, causal):
     g = torch.Generator().manual_seed(3000 + S)
