@@ -662,6 +662,15 @@ def run_stage(args, local):
         gq.gqa_qkv_proj(t["x"], t["Wqkv"], t["q_norm_w"], t["k_norm_w"], cfg.rope_theta, cfg.eps, cfg.B, cfg.S,
                         cfg.hidden, cfg.Hq, cfg.Hkv, d, q, k, v, stream)
         gq.gqa_attention(q, k, v, cfg.B, cfg.S, cfg.Hq, cfg.Hkv, d, cfg.causal, attn, stream)
+        if args.stage == "layer_bwd":
+            dout_ = torch.randn((cfg.B * cfg.S, cfg.hidden), device=dev).to(torch.bfloat16)
+            ldx = torch.empty_like(t["x"])
+            ldW = torch.empty(((cfg.Hq + 2 * cfg.Hkv) * d, cfg.hidden), dtype=torch.float32, device=dev)
+            ldWo = torch.empty((cfg.hidden, cfg.Hq * d), dtype=torch.float32, device=dev)
+            lqn = torch.empty(d, dtype=torch.float32, device=dev) if cfg.qk_norm else None
+            lkn = torch.empty(d, dtype=torch.float32, device=dev) if cfg.qk_norm else None
+            lws = gq.new_workspace(gq.gqa_attn_backward_workspace_size(cfg.B, cfg.S, cfg.hidden, cfg.Hq, cfg.Hkv, d),
+                                   dev)
         if args.stage == "attn_bwd":
             g_ = torch.randn_like(q, dtype=torch.float32).to(torch.float16)
             dq_ = torch.empty(q.shape, dtype=torch.float32, device=dev)
@@ -670,7 +679,11 @@ def run_stage(args, local):
             bws_ = gq.new_workspace(gq.gqa_attention_backward_workspace_size(cfg.B, cfg.S, cfg.Hq, d), dev)
 
         def go():
-            if args.stage == "attn_bwd":
+            if args.stage == "layer_bwd":
+                gq.gqa_attn_backward(t["x"], t["Wqkv"], t["Wo"], t["q_norm_w"], t["k_norm_w"], cfg.rope_theta, cfg.eps,
+                                     cfg.B, cfg.S, cfg.hidden, cfg.Hq, cfg.Hkv, d, cfg.causal, dout_, ldx, ldW, ldWo,
+                                     lqn, lkn, lws, stream)
+            elif args.stage == "attn_bwd":
                 gq.gqa_attention_backward(q, k, v, g_, cfg.B, cfg.S, cfg.Hq, cfg.Hkv, d, cfg.causal, dq_, dk_, dv_,
                                           bws_, stream)
             elif args.stage == "qkv":
@@ -709,7 +722,8 @@ def main(argv=None):
     ap.add_argument("--no-chunk", action="store_true", help="skip the chunked-prefill measurement")
     ap.add_argument("--no-d256", action="store_true", help="skip the head_dim 256 measurement")
     ap.add_argument("--no-bwd", action="store_true", help="skip the backward measurement")
-    ap.add_argument("--stage", choices=["qkv", "attn", "oproj", "decode_attn", "decode_attn_fp8", "attn_bwd"], default=None,
+    ap.add_argument("--stage", choices=["qkv", "attn", "oproj", "decode_attn", "decode_attn_fp8", "attn_bwd",
+                                            "layer_bwd"], default=None,
                     help="launch one stage alone (for profiler captures); prints its time, no benchmark line")
     args = ap.parse_args(argv)
     world, rank, local = dist_setup(args.gpus)
