@@ -40,10 +40,13 @@
  *     validated before anything is launched; a rejected call launches nothing
  *     and writes nothing.  gqa_last_error() returns a message for the last
  *     failing call on the calling thread.
- *   - Supported shapes: head_dim in {64, 128}; hidden a multiple of 8;
- *     Hq a multiple of Hkv.  Other head_dim values return
- *     GQA_ERR_UNSUPPORTED, naming the dimension ([Knob] "Where the
- *     invariance breaks": head_dim is a tile dimension of the fused kernels).
+ *   - Supported shapes: hidden a multiple of 8; Hq a multiple of Hkv;
+ *     head_dim 64, 80, 96, 128 or 256 for the prefill paths (projection,
+ *     attention, layer forward, prefill into a cache), 64 or 128 for decode
+ *     and the backward.  Other head_dim values return GQA_ERR_UNSUPPORTED,
+ *     naming the dimension ([Knob] "Where the invariance breaks": head_dim is
+ *     a tile dimension of the fused kernels; 80 and 96 run in 128-wide tiles
+ *     whose extra columns are zero).
  *   - Device-side waits are bounded.  A wait that runs out records
  *     GQA_ERR_TIMEOUT in a per-device error word that gqa_check_device_error()
  *     reports; the kernel then returns without hanging the GPU.

@@ -651,6 +651,36 @@ def test_forward_partial_rotary_equals_library_composition():
         np.testing.assert_allclose(dec["out"], last, rtol=0, atol=2e-2 * np.abs(last).max())
 
 
+@pytest.mark.parametrize("d,rd", [(80, 80), (80, 20), (96, 96), (96, 48)])
+def test_forward_at_widths_80_96_equals_library_composition(d, rd):
+    """At head widths that are not a power of two ([Knob] "Where the invariance
+    breaks": 80 is Qwen3-4B's hidden/heads quotient, 96 the width it names) the
+    layer still equals the float64 torch composition; the RoPE pairs are
+    (i, i + rd/2), so a dropped or shifted pair at these offsets fails here."""
+    cfg = _tiny(head_dim=d, S=7, hidden=32, Hq=2, Hkv=1)
+    t = make_layer_inputs(cfg, seed=51 + d + rd, w_std=0.3)
+    B, S, h, Hq, Hkv = cfg.B, cfg.S, cfg.hidden, cfg.Hq, cfg.Hkv
+    x, W, Wo = f64(t["x"]), f64(t["Wqkv"]), f64(t["Wo"])
+    q = F.linear(x, W[:Hq * d]).view(B, S, Hq, d)
+    k = F.linear(x, W[Hq * d:(Hq + Hkv) * d]).view(B, S, Hkv, d)
+    v = F.linear(x, W[(Hq + Hkv) * d:]).view(B, S, Hkv, d)
+    q = F.rms_norm(q, (d,), weight=f64(t["q_norm_w"]), eps=cfg.eps)
+    k = F.rms_norm(k, (d,), weight=f64(t["k_norm_w"]), eps=cfg.eps)
+    pos = torch.arange(S, dtype=torch.float64)[:, None]
+    q = _complex_rope(q, pos, cfg.rope_theta, rd).transpose(1, 2)
+    k = _complex_rope(k, pos, cfg.rope_theta, rd).transpose(1, 2)
+    v = v.transpose(1, 2)
+    a = F.scaled_dot_product_attention(q, k.repeat_interleave(Hq // Hkv, 1),
+                                       v.repeat_interleave(Hq // Hkv, 1), is_causal=True)
+    a = a.transpose(1, 2).reshape(B, S, Hq * d)
+    ref = (x + F.linear(a, Wo)).reshape(B * S, h).numpy()
+    got = _fwd(cfg, t, want_stages=True, rotary_dim=rd)
+    np.testing.assert_allclose(got["out"], ref, rtol=1e-11, atol=1e-11)
+    np.testing.assert_allclose(got["q"].reshape(B, S, Hq, d).transpose(0, 2, 1, 3), q.numpy(), rtol=1e-11,
+                               atol=1e-11)
+    np.testing.assert_allclose(got["k"], k.numpy(), rtol=1e-11, atol=1e-11)
+
+
 def test_partial_rotary_rejects_bad_widths():
     v = np.zeros((1, 8))
     for rd in (-2, 3, 10):

@@ -176,8 +176,8 @@ static int check_layer(int B, int S, int hidden, int Hq, int Hkv, int d, const v
     if (d & 1) return fail(GQA_ERR_ARG, "head_dim=%d is odd; RoPE pairs need an even head_dim", d);
     if ((qn == nullptr) != (kn == nullptr))
         return fail(GQA_ERR_ARG, "q_norm_w and k_norm_w must both be given or both be NULL");
-    if (d != 64 && d != 128 && d != 256)
-        return fail(GQA_ERR_UNSUPPORTED, "unsupported head_dim: %d (supported: 64, 128, 256)", d);
+    if (d != 64 && d != 80 && d != 96 && d != 128 && d != 256)
+        return fail(GQA_ERR_UNSUPPORTED, "unsupported head_dim: %d (supported: 64, 80, 96, 128, 256)", d);
     if (hidden % 8) return fail(GQA_ERR_UNSUPPORTED, "unsupported hidden: %d (must be a multiple of 8)", hidden);
     if ((long long)B * S > (1LL << 30) || (long long)(Hq + 2 * Hkv) * d > (1 << 20) || hidden > (1 << 20))
         return fail(GQA_ERR_UNSUPPORTED, "problem too large");
@@ -705,7 +705,7 @@ static int check_decode(int B, int hidden, int Hq, int Hkv, int d, int Lmax, con
     int rc = check_layer(B, 1, hidden, Hq, Hkv, d, qn, kn);
     if (rc) return rc;
     if (Lmax <= 0) return fail(GQA_ERR_ARG, "Lmax must be positive");
-    if (d == 256) return fail(GQA_ERR_UNSUPPORTED, "decode supports head_dim 64 and 128 (got 256)");
+    if (d != 64 && d != 128) return fail(GQA_ERR_UNSUPPORTED, "decode supports head_dim 64 and 128 (got %d)", d);
     const int G = Hq / Hkv;
     if (G != 1 && G != 2 && G != 4 && G != 8)
         return fail(GQA_ERR_UNSUPPORTED, "unsupported decode group size Hq/Hkv=%d (supported: 1, 2, 4, 8)", G);

@@ -20,7 +20,7 @@
 //               softmax, the tensor core works on the other tile.
 //
 // TMEM (512 columns): tile i holds S_i in columns [256i, 256i+128) and O_i in
-// [256i+128, 256i+128+d).  P_i (binary16, two per column) is written over the
+// [256i+128, 256i+128+d') (d' = d rounded up to 64 or 128).  P_i (binary16, two per column) is written over the
 // first 64 columns of S_i and consumed from there by the PV MMA; MMAs issued by
 // one thread run in order, so S_i(j+1) overwrites P_i(j) only after PV_i(j).
 //
@@ -55,11 +55,18 @@ struct AttnParams {
     unsigned *err;
 };
 
+// Head widths that are not a multiple of 64 (80, 96) are staged as 128-wide
+// rows whose columns past d are filled with zeros by the tensor copy; S
+// contracts over the d real columns only, PV runs 128 wide (the zero columns
+// of V give zero columns of O, which are not stored).
+template <int D>
+constexpr int padded_d() { return D <= 64 ? 64 : 128; }
+
 template <int D>
 struct ASmem {
     static constexpr int CHUNK = kRows * 128;             // 128 rows x 64 16-bit = 16 KB
-    static constexpr int NCH = D / 64;                    // 64-wide d chunks
-    static constexpr int STAGES = D == 128 ? 2 : 3;       // K/V ring depth (also keeps 1 CTA per SM)
+    static constexpr int NCH = padded_d<D>() / 64;        // 64-wide d chunks
+    static constexpr int STAGES = NCH == 2 ? 2 : 3;       // K/V ring depth (also keeps 1 CTA per SM)
     static constexpr int Q = 0;
     static constexpr int K = Q + kTiles * NCH * CHUNK;
     static constexpr int V = K + STAGES * NCH * CHUNK;
@@ -71,7 +78,7 @@ struct ASmem {
     static constexpr int ALLOC = TOTAL + 1024;
 };
 
-// D: head_dim.  CACHED: the queries follow kv_start[b] cached keys of a bf16
+// D: head_dim (64, 80, 96, 128).  CACHED: the queries follow kv_start[b] cached keys of a bf16
 // KV cache, so Q, K, V and P are bf16; otherwise they are binary16 and the
 // keys are exactly the S query positions (this variant compiles without any
 // offset arithmetic).
@@ -167,7 +174,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             // S: Q, K K-major over d; O: P from TMEM, V MN-major (d contiguous)
             constexpr uint32_t idesc_s = BF ? idesc_bf16_f32(kRows, kKeys, 0, 0) : idesc_f16_f32(kRows, kKeys, 0, 0);
-            constexpr uint32_t idesc_o = BF ? idesc_bf16_f32(kRows, D, 0, 1) : idesc_f16_f32(kRows, D, 0, 1);
+            constexpr int DP = padded_d<D>();
+            constexpr uint32_t idesc_o = BF ? idesc_bf16_f32(kRows, DP, 0, 1) : idesc_f16_f32(kRows, DP, 0, 1);
             auto issue_s = [&](int i, int j) {  // S_i = Q_i K(j)^T
                 const uint32_t sQ = smem_u32(smem + L::Q + i * L::NCH * L::CHUNK);
                 const uint32_t sK = smem_u32(smem + L::K + (j % ST) * L::NCH * L::CHUNK);
@@ -175,8 +183,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int c = 0; c < L::NCH; ++c)
 #pragma unroll
                     for (int k = 0; k < 4; ++k)
-                        umma_f16_ss(tmem + 256 * i, sw128_desc(sQ + c * L::CHUNK + 32 * k, 16, 1024),
-                                    sw128_desc(sK + c * L::CHUNK + 32 * k, 16, 1024), idesc_s, (c | k) != 0);
+                        if (c * 64 + k * 16 < D)  // d real columns, 16 per step
+                            umma_f16_ss(tmem + 256 * i, sw128_desc(sQ + c * L::CHUNK + 32 * k, 16, 1024),
+                                        sw128_desc(sK + c * L::CHUNK + 32 * k, 16, 1024), idesc_s, (c | k) != 0);
                 umma_commit(s_full + i);
             };
             bool ok = (!CACHED || n_kv > 0) && mbar_wait(q_full, 0, err) && mbar_wait(k_full, 0, err);
@@ -311,14 +320,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int head = g * P.G + hl;
             uint16_t *dst = P.out + ((size_t)(b * P.S + t) * P.Hq + head) * D;
             if (!CACHED && P.lse && row_ok) P.lse[(size_t)(b * P.Hq + head) * P.lse_ld + t] = m_i + log2f(l_i);
+            constexpr int CW = D % 32 == 0 ? 32 : 16;  // columns per TMEM load, tiling d
 #pragma unroll 1
-            for (int c = 0; c < D; c += 32) {
-                uint32_t o[32];
-                tmem_ld32(tO + c, o);
+            for (int c = 0; c < D; c += CW) {
+                uint32_t o[CW];
+                if constexpr (CW == 32)
+                    tmem_ld32(tO + c, o);
+                else
+                    tmem_ld16(tO + c, o);
                 if (row_ok) {
                     uint4 *d4 = reinterpret_cast<uint4 *>(dst + c);
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) {
+                    for (int i = 0; i < CW / 8; ++i) {
                         uint32_t w[4];
 #pragma unroll
                         for (int k = 0; k < 4; ++k)
@@ -391,9 +404,13 @@ cudaError_t launch_attention(const AttentionProblem &p, unsigned *err, int num_s
     if (p.bf16_qkv) {
         if (p.d == 128) return run_attn<128, true>(p, err, stream);
         if (p.d == 64) return run_attn<64, true>(p, err, stream);
+        if (p.d == 80) return run_attn<80, true>(p, err, stream);
+        if (p.d == 96) return run_attn<96, true>(p, err, stream);
     } else {
         if (p.d == 128) return run_attn<128, false>(p, err, stream);
         if (p.d == 64) return run_attn<64, false>(p, err, stream);
+        if (p.d == 80) return run_attn<80, false>(p, err, stream);
+        if (p.d == 96) return run_attn<96, false>(p, err, stream);
     }
     return cudaErrorInvalidValue;
 }

@@ -74,28 +74,65 @@ DEVI void tile_coords(int tile, int num_m, int num_n, int GM, int &mb, int &nb)
     nb = local / gm;
 }
 
-// 32 values of one row -> 16-bit storage (bf16, or binary16 clamped to its
-// finite range; *clamped is set when a value had to be clamped).  dst is
-// 16-byte aligned.
-DEVI void store32(uint16_t *dst, const float *v, bool f16, bool &clamped)
+// W (2, 4, 8, 16 or 32) consecutive TMEM columns of this thread's lane, then wait.
+template <int W>
+DEVI void tmem_ldw(uint32_t taddr, uint32_t (&r)[W])
 {
-    uint4 *d4 = reinterpret_cast<uint4 *>(dst);
-    if (f16) {
-        float c[32];
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-            c[i] = fminf(fmaxf(v[i], -kHalfMax), kHalfMax);
-            clamped |= !(c[i] == v[i]);
-        }
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-            d4[i] = make_uint4(pack_f16(c[8 * i + 0], c[8 * i + 1]), pack_f16(c[8 * i + 2], c[8 * i + 3]),
-                               pack_f16(c[8 * i + 4], c[8 * i + 5]), pack_f16(c[8 * i + 6], c[8 * i + 7]));
+    if constexpr (W == 32) {
+        tmem_ld32(taddr, r);
+    } else if constexpr (W == 16) {
+        tmem_ld16(taddr, r);
+    } else if constexpr (W == 8) {
+        asm volatile(
+            "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];\n\t"
+            "tcgen05.wait::ld.sync.aligned;"
+            : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+            : "r"(taddr)
+            : "memory");
+    } else if constexpr (W == 4) {
+        asm volatile(
+            "tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0,%1,%2,%3}, [%4];\n\t"
+            "tcgen05.wait::ld.sync.aligned;"
+            : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+            : "r"(taddr)
+            : "memory");
     } else {
+        static_assert(W == 2, "TMEM load width");
+        asm volatile(
+            "tcgen05.ld.sync.aligned.32x32b.x2.b32 {%0,%1}, [%2];\n\t"
+            "tcgen05.wait::ld.sync.aligned;"
+            : "=r"(r[0]), "=r"(r[1])
+            : "r"(taddr)
+            : "memory");
+    }
+}
+
+// W values of one row -> 16-bit storage (bf16, or binary16 clamped to its
+// finite range; *clamped is set when a value had to be clamped).  dst is
+// aligned to 2W bytes (16 at most).
+template <int W>
+DEVI void storew(uint16_t *dst, const float *v, bool f16, bool &clamped)
+{
+    uint32_t w[W / 2];
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
-            d4[i] = make_uint4(pack_bf16(v[8 * i + 0], v[8 * i + 1]), pack_bf16(v[8 * i + 2], v[8 * i + 3]),
-                               pack_bf16(v[8 * i + 4], v[8 * i + 5]), pack_bf16(v[8 * i + 6], v[8 * i + 7]));
+    for (int i = 0; i < W / 2; ++i) {
+        float a = v[2 * i], b = v[2 * i + 1];
+        if (f16) {
+            const float ca = fminf(fmaxf(a, -kHalfMax), kHalfMax), cb = fminf(fmaxf(b, -kHalfMax), kHalfMax);
+            clamped |= !(ca == a) || !(cb == b);
+            w[i] = pack_f16(ca, cb);
+        } else {
+            w[i] = pack_bf16(a, b);
+        }
+    }
+    if constexpr (W >= 8) {
+        uint4 *d4 = reinterpret_cast<uint4 *>(dst);
+#pragma unroll
+        for (int i = 0; i < W / 8; ++i) d4[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+    } else if constexpr (W == 4) {
+        *reinterpret_cast<uint2 *>(dst) = make_uint2(w[0], w[1]);
+    } else {
+        *reinterpret_cast<uint32_t *>(dst) = w[0];
     }
 }
 
@@ -106,16 +143,25 @@ struct OutFmt {
     float scale;  // E4M3 only
 };
 
-// Columns [c, c + 32) of a head row whose first element is at dst.
-DEVI void put32(void *dst, int c, const float *v, OutFmt f, bool &clamped)
+// Columns [c, c + W) of a head row whose first element is at dst.
+template <int W>
+DEVI void putw(void *dst, int c, const float *v, OutFmt f, bool &clamped)
 {
     if (f.mode != 2) {
-        store32(reinterpret_cast<uint16_t *>(dst) + c, v, f.mode == 1, clamped);
+        storew<W>(reinterpret_cast<uint16_t *>(dst) + c, v, f.mode == 1, clamped);
         return;
     }
-    uint32_t w[8];
+    uint8_t *d8 = reinterpret_cast<uint8_t *>(dst) + c;
+    if constexpr (W == 2) {
+        const float q0 = __fdiv_rn(v[0], f.scale), q1 = __fdiv_rn(v[1], f.scale);
+        clamped |= !(fabsf(q0) <= 448.0f) || !(fabsf(q1) <= 448.0f);
+        *reinterpret_cast<uint16_t *>(d8) = (uint16_t)f32x2_to_e4m3x2(q0, q1);
+        return;
+    }
+    constexpr int NW = W >= 4 ? W / 4 : 1;
+    uint32_t w[NW];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
+    for (int i = 0; i < W / 4; ++i) {
         float q[4];
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
@@ -124,76 +170,72 @@ DEVI void put32(void *dst, int c, const float *v, OutFmt f, bool &clamped)
         }
         w[i] = f32x2_to_e4m3x2(q[0], q[1]) | (f32x2_to_e4m3x2(q[2], q[3]) << 16);
     }
-    uint4 *d4 = reinterpret_cast<uint4 *>(reinterpret_cast<uint8_t *>(dst) + c);
-    d4[0] = make_uint4(w[0], w[1], w[2], w[3]);
-    d4[1] = make_uint4(w[4], w[5], w[6], w[7]);
+    if constexpr (W >= 16) {
+#pragma unroll
+        for (int i = 0; i < W / 16; ++i)
+            reinterpret_cast<uint4 *>(d8)[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+    } else if constexpr (W == 8) {
+        *reinterpret_cast<uint2 *>(d8) = make_uint2(w[0], w[1]);
+    } else {
+        *reinterpret_cast<uint32_t *>(d8) = w[0];
+    }
+}
+
+// Widest TMEM chunk (<= 32 columns) that tiles n (even) columns.
+__host__ __device__ constexpr int chunk_width(int n)
+{
+    return n % 32 == 0 ? 32 : n % 16 == 0 ? 16 : n % 8 == 0 ? 8 : n % 4 == 0 ? 4 : 2;
 }
 
 // Normalised (x * rinv * w) head row of a Q or K head, rotated on its first
 // RD features (rotate-half pairs (i, i + RD/2), (cos, sin) of angle
 // pos * theta^(-2i/RD) from cs[i]) and stored; features [RD, D) are only
-// normalised.  RD is D, D/2, D/4 or 0; when RD/2 is below 32 the pairs lie
-// inside the first 32 columns and are formed in registers.
+// normalised.  The pairs are taken in chunks of W columns and the rest in
+// chunks of CW, the widest that tile RD/2 and D - RD, so that every TMEM load
+// starts at a multiple of its own width (head offsets are multiples of D).
 template <int D, int RD>
 DEVI void rope_store(uint32_t col, void *dst, float rinv, bool has_norm, const float *w, const float2 *cs,
                      bool row_ok, OutFmt fmt, bool &clamped)
 {
     auto nrm = [&](float x, int c) { return has_norm ? x * rinv * w[c] : x * rinv; };
-    int done = 0;  // columns [0, done) are stored
-    if constexpr (RD >= 64) {
+    if constexpr (RD > 0) {
+        constexpr int H = RD / 2, W = chunk_width(H);
+        static_assert(H % 2 == 0, "pairs of (cos, sin) are read two at a time");
 #pragma unroll 1
-        for (int c = 0; c < RD / 2; c += 32) {
-            uint32_t r1[32], r2[32];
-            tmem_ld32(col + c, r1);
-            tmem_ld32(col + c + RD / 2, r2);
-            float y1[32], y2[32];
+        for (int c = 0; c < H; c += W) {
+            uint32_t r1[W], r2[W];
+            tmem_ldw<W>(col + c, r1);
+            tmem_ldw<W>(col + c + H, r2);
+            float y1[W], y2[W];
 #pragma unroll
-            for (int i = 0; i < 32; i += 2) {
+            for (int i = 0; i < W; i += 2) {
                 const float4 t = __ldg(reinterpret_cast<const float4 *>(cs + c + i));  // (cos, sin) x 2
 #pragma unroll
                 for (int k = 0; k < 2; ++k) {
                     const float co = k ? t.z : t.x, si = k ? t.w : t.y;
                     const float x1 = nrm(__uint_as_float(r1[i + k]), c + i + k);
-                    const float x2 = nrm(__uint_as_float(r2[i + k]), c + i + k + RD / 2);
+                    const float x2 = nrm(__uint_as_float(r2[i + k]), c + i + k + H);
                     y1[i + k] = x1 * co - x2 * si;
                     y2[i + k] = x2 * co + x1 * si;
                 }
             }
             if (row_ok) {
-                put32(dst, c, y1, fmt, clamped);
-                put32(dst, c + RD / 2, y2, fmt, clamped);
+                putw<W>(dst, c, y1, fmt, clamped);
+                putw<W>(dst, c + H, y2, fmt, clamped);
             }
         }
-        done = RD;
-    } else if constexpr (RD > 0) {
-        static_assert(RD == 16 || RD == 32, "pairs inside the first 32 columns");
-        uint32_t r[32];
-        tmem_ld32(col, r);
-        float y[32];
-#pragma unroll
-        for (int i = 0; i < 32; ++i) y[i] = nrm(__uint_as_float(r[i]), i);
-#pragma unroll
-        for (int i = 0; i < RD / 2; i += 2) {
-            const float4 t = __ldg(reinterpret_cast<const float4 *>(cs + i));
-#pragma unroll
-            for (int k = 0; k < 2; ++k) {
-                const float co = k ? t.z : t.x, si = k ? t.w : t.y;
-                const float x1 = y[i + k], x2 = y[i + k + RD / 2];
-                y[i + k] = x1 * co - x2 * si;
-                y[i + k + RD / 2] = x2 * co + x1 * si;
-            }
-        }
-        if (row_ok) put32(dst, 0, y, fmt, clamped);
-        done = 32;
     }
+    if constexpr (RD < D) {
+        constexpr int CW = chunk_width(D - RD);
 #pragma unroll 1
-    for (int c = done; c < D; c += 32) {  // features past the rotary width
-        uint32_t r[32];
-        tmem_ld32(col + c, r);
-        float y[32];
+        for (int c = RD; c < D; c += CW) {  // features past the rotary width
+            uint32_t r[CW];
+            tmem_ldw<CW>(col + c, r);
+            float y[CW];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) y[i] = nrm(__uint_as_float(r[i]), c + i);
-        if (row_ok) put32(dst, c, y, fmt, clamped);
+            for (int i = 0; i < CW; ++i) y[i] = nrm(__uint_as_float(r[i]), c + i);
+            if (row_ok) putw<CW>(dst, c, y, fmt, clamped);
+        }
     }
 }
 
@@ -237,7 +279,7 @@ DEVI void epilogue_head16(const GemmParams &P, uint32_t tcol, int m, int n0, boo
         float v[32];
 #pragma unroll
         for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
-        store32(e.out + ((size_t)(b * e.H + j) * e.S + t) * e.d + cc, v, true, clamped);
+        storew<32>(e.out + ((size_t)(b * e.H + j) * e.S + t) * e.d + cc, v, true, clamped);
     }
     if (clamped) atomicOr(P.err, kErrRange);
 }
@@ -246,6 +288,8 @@ DEVI void epilogue_head16(const GemmParams &P, uint32_t tcol, int m, int n0, boo
 template <int BN, int D>
 DEVI void epilogue_qkv(const GemmParams &P, uint32_t tcol, int m, int n0, bool row_ok, const float *s_norm)
 {
+    static_assert(BN % D == 0, "a tile holds whole heads");
+    constexpr int CWD = chunk_width(D);  // TMEM chunk that tiles a head row (32, or 16 for d = 80)
     const QkvEpilogue &e = P.qkv;
     const int HqD = e.Hq * D, HkvD = e.Hkv * D;
     int b = 0, pos = 0, q_slot = 0, kv_slot = 0;
@@ -303,13 +347,13 @@ DEVI void epilogue_qkv(const GemmParams &P, uint32_t tcol, int m, int n0, bool r
 
         if (kind == 2) {  // V: no norm, no rotation
 #pragma unroll 1
-            for (int c = 0; c < D; c += 32) {
-                uint32_t r[32];
-                tmem_ld32(col + c, r);
-                float v[32];
+            for (int c = 0; c < D; c += CWD) {
+                uint32_t r[CWD];
+                tmem_ldw<CWD>(col + c, r);
+                float v[CWD];
 #pragma unroll
-                for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
-                if (row_ok) put32(dst, c, v, fmt, clamped);
+                for (int i = 0; i < CWD; ++i) v[i] = __uint_as_float(r[i]);
+                if (row_ok) putw<CWD>(dst, c, v, fmt, clamped);
             }
             continue;
         }
@@ -320,18 +364,18 @@ DEVI void epilogue_qkv(const GemmParams &P, uint32_t tcol, int m, int n0, bool r
             float *pre = e.pre_out ? e.pre_out + (size_t)m * (e.Hq + e.Hkv) * D + (kind == 0 ? head : e.Hq + head) * D
                                    : nullptr;
 #pragma unroll 1
-            for (int c = 0; c < D; c += 32) {
-                uint32_t r[32];
-                tmem_ld32(col + c, r);
+            for (int c = 0; c < D; c += CWD) {
+                uint32_t r[CWD];
+                tmem_ldw<CWD>(col + c, r);
 #pragma unroll
-                for (int i = 0; i < 32; ++i) {
+                for (int i = 0; i < CWD; ++i) {
                     const float f = __uint_as_float(r[i]);
                     ss = fmaf(f, f, ss);
                 }
                 if (pre && row_ok) {
                     float4 *d4 = reinterpret_cast<float4 *>(pre + c);
 #pragma unroll
-                    for (int i = 0; i < 8; ++i)
+                    for (int i = 0; i < CWD / 4; ++i)
                         d4[i] = make_float4(__uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1]),
                                             __uint_as_float(r[4 * i + 2]), __uint_as_float(r[4 * i + 3]));
                 }
@@ -386,6 +430,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const GemmParams P)
 {
     constexpr bool AMN = MAJ & 1, BMN = (MAJ >> 1) & 1;
+    // TMEM columns per accumulator: BN rounded up to a power of two (the
+    // allocation unit), so both accumulators start on aligned columns
+    constexpr int ACC = BN <= 64 ? 64 : BN <= 128 ? 128 : 256;
+    static_assert(BN <= ACC && BN % 16 == 0, "MMA N");
     using L = Smem<BN, STAGES>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -418,7 +466,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_prefetch_desc(&tmA);
         tma_prefetch_desc(&tmB);
     }
-    if (warp == 1) tmem_alloc(tmem_slot, 2 * BN);
+    if (warp == 1) tmem_alloc(tmem_slot, 2 * ACC);
     if (EPI == EPI_QKV && warp >= 2 && P.qkv.q_norm_w) {
         for (int i = threadIdx.x - 64; i < D; i += 128) {
             s_norm[i] = __uint_as_float((uint32_t)P.qkv.q_norm_w[i] << 16);
@@ -470,7 +518,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int acc = use & 1;
                 if (!mbar_wait(tempty + acc, ((use >> 1) & 1) ^ 1, err)) break;
                 tc_fence_after();
-                const uint32_t d_tmem = tmem + acc * BN;
+                const uint32_t d_tmem = tmem + acc * ACC;
                 for (int kb = 0; kb < P.num_k; ++kb, ++it) {
                     const int s = it % STAGES;
                     if (!mbar_wait(full + s, (it / STAGES) & 1, err)) {
@@ -508,7 +556,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int acc = use & 1;
             if (!mbar_wait(tfull + acc, (use >> 1) & 1, err)) break;
             tc_fence_after();
-            const uint32_t tcol = tmem + ((uint32_t)(quarter * 32) << 16) + acc * BN;
+            const uint32_t tcol = tmem + ((uint32_t)(quarter * 32) << 16) + acc * ACC;
             const int m = mb * BM + row;
             const bool row_ok = m < P.M;
             if constexpr (EPI == EPI_QKV)
@@ -527,7 +575,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc(tmem, 2 * BN);
+        tmem_dealloc(tmem, 2 * ACC);
     }
 }
 
@@ -601,6 +649,17 @@ cudaError_t launch_gemm_qkv(const GemmProblem &p, const QkvEpilogue &e, unsigned
         GemmParams g = make_params(p, 256, err);
         g.qkv = e;
         return run<256, 4, EPI_QKV, 64>(p, g, num_sms, stream);
+    }
+    // widths that do not divide 256: a tile of whole heads (3 x 80, 2 x 96)
+    if (e.d == 80) {
+        GemmParams g = make_params(p, 240, err);
+        g.qkv = e;
+        return run<240, 4, EPI_QKV, 80>(p, g, num_sms, stream);
+    }
+    if (e.d == 96) {
+        GemmParams g = make_params(p, 192, err);
+        g.qkv = e;
+        return run<192, 4, EPI_QKV, 96>(p, g, num_sms, stream);
     }
     return cudaErrorInvalidValue;
 }

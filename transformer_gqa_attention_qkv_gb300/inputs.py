@@ -15,6 +15,9 @@ seeded ``torch.Generator`` and then rounded to bf16):
 * ``qwen3_32b``   B=1,  S=16384, hidden=5120, Hq=64, Hkv=8, d=128, QK-norm, theta 1e6
 * ``qwen3_8b_decode`` 64 sequences x 1 new token over 8192 cached tokens,
   hidden=4096, Hq=32, Hkv=8, d=128, QK-norm, theta 1e6
+* ``gemma3_d256`` B=4, S=4096, hidden=640, Hq=4, Hkv=1, d=256, QK-norm, theta 1e6
+* ``qwen3_4b_d80`` the Qwen3-4B widths with head_dim = hidden / Hq = 80
+* ``knob_d96``    B=4, S=4096, hidden=3072, Hq=32, Hkv=8, d=96 (= hidden / Hq)
 """
 from __future__ import annotations
 
@@ -71,13 +74,18 @@ PREFILL_CONFIGS = {
     # head_dim 256 at the Gemma-3 example's width (hidden 640, four query heads);
     # one KV head, batch and length are this workload's own choice
     "gemma3_d256": LayerConfig("gemma3_d256", 4, 4096, 640, 4, 1, 256, True, 1e6),
+    # head widths that are not a power of two: Qwen3-4B's hidden / heads quotient
+    # (80) and the width 96; hidden 3072 makes 96 the quotient of 32 heads
+    "qwen3_4b_d80": LayerConfig("qwen3_4b_d80", 4, 4096, 2560, 32, 8, 80, True, 1e6),
+    "knob_d96": LayerConfig("knob_d96", 4, 4096, 3072, 32, 8, 96, True, 1e6),
 }
 DECODE_CONFIGS = {
     "qwen3_8b_decode": DecodeConfig("qwen3_8b_decode", 64, 8192, 4096, 32, 8, 128, True, 1e6),
 }
 # seeds: 1000 + position of the workload in the list above
 SEEDS = {"qwen3_0p6b": 1000, "vaswani_mha": 1001, "qwen3_4b": 1002,
-         "qwen3_32b": 1003, "qwen3_8b_decode": 1004, "gemma3_d256": 1005}
+         "qwen3_32b": 1003, "qwen3_8b_decode": 1004, "gemma3_d256": 1005,
+         "qwen3_4b_d80": 1006, "knob_d96": 1007}
 
 
 def _normal(shape, gen, std, mean=0.0, device="cpu"):
