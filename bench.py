@@ -480,10 +480,10 @@ def run_ours(args, world, rank, local):
                  "flops_per_step": cf["total"]}
         del ct, kc, vc, cout, cws
 
-    # ---- head_dim 256: the layer at the Gemma-3 example's width (4 x 4096 tokens)
-    wide = None
-    if not args.no_d256:
-        wc = PREFILL_CONFIGS["gemma3_d256"]
+    # ---- other head widths: 256 at the Gemma-3 example's width, 80 and 96 at
+    # the Qwen3-4B widths (4 x 4096 tokens each): the layer, then its attention alone
+    def width_line(name, desc):
+        wc = PREFILL_CONFIGS[name]
         wf = prefill_flops(wc)
         wt = make_layer_inputs(wc, seed=SEEDS[wc.name] + 7919 * rank, device=str(dev))
         wout = torch.empty_like(wt["x"])
@@ -495,7 +495,6 @@ def run_ours(args, world, rank, local):
                                    wws, stream)
 
         wms = reduce_max(time_it(wide_step), world, dev)
-        L_ = gq.gqa_attn_workspace_size(wc.B, wc.S, wc.hidden, wc.Hq, wc.Hkv, wc.head_dim)
         n_q = wc.B * wc.S * wc.Hq * wc.head_dim * 2
         n_kv = wc.B * wc.S * wc.Hkv * wc.head_dim * 2
         al = lambda x: (x + 255) // 256 * 256  # noqa: E731
@@ -505,16 +504,25 @@ def run_ours(args, world, rank, local):
         wa = torch.empty((wc.B * wc.S, wc.Hq * wc.head_dim), dtype=torch.bfloat16, device=dev)
         wams = time_it(lambda: gq.gqa_attention(wq, wk, wv, wc.B, wc.S, wc.Hq, wc.Hkv, wc.head_dim, wc.causal, wa,
                                                 stream))
-        wide = {"workload": "gemma3_d256: B=4, S=4096, hidden 640, 4 query heads, 1 KV head, head_dim 256",
+        line = {"workload": desc,
                 "value": round(reduce_sum(wf["total"], world, dev) / (wms * 1e-3) / 1e12, 1), "unit": "TFLOP/s",
                 "ms_per_step": round(wms, 4), "frac_of_peak": round(wf["total"] / (wms * 1e-3) / 1e12 / peak_tf, 4),
-                "roofline": {"bound": "tensor", "kernel": "attn (head_dim 256)",
+                "roofline": {"bound": "tensor", "kernel": f"attn (head_dim {wc.head_dim})",
                              "achieved": round(wf["attn"] / (wams * 1e-3) / 1e12, 1), "peak": peak_tf,
                              "unit": "TFLOP/s", "frac": round(wf["attn"] / (wams * 1e-3) / 1e12 / peak_tf, 4),
                              "kernel_ms": round(wams, 4)}}
         if gq.gqa_check_device_error() != 0:
             raise RuntimeError(gq.gqa_last_error())
-        del wt, wout, wws, wa, L_
+        del wt, wout, wws, wa
+        return line
+
+    wide = wide80 = wide96 = None
+    if not args.no_widths:
+        wide = width_line("gemma3_d256", "gemma3_d256: B=4, S=4096, hidden 640, 4 query heads, 1 KV head, head_dim 256")
+        wide80 = width_line("qwen3_4b_d80", "qwen3_4b_d80: B=4, S=4096, hidden 2560, 32/8 heads, head_dim 80 "
+                                            "(= hidden / heads); attention flops counted at d = 80")
+        wide96 = width_line("knob_d96", "knob_d96: B=4, S=4096, hidden 3072, 32/8 heads, head_dim 96 "
+                                        "(= hidden / heads); attention flops counted at d = 96")
 
     # ---- backward of the same layer (workload qwen3_32b): gradients of x, Wqkv, Wo and the norm weights
     bwd = None
@@ -583,7 +591,8 @@ def run_ours(args, world, rank, local):
                    "Hkv": cfg.Hkv, "head_dim": cfg.head_dim, "qk_norm": cfg.qk_norm, "rope_theta": cfg.rope_theta,
                    "causal": cfg.causal, "flops_per_step": fl["total"], "parallelism": f"replicas x{world}",
                    "l2": "flushed between steps (2x L2 buffer written outside the timed events)"},
-        "roofline": roofline, "decode": decode, "decode_fp8": decode_fp8, "chunked_prefill": chunk, "head_dim_256": wide, "backward": bwd, "e2e": e2e, "cpu_baseline": cpu,
+        "roofline": roofline, "decode": decode, "decode_fp8": decode_fp8, "chunked_prefill": chunk, "head_dim_256": wide,
+        "head_dim_80": wide80, "head_dim_96": wide96, "backward": bwd, "e2e": e2e, "cpu_baseline": cpu,
         "gpu_launches": launches, "wall_s": round(wall, 3), "clocks": clk.summary(),
         "step_ms": [round(x, 4) for x in step_ms],
     }
@@ -720,7 +729,8 @@ def main(argv=None):
     ap.add_argument("--ref-tokens", type=int, default=256, help="tokens per reference-arm step")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-chunk", action="store_true", help="skip the chunked-prefill measurement")
-    ap.add_argument("--no-d256", action="store_true", help="skip the head_dim 256 measurement")
+    ap.add_argument("--no-widths", "--no-d256", dest="no_widths", action="store_true",
+                    help="skip the head_dim 256 / 80 / 96 measurements")
     ap.add_argument("--no-bwd", action="store_true", help="skip the backward measurement")
     ap.add_argument("--stage", choices=["qkv", "attn", "oproj", "decode_attn", "decode_attn_fp8", "attn_bwd",
                                             "layer_bwd"], default=None,
