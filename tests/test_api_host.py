@@ -99,3 +99,19 @@ def test_other_entry_points_validate(L):
                                P(FAKE), None, 100, P(FAKE * 3), P(FAKE * 4), 1 << 30, None) == -1  # cache_len NULL
     assert lib.gqa_attn_workspace_size(0, 1, 1, 1, 1, 1) == 0
     assert L.gqa_attn_workspace_size(1, 16, 64, 4, 2, 128) >= 16 * (4 + 2 + 2 + 4) * 128 * 2
+
+
+def test_resolve_head_dim():
+    """[NeoX] "Proposed configuration behavior": an explicit head_dim wins
+    (no divisibility needed); without one head_dim = hidden / heads, which
+    must divide ([Knob] "Where the invariance breaks": 2560 / 32 = 80)."""
+    from transformer_gqa_attention_qkv_gb300.binding import resolve_head_dim
+    assert resolve_head_dim(2560, 32) == 80
+    assert resolve_head_dim(2560, 32, 128) == 128
+    assert resolve_head_dim(1024, 16, 128) == 128      # Qwen3-0.6B: Q width 2048 != hidden
+    assert resolve_head_dim(512, 8) == 64               # the Vaswani layer
+    assert resolve_head_dim(1000, 16, 128) == 128      # explicit: hidden need not divide
+    with pytest.raises(ValueError):
+        resolve_head_dim(1000, 16)
+    with pytest.raises(ValueError):
+        resolve_head_dim(2560, 32, 0)

@@ -308,6 +308,21 @@ def gqa_decode_attention_noalloc(q, k_cache, v_cache, kv_len, B, Hq, Hkv, head_d
 
 # ---------------------------------------------------------------- accounting
 
+def resolve_head_dim(hidden: int, Hq: int, head_dim: int | None = None) -> int:
+    """The head width a model configuration implies ([NeoX] "Proposed
+    configuration behavior"): an explicit head_dim wins and needs no relation
+    to hidden (Qwen3-4B: hidden 2560, 32 heads, head_dim 128); without one it
+    is hidden / Hq, and only then must Hq divide hidden.  Every entry point
+    of the library takes the resolved value explicitly."""
+    if head_dim is not None:
+        if int(head_dim) <= 0:
+            raise ValueError(f"head_dim={head_dim} must be positive")
+        return int(head_dim)
+    if Hq <= 0 or hidden <= 0 or hidden % Hq:
+        raise ValueError(f"hidden={hidden} is not a positive multiple of Hq={Hq}: give head_dim explicitly")
+    return hidden // Hq
+
+
 def gqa_attn_cost(B, S, hidden, Hq, Hkv, head_dim, causal=True) -> dict:
     vals = [ctypes.c_longlong() for _ in range(4)]
     _check(lib().gqa_attn_cost(B, S, hidden, Hq, Hkv, head_dim, int(causal), *[ctypes.byref(v) for v in vals]))
