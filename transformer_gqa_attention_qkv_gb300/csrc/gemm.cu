@@ -14,6 +14,14 @@
 //               two accumulators so tile i's epilogue overlaps tile i+1's loop
 //   warps 2..5  epilogue: tcgen05.ld (one thread = one output row), fused
 //               math, 16-byte global stores
+//
+// Problems with a single M block (the decode step's projections: 64 rows, a
+// few dozen N tiles) would leave most SMs idle and stream the weights through
+// few CTAs.  There the K dimension is split over a cluster of KS CTAs (one
+// tile per cluster): each accumulates its K slice in its own TMEM, the others
+// then write their partial sums into the first CTA's (now idle) operand ring
+// through distributed shared memory, and the first CTA folds them into its
+// accumulator and runs the epilogue unchanged.
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -425,11 +433,32 @@ DEVI void epilogue_residual(const GemmParams &P, uint32_t tcol, int m, int n0, b
     }
 }
 
-template <int BN, int STAGES, int EPI, int D, int MAJ>
+// The tile's epilogue, one thread per accumulator row.
+template <int BN, int EPI, int D>
+DEVI void epilogue_tile(const GemmParams &P, uint32_t tcol, int m, int n0, bool row_ok, const float *s_norm)
+{
+    if constexpr (EPI == EPI_QKV)
+        epilogue_qkv<BN, D>(P, tcol, m, n0, row_ok, s_norm);
+    else if constexpr (EPI == EPI_RESIDUAL)
+        epilogue_residual<BN>(P, tcol, m, n0, row_ok);
+    else if constexpr (EPI == EPI_F32)
+        epilogue_f32<BN>(P, tcol, m, n0, row_ok);
+    else
+        epilogue_head16<BN>(P, tcol, m, n0, row_ok);
+}
+
+// KS: CTAs of a cluster that split K for one tile (1: no split, persistent
+// over tiles).
+template <int BN, int STAGES, int EPI, int D, int MAJ, int KS>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const GemmParams P)
 {
     constexpr bool AMN = MAJ & 1, BMN = (MAJ >> 1) & 1;
+    static_assert(KS >= 1 && KS <= 4, "K split");
+    // split-K partial sums of one CTA: BM rows of BN fp32, rows padded by 16
+    // bytes so a warp's 16-byte accesses to 32 rows spread over all banks
+    constexpr int PART_LD = BN + 4;
+    constexpr int PART = BM * PART_LD * 4;
     // TMEM columns per accumulator: BN rounded up to a power of two (the
     // allocation unit), so both accumulators start on aligned columns
     constexpr int ACC = BN <= 64 ? 64 : BN <= 128 ? 128 : 256;
@@ -449,6 +478,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     unsigned *err = P.err;
+    // tiles this CTA walks, and its K blocks [kb0, kb1) of each
+    const uint32_t crank = KS > 1 ? cluster_rank() : 0;
+    const int tile0 = KS > 1 ? (int)(blockIdx.x / KS) : (int)blockIdx.x;
+    const int tile_step = KS > 1 ? P.num_tiles : (int)gridDim.x;  // split K: one tile per cluster
+    const int kb0 = (int)(crank * P.num_k / KS), kb1 = (int)((crank + 1) * P.num_k / KS);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
@@ -466,6 +500,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_prefetch_desc(&tmA);
         tma_prefetch_desc(&tmB);
     }
+    bool acc_ready = false;  // split K: this warp's accumulator rows are complete
     if (warp == 1) tmem_alloc(tmem_slot, 2 * ACC);
     if (EPI == EPI_QKV && warp >= 2 && P.qkv.q_norm_w) {
         for (int i = threadIdx.x - 64; i < D; i += 128) {
@@ -481,10 +516,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             int it = 0;
             bool ok = true;
-            for (int tile = blockIdx.x; ok && tile < P.num_tiles; tile += gridDim.x) {
+            for (int tile = tile0; ok && tile < P.num_tiles; tile += tile_step) {
                 int mb, nb;
                 tile_coords(tile, P.num_m, P.num_n, P.group_m, mb, nb);
-                for (int kb = 0; kb < P.num_k; ++kb, ++it) {
+                for (int kb = kb0; kb < kb1; ++kb, ++it) {
                     const int s = it % STAGES;
                     const uint32_t ph = (it / STAGES) & 1;
                     if (!mbar_wait(empty + s, ph ^ 1, err)) {
@@ -514,12 +549,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             constexpr uint32_t idesc = idesc_bf16_f32(BM, BN, AMN ? 1 : 0, BMN ? 1 : 0);
             int it = 0, use = 0;
             bool ok = true;
-            for (int tile = blockIdx.x; ok && tile < P.num_tiles; tile += gridDim.x, ++use) {
+            for (int tile = tile0; ok && tile < P.num_tiles; tile += tile_step, ++use) {
                 const int acc = use & 1;
                 if (!mbar_wait(tempty + acc, ((use >> 1) & 1) ^ 1, err)) break;
                 tc_fence_after();
                 const uint32_t d_tmem = tmem + acc * ACC;
-                for (int kb = 0; kb < P.num_k; ++kb, ++it) {
+                for (int kb = kb0; kb < kb1; ++kb, ++it) {
                     const int s = it % STAGES;
                     if (!mbar_wait(full + s, (it / STAGES) & 1, err)) {
                         ok = false;
@@ -536,7 +571,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                 : sw128_desc(a0 + 32 * k, 16, 1024);
                         const uint64_t bd = BMN ? sw128_desc(b0 + k * 16 * 128, kMnChunk, 1024)
                                                 : sw128_desc(b0 + 32 * k, 16, 1024);
-                        umma_f16_ss(d_tmem, ad, bd, idesc, (kb | k) != 0);
+                        umma_f16_ss(d_tmem, ad, bd, idesc, (kb != kb0 || k != 0) ? 1u : 0u);
                     }
                     umma_commit(empty + s);  // frees the stage once these MMAs have read it
                 }
@@ -550,26 +585,83 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int quarter = warp & 3;  // TMEM lanes this warp may access
         const int row = quarter * 32 + lane;
         int use = 0;
-        for (int tile = blockIdx.x; tile < P.num_tiles; tile += gridDim.x, ++use) {
+        for (int tile = tile0; tile < P.num_tiles; tile += tile_step, ++use) {
             int mb, nb;
             tile_coords(tile, P.num_m, P.num_n, P.group_m, mb, nb);
             const int acc = use & 1;
-            if (!mbar_wait(tfull + acc, (use >> 1) & 1, err)) break;
+            const bool ready = mbar_wait(tfull + acc, (use >> 1) & 1, err);
+            if constexpr (KS > 1) {  // the cluster sums the partials below
+                acc_ready = __all_sync(0xffffffffu, ready);
+                break;
+            }
+            if (!ready) break;
             tc_fence_after();
             const uint32_t tcol = tmem + ((uint32_t)(quarter * 32) << 16) + acc * ACC;
             const int m = mb * BM + row;
-            const bool row_ok = m < P.M;
-            if constexpr (EPI == EPI_QKV)
-                epilogue_qkv<BN, D>(P, tcol, m, nb * BN, row_ok, s_norm);
-            else if constexpr (EPI == EPI_RESIDUAL)
-                epilogue_residual<BN>(P, tcol, m, nb * BN, row_ok);
-            else if constexpr (EPI == EPI_F32)
-                epilogue_f32<BN>(P, tcol, m, nb * BN, row_ok);
-            else
-                epilogue_head16<BN>(P, tcol, m, nb * BN, row_ok);
+            epilogue_tile<BN, EPI, D>(P, tcol, m, nb * BN, m < P.M, s_norm);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(tempty + acc);
+        }
+    }
+    if constexpr (KS > 1) {
+        // Every CTA of the cluster has its K slice in TMEM accumulator 0 (or
+        // gave up on a bounded wait, recorded in *err) and the first CTA's
+        // operand ring is idle: the others add their partials into it.
+        static_assert((KS - 1) * PART <= L::RING, "split-K partials fit in the operand ring");
+        __syncthreads();
+        cluster_sync();
+        const int quarter = warp & 3;
+        const int row = quarter * 32 + lane;
+        const uint32_t tcol = tmem + ((uint32_t)(quarter * 32) << 16);
+        int mb = 0, nb = 0;
+        if (tile0 < P.num_tiles) tile_coords(tile0, P.num_m, P.num_n, P.group_m, mb, nb);
+        const int m = mb * BM + row;
+        const bool active = warp >= 2 && tile0 < P.num_tiles && acc_ready;  // warp-uniform
+        if (active && crank != 0) {
+            tc_fence_after();
+            const uint32_t dst = cluster_map(smem_u32(smem), 0) + (uint32_t)(((crank - 1) * BM + row) * PART_LD * 4);
+#pragma unroll 1
+            for (int c = 0; c < BN; c += 16) {
+                uint32_t r[16];
+                tmem_ld16(tcol + c, r);
+                if (m < P.M)
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        st_cluster_v4(dst + (c + 4 * i) * 4, r[4 * i], r[4 * i + 1], r[4 * i + 2], r[4 * i + 3]);
+            }
+        }
+        cluster_sync();
+        if (active && crank == 0) {
+            tc_fence_after();
+            // every lane loads and stores (the TMEM accesses are warp-collective);
+            // only rows of the problem add partials
+            const float *part = reinterpret_cast<const float *>(smem) + row * PART_LD;
+#pragma unroll 1
+            for (int c = 0; c < BN; c += 16) {
+                uint32_t r[16];
+                tmem_ld16(tcol + c, r);
+                if (m < P.M) {
+#pragma unroll
+                    for (int k = 1; k < KS; ++k) {
+                        const float4 *p4 = reinterpret_cast<const float4 *>(part + (k - 1) * BM * PART_LD + c);
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            const float4 q = p4[i];
+                            r[4 * i] = __float_as_uint(__uint_as_float(r[4 * i]) + q.x);
+                            r[4 * i + 1] = __float_as_uint(__uint_as_float(r[4 * i + 1]) + q.y);
+                            r[4 * i + 2] = __float_as_uint(__uint_as_float(r[4 * i + 2]) + q.z);
+                            r[4 * i + 3] = __float_as_uint(__uint_as_float(r[4 * i + 3]) + q.w);
+                        }
+                    }
+                }
+                tmem_st16_nowait(tcol + c, r);
+            }
+            tmem_st_wait();
+            tc_fence_before();
+            __syncwarp();
+            tc_fence_after();
+            epilogue_tile<BN, EPI, D>(P, tcol, m, nb * BN, m < P.M, s_norm);
         }
     }
     __syncthreads();
@@ -579,7 +671,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-template <int BN, int STAGES, int EPI, int D, int MAJ = 0>
+template <int BN, int STAGES, int EPI, int D, int MAJ = 0, int KS = 1>
 cudaError_t run(const GemmProblem &p, const GemmParams &params, int num_sms, cudaStream_t stream)
 {
     using L = Smem<BN, STAGES>;
@@ -594,12 +686,73 @@ cudaError_t run(const GemmProblem &p, const GemmParams &params, int num_sms, cud
     const uint32_t bB[2] = {BMN ? 64u : (uint32_t)BK, BMN ? (uint32_t)BK : (uint32_t)BN};
     if (encode_tmap(&ta, p.A, 2, dA, sA, bA, true) != CUDA_SUCCESS) return cudaErrorInvalidValue;
     if (encode_tmap(&tb, p.B, 2, dB, sB, bB, true) != CUDA_SUCCESS) return cudaErrorInvalidValue;
-    auto kern = gemm_kernel<BN, STAGES, EPI, D, MAJ>;
+    auto kern = gemm_kernel<BN, STAGES, EPI, D, MAJ, KS>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC);
     if (e != cudaSuccess) return e;
+    if constexpr (KS > 1) {
+        cudaLaunchConfig_t cfg{};
+        cfg.gridDim = dim3(params.num_tiles * KS);
+        cfg.blockDim = dim3(kThreads);
+        cfg.dynamicSmemBytes = L::ALLOC;
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = KS;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        e = cudaLaunchKernelEx(&cfg, kern, ta, tb, params);
+        if (e != cudaSuccess) return e;
+        return cudaGetLastError();
+    }
     const int grid = params.num_tiles < num_sms ? params.num_tiles : num_sms;
     kern<<<grid, kThreads, L::ALLOC, stream>>>(ta, tb, params);
     return cudaGetLastError();
+}
+
+// How many CTAs of this kernel's clusters of KS can be resident at once
+// (0 if the query fails); cached per kernel.
+template <int BN, int STAGES, int EPI, int D, int KS>
+int cluster_capacity()
+{
+    static int cap = -1;
+    if (cap >= 0) return cap;
+    using L = Smem<BN, STAGES>;
+    auto kern = gemm_kernel<BN, STAGES, EPI, D, 0, KS>;
+    int n = 0;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC) == cudaSuccess) {
+        cudaLaunchConfig_t cfg{};
+        cfg.gridDim = dim3(KS);
+        cfg.blockDim = dim3(kThreads);
+        cfg.dynamicSmemBytes = L::ALLOC;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = KS;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) n = 0;
+    }
+    (void)cudaGetLastError();
+    cap = n * KS;
+    return cap;
+}
+
+// A single-M-block problem with few tiles: split K over a cluster of 3 or 2
+// CTAs when every cluster fits on the GPU at once and each CTA keeps at least
+// four K blocks; otherwise no split.
+template <int BN, int STAGES, int EPI, int D>
+cudaError_t run_small_m(const GemmProblem &p, const GemmParams &g, int num_sms, cudaStream_t stream)
+{
+    if (g.num_m == 1) {
+        if (g.num_tiles * 3 <= num_sms && g.num_k >= 12 && g.num_tiles * 3 <= cluster_capacity<BN, STAGES, EPI, D, 3>())
+            return run<BN, STAGES, EPI, D, 0, 3>(p, g, num_sms, stream);
+        if (g.num_tiles * 2 <= num_sms && g.num_k >= 8 && g.num_tiles * 2 <= cluster_capacity<BN, STAGES, EPI, D, 2>())
+            return run<BN, STAGES, EPI, D, 0, 2>(p, g, num_sms, stream);
+    }
+    return run<BN, STAGES, EPI, D>(p, g, num_sms, stream);
 }
 
 GemmParams make_params(const GemmProblem &p, int BN, unsigned *err)
@@ -629,7 +782,7 @@ cudaError_t launch_gemm_qkv(const GemmProblem &p, const QkvEpilogue &e, unsigned
         if (small_m) {
             GemmParams g = make_params(p, 128, err);
             g.qkv = e;
-            return run<128, 6, EPI_QKV, 128>(p, g, num_sms, stream);
+            return run_small_m<128, 6, EPI_QKV, 128>(p, g, num_sms, stream);
         }
         GemmParams g = make_params(p, 256, err);
         g.qkv = e;
@@ -644,7 +797,7 @@ cudaError_t launch_gemm_qkv(const GemmProblem &p, const QkvEpilogue &e, unsigned
         if (small_m) {
             GemmParams g = make_params(p, 64, err);
             g.qkv = e;
-            return run<64, 8, EPI_QKV, 64>(p, g, num_sms, stream);
+            return run_small_m<64, 8, EPI_QKV, 64>(p, g, num_sms, stream);
         }
         GemmParams g = make_params(p, 256, err);
         g.qkv = e;
@@ -670,7 +823,7 @@ cudaError_t launch_gemm_residual(const GemmProblem &p, const ResidualEpilogue &e
     if (p.M <= BM) {
         GemmParams g = make_params(p, 64, err);
         g.res = e;
-        return run<64, 8, EPI_RESIDUAL, 0>(p, g, num_sms, stream);
+        return run_small_m<64, 8, EPI_RESIDUAL, 0>(p, g, num_sms, stream);
     }
     GemmParams g = make_params(p, 256, err);
     g.res = e;

@@ -92,6 +92,37 @@ DEVI bool mbar_wait(uint64_t *bar, uint32_t parity, unsigned *err, uint64_t limi
     }
 }
 
+// ----------------------------------------------------------------- clusters
+
+// Rank of this CTA in its thread-block cluster.
+DEVI uint32_t cluster_rank()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+// Every thread of every CTA of the cluster: shared-memory writes before it
+// (local or remote) are visible to every thread after it.
+DEVI void cluster_sync()
+{
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// The shared::cluster address of the same offset in CTA `rank`'s shared memory.
+DEVI uint32_t cluster_map(uint32_t local_addr, uint32_t rank)
+{
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local_addr), "r"(rank));
+    return r;
+}
+
+DEVI void st_cluster_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d)
+{
+    asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
+                 : "memory");
+}
+
 // --------------------------------------------------------------------- TMA
 
 DEVI void tma_prefetch_desc(const CUtensorMap *tm)
