@@ -268,12 +268,15 @@ static int run_qkv(DeviceState &st, const gqa_bf16 *x, const gqa_bf16 *Wqkv, con
     return GQA_OK;
 }
 
+// pdl (here and below): the kernel follows one of this library's kernels in the
+// same entry point and is launched as its programmatic dependent.
 static int run_attention(DeviceState &st, const uint16_t *q, const uint16_t *k, const uint16_t *v, int B, int S,
                          int Hq, int Hkv, int d, int causal, gqa_bf16 *out, cudaStream_t stream, int kv_seq = 0,
-                         const int *kv_start = nullptr, int bf16_qkv = 0, float *lse = nullptr, int lse_ld = 0)
+                         const int *kv_start = nullptr, int bf16_qkv = 0, float *lse = nullptr, int lse_ld = 0,
+                         int pdl = 0)
 {
     AttentionProblem p{q,         k,        v,        out, B,   S,      Hq, Hkv, d, causal ? 1 : 0,
-                       kv_seq > 0 ? kv_seq : S, kv_start, bf16_qkv, lse, lse_ld};
+                       kv_seq > 0 ? kv_seq : S, kv_start, bf16_qkv, lse, lse_ld, pdl};
     cudaError_t ce = launch_attention(p, st.err, st.num_sms, stream);
     if (ce != cudaSuccess) return cuda_fail(ce, "attention launch");
     ++g_launches;
@@ -281,9 +284,9 @@ static int run_attention(DeviceState &st, const uint16_t *q, const uint16_t *k, 
 }
 
 static int run_oproj(DeviceState &st, const gqa_bf16 *attn, const gqa_bf16 *Wo, const gqa_bf16 *x, int M, int hidden,
-                     int qw, gqa_bf16 *out, cudaStream_t stream)
+                     int qw, gqa_bf16 *out, cudaStream_t stream, int pdl = 0)
 {
-    GemmProblem p{attn, Wo, M, hidden, qw};
+    GemmProblem p{attn, Wo, M, hidden, qw, pdl};
     ResidualEpilogue e{x, out};
     cudaError_t ce = launch_gemm_residual(p, e, st.err, st.num_sms, stream);
     if (ce != cudaSuccess) return cuda_fail(ce, "o_proj launch");
@@ -294,9 +297,10 @@ static int run_oproj(DeviceState &st, const gqa_bf16 *attn, const gqa_bf16 *Wo, 
 static int run_decode_attn(DeviceState &st, const gqa_bf16 *q, const void *kc, const void *vc,
                            const int *len, int bias, int B, int Hq, int Hkv, int d, int Lmax, gqa_bf16 *out,
                            float *partials, int splits, cudaStream_t stream, int fp8 = 0, float k_scale = 1.0f,
-                           float v_scale = 1.0f)
+                           float v_scale = 1.0f, int pdl = 0)
 {
     DecodeAttentionProblem p{};
+    p.pdl = pdl;
     p.q = q;
     p.k_cache = kc;
     p.v_cache = vc;
@@ -421,8 +425,9 @@ int gqa_attn_forward_rd(const gqa_bf16 *x, const gqa_bf16 *Wqkv, const gqa_bf16 
     if ((rc = run_qkv(*st, x, Wqkv, q_norm_w, k_norm_w, rope_theta, eps, rotary_dim, B, S, hidden, Hq, Hkv, head_dim,
                       nullptr, S, S, S, 1, 1, q, k, v, s)))
         return rc;
-    if ((rc = run_attention(*st, q, k, v, B, S, Hq, Hkv, head_dim, causal, attn, s))) return rc;
-    return run_oproj(*st, attn, Wo, x, B * S, hidden, Hq * head_dim, out, s);
+    if ((rc = run_attention(*st, q, k, v, B, S, Hq, Hkv, head_dim, causal, attn, s, 0, nullptr, 0, nullptr, 0, 1)))
+        return rc;
+    return run_oproj(*st, attn, Wo, x, B * S, hidden, Hq * head_dim, out, s, 1);
 }
 
 int gqa_attn_forward(const gqa_bf16 *x, const gqa_bf16 *Wqkv, const gqa_bf16 *Wo, const gqa_bf16 *q_norm_w,
@@ -786,9 +791,10 @@ int gqa_attn_decode_rd(const gqa_bf16 *x, const gqa_bf16 *Wqkv, const gqa_bf16 *
     if ((rc = run_qkv(*st, x, Wqkv, q_norm_w, k_norm_w, rope_theta, eps, rotary_dim, B, 1, hidden, Hq, Hkv, head_dim,
                       cache_len, 1, Lmax, Lmax, 1, 0, q, k_cache, v_cache, s)))
         return rc;
-    if ((rc = run_decode_attn(*st, q, k_cache, v_cache, cache_len, 1, B, Hq, Hkv, head_dim, Lmax, attn, part, sp, s)))
+    if ((rc = run_decode_attn(*st, q, k_cache, v_cache, cache_len, 1, B, Hq, Hkv, head_dim, Lmax, attn, part, sp, s, 0,
+                              1.0f, 1.0f, 1)))
         return rc;
-    return run_oproj(*st, attn, Wo, x, B, hidden, Hq * head_dim, out, s);
+    return run_oproj(*st, attn, Wo, x, B, hidden, Hq * head_dim, out, s, 1);
 }
 
 // ------------------------------------------------------ prefill into a cache
@@ -858,9 +864,10 @@ int gqa_attn_prefill_cached_rd(const gqa_bf16 *x, const gqa_bf16 *Wqkv, const gq
     if ((rc = run_qkv(*st, x, Wqkv, q_norm_w, k_norm_w, rope_theta, eps, rotary_dim, B, S, hidden, Hq, Hkv, head_dim,
                       cache_len, S, Lmax, Lmax, 0, 0, q, k_cache, v_cache, s)))
         return rc;
-    if ((rc = run_attention(*st, q, k_cache, v_cache, B, S, Hq, Hkv, head_dim, causal, attn, s, Lmax, cache_len, 1)))
+    if ((rc = run_attention(*st, q, k_cache, v_cache, B, S, Hq, Hkv, head_dim, causal, attn, s, Lmax, cache_len, 1,
+                            nullptr, 0, 1)))
         return rc;
-    return run_oproj(*st, attn, Wo, x, B * S, hidden, Hq * head_dim, out, s);
+    return run_oproj(*st, attn, Wo, x, B * S, hidden, Hq * head_dim, out, s, 1);
 }
 
 // ------------------------------------------------------ FP8 (E4M3) KV cache
@@ -952,9 +959,9 @@ int gqa_attn_decode_fp8(const gqa_bf16 *x, const gqa_bf16 *Wqkv, const gqa_bf16 
                       v_scale)))
         return rc;
     if ((rc = run_decode_attn(*st, q, k_cache, v_cache, cache_len, 1, B, Hq, Hkv, head_dim, Lmax, attn, part, sp, s,
-                              1, k_scale, v_scale)))
+                              1, k_scale, v_scale, 1)))
         return rc;
-    return run_oproj(*st, attn, Wo, x, B, hidden, Hq * head_dim, out, s);
+    return run_oproj(*st, attn, Wo, x, B, hidden, Hq * head_dim, out, s, 1);
 }
 
 // ------------------------------------------- full rotary (rotary_dim = head_dim)

@@ -105,6 +105,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     unsigned *err = P.err;
+    grid_dep_launch();  // the next kernel may start its prologue meanwhile
 
     // heavy (late) query blocks first
     const int item = blockIdx.x;
@@ -141,6 +142,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    grid_dep_wait();  // Q, K, V come from the previous kernel (cached keys from earlier ones)
 
     if (warp == 0) {
         if (lane == 0) {
@@ -388,7 +390,9 @@ cudaError_t run_attn(const AttentionProblem &p, unsigned *err, cudaStream_t stre
     auto kern = attn_kernel<D, BF>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC);
     if (e != cudaSuccess) return e;
-    kern<<<a.num_items, kThreads, L::ALLOC, stream>>>(tq, tk, tv, a);
+    LaunchCfg lc(dim3(a.num_items), dim3(kThreads), L::ALLOC, stream, p.pdl != 0);
+    e = cudaLaunchKernelEx(&lc.cfg, kern, tq, tk, tv, a);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 

@@ -138,6 +138,7 @@ __global__ void __launch_bounds__(32 * (1 + CW), 1)
     float *red = reinterpret_cast<float *>(smem + L::RED);
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    grid_dep_launch();  // the combine kernel may be scheduled meanwhile
     if (threadIdx.x == 0) {
         for (int s = 0; s < ST; ++s) {
             mbar_init(full + s, 1);
@@ -150,6 +151,7 @@ __global__ void __launch_bounds__(32 * (1 + CW), 1)
         tma_prefetch_desc(&tmV);
     }
     __syncthreads();
+    grid_dep_wait();  // q and the new cache entries come from the previous kernel
 
     if (warp == 0) {
         if (lane == 0) {
@@ -408,6 +410,8 @@ template <int D, int G>
 __global__ void __launch_bounds__(128) decode_combine_kernel(const DecodeAttentionProblem P)
 {
     constexpr int REC = G * (D + 2);
+    grid_dep_launch();
+    grid_dep_wait();  // the split kernel's partial records
     const int bg = blockIdx.x;
     const int b = bg / P.Hkv, g = bg % P.Hkv;
     const float *recs = P.partials + (size_t)bg * P.splits * REC;
@@ -451,10 +455,17 @@ cudaError_t run_decode(const DecodeAttentionProblem &p, unsigned *err, cudaStrea
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC);
     if (e != cudaSuccess) return e;
     const int grid = n_items < sms ? n_items : sms;
-    kern<<<grid, 32 * (1 + CW), L::ALLOC, stream>>>(tk, tv, p, scale_log2, n_items, err);
+    {
+        LaunchCfg lc(dim3(grid), dim3(32 * (1 + CW)), L::ALLOC, stream, p.pdl != 0);
+        e = cudaLaunchKernelEx(&lc.cfg, kern, tk, tv, p, scale_log2, n_items, err);
+        if (e != cudaSuccess) return e;
+    }
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    decode_combine_kernel<D, G><<<p.B * p.Hkv, 128, 0, stream>>>(p);
+    // the combine follows the split kernel as its programmatic dependent
+    LaunchCfg lc(dim3(p.B * p.Hkv), dim3(128), 0, stream, true);
+    e = cudaLaunchKernelEx(&lc.cfg, decode_combine_kernel<D, G>, p);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 

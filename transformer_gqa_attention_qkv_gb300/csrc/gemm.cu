@@ -478,6 +478,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     unsigned *err = P.err;
+    grid_dep_launch();  // the next kernel may start its prologue meanwhile
     // tiles this CTA walks, and its K blocks [kb0, kb1) of each
     const uint32_t crank = KS > 1 ? cluster_rank() : 0;
     const int tile0 = KS > 1 ? (int)(blockIdx.x / KS) : (int)blockIdx.x;
@@ -514,6 +515,35 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp == 0) {
         if (lane == 0) {
+            auto load_a = [&](int s, int mb, int kb) {
+                if constexpr (AMN) {
+                    for (int c = 0; c < BM / 64; ++c)
+                        tma_load_2d(sA + s * L::A_BYTES + c * kMnChunk, &tmA, mb * BM + c * 64, kb * BK, full + s);
+                } else {
+                    tma_load_2d(sA + s * L::A_BYTES, &tmA, kb * BK, mb * BM, full + s);
+                }
+            };
+            auto load_b = [&](int s, int nb, int kb) {
+                if constexpr (BMN) {
+                    for (int c = 0; c < BN / 64; ++c)
+                        tma_load_2d(sB + s * L::B_BYTES + c * kMnChunk, &tmB, nb * BN + c * 64, kb * BK, full + s);
+                } else {
+                    tma_load_2d(sB + s * L::B_BYTES, &tmB, kb * BK, nb * BN, full + s);
+                }
+            };
+            // B (the weight matrix wherever this kernel follows another one as a
+            // programmatic dependent) does not come from the previous kernel: the
+            // first ring fill's B tiles go out before waiting for that kernel
+            int pre = 0;
+            if (tile0 < P.num_tiles) {
+                int mb, nb;
+                tile_coords(tile0, P.num_m, P.num_n, P.group_m, mb, nb);
+                for (int kb = kb0; kb < kb1 && pre < STAGES; ++kb, ++pre) {
+                    mbar_arrive_expect_tx(full + pre, L::A_BYTES + L::B_BYTES);
+                    load_b(pre, nb, kb);
+                }
+            }
+            grid_dep_wait();
             int it = 0;
             bool ok = true;
             for (int tile = tile0; ok && tile < P.num_tiles; tile += tile_step) {
@@ -521,24 +551,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tile_coords(tile, P.num_m, P.num_n, P.group_m, mb, nb);
                 for (int kb = kb0; kb < kb1; ++kb, ++it) {
                     const int s = it % STAGES;
-                    const uint32_t ph = (it / STAGES) & 1;
-                    if (!mbar_wait(empty + s, ph ^ 1, err)) {
-                        ok = false;
-                        break;
+                    if (it >= pre) {
+                        const uint32_t ph = (it / STAGES) & 1;
+                        if (!mbar_wait(empty + s, ph ^ 1, err)) {
+                            ok = false;
+                            break;
+                        }
+                        mbar_arrive_expect_tx(full + s, L::A_BYTES + L::B_BYTES);
+                        load_b(s, nb, kb);
                     }
-                    mbar_arrive_expect_tx(full + s, L::A_BYTES + L::B_BYTES);
-                    if constexpr (AMN) {
-                        for (int c = 0; c < BM / 64; ++c)
-                            tma_load_2d(sA + s * L::A_BYTES + c * kMnChunk, &tmA, mb * BM + c * 64, kb * BK, full + s);
-                    } else {
-                        tma_load_2d(sA + s * L::A_BYTES, &tmA, kb * BK, mb * BM, full + s);
-                    }
-                    if constexpr (BMN) {
-                        for (int c = 0; c < BN / 64; ++c)
-                            tma_load_2d(sB + s * L::B_BYTES + c * kMnChunk, &tmB, nb * BN + c * 64, kb * BK, full + s);
-                    } else {
-                        tma_load_2d(sB + s * L::B_BYTES, &tmB, kb * BK, nb * BN, full + s);
-                    }
+                    load_a(s, mb, kb);
                 }
             }
             // every issued copy has landed before the CTA may exit
@@ -584,6 +606,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else {
         const int quarter = warp & 3;  // TMEM lanes this warp may access
         const int row = quarter * 32 + lane;
+        grid_dep_wait();  // the epilogue reads and writes what the previous kernel may touch
         int use = 0;
         for (int tile = tile0; tile < P.num_tiles; tile += tile_step, ++use) {
             int mb, nb;
@@ -689,25 +712,11 @@ cudaError_t run(const GemmProblem &p, const GemmParams &params, int num_sms, cud
     auto kern = gemm_kernel<BN, STAGES, EPI, D, MAJ, KS>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC);
     if (e != cudaSuccess) return e;
-    if constexpr (KS > 1) {
-        cudaLaunchConfig_t cfg{};
-        cfg.gridDim = dim3(params.num_tiles * KS);
-        cfg.blockDim = dim3(kThreads);
-        cfg.dynamicSmemBytes = L::ALLOC;
-        cfg.stream = stream;
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = KS;
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-        e = cudaLaunchKernelEx(&cfg, kern, ta, tb, params);
-        if (e != cudaSuccess) return e;
-        return cudaGetLastError();
-    }
-    const int grid = params.num_tiles < num_sms ? params.num_tiles : num_sms;
-    kern<<<grid, kThreads, L::ALLOC, stream>>>(ta, tb, params);
+    // split K: one tile per cluster of KS CTAs; otherwise persistent, one CTA per SM at most
+    const int grid = KS > 1 ? params.num_tiles * KS : (params.num_tiles < num_sms ? params.num_tiles : num_sms);
+    LaunchCfg lc(dim3(grid), dim3(kThreads), L::ALLOC, stream, p.pdl != 0, KS);
+    e = cudaLaunchKernelEx(&lc.cfg, kern, ta, tb, params);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 

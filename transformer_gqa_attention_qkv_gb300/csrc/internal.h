@@ -53,6 +53,7 @@ struct GemmProblem {
     const void *A;  // [M, K] bf16 (stored [K, M] when MN-major)
     const void *B;  // [N, K] bf16 (stored [K, N] when MN-major)
     int M, N, K;
+    int pdl = 0;    // launch as the programmatic dependent of the previous kernel (see LaunchCfg)
 };
 
 // Output of launch_gemm_general.
@@ -87,6 +88,7 @@ struct AttentionProblem {
     float *lse;            // non-NULL (plain prefill only): per (b, head, t) log2-sum-exp of the
                            // scaled scores, at lse[(b*Hq + head)*lse_ld + t]: P = 2^(s*log2(e)/sqrt(d) - lse)
     int lse_ld;
+    int pdl = 0;           // launch as the programmatic dependent of the previous kernel
 };
 cudaError_t launch_attention(const AttentionProblem &p, unsigned *err, int num_sms, cudaStream_t stream);
 // Backward of the attention (head_dim 64 / 128, Hq/Hkv <= 32).  q, k, v, dO
@@ -135,6 +137,7 @@ struct DecodeAttentionProblem {
     int B, Hq, Hkv, d, Lmax;
     float *partials;          // split partials (see decode_partials_floats)
     int splits;               // number of key splits per (b, kv head)
+    int pdl;                  // launch the split kernel as the programmatic dependent of the previous kernel
 };
 int decode_choose_splits(int B, int Hkv, int Lmax, int num_sms);
 size_t decode_partials_floats(int B, int Hq, int splits, int d);
@@ -145,6 +148,40 @@ cudaError_t launch_selftest_wait(unsigned *err, unsigned long long limit_ns, cud
 
 // Sets the message gqa_last_error() returns on the calling thread.
 void record_error_message(const char *msg);
+
+// Launch configuration for cudaLaunchKernelEx: optional thread-block cluster
+// (cluster > 1 CTAs along x) and optional programmatic dependent launch (pdl:
+// the kernel may start while the previous kernel in the stream finishes; it
+// must call grid_dep_wait before touching that kernel's outputs).  Used in
+// place: cfg.attrs points into the object.
+struct LaunchCfg {
+    cudaLaunchConfig_t cfg{};
+    cudaLaunchAttribute attr[2];
+    LaunchCfg(dim3 grid, dim3 block, size_t smem, cudaStream_t stream, bool pdl, int cluster = 1)
+    {
+        cfg.gridDim = grid;
+        cfg.blockDim = block;
+        cfg.dynamicSmemBytes = smem;
+        cfg.stream = stream;
+        int n = 0;
+        if (cluster > 1) {
+            attr[n].id = cudaLaunchAttributeClusterDimension;
+            attr[n].val.clusterDim.x = (unsigned)cluster;
+            attr[n].val.clusterDim.y = 1;
+            attr[n].val.clusterDim.z = 1;
+            ++n;
+        }
+        if (pdl) {
+            attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+            attr[n].val.programmaticStreamSerializationAllowed = 1;
+            ++n;
+        }
+        cfg.attrs = attr;
+        cfg.numAttrs = (unsigned)n;
+    }
+    LaunchCfg(const LaunchCfg &) = delete;
+    LaunchCfg &operator=(const LaunchCfg &) = delete;
+};
 
 // Tensor-map encoder (driver entry point, resolved once); elements of 2 bytes
 // (16-bit floats, copied bit for bit), 1 byte (FP8 codes) or 4 bytes (fp32).

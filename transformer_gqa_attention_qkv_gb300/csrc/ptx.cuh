@@ -92,6 +92,17 @@ DEVI bool mbar_wait(uint64_t *bar, uint32_t parity, unsigned *err, uint64_t limi
     }
 }
 
+// ------------------------------------------------ programmatic dependent launch
+
+// Wait until the grids this one depends on (the previous kernel in the stream,
+// when this one was launched as its programmatic dependent) have completed and
+// their memory operations are visible.  Returns at once otherwise.
+DEVI void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Let the next kernel in the stream, if launched as a programmatic dependent,
+// be scheduled (its own grid_dep_wait still orders it after this grid).
+DEVI void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // ----------------------------------------------------------------- clusters
 
 // Rank of this CTA in its thread-block cluster.
