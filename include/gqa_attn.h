@@ -119,6 +119,34 @@ int gqa_attn_forward(const gqa_bf16 *x, const gqa_bf16 *Wqkv, const gqa_bf16 *Wo
                      int B, int S, int hidden, int Hq, int Hkv, int head_dim, int causal,
                      gqa_bf16 *out);
 
+/* Bytes of device workspace gqa_attn_forward_host needs: that of
+ * gqa_attn_workspace_size plus device copies of x and out (each 256-byte
+ * aligned).  Returns 0 for invalid sizes. */
+size_t gqa_attn_forward_host_workspace_size(int B, int S, int hidden, int Hq, int Hkv, int head_dim);
+
+/* The layer forward of gqa_attn_forward_ex with x and out in HOST memory
+ * (x_host [B, S, hidden] read, out_host [B, S, hidden] written; page-locked
+ * memory lets the copies run asynchronously, pageable memory works but the
+ * copies then serialise with the host).  Weights, norm weights and workspace
+ * are device memory as for gqa_attn_forward_ex; workspace: at least
+ * gqa_attn_forward_host_workspace_size(...) bytes, 256-byte aligned.
+ * The copies overlap the compute: x is copied in by token chunks (at most four,
+ * each a multiple of 128 rows, none below 2048 rows) on a copy stream the
+ * library keeps per device, and each chunk's QKV projection starts on `stream`
+ * when its rows have landed; after the attention, o_proj runs chunk by chunk
+ * and each finished chunk of out is copied back while the next is computed.
+ * The result is bit-identical to gqa_attn_forward_ex on the same inputs.  All
+ * of it is ordered after the work already on `stream`, and `stream` resumes
+ * after the last copy, so out_host is complete once `stream` is.  Calls that
+ * share a workspace must not overlap on the device; the host-side enqueue is
+ * serialised per device.  GQA_ERR_ARG also when x_host or out_host is device
+ * memory or they overlap. */
+int gqa_attn_forward_host(const gqa_bf16 *x_host, const gqa_bf16 *Wqkv, const gqa_bf16 *Wo,
+                          const gqa_bf16 *q_norm_w, const gqa_bf16 *k_norm_w,
+                          float rope_theta, float eps,
+                          int B, int S, int hidden, int Hq, int Hkv, int head_dim, int causal,
+                          gqa_bf16 *out_host, void *workspace, size_t workspace_bytes, void *stream);
+
 /* Stage 1 alone: qkv = x @ Wqkv^T, then QK-norm and RoPE at positions
  * 0..S-1, written head-major ([T07] §4 steps 1-4), as binary16:
  *   q_out [B, Hq, S, head_dim], k_out and v_out [B, Hkv, S, head_dim]. */

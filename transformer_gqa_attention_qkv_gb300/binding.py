@@ -35,7 +35,7 @@ EXPORTS = (
     "gqa_attn_forward_rd", "gqa_qkv_proj_rd", "gqa_attn_prefill_cached_rd", "gqa_attn_decode_rd",
     "gqa_decode_qkv_rd", "gqa_attn_decode_fp8", "gqa_decode_qkv_fp8", "gqa_decode_attention_fp8",
     "gqa_attn_backward_workspace_size", "gqa_attn_backward", "gqa_attention_backward_workspace_size",
-    "gqa_attention_backward",
+    "gqa_attention_backward", "gqa_attn_forward_host_workspace_size", "gqa_attn_forward_host",
 )
 
 
@@ -66,6 +66,8 @@ def lib():
         "gqa_attn_workspace_size": (_Z, [_I] * 6),
         "gqa_attn_forward_ex": (_I, [_P] * 5 + [_F, _F] + [_I] * 7 + [_P, _P, _Z, _P]),
         "gqa_attn_forward": (_I, [_P] * 5 + [_F, _F] + [_I] * 7 + [_P]),
+        "gqa_attn_forward_host_workspace_size": (_Z, [_I] * 6),
+        "gqa_attn_forward_host": (_I, [_P] * 5 + [_F, _F] + [_I] * 7 + [_P, _P, _Z, _P]),
         "gqa_qkv_proj": (_I, [_P] * 4 + [_F, _F] + [_I] * 6 + [_P] * 4),
         "gqa_attention": (_I, [_P] * 3 + [_I] * 6 + [_P, _P]),
         "gqa_oproj_residual": (_I, [_P] * 3 + [_I] * 3 + [_P, _P]),
@@ -168,6 +170,33 @@ def gqa_attn_forward_ex(x, Wqkv, Wo, q_norm_w, k_norm_w, rope_theta, eps, B, S, 
                                      _bf16(out), _ptr(workspace), workspace.numel() * workspace.element_size(),
                                      _stream(stream)))
     return out
+
+
+def _host_bf16(t):
+    """A contiguous bf16 tensor in host memory (page-locked for asynchronous copies)."""
+    if not isinstance(t, torch.Tensor):
+        raise TypeError("expected a torch.Tensor")
+    if t.is_cuda:
+        raise ValueError("tensor must be in host memory")
+    if t.dtype != torch.bfloat16:
+        raise TypeError(f"expected bfloat16, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError("tensor must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def gqa_attn_forward_host_workspace_size(B, S, hidden, Hq, Hkv, head_dim) -> int:
+    return int(lib().gqa_attn_forward_host_workspace_size(B, S, hidden, Hq, Hkv, head_dim))
+
+
+def gqa_attn_forward_host(x_host, Wqkv, Wo, q_norm_w, k_norm_w, rope_theta, eps, B, S, hidden, Hq, Hkv,
+                          head_dim, causal, out_host, workspace, stream=None):
+    """x_host / out_host: host tensors (pinned for overlap); out_host is complete once `stream` is."""
+    _check(lib().gqa_attn_forward_host(_host_bf16(x_host), _bf16(Wqkv), _bf16(Wo), _bf16(q_norm_w),
+                                       _bf16(k_norm_w), rope_theta, eps, B, S, hidden, Hq, Hkv, head_dim,
+                                       int(causal), _host_bf16(out_host), _ptr(workspace),
+                                       workspace.numel() * workspace.element_size(), _stream(stream)))
+    return out_host
 
 
 def gqa_attn_forward(x, Wqkv, Wo, q_norm_w, k_norm_w, rope_theta, eps, B, S, hidden, Hq, Hkv,

@@ -227,7 +227,7 @@ static int run_qkv(DeviceState &st, const gqa_bf16 *x, const gqa_bf16 *Wqkv, con
                    float theta, float eps, int rd, int B, int S, int hidden, int Hq, int Hkv, int d, const int *pos_dev,
                    int q_seq, int kv_seq, int rope_rows, int q_f16, int kv_f16, uint16_t *q_out, uint16_t *k_out,
                    uint16_t *v_out, cudaStream_t stream, int kv_fp8 = 0, float k_scale = 1.0f, float v_scale = 1.0f,
-                   float *pre_out = nullptr)
+                   float *pre_out = nullptr, int rows = -1, int m0 = 0)
 {
     const float2 *rope = nullptr;
     if (rd > 0) {
@@ -238,8 +238,10 @@ static int run_qkv(DeviceState &st, const gqa_bf16 *x, const gqa_bf16 *Wqkv, con
         }
         if (rc) return rc;
     }
-    GemmProblem p{x, Wqkv, B * S, (Hq + 2 * Hkv) * d, hidden};
+    // rows >= 0: rows [m0, m0 + rows) of the B*S token rows, x pointing at row m0
+    GemmProblem p{x, Wqkv, rows >= 0 ? rows : B * S, (Hq + 2 * Hkv) * d, hidden};
     QkvEpilogue e{};
+    e.m0 = m0;
     e.Hq = Hq;
     e.Hkv = Hkv;
     e.d = d;
@@ -428,6 +430,139 @@ int gqa_attn_forward_rd(const gqa_bf16 *x, const gqa_bf16 *Wqkv, const gqa_bf16 
     if ((rc = run_attention(*st, q, k, v, B, S, Hq, Hkv, head_dim, causal, attn, s, 0, nullptr, 0, nullptr, 0, 1)))
         return rc;
     return run_oproj(*st, attn, Wo, x, B * S, hidden, Hq * head_dim, out, s, 1);
+}
+
+// ----------------------------------------------- forward from host buffers
+
+size_t gqa_attn_forward_host_workspace_size(int B, int S, int hidden, int Hq, int Hkv, int head_dim)
+{
+    if (B <= 0 || S <= 0 || hidden <= 0 || Hq <= 0 || Hkv <= 0 || head_dim <= 0) return 0;
+    const size_t nx = align256((size_t)B * S * hidden * 2);
+    return fwd_layout(B, S, Hq, Hkv, head_dim).total + 2 * nx;  // + device copies of x and out
+}
+
+// Token chunks of the host pipeline: at most kHostChunks, each a multiple of
+// the 128-row GEMM tile (so every output element is computed exactly as by
+// the one-shot forward), and none below 2048 rows.
+static constexpr int kHostChunks = 4;
+static int host_chunk_rows(int M)
+{
+    int n = M / 2048;
+    n = n < 1 ? 1 : (n > kHostChunks ? kHostChunks : n);
+    int r = (M + n - 1) / n;
+    return (r + 127) / 128 * 128;
+}
+
+// A copy stream and its events, per device, created on first use.
+struct HostPipe {
+    std::mutex mu;  // one call at a time enqueues through these events
+    bool init = false;
+    cudaStream_t copy = nullptr;
+    cudaEvent_t fork = nullptr, join = nullptr, in[kHostChunks] = {}, out[kHostChunks] = {};
+};
+static HostPipe g_pipe[64];
+
+static int host_pipe(HostPipe **out)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= 64) return fail(GQA_ERR_CUDA, "device index %d out of range", dev);
+    std::lock_guard<std::mutex> lk(g_mu);
+    HostPipe &p = g_pipe[dev];
+    if (!p.init) {
+        if ((e = cudaStreamCreateWithFlags(&p.copy, cudaStreamNonBlocking)) != cudaSuccess)
+            return cuda_fail(e, "copy stream");
+        cudaEvent_t *evs[2 + 2 * kHostChunks] = {&p.fork, &p.join};
+        for (int i = 0; i < kHostChunks; ++i) {
+            evs[2 + i] = &p.in[i];
+            evs[2 + kHostChunks + i] = &p.out[i];
+        }
+        for (cudaEvent_t *ev : evs)
+            if ((e = cudaEventCreateWithFlags(ev, cudaEventDisableTiming)) != cudaSuccess)
+                return cuda_fail(e, "pipeline event");
+        p.init = true;
+    }
+    *out = &p;
+    return GQA_OK;
+}
+
+int gqa_attn_forward_host(const gqa_bf16 *x_host, const gqa_bf16 *Wqkv, const gqa_bf16 *Wo,
+                          const gqa_bf16 *q_norm_w, const gqa_bf16 *k_norm_w, float rope_theta, float eps, int B,
+                          int S, int hidden, int Hq, int Hkv, int head_dim, int causal, gqa_bf16 *out_host,
+                          void *workspace, size_t workspace_bytes, void *stream)
+{
+    g_launches = 0;
+    int rc = check_layer(B, S, hidden, Hq, Hkv, head_dim, q_norm_w, k_norm_w);
+    if (rc) return rc;
+    if ((rc = check_group_pow2(Hq, Hkv))) return rc;
+    if (!x_host || !Wqkv || !Wo || !out_host) return fail(GQA_ERR_ARG, "null tensor pointer");
+    if (!aligned16(Wqkv) || !aligned16(Wo)) return fail(GQA_ERR_ARG, "weight pointers must be 16-byte aligned");
+    if (!(rope_theta > 0.0f) || !(eps >= 0.0f)) return fail(GQA_ERR_ARG, "rope_theta must be > 0 and eps >= 0");
+    const size_t nx = (size_t)B * S * hidden * 2;
+    if (overlap(out_host, nx, x_host, nx)) return fail(GQA_ERR_ARG, "out_host must not overlap x_host");
+    for (const void *h : {(const void *)x_host, (const void *)out_host}) {
+        cudaPointerAttributes a{};
+        if (cudaPointerGetAttributes(&a, h) == cudaSuccess && a.type == cudaMemoryTypeDevice)
+            return fail(GQA_ERR_ARG, "x_host and out_host must be host memory");
+        (void)cudaGetLastError();
+    }
+    const FwdLayout L = fwd_layout(B, S, Hq, Hkv, head_dim);
+    const size_t nx_al = align256(nx);
+    const size_t need = L.total + 2 * nx_al;
+    if (!workspace || workspace_bytes < need)
+        return fail(GQA_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", need,
+                    workspace ? workspace_bytes : (size_t)0);
+    if (((uintptr_t)workspace & 255u) != 0) return fail(GQA_ERR_ARG, "workspace must be 256-byte aligned");
+    DeviceState *st;
+    if ((rc = device_state(&st))) return rc;
+    HostPipe *pp;
+    if ((rc = host_pipe(&pp))) return rc;
+    std::lock_guard<std::mutex> lk(pp->mu);
+    uint8_t *ws = (uint8_t *)workspace;
+    gqa_bf16 *q = (gqa_bf16 *)(ws + L.q), *k = (gqa_bf16 *)(ws + L.k), *v = (gqa_bf16 *)(ws + L.v);
+    gqa_bf16 *attn = (gqa_bf16 *)(ws + L.attn);
+    gqa_bf16 *x = (gqa_bf16 *)(ws + L.total), *out = (gqa_bf16 *)(ws + L.total + nx_al);
+    cudaStream_t s = (cudaStream_t)stream, c = pp->copy;
+    const int M = B * S, R = host_chunk_rows(M), n = (M + R - 1) / R;
+    const int qw = Hq * head_dim;
+    cudaError_t e;
+    // copies of x in, chunk by chunk, on the copy stream (after the caller's prior work)
+    if ((e = cudaEventRecord(pp->fork, s)) != cudaSuccess || (e = cudaStreamWaitEvent(c, pp->fork, 0)) != cudaSuccess)
+        return cuda_fail(e, "pipeline fork");
+    for (int i = 0; i < n; ++i) {
+        const size_t r0 = (size_t)i * R, rows = (size_t)(i + 1 < n ? R : M - i * R);
+        if ((e = cudaMemcpyAsync(x + r0 * hidden, x_host + r0 * hidden, rows * hidden * 2, cudaMemcpyHostToDevice,
+                                 c)) != cudaSuccess ||
+            (e = cudaEventRecord(pp->in[i], c)) != cudaSuccess)
+            return cuda_fail(e, "host-to-device copy");
+    }
+    // each chunk's projection as soon as its rows have landed
+    for (int i = 0; i < n; ++i) {
+        const int r0 = i * R, rows = i + 1 < n ? R : M - i * R;
+        if ((e = cudaStreamWaitEvent(s, pp->in[i], 0)) != cudaSuccess) return cuda_fail(e, "pipeline wait");
+        if ((rc = run_qkv(*st, x + (size_t)r0 * hidden, Wqkv, q_norm_w, k_norm_w, rope_theta, eps, head_dim, B, S,
+                          hidden, Hq, Hkv, head_dim, nullptr, S, S, S, 1, 1, q, k, v, s, 0, 1.0f, 1.0f, nullptr,
+                          rows, r0)))
+            return rc;
+    }
+    if ((rc = run_attention(*st, q, k, v, B, S, Hq, Hkv, head_dim, causal, attn, s, 0, nullptr, 0, nullptr, 0, 1)))
+        return rc;
+    // o_proj chunk by chunk, each copied out while the next one is computed
+    for (int i = 0; i < n; ++i) {
+        const int r0 = i * R, rows = i + 1 < n ? R : M - i * R;
+        if ((rc = run_oproj(*st, attn + (size_t)r0 * qw, Wo, x + (size_t)r0 * hidden, rows, hidden, qw,
+                            out + (size_t)r0 * hidden, s, i == 0 ? 1 : 0)))
+            return rc;
+        if ((e = cudaEventRecord(pp->out[i], s)) != cudaSuccess || (e = cudaStreamWaitEvent(c, pp->out[i], 0)) != cudaSuccess ||
+            (e = cudaMemcpyAsync(out_host + (size_t)r0 * hidden, out + (size_t)r0 * hidden, (size_t)rows * hidden * 2,
+                                 cudaMemcpyDeviceToHost, c)) != cudaSuccess)
+            return cuda_fail(e, "device-to-host copy");
+    }
+    // the caller's stream resumes after the last copy
+    if ((e = cudaEventRecord(pp->join, c)) != cudaSuccess || (e = cudaStreamWaitEvent(s, pp->join, 0)) != cudaSuccess)
+        return cuda_fail(e, "pipeline join");
+    return GQA_OK;
 }
 
 int gqa_attn_forward(const gqa_bf16 *x, const gqa_bf16 *Wqkv, const gqa_bf16 *Wo, const gqa_bf16 *q_norm_w,

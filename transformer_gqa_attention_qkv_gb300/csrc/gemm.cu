@@ -308,8 +308,9 @@ DEVI void epilogue_qkv(const GemmParams &P, uint32_t tcol, int m, int n0, bool r
             pos = e.pos_dev[b] + q_slot;
             kv_slot = pos;
         } else {
-            b = m / e.S;
-            pos = m - b * e.S;
+            const int mg = e.m0 + m;  // row of the whole problem
+            b = mg / e.S;
+            pos = mg - b * e.S;
             q_slot = kv_slot = pos;
         }
         if (pos < 0 || pos >= e.rope_rows || kv_slot >= e.kv_seq) {

@@ -18,7 +18,8 @@ namespace gqa {
 // rotated (RoPE) at the row's position; results are written head-major.
 struct QkvEpilogue {
     int Hq, Hkv, d;
-    int S;                 // tokens per sequence (row m = b*S + t)
+    int S;                 // tokens per sequence (row m0 + m = b*S + t)
+    int m0;                // rows of the whole problem before this GEMM's row 0 (token chunks; pos_dev NULL only)
     const int *pos_dev;    // cached: position = K/V slot = pos_dev[b] + t; NULL: position t
     int q_seq;             // sequence extent of q_out (S, or 1 for decode)
     int kv_seq;            // sequence extent of k_out / v_out (S, or Lmax for decode)
