@@ -174,7 +174,12 @@ int gqa_oproj_residual(const gqa_bf16 *attn, const gqa_bf16 *Wo, const gqa_bf16 
 /* ---------------------------------------------------- prefill into a cache */
 
 /* Bytes of workspace gqa_attn_prefill_cached needs: Q [B,Hq,S,d] and attn
- * [B,S,Hq*d], both bf16, 256-byte aligned. */
+ * [B,S,Hq*d], both bf16, and room for the attention's two key splits (their
+ * binary16 outputs [2][B,S,Hq*d] and fp32 log2-sum-exp rows [2][B*Hq,S]), each
+ * 256-byte aligned.  The keys are split when the attention would otherwise
+ * run fewer than eight waves of work items on the GPU (B*Hq*S/256 items
+ * against the SM count); a binary16 partial beyond +-65504 is clamped and
+ * reported as GQA_ERR_RANGE. */
 size_t gqa_attn_prefill_cached_workspace_size(int B, int S, int Hq, int head_dim);
 
 /* Chunked prefill: S new tokens per sequence appended to a KV cache

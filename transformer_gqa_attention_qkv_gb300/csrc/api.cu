@@ -275,13 +275,13 @@ static int run_qkv(DeviceState &st, const gqa_bf16 *x, const gqa_bf16 *Wqkv, con
 static int run_attention(DeviceState &st, const uint16_t *q, const uint16_t *k, const uint16_t *v, int B, int S,
                          int Hq, int Hkv, int d, int causal, gqa_bf16 *out, cudaStream_t stream, int kv_seq = 0,
                          const int *kv_start = nullptr, int bf16_qkv = 0, float *lse = nullptr, int lse_ld = 0,
-                         int pdl = 0)
+                         int pdl = 0, int kv_splits = 1, uint16_t *part_o = nullptr, float *part_lse = nullptr)
 {
     AttentionProblem p{q,         k,        v,        out, B,   S,      Hq, Hkv, d, causal ? 1 : 0,
-                       kv_seq > 0 ? kv_seq : S, kv_start, bf16_qkv, lse, lse_ld, pdl};
+                       kv_seq > 0 ? kv_seq : S, kv_start, bf16_qkv, lse, lse_ld, pdl, kv_splits, part_o, part_lse};
     cudaError_t ce = launch_attention(p, st.err, st.num_sms, stream);
     if (ce != cudaSuccess) return cuda_fail(ce, "attention launch");
-    ++g_launches;
+    g_launches += kv_splits > 1 && part_o && part_lse && bf16_qkv && d != 256 ? 2 : 1;
     return GQA_OK;
 }
 
@@ -934,11 +934,40 @@ int gqa_attn_decode_rd(const gqa_bf16 *x, const gqa_bf16 *Wqkv, const gqa_bf16 *
 
 // ------------------------------------------------------ prefill into a cache
 
+// Workspace of the cached prefill: Q (bf16), attn (bf16), and for the
+// attention's key splits (kCachedSplits at most) their binary16 partial
+// outputs and fp32 log2-sum-exp rows.
+static constexpr int kCachedSplits = 2;
+struct CachedLayout {
+    size_t q, attn, part_o, part_lse, total;
+};
+static CachedLayout cached_layout(int B, int S, int Hq, int d)
+{
+    CachedLayout L;
+    const size_t n = align256((size_t)B * S * Hq * d * 2);
+    L.q = 0;
+    L.attn = n;
+    L.part_o = 2 * n;
+    L.part_lse = L.part_o + kCachedSplits * n;
+    L.total = L.part_lse + align256((size_t)kCachedSplits * B * Hq * S * 4);
+    return L;
+}
+
 size_t gqa_attn_prefill_cached_workspace_size(int B, int S, int Hq, int head_dim)
 {
     if (B <= 0 || S <= 0 || Hq <= 0 || head_dim <= 0) return 0;
-    const size_t n = (size_t)B * S * Hq * head_dim * 2;
-    return 2 * align256(n);  // Q (bf16) and attn (bf16)
+    return cached_layout(B, S, Hq, head_dim).total;
+}
+
+// Key splits for the cached prefill's attention.  Its work items (sequence,
+// KV head, block of 256/G query positions: B*Hq*S/256 of them) all see the
+// whole cache, so they are about equally long, and below eight waves of the
+// GPU the last, partly filled wave leaves many SMs idle; splitting every
+// item's keys in two halves that idle share.
+static int cached_splits(int B, int S, int Hq, int num_sms)
+{
+    const long long items = ((long long)B * Hq * S + 255) / 256;
+    return items < 8LL * num_sms ? kCachedSplits : 1;
 }
 
 static int check_cached(int B, int S, int hidden, int Hq, int Hkv, int d, int Lmax, const void *qn, const void *kn)
@@ -992,15 +1021,17 @@ int gqa_attn_prefill_cached_rd(const gqa_bf16 *x, const gqa_bf16 *Wqkv, const gq
     DeviceState *st;
     if ((rc = device_state(&st))) return rc;
     uint8_t *ws = (uint8_t *)workspace;
-    gqa_bf16 *q = (gqa_bf16 *)ws;  // bf16: it meets the bf16 cache in the score MMA
-    gqa_bf16 *attn = (gqa_bf16 *)(ws + need / 2);
+    const CachedLayout CL = cached_layout(B, S, Hq, head_dim);
+    gqa_bf16 *q = (gqa_bf16 *)(ws + CL.q);  // bf16: it meets the bf16 cache in the score MMA
+    gqa_bf16 *attn = (gqa_bf16 *)(ws + CL.attn);
+    const int splits = cached_splits(B, S, Hq, st->num_sms);
     cudaStream_t s = (cudaStream_t)stream;
     // K/V of the new tokens go straight into the cache at slots cache_len[b] + t
     if ((rc = run_qkv(*st, x, Wqkv, q_norm_w, k_norm_w, rope_theta, eps, rotary_dim, B, S, hidden, Hq, Hkv, head_dim,
                       cache_len, S, Lmax, Lmax, 0, 0, q, k_cache, v_cache, s)))
         return rc;
     if ((rc = run_attention(*st, q, k_cache, v_cache, B, S, Hq, Hkv, head_dim, causal, attn, s, Lmax, cache_len, 1,
-                            nullptr, 0, 1)))
+                            nullptr, 0, 1, splits, (uint16_t *)(ws + CL.part_o), (float *)(ws + CL.part_lse))))
         return rc;
     return run_oproj(*st, attn, Wo, x, B * S, hidden, Hq * head_dim, out, s, 1);
 }

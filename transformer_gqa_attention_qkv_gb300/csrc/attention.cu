@@ -28,6 +28,12 @@
 // rescaled in TMEM only when a row's running max grows by more than 2^8; P
 // stays <= 2^8 in between, and the final O / l is exact either way.
 //
+// Cached variant with kv_splits > 1: the keys of a work item are split into
+// kv_splits consecutive ranges of key tiles, each its own work item (a grid of
+// few, equally long items otherwise leaves most SMs idle in its last wave);
+// each writes its rows' O normalised by its own row sum (binary16) and its
+// log2-sum-exp, and combine_kernel merges them.
+//
 // Q, K and V arrive as binary16: with QK-norm their rows are bounded by
 // sqrt(d) * max|w|, and binary16 keeps 3 more mantissa bits than bf16, which
 // cuts the rounding error that storage adds to scores and outputs.
@@ -52,6 +58,9 @@ struct AttnParams {
     uint16_t *out;
     float *lse;        // optional log2-sum-exp at lse[(b*Hq + head)*lse_ld + t] (plain prefill)
     int lse_ld;
+    int kv_splits;        // cached variant: key ranges per query block (1: none)
+    uint16_t *part_o;     // kv_splits > 1: [split][B, S, Hq*d] binary16, O / l of the split
+    float *part_lse;      // kv_splits > 1: [split][B*Hq, S] log2-sum-exp of the split (-inf: no key)
     unsigned *err;
 };
 
@@ -107,8 +116,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     unsigned *err = P.err;
     grid_dep_launch();  // the next kernel may start its prologue meanwhile
 
-    // heavy (late) query blocks first
-    const int item = blockIdx.x;
+    // heavy (late) query blocks first; the key splits of one block adjacent
+    const int KSPL = CACHED ? P.kv_splits : 1;
+    const int split = (int)blockIdx.x % KSPL;
+    const int item = (int)blockIdx.x / KSPL;
     const int bh = item % (P.B * P.Hkv);
     const int qblk = P.n_qblk - 1 - item / (P.B * P.Hkv);
     const int b = bh / P.Hkv, g = bh % P.Hkv;
@@ -125,7 +136,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             p0 = 0;
         }
     }
-    const int n_kv = bad ? 0 : (P.causal ? ((p0 + t_last) / kKeys + 1) : (p0 + P.S + kKeys - 1) / kKeys);
+    const int n_all = bad ? 0 : (P.causal ? ((p0 + t_last) / kKeys + 1) : (p0 + P.S + kKeys - 1) / kKeys);
+    // this item's key tiles: [kb0, kb0 + n_kv) (loop indices below are local)
+    const int kb0 = split * n_all / KSPL;
+    const int n_kv = (split + 1) * n_all / KSPL - kb0;
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < L::NBARS; ++i) mbar_init(bars + i, 1);
@@ -158,12 +172,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!mbar_wait(kv_empty + s, ((j / ST) & 1) ^ 1, err)) break;
                 mbar_arrive_expect_tx(k_full + s, L::NCH * L::CHUNK);
                 for (int c = 0; c < L::NCH; ++c)
-                    tma_load_3d(smem + L::K + (s * L::NCH + c) * L::CHUNK, &tmK, c * 64, j * kKeys, b * P.Hkv + g,
-                                k_full + s);
+                    tma_load_3d(smem + L::K + (s * L::NCH + c) * L::CHUNK, &tmK, c * 64, (kb0 + j) * kKeys,
+                                b * P.Hkv + g, k_full + s);
                 mbar_arrive_expect_tx(v_full + s, L::NCH * L::CHUNK);
                 for (int c = 0; c < L::NCH; ++c)
-                    tma_load_3d(smem + L::V + (s * L::NCH + c) * L::CHUNK, &tmV, c * 64, j * kKeys, b * P.Hkv + g,
-                                v_full + s);
+                    tma_load_3d(smem + L::V + (s * L::NCH + c) * L::CHUNK, &tmV, c * 64, (kb0 + j) * kKeys,
+                                b * P.Hkv + g, v_full + s);
             }
             // every issued copy has landed before the CTA may exit
             mbar_wait(q_full, 0, err);
@@ -250,7 +264,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int j = 0; j < n_kv; ++j) {
             if (!mbar_wait(s_full + wg, j & 1, err)) break;
             tc_fence_after();
-            const int u0 = j * kKeys;
+            const int u0 = (kb0 + j) * kKeys;
             // the whole S row in registers (one TMEM load, one wait)
             uint32_t v[kKeys];
             tmem_ld128(tS, v);
@@ -311,17 +325,28 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(p_full + wg);
         }
-        if (CACHED && n_kv == 0) {  // rejected offset (reported): zero rows, nothing else ran
+        const int head = g * P.G + hl;
+        const size_t row = (size_t)(b * P.S + t) * P.Hq + head;  // output row, [B, S, Hq] order
+        const bool split_out = CACHED && KSPL > 1;
+        if (CACHED && n_kv == 0) {
+            // no keys for this item: a rejected offset (reported; zero rows) or an
+            // empty key split (weight zero in the combine); nothing else ran
             if (row_ok) {
-                uint4 *d4 = reinterpret_cast<uint4 *>(P.out + ((size_t)(b * P.S + t) * P.Hq + g * P.G + hl) * D);
+                uint16_t *dst = split_out ? P.part_o + (size_t)split * P.B * P.S * P.Hq * D + row * D
+                                          : P.out + row * D;
+                uint4 *d4 = reinterpret_cast<uint4 *>(dst);
                 for (int c = 0; c < D / 8; ++c) d4[c] = make_uint4(0, 0, 0, 0);
+                if (split_out) P.part_lse[((size_t)split * P.B * P.Hq + b * P.Hq + head) * P.S + t] = -INFINITY;
             }
         } else if (mbar_wait(o_done + wg, 0, err)) {
             tc_fence_after();
             const float inv_l = (l_i > 0.0f) ? 1.0f / l_i : 0.0f;
-            const int head = g * P.G + hl;
-            uint16_t *dst = P.out + ((size_t)(b * P.S + t) * P.Hq + head) * D;
+            uint16_t *dst = split_out ? P.part_o + (size_t)split * P.B * P.S * P.Hq * D + row * D : P.out + row * D;
             if (!CACHED && P.lse && row_ok) P.lse[(size_t)(b * P.Hq + head) * P.lse_ld + t] = m_i + log2f(l_i);
+            if (split_out && row_ok)
+                P.part_lse[((size_t)split * P.B * P.Hq + b * P.Hq + head) * P.S + t] =
+                    l_i > 0.0f ? m_i + log2f(l_i) : -INFINITY;
+            bool clamped = false;
             constexpr int CW = D % 32 == 0 ? 32 : 16;  // columns per TMEM load, tiling d
 #pragma unroll 1
             for (int c = 0; c < D; c += CW) {
@@ -336,13 +361,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int i = 0; i < CW / 8; ++i) {
                         uint32_t w[4];
 #pragma unroll
-                        for (int k = 0; k < 4; ++k)
-                            w[k] = pack_bf16(__uint_as_float(o[8 * i + 2 * k]) * inv_l,
-                                             __uint_as_float(o[8 * i + 2 * k + 1]) * inv_l);
+                        for (int k = 0; k < 4; ++k) {
+                            float lo = __uint_as_float(o[8 * i + 2 * k]) * inv_l;
+                            float hi = __uint_as_float(o[8 * i + 2 * k + 1]) * inv_l;
+                            if (split_out) {  // binary16 partials: clamp to its range (reported)
+                                if (fabsf(lo) > 65504.0f || fabsf(hi) > 65504.0f) {
+                                    clamped = true;
+                                    lo = fminf(fmaxf(lo, -65504.0f), 65504.0f);
+                                    hi = fminf(fmaxf(hi, -65504.0f), 65504.0f);
+                                }
+                                w[k] = pack_f16(lo, hi);
+                            } else {
+                                w[k] = pack_bf16(lo, hi);
+                            }
+                        }
                         d4[i] = make_uint4(w[0], w[1], w[2], w[3]);
                     }
                 }
             }
+            if (clamped) atomicOr(P.err, kErrRange);
         }
     }
     __syncthreads();
@@ -350,6 +387,47 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         tmem_dealloc(tmem, 512);
     }
+}
+
+// Merges the key splits of the cached variant, one thread per 8 output
+// values: out = sum_s 2^(lse_s - M) O_s / sum_s 2^(lse_s - M), M = max_s lse_s
+// (a split without keys has lse = -inf and weight 0).
+template <int D>
+__global__ void __launch_bounds__(256) combine_kernel(const AttnParams P, int rows)
+{
+    grid_dep_launch();
+    grid_dep_wait();  // the split partials come from the attention kernel
+    constexpr int TPR = D / 8;  // threads per (token, head) row
+    const int gt = blockIdx.x * blockDim.x + threadIdx.x;
+    const int r = gt / TPR, c8 = (gt - r * TPR) * 8;
+    if (r >= rows) return;  // rows = B*S*Hq in [B, S, Hq] order
+    const int head = r % P.Hq, bt = r / P.Hq;
+    const int b = bt / P.S, t = bt - b * P.S;
+    const size_t split_o = (size_t)P.B * P.S * P.Hq * D, split_l = (size_t)P.B * P.Hq * P.S;
+    const size_t li = (size_t)(b * P.Hq + head) * P.S + t;
+    float M = -INFINITY;
+    for (int s = 0; s < P.kv_splits; ++s) M = fmaxf(M, P.part_lse[s * split_l + li]);
+    float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0}, wsum = 0.0f;
+    if (M != -INFINITY) {
+        for (int s = 0; s < P.kv_splits; ++s) {
+            const float ls = P.part_lse[s * split_l + li];
+            const float w = ls == -INFINITY ? 0.0f : ex2(ls - M);
+            wsum += w;
+            const uint4 v = *reinterpret_cast<const uint4 *>(P.part_o + s * split_o + (size_t)r * D + c8);
+            const uint32_t vs[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&vs[k]));
+                acc[2 * k] = fmaf(w, f.x, acc[2 * k]);
+                acc[2 * k + 1] = fmaf(w, f.y, acc[2 * k + 1]);
+            }
+        }
+    }
+    const float inv = wsum > 0.0f ? 1.0f / wsum : 0.0f;
+    uint32_t w4[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) w4[k] = pack_bf16(acc[2 * k] * inv, acc[2 * k + 1] * inv);
+    *reinterpret_cast<uint4 *>(P.out + (size_t)r * D + c8) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
 }
 
 template <int D, bool BF>
@@ -379,7 +457,10 @@ cudaError_t run_attn(const AttentionProblem &p, unsigned *err, cudaStream_t stre
     a.R = R;
     a.n_qblk = (p.S + kTiles * R - 1) / (kTiles * R);
     a.causal = p.causal;
-    a.num_items = p.B * p.Hkv * a.n_qblk;
+    a.kv_splits = (BF && p.kv_splits > 1 && p.part_o && p.part_lse) ? p.kv_splits : 1;  // the cached variant only
+    a.part_o = p.part_o;
+    a.part_lse = p.part_lse;
+    a.num_items = p.B * p.Hkv * a.n_qblk * a.kv_splits;
     a.scale_log2 = 1.4426950408889634f / sqrtf((float)D);
     a.kv_seq = p.kv_seq;
     a.kv_start = p.kv_start;
@@ -390,9 +471,18 @@ cudaError_t run_attn(const AttentionProblem &p, unsigned *err, cudaStream_t stre
     auto kern = attn_kernel<D, BF>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC);
     if (e != cudaSuccess) return e;
-    LaunchCfg lc(dim3(a.num_items), dim3(kThreads), L::ALLOC, stream, p.pdl != 0);
-    e = cudaLaunchKernelEx(&lc.cfg, kern, tq, tk, tv, a);
-    if (e != cudaSuccess) return e;
+    {
+        LaunchCfg lc(dim3(a.num_items), dim3(kThreads), L::ALLOC, stream, p.pdl != 0);
+        e = cudaLaunchKernelEx(&lc.cfg, kern, tq, tk, tv, a);
+        if (e != cudaSuccess) return e;
+    }
+    if (a.kv_splits > 1) {  // merge the key splits, as the attention kernel's programmatic dependent
+        const int rows = p.B * p.S * p.Hq;
+        const long long threads = (long long)rows * (D / 8);
+        LaunchCfg lc(dim3((unsigned)((threads + 255) / 256)), dim3(256), 0, stream, true);
+        e = cudaLaunchKernelEx(&lc.cfg, combine_kernel<D>, a, rows);
+        if (e != cudaSuccess) return e;
+    }
     return cudaGetLastError();
 }
 

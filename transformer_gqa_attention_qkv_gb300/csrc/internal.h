@@ -90,6 +90,12 @@ struct AttentionProblem {
                            // scaled scores, at lse[(b*Hq + head)*lse_ld + t]: P = 2^(s*log2(e)/sqrt(d) - lse)
     int lse_ld;
     int pdl = 0;           // launch as the programmatic dependent of the previous kernel
+    // cached variant (bf16_qkv, kv_start): split each query block's keys into kv_splits
+    // ranges, partials in part_o [kv_splits][B, S, Hq*d] binary16 and part_lse
+    // [kv_splits][B*Hq, S] fp32, merged by a second kernel (1 or NULL buffers: no split)
+    int kv_splits = 1;
+    uint16_t *part_o = nullptr;
+    float *part_lse = nullptr;
 };
 cudaError_t launch_attention(const AttentionProblem &p, unsigned *err, int num_sms, cudaStream_t stream);
 // Backward of the attention (head_dim 64 / 128, Hq/Hkv <= 32).  q, k, v, dO
