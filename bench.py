@@ -408,18 +408,20 @@ def run_ours(args, world, rank, local):
                                dt_["cache_len"], dc.lmax, dout, dws, stream)
 
     def time_it(fn):
+        """fn may return the launches of the entry points it called before its
+        last one (the last one's count is read after it)."""
         nonlocal launches
         ts = []
         for i in range(args.warmup + args.steps):
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             flush.zero_()
             e0.record(stream)
-            fn()
+            earlier = fn() or 0
             e1.record(stream)
             torch.cuda.synchronize()
             if i >= args.warmup:
                 ts.append(e0.elapsed_time(e1))
-                launches += gq.gqa_last_launch_count()
+                launches += earlier + gq.gqa_last_launch_count()
         return statistics.mean(ts)
 
     d8ms = reduce_max(time_it(dec8), world, dev)
@@ -552,7 +554,30 @@ def run_ours(args, world, rank, local):
         bms = reduce_max(time_it(bwd_step), world, dev)
         # algorithmic: each projection twice (input and weight gradients), attention 2.5x its forward
         bflops = 2 * (fl["qkv"] + fl["oproj"]) + 5 * fl["attn"] // 2
-        del bdW, bdWo, bws
+        # the training pair: forward keeping the backward's inputs, backward from them
+        bout = torch.empty_like(bt["x"])
+
+        def fwd_train():
+            gq.gqa_attn_forward_train(bt["x"], bt["Wqkv"], bt["Wo"], bt["q_norm_w"], bt["k_norm_w"], cfg.rope_theta,
+                                      cfg.eps, cfg.B, cfg.S, cfg.hidden, cfg.Hq, cfg.Hkv, d_, cfg.causal, bout, bws,
+                                      stream)
+
+        def bwd_saved():
+            gq.gqa_attn_backward_saved(bt["x"], bt["Wqkv"], bt["Wo"], bt["q_norm_w"], bt["k_norm_w"],
+                                       cfg.rope_theta, cfg.eps, cfg.B, cfg.S, cfg.hidden, cfg.Hq, cfg.Hkv, d_,
+                                       cfg.causal, dout, bdx, bdW, bdWo, bqn, bkn, bws, stream)
+
+        fwd_train()
+        sms_ = reduce_max(time_it(bwd_saved), world, dev)  # the saved inputs are read, not changed
+
+        def train_step():
+            fwd_train()
+            n = gq.gqa_last_launch_count()
+            bwd_saved()
+            return n
+
+        tms = reduce_max(time_it(train_step), world, dev)
+        del bdW, bdWo, bws, bout
         # the attention backward alone (forward attention recomputed for O and lse, then D, dK/dV, dQ)
         aq = torch.randn((cfg.B, cfg.Hq, cfg.S, d_), generator=gen, device=dev).to(torch.float16)
         ak = torch.randn((cfg.B, cfg.Hkv, cfg.S, d_), generator=gen, device=dev).to(torch.float16)
@@ -569,6 +594,14 @@ def run_ours(args, world, rank, local):
                "ms_per_step": round(bms, 4), "frac_of_peak": round(bflops / (bms * 1e-3) / 1e12 / peak_tf, 4),
                "flops_per_step": bflops,
                "note": "algorithmic flops exclude the recomputed forward (Q, K, V and the attention) the time includes",
+               "from_saved": {"ms": round(sms_, 4),
+                              "value": round(reduce_sum(bflops, world, dev) / (sms_ * 1e-3) / 1e12, 1),
+                              "frac_of_peak": round(bflops / (sms_ * 1e-3) / 1e12 / peak_tf, 4),
+                              "note": "gqa_attn_backward_saved after gqa_attn_forward_train: nothing recomputed"},
+               "train_step": {"ms": round(tms, 4),
+                              "value": round(reduce_sum(bflops + fl["total"], world, dev) / (tms * 1e-3) / 1e12, 1),
+                              "frac_of_peak": round((bflops + fl["total"]) / (tms * 1e-3) / 1e12 / peak_tf, 4),
+                              "note": "gqa_attn_forward_train + gqa_attn_backward_saved, forward and backward flops"},
                "attention_backward": {"ms": round(abms, 4),
                                       "tflops": round(2.5 * fl["attn"] / (abms * 1e-3) / 1e12, 1),
                                       "frac_of_peak": round(2.5 * fl["attn"] / (abms * 1e-3) / 1e12 / peak_tf, 4),

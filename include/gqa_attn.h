@@ -396,6 +396,31 @@ int gqa_attn_backward(const gqa_bf16 *x, const gqa_bf16 *Wqkv, const gqa_bf16 *W
                       float *dq_norm_w, float *dk_norm_w,
                       void *workspace, size_t workspace_bytes, void *stream);
 
+/* Training pair.  gqa_attn_forward_train is the layer forward of
+ * gqa_attn_forward_ex (same arguments, same out bit for bit) that also keeps,
+ * in `workspace` (gqa_attn_backward_workspace_size bytes, 256-byte aligned),
+ * what the backward needs: Q, K, V (binary16, head-major), the pre-norm Q and
+ * K rows (fp32, with QK-norm), the attention output and its log2-sum-exp.
+ * gqa_attn_backward_saved then computes the gradients of gqa_attn_backward
+ * (same arguments, same results bit for bit) from that workspace instead of
+ * recomputing the QKV projection and the forward attention.  Between the two
+ * calls the workspace must not be changed, and x, the weights, the norm
+ * weights, rope_theta, eps, sizes and causal must be the same; nothing checks
+ * this.  head_dim 64 or 128, Hq/Hkv a power of two up to 32 (as for
+ * gqa_attn_backward). */
+int gqa_attn_forward_train(const gqa_bf16 *x, const gqa_bf16 *Wqkv, const gqa_bf16 *Wo,
+                           const gqa_bf16 *q_norm_w, const gqa_bf16 *k_norm_w,
+                           float rope_theta, float eps,
+                           int B, int S, int hidden, int Hq, int Hkv, int head_dim, int causal,
+                           gqa_bf16 *out, void *workspace, size_t workspace_bytes, void *stream);
+int gqa_attn_backward_saved(const gqa_bf16 *x, const gqa_bf16 *Wqkv, const gqa_bf16 *Wo,
+                            const gqa_bf16 *q_norm_w, const gqa_bf16 *k_norm_w,
+                            float rope_theta, float eps,
+                            int B, int S, int hidden, int Hq, int Hkv, int head_dim, int causal,
+                            const gqa_bf16 *dout, gqa_bf16 *dx, float *dWqkv, float *dWo,
+                            float *dq_norm_w, float *dk_norm_w,
+                            void *workspace, size_t workspace_bytes, void *stream);
+
 /* Stage alone: the attention backward.  q [B, Hq, S, head_dim], k and v
  * [B, Hkv, S, head_dim], dO [B, Hq, S, head_dim] (all binary16, head-major);
  * writes dq [B, Hq, S, head_dim] and dk, dv [B, Hkv, S, head_dim] in fp32

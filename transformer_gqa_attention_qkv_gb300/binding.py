@@ -36,6 +36,7 @@ EXPORTS = (
     "gqa_decode_qkv_rd", "gqa_attn_decode_fp8", "gqa_decode_qkv_fp8", "gqa_decode_attention_fp8",
     "gqa_attn_backward_workspace_size", "gqa_attn_backward", "gqa_attention_backward_workspace_size",
     "gqa_attention_backward", "gqa_attn_forward_host_workspace_size", "gqa_attn_forward_host",
+    "gqa_attn_forward_train", "gqa_attn_backward_saved",
 )
 
 
@@ -98,6 +99,8 @@ def lib():
     sig["gqa_decode_attention_fp8"] = (_I, [_P] * 3 + [_F, _F, _P] + [_I] * 5 + [_P, _P, _Z, _P])
     sig["gqa_attn_backward_workspace_size"] = (_Z, [_I] * 6)
     sig["gqa_attn_backward"] = (_I, [_P] * 5 + [_F, _F] + [_I] * 7 + [_P] * 6 + [_P, _Z, _P])
+    sig["gqa_attn_backward_saved"] = sig["gqa_attn_backward"]
+    sig["gqa_attn_forward_train"] = (_I, [_P] * 5 + [_F, _F] + [_I] * 7 + [_P, _P, _Z, _P])
     sig["gqa_attention_backward_workspace_size"] = (_Z, [_I] * 4)
     sig["gqa_attention_backward"] = (_I, [_P] * 4 + [_I] * 6 + [_P] * 3 + [_P, _Z, _P])
     for name, (res, args) in sig.items():
@@ -418,6 +421,27 @@ def _f32(t):
 
 def gqa_attn_backward_workspace_size(B, S, hidden, Hq, Hkv, head_dim) -> int:
     return int(lib().gqa_attn_backward_workspace_size(B, S, hidden, Hq, Hkv, head_dim))
+
+
+def gqa_attn_forward_train(x, Wqkv, Wo, q_norm_w, k_norm_w, rope_theta, eps, B, S, hidden, Hq, Hkv, head_dim,
+                           causal, out, workspace, stream=None):
+    """The forward, keeping in `workspace` (gqa_attn_backward_workspace_size bytes) what
+    gqa_attn_backward_saved needs."""
+    _check(lib().gqa_attn_forward_train(_bf16(x), _bf16(Wqkv), _bf16(Wo), _bf16(q_norm_w), _bf16(k_norm_w),
+                                        rope_theta, eps, B, S, hidden, Hq, Hkv, head_dim, int(causal), _bf16(out),
+                                        _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                        _stream(stream)))
+    return out
+
+
+def gqa_attn_backward_saved(x, Wqkv, Wo, q_norm_w, k_norm_w, rope_theta, eps, B, S, hidden, Hq, Hkv, head_dim,
+                            causal, dout, dx, dWqkv, dWo, dq_norm_w, dk_norm_w, workspace, stream=None):
+    """gqa_attn_backward from the workspace gqa_attn_forward_train filled (nothing recomputed)."""
+    _check(lib().gqa_attn_backward_saved(_bf16(x), _bf16(Wqkv), _bf16(Wo), _bf16(q_norm_w), _bf16(k_norm_w),
+                                         rope_theta, eps, B, S, hidden, Hq, Hkv, head_dim, int(causal), _bf16(dout),
+                                         _bf16(dx), _f32(dWqkv), _f32(dWo), _f32(dq_norm_w), _f32(dk_norm_w),
+                                         _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                         _stream(stream)))
 
 
 def gqa_attn_backward(x, Wqkv, Wo, q_norm_w, k_norm_w, rope_theta, eps, B, S, hidden, Hq, Hkv, head_dim, causal,

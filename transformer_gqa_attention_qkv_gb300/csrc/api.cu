@@ -626,20 +626,21 @@ static int check_backward(int B, int S, int hidden, int Hq, int Hkv, int d, cons
     return GQA_OK;
 }
 
-// The attention backward from q, k, v (forward recomputed for o and lse).
+// The attention backward from q, k, v: the forward attention (o and lse) is
+// recomputed into ws, or, with saved, already there (gqa_attn_forward_train).
 static int run_attention_bwd(DeviceState &st, const uint16_t *q, const uint16_t *k, const uint16_t *v,
                              const uint16_t *dO, int B, int S, int Hq, int Hkv, int d, int causal, float *dq,
-                             float *dk, float *dv, uint8_t *ws, cudaStream_t s)
+                             float *dk, float *dv, uint8_t *ws, cudaStream_t s, bool saved = false)
 {
     const AttnBwdLayout L = attn_bwd_layout(B, S, Hq, d);
     gqa_bf16 *o = (gqa_bf16 *)(ws + L.o);
     float *lse = (float *)(ws + L.lse), *dsum = (float *)(ws + L.dsum);
-    int rc = run_attention(st, q, k, v, B, S, Hq, Hkv, d, causal, o, s, 0, nullptr, 0, lse, L.ld);
+    int rc = saved ? GQA_OK : run_attention(st, q, k, v, B, S, Hq, Hkv, d, causal, o, s, 0, nullptr, 0, lse, L.ld);
     if (rc) return rc;
     AttnBwdProblem p{q, k, v, o, dO, lse, dsum, L.ld, dq, dk, dv, B, S, Hq, Hkv, d, causal ? 1 : 0};
     cudaError_t ce = launch_attention_backward(p, st.err, s);
     if (ce != cudaSuccess) return cuda_fail(ce, "attention backward launch");
-    g_launches += 3;
+    g_launches += 3;  // D, dK/dV, dQ
     return GQA_OK;
 }
 
@@ -709,11 +710,13 @@ size_t gqa_attn_backward_workspace_size(int B, int S, int hidden, int Hq, int Hk
     return layer_bwd_layout(B, S, Hq, Hkv, head_dim).total;
 }
 
-int gqa_attn_backward(const gqa_bf16 *x, const gqa_bf16 *Wqkv, const gqa_bf16 *Wo, const gqa_bf16 *q_norm_w,
-                      const gqa_bf16 *k_norm_w, float rope_theta, float eps, int B, int S, int hidden, int Hq,
-                      int Hkv, int head_dim, int causal, const gqa_bf16 *dout, gqa_bf16 *dx, float *dWqkv,
-                      float *dWo, float *dq_norm_w, float *dk_norm_w, void *workspace, size_t workspace_bytes,
-                      void *stream)
+// The layer backward; saved: the forward's Q, K, V, pre-norm rows, O and lse
+// are already in the workspace (gqa_attn_forward_train), so nothing is recomputed.
+static int layer_backward(const gqa_bf16 *x, const gqa_bf16 *Wqkv, const gqa_bf16 *Wo, const gqa_bf16 *q_norm_w,
+                          const gqa_bf16 *k_norm_w, float rope_theta, float eps, int B, int S, int hidden, int Hq,
+                          int Hkv, int head_dim, int causal, const gqa_bf16 *dout, gqa_bf16 *dx, float *dWqkv,
+                          float *dWo, float *dq_norm_w, float *dk_norm_w, void *workspace, size_t workspace_bytes,
+                          void *stream, bool saved)
 {
     g_launches = 0;
     int rc = check_backward(B, S, hidden, Hq, Hkv, head_dim, q_norm_w, k_norm_w);
@@ -746,8 +749,8 @@ int gqa_attn_backward(const gqa_bf16 *x, const gqa_bf16 *Wqkv, const gqa_bf16 *W
     const gqa_bf16 *o = (const gqa_bf16 *)(aws + attn_bwd_layout(B, S, Hq, d).o);
     cudaStream_t s = (cudaStream_t)stream;
     // 1. the forward's Q, K, V (binary16) and pre-norm rows
-    if ((rc = run_qkv(*st, x, Wqkv, q_norm_w, k_norm_w, rope_theta, eps, d, B, S, hidden, Hq, Hkv, d, nullptr, S, S,
-                      S, 1, 1, q, k, v, s, 0, 1.0f, 1.0f, pre)))
+    if (!saved && (rc = run_qkv(*st, x, Wqkv, q_norm_w, k_norm_w, rope_theta, eps, d, B, S, hidden, Hq, Hkv, d, nullptr,
+                                S, S, S, 1, 1, q, k, v, s, 0, 1.0f, 1.0f, pre)))
         return rc;
     // 2. dO = dout Wo, head-major binary16
     {
@@ -758,8 +761,8 @@ int gqa_attn_backward(const gqa_bf16 *x, const gqa_bf16 *Wqkv, const gqa_bf16 *W
         if (ce != cudaSuccess) return cuda_fail(ce, "dO = dout Wo launch");
         ++g_launches;
     }
-    // 3. attention backward (forward recomputed for o and lse)
-    if ((rc = run_attention_bwd(*st, q, k, v, dO, B, S, Hq, Hkv, d, causal, dq, dk, dv, aws, s))) return rc;
+    // 3. attention backward (forward recomputed for o and lse unless saved)
+    if ((rc = run_attention_bwd(*st, q, k, v, dO, B, S, Hq, Hkv, d, causal, dq, dk, dv, aws, s, saved))) return rc;
     // 4. inverse RoPE and the QK-norm gradient -> dqkv
     {
         const float2 *rope = nullptr;
@@ -803,6 +806,67 @@ int gqa_attn_backward(const gqa_bf16 *x, const gqa_bf16 *Wqkv, const gqa_bf16 *W
         ++g_launches;
     }
     return GQA_OK;
+}
+
+int gqa_attn_backward(const gqa_bf16 *x, const gqa_bf16 *Wqkv, const gqa_bf16 *Wo, const gqa_bf16 *q_norm_w,
+                      const gqa_bf16 *k_norm_w, float rope_theta, float eps, int B, int S, int hidden, int Hq,
+                      int Hkv, int head_dim, int causal, const gqa_bf16 *dout, gqa_bf16 *dx, float *dWqkv,
+                      float *dWo, float *dq_norm_w, float *dk_norm_w, void *workspace, size_t workspace_bytes,
+                      void *stream)
+{
+    return layer_backward(x, Wqkv, Wo, q_norm_w, k_norm_w, rope_theta, eps, B, S, hidden, Hq, Hkv, head_dim, causal,
+                          dout, dx, dWqkv, dWo, dq_norm_w, dk_norm_w, workspace, workspace_bytes, stream, false);
+}
+
+int gqa_attn_backward_saved(const gqa_bf16 *x, const gqa_bf16 *Wqkv, const gqa_bf16 *Wo, const gqa_bf16 *q_norm_w,
+                            const gqa_bf16 *k_norm_w, float rope_theta, float eps, int B, int S, int hidden, int Hq,
+                            int Hkv, int head_dim, int causal, const gqa_bf16 *dout, gqa_bf16 *dx, float *dWqkv,
+                            float *dWo, float *dq_norm_w, float *dk_norm_w, void *workspace, size_t workspace_bytes,
+                            void *stream)
+{
+    return layer_backward(x, Wqkv, Wo, q_norm_w, k_norm_w, rope_theta, eps, B, S, hidden, Hq, Hkv, head_dim, causal,
+                          dout, dx, dWqkv, dWo, dq_norm_w, dk_norm_w, workspace, workspace_bytes, stream, true);
+}
+
+int gqa_attn_forward_train(const gqa_bf16 *x, const gqa_bf16 *Wqkv, const gqa_bf16 *Wo, const gqa_bf16 *q_norm_w,
+                           const gqa_bf16 *k_norm_w, float rope_theta, float eps, int B, int S, int hidden, int Hq,
+                           int Hkv, int head_dim, int causal, gqa_bf16 *out, void *workspace, size_t workspace_bytes,
+                           void *stream)
+{
+    g_launches = 0;
+    int rc = check_backward(B, S, hidden, Hq, Hkv, head_dim, q_norm_w, k_norm_w);
+    if (rc) return rc;
+    if (!x || !Wqkv || !Wo || !out) return fail(GQA_ERR_ARG, "null tensor pointer");
+    if (!aligned16(x) || !aligned16(Wqkv) || !aligned16(Wo) || !aligned16(out))
+        return fail(GQA_ERR_ARG, "tensor pointers must be 16-byte aligned");
+    if (!(rope_theta > 0.0f) || !(eps >= 0.0f)) return fail(GQA_ERR_ARG, "rope_theta must be > 0 and eps >= 0");
+    const size_t nx = (size_t)B * S * hidden * 2;
+    const size_t nw = (size_t)(Hq + 2 * Hkv) * head_dim * hidden * 2, no = (size_t)hidden * Hq * head_dim * 2;
+    if (overlap(out, nx, x, nx) || overlap(out, nx, Wqkv, nw) || overlap(out, nx, Wo, no))
+        return fail(GQA_ERR_ARG, "out must not overlap x or the weights");
+    const LayerBwdLayout L = layer_bwd_layout(B, S, Hq, Hkv, head_dim);
+    if (!workspace || workspace_bytes < L.total)
+        return fail(GQA_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", L.total,
+                    workspace ? workspace_bytes : (size_t)0);
+    if (((uintptr_t)workspace & 255u) != 0) return fail(GQA_ERR_ARG, "workspace must be 256-byte aligned");
+    if (overlap(workspace, L.total, out, nx) || overlap(workspace, L.total, x, nx))
+        return fail(GQA_ERR_ARG, "workspace must not overlap the arguments");
+    DeviceState *st;
+    if ((rc = device_state(&st))) return rc;
+    uint8_t *ws = (uint8_t *)workspace;
+    const int d = head_dim;
+    uint16_t *q = (uint16_t *)(ws + L.q), *k = (uint16_t *)(ws + L.k), *v = (uint16_t *)(ws + L.v);
+    float *pre = q_norm_w ? (float *)(ws + L.pre) : nullptr;
+    const AttnBwdLayout A = attn_bwd_layout(B, S, Hq, d);
+    gqa_bf16 *o = (gqa_bf16 *)(ws + L.attn + A.o);
+    float *lse = (float *)(ws + L.attn + A.lse);
+    cudaStream_t s = (cudaStream_t)stream;
+    // the backward's inputs, written where gqa_attn_backward_saved reads them
+    if ((rc = run_qkv(*st, x, Wqkv, q_norm_w, k_norm_w, rope_theta, eps, d, B, S, hidden, Hq, Hkv, d, nullptr, S, S, S,
+                      1, 1, q, k, v, s, 0, 1.0f, 1.0f, pre)))
+        return rc;
+    if ((rc = run_attention(*st, q, k, v, B, S, Hq, Hkv, d, causal, o, s, 0, nullptr, 0, lse, A.ld, 1))) return rc;
+    return run_oproj(*st, o, Wo, x, B * S, hidden, Hq * d, out, s, 1);
 }
 
 // ------------------------------------------------------------------ decode
