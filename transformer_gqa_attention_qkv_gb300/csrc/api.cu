@@ -87,7 +87,8 @@ struct RopeTable {
     double theta;
     int d;
     int rows;
-    float2 *dev;
+    float2 *dev;    // [rows][d/2]: position-major (a warp reads one position's pairs)
+    float2 *dev_t;  // [d/2][rows]: pair-major (a warp reads one pair at 32 consecutive positions)
 };
 
 struct DeviceState {
@@ -132,28 +133,40 @@ static int device_state(DeviceState **out)
 // cos/sin(pos * theta^(-2i/d)) for pos < rows, i < d/2 (d: the rotary width), computed in double on
 // the host and stored as fp32 (cos, sin) pairs.  Angles reach ~1.6e4 rad, where
 // an fp32 angle would already be off by ~1e-3 rad.
-static int rope_table(DeviceState &st, double theta, int d, int rows, const float2 **out)
+// The (cos, sin) table of RoPE for (theta, width d) and at least `rows`
+// positions, in both layouts; *ld (if given) is the pair-major row length.
+static int rope_table(DeviceState &st, double theta, int d, int rows, const float2 **out,
+                      const float2 **out_t = nullptr, int *ld = nullptr)
 {
     for (const RopeTable &t : st.ropes)
         if (t.theta == theta && t.d == d && t.rows >= rows) {
             *out = t.dev;
+            if (out_t) *out_t = t.dev_t;
+            if (ld) *ld = t.rows;
             return GQA_OK;
         }
     int cap = 4096;
     while (cap < rows) cap *= 2;
-    std::vector<float2> host((size_t)cap * (d / 2));
+    const int H = d / 2;
+    std::vector<float2> host((size_t)cap * H), host_t((size_t)cap * H);
     for (int p = 0; p < cap; ++p)
-        for (int i = 0; i < d / 2; ++i) {
+        for (int i = 0; i < H; ++i) {
             const double f = (double)p * pow(theta, -2.0 * i / d);
-            host[(size_t)p * (d / 2) + i] = make_float2((float)cos(f), (float)sin(f));
+            const float2 cs = make_float2((float)cos(f), (float)sin(f));
+            host[(size_t)p * H + i] = cs;
+            host_t[(size_t)i * cap + p] = cs;
         }
-    float2 *dev = nullptr;
+    float2 *dev = nullptr, *dev_t = nullptr;
     cudaError_t e = cudaMalloc(&dev, host.size() * sizeof(float2));
+    if (e == cudaSuccess) e = cudaMalloc(&dev_t, host_t.size() * sizeof(float2));
     if (e != cudaSuccess) return cuda_fail(e, "cudaMalloc(rope table)");
     e = cudaMemcpy(dev, host.data(), host.size() * sizeof(float2), cudaMemcpyHostToDevice);
+    if (e == cudaSuccess) e = cudaMemcpy(dev_t, host_t.data(), host_t.size() * sizeof(float2), cudaMemcpyHostToDevice);
     if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpy(rope table)");
-    st.ropes.push_back({theta, d, cap, dev});
+    st.ropes.push_back({theta, d, cap, dev, dev_t});
     *out = dev;
+    if (out_t) *out_t = dev_t;
+    if (ld) *ld = cap;
     return GQA_OK;
 }
 
@@ -229,12 +242,13 @@ static int run_qkv(DeviceState &st, const gqa_bf16 *x, const gqa_bf16 *Wqkv, con
                    uint16_t *v_out, cudaStream_t stream, int kv_fp8 = 0, float k_scale = 1.0f, float v_scale = 1.0f,
                    float *pre_out = nullptr, int rows = -1, int m0 = 0)
 {
-    const float2 *rope = nullptr;
+    const float2 *rope = nullptr, *rope_t = nullptr;
+    int rope_ld = 0;
     if (rd > 0) {
         int rc;
         {
             std::lock_guard<std::mutex> lk(g_mu);
-            rc = rope_table(st, (double)theta, rd, rope_rows, &rope);
+            rc = rope_table(st, (double)theta, rd, rope_rows, &rope, &rope_t, &rope_ld);
         }
         if (rc) return rc;
     }
@@ -253,7 +267,8 @@ static int run_qkv(DeviceState &st, const gqa_bf16 *x, const gqa_bf16 *Wqkv, con
     e.k_norm_w = kn;
     e.eps = eps;
     e.rd = rd;
-    e.rope = rope;
+    e.rope = rope_t;
+    e.rope_ld = rope_ld;
     e.rope_rows = rope_rows;
     e.q_f16 = q_f16;     // binary16 unless Q meets a bf16 cache in the same MMA
     e.kv_f16 = kv_f16;   // prefill: binary16 workspace; cached paths: the bf16 cache

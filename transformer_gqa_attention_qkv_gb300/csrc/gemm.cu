@@ -197,35 +197,34 @@ __host__ __device__ constexpr int chunk_width(int n)
 
 // Normalised (x * rinv * w) head row of a Q or K head, rotated on its first
 // RD features (rotate-half pairs (i, i + RD/2), (cos, sin) of angle
-// pos * theta^(-2i/RD) from cs[i]) and stored; features [RD, D) are only
+// pos * theta^(-2i/RD) from cs[i * ld], the pair-major table at this row's
+// position: the 32 rows of a warp are consecutive positions of one sequence in
+// a prefill, so each of these loads is one coalesced read) and stored; features [RD, D) are only
 // normalised.  The pairs are taken in chunks of W columns and the rest in
 // chunks of CW, the widest that tile RD/2 and D - RD, so that every TMEM load
 // starts at a multiple of its own width (head offsets are multiples of D).
 template <int D, int RD>
 DEVI void rope_store(uint32_t col, void *dst, float rinv, bool has_norm, const float *w, const float2 *cs,
-                     bool row_ok, OutFmt fmt, bool &clamped)
+                     int ld, bool row_ok, OutFmt fmt, bool &clamped)
 {
     auto nrm = [&](float x, int c) { return has_norm ? x * rinv * w[c] : x * rinv; };
     if constexpr (RD > 0) {
         constexpr int H = RD / 2, W = chunk_width(H);
-        static_assert(H % 2 == 0, "pairs of (cos, sin) are read two at a time");
 #pragma unroll 1
         for (int c = 0; c < H; c += W) {
             uint32_t r1[W], r2[W];
             tmem_ldw<W>(col + c, r1);
             tmem_ldw<W>(col + c + H, r2);
             float y1[W], y2[W];
+            float2 t[W];
 #pragma unroll
-            for (int i = 0; i < W; i += 2) {
-                const float4 t = __ldg(reinterpret_cast<const float4 *>(cs + c + i));  // (cos, sin) x 2
+            for (int i = 0; i < W; ++i) t[i] = __ldg(cs + (size_t)(c + i) * ld);  // (cos, sin)
 #pragma unroll
-                for (int k = 0; k < 2; ++k) {
-                    const float co = k ? t.z : t.x, si = k ? t.w : t.y;
-                    const float x1 = nrm(__uint_as_float(r1[i + k]), c + i + k);
-                    const float x2 = nrm(__uint_as_float(r2[i + k]), c + i + k + H);
-                    y1[i + k] = x1 * co - x2 * si;
-                    y2[i + k] = x2 * co + x1 * si;
-                }
+            for (int i = 0; i < W; ++i) {
+                const float x1 = nrm(__uint_as_float(r1[i]), c + i);
+                const float x2 = nrm(__uint_as_float(r2[i]), c + i + H);
+                y1[i] = x1 * t[i].x - x2 * t[i].y;
+                y2[i] = x2 * t[i].x + x1 * t[i].y;
             }
             if (row_ok) {
                 putw<W>(dst, c, y1, fmt, clamped);
@@ -393,14 +392,15 @@ DEVI void epilogue_qkv(const GemmParams &P, uint32_t tcol, int m, int n0, bool r
         }
         const float *w = s_norm + (kind == 0 ? 0 : 256);
         const int p = row_ok ? pos : 0;
+        const float2 *cs = e.rope ? e.rope + p : nullptr;  // pair 0 at this position
         if (e.rd == D)
-            rope_store<D, D>(col, dst, rinv, has_norm, w, e.rope + (size_t)p * (D / 2), row_ok, fmt, clamped);
+            rope_store<D, D>(col, dst, rinv, has_norm, w, cs, e.rope_ld, row_ok, fmt, clamped);
         else if (e.rd == D / 2)
-            rope_store<D, D / 2>(col, dst, rinv, has_norm, w, e.rope + (size_t)p * (D / 4), row_ok, fmt, clamped);
+            rope_store<D, D / 2>(col, dst, rinv, has_norm, w, cs, e.rope_ld, row_ok, fmt, clamped);
         else if (e.rd == D / 4)
-            rope_store<D, D / 4>(col, dst, rinv, has_norm, w, e.rope + (size_t)p * (D / 8), row_ok, fmt, clamped);
+            rope_store<D, D / 4>(col, dst, rinv, has_norm, w, cs, e.rope_ld, row_ok, fmt, clamped);
         else
-            rope_store<D, 0>(col, dst, rinv, has_norm, w, nullptr, row_ok, fmt, clamped);
+            rope_store<D, 0>(col, dst, rinv, has_norm, w, nullptr, 0, row_ok, fmt, clamped);
     }
     if (clamped) atomicOr(P.err, kErrRange);
 }
@@ -409,28 +409,57 @@ template <int BN>
 DEVI void epilogue_residual(const GemmParams &P, uint32_t tcol, int m, int n0, bool row_ok)
 {
     const ResidualEpilogue &e = P.res;
+    // the residual of the next 32 columns is loaded while this chunk is added
+    auto load = [&](int c, uint4 (&x)[4]) {
+        const int n = n0 + c;
+        const uint4 *src = reinterpret_cast<const uint4 *>(e.resid + (size_t)m * P.N + n);
+#pragma unroll
+        for (int v = 0; v < 4; ++v) x[v] = (row_ok && n + 8 * v < P.N) ? src[v] : make_uint4(0, 0, 0, 0);
+    };
+    uint4 cur[4], nxt[4];
+    load(0, cur);
 #pragma unroll 1
     for (int c = 0; c < BN; c += 32) {
         const int n = n0 + c;
         if (n >= P.N) break;  // uniform across the warp
+        if (c + 32 < BN && n + 32 < P.N) load(c + 32, nxt);
         uint32_t r[32];
         tmem_ld32(tcol + c, r);
-        if (!row_ok) continue;
-        const size_t off = (size_t)m * P.N + n;
-        const uint4 *src = reinterpret_cast<const uint4 *>(e.resid + off);
-        uint4 *dst = reinterpret_cast<uint4 *>(e.out + off);
+        if (row_ok) {
+            uint4 *dst = reinterpret_cast<uint4 *>(e.out + (size_t)m * P.N + n);
 #pragma unroll
-        for (int v = 0; v < 4; ++v) {
-            if (n + 8 * v >= P.N) break;
-            const uint4 x = src[v];
-            const uint32_t xs[4] = {x.x, x.y, x.z, x.w};
-            uint32_t o[4];
+            for (int v = 0; v < 4; ++v) {
+                if (n + 8 * v >= P.N) break;
+                const uint32_t xs[4] = {cur[v].x, cur[v].y, cur[v].z, cur[v].w};
+                uint32_t o[4];
 #pragma unroll
-            for (int k = 0; k < 4; ++k)
-                o[k] = pack_bf16(__uint_as_float(r[8 * v + 2 * k]) + bf16lo(xs[k]),
-                                 __uint_as_float(r[8 * v + 2 * k + 1]) + bf16hi(xs[k]));
-            dst[v] = make_uint4(o[0], o[1], o[2], o[3]);
+                for (int k = 0; k < 4; ++k)
+                    o[k] = pack_bf16(__uint_as_float(r[8 * v + 2 * k]) + bf16lo(xs[k]),
+                                     __uint_as_float(r[8 * v + 2 * k + 1]) + bf16hi(xs[k]));
+                dst[v] = make_uint4(o[0], o[1], o[2], o[3]);
+            }
         }
+#pragma unroll
+        for (int v = 0; v < 4; ++v) cur[v] = nxt[v];
+    }
+}
+
+// Before a tile's accumulator is ready, the residual rows its epilogue adds are
+// requested into L2 (one bulk prefetch per row segment), so the epilogue does
+// not wait on DRAM once per chunk; short-K problems are otherwise bound by it.
+// (The same for the RoPE table rows of the QKV epilogue measured slower.)
+DEVI void prefetch_l2(const void *p, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
+template <int BN, int EPI, int D>
+DEVI void epilogue_prefetch(const GemmParams &P, int m, int n0, bool row_ok)
+{
+    if (!row_ok) return;
+    if constexpr (EPI == EPI_RESIDUAL) {
+        const int cols = min(BN, P.N - n0);  // a multiple of 8: whole 16-byte units
+        if (cols > 0) prefetch_l2(P.res.resid + (size_t)m * P.N + n0, (uint32_t)cols * 2);
     }
 }
 
@@ -613,6 +642,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             int mb, nb;
             tile_coords(tile, P.num_m, P.num_n, P.group_m, mb, nb);
             const int acc = use & 1;
+            epilogue_prefetch<BN, EPI, D>(P, mb * BM + row, nb * BN, mb * BM + row < P.M);
             const bool ready = mbar_wait(tfull + acc, (use >> 1) & 1, err);
             if constexpr (KS > 1) {  // the cluster sums the partials below
                 acc_ready = __all_sync(0xffffffffu, ready);
