@@ -115,6 +115,23 @@ DEVI void tmem_ldw(uint32_t taddr, uint32_t (&r)[W])
     }
 }
 
+// 32 bytes to global memory: one 256-bit store when p is 32-byte aligned
+// (the epilogues write one row per thread, so every store is its own
+// transaction and whole 32-byte sectors halve their count), else two
+// 16-byte stores (the interface guarantees 16-byte alignment only).
+DEVI void st_global32(void *p, const uint32_t (&w)[8])
+{
+    if (((uintptr_t)p & 31u) == 0) {
+        asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(w[0]), "r"(w[1]),
+                     "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+                     : "memory");
+    } else {
+        uint4 *d4 = reinterpret_cast<uint4 *>(p);
+        d4[0] = make_uint4(w[0], w[1], w[2], w[3]);
+        d4[1] = make_uint4(w[4], w[5], w[6], w[7]);
+    }
+}
+
 // W values of one row -> 16-bit storage (bf16, or binary16 clamped to its
 // finite range; *clamped is set when a value had to be clamped).  dst is
 // aligned to 2W bytes (16 at most).
@@ -133,10 +150,15 @@ DEVI void storew(uint16_t *dst, const float *v, bool f16, bool &clamped)
             w[i] = pack_bf16(a, b);
         }
     }
-    if constexpr (W >= 8) {
-        uint4 *d4 = reinterpret_cast<uint4 *>(dst);
+    if constexpr (W >= 16) {
 #pragma unroll
-        for (int i = 0; i < W / 8; ++i) d4[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+        for (int i = 0; i < W / 16; ++i) {
+            const uint32_t w8[8] = {w[8 * i], w[8 * i + 1], w[8 * i + 2], w[8 * i + 3],
+                                    w[8 * i + 4], w[8 * i + 5], w[8 * i + 6], w[8 * i + 7]};
+            st_global32(dst + 16 * i, w8);
+        }
+    } else if constexpr (W == 8) {
+        *reinterpret_cast<uint4 *>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
     } else if constexpr (W == 4) {
         *reinterpret_cast<uint2 *>(dst) = make_uint2(w[0], w[1]);
     } else {
@@ -426,17 +448,26 @@ DEVI void epilogue_residual(const GemmParams &P, uint32_t tcol, int m, int n0, b
         uint32_t r[32];
         tmem_ld32(tcol + c, r);
         if (row_ok) {
-            uint4 *dst = reinterpret_cast<uint4 *>(e.out + (size_t)m * P.N + n);
+            uint16_t *dst = e.out + (size_t)m * P.N + n;
+            uint32_t o[16];
 #pragma unroll
             for (int v = 0; v < 4; ++v) {
-                if (n + 8 * v >= P.N) break;
                 const uint32_t xs[4] = {cur[v].x, cur[v].y, cur[v].z, cur[v].w};
-                uint32_t o[4];
 #pragma unroll
                 for (int k = 0; k < 4; ++k)
-                    o[k] = pack_bf16(__uint_as_float(r[8 * v + 2 * k]) + bf16lo(xs[k]),
-                                     __uint_as_float(r[8 * v + 2 * k + 1]) + bf16hi(xs[k]));
-                dst[v] = make_uint4(o[0], o[1], o[2], o[3]);
+                    o[4 * v + k] = pack_bf16(__uint_as_float(r[8 * v + 2 * k]) + bf16lo(xs[k]),
+                                             __uint_as_float(r[8 * v + 2 * k + 1]) + bf16hi(xs[k]));
+            }
+            if (n + 32 <= P.N) {  // the whole chunk: two 32-byte stores
+                const uint32_t a[8] = {o[0], o[1], o[2], o[3], o[4], o[5], o[6], o[7]};
+                const uint32_t b[8] = {o[8], o[9], o[10], o[11], o[12], o[13], o[14], o[15]};
+                st_global32(dst, a);
+                st_global32(dst + 16, b);
+            } else {
+                uint4 *d4 = reinterpret_cast<uint4 *>(dst);
+#pragma unroll
+                for (int v = 0; v < 4; ++v)
+                    if (n + 8 * v < P.N) d4[v] = make_uint4(o[4 * v], o[4 * v + 1], o[4 * v + 2], o[4 * v + 3]);
             }
         }
 #pragma unroll
