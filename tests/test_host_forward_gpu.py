@@ -73,3 +73,24 @@ def test_host_forward_rejects_device_buffers():
                                         1, 128, 256, 2, 1, 128, 1, gq._host_bf16(torch.empty_like(t["x"])),
                                         gq._ptr(ws), ws.numel(), gq._stream(None))
     assert rc == -1
+
+
+def test_host_forward_from_pageable_memory():
+    """Page-locked memory is only faster: pageable x and out give the same
+    bits (the copies then run synchronously with the host)."""
+    cfg = LayerConfig("h", 2, 2048, 256, 4, 2, 128, True, 1e6)
+    t = make_layer_inputs(cfg, seed=4343)
+    x_host = t["x"].contiguous()
+    assert not x_host.is_pinned()
+    out_host = torch.empty_like(x_host)
+    W, Wo, qn, kn = dev(t["Wqkv"]), dev(t["Wo"]), dev(t["q_norm_w"]), dev(t["k_norm_w"])
+    ws = gq.new_workspace(gq.gqa_attn_forward_host_workspace_size(2, 2048, 256, 4, 2, 128), torch.device(DEV))
+    gq.gqa_attn_forward_host(x_host, W, Wo, qn, kn, 1e6, cfg.eps, 2, 2048, 256, 4, 2, 128, True, out_host, ws)
+    torch.cuda.current_stream().synchronize()
+    x = dev(t["x"])
+    out = torch.empty_like(x)
+    gq.gqa_attn_forward_ex(x, W, Wo, qn, kn, 1e6, cfg.eps, 2, 2048, 256, 4, 2, 128, True, out,
+                           gq.new_workspace(gq.gqa_attn_workspace_size(2, 2048, 256, 4, 2, 128), torch.device(DEV)))
+    torch.cuda.synchronize()
+    assert gq.gqa_check_device_error() == 0
+    assert torch.equal(out_host.view(torch.int16), out.cpu().view(torch.int16))
