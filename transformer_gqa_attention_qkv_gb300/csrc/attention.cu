@@ -44,6 +44,31 @@ namespace gqa {
 
 namespace {
 
+// L2 residency hints for the tensor copies: K and V tiles are read again by
+// every later query block of their KV head, Q and the output stream through
+// once, so K/V are kept (evict_last) and Q goes first (evict_first).
+__device__ __forceinline__ uint64_t l2_policy_keep()
+{
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+__device__ __forceinline__ uint64_t l2_policy_stream()
+{
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+__device__ __forceinline__ void tma_load_3d_hint(void *dst, const CUtensorMap *tm, int x, int y, int z, uint64_t *bar,
+                                                 uint64_t policy)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(smem_u32(dst)),
+        "l"((uint64_t)tm), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar)), "l"(policy)
+        : "memory");
+}
+
 constexpr int kRows = 128;      // MMA M: packed query rows per tile
 constexpr int kKeys = 128;      // keys per K/V tile
 constexpr int kTiles = 2;       // query tiles per CTA
@@ -160,24 +185,25 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp == 0) {
         if (lane == 0) {
+            const uint64_t keep = l2_policy_keep(), stream = l2_policy_stream();
             const uint32_t q_bytes = kTiles * L::NCH * 64 * 2 * P.R * P.G;
             mbar_arrive_expect_tx(q_full, q_bytes);
             for (int i = 0; i < kTiles; ++i)
                 for (int c = 0; c < L::NCH; ++c)
-                    tma_load_3d(smem + L::Q + (i * L::NCH + c) * L::CHUNK, &tmQ, c * 64, t0 + i * P.R,
-                                b * P.Hq + g * P.G, q_full);
+                    tma_load_3d_hint(smem + L::Q + (i * L::NCH + c) * L::CHUNK, &tmQ, c * 64, t0 + i * P.R,
+                                     b * P.Hq + g * P.G, q_full, stream);
             int j = 0;
             for (; j < n_kv; ++j) {
                 const int s = j % ST;
                 if (!mbar_wait(kv_empty + s, ((j / ST) & 1) ^ 1, err)) break;
                 mbar_arrive_expect_tx(k_full + s, L::NCH * L::CHUNK);
                 for (int c = 0; c < L::NCH; ++c)
-                    tma_load_3d(smem + L::K + (s * L::NCH + c) * L::CHUNK, &tmK, c * 64, (kb0 + j) * kKeys,
-                                b * P.Hkv + g, k_full + s);
+                    tma_load_3d_hint(smem + L::K + (s * L::NCH + c) * L::CHUNK, &tmK, c * 64, (kb0 + j) * kKeys,
+                                     b * P.Hkv + g, k_full + s, keep);
                 mbar_arrive_expect_tx(v_full + s, L::NCH * L::CHUNK);
                 for (int c = 0; c < L::NCH; ++c)
-                    tma_load_3d(smem + L::V + (s * L::NCH + c) * L::CHUNK, &tmV, c * 64, (kb0 + j) * kKeys,
-                                b * P.Hkv + g, v_full + s);
+                    tma_load_3d_hint(smem + L::V + (s * L::NCH + c) * L::CHUNK, &tmV, c * 64, (kb0 + j) * kKeys,
+                                     b * P.Hkv + g, v_full + s, keep);
             }
             // every issued copy has landed before the CTA may exit
             mbar_wait(q_full, 0, err);
