@@ -13,7 +13,9 @@
 //   warp 1      MMA issuer: tcgen05.mma 128 x BN x 16 into a TMEM accumulator;
 //               two accumulators so tile i's epilogue overlaps tile i+1's loop
 //   warps 2..5  epilogue: tcgen05.ld (one thread = one output row), fused
-//               math, 16-byte global stores
+//               math, 32-byte global stores where the row address allows;
+//               inputs it reads from memory (residual rows) are requested
+//               into L2 before the accumulator is ready
 //
 // Problems with a single M block (the decode step's projections: 64 rows, a
 // few dozen N tiles) would leave most SMs idle and stream the weights through
