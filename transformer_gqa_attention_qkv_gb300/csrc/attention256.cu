@@ -35,6 +35,27 @@ namespace gqa {
 
 namespace {
 
+// TMEM -> registers, 32 lanes x 32 bits, 64 consecutive columns, then wait;
+// *mx is this thread's maximum over the 64 values (a reducing load).
+__device__ __forceinline__ void tmem_ld64_max(uint32_t taddr, uint32_t (&r)[64], float &mx)
+{
+    asm volatile(
+        "tcgen05.ld.red.sync.aligned.32x32b.x64.max.f32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, %64, [%65];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), 
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), 
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), 
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]), 
+          "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]), 
+          "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]), 
+          "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]), 
+          "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63]), 
+          "=f"(mx)
+        : "r"(taddr)
+        : "memory");
+}
+
+
 constexpr int kD = 256;
 constexpr int kRows = 128;       // MMA M: packed query rows
 constexpr int kKeys = 64;        // keys per K/V tile
@@ -247,21 +268,23 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
             const uint32_t tS = tmem + lane_off + 64 * buf;
             const int u0 = j * kKeys;
+            // the S row and its maximum from one reducing TMEM load
+            static_assert(kKeys == 64, "one 64-column load");
             uint32_t v[kKeys];
-            tmem_ld32(tS, *reinterpret_cast<uint32_t(*)[32]>(v));
-            tmem_ld32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(v + 32));
-            if (u0 + kKeys - 1 > lim) {  // diagonal or ragged tile: mask keys past lim
+            float mx;
+            tmem_ld64_max(tS, v, mx);
+            if (u0 + kKeys - 1 > lim) {  // diagonal or ragged tile: mask keys past lim, max of the rest
 #pragma unroll
                 for (int e = 0; e < kKeys; ++e)
                     if (u0 + e > lim) v[e] = __float_as_uint(-INFINITY);
+                float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+                for (int e = 0; e < kKeys; e += 8)
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        mx4[k] = fmax3(mx4[k], __uint_as_float(v[e + 2 * k]), __uint_as_float(v[e + 2 * k + 1]));
+                mx = fmaxf(fmax3(mx4[0], mx4[1], mx4[2]), mx4[3]);
             }
-            float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll
-            for (int e = 0; e < kKeys; e += 8)
-#pragma unroll
-                for (int k = 0; k < 4; ++k)
-                    mx4[k] = fmax3(mx4[k], __uint_as_float(v[e + 2 * k]), __uint_as_float(v[e + 2 * k + 1]));
-            const float mx = fmaxf(fmax3(mx4[0], mx4[1], mx4[2]), mx4[3]);
             const float m_cand = fmaxf(m_i, mx * sl);
             float m_new = m_i, alpha = 1.0f;
             if (m_cand > m_i + kRescaleThreshold) {
