@@ -8,9 +8,12 @@
 //   u = x r, r = (mean(x^2) + eps)^(-1/2)  (x: the pre-norm row of the forward)
 //   dx_i = r (w_i dn_i - u_i / d * sum_k u_k w_k dn_k),   dw_i += u_i dn_i
 // Without QK-norm dx = dn.  V rows pass unchanged.  One warp per (token,
-// head) row; lane l holds elements l, l + 32, ... (so the rotation pairs are
-// lane-local); the norm-weight gradients are summed per block in shared
-// memory and added to the global [d] vectors once per block.
+// head) row at a time, each warp walking rows with a grid stride (a few
+// blocks per SM); lane l holds elements l, l + 32, ... (so the rotation pairs
+// are lane-local).  The norm-weight gradients are summed in each lane's
+// registers over its rows, then per block in shared memory, and added to the
+// global [d] vectors once per block (a block per row would send every row's
+// terms through the same d global addresses).
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -30,8 +33,12 @@ __global__ void __launch_bounds__(32 * kWarpsPerBlock)
     __syncthreads();
     const int lane = threadIdx.x % 32;
     const int NH = P.Hq + P.Hkv;
-    const long row = (long)blockIdx.x * kWarpsPerBlock + threadIdx.x / 32;  // m * NH + h
-    if (row < (long)P.M * NH) {
+    float accq[E], acck[E];  // this lane's norm-weight gradient terms (q_norm_w, k_norm_w) over its rows
+#pragma unroll
+    for (int e = 0; e < E; ++e) accq[e] = acck[e] = 0.0f;
+    const long rows = (long)P.M * NH;
+    for (long row = (long)blockIdx.x * kWarpsPerBlock + threadIdx.x / 32; row < rows;
+         row += (long)gridDim.x * kWarpsPerBlock) {  // row = m * NH + h
         const long m = row / NH;
         const int h = (int)(row - m * NH);
         const int b = (int)(m / P.S), t = (int)(m - (long)b * P.S);
@@ -74,7 +81,9 @@ __global__ void __launch_bounds__(32 * kWarpsPerBlock)
 #pragma unroll
             for (int e = 0; e < E; ++e) {
                 const float u = xv[e] * r;
-                atomicAdd(&s_dw[isq ? 0 : 1][lane + 32 * e], u * y[e]);
+                const float term = u * y[e];
+                accq[e] += isq ? term : 0.0f;
+                acck[e] += isq ? 0.0f : term;
                 y[e] = r * (wv[e] * y[e] - u * dot * (1.0f / D));
             }
         }
@@ -94,6 +103,11 @@ __global__ void __launch_bounds__(32 * kWarpsPerBlock)
         }
     }
     if (P.pre) {
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+            atomicAdd(&s_dw[0][lane + 32 * e], accq[e]);
+            atomicAdd(&s_dw[1][lane + 32 * e], acck[e]);
+        }
         __syncthreads();
         for (int i = threadIdx.x; i < D; i += blockDim.x) {
             atomicAdd(P.dq_norm_w + i, s_dw[0][i]);
@@ -107,7 +121,11 @@ __global__ void __launch_bounds__(32 * kWarpsPerBlock)
 cudaError_t launch_rope_norm_bwd(const RopeNormBwd &p, cudaStream_t stream)
 {
     const long rows = (long)p.M * (p.Hq + p.Hkv);
-    const unsigned grid = (unsigned)((rows + kWarpsPerBlock - 1) / kWarpsPerBlock);
+    int dev = 0, sms = 148;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const long blocks = (rows + kWarpsPerBlock - 1) / kWarpsPerBlock;
+    const unsigned grid = (unsigned)(blocks < 4L * sms ? blocks : 4L * sms);  // grid-stride over the rest
     if (p.d == 128)
         rope_norm_bwd_kernel<128><<<grid, 32 * kWarpsPerBlock, 0, stream>>>(p);
     else if (p.d == 64)
