@@ -115,3 +115,37 @@ def test_resolve_head_dim():
         resolve_head_dim(1000, 16)
     with pytest.raises(ValueError):
         resolve_head_dim(2560, 32, 0)
+
+
+def test_host_forward_and_training_pair_validate(L):
+    """The host-buffer forward and the training pair reject bad arguments
+    before touching a device (no GPU needed)."""
+    lib = L.lib()
+    P = ctypes.c_void_p
+
+    def host(x=FAKE, out=FAKE * 6, d=128, ws=FAKE * 8, wsb=1 << 34):
+        return lib.gqa_attn_forward_host(P(x), P(FAKE * 2), P(FAKE * 3), P(FAKE * 4), P(FAKE * 5), 1e6, 1e-6,
+                                         1, 16, 64, 4, 2, d, 1, P(out), P(ws), wsb, None)
+    assert host(x=0) == -1
+    assert host(d=160) == -2
+    assert host(out=FAKE) == -1                      # out_host overlaps x_host
+    assert host(wsb=100) == -5
+    assert host(ws=FAKE * 8 + 16) == -1              # workspace not 256-byte aligned
+    assert lib.gqa_attn_forward_host_workspace_size(0, 16, 64, 4, 2, 128) == 0
+    assert (L.gqa_attn_forward_host_workspace_size(1, 16, 64, 4, 2, 128)
+            >= L.gqa_attn_workspace_size(1, 16, 64, 4, 2, 128) + 2 * 16 * 64 * 2)
+
+    def train(d=128, x=FAKE, wsb=1 << 34):
+        return lib.gqa_attn_forward_train(P(x), P(FAKE * 2), P(FAKE * 3), P(FAKE * 4), P(FAKE * 5), 1e6, 1e-6,
+                                          1, 16, 64, 4, 2, d, 1, P(FAKE * 6), P(FAKE * 8), wsb, None)
+    assert train(x=0) == -1
+    assert train(d=256) == -2                        # the backward's head widths: 64 and 128
+    assert train(wsb=100) == -5
+
+    def saved(d=128, dout=FAKE * 7):
+        return lib.gqa_attn_backward_saved(P(FAKE), P(FAKE * 2), P(FAKE * 3), P(FAKE * 4), P(FAKE * 5), 1e6, 1e-6,
+                                           1, 16, 64, 4, 2, d, 1, P(dout), P(FAKE * 9), P(FAKE * 10),
+                                           P(FAKE * 11), P(FAKE * 12), P(FAKE * 13), P(FAKE * 16), 100, None)
+    assert saved(dout=0) == -1
+    assert saved(d=80) == -2
+    assert saved() == -5                             # 100 bytes of workspace
