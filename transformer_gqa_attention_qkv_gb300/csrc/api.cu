@@ -542,6 +542,12 @@ int gqa_attn_forward_host(const gqa_bf16 *x_host, const gqa_bf16 *Wqkv, const gq
     const int M = B * S, R = host_chunk_rows(M), n = (M + R - 1) / R;
     const int qw = Hq * head_dim;
     cudaError_t e;
+    // on any failure past this point the caller's stream still waits for the
+    // copies already queued, so no later work of the caller races them
+    auto bail = [&](int code) {
+        if (cudaEventRecord(pp->join, c) == cudaSuccess) cudaStreamWaitEvent(s, pp->join, 0);
+        return code;
+    };
     // copies of x in, chunk by chunk, on the copy stream (after the caller's prior work)
     if ((e = cudaEventRecord(pp->fork, s)) != cudaSuccess || (e = cudaStreamWaitEvent(c, pp->fork, 0)) != cudaSuccess)
         return cuda_fail(e, "pipeline fork");
@@ -550,29 +556,29 @@ int gqa_attn_forward_host(const gqa_bf16 *x_host, const gqa_bf16 *Wqkv, const gq
         if ((e = cudaMemcpyAsync(x + r0 * hidden, x_host + r0 * hidden, rows * hidden * 2, cudaMemcpyHostToDevice,
                                  c)) != cudaSuccess ||
             (e = cudaEventRecord(pp->in[i], c)) != cudaSuccess)
-            return cuda_fail(e, "host-to-device copy");
+            return bail(cuda_fail(e, "host-to-device copy"));
     }
     // each chunk's projection as soon as its rows have landed
     for (int i = 0; i < n; ++i) {
         const int r0 = i * R, rows = i + 1 < n ? R : M - i * R;
-        if ((e = cudaStreamWaitEvent(s, pp->in[i], 0)) != cudaSuccess) return cuda_fail(e, "pipeline wait");
+        if ((e = cudaStreamWaitEvent(s, pp->in[i], 0)) != cudaSuccess) return bail(cuda_fail(e, "pipeline wait"));
         if ((rc = run_qkv(*st, x + (size_t)r0 * hidden, Wqkv, q_norm_w, k_norm_w, rope_theta, eps, head_dim, B, S,
                           hidden, Hq, Hkv, head_dim, nullptr, S, S, S, 1, 1, q, k, v, s, 0, 1.0f, 1.0f, nullptr,
                           rows, r0)))
-            return rc;
+            return bail(rc);
     }
     if ((rc = run_attention(*st, q, k, v, B, S, Hq, Hkv, head_dim, causal, attn, s, 0, nullptr, 0, nullptr, 0, 1)))
-        return rc;
+        return bail(rc);
     // o_proj chunk by chunk, each copied out while the next one is computed
     for (int i = 0; i < n; ++i) {
         const int r0 = i * R, rows = i + 1 < n ? R : M - i * R;
         if ((rc = run_oproj(*st, attn + (size_t)r0 * qw, Wo, x + (size_t)r0 * hidden, rows, hidden, qw,
                             out + (size_t)r0 * hidden, s, i == 0 ? 1 : 0)))
-            return rc;
+            return bail(rc);
         if ((e = cudaEventRecord(pp->out[i], s)) != cudaSuccess || (e = cudaStreamWaitEvent(c, pp->out[i], 0)) != cudaSuccess ||
             (e = cudaMemcpyAsync(out_host + (size_t)r0 * hidden, out + (size_t)r0 * hidden, (size_t)rows * hidden * 2,
                                  cudaMemcpyDeviceToHost, c)) != cudaSuccess)
-            return cuda_fail(e, "device-to-host copy");
+            return bail(cuda_fail(e, "device-to-host copy"));
     }
     // the caller's stream resumes after the last copy
     if ((e = cudaEventRecord(pp->join, c)) != cudaSuccess || (e = cudaStreamWaitEvent(s, pp->join, 0)) != cudaSuccess)
