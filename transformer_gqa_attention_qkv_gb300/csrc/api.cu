@@ -109,6 +109,7 @@ static int device_state(DeviceState **out)
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
     if (dev < 0 || dev >= 64) return fail(GQA_ERR_CUDA, "device index %d out of range", dev);
+    std::lock_guard<std::mutex> lk(g_mu);  // first calls from several threads initialise once
     DeviceState &st = g_dev[dev];
     if (!st.init) {
         int major = 0, minor = 0;
