@@ -162,8 +162,7 @@ def cpu_oracle_sample(cfg, tokens, seed):
                    sub.B, sub.S, sub.hidden, sub.Hq, sub.Hkv, sub.head_dim, causal=sub.causal, threads=threads)
     dt = time.perf_counter() - t0
     fl = prefill_flops(sub)["total"]
-    desc = (f"fp64 oracle, full layer on the first {tokens} tokens of one sequence of {cfg.name} "
-            f"(all {cfg.Hq} query heads; {fl / 1e9:.1f} GFLOP algorithmic)")
+    desc = f"fp64 oracle, whole layer, first {tokens} tokens of one {cfg.name} sequence ({fl / 1e9:.1f} GFLOP)"
     return fl / dt, dt, threads, desc
 
 
@@ -209,6 +208,10 @@ def reduce_sum(value, world, device=None):
 
 # --------------------------------------------------------------- our arm
 
+def _r(x, n=4):
+    return None if x is None else round(x, n)
+
+
 def run_ours(args, world, rank, local):
     import torch
 
@@ -223,29 +226,85 @@ def run_ours(args, world, rank, local):
     stream = torch.cuda.Stream(device=dev)
     torch.cuda.set_stream(stream)
     peaks, peak_src = load_peaks()
+    peak_tf = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
     cfg = PREFILL_CONFIGS[args.workload]
     fl = prefill_flops(cfg)
-
-    # ---- prefill inputs (generated on the device, seeded; larger than L2)
-    t = make_layer_inputs(cfg, seed=SEEDS[cfg.name] + 7919 * rank, device=str(dev))
-    out = torch.empty_like(t["x"])
-    ws = gq.new_workspace(gq.gqa_attn_workspace_size(cfg.B, cfg.S, cfg.hidden, cfg.Hq, cfg.Hkv,
-                                                     cfg.head_dim), dev)
     flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev)
+    launches = 0
 
-    def fwd():
-        gq.gqa_attn_forward_ex(t["x"], t["Wqkv"], t["Wo"], t["q_norm_w"], t["k_norm_w"], cfg.rope_theta,
-                               cfg.eps, cfg.B, cfg.S, cfg.hidden, cfg.Hq, cfg.Hkv, cfg.head_dim, cfg.causal,
-                               out, ws, stream)
+    def check_dev():
+        if gq.gqa_check_device_error() != 0:
+            raise RuntimeError("device error word set: " + gq.gqa_last_error())
 
+    def time_it(fn, count=True):
+        """Mean CUDA-event time (ms) of fn over args.steps launches after
+        args.warmup, L2 flushed before each.  fn may return the launches of the
+        entry points it called before its last one (the last one's count is
+        read after it)."""
+        nonlocal launches
+        ts = []
+        for i in range(args.warmup + args.steps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            flush.zero_()
+            e0.record(stream)
+            earlier = fn() or 0
+            e1.record(stream)
+            torch.cuda.synchronize()
+            if i >= args.warmup:
+                ts.append(e0.elapsed_time(e1))
+                if count:
+                    launches += earlier + gq.gqa_last_launch_count()
+        return statistics.mean(ts)
+
+    def layer_setup(c, seed_extra=0):
+        t = make_layer_inputs(c, seed=SEEDS[c.name] + seed_extra + 7919 * rank, device=str(dev))
+        out = torch.empty_like(t["x"])
+        ws = gq.new_workspace(gq.gqa_attn_workspace_size(c.B, c.S, c.hidden, c.Hq, c.Hkv, c.head_dim), dev)
+
+        def fwd():
+            gq.gqa_attn_forward_ex(t["x"], t["Wqkv"], t["Wo"], t["q_norm_w"], t["k_norm_w"], c.rope_theta, c.eps,
+                                   c.B, c.S, c.hidden, c.Hq, c.Hkv, c.head_dim, c.causal, out, ws, stream)
+        return t, out, ws, fwd
+
+    def stage_times(c, t, out, ws):
+        """The layer's three kernels launched one by one on the same stream
+        (Q, K, V and attn in the layer's own workspace layout), CUDA events
+        between them: mean ms per stage."""
+        d = c.head_dim
+        n_q, n_kv = c.B * c.S * c.Hq * d * 2, c.B * c.S * c.Hkv * d * 2
+        al = lambda x: (x + 255) // 256 * 256  # noqa: E731
+        q = ws[:n_q].view(torch.float16)
+        k = ws[al(n_q):al(n_q) + n_kv].view(torch.float16)
+        v = ws[al(n_q) + al(n_kv):al(n_q) + al(n_kv) + n_kv].view(torch.float16)
+        o0 = al(n_q) + 2 * al(n_kv)
+        attn = ws[o0:o0 + n_q].view(torch.bfloat16)
+        acc = {"qkv": [], "attn": [], "oproj": []}
+        for i in range(args.warmup + args.steps):
+            e = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+            flush.zero_()
+            e[0].record(stream)
+            gq.gqa_qkv_proj(t["x"], t["Wqkv"], t["q_norm_w"], t["k_norm_w"], c.rope_theta, c.eps, c.B, c.S,
+                            c.hidden, c.Hq, c.Hkv, d, q, k, v, stream)
+            e[1].record(stream)
+            gq.gqa_attention(q, k, v, c.B, c.S, c.Hq, c.Hkv, d, c.causal, attn, stream)
+            e[2].record(stream)
+            gq.gqa_oproj_residual(attn, t["Wo"], t["x"], c.B * c.S, c.hidden, c.Hq * d, out, stream)
+            e[3].record(stream)
+            torch.cuda.synchronize()
+            if i >= args.warmup:
+                for j, s in enumerate(("qkv", "attn", "oproj")):
+                    acc[s].append(e[j].elapsed_time(e[j + 1]))
+        check_dev()
+        return {s: statistics.mean(x) for s, x in acc.items()}
+
+    # ---- headline: the prefill layer forward (inputs generated on the device, seeded; larger than L2)
+    t, out, ws, fwd = layer_setup(cfg)
     for _ in range(args.warmup):
         fwd()
     torch.cuda.synchronize()
-    if gq.gqa_check_device_error() != 0:
-        raise RuntimeError("device error during warm-up: " + gq.gqa_last_error())
-
+    check_dev()
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-    launches = 0
     # clocks are sampled from here to the end of the last timed loop (decode)
     clk = ClockSampler(local).__enter__()
     time.sleep(0.25)
@@ -265,44 +324,23 @@ def run_ours(args, world, rank, local):
     ms = statistics.mean(step_ms)
     ms_job = reduce_max(ms, world, dev)
     value = reduce_sum(fl["total"], world, dev) / (ms_job * 1e-3) / 1e12
+    check_dev()
 
-    # ---- per-kernel durations (same kernels, launched stage by stage, events between)
-    d = cfg.head_dim
-    q = ws[:cfg.B * cfg.Hq * cfg.S * d * 2].view(torch.float16)
-    k = torch.empty((cfg.B, cfg.Hkv, cfg.S, d), dtype=torch.float16, device=dev)
-    v = torch.empty_like(k)
-    attn = torch.empty((cfg.B * cfg.S, cfg.Hq * d), dtype=torch.bfloat16, device=dev)
-    stage_ms = {"qkv": [], "attn": [], "oproj": []}
-    for i in range(args.warmup + args.steps):
-        e = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
-        flush.zero_()
-        e[0].record(stream)
-        gq.gqa_qkv_proj(t["x"], t["Wqkv"], t["q_norm_w"], t["k_norm_w"], cfg.rope_theta, cfg.eps, cfg.B, cfg.S,
-                        cfg.hidden, cfg.Hq, cfg.Hkv, d, q, k, v, stream)
-        e[1].record(stream)
-        gq.gqa_attention(q, k, v, cfg.B, cfg.S, cfg.Hq, cfg.Hkv, d, cfg.causal, attn, stream)
-        e[2].record(stream)
-        gq.gqa_oproj_residual(attn, t["Wo"], t["x"], cfg.B * cfg.S, cfg.hidden, cfg.Hq * d, out, stream)
-        e[3].record(stream)
-        torch.cuda.synchronize()
-        if i >= args.warmup:
-            stage_ms["qkv"].append(e[0].elapsed_time(e[1]))
-            stage_ms["attn"].append(e[1].elapsed_time(e[2]))
-            stage_ms["oproj"].append(e[2].elapsed_time(e[3]))
-    kern = {s: statistics.mean(v_) for s, v_ in stage_ms.items()}
-    dom = max(("qkv", "attn", "oproj"), key=lambda s: kern[s])
-    peak_tf = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    # ---- per-kernel durations of the headline workload (roofline of the dominant kernel)
+    kern = stage_times(cfg, t, out, ws)
+    dom = max(kern, key=lambda s: kern[s])
     dom_src = {"attn": [CSRC + "attention.cu", CSRC + "ptx.cuh"],
                "qkv": [CSRC + "gemm.cu", CSRC + "ptx.cuh"],
                "oproj": [CSRC + "gemm.cu", CSRC + "ptx.cuh"]}[dom]
     achieved = fl[dom] / (kern[dom] * 1e-3) / 1e12
     roofline = {"bound": "tensor", "kernel": dom, "achieved": round(achieved, 1), "peak": peak_tf,
                 "unit": "TFLOP/s", "frac": round(achieved / peak_tf, 4),
-                "peak_source": f"{peak_src} bf16 dense (burst); binary16 and bf16 share the dense rate",
-                "traffic": recorded_traffic(f"{dom}_{cfg.name}", dom_src),
-                "kernel_ms": {s: round(x, 4) for s, x in kern.items()},
-                "kernel_tflops": {s: round(fl[s] / (kern[s] * 1e-3) / 1e12, 1) for s in kern}}
-    del q, k, v, attn
+                "peak_source": f"{peak_src} bf16 dense burst (binary16 shares the rate)",
+                "traffic": recorded_traffic(f"{dom}_{cfg.name}", dom_src)}
+    configs = {cfg.name: {"tflops": round(value, 1), "frac": round(value / world / peak_tf, 4), "ms": _r(ms_job),
+                          "stage_ms": [_r(kern[s]) for s in ("qkv", "attn", "oproj")],
+                          "stage_tflops": [round(fl[s] / (kern[s] * 1e-3) / 1e12, 1)
+                                           for s in ("qkv", "attn", "oproj")]}}
 
     # ---- e2e: through the C-ABI entry point that takes host buffers (pinned x in,
     # out back); its copies run inside the timed region, overlapped with compute
@@ -332,7 +370,24 @@ def run_ours(args, world, rank, local):
     e2e = {"value": round(reduce_sum(fl["total"], world, dev) / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
            "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": x_host.numel() * 2,
            "d2h_bytes_per_step": out_host.numel() * 2}
+    check_dev()
     del t, out, ws, x_host, out_host, hws
+    torch.cuda.empty_cache()
+
+    # ---- the other prefill workloads: whole layer, then its kernels one by one
+    for name in ("qwen3_0p6b", "vaswani_mha", "qwen3_4b"):
+        if name == cfg.name:
+            continue
+        c = PREFILL_CONFIGS[name]
+        cf = prefill_flops(c)
+        ct, cout, cws, cfwd = layer_setup(c)
+        cms = reduce_max(time_it(cfwd), world, dev)
+        ck = stage_times(c, ct, cout, cws)
+        configs[name] = {"tflops": round(reduce_sum(cf["total"], world, dev) / (cms * 1e-3) / 1e12, 1),
+                         "frac": round(cf["total"] / (cms * 1e-3) / 1e12 / peak_tf, 4), "ms": _r(cms),
+                         "stage_ms": [_r(ck[s]) for s in ("qkv", "attn", "oproj")],
+                         "stage_tflops": [round(cf[s] / (ck[s] * 1e-3) / 1e12, 1) for s in ("qkv", "attn", "oproj")]}
+        del ct, cout, cws
     torch.cuda.empty_cache()
 
     # ---- decode step
@@ -348,51 +403,31 @@ def run_ours(args, world, rank, local):
                            dc.eps, dc.B, dc.hidden, dc.Hq, dc.Hkv, dc.head_dim, dt_["k_cache"], dt_["v_cache"],
                            dt_["cache_len"], dc.lmax, dout, dws, stream)
 
-    for _ in range(args.warmup):
-        dec()
-    torch.cuda.synchronize()
-    dev_ = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     barrier(world)
-    for i in range(args.steps):
-        flush.zero_()
-        dev_[i][0].record(stream)
-        dec()
-        launches += gq.gqa_last_launch_count()
-        dev_[i][1].record(stream)
-    torch.cuda.synchronize()
-    barrier(world)
-    dms = reduce_max(statistics.mean(a.elapsed_time(b) for a, b in dev_), world, dev)
+    dms = reduce_max(time_it(dec), world, dev)
     clk.__exit__(None, None, None)
-    # decode attention kernel alone (split + combine), for its roofline
-    qd = torch.zeros((dc.B, dc.Hq, dc.head_dim), dtype=torch.float16, device=dev)
+    # decode attention kernel alone (split + combine), for its roofline: a query
+    # of unit-RMS rows (as QK-norm leaves them), so scores and the running max
+    # move as in the real step
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(SEEDS[dc.name] + 3)
+    qd = torch.randn((dc.B, dc.Hq, dc.head_dim), generator=gen, device=dev).to(torch.float16)
     ad = torch.empty((dc.B, dc.Hq * dc.head_dim), dtype=torch.bfloat16, device=dev)
     kl = (dt_["cache_len"] + 1).to(torch.int32)
     aws = gq.new_workspace(gq.gqa_decode_attention_workspace_size(dc.B, dc.Hq, dc.Hkv, dc.head_dim, dc.lmax),
                            dev)
-    ams = []
-    for i in range(args.warmup + args.steps):
-        a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        flush.zero_()
-        a0.record(stream)
-        gq.gqa_decode_attention(qd, dt_["k_cache"], dt_["v_cache"], kl, dc.B, dc.Hq, dc.Hkv, dc.head_dim,
-                                dc.lmax, ad, aws, stream)
-        a1.record(stream)
-        torch.cuda.synchronize()
-        if i >= args.warmup:
-            ams.append(a0.elapsed_time(a1))
-    ams_ = statistics.mean(ams)
-    hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    ams = time_it(lambda: gq.gqa_decode_attention(qd, dt_["k_cache"], dt_["v_cache"], kl, dc.B, dc.Hq, dc.Hkv,
+                                                  dc.head_dim, dc.lmax, ad, aws, stream), count=False)
     attn_bytes = db["kv_read"] + dc.B * dc.Hq * dc.head_dim * 2 * 2
-    dec_ach = attn_bytes / (ams_ * 1e-3) / 1e9
+    dec_ach = attn_bytes / (ams * 1e-3) / 1e9
     decode = {"workload": dc.name, "value": round(reduce_sum(db["total"], world, dev) / (dms * 1e-3) / 1e9, 1),
-              "unit": "GB/s", "ms_per_step": round(dms, 4), "frac_of_hbm": round(db["total"] / (dms * 1e-3) / 1e9 / hbm, 4),
-              "bytes_per_step": db["total"],
-              "roofline": {"bound": "hbm", "kernel": "decode_attention", "achieved": round(dec_ach, 1),
-                           "peak": hbm, "unit": "GB/s", "frac": round(dec_ach / hbm, 4),
-                           "peak_source": f"{peak_src} copy bandwidth",
-                           "traffic": recorded_traffic("decode_attention_" + dc.name,
-                                                       [CSRC + "decode.cu", CSRC + "ptx.cuh"]),
-                           "kernel_ms": round(ams_, 4)}}
+              "unit": "GB/s", "ms": _r(dms), "frac": round(db["total"] / (dms * 1e-3) / 1e9 / hbm, 4),
+              "bytes": db["total"],
+              "kernel": {"name": "decode_attention", "achieved": round(dec_ach, 1), "frac": round(dec_ach / hbm, 4),
+                         "ms": _r(ams),
+                         "traffic": recorded_traffic("decode_attention_" + dc.name,
+                                                     [CSRC + "decode.cu", CSRC + "ptx.cuh"])}}
+    check_dev()
 
     # ---- the same decode step over E4M3 caches (scale 2^-5: the N(0,1)
     # cache entries land well inside E4M3's range)
@@ -407,135 +442,69 @@ def run_ours(args, world, rank, local):
                                dc.eps, dc.B, dc.hidden, dc.Hq, dc.Hkv, dc.head_dim, kc8, vc8, f8s, f8s,
                                dt_["cache_len"], dc.lmax, dout, dws, stream)
 
-    def time_it(fn):
-        """fn may return the launches of the entry points it called before its
-        last one (the last one's count is read after it)."""
-        nonlocal launches
-        ts = []
-        for i in range(args.warmup + args.steps):
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            flush.zero_()
-            e0.record(stream)
-            earlier = fn() or 0
-            e1.record(stream)
-            torch.cuda.synchronize()
-            if i >= args.warmup:
-                ts.append(e0.elapsed_time(e1))
-                launches += earlier + gq.gqa_last_launch_count()
-        return statistics.mean(ts)
-
     d8ms = reduce_max(time_it(dec8), world, dev)
     a8ms = time_it(lambda: gq.gqa_decode_attention_fp8(qd, kc8, vc8, f8s, f8s, kl, dc.B, dc.Hq, dc.Hkv,
-                                                        dc.head_dim, dc.lmax, ad, aws, stream))
-    a8_bytes = db8["kv_read"] + dc.B * dc.Hq * dc.head_dim * 2 * 2
-    a8_ach = a8_bytes / (a8ms * 1e-3) / 1e9
-    decode_fp8 = {"workload": dc.name + " with E4M3 K/V caches (per-tensor scales)",
-                  "value": round(reduce_sum(db8["total"], world, dev) / (d8ms * 1e-3) / 1e9, 1), "unit": "GB/s",
-                  "ms_per_step": round(d8ms, 4), "frac_of_hbm": round(db8["total"] / (d8ms * 1e-3) / 1e9 / hbm, 4),
-                  "bytes_per_step": db8["total"], "speedup_vs_bf16_cache": round(dms / d8ms, 3),
-                  "roofline": {"bound": "hbm", "kernel": "decode_attention_fp8", "achieved": round(a8_ach, 1),
-                               "peak": hbm, "unit": "GB/s", "frac": round(a8_ach / hbm, 4),
-                               "peak_source": f"{peak_src} copy bandwidth",
-                               "traffic": recorded_traffic("decode_attention_fp8_" + dc.name,
-                                                           [CSRC + "decode.cu", CSRC + "ptx.cuh"]),
-                               "kernel_ms": round(a8ms, 4)}}
-    if gq.gqa_check_device_error() != 0:
-        raise RuntimeError(gq.gqa_last_error())
-    del dt_, dout, dws, kc8, vc8
+                                                        dc.head_dim, dc.lmax, ad, aws, stream), count=False)
+    a8_ach = (db8["kv_read"] + dc.B * dc.Hq * dc.head_dim * 2 * 2) / (a8ms * 1e-3) / 1e9
+    decode_fp8 = {"value": round(reduce_sum(db8["total"], world, dev) / (d8ms * 1e-3) / 1e9, 1), "unit": "GB/s",
+                  "ms": _r(d8ms), "frac": round(db8["total"] / (d8ms * 1e-3) / 1e9 / hbm, 4),
+                  "speedup_vs_bf16": round(dms / d8ms, 3),
+                  "kernel": {"name": "decode_attention_fp8", "achieved": round(a8_ach, 1),
+                             "frac": round(a8_ach / hbm, 4), "ms": _r(a8ms),
+                             "traffic": recorded_traffic("decode_attention_fp8_" + dc.name,
+                                                         [CSRC + "decode.cu", CSRC + "ptx.cuh"])}}
+    check_dev()
+    del dt_, dout, dws, kc8, vc8, aws
+    torch.cuda.empty_cache()
 
+    details = {}
     # ---- chunked prefill: the last 2048 tokens of a 16384-token Qwen3-32B context
-    chunk = None
     if not args.no_chunk:
-        cc = cfg.with_(S=2048)
+        cc = PREFILL_CONFIGS["qwen3_32b"].with_(S=2048)
         p0, Lmax = 14336, 16384
-        ct = make_layer_inputs(cc, seed=SEEDS[cfg.name] + 17 + 7919 * rank, device=str(dev))
-        gen = torch.Generator(device=dev)
-        gen.manual_seed(SEEDS[cfg.name] + 18)
+        ct = make_layer_inputs(cc, seed=SEEDS["qwen3_32b"] + 17 + 7919 * rank, device=str(dev))
+        gen.manual_seed(SEEDS["qwen3_32b"] + 18)
         kc = torch.randn((1, cc.Hkv, Lmax, cc.head_dim), generator=gen, device=dev).to(torch.bfloat16)
         vc = torch.randn((1, cc.Hkv, Lmax, cc.head_dim), generator=gen, device=dev).to(torch.bfloat16)
         cl = torch.full((1,), p0, dtype=torch.int32, device=dev)
         cout = torch.empty_like(ct["x"])
         cws = gq.new_workspace(gq.gqa_attn_prefill_cached_workspace_size(1, cc.S, cc.Hq, cc.head_dim), dev)
-        cf = {"qkv": 2 * cc.S * (cc.Hq + 2 * cc.Hkv) * cc.head_dim * cc.hidden,
-              "attn": 4 * cc.Hq * cc.head_dim * (cc.S * p0 + cc.S * (cc.S + 1) // 2),
-              "oproj": 2 * cc.S * cc.hidden * cc.Hq * cc.head_dim}
-        cf["total"] = sum(cf.values())
+        cf = (2 * cc.S * (cc.Hq + 2 * cc.Hkv) * cc.head_dim * cc.hidden
+              + 4 * cc.Hq * cc.head_dim * (cc.S * p0 + cc.S * (cc.S + 1) // 2)
+              + 2 * cc.S * cc.hidden * cc.Hq * cc.head_dim)
 
         def chunk_step():
             gq.gqa_attn_prefill_cached(ct["x"], ct["Wqkv"], ct["Wo"], ct["q_norm_w"], ct["k_norm_w"], cc.rope_theta,
                                        cc.eps, 1, cc.S, cc.hidden, cc.Hq, cc.Hkv, cc.head_dim, True, kc, vc, cl,
                                        Lmax, cout, cws, stream)
 
-        for _ in range(args.warmup):
-            chunk_step()
-        torch.cuda.synchronize()
-        cev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-               for _ in range(args.steps)]
-        for i in range(args.steps):
-            flush.zero_()
-            cev[i][0].record(stream)
-            chunk_step()
-            launches += gq.gqa_last_launch_count()
-            cev[i][1].record(stream)
-        torch.cuda.synchronize()
-        cms = reduce_max(statistics.mean(a.elapsed_time(b) for a, b in cev), world, dev)
-        chunk = {"workload": "qwen3_32b last 2048-token chunk after 14336 cached (Lmax 16384)",
-                 "value": round(reduce_sum(cf["total"], world, dev) / (cms * 1e-3) / 1e12, 1), "unit": "TFLOP/s",
-                 "ms_per_step": round(cms, 4), "frac_of_peak": round(cf["total"] / (cms * 1e-3) / 1e12 / peak_tf, 4),
-                 "flops_per_step": cf["total"]}
+        cms = reduce_max(time_it(chunk_step), world, dev)
+        details["chunked_prefill"] = {"workload": "qwen3_32b, 2048 new tokens after 14336 cached",
+                                      "tflops": round(reduce_sum(cf, world, dev) / (cms * 1e-3) / 1e12, 1),
+                                      "frac": round(cf / (cms * 1e-3) / 1e12 / peak_tf, 4), "ms": _r(cms)}
+        check_dev()
         del ct, kc, vc, cout, cws
 
     # ---- other head widths: 256 at the Gemma-3 example's width, 80 and 96 at
     # the Qwen3-4B widths (4 x 4096 tokens each): the layer, then its attention alone
-    def width_line(name, desc):
-        wc = PREFILL_CONFIGS[name]
-        wf = prefill_flops(wc)
-        wt = make_layer_inputs(wc, seed=SEEDS[wc.name] + 7919 * rank, device=str(dev))
-        wout = torch.empty_like(wt["x"])
-        wws = gq.new_workspace(gq.gqa_attn_workspace_size(wc.B, wc.S, wc.hidden, wc.Hq, wc.Hkv, wc.head_dim), dev)
-
-        def wide_step():
-            gq.gqa_attn_forward_ex(wt["x"], wt["Wqkv"], wt["Wo"], wt["q_norm_w"], wt["k_norm_w"], wc.rope_theta,
-                                   wc.eps, wc.B, wc.S, wc.hidden, wc.Hq, wc.Hkv, wc.head_dim, wc.causal, wout,
-                                   wws, stream)
-
-        wms = reduce_max(time_it(wide_step), world, dev)
-        n_q = wc.B * wc.S * wc.Hq * wc.head_dim * 2
-        n_kv = wc.B * wc.S * wc.Hkv * wc.head_dim * 2
-        al = lambda x: (x + 255) // 256 * 256  # noqa: E731
-        wq = wws[:n_q].view(torch.float16)
-        wk = wws[al(n_q):al(n_q) + n_kv].view(torch.float16)
-        wv = wws[al(n_q) + al(n_kv):al(n_q) + al(n_kv) + n_kv].view(torch.float16)
-        wa = torch.empty((wc.B * wc.S, wc.Hq * wc.head_dim), dtype=torch.bfloat16, device=dev)
-        wams = time_it(lambda: gq.gqa_attention(wq, wk, wv, wc.B, wc.S, wc.Hq, wc.Hkv, wc.head_dim, wc.causal, wa,
-                                                stream))
-        line = {"workload": desc,
-                "value": round(reduce_sum(wf["total"], world, dev) / (wms * 1e-3) / 1e12, 1), "unit": "TFLOP/s",
-                "ms_per_step": round(wms, 4), "frac_of_peak": round(wf["total"] / (wms * 1e-3) / 1e12 / peak_tf, 4),
-                "roofline": {"bound": "tensor", "kernel": f"attn (head_dim {wc.head_dim})",
-                             "achieved": round(wf["attn"] / (wams * 1e-3) / 1e12, 1), "peak": peak_tf,
-                             "unit": "TFLOP/s", "frac": round(wf["attn"] / (wams * 1e-3) / 1e12 / peak_tf, 4),
-                             "kernel_ms": round(wams, 4)}}
-        if gq.gqa_check_device_error() != 0:
-            raise RuntimeError(gq.gqa_last_error())
-        del wt, wout, wws, wa
-        return line
-
-    wide = wide80 = wide96 = None
     if not args.no_widths:
-        wide = width_line("gemma3_d256", "gemma3_d256: B=4, S=4096, hidden 640, 4 query heads, 1 KV head, head_dim 256")
-        wide80 = width_line("qwen3_4b_d80", "qwen3_4b_d80: B=4, S=4096, hidden 2560, 32/8 heads, head_dim 80 "
-                                            "(= hidden / heads); attention flops counted at d = 80")
-        wide96 = width_line("knob_d96", "knob_d96: B=4, S=4096, hidden 3072, 32/8 heads, head_dim 96 "
-                                        "(= hidden / heads); attention flops counted at d = 96")
+        for name in ("gemma3_d256", "qwen3_4b_d80", "knob_d96"):
+            wc = PREFILL_CONFIGS[name]
+            wf = prefill_flops(wc)
+            wt, wout, wws, wstep = layer_setup(wc)
+            wms = reduce_max(time_it(wstep), world, dev)
+            wk = stage_times(wc, wt, wout, wws)
+            details[name] = {"tflops": round(reduce_sum(wf["total"], world, dev) / (wms * 1e-3) / 1e12, 1),
+                             "frac": round(wf["total"] / (wms * 1e-3) / 1e12 / peak_tf, 4), "ms": _r(wms),
+                             "stage_ms": [_r(wk[s]) for s in ("qkv", "attn", "oproj")],
+                             "attn_frac": round(wf["attn"] / (wk["attn"] * 1e-3) / 1e12 / peak_tf, 4)}
+            del wt, wout, wws
 
-    # ---- backward of the same layer (workload qwen3_32b): gradients of x, Wqkv, Wo and the norm weights
-    bwd = None
+    # ---- backward of the headline layer: gradients of x, Wqkv, Wo and the norm weights
     if not args.no_bwd:
         bt = make_layer_inputs(cfg, seed=SEEDS[cfg.name] + 29 + 7919 * rank, device=str(dev))
-        gen = torch.Generator(device=dev)
         gen.manual_seed(SEEDS[cfg.name] + 31)
-        dout = torch.randn((cfg.B * cfg.S, cfg.hidden), generator=gen, device=dev).to(torch.bfloat16)
+        bdo = torch.randn((cfg.B * cfg.S, cfg.hidden), generator=gen, device=dev).to(torch.bfloat16)
         d_ = cfg.head_dim
         Nq = (cfg.Hq + 2 * cfg.Hkv) * d_
         bdx = torch.empty_like(bt["x"])
@@ -545,30 +514,18 @@ def run_ours(args, world, rank, local):
         bkn = torch.empty(d_, dtype=torch.float32, device=dev)
         bws = gq.new_workspace(gq.gqa_attn_backward_workspace_size(cfg.B, cfg.S, cfg.hidden, cfg.Hq, cfg.Hkv, d_),
                                dev)
+        bout = torch.empty_like(bt["x"])
+        args_ = (bt["x"], bt["Wqkv"], bt["Wo"], bt["q_norm_w"], bt["k_norm_w"], cfg.rope_theta, cfg.eps, cfg.B,
+                 cfg.S, cfg.hidden, cfg.Hq, cfg.Hkv, d_, cfg.causal)
 
         def bwd_step():
-            gq.gqa_attn_backward(bt["x"], bt["Wqkv"], bt["Wo"], bt["q_norm_w"], bt["k_norm_w"], cfg.rope_theta,
-                                 cfg.eps, cfg.B, cfg.S, cfg.hidden, cfg.Hq, cfg.Hkv, d_, cfg.causal, dout, bdx, bdW,
-                                 bdWo, bqn, bkn, bws, stream)
-
-        bms = reduce_max(time_it(bwd_step), world, dev)
-        # algorithmic: each projection twice (input and weight gradients), attention 2.5x its forward
-        bflops = 2 * (fl["qkv"] + fl["oproj"]) + 5 * fl["attn"] // 2
-        # the training pair: forward keeping the backward's inputs, backward from them
-        bout = torch.empty_like(bt["x"])
+            gq.gqa_attn_backward(*args_, bdo, bdx, bdW, bdWo, bqn, bkn, bws, stream)
 
         def fwd_train():
-            gq.gqa_attn_forward_train(bt["x"], bt["Wqkv"], bt["Wo"], bt["q_norm_w"], bt["k_norm_w"], cfg.rope_theta,
-                                      cfg.eps, cfg.B, cfg.S, cfg.hidden, cfg.Hq, cfg.Hkv, d_, cfg.causal, bout, bws,
-                                      stream)
+            gq.gqa_attn_forward_train(*args_, bout, bws, stream)
 
         def bwd_saved():
-            gq.gqa_attn_backward_saved(bt["x"], bt["Wqkv"], bt["Wo"], bt["q_norm_w"], bt["k_norm_w"],
-                                       cfg.rope_theta, cfg.eps, cfg.B, cfg.S, cfg.hidden, cfg.Hq, cfg.Hkv, d_,
-                                       cfg.causal, dout, bdx, bdW, bdWo, bqn, bkn, bws, stream)
-
-        fwd_train()
-        sms_ = reduce_max(time_it(bwd_saved), world, dev)  # the saved inputs are read, not changed
+            gq.gqa_attn_backward_saved(*args_, bdo, bdx, bdW, bdWo, bqn, bkn, bws, stream)
 
         def train_step():
             fwd_train()
@@ -576,40 +533,20 @@ def run_ours(args, world, rank, local):
             bwd_saved()
             return n
 
+        bms = reduce_max(time_it(bwd_step), world, dev)
+        fwd_train()
+        sms_ = reduce_max(time_it(bwd_saved), world, dev)  # the saved inputs are read, not changed
         tms = reduce_max(time_it(train_step), world, dev)
-        del bdW, bdWo, bws, bout
-        # the attention backward alone (forward attention recomputed for O and lse, then D, dK/dV, dQ)
-        aq = torch.randn((cfg.B, cfg.Hq, cfg.S, d_), generator=gen, device=dev).to(torch.float16)
-        ak = torch.randn((cfg.B, cfg.Hkv, cfg.S, d_), generator=gen, device=dev).to(torch.float16)
-        av = torch.randn((cfg.B, cfg.Hkv, cfg.S, d_), generator=gen, device=dev).to(torch.float16)
-        ag = torch.randn((cfg.B, cfg.Hq, cfg.S, d_), generator=gen, device=dev).to(torch.float16)
-        adq = torch.empty((cfg.B, cfg.Hq, cfg.S, d_), dtype=torch.float32, device=dev)
-        adk = torch.empty((cfg.B, cfg.Hkv, cfg.S, d_), dtype=torch.float32, device=dev)
-        adv = torch.empty_like(adk)
-        aws = gq.new_workspace(gq.gqa_attention_backward_workspace_size(cfg.B, cfg.S, cfg.Hq, d_), dev)
-        abms = time_it(lambda: gq.gqa_attention_backward(aq, ak, av, ag, cfg.B, cfg.S, cfg.Hq, cfg.Hkv, d_,
-                                                         cfg.causal, adq, adk, adv, aws, stream))
-        bwd = {"workload": cfg.name + " backward: dx, dWqkv, dWo, dq_norm_w, dk_norm_w from dout",
-               "value": round(reduce_sum(bflops, world, dev) / (bms * 1e-3) / 1e12, 1), "unit": "TFLOP/s",
-               "ms_per_step": round(bms, 4), "frac_of_peak": round(bflops / (bms * 1e-3) / 1e12 / peak_tf, 4),
-               "flops_per_step": bflops,
-               "note": "algorithmic flops exclude the recomputed forward (Q, K, V and the attention) the time includes",
-               "from_saved": {"ms": round(sms_, 4),
-                              "value": round(reduce_sum(bflops, world, dev) / (sms_ * 1e-3) / 1e12, 1),
-                              "frac_of_peak": round(bflops / (sms_ * 1e-3) / 1e12 / peak_tf, 4),
-                              "note": "gqa_attn_backward_saved after gqa_attn_forward_train: nothing recomputed"},
-               "train_step": {"ms": round(tms, 4),
-                              "value": round(reduce_sum(bflops + fl["total"], world, dev) / (tms * 1e-3) / 1e12, 1),
-                              "frac_of_peak": round((bflops + fl["total"]) / (tms * 1e-3) / 1e12 / peak_tf, 4),
-                              "note": "gqa_attn_forward_train + gqa_attn_backward_saved, forward and backward flops"},
-               "attention_backward": {"ms": round(abms, 4),
-                                      "tflops": round(2.5 * fl["attn"] / (abms * 1e-3) / 1e12, 1),
-                                      "frac_of_peak": round(2.5 * fl["attn"] / (abms * 1e-3) / 1e12 / peak_tf, 4),
-                                      "note": "2.5x the forward attention flops over the time of forward recompute "
-                                              "+ D + dK/dV + dQ"}}
-        if gq.gqa_check_device_error() != 0:
-            raise RuntimeError(gq.gqa_last_error())
-        del bt, dout, bdx, aq, ak, av, ag, adq, adk, adv, aws
+        # algorithmic: each projection twice (input and weight gradients), attention 2.5x its forward
+        bflops = 2 * (fl["qkv"] + fl["oproj"]) + 5 * fl["attn"] // 2
+        details["backward"] = {
+            "workload": cfg.name, "tflops": round(reduce_sum(bflops, world, dev) / (bms * 1e-3) / 1e12, 1),
+            "frac": round(bflops / (bms * 1e-3) / 1e12 / peak_tf, 4), "ms": _r(bms),
+            "from_saved_ms": _r(sms_), "from_saved_frac": round(bflops / (sms_ * 1e-3) / 1e12 / peak_tf, 4),
+            "train_step_ms": _r(tms),
+            "train_step_frac": round((bflops + fl["total"]) / (tms * 1e-3) / 1e12 / peak_tf, 4)}
+        check_dev()
+        del bt, bdo, bdx, bdW, bdWo, bws, bout
 
     # ---- CPU baseline (rank 0, N=1 only)
     cpu = None
@@ -626,13 +563,14 @@ def run_ours(args, world, rank, local):
         "config": {"workload": cfg.name, "B": cfg.B, "S": cfg.S, "hidden": cfg.hidden, "Hq": cfg.Hq,
                    "Hkv": cfg.Hkv, "head_dim": cfg.head_dim, "qk_norm": cfg.qk_norm, "rope_theta": cfg.rope_theta,
                    "causal": cfg.causal, "flops_per_step": fl["total"], "parallelism": f"replicas x{world}",
-                   "l2": "flushed between steps (2x L2 buffer written outside the timed events)"},
-        "roofline": roofline, "decode": decode, "decode_fp8": decode_fp8, "chunked_prefill": chunk, "head_dim_256": wide,
-        "head_dim_80": wide80, "head_dim_96": wide96, "backward": bwd, "e2e": e2e, "cpu_baseline": cpu,
-        "gpu_launches": launches, "wall_s": round(wall, 3), "clocks": clk.summary(),
-        "step_ms": [round(x, 4) for x in step_ms],
+                   "l2": "flushed before every timed launch"},
+        "roofline": roofline, "configs": configs, "decode": decode, "decode_fp8": decode_fp8,
+        "e2e": e2e, "cpu_baseline": cpu, "gpu_launches": launches, "clocks": clk.summary(),
     }
     if rank == 0:
+        # the per-workload extras on stderr, the one benchmark line last on stdout
+        print("bench details: " + json.dumps({"step_ms": [round(x, 3) for x in step_ms], "wall_s": round(wall, 3),
+                                              **details}), file=sys.stderr, flush=True)
         print(json.dumps(line), flush=True)
 
 
@@ -656,8 +594,9 @@ def run_reference(args, world, rank):
     line = {"impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * statistics.mean(secs), 1),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": cfg.name, "B": cfg.B, "S": cfg.S, "hidden": cfg.hidden, "Hq": cfg.Hq,
-                       "Hkv": cfg.Hkv, "head_dim": cfg.head_dim, "parallelism": "host cores"},
+            "config": {"workload": f"{cfg.name}, first {args.ref_tokens} tokens of one sequence", "B": 1,
+                       "S": args.ref_tokens, "hidden": cfg.hidden, "Hq": cfg.Hq, "Hkv": cfg.Hkv,
+                       "head_dim": cfg.head_dim, "causal": cfg.causal, "parallelism": "host cores"},
             "cpu_baseline": {"kind": "oracle", "cores": threads, "sample": desc, "value": round(value, 6),
                              "unit": "TFLOP/s"},
             "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}

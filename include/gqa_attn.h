@@ -280,8 +280,16 @@ int gqa_decode_attention(const gqa_f16 *q, const gqa_bf16 *k_cache, const gqa_bf
  *   them (one stream, or events).
  *   Set-up: the first call on a device looks up the array's device address
  *   with that device current; make that first call before any stream capture.
- * Arguments as for gqa_decode_attention; device-side length errors are not
- * reported (those sequences get zero rows). */
+ *   Errors found on the device: a bounded wait that gave up (GQA_ERR_TIMEOUT)
+ *   or a kv_len outside [1, Lmax] (GQA_ERR_ARG; that sequence gets zero rows)
+ *   is recorded in an error word that lives beside the array.  Each call
+ *   clears that word on its stream before its kernels run, so one call's
+ *   timeout never affects a later call; gqa_check_device_error() reads and
+ *   clears it, so check after a call and before the next one is enqueued to
+ *   see that call's errors.  Neither the clearing nor the check allocates.
+ * Arguments, size limits and the statuses of invalid arguments are those of
+ * gqa_decode_attention; gqa_last_launch_count() is 2 after a call that
+ * launched. */
 int gqa_decode_attention_noalloc(const gqa_f16 *q, const gqa_bf16 *k_cache, const gqa_bf16 *v_cache,
                                  const int *kv_len, int B, int Hq, int Hkv, int head_dim, int Lmax,
                                  gqa_bf16 *attn_out, void *stream);
@@ -454,8 +462,11 @@ int gqa_attn_cost(int B, int S, int hidden, int Hq, int Hkv, int head_dim, int c
 const char *gqa_last_error(void);
 
 /* Synchronises the current device, then reads and clears its device error
- * word.  Returns GQA_OK, GQA_ERR_TIMEOUT (a bounded wait gave up),
- * GQA_ERR_ARG (a device-side index check failed) or GQA_ERR_CUDA. */
+ * words: the per-device word of the workspace-taking entry points and the one
+ * of gqa_decode_attention_noalloc.  Returns GQA_OK, GQA_ERR_TIMEOUT (a bounded
+ * wait gave up), GQA_ERR_ARG (a device-side index check failed),
+ * GQA_ERR_RANGE (a value was clamped) or GQA_ERR_CUDA.  Allocates nothing on
+ * a device where only gqa_decode_attention_noalloc has run. */
 int gqa_check_device_error(void);
 
 /* Watchdog self-test: launches one kernel whose mbarrier wait can never

@@ -34,6 +34,8 @@ static int fail(int code, const char *fmt, ...)
 
 void record_error_message(const char *msg) { snprintf(g_msg, sizeof g_msg, "%s", msg); }
 
+void set_launch_count(int n) { g_launches = n; }
+
 static int cuda_fail(cudaError_t e, const char *what)
 {
     return fail(GQA_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
@@ -1285,18 +1287,31 @@ int gqa_attn_cost(int B, int S, int hidden, int Hq, int Hkv, int head_dim, int c
 
 int gqa_check_device_error(void)
 {
-    DeviceState *st;
-    int rc = device_state(&st);
-    if (rc) return rc;
-    cudaError_t e = cudaDeviceSynchronize();
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= 64) return fail(GQA_ERR_CUDA, "device index %d out of range", dev);
+    e = cudaDeviceSynchronize();
     if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
-    unsigned word = 0;
-    e = cudaMemcpy(&word, st->err, sizeof word, cudaMemcpyDeviceToHost);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpy(error word)");
-    if (word) {
-        e = cudaMemset(st->err, 0, sizeof word);
-        if (e != cudaSuccess) return cuda_fail(e, "cudaMemset(error word)");
+    bool have_state;
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        have_state = g_dev[dev].init;
     }
+    // Without per-device state no kernel of the workspace-taking entry points
+    // has run on this device, so its word is not read (nor set up: a caller of
+    // gqa_decode_attention_noalloc alone gets this check without an allocation).
+    unsigned word = 0;
+    if (have_state) {
+        DeviceState &st = g_dev[dev];
+        e = cudaMemcpy(&word, st.err, sizeof word, cudaMemcpyDeviceToHost);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpy(error word)");
+        if (word) {
+            e = cudaMemset(st.err, 0, sizeof word);
+            if (e != cudaSuccess) return cuda_fail(e, "cudaMemset(error word)");
+        }
+    }
+    word |= noalloc_take_error_word(dev);
     if (word & kErrTimeout) return fail(GQA_ERR_TIMEOUT, "a bounded device wait gave up (error word 0x%x)", word);
     if (word & kErrIndex) return fail(GQA_ERR_ARG, "a device-side index check failed (error word 0x%x)", word);
     if (word & kErrRange)
@@ -1317,3 +1332,12 @@ int gqa_selftest_bounded_wait(int limit_ms)
 }
 
 }  // extern "C"
+
+namespace gqa {
+
+int check_decode_attention_args(int B, int Hq, int Hkv, int d, int Lmax)
+{
+    return check_decode(B, 8, Hq, Hkv, d, Lmax, nullptr, nullptr);
+}
+
+}  // namespace gqa

@@ -156,6 +156,15 @@ cudaError_t launch_selftest_wait(unsigned *err, unsigned long long limit_ns, cud
 
 // Sets the message gqa_last_error() returns on the calling thread.
 void record_error_message(const char *msg);
+// Sets the count gqa_last_launch_count() returns on the calling thread.
+void set_launch_count(int n);
+// The argument checks of gqa_decode_attention (sizes, group size, head_dim,
+// cache size): GQA_OK or the status (with the message recorded) it returns.
+int check_decode_attention_args(int B, int Hq, int Hkv, int d, int Lmax);
+// Reads and clears the error word of gqa_decode_attention_noalloc on device
+// `dev` (0 if that entry point never ran there).  Host-synchronous: call with
+// the device idle.  Allocates nothing.
+unsigned noalloc_take_error_word(int dev);
 
 // Launch configuration for cudaLaunchKernelEx: optional thread-block cluster
 // (cluster > 1 CTAs along x) and optional programmatic dependent launch (pdl:

@@ -18,7 +18,13 @@
 //     ordering between them) race on it and give wrong results;
 //   - the first call on a device looks up the array's device address (once
 //     per device, with that device current), so make that first call before
-//     any stream capture begins.
+//     any stream capture begins;
+//   - the kernels' error word (a bounded wait that gave up) sits beside the
+//     array: each call clears it on its own stream before its kernels run, so
+//     a timeout in one call cannot cut short the waits of later calls, and
+//     gqa_check_device_error() reads and clears it (it reports GQA_ERR_TIMEOUT
+//     for a call whose waits gave up, if made before the next call's clearing
+//     runs).  Neither needs an allocation.
 #include <cuda_runtime.h>
 #include <stdio.h>
 
@@ -33,7 +39,7 @@ namespace {
 constexpr size_t kScratchFloats = (size_t)4 << 20;  // 16 MiB of fp32 partials
 
 __device__ __align__(256) float g_noalloc_scratch[kScratchFloats];
-__device__ __align__(256) unsigned g_noalloc_err[64];
+__device__ __align__(256) unsigned g_noalloc_err[64];  // word 0 is used
 
 struct NoAllocDevice {
     bool ready = false;
@@ -78,6 +84,22 @@ int noalloc_setup(NoAllocDevice **out)
 }
 
 }  // namespace
+
+unsigned noalloc_take_error_word(int dev)
+{
+    if (dev < 0 || dev >= 64) return 0;
+    unsigned *err;
+    {
+        std::lock_guard<std::mutex> lk(g_noalloc_mu);
+        if (!g_noalloc_dev[dev].ready) return 0;
+        err = g_noalloc_dev[dev].err;
+    }
+    unsigned word = 0;
+    if (cudaMemcpy(&word, err, sizeof word, cudaMemcpyDeviceToHost) != cudaSuccess) return 0;
+    if (word) cudaMemset(err, 0, sizeof word);
+    return word;
+}
+
 }  // namespace gqa
 
 using namespace gqa;
@@ -86,14 +108,10 @@ extern "C" int gqa_decode_attention_noalloc(const gqa_f16 *q, const gqa_bf16 *k_
                                             const int *kv_len, int B, int Hq, int Hkv, int head_dim, int Lmax,
                                             gqa_bf16 *attn_out, void *stream)
 {
-    if (B <= 0 || Hq <= 0 || Hkv <= 0 || head_dim <= 0 || Lmax <= 0)
-        return noalloc_fail(GQA_ERR_ARG, "gqa_decode_attention_noalloc: sizes must be positive");
-    if (Hq % Hkv) return noalloc_fail(GQA_ERR_ARG, "gqa_decode_attention_noalloc: Hq must be a multiple of Hkv");
-    const int G = Hq / Hkv;
-    if (head_dim != 64 && head_dim != 128)
-        return noalloc_fail(GQA_ERR_UNSUPPORTED, "gqa_decode_attention_noalloc: head_dim must be 64 or 128");
-    if (G != 1 && G != 2 && G != 4 && G != 8)
-        return noalloc_fail(GQA_ERR_UNSUPPORTED, "gqa_decode_attention_noalloc: Hq/Hkv must be 1, 2, 4 or 8");
+    set_launch_count(0);
+    // the same sizes, group sizes and head widths as gqa_decode_attention, with the same statuses
+    int rc = check_decode_attention_args(B, Hq, Hkv, head_dim, Lmax);
+    if (rc) return rc;
     if (!q || !k_cache || !v_cache || !kv_len || !attn_out)
         return noalloc_fail(GQA_ERR_ARG, "gqa_decode_attention_noalloc: null pointer");
     if (((uintptr_t)q | (uintptr_t)k_cache | (uintptr_t)v_cache | (uintptr_t)attn_out) & 15u)
@@ -109,7 +127,7 @@ extern "C" int gqa_decode_attention_noalloc(const gqa_f16 *q, const gqa_bf16 *k_
         return noalloc_fail(GQA_ERR_UNSUPPORTED, m);
     }
     NoAllocDevice *d;
-    int rc = noalloc_setup(&d);
+    rc = noalloc_setup(&d);
     if (rc) return rc;
     int splits = decode_choose_splits(B, Hkv, Lmax, d->num_sms);
     const int fit = (int)(kScratchFloats / per_split);
@@ -128,7 +146,12 @@ extern "C" int gqa_decode_attention_noalloc(const gqa_f16 *q, const gqa_bf16 *k_
     p.Lmax = Lmax;
     p.partials = d->scratch;
     p.splits = splits;
-    cudaError_t e = launch_decode_attention(p, d->err, (cudaStream_t)stream);
+    // a timeout recorded by an earlier call must not make this call's waits give up
+    cudaError_t e = cudaMemsetAsync(d->err, 0, sizeof(unsigned), (cudaStream_t)stream);
+    if (e != cudaSuccess)
+        return noalloc_fail(GQA_ERR_CUDA, "gqa_decode_attention_noalloc: clearing the error word failed");
+    e = launch_decode_attention(p, d->err, (cudaStream_t)stream);
     if (e != cudaSuccess) return noalloc_fail(GQA_ERR_CUDA, "gqa_decode_attention_noalloc: launch failed");
+    set_launch_count(2);
     return GQA_OK;
 }
