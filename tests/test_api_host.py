@@ -73,7 +73,7 @@ def fwd(L, **kw):
 
 @pytest.mark.parametrize("kw,code", [
     ({"S": 0}, -1), ({"B": -1}, -1), ({"Hq": 3}, -1), ({"d": 127}, -1), ({"qn": 0}, -1),
-    ({"d": 160}, -2), ({"d": 512}, -2), ({"d": 320}, -2), ({"hidden": 100}, -2), ({"Hq": 24, "Hkv": 8}, -2),
+    ({"d": 160}, -2), ({"d": 512}, -2), ({"d": 320}, -2), ({"hidden": 100}, -2), ({"Hq": 258, "Hkv": 2}, -2),
     ({"x": 0}, -1), ({"out": FAKE + 2}, -1), ({"out": FAKE}, -1), ({"theta": 0.0}, -1),
     ({"wsb": 100}, -5), ({"ws": 0}, -5), ({"ws": FAKE * 8 + 16}, -1),
 ])
@@ -91,8 +91,8 @@ def test_other_entry_points_validate(L):
     assert lib.gqa_attention(P(FAKE), P(FAKE), P(FAKE), 1, 8, 6, 4, 128, 1, P(FAKE), None) == -1
     assert lib.gqa_oproj_residual(P(FAKE), P(FAKE), P(FAKE), 4, 100, 64, P(FAKE * 2), None) == -2
     assert lib.gqa_oproj_residual(P(FAKE), P(FAKE), P(FAKE), 4, 64, 64, P(FAKE), None) == -1
-    assert lib.gqa_decode_attention(P(FAKE), P(FAKE), P(FAKE), P(FAKE), 2, 48, 2, 128, 100, P(FAKE), P(FAKE),
-                                    1 << 30, None) == -2   # group of 24
+    assert lib.gqa_decode_attention(P(FAKE), P(FAKE), P(FAKE), P(FAKE), 2, 260, 2, 128, 100, P(FAKE), P(FAKE),
+                                    1 << 30, None) == -2   # group of 130
     assert lib.gqa_decode_attention(P(FAKE), P(FAKE), P(FAKE), P(FAKE), 2, 8, 2, 80, 100, P(FAKE), P(FAKE),
                                     1 << 30, None) == -2   # decode: head_dim 64 or 128 only
     assert lib.gqa_attn_decode(P(FAKE), P(FAKE), P(FAKE), None, None, 1e6, 1e-6, 2, 64, 8, 2, 128, P(FAKE),

@@ -200,6 +200,16 @@ static int check_layer(int B, int S, int hidden, int Hq, int Hkv, int d, const v
     return GQA_OK;
 }
 
+// Forward attention: any group size up to the 128 rows of a query tile (the
+// tile packs floor(128 / G) positions of each of the G heads).
+static int check_group(int Hq, int Hkv)
+{
+    const int G = Hq / Hkv;
+    if (G > 128) return fail(GQA_ERR_UNSUPPORTED, "unsupported group size Hq/Hkv=%d (at most 128)", G);
+    return GQA_OK;
+}
+
+// The backward packs 128 / G positions per tile with power-of-two index masks.
 static int check_group_pow2(int Hq, int Hkv)
 {
     const int G = Hq / Hkv;
@@ -385,7 +395,7 @@ int gqa_attention(const gqa_f16 *q, const gqa_f16 *k, const gqa_f16 *v, int B, i
     g_launches = 0;
     int rc = check_layer(B, S, 8, Hq, Hkv, head_dim, nullptr, nullptr);
     if (rc) return rc;
-    if ((rc = check_group_pow2(Hq, Hkv))) return rc;
+    if ((rc = check_group(Hq, Hkv))) return rc;
     if (!q || !k || !v || !attn_out) return fail(GQA_ERR_ARG, "null tensor pointer");
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(attn_out))
         return fail(GQA_ERR_ARG, "tensor pointers must be 16-byte aligned");
@@ -419,7 +429,7 @@ int gqa_attn_forward_rd(const gqa_bf16 *x, const gqa_bf16 *Wqkv, const gqa_bf16 
     g_launches = 0;
     int rc = check_layer(B, S, hidden, Hq, Hkv, head_dim, q_norm_w, k_norm_w);
     if (rc) return rc;
-    if ((rc = check_group_pow2(Hq, Hkv))) return rc;
+    if ((rc = check_group(Hq, Hkv))) return rc;
     if (!x || !Wqkv || !Wo || !out) return fail(GQA_ERR_ARG, "null tensor pointer");
     if (!aligned16(x) || !aligned16(Wqkv) || !aligned16(Wo) || !aligned16(out))
         return fail(GQA_ERR_ARG, "tensor pointers must be 16-byte aligned");
@@ -513,7 +523,7 @@ int gqa_attn_forward_host(const gqa_bf16 *x_host, const gqa_bf16 *Wqkv, const gq
     g_launches = 0;
     int rc = check_layer(B, S, hidden, Hq, Hkv, head_dim, q_norm_w, k_norm_w);
     if (rc) return rc;
-    if ((rc = check_group_pow2(Hq, Hkv))) return rc;
+    if ((rc = check_group(Hq, Hkv))) return rc;
     if (!x_host || !Wqkv || !Wo || !out_host) return fail(GQA_ERR_ARG, "null tensor pointer");
     if (!aligned16(Wqkv) || !aligned16(Wo)) return fail(GQA_ERR_ARG, "weight pointers must be 16-byte aligned");
     if (!(rope_theta > 0.0f) || !(eps >= 0.0f)) return fail(GQA_ERR_ARG, "rope_theta must be > 0 and eps >= 0");
@@ -935,8 +945,7 @@ static int check_decode(int B, int hidden, int Hq, int Hkv, int d, int Lmax, con
     if (Lmax <= 0) return fail(GQA_ERR_ARG, "Lmax must be positive");
     if (d != 64 && d != 128) return fail(GQA_ERR_UNSUPPORTED, "decode supports head_dim 64 and 128 (got %d)", d);
     const int G = Hq / Hkv;
-    if (G != 1 && G != 2 && G != 4 && G != 8)
-        return fail(GQA_ERR_UNSUPPORTED, "unsupported decode group size Hq/Hkv=%d (supported: 1, 2, 4, 8)", G);
+    if (G > 128) return fail(GQA_ERR_UNSUPPORTED, "unsupported decode group size Hq/Hkv=%d (at most 128)", G);
     if ((long long)B * Hkv * Lmax * d > (1LL << 40)) return fail(GQA_ERR_UNSUPPORTED, "cache too large");
     return GQA_OK;
 }
@@ -1062,7 +1071,7 @@ static int check_cached(int B, int S, int hidden, int Hq, int Hkv, int d, int Lm
 {
     int rc = check_layer(B, S, hidden, Hq, Hkv, d, qn, kn);
     if (rc) return rc;
-    if ((rc = check_group_pow2(Hq, Hkv))) return rc;
+    if ((rc = check_group(Hq, Hkv))) return rc;
     if (Lmax < S) return fail(GQA_ERR_ARG, "Lmax=%d is smaller than the %d new tokens", Lmax, S);
     if ((long long)B * Hkv * Lmax * d > (1LL << 40)) return fail(GQA_ERR_UNSUPPORTED, "cache too large");
     return GQA_OK;

@@ -10,7 +10,8 @@
 // and spends as few instructions per key as possible.
 //
 // Pass 1 (decode_split_kernel), persistent, one CTA per SM.  Work item =
-// (sequence b, KV head g, split s): a contiguous range of that head's keys.
+// (sequence b, KV head g, split s, head sub-group): a contiguous range of that
+// head's keys for up to GM of the query heads that share it.
 //   warp 0      TMA: the item's keys and values in chunks of 64 keys
 //               (128-byte swizzled tiles), into a shared-memory ring, across
 //               items without pausing;
@@ -18,19 +19,30 @@
 //               chunks in turn (one group for bf16 caches; two for E4M3
 //               caches, whose chunks carry half the bytes and would otherwise
 //               leave the SM waiting on instruction latency); each warp of a
-//               group takes 16 keys of its group's chunks.  The G query heads
-//               sharing each K/V row are a genuine G x d by d x keys product,
-//               computed with warp-level mma.sync m16n8k16 (heads in the M
-//               rows, padded to 16): S = Q K^T with K fragments read by
-//               ldmatrix from the swizzled tile; for bf16 caches the binary16
-//               query is split into bf16 high and low parts (two MMAs) so no
-//               query precision is lost; online softmax in the S accumulator
-//               registers; the probabilities are already laid out as the A
-//               fragment of O += P V, with V fragments from ldmatrix.trans.
+//               group takes 16 keys of its group's chunks.  The query heads
+//               sharing each K/V row make it a genuine heads x d by d x keys
+//               product, computed with warp-level mma.sync m16n8k16:
+//     bf16 caches: heads in the MMA's 16 rows (up to GM = 16 heads per item),
+//               S = Q K^T with K fragments read by ldmatrix from the swizzled
+//               tile; the binary16 query is split into bf16 high and low parts
+//               (two MMAs) so no query precision is lost; online softmax in the
+//               S accumulator registers, whose layout is already the A
+//               fragment of O += P V (P also split into high and low parts),
+//               with V fragments from ldmatrix.trans;
+//     E4M3 caches: transposed products, S^T = K Q^T (16 keys in the rows, up
+//               to GM = 8 heads in the 8 columns) and O^T = V^T P^T (d in the
+//               rows): one MMA covers 16 keys x 8 heads, half the MMAs of the
+//               heads-in-rows form, and P^T reaches the B-fragment layout by
+//               an 8x8 transpose (movmatrix).  E4M3 widens exactly to binary16,
+//               so the MMAs are binary16 and the query needs no split.
 //   At the end of an item the warps' (max, sum, unnormalised output) are
 //   merged in shared memory into one fp32 partial record.
-// Pass 2 (decode_combine_kernel): per (b, g), merge the splits by their
-// log-sum-exp weights and write attn[b, j*d + c] in bf16.
+// A group of more than GM query heads is taken as vsub sub-groups of G / vsub
+// heads each; the sub-groups of one key range are consecutive work items, so
+// they run at the same time on neighbouring SMs and the second read of each
+// chunk comes from L2.
+// Pass 2 (decode_combine_kernel): per (b, sub-group), merge the splits by
+// their log-sum-exp weights and write attn[b, j*d + c] in bf16.
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -44,7 +56,8 @@ constexpr int kGroup = 4;      // consumer warps per chunk, 16 keys each
 // F8: the caches hold one-byte E4M3 codes, so a 128-wide row is one 128-byte
 // swizzled box row and a chunk is half the bytes (twice the stages in flight).
 // CW consumer warps: CW / kGroup groups of four take the staged chunks in turn.
-template <int D, bool F8 = false, int CW = kGroup>
+// GM: query heads per work item (rows of the per-warp partials).
+template <int D, int GM, bool F8 = false, int CW = kGroup>
 struct DSmem {
     static constexpr int NCH = F8 ? 1 : D / 64;   // 128-byte boxes per row: 64-wide d halves, or all 128 codes
     static constexpr int BOX = kChunk * 128;       // one 64-key x 128-byte swizzled box (8 KB)
@@ -54,8 +67,8 @@ struct DSmem {
     static constexpr int STAGES = F8 ? 12 : (D == 128 ? 6 : 12);
     static constexpr int K = 0;
     static constexpr int V = STAGES * CB;
-    static constexpr int RED = 2 * STAGES * CB;    // [CW][8][D + 2] floats
-    static constexpr int BARS = RED + CW * 8 * (D + 2) * 4;
+    static constexpr int RED = 2 * STAGES * CB;    // [CW][GM][D + 2] floats
+    static constexpr int BARS = RED + CW * GM * (D + 2) * 4;
     static constexpr int TOTAL = BARS + 2 * STAGES * 8;
     static constexpr int ALLOC = TOTAL + 1024;
 };
@@ -63,18 +76,25 @@ struct DSmem {
 template <int CW>
 DEVI void consumer_sync() { asm volatile("bar.sync 1, %0;" ::"n"(CW * 32) : "memory"); }
 
-// Key range of one work item.
+// One work item: keys [begin, end) of cache head g of sequence b, for the
+// query heads vg*Gv .. vg*Gv + Gv - 1 (vg = g*vsub + sub); its partial record
+// is number rec.
 struct ItemRange {
-    int b, g, s, begin, end;  // keys [begin, end)
+    int b, g, vg, rec, begin, end;
 };
 
 DEVI ItemRange item_range(const DecodeAttentionProblem &P, int item, unsigned *err, bool report)
 {
     ItemRange r;
-    const int bg = item / P.splits;
-    r.s = item - bg * P.splits;
+    const int vsub = P.vsub;
+    const int sub = item % vsub;
+    const int t = item / vsub;
+    const int s = t % P.splits;
+    const int bg = t / P.splits;
     r.b = bg / P.Hkv;
     r.g = bg - r.b * P.Hkv;
+    r.vg = r.g * vsub + sub;
+    r.rec = (bg * vsub + sub) * P.splits + s;
     int len = P.len[r.b] + P.len_bias;
     if (len < 1 || len > P.Lmax) {
         if (report) atomicOr(err, kErrIndex);
@@ -82,7 +102,7 @@ DEVI ItemRange item_range(const DecodeAttentionProblem &P, int item, unsigned *e
     }
     const int chunks = (len + kChunk - 1) / kChunk;
     const int per = (chunks + P.splits - 1) / P.splits;
-    const int c0 = min(chunks, r.s * per), c1 = min(chunks, c0 + per);
+    const int c0 = min(chunks, s * per), c1 = min(chunks, c0 + per);
     r.begin = c0 * kChunk;
     r.end = min(c1 * kChunk, len);
     if (r.end < r.begin) r.end = r.begin;
@@ -94,7 +114,7 @@ DEVI ItemRange item_range(const DecodeAttentionProblem &P, int item, unsigned *e
 template <int D>
 DEVI uint32_t swz(int key, int dcol)
 {
-    return (uint32_t)((dcol >> 6) * DSmem<D>::BOX + key * 128 + ((((dcol & 63) >> 3) ^ (key & 7)) << 4));
+    return (uint32_t)((dcol >> 6) * DSmem<D, 8>::BOX + key * 128 + ((((dcol & 63) >> 3) ^ (key & 7)) << 4));
 }
 
 // Byte offset of code (key, byte) inside an E4M3 chunk of 128-byte rows.
@@ -105,32 +125,395 @@ DEVI uint32_t swz8(int key, int byte)
 
 DEVI uint32_t bf16x2_bits(float lo, float hi) { return pack_bf16(lo, hi); }
 
-// F8 = false: bf16 caches, bf16 MMAs with the query and P split into high
-// and low bf16 parts.  F8 = true: E4M3 caches, binary16 MMAs (E4M3 widens
-// exactly to binary16, the binary16 query needs no split, P is split into
-// binary16 high and low parts).  In the F8 path the 16 d-values of one
-// k-step reach the K fragment in the order ldmatrix delivers 4-byte groups:
-// MMA k-index 2t+e holds d = 4t+e and k-index 2t+8+e holds d = 4t+2+e
-// (t = lane % 4); the query fragment uses the same order, which leaves the
-// dot product unchanged.  V fragments come from a transposed ldmatrix whose
-// 4 bytes (keys k, k+1 x d-values c, c+1) a byte permute splits into an
-// even-d and an odd-d n-tile: output columns arrive interleaved and are put
-// back in order when written to shared memory.
-template <int D, int G, bool F8, int CW>
+// Transpose of an 8x8 matrix of 16-bit elements held as the warp's A/C
+// fragment rows (lane: row lane/4, elements 2(lane%4), +1).
+DEVI uint32_t movmatrix_t(uint32_t x)
+{
+    uint32_t r;
+    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(r) : "r"(x));
+    return r;
+}
+
+// bf16 high part of (lo, hi) and the bf16 of what it leaves over.
+DEVI void split_bf16(float lo, float hi, uint32_t &h, uint32_t &l)
+{
+    const __nv_bfloat162 b = __floats2bfloat162_rn(lo, hi);
+    const float2 f = __bfloat1622float2(b);
+    h = *reinterpret_cast<const uint32_t *>(&b);
+    l = bf16x2_bits(lo - f.x, hi - f.y);
+}
+
+// Value rows past the item's last key may hold anything (slots past the
+// sequence are not initialised); 0 * NaN would poison O, so the rows of this
+// warp's 16 keys at or past `end` are zeroed.  Masked scores need no such care.
+template <int NCH>
+DEVI void zero_v_tail(uint8_t *vchunk, int u0, int end, int cw, int lane)
+{
+    const int first = max(end - u0, cw * 16);
+    uint4 *vrow = reinterpret_cast<uint4 *>(vchunk);
+    for (int idx = lane; idx < (cw * 16 + 16 - first) * NCH * 8; idx += 32) {
+        const int key = first + idx / (NCH * 8), rem = idx % (NCH * 8);
+        vrow[((rem >> 3) * (kChunk * 128) + key * 128) / 16 + (rem & 7)] = make_uint4(0, 0, 0, 0);
+    }
+    __syncwarp();
+}
+
+// One step of the online softmax for the four scores a lane holds of one
+// query row (keys kbase, +1, +8, +9; scaled to log2 units, masked ones
+// -inf): the row max over the four lanes of the row, the rescale factor of the
+// running sums and the probabilities.  lazy: the running max moves only when a
+// score passes it by more than 2^8 (P then stays <= 2^8), so O is rescaled
+// rarely; otherwise it moves whenever the max grows.
+template <bool LAZY>
+DEVI void softmax_step(const float (&v)[4], float &m_run, float &l_run, float &alpha, float (&p)[4])
+{
+    float mx = fmaxf(fmaxf(v[0], v[1]), fmaxf(v[2], v[3]));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+    float m_new = fmaxf(m_run, mx);
+    if (LAZY && !(mx > m_run + 8.0f)) m_new = m_run;
+    const float m_use = (m_new == -INFINITY) ? 0.0f : m_new;
+    alpha = ex2(m_run - m_use);
+    m_run = m_new;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) p[e] = (v[e] == -INFINITY) ? 0.0f : ex2(v[e] - m_use);
+    l_run = l_run * alpha + ((p[0] + p[1]) + (p[2] + p[3]));
+}
+
+// Merge of the consumer warps' per-head (o, max, sum) rows in `red` into the
+// item's partial record: o = sum_w 2^(m_w - M) o_w, l likewise, M = max_w m_w.
+template <int D, int GM, int CW>
+DEVI void write_record(const float *red, float *rec, int Gv)
+{
+    for (int idx = threadIdx.x - 32; idx < Gv * D; idx += CW * 32) {
+        const int h = idx / D, c = idx - h * D;
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < CW; ++w) M = fmaxf(M, red[(w * GM + h) * (D + 2) + D]);
+        const float Mu = (M == -INFINITY) ? 0.0f : M;
+        float acc = 0.0f, lsum = 0.0f;
+#pragma unroll
+        for (int w = 0; w < CW; ++w) {
+            const float *rr = red + (w * GM + h) * (D + 2);
+            const float f = ex2(rr[D] - Mu);
+            acc = fmaf(f, rr[c], acc);
+            lsum = fmaf(f, rr[D + 1], lsum);
+        }
+        rec[h * (D + 2) + c] = acc;
+        if (c == 0) {
+            rec[h * (D + 2) + D] = M;
+            rec[h * (D + 2) + D + 1] = lsum;
+        }
+    }
+}
+
+// Consumer warps over bf16 caches: heads in the MMA rows (row grp: head grp,
+// row grp + 8: head grp + 8 when GM = 16), bf16 MMAs with the query and P
+// split into high and low bf16 parts.
+template <int D, int GM, int CW>
+DEVI void consume_bf16(const DecodeAttentionProblem &P, uint8_t *smem, uint64_t *full, uint64_t *empty, float *red,
+                       float scale_log2, int n_items, unsigned *err)
+{
+    using L = DSmem<D, GM, false, CW>;
+    static_assert(CW == kGroup, "bf16 caches: one group of four consumer warps");
+    static_assert(GM == 8 || GM == 16, "8 or 16 heads per item");
+    constexpr bool TWO = GM > 8;  // MMA rows 8..15 carry heads 8..15
+    constexpr int ST = L::STAGES;
+    constexpr int KS = D / 16;    // k-steps of the QK product
+    constexpr int NT = D / 8;     // n-tiles of the PV product
+    const int Gv = P.Hq / P.Hkv / P.vsub;
+    const int lane = threadIdx.x % 32;
+    const int cw = threadIdx.x / 32 - 1;  // keys [16 cw, 16 cw + 16) of each chunk
+    const int grp = lane >> 2, tig = lane & 3;
+    const bool va = grp < Gv, vb = TWO && grp + 8 < Gv;
+    // ldmatrix row addresses (relative to a chunk): lane i serves row i%8 of matrix i/8
+    const int mi = lane >> 3, mr = lane & 7;
+    const int qk_key = cw * 16 + (mi >> 1) * 8 + mr, qk_dofs = (mi & 1) * 8;  // K: (keys, d) blocks
+    const int pv_key = cw * 16 + (mi & 1) * 8 + mr, pv_dofs = (mi >> 1) * 8;  // V: transposed blocks
+
+    int it = 0;
+    for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
+        const ItemRange r = item_range(P, item, err, false);
+        const uint16_t *qbase = P.q + (size_t)(r.b * P.Hq + r.vg * Gv) * D;
+        // A fragments of Q: [0] row grp, k 2t..; [1] row grp+8, k 2t..; [2] row grp, k 2t+8..;
+        // [3] row grp+8, k 2t+8.. (binary16 split into bf16 hi + lo)
+        uint32_t qh[KS][4], ql[KS][4];
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks)
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                float2 f = make_float2(0.0f, 0.0f);
+                if (va) f = __half22float2(*reinterpret_cast<const __half2 *>(qbase + grp * D + ks * 16 + half * 8 + 2 * tig));
+                split_bf16(f.x, f.y, qh[ks][2 * half], ql[ks][2 * half]);
+                qh[ks][2 * half + 1] = ql[ks][2 * half + 1] = 0u;
+                if (TWO && vb) {
+                    f = __half22float2(
+                        *reinterpret_cast<const __half2 *>(qbase + (grp + 8) * D + ks * 16 + half * 8 + 2 * tig));
+                    split_bf16(f.x, f.y, qh[ks][2 * half + 1], ql[ks][2 * half + 1]);
+                }
+            }
+        float o[NT][4];
+#pragma unroll
+        for (int n = 0; n < NT; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.0f;
+        float mA = -INFINITY, lA = 0.0f, mB = -INFINITY, lB = 0.0f;  // rows grp, grp + 8
+
+        for (int u0 = r.begin; u0 < r.end; u0 += kChunk, ++it) {
+            const int s = it % ST;
+            if (!mbar_wait(full + s, (it / ST) & 1, err)) break;
+            const uint32_t kb = smem_u32(smem + L::K + s * L::CB);
+            const uint32_t vbase = smem_u32(smem + L::V + s * L::CB);
+            if (u0 + kChunk > r.end) zero_v_tail<L::NCH>(smem + L::V + s * L::CB, u0, r.end, cw, lane);
+            // S[heads x 16 keys] = Q K^T
+            float sc[2][4] = {{0.0f, 0.0f, 0.0f, 0.0f}, {0.0f, 0.0f, 0.0f, 0.0f}};
+#pragma unroll
+            for (int ks = 0; ks < KS; ++ks) {
+                uint32_t b00, b01, b10, b11;
+                ldsm_x4(kb + swz<D>(qk_key, ks * 16 + qk_dofs), b00, b01, b10, b11);
+                mma_bf16_16816(sc[0], qh[ks][0], qh[ks][1], qh[ks][2], qh[ks][3], b00, b01);
+                mma_bf16_16816(sc[1], qh[ks][0], qh[ks][1], qh[ks][2], qh[ks][3], b10, b11);
+                mma_bf16_16816(sc[0], ql[ks][0], ql[ks][1], ql[ks][2], ql[ks][3], b00, b01);
+                mma_bf16_16816(sc[1], ql[ks][0], ql[ks][1], ql[ks][2], ql[ks][3], b10, b11);
+            }
+            // this lane's keys: kbase, +1 (n-tile 0) and kbase + 8, +9 (n-tile 1)
+            const int kbase = u0 + cw * 16 + 2 * tig;
+            const bool k0 = kbase < r.end, k1 = kbase + 1 < r.end, k8 = kbase + 8 < r.end, k9 = kbase + 9 < r.end;
+            const float vA[4] = {k0 ? sc[0][0] * scale_log2 : -INFINITY, k1 ? sc[0][1] * scale_log2 : -INFINITY,
+                                 k8 ? sc[1][0] * scale_log2 : -INFINITY, k9 ? sc[1][1] * scale_log2 : -INFINITY};
+            float pA[4], aA;
+            softmax_step<false>(vA, mA, lA, aA, pA);
+            // P as the A fragment of O += P V, split into bf16 high and low parts
+            uint32_t a0h = 0u, a2h = 0u, a0l = 0u, a2l = 0u, a1h = 0u, a3h = 0u, a1l = 0u, a3l = 0u;
+            if (va) {
+                split_bf16(pA[0], pA[1], a0h, a0l);
+                split_bf16(pA[2], pA[3], a2h, a2l);
+            }
+            float aB = 1.0f;
+            if constexpr (TWO) {
+                const float vB[4] = {k0 ? sc[0][2] * scale_log2 : -INFINITY, k1 ? sc[0][3] * scale_log2 : -INFINITY,
+                                     k8 ? sc[1][2] * scale_log2 : -INFINITY, k9 ? sc[1][3] * scale_log2 : -INFINITY};
+                float pB[4];
+                softmax_step<false>(vB, mB, lB, aB, pB);
+                if (vb) {
+                    split_bf16(pB[0], pB[1], a1h, a1l);
+                    split_bf16(pB[2], pB[3], a3h, a3l);
+                }
+            }
+#pragma unroll
+            for (int n = 0; n < NT; ++n) {
+                o[n][0] *= aA;
+                o[n][1] *= aA;
+                if (TWO) {
+                    o[n][2] *= aB;
+                    o[n][3] *= aB;
+                }
+            }
+#pragma unroll
+            for (int nb = 0; nb < NT / 2; ++nb) {
+                uint32_t b0a, b1a, b0b, b1b;
+                ldsm_x4_trans(vbase + swz<D>(pv_key, nb * 16 + pv_dofs), b0a, b1a, b0b, b1b);
+                mma_bf16_16816(o[2 * nb], a0h, a1h, a2h, a3h, b0a, b1a);
+                mma_bf16_16816(o[2 * nb + 1], a0h, a1h, a2h, a3h, b0b, b1b);
+                mma_bf16_16816(o[2 * nb], a0l, a1l, a2l, a3l, b0a, b1a);
+                mma_bf16_16816(o[2 * nb + 1], a0l, a1l, a2l, a3l, b0b, b1b);
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(empty + s);
+        }
+        // row sums over the four lanes of a row; the maxima are already row-uniform
+        lA += __shfl_xor_sync(0xffffffffu, lA, 1);
+        lA += __shfl_xor_sync(0xffffffffu, lA, 2);
+        lB += __shfl_xor_sync(0xffffffffu, lB, 1);
+        lB += __shfl_xor_sync(0xffffffffu, lB, 2);
+        float *rw = red + cw * GM * (D + 2);
+        if (va) {
+#pragma unroll
+            for (int n = 0; n < NT; ++n) {
+                rw[grp * (D + 2) + 8 * n + 2 * tig] = o[n][0];
+                rw[grp * (D + 2) + 8 * n + 2 * tig + 1] = o[n][1];
+            }
+            if (tig == 0) {
+                rw[grp * (D + 2) + D] = mA;
+                rw[grp * (D + 2) + D + 1] = lA;
+            }
+        }
+        if (TWO && vb) {
+#pragma unroll
+            for (int n = 0; n < NT; ++n) {
+                rw[(grp + 8) * (D + 2) + 8 * n + 2 * tig] = o[n][2];
+                rw[(grp + 8) * (D + 2) + 8 * n + 2 * tig + 1] = o[n][3];
+            }
+            if (tig == 0) {
+                rw[(grp + 8) * (D + 2) + D] = mB;
+                rw[(grp + 8) * (D + 2) + D + 1] = lB;
+            }
+        }
+        consumer_sync<CW>();
+        write_record<D, GM, CW>(red, P.partials + (size_t)r.rec * Gv * (D + 2), Gv);
+        consumer_sync<CW>();  // red is reused by the next item
+    }
+}
+
+// Consumer warps over E4M3 caches: transposed products with the group's heads
+// in the MMA's 8 columns (GM = 8), binary16 MMAs.  In the S^T product the 16
+// d-values of one k-step reach the K (A) fragment in the order ldmatrix
+// delivers 4-byte groups: MMA k-index 2t+e holds d = 4t+e and k-index 2t+8+e
+// holds d = 4t+2+e (t = lane % 4); the query (B) fragment uses the same order,
+// which leaves the dot product unchanged.  V fragments come from a transposed
+// ldmatrix whose 4 bytes (keys k, k+1 x d-values c, c+1) a byte permute splits
+// into an even-d and an odd-d half: rows of O^T arrive interleaved (m-tile b
+// holds d = 16b + 2grp and 16b + 2grp + 1) and are put back in order when
+// written to shared memory.  P stays <= 2^8 (lazy running max), exact in
+// binary16's range, so O is rescaled rarely.
+template <int D, int CW>
+DEVI void consume_f8(const DecodeAttentionProblem &P, uint8_t *smem, uint64_t *full, uint64_t *empty, float *red,
+                     float scale_log2, int n_items, unsigned *err)
+{
+    constexpr int GM = 8;
+    using L = DSmem<D, GM, true, CW>;
+    static_assert(D == 128, "E4M3 caches: 128-wide heads");
+    constexpr int NG = CW / kGroup;  // chunk it goes to group it % NG
+    static_assert(L::STAGES % NG == 0, "each ring stage must belong to one group (phase parity)");
+    constexpr int ST = L::STAGES;
+    constexpr int KS = D / 16;
+    const int Gv = P.Hq / P.Hkv / P.vsub;
+    const int lane = threadIdx.x % 32;
+    const int cwi = threadIdx.x / 32 - 1;  // consumer warp index (partials slot)
+    const int grpi = cwi / kGroup;         // its group: chunks it with it % NG == grpi
+    const int cw = cwi % kGroup;           // keys [16 cw, 16 cw + 16) of each of its chunks
+    const int grp = lane >> 2, tig = lane & 3;
+    const bool head_valid = grp < Gv;      // B-fragment column grp = query head vg*Gv + grp
+    // matrix mi of an ldmatrix covers keys 8*(mi&1).. of the warp and 16-byte block mi>>1 of the pair
+    const int mi = lane >> 3, mr = lane & 7;
+    const int f8_key = cw * 16 + (mi & 1) * 8 + mr, f8_blk = mi >> 1;
+
+    int it = 0;
+    for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
+        const ItemRange r = item_range(P, item, err, false);
+        // B fragments of Q^T, d in the order described above
+        uint32_t qb[KS][2];
+        const uint16_t *qrow = P.q + (size_t)(r.b * P.Hq + r.vg * Gv + (head_valid ? grp : 0)) * D;
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks) {
+            uint2 v = make_uint2(0u, 0u);
+            if (head_valid) v = *reinterpret_cast<const uint2 *>(qrow + ks * 16 + 4 * tig);
+            qb[ks][0] = v.x;
+            qb[ks][1] = v.y;
+        }
+        float o[D / 16][4];  // m-tile b: rows d = 16b + 2grp (c0, c1) and 16b + 2grp + 1 (c2, c3)
+#pragma unroll
+        for (int b = 0; b < D / 16; ++b) o[b][0] = o[b][1] = o[b][2] = o[b][3] = 0.0f;
+        float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.0f, l1 = 0.0f;  // heads 2 tig, 2 tig + 1
+
+        for (int u0 = r.begin; u0 < r.end; u0 += kChunk, ++it) {
+            if (NG > 1 && it % NG != grpi) continue;  // another group's chunk
+            const int s = it % ST;
+            if (!mbar_wait(full + s, (it / ST) & 1, err)) break;
+            const uint32_t kb = smem_u32(smem + L::K + s * L::CB);
+            const uint32_t vb = smem_u32(smem + L::V + s * L::CB);
+            if (u0 + kChunk > r.end) zero_v_tail<L::NCH>(smem + L::V + s * L::CB, u0, r.end, cw, lane);
+            // S^T [16 keys x 8 heads], two accumulators (k-step parity)
+            float sc[2][4] = {{0.0f, 0.0f, 0.0f, 0.0f}, {0.0f, 0.0f, 0.0f, 0.0f}};
+#pragma unroll
+            for (int kp = 0; kp < KS / 2; ++kp) {
+                uint32_t rk[4];  // (keys 0-7, block 2kp), (8-15, 2kp), (0-7, 2kp+1), (8-15, 2kp+1)
+                ldsm_x4(kb + swz8(f8_key, (2 * kp + f8_blk) * 16), rk[0], rk[1], rk[2], rk[3]);
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    uint32_t lo0, hi0, lo1, hi1;
+                    e4m3x4_to_f16x4(rk[2 * j], lo0, hi0);
+                    e4m3x4_to_f16x4(rk[2 * j + 1], lo1, hi1);
+                    mma_f16_16816(sc[j], lo0, lo1, hi0, hi1, qb[2 * kp + j][0], qb[2 * kp + j][1]);
+                }
+            }
+            const int ka = u0 + cw * 16 + grp;  // this lane's keys: ka, ka + 8
+            const float v0 = (ka < r.end) ? (sc[0][0] + sc[1][0]) * scale_log2 : -INFINITY;      // head 2t
+            const float v1 = (ka < r.end) ? (sc[0][1] + sc[1][1]) * scale_log2 : -INFINITY;      // head 2t+1
+            const float v2 = (ka + 8 < r.end) ? (sc[0][2] + sc[1][2]) * scale_log2 : -INFINITY;  // head 2t
+            const float v3 = (ka + 8 < r.end) ? (sc[0][3] + sc[1][3]) * scale_log2 : -INFINITY;  // head 2t+1
+            float x0 = fmaxf(v0, v2), x1 = fmaxf(v1, v3);
+#pragma unroll
+            for (int sh = 4; sh <= 16; sh <<= 1) {
+                x0 = fmaxf(x0, __shfl_xor_sync(0xffffffffu, x0, sh));
+                x1 = fmaxf(x1, __shfl_xor_sync(0xffffffffu, x1, sh));
+            }
+            // the running max moves only past a 2^8 growth (P <= 2^8 in binary16)
+            const float n0 = (x0 > m0 + 8.0f) ? fmaxf(m0, x0) : m0;
+            const float n1 = (x1 > m1 + 8.0f) ? fmaxf(m1, x1) : m1;
+            const float u0m = (n0 == -INFINITY) ? 0.0f : n0, u1m = (n1 == -INFINITY) ? 0.0f : n1;
+            const float a0 = ex2(m0 - u0m), a1 = ex2(m1 - u1m);
+            m0 = n0;
+            m1 = n1;
+            const float p0 = (v0 == -INFINITY) ? 0.0f : ex2(v0 - u0m);
+            const float p1 = (v1 == -INFINITY) ? 0.0f : ex2(v1 - u1m);
+            const float p2 = (v2 == -INFINITY) ? 0.0f : ex2(v2 - u0m);
+            const float p3 = (v3 == -INFINITY) ? 0.0f : ex2(v3 - u1m);
+            l0 = l0 * a0 + (p0 + p2);
+            l1 = l1 * a1 + (p1 + p3);
+            // P^T as the B fragment: transpose the (key x head) 8x8 blocks
+            const uint32_t pb0 = movmatrix_t(pack_f16(p0, p1)), pb1 = movmatrix_t(pack_f16(p2, p3));
+            if (__any_sync(0xffffffffu, a0 != 1.0f || a1 != 1.0f)) {
+#pragma unroll
+                for (int b = 0; b < D / 16; ++b) {
+                    o[b][0] *= a0;
+                    o[b][1] *= a1;
+                    o[b][2] *= a0;
+                    o[b][3] *= a1;
+                }
+            }
+#pragma unroll
+            for (int j2 = 0; j2 < D / 32; ++j2) {
+                uint32_t rv[4];  // (keys 0-7, block 2j2), (8-15, 2j2), (0-7, 2j2+1), (8-15, 2j2+1)
+                ldsm_x4_trans(vb + swz8(f8_key, (2 * j2 + f8_blk) * 16), rv[0], rv[1], rv[2], rv[3]);
+#pragma unroll
+                for (int x = 0; x < 2; ++x) {
+                    // bytes (k c, k c+1, k+1 c, k+1 c+1) -> (k c, k+1 c | k c+1, k+1 c+1)
+                    uint32_t lo0, hi0, lo1, hi1;
+                    e4m3x4_to_f16x4(prmt(rv[2 * x], 0u, 0x3120u), lo0, hi0);
+                    e4m3x4_to_f16x4(prmt(rv[2 * x + 1], 0u, 0x3120u), lo1, hi1);
+                    mma_f16_16816(o[2 * j2 + x], lo0, hi0, lo1, hi1, pb0, pb1);
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(empty + s);
+        }
+        // sums over the eight lanes of a head column; the max is already uniform there
+#pragma unroll
+        for (int sh = 4; sh <= 16; sh <<= 1) {
+            l0 += __shfl_xor_sync(0xffffffffu, l0, sh);
+            l1 += __shfl_xor_sync(0xffffffffu, l1, sh);
+        }
+        float *rw = red + cwi * GM * (D + 2);
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const int h = 2 * tig + e;
+            if (h < Gv) {
+                float *dst = rw + h * (D + 2);
+#pragma unroll
+                for (int b = 0; b < D / 16; ++b) {
+                    dst[16 * b + 2 * grp] = o[b][e];
+                    dst[16 * b + 2 * grp + 1] = o[b][2 + e];
+                }
+                if (grp == 0) {
+                    dst[D] = e ? m1 : m0;
+                    dst[D + 1] = e ? l1 : l0;
+                }
+            }
+        }
+        consumer_sync<CW>();
+        write_record<D, GM, CW>(red, P.partials + (size_t)r.rec * Gv * (D + 2), Gv);
+        consumer_sync<CW>();  // red is reused by the next item
+    }
+}
+
+template <int D, int GM, bool F8, int CW>
 __global__ void __launch_bounds__(32 * (1 + CW), 1)
     decode_split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                         const DecodeAttentionProblem P, float scale_log2, int n_items, unsigned *err)
 {
-    static_assert(!F8 || D == 128, "E4M3 caches: 128-wide heads");
     static_assert(CW % kGroup == 0, "whole groups of four consumer warps");
-    constexpr int NG = CW / kGroup;  // chunk it goes to group it % NG
-    using L = DSmem<D, F8, CW>;
-    static_assert(L::STAGES % NG == 0, "each ring stage must belong to one group (phase parity)");
+    using L = DSmem<D, GM, F8, CW>;
     static_assert(L::ALLOC <= 232448, "shared memory per CTA");
     constexpr int ST = L::STAGES;
-    constexpr int KS = D / 16;   // k-steps of the QK product
-    constexpr int NT = D / 8;    // n-tiles of the PV product
-    constexpr int REC = G * (D + 2);
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + L::BARS);
@@ -178,245 +561,26 @@ __global__ void __launch_bounds__(32 * (1 + CW), 1)
         }
         return;  // the producer takes no part in the consumer barriers below
     }
-
-    const int cwi = warp - 1;           // consumer warp index (partials slot)
-    const int grpi = cwi / kGroup;      // its group: chunks it with it % NG == grpi
-    const int cw = cwi % kGroup;        // keys [16 cw, 16 cw + 16) of each of its chunks
-    const int grp = lane >> 2, tig = lane & 3;
-    const bool row_valid = grp < G;     // MMA row grp = query head g*G + grp
-    // ldmatrix row addresses (relative to a chunk): lane i serves row i%8 of matrix i/8
-    const int mi = lane >> 3, mr = lane & 7;
-    const int qk_key = cw * 16 + (mi >> 1) * 8 + mr, qk_dofs = (mi & 1) * 8;  // K: (keys, d) blocks
-    const int pv_key = cw * 16 + (mi & 1) * 8 + mr, pv_dofs = (mi >> 1) * 8;  // V: transposed blocks
-    // E4M3: matrix mi covers keys 8*(mi&1).. of the warp and 16-byte block mi>>1 of the pair
-    const int f8_key = cw * 16 + (mi & 1) * 8 + mr, f8_blk = mi >> 1;
-
-    int it = 0;
-    for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
-        const ItemRange r = item_range(P, item, err, false);
-        // A fragments of Q (rows = heads of the group, binary16 split into bf16 hi + lo)
-        uint32_t qh[KS][2], ql[KS][2];
-        if constexpr (F8) {  // binary16 as it is, d in the fragment order described above
-            const uint16_t *qrow = P.q + ((size_t)(r.b * P.Hq + r.g * G + (row_valid ? grp : 0)) * D);
-#pragma unroll
-            for (int ks = 0; ks < KS; ++ks) {
-                uint2 v = make_uint2(0u, 0u);
-                if (row_valid) v = *reinterpret_cast<const uint2 *>(qrow + ks * 16 + 4 * tig);
-                qh[ks][0] = v.x;
-                qh[ks][1] = v.y;
-                ql[ks][0] = ql[ks][1] = 0u;
-            }
-        } else {
-            const uint16_t *qrow = P.q + ((size_t)(r.b * P.Hq + r.g * G + (row_valid ? grp : 0)) * D);
-#pragma unroll
-            for (int ks = 0; ks < KS; ++ks)
-#pragma unroll
-                for (int half = 0; half < 2; ++half) {
-                    float2 f = make_float2(0.0f, 0.0f);
-                    if (row_valid)
-                        f = __half22float2(*reinterpret_cast<const __half2 *>(qrow + ks * 16 + half * 8 + 2 * tig));
-                    const __nv_bfloat162 hi = __floats2bfloat162_rn(f.x, f.y);
-                    const float2 hf = __bfloat1622float2(hi);
-                    qh[ks][half] = *reinterpret_cast<const uint32_t *>(&hi);
-                    ql[ks][half] = bf16x2_bits(f.x - hf.x, f.y - hf.y);
-                }
-        }
-        float o[NT][4];
-#pragma unroll
-        for (int n = 0; n < NT; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.0f;
-        float m_run = -INFINITY, l_run = 0.0f;  // for row grp (scaled log2 domain)
-
-        for (int u0 = r.begin; u0 < r.end; u0 += kChunk, ++it) {
-            if (NG > 1 && it % NG != grpi) continue;  // another group's chunk
-            const int s = it % ST;
-            if (!mbar_wait(full + s, (it / ST) & 1, err)) break;
-            const uint32_t kb = smem_u32(smem + L::K + s * L::CB);
-            const uint32_t vb = smem_u32(smem + L::V + s * L::CB);
-            // Value rows past the item's last key may hold anything (slots past
-            // the sequence are not initialised); 0 * NaN would poison O, so the
-            // rows this warp reads are zeroed.  Masked scores need no such care.
-            if (u0 + kChunk > r.end) {
-                const int first = max(r.end - u0, cw * 16);
-                uint4 *vrow = reinterpret_cast<uint4 *>(smem + L::V + s * L::CB);
-                for (int idx = lane; idx < (cw * 16 + 16 - first) * L::NCH * 8; idx += 32) {
-                    const int key = first + idx / (L::NCH * 8), rem = idx % (L::NCH * 8);
-                    vrow[((rem >> 3) * L::BOX + key * 128) / 16 + (rem & 7)] = make_uint4(0, 0, 0, 0);
-                }
-                __syncwarp();
-            }
-            // S[heads x 16 keys] = Q K^T
-            float sc[2][4] = {{0.0f, 0.0f, 0.0f, 0.0f}, {0.0f, 0.0f, 0.0f, 0.0f}};
-            if constexpr (F8) {
-                // four independent accumulators (n-tile x k-step parity) halve the MMA chains
-                float sc2[2][4] = {{0.0f, 0.0f, 0.0f, 0.0f}, {0.0f, 0.0f, 0.0f, 0.0f}};
-#pragma unroll
-                for (int kp = 0; kp < KS / 2; ++kp) {  // two k-steps (32 codes) per ldmatrix
-                    uint32_t rk[4];  // (keys 0-7, k-step 2kp), (8-15, 2kp), (0-7, 2kp+1), (8-15, 2kp+1)
-                    ldsm_x4(kb + swz8(f8_key, (2 * kp + f8_blk) * 16), rk[0], rk[1], rk[2], rk[3]);
-                    uint32_t bk[4][2];
-#pragma unroll
-                    for (int m = 0; m < 4; ++m) e4m3x4_to_f16x4(rk[m], bk[m][0], bk[m][1]);
-                    mma_f16_16816(sc[0], qh[2 * kp][0], 0u, qh[2 * kp][1], 0u, bk[0][0], bk[0][1]);
-                    mma_f16_16816(sc[1], qh[2 * kp][0], 0u, qh[2 * kp][1], 0u, bk[1][0], bk[1][1]);
-                    mma_f16_16816(sc2[0], qh[2 * kp + 1][0], 0u, qh[2 * kp + 1][1], 0u, bk[2][0], bk[2][1]);
-                    mma_f16_16816(sc2[1], qh[2 * kp + 1][0], 0u, qh[2 * kp + 1][1], 0u, bk[3][0], bk[3][1]);
-                }
-#pragma unroll
-                for (int n = 0; n < 2; ++n) {
-                    sc[n][0] += sc2[n][0];
-                    sc[n][1] += sc2[n][1];
-                }
-            } else {
-#pragma unroll
-                for (int ks = 0; ks < KS; ++ks) {
-                    uint32_t b00, b01, b10, b11;
-                    ldsm_x4(kb + swz<D>(qk_key, ks * 16 + qk_dofs), b00, b01, b10, b11);
-                    mma_bf16_16816(sc[0], qh[ks][0], 0u, qh[ks][1], 0u, b00, b01);
-                    mma_bf16_16816(sc[1], qh[ks][0], 0u, qh[ks][1], 0u, b10, b11);
-                    mma_bf16_16816(sc[0], ql[ks][0], 0u, ql[ks][1], 0u, b00, b01);
-                    mma_bf16_16816(sc[1], ql[ks][0], 0u, ql[ks][1], 0u, b10, b11);
-                }
-            }
-            // mask keys beyond the item and take the row max over this warp's 16 keys
-            const int kbase = u0 + cw * 16 + 2 * tig;
-            float v[4] = {sc[0][0], sc[0][1], sc[1][0], sc[1][1]};  // keys kbase, +1, +8, +9
-            const int koff[4] = {0, 1, 8, 9};
-            float mx = -INFINITY;
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                v[e] = (kbase + koff[e] < r.end) ? v[e] * scale_log2 : -INFINITY;
-                mx = fmaxf(mx, v[e]);
-            }
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-            // F8: the running max moves only when a score passes it by more than
-            // 2^8 (P then stays <= 2^8, exact in binary16's range), so O is
-            // rescaled rarely; bf16: every time the max grows
-            float m_new = fmaxf(m_run, mx);
-            if (F8 && !(mx > m_run + 8.0f)) m_new = m_run;
-            const float m_use = (m_new == -INFINITY) ? 0.0f : m_new;
-            const float alpha = ex2(m_run - m_use);
-            m_run = m_new;
-            float p[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) p[e] = (v[e] == -INFINITY) ? 0.0f : ex2(v[e] - m_use);
-            l_run = l_run * alpha + (p[0] + p[1] + p[2] + p[3]);
-            // P as the A fragment of O += P V (rows 8..15 are padding), split
-            // into bf16 high and low parts so P keeps ~16 mantissa bits
-            uint32_t a0h = 0u, a2h = 0u, a0l = 0u, a2l = 0u;
-            if (F8 && row_valid) {  // binary16 (11-bit significand), one MMA per tile
-                a0h = pack_f16(p[0], p[1]);
-                a2h = pack_f16(p[2], p[3]);
-            } else if (row_valid) {
-                const __nv_bfloat162 h01 = __floats2bfloat162_rn(p[0], p[1]);
-                const __nv_bfloat162 h23 = __floats2bfloat162_rn(p[2], p[3]);
-                const float2 f01 = __bfloat1622float2(h01), f23 = __bfloat1622float2(h23);
-                a0h = *reinterpret_cast<const uint32_t *>(&h01);
-                a2h = *reinterpret_cast<const uint32_t *>(&h23);
-                a0l = bf16x2_bits(p[0] - f01.x, p[1] - f01.y);
-                a2l = bf16x2_bits(p[2] - f23.x, p[3] - f23.y);
-            }
-            if (!F8 || __any_sync(0xffffffffu, alpha != 1.0f)) {
-#pragma unroll
-                for (int n = 0; n < NT; ++n) {
-                    o[n][0] *= alpha;
-                    o[n][1] *= alpha;
-                }
-            }
-            if constexpr (F8) {
-#pragma unroll
-                for (int j2 = 0; j2 < D / 32; ++j2) {  // two 16-wide d blocks per ldmatrix
-                    uint32_t rv[4];  // (keys 0-7, block 2j2), (8-15, 2j2), (0-7, 2j2+1), (8-15, 2j2+1)
-                    ldsm_x4_trans(vb + swz8(f8_key, (2 * j2 + f8_blk) * 16), rv[0], rv[1], rv[2], rv[3]);
-                    uint32_t bv[4][2];  // n-tiles 4 j2 .. 4 j2 + 3: (even d, odd d) of blocks 2 j2, 2 j2 + 1
-#pragma unroll
-                    for (int x = 0; x < 2; ++x) {
-                        // bytes (k c, k c+1, k+1 c, k+1 c+1) -> (k c, k+1 c | k c+1, k+1 c+1)
-                        const uint32_t lo = prmt(rv[2 * x], 0u, 0x3120u), hi = prmt(rv[2 * x + 1], 0u, 0x3120u);
-                        e4m3x4_to_f16x4(lo, bv[2 * x][0], bv[2 * x + 1][0]);
-                        e4m3x4_to_f16x4(hi, bv[2 * x][1], bv[2 * x + 1][1]);
-                    }
-#pragma unroll
-                    for (int n = 0; n < 4; ++n) mma_f16_16816(o[4 * j2 + n], a0h, 0u, a2h, 0u, bv[n][0], bv[n][1]);
-                }
-            } else {
-#pragma unroll
-                for (int nb = 0; nb < NT / 2; ++nb) {
-                    uint32_t b0a, b1a, b0b, b1b;
-                    ldsm_x4_trans(vb + swz<D>(pv_key, nb * 16 + pv_dofs), b0a, b1a, b0b, b1b);
-                    mma_bf16_16816(o[2 * nb], a0h, 0u, a2h, 0u, b0a, b1a);
-                    mma_bf16_16816(o[2 * nb + 1], a0h, 0u, a2h, 0u, b0b, b1b);
-                    mma_bf16_16816(o[2 * nb], a0l, 0u, a2l, 0u, b0a, b1a);
-                    mma_bf16_16816(o[2 * nb + 1], a0l, 0u, a2l, 0u, b0b, b1b);
-                }
-            }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(empty + s);
-        }
-        // row sum over the four lanes of a row; the max is already row-uniform
-        l_run += __shfl_xor_sync(0xffffffffu, l_run, 1);
-        l_run += __shfl_xor_sync(0xffffffffu, l_run, 2);
-        float *rw = red + cwi * 8 * (D + 2);
-        if (row_valid) {
-            if constexpr (F8) {  // n-tile 2j: d = 16j + 4t + {0, 2}; n-tile 2j+1: d = 16j + 4t + {1, 3}
-#pragma unroll
-                for (int j = 0; j < NT / 2; ++j) {
-                    float *dst = rw + grp * (D + 2) + 16 * j + 4 * tig;
-                    dst[0] = o[2 * j][0];
-                    dst[1] = o[2 * j + 1][0];
-                    dst[2] = o[2 * j][1];
-                    dst[3] = o[2 * j + 1][1];
-                }
-            } else {
-#pragma unroll
-                for (int n = 0; n < NT; ++n) {
-                    rw[grp * (D + 2) + 8 * n + 2 * tig] = o[n][0];
-                    rw[grp * (D + 2) + 8 * n + 2 * tig + 1] = o[n][1];
-                }
-            }
-            if (tig == 0) {
-                rw[grp * (D + 2) + D] = m_run;
-                rw[grp * (D + 2) + D + 1] = l_run;
-            }
-        }
-        consumer_sync<CW>();
-        float *rec = P.partials + (size_t)item * REC;
-        for (int idx = threadIdx.x - 32; idx < G * D; idx += CW * 32) {
-            const int h = idx / D, c = idx - h * D;
-            float M = -INFINITY;
-#pragma unroll
-            for (int w = 0; w < CW; ++w) M = fmaxf(M, red[(w * 8 + h) * (D + 2) + D]);
-            const float Mu = (M == -INFINITY) ? 0.0f : M;
-            float acc = 0.0f, lsum = 0.0f;
-#pragma unroll
-            for (int w = 0; w < CW; ++w) {
-                const float* rr = red + (w * 8 + h) * (D + 2);
-                const float f = ex2(rr[D] - Mu);
-                acc = fmaf(f, rr[c], acc);
-                lsum = fmaf(f, rr[D + 1], lsum);
-            }
-            rec[h * (D + 2) + c] = acc;
-            if (c == 0) {
-                rec[h * (D + 2) + D] = M;
-                rec[h * (D + 2) + D + 1] = lsum;
-            }
-        }
-        consumer_sync<CW>();  // red is reused by the next item
-    }
+    if constexpr (F8)
+        consume_f8<D, CW>(P, smem, full, empty, red, scale_log2, n_items, err);
+    else
+        consume_bf16<D, GM, CW>(P, smem, full, empty, red, scale_log2, n_items, err);
 }
 
-// One CTA per (b, g): merge the splits and write bf16 attn.
-template <int D, int G>
+// One CTA per (b, head sub-group): merge the splits and write bf16 attn.
+template <int D>
 __global__ void __launch_bounds__(128) decode_combine_kernel(const DecodeAttentionProblem P)
 {
-    constexpr int REC = G * (D + 2);
+    const int Gv = P.Hq / P.Hkv / P.vsub;
+    const int REC = Gv * (D + 2);
     grid_dep_launch();
     grid_dep_wait();  // the split kernel's partial records
-    const int bg = blockIdx.x;
-    const int b = bg / P.Hkv, g = bg % P.Hkv;
-    const float *recs = P.partials + (size_t)bg * P.splits * REC;
-    for (int idx = threadIdx.x; idx < G * D; idx += blockDim.x) {
-        const int h = idx / D, c = idx % D;
+    const int bvg = blockIdx.x;
+    const int nvg = P.Hkv * P.vsub;
+    const int b = bvg / nvg, vg = bvg - b * nvg;
+    const float *recs = P.partials + (size_t)bvg * P.splits * REC;
+    for (int idx = threadIdx.x; idx < Gv * D; idx += blockDim.x) {
+        const int h = idx / D, c = idx - h * D;
         float M = -INFINITY;
         for (int s = 0; s < P.splits; ++s) M = fmaxf(M, recs[s * REC + h * (D + 2) + D]);
         const float Mu = (M == -INFINITY) ? 0.0f : M;
@@ -429,17 +593,19 @@ __global__ void __launch_bounds__(128) decode_combine_kernel(const DecodeAttenti
         }
         const float out = lsum > 0.0f ? acc / lsum * (P.fp8 ? P.v_scale : 1.0f) : 0.0f;
         const __nv_bfloat16 ob = __float2bfloat16_rn(out);
-        P.out[(size_t)b * P.Hq * D + (size_t)(g * G + h) * D + c] = *reinterpret_cast<const uint16_t *>(&ob);
+        P.out[(size_t)b * P.Hq * D + (size_t)(vg * Gv + h) * D + c] = *reinterpret_cast<const uint16_t *>(&ob);
     }
 }
 
-template <int D, int G, bool F8, int CW = (F8 ? 8 : 4)>
-cudaError_t run_decode(const DecodeAttentionProblem &p, unsigned *err, cudaStream_t stream)
+template <int D, int GM, bool F8, int CW = (F8 ? 8 : 4)>
+cudaError_t run_decode(const DecodeAttentionProblem &p0, unsigned *err, cudaStream_t stream)
 {
-    using L = DSmem<D, F8, CW>;
+    using L = DSmem<D, GM, F8, CW>;
+    DecodeAttentionProblem p = p0;
+    p.vsub = decode_head_subgroups(p.Hq / p.Hkv, GM);
     // E4M3 keys are code * k_scale: the scale joins the softmax scale
     const float scale_log2 = 1.4426950408889634f / sqrtf((float)D) * (F8 ? p.k_scale : 1.0f);
-    const int n_items = p.B * p.Hkv * p.splits;
+    const int n_items = p.B * p.Hkv * p.vsub * p.splits;
     int dev = 0, sms = 148;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
@@ -451,7 +617,7 @@ cudaError_t run_decode(const DecodeAttentionProblem &p, unsigned *err, cudaStrea
     const uint32_t box[3] = {(uint32_t)(128 / eb), (uint32_t)kChunk, 1};
     if (encode_tmap(&tk, p.k_cache, 3, dims, strides, box, true, eb) != CUDA_SUCCESS) return cudaErrorInvalidValue;
     if (encode_tmap(&tv, p.v_cache, 3, dims, strides, box, true, eb) != CUDA_SUCCESS) return cudaErrorInvalidValue;
-    auto kern = decode_split_kernel<D, G, F8, CW>;
+    auto kern = decode_split_kernel<D, GM, F8, CW>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC);
     if (e != cudaSuccess) return e;
     const int grid = n_items < sms ? n_items : sms;
@@ -463,25 +629,21 @@ cudaError_t run_decode(const DecodeAttentionProblem &p, unsigned *err, cudaStrea
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     // the combine follows the split kernel as its programmatic dependent
-    LaunchCfg lc(dim3(p.B * p.Hkv), dim3(128), 0, stream, true);
-    e = cudaLaunchKernelEx(&lc.cfg, decode_combine_kernel<D, G>, p);
+    LaunchCfg lc(dim3(p.B * p.Hkv * p.vsub), dim3(128), 0, stream, true);
+    e = cudaLaunchKernelEx(&lc.cfg, decode_combine_kernel<D>, p);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
-template <int D, bool F8>
-cudaError_t run_decode_d(const DecodeAttentionProblem &p, unsigned *err, cudaStream_t stream)
-{
-    switch (p.Hq / p.Hkv) {
-    case 1: return run_decode<D, 1, F8>(p, err, stream);
-    case 2: return run_decode<D, 2, F8>(p, err, stream);
-    case 4: return run_decode<D, 4, F8>(p, err, stream);
-    case 8: return run_decode<D, 8, F8>(p, err, stream);
-    default: return cudaErrorInvalidValue;
-    }
-}
-
 }  // namespace
+
+int decode_head_subgroups(int G, int gm)
+{
+    // the fewest sub-groups of equal size that hold at most gm heads each
+    for (int v = (G + gm - 1) / gm; v < G; ++v)
+        if (G % v == 0) return v;
+    return G;
+}
 
 int decode_choose_splits(int B, int Hkv, int Lmax, int num_sms)
 {
@@ -513,9 +675,11 @@ size_t decode_partials_floats(int B, int Hq, int splits, int d)
 
 cudaError_t launch_decode_attention(const DecodeAttentionProblem &p, unsigned *err, cudaStream_t stream)
 {
-    if (p.fp8) return p.d == 128 ? run_decode_d<128, true>(p, err, stream) : cudaErrorInvalidValue;
-    if (p.d == 128) return run_decode_d<128, false>(p, err, stream);
-    if (p.d == 64) return run_decode_d<64, false>(p, err, stream);
+    if (p.Hkv <= 0 || p.Hq % p.Hkv) return cudaErrorInvalidValue;
+    const int G = p.Hq / p.Hkv;
+    if (p.fp8) return p.d == 128 ? run_decode<128, 8, true>(p, err, stream) : cudaErrorInvalidValue;
+    if (p.d == 128) return G <= 8 ? run_decode<128, 8, false>(p, err, stream) : run_decode<128, 16, false>(p, err, stream);
+    if (p.d == 64) return G <= 8 ? run_decode<64, 8, false>(p, err, stream) : run_decode<64, 16, false>(p, err, stream);
     return cudaErrorInvalidValue;
 }
 

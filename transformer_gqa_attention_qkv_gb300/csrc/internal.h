@@ -146,7 +146,11 @@ struct DecodeAttentionProblem {
     float *partials;          // split partials (see decode_partials_floats)
     int splits;               // number of key splits per (b, kv head)
     int pdl;                  // launch the split kernel as the programmatic dependent of the previous kernel
+    int vsub;                 // set by the launcher: sub-groups of Hq/Hkv/vsub query heads per KV head
 };
+// Sub-groups a group of G query heads is taken as when a work item holds at
+// most gm of them (the fewest that divide G).
+int decode_head_subgroups(int G, int gm);
 int decode_choose_splits(int B, int Hkv, int Lmax, int num_sms);
 size_t decode_partials_floats(int B, int Hq, int splits, int d);
 cudaError_t launch_decode_attention(const DecodeAttentionProblem &p, unsigned *err, cudaStream_t stream);
