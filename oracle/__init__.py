@@ -70,6 +70,8 @@ def _load():
     lib.oracle_attention_stage.restype = _I
     lib.oracle_attention_stage.argtypes = [_u16p, _u16p, _u16p, _I, _L, _L, _L, _L, _L, _I,
                                            _i64p, _L, _f64p, _I]
+    lib.oracle_round_bf16.restype = _I
+    lib.oracle_round_bf16.argtypes = [_f64p, _L, _f64p]
     lib.oracle_f16_to_double.restype = None
     lib.oracle_f16_to_double.argtypes = [_u16p, _L, _f64p]
     lib.oracle_oproj_stage.restype = _I
@@ -235,6 +237,15 @@ def qkv_stage(x, Wqkv, q_norm_w, k_norm_w, rope_theta, eps, B, S, hidden, Hq, Hk
                                        _rd(rotary_dim, d), B, S, hidden, Hq, Hkv, d, _pf(q), _pf(k), _pf(v),
                                     threads or default_threads()), "qkv_stage")
     return q, k, v
+
+
+def round_bf16(x) -> np.ndarray:
+    """x (float64) rounded to the nearest bf16 value, ties to even: how a bf16
+    KV cache stores a new key or value (reading R21)."""
+    a = np.ascontiguousarray(np.asarray(x, dtype=np.float64))
+    out = np.empty_like(a)
+    _check(_load().oracle_round_bf16(_pf(a), a.size, _pf(out)), "round_bf16")
+    return out
 
 
 def f16_to_double(bits: np.ndarray) -> np.ndarray:

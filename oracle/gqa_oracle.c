@@ -46,6 +46,12 @@
  *      code to value / scale, ties to even, saturating at +-448; the new
  *      token's key and value are appended as codes and attended like the
  *      rest ("Head Dimension" article, §5.2: FP8 for the K, V cache).
+ *   R21 a bf16 KV cache (decode, prefill into a cache): the new tokens' keys
+ *      and values are stored in the cache as bf16 (nearest value, ties to
+ *      even) and attention reads them back from it, as it reads the earlier
+ *      entries ([T07] §4 step 5: the cache's update-and-fetch returns what the
+ *      cache holds and the attention of step 6 consumes that; R17 does the
+ *      same for an FP8 cache).
  *   R19 backward: the gradients are the derivatives of the forward steps
  *      above in reverse order (the pages print none); a KV head's K and V
  *      gradients sum over the query heads of its group.
@@ -69,6 +75,29 @@ static double bf(uint16_t h)
     float f;
     memcpy(&f, &u, sizeof f);
     return (double)f;
+}
+
+/* x rounded to the nearest bf16 value (8 significant bits, ties to even).
+ * bf16 has binary32's exponent range: below 2^-126 the spacing stays 2^-133
+ * (subnormals), and values rounding past the largest finite bf16,
+ * (2 - 2^-7) * 2^127, become infinite (R21). */
+static double round_bf16(double x)
+{
+    if (x == 0.0 || !isfinite(x)) return x;
+    int e;
+    frexp(x, &e);                   /* |x| in [2^(e-1), 2^e) */
+    if (e < -125) e = -125;
+    double q = ldexp(1.0, e - 8);   /* spacing of 8 significant bits */
+    double r = nearbyint(x / q) * q;
+    if (fabs(r) > 0x1.fep127) return copysign(INFINITY, x);
+    return r;
+}
+
+int oracle_round_bf16(const double *x, long n, double *out)
+{
+    if (!x || !out || n < 0) return ORACLE_EARG;
+    for (long i = 0; i < n; ++i) out[i] = round_bf16(x[i]);
+    return ORACLE_OK;
 }
 
 /* IEEE binary16 bit pattern -> double, exact (subnormals, infinities, NaN). */
@@ -526,10 +555,11 @@ int oracle_decode_attention_stage(const uint16_t *q, int q_f16, const uint16_t *
 
 /* The whole decode step ([T07] §4 steps 1-7 with L = 1): for each sequence
  * b the new token sits at position p = cache_len[b]; its Q/K are normed and
- * rotated at p; its K/V join the cached entries [0, p) (read from the bf16
- * cache, which this function does not modify) and the query attends to all
- * p+1 keys.  x [B, hidden]; out [B, hidden].  Optional outputs:
- * q_new [B,Hq,d], k_new/v_new [B,Hkv,d], attn [B,Hq*d]. */
+ * rotated at p; its K/V, as the bf16 cache stores them (R21), join the
+ * cached entries [0, p) (read from the bf16 cache, which this function does
+ * not modify) and the query attends to all p+1 keys.  x [B, hidden];
+ * out [B, hidden].  Optional outputs: q_new [B,Hq,d], k_new/v_new [B,Hkv,d]
+ * (the new cache entries), attn [B,Hq*d]. */
 int oracle_decode_rd(const uint16_t *x, const uint16_t *Wqkv, const uint16_t *Wo,
                   const uint16_t *q_norm_w, const uint16_t *k_norm_w,
                   double rope_theta, double eps, long rd,
@@ -565,6 +595,8 @@ int oracle_decode_rd(const uint16_t *x, const uint16_t *Wqkv, const uint16_t *Wo
             if (k_norm_w) rmsnorm_head(row + NQ + g * d, d, k_norm_w, eps);
             rope_head(row + NQ + g * d, rd, p, rope_theta);
         }
+        /* R21: the new key and value as the bf16 cache holds them */
+        for (long c = NQ; c < N; ++c) row[c] = round_bf16(row[c]);
     }
 
 #pragma omp parallel for collapse(2) schedule(dynamic, 1)
@@ -610,10 +642,12 @@ int oracle_decode_rd(const uint16_t *x, const uint16_t *Wqkv, const uint16_t *Wo
  * history; [Part]: position encodings and masks use the same global token
  * positions).  Keys and values [0, p0[b]) come from the bf16 caches
  * [B, Hkv, Lmax, d] (not modified here); the new tokens' keys and values are
- * computed in double.  Query t attends to keys u <= p0[b] + t (causal) or to
- * all p0[b] + S keys.  x [B, S, hidden]; out [B, S, hidden].  Optional:
- * k_new/v_new [B, Hkv, S, d] and attn [B, S, Hq*d].  With p0 = 0 this is the
- * plain prefill; with S = 1 it is the decode step. */
+ * computed in double and attended as the bf16 cache stores them (R21).  Query
+ * t attends to keys u <= p0[b] + t (causal) or to all p0[b] + S keys.
+ * x [B, S, hidden]; out [B, S, hidden].  Optional: k_new/v_new [B, Hkv, S, d]
+ * (the new cache entries) and attn [B, S, Hq*d].  With p0 = 0 this is the
+ * plain prefill with K and V rounded to bf16; with S = 1 it is the decode
+ * step. */
 int oracle_prefill_cached_rd(const uint16_t *x, const uint16_t *Wqkv, const uint16_t *Wo,
                           const uint16_t *q_norm_w, const uint16_t *k_norm_w,
                           double rope_theta, double eps, long rd,
@@ -653,8 +687,11 @@ int oracle_prefill_cached_rd(const uint16_t *x, const uint16_t *Wqkv, const uint
             double *k = row + NQ + g * d;
             if (k_norm_w) rmsnorm_head(k, d, k_norm_w, eps);
             rope_head(k, rd, pos, rope_theta);
-            memcpy(Kn + ((b * Hkv + g) * S + t) * d, k, (size_t)d * sizeof(double));
-            memcpy(Vn + ((b * Hkv + g) * S + t) * d, row + NQ + NKV + g * d, (size_t)d * sizeof(double));
+            /* R21: the new key and value as the bf16 cache holds them */
+            for (long c = 0; c < d; ++c) {
+                Kn[((b * Hkv + g) * S + t) * d + c] = round_bf16(k[c]);
+                Vn[((b * Hkv + g) * S + t) * d + c] = round_bf16(row[NQ + NKV + g * d + c]);
+            }
         }
     }
 

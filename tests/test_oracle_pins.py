@@ -36,6 +36,16 @@ def f64(t):
     return t.float().double()
 
 
+def _bf16_rne(x):
+    """float64 -> nearest bf16 value, ties to even, written out with numpy
+    (8 significant bits: spacing 2^(e-8) for |x| in [2^(e-1), 2^e); np.round
+    rounds halves to even).  Finite values inside bf16's normal range only."""
+    x = np.asarray(x, dtype=np.float64)
+    _, e = np.frexp(x)
+    q = np.ldexp(1.0, e - 8)
+    return np.round(x / q) * q
+
+
 # ----------------------------------------------------------------- geometry / cost
 
 def test_geometry_matches_pages():
@@ -426,6 +436,36 @@ def test_forward_value_only_weights():
 
 # ----------------------------------------------------------------- decode
 
+def test_round_bf16_is_nearest_even():
+    """R21: a new key or value enters a bf16 cache as the nearest bf16 value,
+    ties to even.  Against torch's binary32 -> bf16 conversion on values that
+    binary32 holds exactly, the numpy restatement on arbitrary doubles, and
+    closed forms: halfway cases go to the even neighbour, a double just above
+    a halfway point rounds up (directly, not through binary32, which would make
+    it a tie), bf16 subnormals keep the 2^-133 spacing, and a value past the
+    largest finite bf16 by half a step or more becomes infinite."""
+    rng = np.random.default_rng(41)
+    f32 = (rng.standard_normal(4096) * np.exp2(rng.integers(-30, 30, 4096))).astype(np.float32).astype(np.float64)
+    lib = torch.from_numpy(f32).float().to(torch.bfloat16).double().numpy()
+    np.testing.assert_array_equal(oracle.round_bf16(f32), lib)
+    x = rng.standard_normal(4096) * 3.0
+    np.testing.assert_array_equal(oracle.round_bf16(x), _bf16_rne(x))
+    one = 1.0
+    cases = {
+        one + 2.0 ** -8: one,                             # halfway between 1 and 1 + 2^-7: even is 1
+        one + 3 * 2.0 ** -8: one + 2.0 ** -6,             # halfway, odd below: up to 1 + 2^-6
+        one + 2.0 ** -8 + 2.0 ** -40: one + 2.0 ** -7,    # just above halfway (not a binary32 value)
+        -(one + 2.0 ** -8 + 2.0 ** -40): -(one + 2.0 ** -7),
+        3.0 * 2.0 ** -135: 2.0 ** -133,                   # subnormal range: 0.75 of the 2^-133 spacing rounds up
+        2.0 ** -135: 0.0,                                  # and 0.25 of it rounds down to zero
+        0.0: 0.0,
+        (2 - 2.0 ** -7) * 2.0 ** 127: (2 - 2.0 ** -7) * 2.0 ** 127,
+        (2 - 2.0 ** -8) * 2.0 ** 127: math.inf,           # halfway to 2^128: ties to even overflow
+    }
+    got = oracle.round_bf16(np.array(list(cases)))
+    np.testing.assert_array_equal(got, np.array(list(cases.values())))
+
+
 def test_decode_matches_prefill_last_token():
     """[T07] §4 step 5 (the cache returns the whole history) and the RoPE
     offset: decoding token S-1 over a cache holding the prefill's keys and
@@ -445,7 +485,8 @@ def test_decode_matches_prefill_last_token():
                         [S - 1] * B, Lmax, threads=T)
     last = pre["out"].reshape(B, S, -1)[:, S - 1]
     np.testing.assert_allclose(dec["out"], last, rtol=0, atol=2e-2 * np.abs(last).max())
-    np.testing.assert_allclose(dec["k"], pre["k"][:, :, S - 1], rtol=1e-12, atol=1e-13)
+    # the new key as the bf16 cache stores it (R21)
+    np.testing.assert_allclose(dec["k"], _bf16_rne(pre["k"][:, :, S - 1]), rtol=1e-12, atol=1e-13)
     # a decode at the wrong position (S instead of S-1) must disagree clearly
     wrong = oracle.decode(t["x"][:, S - 1], t["Wqkv"], t["Wo"], t["q_norm_w"], t["k_norm_w"],
                           cfg.rope_theta, cfg.eps, B, cfg.hidden, Hq, Hkv, d, kc, vc,
@@ -492,17 +533,26 @@ def _empty_cache(B, Hkv, Lmax, d):
 
 
 def test_prefill_cached_at_offset_zero_is_the_plain_prefill():
-    """With nothing cached (p0 = 0) the cached prefill is the plain layer."""
+    """With nothing cached (p0 = 0) the cached prefill is the plain layer whose
+    keys and values pass through the bf16 cache (R21: attention reads what the
+    cache holds): the float64 torch composition with K and V rounded to bf16
+    after RoPE.  Without the rounding the two differ by far more than the
+    composition's own error."""
     cfg = _tiny(S=21)
     t = make_layer_inputs(cfg, seed=19, w_std=0.3)
     kc, vc = _empty_cache(cfg.B, cfg.Hkv, 32, cfg.head_dim)
     got = oracle.prefill_cached(t["x"], t["Wqkv"], t["Wo"], t["q_norm_w"], t["k_norm_w"], cfg.rope_theta, cfg.eps,
                                 cfg.B, cfg.S, cfg.hidden, cfg.Hq, cfg.Hkv, cfg.head_dim, kc, vc, [0] * cfg.B, 32,
                                 threads=T)
-    ref = _fwd(cfg, t, want_stages=True)
-    np.testing.assert_allclose(got["out"], ref["out"], rtol=1e-13, atol=1e-13)
-    np.testing.assert_allclose(got["k"], ref["k"], rtol=1e-13, atol=1e-13)
-    np.testing.assert_allclose(got["attn"], ref["attn"], rtol=1e-13, atol=1e-13)
+    keep = {}
+    _, out = _torch_layer(cfg, t, keep=keep, kv_round=lambda a: torch.from_numpy(_bf16_rne(a.detach().numpy())))
+    B, S, h = cfg.B, cfg.S, cfg.hidden
+    np.testing.assert_allclose(got["out"], out.detach().reshape(B * S, h).numpy(), rtol=1e-11, atol=1e-11)
+    np.testing.assert_allclose(got["attn"], keep["attn"].detach().reshape(B * S, -1).numpy(), rtol=1e-11, atol=1e-11)
+    np.testing.assert_allclose(got["k"], keep["k"].detach().numpy(), rtol=0, atol=0)
+    np.testing.assert_allclose(got["v"], keep["v"].detach().numpy(), rtol=0, atol=0)
+    plain = _fwd(cfg, t, want_stages=True)
+    assert np.abs(got["attn"] - plain["attn"]).max() > 1e-5
 
 
 def test_prefill_cached_single_token_is_the_decode_step():
@@ -538,7 +588,7 @@ def test_prefill_in_two_chunks_matches_one_prefill():
                                 kc, vc, [S1] * cfg.B, Lmax, threads=T)
     ref = full["out"].reshape(cfg.B, cfg.S, -1)[:, S1:].reshape(-1, cfg.hidden)
     np.testing.assert_allclose(got["out"], ref, rtol=0, atol=2e-2 * np.abs(ref).max())
-    np.testing.assert_allclose(got["k"], full["k"][:, :, S1:], rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(got["k"], _bf16_rne(full["k"][:, :, S1:]), rtol=1e-12, atol=1e-13)
     # the wrong offset is caught
     bad = oracle.prefill_cached(t["x"][:, S1:].contiguous(), t["Wqkv"], t["Wo"], t["q_norm_w"], t["k_norm_w"],
                                 cfg.rope_theta, cfg.eps, cfg.B, S2, cfg.hidden, cfg.Hq, cfg.Hkv, cfg.head_dim,
@@ -641,12 +691,17 @@ def test_forward_partial_rotary_equals_library_composition():
         kc, vc = _empty_cache(B, Hkv, 32, d)
         pc = oracle.prefill_cached(t["x"], t["Wqkv"], t["Wo"], t["q_norm_w"], t["k_norm_w"], cfg.rope_theta,
                                    cfg.eps, B, S, h, Hq, Hkv, d, kc, vc, [0] * B, 32, threads=T, rotary_dim=rd)
-        np.testing.assert_allclose(pc["out"], ref, rtol=1e-11, atol=1e-11)
+        # the cached prefill attends over K and V as the bf16 cache stores them (R21)
+        kr, vr = torch.from_numpy(_bf16_rne(k.numpy())), torch.from_numpy(_bf16_rne(v.numpy()))
+        ar = F.scaled_dot_product_attention(q, kr.repeat_interleave(Hq // Hkv, 1),
+                                            vr.repeat_interleave(Hq // Hkv, 1), is_causal=True)
+        ref_c = (x + F.linear(ar.transpose(1, 2).reshape(B, S, Hq * d), Wo)).reshape(B * S, h).numpy()
+        np.testing.assert_allclose(pc["out"], ref_c, rtol=1e-11, atol=1e-11)
         kc[:, :, :S - 1] = torch.from_numpy(got["k"][:, :, :S - 1]).to(torch.bfloat16)
         vc[:, :, :S - 1] = torch.from_numpy(got["v"][:, :, :S - 1]).to(torch.bfloat16)
         dec = oracle.decode(t["x"][:, S - 1], t["Wqkv"], t["Wo"], t["q_norm_w"], t["k_norm_w"], cfg.rope_theta,
                             cfg.eps, B, h, Hq, Hkv, d, kc, vc, [S - 1] * B, 32, threads=T, rotary_dim=rd)
-        np.testing.assert_allclose(dec["k"], got["k"][:, :, S - 1], rtol=1e-12, atol=1e-13)
+        np.testing.assert_allclose(dec["k"], _bf16_rne(got["k"][:, :, S - 1]), rtol=1e-12, atol=1e-13)
         last = got["out"].reshape(B, S, -1)[:, S - 1]
         np.testing.assert_allclose(dec["out"], last, rtol=0, atol=2e-2 * np.abs(last).max())
 
@@ -755,12 +810,12 @@ def test_fp8_decode_step_equals_library_composition():
                             Hq, Hkv, d, kc8, vc8, ks, vs, cl, Lmax, threads=T)
     np.testing.assert_array_equal(got["k_code"], oracle.e4m3_encode(got["k"] / ks))
     np.testing.assert_array_equal(got["v_code"], oracle.e4m3_encode(got["v"] / vs))
-    # the bf16 decode computes the same q, k, v before quantisation
+    # the bf16 decode computes the same q, k, v before its cache's bf16 rounding (R21)
     ref_bf = oracle.decode(x1, t["Wqkv"], t["Wo"], t["q_norm_w"], t["k_norm_w"], cfg.rope_theta, cfg.eps, B, h,
                            Hq, Hkv, d, bf16(np.zeros((B, Hkv, Lmax, d))), bf16(np.zeros((B, Hkv, Lmax, d))), cl,
                            Lmax, threads=T)
     np.testing.assert_allclose(got["q"], ref_bf["q"], rtol=1e-13, atol=1e-14)
-    np.testing.assert_allclose(got["k"], ref_bf["k"], rtol=1e-13, atol=1e-14)
+    np.testing.assert_allclose(_bf16_rne(got["k"]), ref_bf["k"], rtol=1e-13, atol=1e-14)
     kd = oracle.e4m3_decode(kc8) * ks
     vd = oracle.e4m3_decode(vc8) * vs
     for b in range(B):
@@ -778,10 +833,11 @@ def test_fp8_decode_step_equals_library_composition():
 
 # ----------------------------------------------------------------- backward
 
-def _torch_layer(cfg, t, causal=True, keep=None):
+def _torch_layer(cfg, t, causal=True, keep=None, kv_round=None):
     """The layer as a float64 torch composition (F.linear, F.rms_norm, complex
     RoPE, SDPA); parameters are leaves with requires_grad.  keep (a dict)
-    receives the attention's q, k, v and attn with retained gradients."""
+    receives the attention's q, k, v and attn with retained gradients.
+    kv_round (forward only): applied to K and V after RoPE."""
     B, S, h, Hq, Hkv, d = cfg.B, cfg.S, cfg.hidden, cfg.Hq, cfg.Hkv, cfg.head_dim
     leaves = {k: f64(v).requires_grad_(True) for k, v in t.items() if v is not None}
     x, W, Wo = leaves["x"], leaves["Wqkv"], leaves["Wo"]
@@ -795,15 +851,20 @@ def _torch_layer(cfg, t, causal=True, keep=None):
     q = _complex_rope(q, pos, cfg.rope_theta, d).transpose(1, 2)
     k = _complex_rope(k, pos, cfg.rope_theta, d).transpose(1, 2)
     v = v.transpose(1, 2)
-    if keep is not None:
+    if kv_round is not None:
+        k, v = kv_round(k), kv_round(v)
+    if keep is not None and kv_round is None:
         for name, tt in (("q", q), ("k", k), ("v", v)):
             tt.retain_grad()
             keep[name] = tt
+    elif keep is not None:
+        keep.update(q=q, k=k, v=v)
     a = F.scaled_dot_product_attention(q, k.repeat_interleave(Hq // Hkv, 1), v.repeat_interleave(Hq // Hkv, 1),
                                        is_causal=causal)
     a = a.transpose(1, 2).reshape(B, S, Hq * d)
     if keep is not None:
-        a.retain_grad()
+        if a.requires_grad:
+            a.retain_grad()
         keep["attn"] = a
     return leaves, x + F.linear(a, Wo)
 
