@@ -468,7 +468,7 @@ def run_ours(args, world, rank, local):
         vc = torch.randn((1, cc.Hkv, Lmax, cc.head_dim), generator=gen, device=dev).to(torch.bfloat16)
         cl = torch.full((1,), p0, dtype=torch.int32, device=dev)
         cout = torch.empty_like(ct["x"])
-        cws = gq.new_workspace(gq.gqa_attn_prefill_cached_workspace_size(1, cc.S, cc.Hq, cc.head_dim), dev)
+        cws = gq.new_workspace(gq.gqa_attn_prefill_cached_workspace_size(1, cc.S, cc.Hq, cc.Hkv, cc.head_dim, Lmax), dev)
         cf = (2 * cc.S * (cc.Hq + 2 * cc.Hkv) * cc.head_dim * cc.hidden
               + 4 * cc.Hq * cc.head_dim * (cc.S * p0 + cc.S * (cc.S + 1) // 2)
               + 2 * cc.S * cc.hidden * cc.Hq * cc.head_dim)

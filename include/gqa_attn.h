@@ -173,14 +173,16 @@ int gqa_oproj_residual(const gqa_bf16 *attn, const gqa_bf16 *Wo, const gqa_bf16 
 
 /* ---------------------------------------------------- prefill into a cache */
 
-/* Bytes of workspace gqa_attn_prefill_cached needs: Q [B,Hq,S,d] and attn
- * [B,S,Hq*d], both bf16, and room for the attention's two key splits (their
- * binary16 outputs [2][B,S,Hq*d] and fp32 log2-sum-exp rows [2][B*Hq,S]), each
- * 256-byte aligned.  The keys are split when the attention would otherwise
- * run fewer than eight waves of work items on the GPU (B*Hq*S/256 items
- * against the SM count); a binary16 partial beyond +-65504 is clamped and
- * reported as GQA_ERR_RANGE. */
-size_t gqa_attn_prefill_cached_workspace_size(int B, int S, int Hq, int head_dim);
+/* Bytes of workspace gqa_attn_prefill_cached needs, each part 256-byte
+ * aligned: Q [B,Hq,S,d] binary16 and attn [B,S,Hq*d] bf16; room for the
+ * attention's two key splits (their binary16 outputs [2][B,S,Hq*d] and fp32
+ * log2-sum-exp rows [2][B*Hq,S]); and binary16 copies of both caches
+ * [B,Hkv,Lmax,d], of which the call fills the rows it attends.  The keys are
+ * split when the attention would otherwise run fewer than eight waves of work
+ * items on the GPU (B*Hq*S/256 items against the SM count); a binary16 partial
+ * beyond +-65504 is clamped and reported as GQA_ERR_RANGE.  Returns 0 for
+ * invalid sizes. */
+size_t gqa_attn_prefill_cached_workspace_size(int B, int S, int Hq, int Hkv, int head_dim, int Lmax);
 
 /* Chunked prefill: S new tokens per sequence appended to a KV cache
  * ([T07] §4: RoPE at the position offsets, step 5 the cache returns the
@@ -197,8 +199,13 @@ size_t gqa_attn_prefill_cached_workspace_size(int B, int S, int Hq, int head_dim
  *              cache_len[b] + S keys
  *   out        [B, S, hidden] = x + o_proj(attn)
  * With cache_len = 0 this is the plain prefill that also fills the cache.
- * Q meets the bf16 cache in the score MMA, so on this path Q and P are bf16
- * (the plain prefill keeps binary16). */
+ * Q and P are binary16 as in the plain prefill: after the projection a
+ * streaming kernel copies cache rows [0, cache_len[b] + S) of both caches,
+ * widened to binary16, into the workspace (exact for every bf16 value below
+ * 2^16; a cached value beyond +-65504 is saturated and reported as
+ * GQA_ERR_RANGE by gqa_check_device_error), and the attention reads those
+ * copies.  Cache slots past cache_len[b] + S are never read as keys or
+ * values, whatever they hold. */
 int gqa_attn_prefill_cached(const gqa_bf16 *x, const gqa_bf16 *Wqkv, const gqa_bf16 *Wo,
                             const gqa_bf16 *q_norm_w, const gqa_bf16 *k_norm_w,
                             float rope_theta, float eps,
@@ -206,12 +213,19 @@ int gqa_attn_prefill_cached(const gqa_bf16 *x, const gqa_bf16 *Wqkv, const gqa_b
                             gqa_bf16 *k_cache, gqa_bf16 *v_cache, const int *cache_len, int Lmax,
                             gqa_bf16 *out, void *workspace, size_t workspace_bytes, void *stream);
 
-/* Its attention stage alone: q [B, Hq, S, head_dim] bf16 (positions
- * cache_len[b] + t) over keys [0, cache_len[b] + S) of the caches (the new
- * tokens' keys already appended); attn_out [B, S, Hq*head_dim] bf16. */
-int gqa_attention_cached(const gqa_bf16 *q, const gqa_bf16 *k_cache, const gqa_bf16 *v_cache,
+/* Bytes of workspace gqa_attention_cached needs: binary16 copies of both
+ * caches [B,Hkv,Lmax,d], each 256-byte aligned.  0 for invalid sizes. */
+size_t gqa_attention_cached_workspace_size(int B, int Hkv, int head_dim, int Lmax);
+
+/* Its attention stage alone (the widening copy, then the attention):
+ * q [B, Hq, S, head_dim] binary16 (positions cache_len[b] + t) over keys
+ * [0, cache_len[b] + S) of the bf16 caches (the new tokens' keys already
+ * appended); attn_out [B, S, Hq*head_dim] bf16; workspace at least
+ * gqa_attention_cached_workspace_size(...) bytes, 256-byte aligned. */
+int gqa_attention_cached(const gqa_f16 *q, const gqa_bf16 *k_cache, const gqa_bf16 *v_cache,
                          const int *cache_len, int B, int S, int Hq, int Hkv, int head_dim, int Lmax,
-                         int causal, gqa_bf16 *attn_out, void *stream);
+                         int causal, gqa_bf16 *attn_out, void *workspace, size_t workspace_bytes,
+                         void *stream);
 
 /* ------------------------------------------------------------------- decode */
 

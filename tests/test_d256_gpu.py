@@ -86,7 +86,7 @@ def test_attention_cached_d256():
     B, S, Hq, Hkv, Lmax = 2, 100, 4, 1, 400
     p0 = [0, 237]
     g = torch.Generator().manual_seed(2100)
-    q = (torch.randn((B, Hq, S, D), generator=g) * 1.5).to(torch.bfloat16)
+    q = (torch.randn((B, Hq, S, D), generator=g) * 1.5).to(torch.float16)
     kc = (torch.randn((B, Hkv, Lmax, D), generator=g) * 1.5).to(torch.bfloat16)
     vc = torch.randn((B, Hkv, Lmax, D), generator=g).to(torch.bfloat16)
     cl = torch.tensor(p0, dtype=torch.int32)
@@ -98,8 +98,7 @@ def test_attention_cached_d256():
     for t in range(S):
         ref[:, t] = oracle.decode_attention_stage(q[:, :, t].contiguous(), kc, vc, [p + t + 1 for p in p0],
                                                   B, Hq, Hkv, D, Lmax)
-    # bf16 Q and P on the cached path (as for the narrower heads)
-    assert_parity("cached attn d256", to64(out).reshape(B, S, -1), ref, tol_rel=4e-3)
+    assert_parity("cached attn d256", to64(out).reshape(B, S, -1), ref)
 
 
 @pytest.mark.parametrize("rd", [256, 64, 0])

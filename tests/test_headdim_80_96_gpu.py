@@ -93,7 +93,7 @@ def test_attention_cached(D):
     B, S, Hq, Hkv, Lmax = 2, 100, 8, 2, 400
     p0 = [0, 237]
     g = torch.Generator().manual_seed(4200 + D)
-    q = bf16_randn((B, Hq, S, D), g, 1.5)
+    q = (torch.randn((B, Hq, S, D), generator=g) * 1.5).to(torch.float16)
     kc = bf16_randn((B, Hkv, Lmax, D), g, 1.5)
     vc = bf16_randn((B, Hkv, Lmax, D), g)
     cl = torch.tensor(p0, dtype=torch.int32)
@@ -105,7 +105,7 @@ def test_attention_cached(D):
     for t in range(S):
         ref[:, t] = oracle.decode_attention_stage(q[:, :, t].contiguous(), kc, vc, [p + t + 1 for p in p0],
                                                   B, Hq, Hkv, D, Lmax)
-    assert_parity(f"cached attn d{D}", to64(out).reshape(B, S, -1), ref, tol_rel=4e-3)
+    assert_parity(f"cached attn d{D}", to64(out).reshape(B, S, -1), ref)
 
 
 @pytest.mark.parametrize("D,rd", [(80, 80), (80, 40), (80, 20), (80, 0), (96, 96), (96, 48), (96, 24), (96, 0)])
@@ -157,7 +157,7 @@ def test_prefill_cached_layer(D):
         vc[b, :, :p] = bf16_randn((cfg.Hkv, p, D), g)
     kd, vd = dev(kc), dev(vc)
     out = torch.empty((cfg.B, cfg.S, cfg.hidden), dtype=torch.bfloat16, device=DEV)
-    ws = gq.new_workspace(gq.gqa_attn_prefill_cached_workspace_size(cfg.B, cfg.S, cfg.Hq, D))
+    ws = gq.new_workspace(gq.gqa_attn_prefill_cached_workspace_size(cfg.B, cfg.S, cfg.Hq, cfg.Hkv, D, Lmax))
     gq.gqa_attn_prefill_cached(dev(t["x"]), dev(t["Wqkv"]), dev(t["Wo"]), dev(t["q_norm_w"]), dev(t["k_norm_w"]),
                                cfg.rope_theta, cfg.eps, cfg.B, cfg.S, cfg.hidden, cfg.Hq, cfg.Hkv, D, True,
                                kd, vd, dev(torch.tensor(p0, dtype=torch.int32)), Lmax, out, ws)

@@ -150,7 +150,7 @@ def test_prefill_cached_partial_rotary():
         vc[b, :, :p] = torch.randn((cfg.Hkv, p, cfg.head_dim), generator=g).to(torch.bfloat16)
     kd, vd = dev(kc), dev(vc)
     out = torch.empty((cfg.B, cfg.S, cfg.hidden), dtype=torch.bfloat16, device=DEV)
-    ws = gq.new_workspace(gq.gqa_attn_prefill_cached_workspace_size(cfg.B, cfg.S, cfg.Hq, cfg.head_dim))
+    ws = gq.new_workspace(gq.gqa_attn_prefill_cached_workspace_size(cfg.B, cfg.S, cfg.Hq, cfg.Hkv, cfg.head_dim, Lmax))
     gq.gqa_attn_prefill_cached_rd(dev(t["x"]), dev(t["Wqkv"]), dev(t["Wo"]), dev(t["q_norm_w"]),
                                   dev(t["k_norm_w"]), cfg.rope_theta, cfg.eps, rd, cfg.B, cfg.S, cfg.hidden, cfg.Hq,
                                   cfg.Hkv, cfg.head_dim, True, kd, vd, dev(torch.tensor(p0, dtype=torch.int32)),

@@ -32,6 +32,7 @@ EXPORTS = (
     "gqa_attn_cost", "gqa_last_error", "gqa_check_device_error", "gqa_selftest_bounded_wait",
     "gqa_last_launch_count", "gqa_decode_attention_noalloc",
     "gqa_attn_prefill_cached_workspace_size", "gqa_attn_prefill_cached", "gqa_attention_cached",
+    "gqa_attention_cached_workspace_size",
     "gqa_attn_forward_rd", "gqa_qkv_proj_rd", "gqa_attn_prefill_cached_rd", "gqa_attn_decode_rd",
     "gqa_decode_qkv_rd", "gqa_attn_decode_fp8", "gqa_decode_qkv_fp8", "gqa_decode_attention_fp8",
     "gqa_attn_backward_workspace_size", "gqa_attn_backward", "gqa_attention_backward_workspace_size",
@@ -83,9 +84,10 @@ def lib():
         "gqa_selftest_bounded_wait": (_I, [_I]),
         "gqa_last_launch_count": (_I, []),
         "gqa_decode_attention_noalloc": (_I, [_P] * 4 + [_I] * 5 + [_P, _P]),
-        "gqa_attn_prefill_cached_workspace_size": (_Z, [_I] * 4),
+        "gqa_attn_prefill_cached_workspace_size": (_Z, [_I] * 6),
+        "gqa_attention_cached_workspace_size": (_Z, [_I] * 4),
         "gqa_attn_prefill_cached": (_I, [_P] * 5 + [_F, _F] + [_I] * 7 + [_P, _P, _P, _I, _P, _P, _Z, _P]),
-        "gqa_attention_cached": (_I, [_P] * 4 + [_I] * 7 + [_P, _P]),
+        "gqa_attention_cached": (_I, [_P] * 4 + [_I] * 7 + [_P, _P, _Z, _P]),
     }
     # the *_rd forms: rotary_dim (int) right after rope_theta and eps
     for base, name in (("gqa_attn_forward_ex", "gqa_attn_forward_rd"), ("gqa_qkv_proj", "gqa_qkv_proj_rd"),
@@ -276,8 +278,12 @@ def gqa_oproj_residual(attn, Wo, x, M, hidden, q_width, out, stream=None):
 
 # ------------------------------------------------------ prefill into a cache
 
-def gqa_attn_prefill_cached_workspace_size(B, S, Hq, head_dim) -> int:
-    return int(lib().gqa_attn_prefill_cached_workspace_size(B, S, Hq, head_dim))
+def gqa_attn_prefill_cached_workspace_size(B, S, Hq, Hkv, head_dim, Lmax) -> int:
+    return int(lib().gqa_attn_prefill_cached_workspace_size(B, S, Hq, Hkv, head_dim, Lmax))
+
+
+def gqa_attention_cached_workspace_size(B, Hkv, head_dim, Lmax) -> int:
+    return int(lib().gqa_attention_cached_workspace_size(B, Hkv, head_dim, Lmax))
 
 
 def gqa_attn_prefill_cached(x, Wqkv, Wo, q_norm_w, k_norm_w, rope_theta, eps, B, S, hidden, Hq, Hkv, head_dim,
@@ -291,9 +297,13 @@ def gqa_attn_prefill_cached(x, Wqkv, Wo, q_norm_w, k_norm_w, rope_theta, eps, B,
 
 
 def gqa_attention_cached(q, k_cache, v_cache, cache_len, B, S, Hq, Hkv, head_dim, Lmax, causal, attn_out,
-                         stream=None):
-    _check(lib().gqa_attention_cached(_bf16(q), _bf16(k_cache), _bf16(v_cache), _i32(cache_len), B, S, Hq, Hkv,
-                                      head_dim, Lmax, int(causal), _bf16(attn_out), _stream(stream)))
+                         workspace=None, stream=None):
+    """workspace: None allocates one of gqa_attention_cached_workspace_size bytes."""
+    if workspace is None:
+        workspace = new_workspace(gqa_attention_cached_workspace_size(B, Hkv, head_dim, Lmax), q.device)
+    _check(lib().gqa_attention_cached(_f16(q), _bf16(k_cache), _bf16(v_cache), _i32(cache_len), B, S, Hq, Hkv,
+                                      head_dim, Lmax, int(causal), _bf16(attn_out), _ptr(workspace),
+                                      workspace.numel() * workspace.element_size(), _stream(stream)))
 
 
 # -------------------------------------------------------------------- decode

@@ -302,14 +302,14 @@ static int run_qkv(DeviceState &st, const gqa_bf16 *x, const gqa_bf16 *Wqkv, con
 // same entry point and is launched as its programmatic dependent.
 static int run_attention(DeviceState &st, const uint16_t *q, const uint16_t *k, const uint16_t *v, int B, int S,
                          int Hq, int Hkv, int d, int causal, gqa_bf16 *out, cudaStream_t stream, int kv_seq = 0,
-                         const int *kv_start = nullptr, int bf16_qkv = 0, float *lse = nullptr, int lse_ld = 0,
+                         const int *kv_start = nullptr, int cached = 0, float *lse = nullptr, int lse_ld = 0,
                          int pdl = 0, int kv_splits = 1, uint16_t *part_o = nullptr, float *part_lse = nullptr)
 {
     AttentionProblem p{q,         k,        v,        out, B,   S,      Hq, Hkv, d, causal ? 1 : 0,
-                       kv_seq > 0 ? kv_seq : S, kv_start, bf16_qkv, lse, lse_ld, pdl, kv_splits, part_o, part_lse};
+                       kv_seq > 0 ? kv_seq : S, kv_start, cached, lse, lse_ld, pdl, kv_splits, part_o, part_lse};
     cudaError_t ce = launch_attention(p, st.err, st.num_sms, stream);
     if (ce != cudaSuccess) return cuda_fail(ce, "attention launch");
-    g_launches += kv_splits > 1 && part_o && part_lse && bf16_qkv && d != 256 ? 2 : 1;
+    g_launches += kv_splits > 1 && part_o && part_lse && cached && d != 256 ? 2 : 1;
     return GQA_OK;
 }
 
@@ -1033,12 +1033,14 @@ int gqa_attn_decode_rd(const gqa_bf16 *x, const gqa_bf16 *Wqkv, const gqa_bf16 *
 
 // Workspace of the cached prefill: Q (bf16), attn (bf16), and for the
 // attention's key splits (kCachedSplits at most) their binary16 partial
-// outputs and fp32 log2-sum-exp rows.
+// outputs and fp32 log2-sum-exp rows; then the binary16 copies of the two
+// caches that the attention reads ([B, Hkv, Lmax, d] each).
 static constexpr int kCachedSplits = 2;
 struct CachedLayout {
-    size_t q, attn, part_o, part_lse, total;
+    size_t q, attn, part_o, part_lse, k16, v16, total;
 };
-static CachedLayout cached_layout(int B, int S, int Hq, int d)
+static size_t widened_bytes(int B, int Hkv, int d, int Lmax) { return align256((size_t)B * Hkv * Lmax * d * 2); }
+static CachedLayout cached_layout(int B, int S, int Hq, int Hkv, int d, int Lmax)
 {
     CachedLayout L;
     const size_t n = align256((size_t)B * S * Hq * d * 2);
@@ -1046,14 +1048,22 @@ static CachedLayout cached_layout(int B, int S, int Hq, int d)
     L.attn = n;
     L.part_o = 2 * n;
     L.part_lse = L.part_o + kCachedSplits * n;
-    L.total = L.part_lse + align256((size_t)kCachedSplits * B * Hq * S * 4);
+    L.k16 = L.part_lse + align256((size_t)kCachedSplits * B * Hq * S * 4);
+    L.v16 = L.k16 + widened_bytes(B, Hkv, d, Lmax);
+    L.total = L.v16 + widened_bytes(B, Hkv, d, Lmax);
     return L;
 }
 
-size_t gqa_attn_prefill_cached_workspace_size(int B, int S, int Hq, int head_dim)
+size_t gqa_attn_prefill_cached_workspace_size(int B, int S, int Hq, int Hkv, int head_dim, int Lmax)
 {
-    if (B <= 0 || S <= 0 || Hq <= 0 || head_dim <= 0) return 0;
-    return cached_layout(B, S, Hq, head_dim).total;
+    if (B <= 0 || S <= 0 || Hq <= 0 || Hkv <= 0 || head_dim <= 0 || Lmax <= 0) return 0;
+    return cached_layout(B, S, Hq, Hkv, head_dim, Lmax).total;
+}
+
+size_t gqa_attention_cached_workspace_size(int B, int Hkv, int head_dim, int Lmax)
+{
+    if (B <= 0 || Hkv <= 0 || head_dim <= 0 || Lmax <= 0) return 0;
+    return 2 * widened_bytes(B, Hkv, head_dim, Lmax);
 }
 
 // Key splits for the cached prefill's attention.  Its work items (sequence,
@@ -1077,9 +1087,22 @@ static int check_cached(int B, int S, int hidden, int Hq, int Hkv, int d, int Lm
     return GQA_OK;
 }
 
-int gqa_attention_cached(const gqa_bf16 *q, const gqa_bf16 *k_cache, const gqa_bf16 *v_cache, const int *cache_len,
+// Binary16 copies of cache rows [0, cache_len[b] + S) into k16 / v16, the keys
+// and values the cached attention reads.
+static int run_widen(DeviceState &st, const gqa_bf16 *k_cache, const gqa_bf16 *v_cache, uint16_t *k16,
+                     uint16_t *v16, const int *cache_len, int B, int S, int Hkv, int d, int Lmax, cudaStream_t stream,
+                     int pdl)
+{
+    CacheWiden w{k_cache, v_cache, k16, v16, cache_len, B, S, Hkv, Lmax, d, d == 256 ? 64 : 128, pdl};
+    cudaError_t ce = launch_cache_widen(w, st.err, stream);
+    if (ce != cudaSuccess) return cuda_fail(ce, "cache widening launch");
+    ++g_launches;
+    return GQA_OK;
+}
+
+int gqa_attention_cached(const gqa_f16 *q, const gqa_bf16 *k_cache, const gqa_bf16 *v_cache, const int *cache_len,
                          int B, int S, int Hq, int Hkv, int head_dim, int Lmax, int causal, gqa_bf16 *attn_out,
-                         void *stream)
+                         void *workspace, size_t workspace_bytes, void *stream)
 {
     g_launches = 0;
     int rc = check_cached(B, S, 8, Hq, Hkv, head_dim, Lmax, nullptr, nullptr);
@@ -1087,10 +1110,18 @@ int gqa_attention_cached(const gqa_bf16 *q, const gqa_bf16 *k_cache, const gqa_b
     if (!q || !k_cache || !v_cache || !cache_len || !attn_out) return fail(GQA_ERR_ARG, "null pointer");
     if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(attn_out))
         return fail(GQA_ERR_ARG, "tensor pointers must be 16-byte aligned");
+    const size_t need = gqa_attention_cached_workspace_size(B, Hkv, head_dim, Lmax);
+    if (!workspace || workspace_bytes < need)
+        return fail(GQA_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", need,
+                    workspace ? workspace_bytes : (size_t)0);
+    if (((uintptr_t)workspace & 255u) != 0) return fail(GQA_ERR_ARG, "workspace must be 256-byte aligned");
     DeviceState *st;
     if ((rc = device_state(&st))) return rc;
-    return run_attention(*st, q, k_cache, v_cache, B, S, Hq, Hkv, head_dim, causal, attn_out, (cudaStream_t)stream,
-                         Lmax, cache_len, 1);
+    uint16_t *k16 = (uint16_t *)workspace, *v16 = k16 + widened_bytes(B, Hkv, head_dim, Lmax) / 2;
+    cudaStream_t s = (cudaStream_t)stream;
+    if ((rc = run_widen(*st, k_cache, v_cache, k16, v16, cache_len, B, S, Hkv, head_dim, Lmax, s, 0))) return rc;
+    return run_attention(*st, q, k16, v16, B, S, Hq, Hkv, head_dim, causal, attn_out, s, Lmax, cache_len, 1, nullptr,
+                         0, 1);
 }
 
 int gqa_attn_prefill_cached_rd(const gqa_bf16 *x, const gqa_bf16 *Wqkv, const gqa_bf16 *Wo, const gqa_bf16 *q_norm_w,
@@ -1110,7 +1141,7 @@ int gqa_attn_prefill_cached_rd(const gqa_bf16 *x, const gqa_bf16 *Wqkv, const gq
     if ((rc = check_rotary(rotary_dim, head_dim))) return rc;
     const size_t nx = (size_t)B * S * hidden * 2;
     if (overlap(out, nx, x, nx)) return fail(GQA_ERR_ARG, "out must not overlap x");
-    const size_t need = gqa_attn_prefill_cached_workspace_size(B, S, Hq, head_dim);
+    const size_t need = gqa_attn_prefill_cached_workspace_size(B, S, Hq, Hkv, head_dim, Lmax);
     if (!workspace || workspace_bytes < need)
         return fail(GQA_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", need,
                     workspace ? workspace_bytes : (size_t)0);
@@ -1118,17 +1149,19 @@ int gqa_attn_prefill_cached_rd(const gqa_bf16 *x, const gqa_bf16 *Wqkv, const gq
     DeviceState *st;
     if ((rc = device_state(&st))) return rc;
     uint8_t *ws = (uint8_t *)workspace;
-    const CachedLayout CL = cached_layout(B, S, Hq, head_dim);
-    gqa_bf16 *q = (gqa_bf16 *)(ws + CL.q);  // bf16: it meets the bf16 cache in the score MMA
+    const CachedLayout CL = cached_layout(B, S, Hq, Hkv, head_dim, Lmax);
+    gqa_f16 *q = (gqa_f16 *)(ws + CL.q);  // binary16; the attention widens the bf16 cache tiles to match
     gqa_bf16 *attn = (gqa_bf16 *)(ws + CL.attn);
     const int splits = cached_splits(B, S, Hq, st->num_sms);
     cudaStream_t s = (cudaStream_t)stream;
     // K/V of the new tokens go straight into the cache at slots cache_len[b] + t
     if ((rc = run_qkv(*st, x, Wqkv, q_norm_w, k_norm_w, rope_theta, eps, rotary_dim, B, S, hidden, Hq, Hkv, head_dim,
-                      cache_len, S, Lmax, Lmax, 0, 0, q, k_cache, v_cache, s)))
+                      cache_len, S, Lmax, Lmax, 1, 0, q, k_cache, v_cache, s)))
         return rc;
-    if ((rc = run_attention(*st, q, k_cache, v_cache, B, S, Hq, Hkv, head_dim, causal, attn, s, Lmax, cache_len, 1,
-                            nullptr, 0, 1, splits, (uint16_t *)(ws + CL.part_o), (float *)(ws + CL.part_lse))))
+    uint16_t *k16 = (uint16_t *)(ws + CL.k16), *v16 = (uint16_t *)(ws + CL.v16);
+    if ((rc = run_widen(*st, k_cache, v_cache, k16, v16, cache_len, B, S, Hkv, head_dim, Lmax, s, 1))) return rc;
+    if ((rc = run_attention(*st, q, k16, v16, B, S, Hq, Hkv, head_dim, causal, attn, s, Lmax, cache_len, 1, nullptr,
+                            0, 1, splits, (uint16_t *)(ws + CL.part_o), (float *)(ws + CL.part_lse))))
         return rc;
     return run_oproj(*st, attn, Wo, x, B * S, hidden, Hq * head_dim, out, s, 1);
 }

@@ -36,7 +36,10 @@
 //
 // Q, K and V arrive as binary16: with QK-norm their rows are bounded by
 // sqrt(d) * max|w|, and binary16 keeps 3 more mantissa bits than bf16, which
-// cuts the rounding error that storage adds to scores and outputs.
+// cuts the rounding error that storage adds to scores and outputs.  The
+// cached variant reads a binary16 copy of the bf16 cache rows it attends
+// (made by cache_widen_kernel, exact for every bf16 value below 2^16), so Q
+// and P stay binary16 there too.
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -141,16 +144,16 @@ struct ASmem {
     static constexpr int ALLOC = TOTAL + 1024;
 };
 
-// D: head_dim (64, 80, 96, 128).  CACHED: the queries follow kv_start[b] cached keys of a bf16
-// KV cache, so Q, K, V and P are bf16; otherwise they are binary16 and the
-// keys are exactly the S query positions (this variant compiles without any
-// offset arithmetic).
+// D: head_dim (64, 80, 96, 128).  Q, K, V and P are binary16 in the MMAs.
+// CACHED: the queries follow kv_start[b] cached keys (K and V: the binary16
+// copy of a bf16 cache that cache_widen_kernel makes, kv_seq rows per head);
+// otherwise the keys are exactly the S query positions (this variant compiles
+// without any offset arithmetic).
 template <int D, bool CACHED>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                 const __grid_constant__ CUtensorMap tmV, const AttnParams P)
 {
-    constexpr bool BF = CACHED;
     using L = ASmem<D>;
     constexpr int ST = L::STAGES;
     extern __shared__ uint8_t smem_raw[];
@@ -244,9 +247,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == 1) {
         if (lane == 0) {
             // S: Q, K K-major over d; O: P from TMEM, V MN-major (d contiguous)
-            constexpr uint32_t idesc_s = BF ? idesc_bf16_f32(kRows, kKeys, 0, 0) : idesc_f16_f32(kRows, kKeys, 0, 0);
+            constexpr uint32_t idesc_s = idesc_f16_f32(kRows, kKeys, 0, 0);
             constexpr int DP = padded_d<D>();
-            constexpr uint32_t idesc_o = BF ? idesc_bf16_f32(kRows, DP, 0, 1) : idesc_f16_f32(kRows, DP, 0, 1);
+            constexpr uint32_t idesc_o = idesc_f16_f32(kRows, DP, 0, 1);
             auto issue_s = [&](int i, int j) {  // S_i = Q_i K(j)^T
                 const uint32_t sQ = smem_u32(smem + L::Q + i * L::NCH * L::CHUNK);
                 const uint32_t sK = smem_u32(smem + L::K + (j % ST) * L::NCH * L::CHUNK);
@@ -358,7 +361,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         nm2);
                     const float2 p = make_float2(ex2(x.x), ex2(x.y));
                     rs2[e & 1] = __fadd2_rn(rs2[e & 1], p);
-                    pk[e] = BF ? pack_bf16(p.x, p.y) : pack_f16(p.x, p.y);
+                    pk[e] = pack_f16(p.x, p.y);
                 }
                 tmem_st16_nowait(tS + 16 * c, pk);
             }
@@ -486,7 +489,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const AttnParams P, int ro
     *reinterpret_cast<uint4 *>(P.out + (size_t)r * D + c8) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
 }
 
-template <int D, bool BF>
+template <int D, bool CACHED>
 cudaError_t run_attn(const AttentionProblem &p, unsigned *err, cudaStream_t stream)
 {
     using L = ASmem<D>;
@@ -513,7 +516,7 @@ cudaError_t run_attn(const AttentionProblem &p, unsigned *err, cudaStream_t stre
     a.R = R;
     a.n_qblk = (p.S + kTiles * R - 1) / (kTiles * R);
     a.causal = p.causal;
-    a.kv_splits = (BF && p.kv_splits > 1 && p.part_o && p.part_lse) ? p.kv_splits : 1;  // the cached variant only
+    a.kv_splits = (CACHED && p.kv_splits > 1 && p.part_o && p.part_lse) ? p.kv_splits : 1;  // the cached variant only
     a.part_o = p.part_o;
     a.part_lse = p.part_lse;
     a.num_items = p.B * p.Hkv * a.n_qblk * a.kv_splits;
@@ -524,7 +527,7 @@ cudaError_t run_attn(const AttentionProblem &p, unsigned *err, cudaStream_t stre
     a.lse = p.lse;
     a.lse_ld = p.lse_ld;
     a.err = err;
-    auto kern = attn_kernel<D, BF>;
+    auto kern = attn_kernel<D, CACHED>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC);
     if (e != cudaSuccess) return e;
     {
@@ -551,7 +554,7 @@ cudaError_t launch_attention(const AttentionProblem &p, unsigned *err, int num_s
     if (p.Hkv <= 0 || p.Hq % p.Hkv) return cudaErrorInvalidValue;
     const int G = p.Hq / p.Hkv;
     if (G > kRows) return cudaErrorInvalidValue;
-    if (p.bf16_qkv) {
+    if (p.cached) {
         if (p.d == 128) return run_attn<128, true>(p, err, stream);
         if (p.d == 64) return run_attn<64, true>(p, err, stream);
         if (p.d == 80) return run_attn<80, true>(p, err, stream);

@@ -26,8 +26,9 @@
 //           rescaled only past a 2^8 growth of the running max, after the
 //           previous PV has completed (an mbarrier committed after each PV).
 //
-// G query heads of one KV group share the 128 MMA rows (R = 128/G positions
-// each), so every K/V tile is brought in once for all of them.
+//
+// G query heads of one KV group share the 128 MMA rows (floor(128/G)
+// positions each), so every K/V tile is brought in once for all of them.
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -89,14 +90,14 @@ struct Smem256 {
 };
 static_assert(Smem256::ALLOC <= 232448, "shared memory per CTA");
 
-// CACHED: the queries follow kv_start[b] cached keys of a bf16 cache (Q, K,
-// V and P bf16); otherwise binary16 and keys = the S query positions.
+// Q, K, V and P are binary16 in the MMAs.  CACHED: the queries follow
+// kv_start[b] cached keys (K and V: the binary16 copy of a bf16 cache that
+// cache_widen_kernel makes); otherwise the keys are the S query positions.
 template <bool CACHED>
 __global__ void __launch_bounds__(kThreads, 1)
     attn256_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                    const __grid_constant__ CUtensorMap tmV, const Params256 P)
 {
-    constexpr bool BF = CACHED;
     using L = Smem256;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -194,8 +195,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp == 1) {
         if (lane == 0) {
-            constexpr uint32_t idesc_s = BF ? idesc_bf16_f32(kRows, kKeys, 0, 0) : idesc_f16_f32(kRows, kKeys, 0, 0);
-            constexpr uint32_t idesc_o = BF ? idesc_bf16_f32(kRows, kD, 0, 1) : idesc_f16_f32(kRows, kD, 0, 1);
+            constexpr uint32_t idesc_s = idesc_f16_f32(kRows, kKeys, 0, 0);
+            constexpr uint32_t idesc_o = idesc_f16_f32(kRows, kD, 0, 1);
             const uint32_t sQ = smem_u32(smem + L::Q);
             auto issue_s = [&](int buf, int j) {  // S(j) = Q K(j)^T into S buffer buf
                 const uint32_t sK = smem_u32(smem + L::K + (j % kKst) * kNch * L::KCH);
@@ -304,7 +305,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         nm2);
                     const float2 p = make_float2(ex2(x.x), ex2(x.y));
                     rs2[e & 1] = __fadd2_rn(rs2[e & 1], p);
-                    pk[e] = BF ? pack_bf16(p.x, p.y) : pack_f16(p.x, p.y);
+                    pk[e] = pack_f16(p.x, p.y);
                 }
                 tmem_st16_nowait(tS + 16 * c, pk);
             }
@@ -364,7 +365,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-template <bool BF>
+template <bool CACHED>
 cudaError_t run_attn256(const AttentionProblem &p, unsigned *err, cudaStream_t stream)
 {
     using L = Smem256;
@@ -396,7 +397,7 @@ cudaError_t run_attn256(const AttentionProblem &p, unsigned *err, cudaStream_t s
     a.scale_log2 = 1.4426950408889634f / 16.0f;  // log2(e) / sqrt(256)
     a.out = p.out;
     a.err = err;
-    auto kern = attn256_kernel<BF>;
+    auto kern = attn256_kernel<CACHED>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC);
     if (e != cudaSuccess) return e;
     kern<<<p.B * p.Hkv * a.n_qblk, kThreads, L::ALLOC, stream>>>(tq, tk, tv, a);
@@ -408,7 +409,7 @@ cudaError_t run_attn256(const AttentionProblem &p, unsigned *err, cudaStream_t s
 cudaError_t launch_attention256(const AttentionProblem &p, unsigned *err, cudaStream_t stream)
 {
     if (p.d != kD || p.Hkv <= 0 || p.Hq % p.Hkv || p.Hq / p.Hkv > kRows) return cudaErrorInvalidValue;
-    return p.bf16_qkv ? run_attn256<true>(p, err, stream) : run_attn256<false>(p, err, stream);
+    return p.cached ? run_attn256<true>(p, err, stream) : run_attn256<false>(p, err, stream);
 }
 
 }  // namespace gqa

@@ -77,6 +77,20 @@ cudaError_t launch_gemm_residual(const GemmProblem &p, const ResidualEpilogue &e
 cudaError_t launch_gemm_general(const GemmProblem &p, int a_mn, int b_mn, int epi, const GemmOut &o, unsigned *err,
                                 int num_sms, cudaStream_t stream);
 
+// ------------------------------------------------------ KV-cache widening
+// Binary16 copies k16 / v16 [B, Hkv, Lmax, d] of the bf16 caches' rows
+// [0, cache_len[b] + S), zero-filled up to the next multiple of `tile` keys
+// (the attention's key tile); values beyond +-65504 saturate and set
+// kErrRange.  Sequences with cache_len[b] + S > Lmax are skipped.
+struct CacheWiden {
+    const uint16_t *k_cache, *v_cache;
+    uint16_t *k16, *v16;
+    const int *cache_len;
+    int B, S, Hkv, Lmax, d, tile;
+    int pdl = 0;
+};
+cudaError_t launch_cache_widen(const CacheWiden &p, unsigned *err, cudaStream_t stream);
+
 // ------------------------------------------------------- prefill attention
 struct AttentionProblem {
     const uint16_t *q;  // [B, Hq, S, d]
@@ -86,12 +100,12 @@ struct AttentionProblem {
     int B, S, Hq, Hkv, d, causal;
     int kv_seq;            // sequence extent of k/v (S, or Lmax for a cache)
     const int *kv_start;   // device [B]: keys already cached before the S queries (NULL: 0)
-    int bf16_qkv;          // 1: q/k/v bf16 (P bf16); 0: binary16 (P binary16)
+    int cached;            // 1: queries after kv_start[b] cached keys (k/v: kv_seq rows per head); all binary16
     float *lse;            // non-NULL (plain prefill only): per (b, head, t) log2-sum-exp of the
                            // scaled scores, at lse[(b*Hq + head)*lse_ld + t]: P = 2^(s*log2(e)/sqrt(d) - lse)
     int lse_ld;
     int pdl = 0;           // launch as the programmatic dependent of the previous kernel
-    // cached variant (bf16_qkv, kv_start): split each query block's keys into kv_splits
+    // cached variant (kv_start): split each query block's keys into kv_splits
     // ranges, partials in part_o [kv_splits][B, S, Hq*d] binary16 and part_lse
     // [kv_splits][B*Hq, S] fp32, merged by a second kernel (1 or NULL buffers: no split)
     int kv_splits = 1;

@@ -92,6 +92,22 @@ DEVI bool mbar_wait(uint64_t *bar, uint32_t parity, unsigned *err, uint64_t limi
     }
 }
 
+// ------------------------------------------------------ bf16 -> binary16
+
+// Two bf16 values (one 32-bit word) as binary16, saturated to +-65504;
+// `over` collects bit 15 of each half of (|x| bits + 0x3880), which is set
+// exactly when |x| >= 2^16 (the bf16 values beyond binary16's range: every
+// bf16 below 2^16 is at most 65280) or x is not finite.
+DEVI uint32_t bf16x2_to_f16x2(uint32_t x, uint32_t &over)
+{
+    over |= (x & 0x7fff7fffu) + 0x38803880u;
+    uint32_t r;
+    asm("cvt.rn.satfinite.f16x2.f32 %0, %1, %2;"
+        : "=r"(r)
+        : "f"(__uint_as_float(x & 0xffff0000u)), "f"(__uint_as_float(x << 16)));
+    return r;
+}
+
 // ------------------------------------------------ programmatic dependent launch
 
 // Wait until the grids this one depends on (the previous kernel in the stream,
