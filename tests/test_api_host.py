@@ -93,8 +93,8 @@ def test_other_entry_points_validate(L):
     assert lib.gqa_oproj_residual(P(FAKE), P(FAKE), P(FAKE), 4, 64, 64, P(FAKE), None) == -1
     assert lib.gqa_decode_attention(P(FAKE), P(FAKE), P(FAKE), P(FAKE), 2, 260, 2, 128, 100, P(FAKE), P(FAKE),
                                     1 << 30, None) == -2   # group of 130
-    assert lib.gqa_decode_attention(P(FAKE), P(FAKE), P(FAKE), P(FAKE), 2, 8, 2, 80, 100, P(FAKE), P(FAKE),
-                                    1 << 30, None) == -2   # decode: head_dim 64 or 128 only
+    assert lib.gqa_decode_attention(P(FAKE), P(FAKE), P(FAKE), P(FAKE), 2, 8, 2, 160, 100, P(FAKE), P(FAKE),
+                                    1 << 30, None) == -2   # decode: no tile for head_dim 160
     assert lib.gqa_attn_decode(P(FAKE), P(FAKE), P(FAKE), None, None, 1e6, 1e-6, 2, 64, 8, 2, 128, P(FAKE),
                                P(FAKE), None, 100, P(FAKE * 3), P(FAKE * 4), 1 << 30, None) == -1  # cache_len NULL
     assert lib.gqa_attn_workspace_size(0, 1, 1, 1, 1, 1) == 0

@@ -7,7 +7,7 @@ its own (one query tile with two S buffers, 64-key tiles).  Checked: the
 attention stage over group sizes 1, 4, 8 and 16, ragged lengths and the
 unmasked case, with marker values for the head map; the cached-prefill
 attention; the QKV stage with full and partial rotary; the whole layer at
-the Gemma-3 width; decode at head_dim 256 is rejected.
+the Gemma-3 width (decode at head_dim 256: tests/test_decode_widths_gpu.py).
 
 Tolerance: max|err| <= 1e-2 max|ref| and relative L1 <= 2e-3 (tests/parity.py).
 """
@@ -18,8 +18,7 @@ import torch
 import oracle
 from parity import assert_parity, to64
 from transformer_gqa_attention_qkv_gb300 import binding as gq
-from transformer_gqa_attention_qkv_gb300.inputs import PREFILL_CONFIGS, DecodeConfig, make_decode_inputs, \
-    make_layer_inputs
+from transformer_gqa_attention_qkv_gb300.inputs import PREFILL_CONFIGS, make_layer_inputs
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -155,14 +154,3 @@ def test_forward_d256_full_workload_sampled():
     ref = oracle.forward(t["x"], t["Wqkv"], t["Wo"], t["q_norm_w"], t["k_norm_w"], cfg.rope_theta, cfg.eps,
                          cfg.B, cfg.S, cfg.hidden, cfg.Hq, cfg.Hkv, D, sel=rows)
     assert_parity("out d256 sampled", to64(out).reshape(-1, cfg.hidden)[rows], ref)
-
-
-def test_decode_d256_is_rejected():
-    cfg = DecodeConfig("t", 2, 16, 640, 4, 1, D, True, 1e6, Lmax=32)
-    t = make_decode_inputs(cfg, seed=1)
-    out = torch.empty((2, 640), dtype=torch.bfloat16, device=DEV)
-    ws = gq.new_workspace(1 << 20)
-    with pytest.raises(gq.GqaError, match=f"status {gq.GQA_ERR_UNSUPPORTED}"):
-        gq.gqa_attn_decode(dev(t["x"]), dev(t["Wqkv"]), dev(t["Wo"]), dev(t["q_norm_w"]), dev(t["k_norm_w"]),
-                           1e6, 1e-6, 2, 640, 4, 1, D, dev(t["k_cache"]), dev(t["v_cache"]),
-                           dev(torch.full((2,), 16, dtype=torch.int32)), 32, out, ws)

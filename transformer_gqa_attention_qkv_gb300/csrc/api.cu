@@ -943,7 +943,8 @@ static int check_decode(int B, int hidden, int Hq, int Hkv, int d, int Lmax, con
     int rc = check_layer(B, 1, hidden, Hq, Hkv, d, qn, kn);
     if (rc) return rc;
     if (Lmax <= 0) return fail(GQA_ERR_ARG, "Lmax must be positive");
-    if (d != 64 && d != 128) return fail(GQA_ERR_UNSUPPORTED, "decode supports head_dim 64 and 128 (got %d)", d);
+    if (d != 64 && d != 80 && d != 96 && d != 128 && d != 256)
+        return fail(GQA_ERR_UNSUPPORTED, "decode supports head_dim 64, 80, 96, 128 and 256 (got %d)", d);
     const int G = Hq / Hkv;
     if (G > 128) return fail(GQA_ERR_UNSUPPORTED, "unsupported decode group size Hq/Hkv=%d (at most 128)", G);
     if ((long long)B * Hkv * Lmax * d > (1LL << 40)) return fail(GQA_ERR_UNSUPPORTED, "cache too large");

@@ -55,16 +55,19 @@ constexpr int kGroup = 4;      // consumer warps per chunk, 16 keys each
 
 // F8: the caches hold one-byte E4M3 codes, so a 128-wide row is one 128-byte
 // swizzled box row and a chunk is half the bytes (twice the stages in flight).
+// bf16 rows are NCH boxes of 64 values; at head widths 80 and 96 the second
+// box is zero-filled past d by the tensor copy (dims end at d), and the
+// products run over the d real columns only.
 // CW consumer warps: CW / kGroup groups of four take the staged chunks in turn.
 // GM: query heads per work item (rows of the per-warp partials).
 template <int D, int GM, bool F8 = false, int CW = kGroup>
 struct DSmem {
-    static constexpr int NCH = F8 ? 1 : D / 64;   // 128-byte boxes per row: 64-wide d halves, or all 128 codes
+    static constexpr int NCH = F8 ? 1 : (D + 63) / 64;  // 128-byte boxes per row: 64-wide d chunks, or 128 codes
     static constexpr int BOX = kChunk * 128;       // one 64-key x 128-byte swizzled box (8 KB)
     static constexpr int CB = NCH * BOX;           // one K (or V) chunk
     // a multiple of the group count: stage s then always serves group s % (CW / kGroup),
     // so a group waiting for a stage's next fill has consumed its previous one
-    static constexpr int STAGES = F8 ? 12 : (D == 128 ? 6 : 12);
+    static constexpr int STAGES = F8 ? 12 : (NCH == 4 ? 3 : NCH == 2 ? 6 : 12);
     static constexpr int K = 0;
     static constexpr int V = STAGES * CB;
     static constexpr int RED = 2 * STAGES * CB;    // [CW][GM][D + 2] floats
@@ -353,6 +356,148 @@ DEVI void consume_bf16(const DecodeAttentionProblem &P, uint8_t *smem, uint64_t 
     }
 }
 
+// Consumer warps over bf16 caches for groups of up to 8 heads, transposed
+// products: S^T = K Q^T (16 keys in the MMA rows, the heads in its 8 columns)
+// and O^T = V^T P^T (16 values of d in the rows), so one m16n8k16 covers 16
+// keys x 8 heads and O takes D/16 x 4 registers (heads-in-rows needs twice
+// both).  K is the A fragment straight from ldmatrix; V^T from ldmatrix.trans;
+// the binary16 query (the B fragment of S^T) and P (the B fragment of O^T,
+// reached through an 8x8 movmatrix transpose) are split into bf16 high and low
+// parts, two MMAs each, so no precision is lost.  A lane holds the scores of
+// keys grp and grp + 8 for heads 2 tig and 2 tig + 1.
+template <int D, int CW>
+DEVI void consume_bf16_t(const DecodeAttentionProblem &P, uint8_t *smem, uint64_t *full, uint64_t *empty,
+                         float *red, float scale_log2, int n_items, unsigned *err)
+{
+    constexpr int GM = 8;
+    using L = DSmem<D, GM, false, CW>;
+    static_assert(CW == kGroup, "bf16 caches: one group of four consumer warps");
+    static_assert(D % 16 == 0, "16-wide k-steps and d blocks");
+    constexpr int ST = L::STAGES;
+    constexpr int KS = D / 16;  // k-steps of S^T, and 16-row d blocks of O^T
+    const int Gv = P.Hq / P.Hkv / P.vsub;
+    const int lane = threadIdx.x % 32;
+    const int cw = threadIdx.x / 32 - 1;  // keys [16 cw, 16 cw + 16) of each chunk
+    const int grp = lane >> 2, tig = lane & 3;
+    const bool head_valid = grp < Gv;     // B-fragment column grp = query head vg*Gv + grp
+    // ldmatrix: matrix mi covers keys 8*(mi&1).. and d block (mi>>1) (K, the A fragment),
+    // and keys 8*(mi>>1).. of d block (mi&1) (V, read transposed as the A fragment of O^T)
+    const int mi = lane >> 3, mr = lane & 7;
+    const int k_key = cw * 16 + (mi & 1) * 8 + mr, k_dofs = (mi >> 1) * 8;
+    const int v_key = cw * 16 + (mi >> 1) * 8 + mr, v_dofs = (mi & 1) * 8;
+
+    int it = 0;
+    for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
+        const ItemRange r = item_range(P, item, err, false);
+        // B fragments of Q^T: [0] d 2t, 2t+1 and [1] d 2t+8, 2t+9 of k-step ks, head grp
+        uint32_t qh[KS][2], ql[KS][2];
+        const uint16_t *qrow = P.q + (size_t)(r.b * P.Hq + r.vg * Gv + (head_valid ? grp : 0)) * D;
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks)
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                float2 f = make_float2(0.0f, 0.0f);
+                if (head_valid) f = __half22float2(*reinterpret_cast<const __half2 *>(qrow + ks * 16 + half * 8 + 2 * tig));
+                split_bf16(f.x, f.y, qh[ks][half], ql[ks][half]);
+            }
+        float o[KS][4];  // d block b: c0/c1 d = 16b + grp (heads 2t, 2t+1), c2/c3 d = 16b + grp + 8
+#pragma unroll
+        for (int b = 0; b < KS; ++b) o[b][0] = o[b][1] = o[b][2] = o[b][3] = 0.0f;
+        float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.0f, l1 = 0.0f;  // heads 2 tig, 2 tig + 1
+
+        for (int u0 = r.begin; u0 < r.end; u0 += kChunk, ++it) {
+            const int s = it % ST;
+            if (!mbar_wait(full + s, (it / ST) & 1, err)) break;
+            const uint32_t kb = smem_u32(smem + L::K + s * L::CB);
+            const uint32_t vb = smem_u32(smem + L::V + s * L::CB);
+            if (u0 + kChunk > r.end) zero_v_tail<L::NCH>(smem + L::V + s * L::CB, u0, r.end, cw, lane);
+            // S^T [16 keys x 8 heads], two accumulators (k-step parity)
+            float sc[2][4] = {{0.0f, 0.0f, 0.0f, 0.0f}, {0.0f, 0.0f, 0.0f, 0.0f}};
+#pragma unroll
+            for (int ks = 0; ks < KS; ++ks) {
+                uint32_t a0, a1, a2, a3;
+                ldsm_x4(kb + swz<D>(k_key, ks * 16 + k_dofs), a0, a1, a2, a3);
+                mma_bf16_16816(sc[ks & 1], a0, a1, a2, a3, qh[ks][0], qh[ks][1]);
+                mma_bf16_16816(sc[ks & 1], a0, a1, a2, a3, ql[ks][0], ql[ks][1]);
+            }
+            const int ka = u0 + cw * 16 + grp;  // this lane's keys: ka, ka + 8
+            const float v0 = (ka < r.end) ? (sc[0][0] + sc[1][0]) * scale_log2 : -INFINITY;      // head 2t
+            const float v1 = (ka < r.end) ? (sc[0][1] + sc[1][1]) * scale_log2 : -INFINITY;      // head 2t+1
+            const float v2 = (ka + 8 < r.end) ? (sc[0][2] + sc[1][2]) * scale_log2 : -INFINITY;  // head 2t
+            const float v3 = (ka + 8 < r.end) ? (sc[0][3] + sc[1][3]) * scale_log2 : -INFINITY;  // head 2t+1
+            float x0 = fmaxf(v0, v2), x1 = fmaxf(v1, v3);
+#pragma unroll
+            for (int sh = 4; sh <= 16; sh <<= 1) {
+                x0 = fmaxf(x0, __shfl_xor_sync(0xffffffffu, x0, sh));
+                x1 = fmaxf(x1, __shfl_xor_sync(0xffffffffu, x1, sh));
+            }
+            // the running max moves only past a 2^8 growth, so O is rescaled rarely
+            const float n0 = (x0 > m0 + 8.0f) ? fmaxf(m0, x0) : m0;
+            const float n1 = (x1 > m1 + 8.0f) ? fmaxf(m1, x1) : m1;
+            const float u0m = (n0 == -INFINITY) ? 0.0f : n0, u1m = (n1 == -INFINITY) ? 0.0f : n1;
+            const float a0s = ex2(m0 - u0m), a1s = ex2(m1 - u1m);
+            m0 = n0;
+            m1 = n1;
+            const float p0 = (v0 == -INFINITY) ? 0.0f : ex2(v0 - u0m);
+            const float p1 = (v1 == -INFINITY) ? 0.0f : ex2(v1 - u1m);
+            const float p2 = (v2 == -INFINITY) ? 0.0f : ex2(v2 - u0m);
+            const float p3 = (v3 == -INFINITY) ? 0.0f : ex2(v3 - u1m);
+            l0 = l0 * a0s + (p0 + p2);
+            l1 = l1 * a1s + (p1 + p3);
+            // P^T as the B fragment (high and low bf16 parts): transpose the (key x head) 8x8 blocks
+            uint32_t h01, l01, h23, l23;
+            split_bf16(p0, p1, h01, l01);
+            split_bf16(p2, p3, h23, l23);
+            const uint32_t pbh0 = movmatrix_t(h01), pbh1 = movmatrix_t(h23);
+            const uint32_t pbl0 = movmatrix_t(l01), pbl1 = movmatrix_t(l23);
+            if (__any_sync(0xffffffffu, a0s != 1.0f || a1s != 1.0f)) {
+#pragma unroll
+                for (int b = 0; b < KS; ++b) {
+                    o[b][0] *= a0s;
+                    o[b][1] *= a1s;
+                    o[b][2] *= a0s;
+                    o[b][3] *= a1s;
+                }
+            }
+#pragma unroll
+            for (int b = 0; b < KS; ++b) {
+                uint32_t a0, a1, a2, a3;
+                ldsm_x4_trans(vb + swz<D>(v_key, b * 16 + v_dofs), a0, a1, a2, a3);
+                mma_bf16_16816(o[b], a0, a1, a2, a3, pbh0, pbh1);
+                mma_bf16_16816(o[b], a0, a1, a2, a3, pbl0, pbl1);
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(empty + s);
+        }
+        // sums over the eight lanes of a head column; the max is already uniform there
+#pragma unroll
+        for (int sh = 4; sh <= 16; sh <<= 1) {
+            l0 += __shfl_xor_sync(0xffffffffu, l0, sh);
+            l1 += __shfl_xor_sync(0xffffffffu, l1, sh);
+        }
+        float *rw = red + cw * GM * (D + 2);
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const int h = 2 * tig + e;
+            if (h < Gv) {
+                float *dst = rw + h * (D + 2);
+#pragma unroll
+                for (int b = 0; b < KS; ++b) {
+                    dst[16 * b + grp] = o[b][e];
+                    dst[16 * b + grp + 8] = o[b][2 + e];
+                }
+                if (grp == 0) {
+                    dst[D] = e ? m1 : m0;
+                    dst[D + 1] = e ? l1 : l0;
+                }
+            }
+        }
+        consumer_sync<CW>();
+        write_record<D, GM, CW>(red, P.partials + (size_t)r.rec * Gv * (D + 2), Gv);
+        consumer_sync<CW>();  // red is reused by the next item
+    }
+}
+
 // Consumer warps over E4M3 caches: transposed products with the group's heads
 // in the MMA's 8 columns (GM = 8), binary16 MMAs.  In the S^T product the 16
 // d-values of one k-step reach the K (A) fragment in the order ldmatrix
@@ -563,6 +708,8 @@ __global__ void __launch_bounds__(32 * (1 + CW), 1)
     }
     if constexpr (F8)
         consume_f8<D, CW>(P, smem, full, empty, red, scale_log2, n_items, err);
+    else if constexpr (GM == 8)
+        consume_bf16_t<D, CW>(P, smem, full, empty, red, scale_log2, n_items, err);
     else
         consume_bf16<D, GM, CW>(P, smem, full, empty, red, scale_log2, n_items, err);
 }
@@ -680,6 +827,9 @@ cudaError_t launch_decode_attention(const DecodeAttentionProblem &p, unsigned *e
     if (p.fp8) return p.d == 128 ? run_decode<128, 8, true>(p, err, stream) : cudaErrorInvalidValue;
     if (p.d == 128) return G <= 8 ? run_decode<128, 8, false>(p, err, stream) : run_decode<128, 16, false>(p, err, stream);
     if (p.d == 64) return G <= 8 ? run_decode<64, 8, false>(p, err, stream) : run_decode<64, 16, false>(p, err, stream);
+    if (p.d == 80) return G <= 8 ? run_decode<80, 8, false>(p, err, stream) : run_decode<80, 16, false>(p, err, stream);
+    if (p.d == 96) return G <= 8 ? run_decode<96, 8, false>(p, err, stream) : run_decode<96, 16, false>(p, err, stream);
+    if (p.d == 256) return run_decode<256, 8, false>(p, err, stream);  // partials of 16 heads would not fit
     return cudaErrorInvalidValue;
 }
 
