@@ -106,6 +106,9 @@ def _load():
     lib.oracle_backward.restype = _I
     lib.oracle_backward.argtypes = [_u16p, _u16p, _u16p, _u16p, _u16p, _D, _D, _L, _L, _L, _L, _L, _L, _I,
                                     _u16p, _f64p, _f64p, _f64p, _f64p, _f64p, _f64p, _f64p, _f64p, _f64p, _I]
+    lib.oracle_backward_rd.restype = _I
+    lib.oracle_backward_rd.argtypes = [_u16p, _u16p, _u16p, _u16p, _u16p, _D, _D, _L, _L, _L, _L, _L, _L, _L, _I,
+                                       _u16p, _f64p, _f64p, _f64p, _f64p, _f64p, _f64p, _f64p, _f64p, _f64p, _I]
     lib.oracle_attention_backward.restype = _I
     lib.oracle_attention_backward.argtypes = [_u16p, _u16p, _u16p, _u16p, _I, _L, _L, _L, _L, _L, _I,
                                               _f64p, _f64p, _f64p, _I]
@@ -418,7 +421,7 @@ def decode_fp8(x, Wqkv, Wo, q_norm_w, k_norm_w, rope_theta, eps, B, hidden, Hq, 
 # ------------------------------------------------------------- backward
 
 def backward(x, Wqkv, Wo, q_norm_w, k_norm_w, rope_theta, eps, B, S, hidden, Hq, Hkv, d, dout,
-             causal=True, want_stages=False, threads=None):
+             causal=True, want_stages=False, threads=None, rotary_dim=None):
     """Gradients of the layer given dout = dL/dout [B*S, hidden] (bf16).
     Returns dict dx [B*S, hidden], dWqkv [(Hq+2Hkv)d, hidden], dWo [hidden,
     Hq*d], dq_norm_w / dk_norm_w [d]; with want_stages also d_attn [B*S,
@@ -432,9 +435,10 @@ def backward(x, Wqkv, Wo, q_norm_w, k_norm_w, rope_theta, eps, B, S, hidden, Hq,
     dk = np.empty((B, Hkv, S, d)) if want_stages else None
     dv = np.empty((B, Hkv, S, d)) if want_stages else None
     xb, wb, ob, qn, kn, gb = _bits(x), _bits(Wqkv), _bits(Wo), _bits(q_norm_w), _bits(k_norm_w), _bits(dout)
-    _check(lib.oracle_backward(_p16(xb), _p16(wb), _p16(ob), _p16(qn), _p16(kn), rope_theta, eps, B, S, hidden,
-                               Hq, Hkv, d, int(causal), _p16(gb), _pf(dx), _pf(dW), _pf(dWo), _pf(dqn), _pf(dkn),
-                               _pf(da), _pf(dq), _pf(dk), _pf(dv), threads or default_threads()), "backward")
+    _check(lib.oracle_backward_rd(_p16(xb), _p16(wb), _p16(ob), _p16(qn), _p16(kn), rope_theta, eps,
+                                  _rd(rotary_dim, d), B, S, hidden, Hq, Hkv, d, int(causal), _p16(gb), _pf(dx),
+                                  _pf(dW), _pf(dWo), _pf(dqn), _pf(dkn), _pf(da), _pf(dq), _pf(dk), _pf(dv),
+                                  threads or default_threads()), "backward")
     res = {"dx": dx, "dWqkv": dW, "dWo": dWo, "dq_norm_w": dqn, "dk_norm_w": dkn}
     if want_stages:
         res.update({"d_attn": da, "dq": dq, "dk": dk, "dv": dv})

@@ -979,7 +979,7 @@ done:
  *                                    dw_i += q_pre_i r dq_n_i (over every Q row; k_norm_w over K rows)
  *   qkv_pre = x Wqkv^T            -> dx += d_qkv_pre Wqkv, dWqkv = d_qkv_pre^T x
  * K and V gradients of a KV head sum over the G query heads of its group.
- * Full rotary (rotary_dim = d).  Outputs (all required): dx [B*S, hidden],
+ * Rotary width rd (R16; oracle_backward: rd = d).  Outputs (all required): dx [B*S, hidden],
  * dWqkv [(Hq+2Hkv)*d, hidden], dWo [hidden, Hq*d], dqn/dkn [d] (zeroed
  * when there is no QK-norm).  Optional: d_attn [B*S, Hq*d] and the
  * attention-input gradients dq [B,Hq,S,d], dk/dv [B,Hkv,S,d] (after RoPE,
@@ -1014,16 +1014,17 @@ static void rmsnorm_head_bwd(const double *x, const double *dy, long d, const ui
     }
 }
 
-int oracle_backward(const uint16_t *x, const uint16_t *Wqkv, const uint16_t *Wo,
-                    const uint16_t *q_norm_w, const uint16_t *k_norm_w,
-                    double rope_theta, double eps,
-                    long B, long S, long hidden, long Hq, long Hkv, long d, int causal,
-                    const uint16_t *dout,
-                    double *dx, double *dWqkv, double *dWo, double *dqn, double *dkn,
-                    double *d_attn_out, double *dq_out, double *dk_out, double *dv_out, int nthreads)
+int oracle_backward_rd(const uint16_t *x, const uint16_t *Wqkv, const uint16_t *Wo,
+                       const uint16_t *q_norm_w, const uint16_t *k_norm_w,
+                       double rope_theta, double eps, long rd,
+                       long B, long S, long hidden, long Hq, long Hkv, long d, int causal,
+                       const uint16_t *dout,
+                       double *dx, double *dWqkv, double *dWo, double *dqn, double *dkn,
+                       double *d_attn_out, double *dq_out, double *dk_out, double *dv_out, int nthreads)
 {
     if (!x || !Wqkv || !Wo || !dout || !dx || !dWqkv || !dWo || !dqn || !dkn) return ORACLE_EARG;
     if (B <= 0 || S <= 0 || hidden <= 0 || Hq <= 0 || Hkv <= 0 || d <= 0 || (d & 1) || d > 1024) return ORACLE_EARG;
+    if (rd < 0 || rd > d || (rd & 1)) return ORACLE_EARG;
     if (Hq % Hkv) return ORACLE_EARG;
     if ((q_norm_w == NULL) != (k_norm_w == NULL)) return ORACLE_EARG;
     const long M = B * S, NQ = Hq * d, NKV = Hkv * d, N = NQ + 2 * NKV, G = Hq / Hkv;
@@ -1052,13 +1053,13 @@ int oracle_backward(const uint16_t *x, const uint16_t *Wqkv, const uint16_t *Wo,
         for (long j = 0; j < Hq; ++j) {
             memcpy(tmp, row + j * d, (size_t)d * sizeof(double));
             if (q_norm_w) rmsnorm_head(tmp, d, q_norm_w, eps);
-            rope_head(tmp, d, (double)t, rope_theta);
+            rope_head(tmp, rd, (double)t, rope_theta);
             memcpy(Q + ((b * Hq + j) * S + t) * d, tmp, (size_t)d * sizeof(double));
         }
         for (long g = 0; g < Hkv; ++g) {
             memcpy(tmp, row + NQ + g * d, (size_t)d * sizeof(double));
             if (k_norm_w) rmsnorm_head(tmp, d, k_norm_w, eps);
-            rope_head(tmp, d, (double)t, rope_theta);
+            rope_head(tmp, rd, (double)t, rope_theta);
             memcpy(K + ((b * Hkv + g) * S + t) * d, tmp, (size_t)d * sizeof(double));
             memcpy(V + ((b * Hkv + g) * S + t) * d, row + NQ + NKV + g * d, (size_t)d * sizeof(double));
         }
@@ -1145,7 +1146,7 @@ int oracle_backward(const uint16_t *x, const uint16_t *Wqkv, const uint16_t *Wo,
             double dy[1024];
             for (long j = 0; j < Hq; ++j) {
                 memcpy(dy, dQ + ((b * Hq + j) * S + t) * d, (size_t)d * sizeof(double));
-                rope_head_inv(dy, d, (double)t, rope_theta);
+                rope_head_inv(dy, rd, (double)t, rope_theta);
                 if (q_norm_w)
                     rmsnorm_head_bwd(pre + m * N + j * d, dy, d, q_norm_w, eps, dpre + m * N + j * d, dqn_rows + m * d);
                 else
@@ -1153,7 +1154,7 @@ int oracle_backward(const uint16_t *x, const uint16_t *Wqkv, const uint16_t *Wo,
             }
             for (long g = 0; g < Hkv; ++g) {
                 memcpy(dy, dK + ((b * Hkv + g) * S + t) * d, (size_t)d * sizeof(double));
-                rope_head_inv(dy, d, (double)t, rope_theta);
+                rope_head_inv(dy, rd, (double)t, rope_theta);
                 if (k_norm_w)
                     rmsnorm_head_bwd(pre + m * N + NQ + g * d, dy, d, k_norm_w, eps, dpre + m * N + NQ + g * d,
                                      dkn_rows + m * d);
@@ -1189,6 +1190,18 @@ int oracle_backward(const uint16_t *x, const uint16_t *Wqkv, const uint16_t *Wo,
 done:
     free(pre); free(Q); free(K); free(V); free(attn); free(dattn); free(dQ); free(dK); free(dV); free(dpre);
     return err;
+}
+
+int oracle_backward(const uint16_t *x, const uint16_t *Wqkv, const uint16_t *Wo,
+                    const uint16_t *q_norm_w, const uint16_t *k_norm_w,
+                    double rope_theta, double eps,
+                    long B, long S, long hidden, long Hq, long Hkv, long d, int causal,
+                    const uint16_t *dout,
+                    double *dx, double *dWqkv, double *dWo, double *dqn, double *dkn,
+                    double *d_attn_out, double *dq_out, double *dk_out, double *dv_out, int nthreads)
+{
+    return oracle_backward_rd(x, Wqkv, Wo, q_norm_w, k_norm_w, rope_theta, eps, d, B, S, hidden, Hq, Hkv, d,
+                              causal, dout, dx, dWqkv, dWo, dqn, dkn, d_attn_out, dq_out, dk_out, dv_out, nthreads);
 }
 
 /* Attention backward alone, from 16-bit Q [B,Hq,S,d], K/V [B,Hkv,S,d] and

@@ -833,11 +833,12 @@ def test_fp8_decode_step_equals_library_composition():
 
 # ----------------------------------------------------------------- backward
 
-def _torch_layer(cfg, t, causal=True, keep=None, kv_round=None):
+def _torch_layer(cfg, t, causal=True, keep=None, kv_round=None, rd=None):
     """The layer as a float64 torch composition (F.linear, F.rms_norm, complex
     RoPE, SDPA); parameters are leaves with requires_grad.  keep (a dict)
     receives the attention's q, k, v and attn with retained gradients.
-    kv_round (forward only): applied to K and V after RoPE."""
+    kv_round (forward only): applied to K and V after RoPE.  rd: rotary width
+    (default head_dim)."""
     B, S, h, Hq, Hkv, d = cfg.B, cfg.S, cfg.hidden, cfg.Hq, cfg.Hkv, cfg.head_dim
     leaves = {k: f64(v).requires_grad_(True) for k, v in t.items() if v is not None}
     x, W, Wo = leaves["x"], leaves["Wqkv"], leaves["Wo"]
@@ -848,8 +849,8 @@ def _torch_layer(cfg, t, causal=True, keep=None, kv_round=None):
         q = F.rms_norm(q, (d,), weight=leaves["q_norm_w"], eps=cfg.eps)
         k = F.rms_norm(k, (d,), weight=leaves["k_norm_w"], eps=cfg.eps)
     pos = torch.arange(S, dtype=torch.float64)[:, None]
-    q = _complex_rope(q, pos, cfg.rope_theta, d).transpose(1, 2)
-    k = _complex_rope(k, pos, cfg.rope_theta, d).transpose(1, 2)
+    q = _complex_rope(q, pos, cfg.rope_theta, d if rd is None else rd).transpose(1, 2)
+    k = _complex_rope(k, pos, cfg.rope_theta, d if rd is None else rd).transpose(1, 2)
     v = v.transpose(1, 2)
     if kv_round is not None:
         k, v = kv_round(k), kv_round(v)
@@ -896,6 +897,32 @@ def test_backward_equals_library_autograd(qk, causal):
         np.testing.assert_allclose(got["dk_norm_w"], leaves["k_norm_w"].grad.numpy(), **tol)
     else:
         assert not got["dq_norm_w"].any() and not got["dk_norm_w"].any()
+
+
+@pytest.mark.parametrize("rd", [4, 2, 0])
+def test_backward_partial_rotary_equals_library_autograd(rd):
+    """The backward with RoPE on the first rd features only (R16: [NeoX]
+    "Scaling and RoPE", rotary_pct): every gradient equals float64 autograd
+    through the composition rotating those features; the unrotated features'
+    gradients pass the inverse rotation unchanged (rd = 0: no rotation)."""
+    cfg = _tiny()
+    t = make_layer_inputs(cfg, seed=53, w_std=0.3)
+    dout = bf16(np.random.default_rng(53).standard_normal((cfg.B * cfg.S, cfg.hidden)))
+    keep = {}
+    leaves, out = _torch_layer(cfg, t, True, keep, rd=rd)
+    (out.reshape(-1, cfg.hidden) * f64(dout)).sum().backward()
+    got = oracle.backward(t["x"], t["Wqkv"], t["Wo"], t["q_norm_w"], t["k_norm_w"], cfg.rope_theta, cfg.eps,
+                          cfg.B, cfg.S, cfg.hidden, cfg.Hq, cfg.Hkv, cfg.head_dim, dout, want_stages=True, threads=T,
+                          rotary_dim=rd)
+    tol = dict(rtol=1e-10, atol=1e-11)
+    np.testing.assert_allclose(got["dx"], leaves["x"].grad.reshape(-1, cfg.hidden).numpy(), **tol)
+    np.testing.assert_allclose(got["dWqkv"], leaves["Wqkv"].grad.numpy(), **tol)
+    np.testing.assert_allclose(got["dq_norm_w"], leaves["q_norm_w"].grad.numpy(), **tol)
+    np.testing.assert_allclose(got["dk_norm_w"], leaves["k_norm_w"].grad.numpy(), **tol)
+    np.testing.assert_allclose(got["dk"], keep["k"].grad.numpy(), **tol)
+    full = oracle.backward(t["x"], t["Wqkv"], t["Wo"], t["q_norm_w"], t["k_norm_w"], cfg.rope_theta, cfg.eps,
+                           cfg.B, cfg.S, cfg.hidden, cfg.Hq, cfg.Hkv, cfg.head_dim, dout, threads=T)
+    assert np.abs(full["dx"] - got["dx"]).max() > 1e-6  # the rotary width matters
 
 
 def test_attention_backward_stage_equals_library_autograd():
