@@ -405,8 +405,10 @@ int gqa_decode_qkv_rd(const gqa_bf16 *x, const gqa_bf16 *Wqkv,
  *   dq_norm_w, dk_norm_w [head_dim]        fp32  (required with QK-norm, else may be NULL)
  * The forward is recomputed (Q, K, V, the attention's per-row log-sum-exp);
  * the attention backward recomputes its probabilities from them.  Full
- * rotary; head_dim 64 or 128; Hq/Hkv a power of two up to 32, else
- * GQA_ERR_UNSUPPORTED.  dx must not overlap x or dout.  workspace: at least
+ * rotary (the *_rd forms below take a rotary width); head_dim 64, 80, 96 or
+ * 128; Hq/Hkv a power of two up to 32, else GQA_ERR_UNSUPPORTED (head_dim
+ * 256: the dK and dV accumulators of a 128-key block would fill all 512 TMEM
+ * columns).  dx must not overlap x or dout.  workspace: at least
  * gqa_attn_backward_workspace_size(...) bytes, 256-byte aligned.  Enqueued on
  * `stream`. */
 size_t gqa_attn_backward_workspace_size(int B, int S, int hidden, int Hq, int Hkv, int head_dim);
@@ -428,8 +430,7 @@ int gqa_attn_backward(const gqa_bf16 *x, const gqa_bf16 *Wqkv, const gqa_bf16 *W
  * recomputing the QKV projection and the forward attention.  Between the two
  * calls the workspace must not be changed, and x, the weights, the norm
  * weights, rope_theta, eps, sizes and causal must be the same; nothing checks
- * this.  head_dim 64 or 128, Hq/Hkv a power of two up to 32 (as for
- * gqa_attn_backward). */
+ * this.  Shape limits as for gqa_attn_backward. */
 int gqa_attn_forward_train(const gqa_bf16 *x, const gqa_bf16 *Wqkv, const gqa_bf16 *Wo,
                            const gqa_bf16 *q_norm_w, const gqa_bf16 *k_norm_w,
                            float rope_theta, float eps,
@@ -442,6 +443,32 @@ int gqa_attn_backward_saved(const gqa_bf16 *x, const gqa_bf16 *Wqkv, const gqa_b
                             const gqa_bf16 *dout, gqa_bf16 *dx, float *dWqkv, float *dWo,
                             float *dq_norm_w, float *dk_norm_w,
                             void *workspace, size_t workspace_bytes, void *stream);
+
+/* The three above with RoPE on the first rotary_dim features only ([NeoX]
+ * "Scaling and RoPE", rotary_pct; as the other *_rd entry points: rotary_dim
+ * head_dim, head_dim/2, head_dim/4 or 0, else GQA_ERR_UNSUPPORTED; odd or out
+ * of [0, head_dim]: GQA_ERR_ARG).  The inverse rotation of the backward
+ * acts on the same features; the training pair's two calls must take the same
+ * rotary_dim. */
+int gqa_attn_backward_rd(const gqa_bf16 *x, const gqa_bf16 *Wqkv, const gqa_bf16 *Wo,
+                         const gqa_bf16 *q_norm_w, const gqa_bf16 *k_norm_w,
+                         float rope_theta, float eps, int rotary_dim,
+                         int B, int S, int hidden, int Hq, int Hkv, int head_dim, int causal,
+                         const gqa_bf16 *dout, gqa_bf16 *dx, float *dWqkv, float *dWo,
+                         float *dq_norm_w, float *dk_norm_w,
+                         void *workspace, size_t workspace_bytes, void *stream);
+int gqa_attn_forward_train_rd(const gqa_bf16 *x, const gqa_bf16 *Wqkv, const gqa_bf16 *Wo,
+                              const gqa_bf16 *q_norm_w, const gqa_bf16 *k_norm_w,
+                              float rope_theta, float eps, int rotary_dim,
+                              int B, int S, int hidden, int Hq, int Hkv, int head_dim, int causal,
+                              gqa_bf16 *out, void *workspace, size_t workspace_bytes, void *stream);
+int gqa_attn_backward_saved_rd(const gqa_bf16 *x, const gqa_bf16 *Wqkv, const gqa_bf16 *Wo,
+                               const gqa_bf16 *q_norm_w, const gqa_bf16 *k_norm_w,
+                               float rope_theta, float eps, int rotary_dim,
+                               int B, int S, int hidden, int Hq, int Hkv, int head_dim, int causal,
+                               const gqa_bf16 *dout, gqa_bf16 *dx, float *dWqkv, float *dWo,
+                               float *dq_norm_w, float *dk_norm_w,
+                               void *workspace, size_t workspace_bytes, void *stream);
 
 /* Stage alone: the attention backward.  q [B, Hq, S, head_dim], k and v
  * [B, Hkv, S, head_dim], dO [B, Hq, S, head_dim] (all binary16, head-major);

@@ -37,7 +37,8 @@ EXPORTS = (
     "gqa_decode_qkv_rd", "gqa_attn_decode_fp8", "gqa_decode_qkv_fp8", "gqa_decode_attention_fp8",
     "gqa_attn_backward_workspace_size", "gqa_attn_backward", "gqa_attention_backward_workspace_size",
     "gqa_attention_backward", "gqa_attn_forward_host_workspace_size", "gqa_attn_forward_host",
-    "gqa_attn_forward_train", "gqa_attn_backward_saved",
+    "gqa_attn_forward_train", "gqa_attn_backward_saved", "gqa_attn_backward_rd", "gqa_attn_forward_train_rd",
+    "gqa_attn_backward_saved_rd",
 )
 
 
@@ -103,6 +104,10 @@ def lib():
     sig["gqa_attn_backward"] = (_I, [_P] * 5 + [_F, _F] + [_I] * 7 + [_P] * 6 + [_P, _Z, _P])
     sig["gqa_attn_backward_saved"] = sig["gqa_attn_backward"]
     sig["gqa_attn_forward_train"] = (_I, [_P] * 5 + [_F, _F] + [_I] * 7 + [_P, _P, _Z, _P])
+    for base in ("gqa_attn_backward", "gqa_attn_backward_saved", "gqa_attn_forward_train"):
+        res, args = sig[base]
+        k = args.index(_F) + 2
+        sig[base + "_rd"] = (res, args[:k] + [_I] + args[k:])
     sig["gqa_attention_backward_workspace_size"] = (_Z, [_I] * 4)
     sig["gqa_attention_backward"] = (_I, [_P] * 4 + [_I] * 6 + [_P] * 3 + [_P, _Z, _P])
     for name, (res, args) in sig.items():
@@ -472,3 +477,32 @@ def gqa_attention_backward(q, k, v, dO, B, S, Hq, Hkv, head_dim, causal, dq, dk,
     _check(lib().gqa_attention_backward(_f16(q), _f16(k), _f16(v), _f16(dO), B, S, Hq, Hkv, head_dim, int(causal),
                                         _f32(dq), _f32(dk), _f32(dv), _ptr(workspace),
                                         workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+# ----------------------------------------------- backward with partial rotary
+
+def gqa_attn_backward_rd(x, Wqkv, Wo, q_norm_w, k_norm_w, rope_theta, eps, rotary_dim, B, S, hidden, Hq, Hkv,
+                         head_dim, causal, dout, dx, dWqkv, dWo, dq_norm_w, dk_norm_w, workspace, stream=None):
+    _check(lib().gqa_attn_backward_rd(_bf16(x), _bf16(Wqkv), _bf16(Wo), _bf16(q_norm_w), _bf16(k_norm_w),
+                                      rope_theta, eps, rotary_dim, B, S, hidden, Hq, Hkv, head_dim, int(causal),
+                                      _bf16(dout), _bf16(dx), _f32(dWqkv), _f32(dWo), _f32(dq_norm_w),
+                                      _f32(dk_norm_w), _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                      _stream(stream)))
+
+
+def gqa_attn_forward_train_rd(x, Wqkv, Wo, q_norm_w, k_norm_w, rope_theta, eps, rotary_dim, B, S, hidden, Hq, Hkv,
+                              head_dim, causal, out, workspace, stream=None):
+    _check(lib().gqa_attn_forward_train_rd(_bf16(x), _bf16(Wqkv), _bf16(Wo), _bf16(q_norm_w), _bf16(k_norm_w),
+                                           rope_theta, eps, rotary_dim, B, S, hidden, Hq, Hkv, head_dim, int(causal),
+                                           _bf16(out), _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                           _stream(stream)))
+    return out
+
+
+def gqa_attn_backward_saved_rd(x, Wqkv, Wo, q_norm_w, k_norm_w, rope_theta, eps, rotary_dim, B, S, hidden, Hq, Hkv,
+                               head_dim, causal, dout, dx, dWqkv, dWo, dq_norm_w, dk_norm_w, workspace, stream=None):
+    _check(lib().gqa_attn_backward_saved_rd(_bf16(x), _bf16(Wqkv), _bf16(Wo), _bf16(q_norm_w), _bf16(k_norm_w),
+                                            rope_theta, eps, rotary_dim, B, S, hidden, Hq, Hkv, head_dim,
+                                            int(causal), _bf16(dout), _bf16(dx), _f32(dWqkv), _f32(dWo),
+                                            _f32(dq_norm_w), _f32(dk_norm_w), _ptr(workspace),
+                                            workspace.numel() * workspace.element_size(), _stream(stream)))

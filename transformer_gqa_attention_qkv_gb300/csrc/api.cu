@@ -654,7 +654,8 @@ static int check_backward(int B, int S, int hidden, int Hq, int Hkv, int d, cons
     int rc = check_layer(B, S, hidden, Hq, Hkv, d, qn, kn);
     if (rc) return rc;
     if ((rc = check_group_pow2(Hq, Hkv))) return rc;
-    if (d != 64 && d != 128) return fail(GQA_ERR_UNSUPPORTED, "the backward supports head_dim 64 and 128 (got %d)", d);
+    if (d != 64 && d != 80 && d != 96 && d != 128)
+        return fail(GQA_ERR_UNSUPPORTED, "the backward supports head_dim 64, 80, 96 and 128 (got %d)", d);
     if (Hq / Hkv > 32)
         return fail(GQA_ERR_UNSUPPORTED, "the backward supports groups of up to 32 query heads (got %d)", Hq / Hkv);
     return GQA_OK;
@@ -747,14 +748,15 @@ size_t gqa_attn_backward_workspace_size(int B, int S, int hidden, int Hq, int Hk
 // The layer backward; saved: the forward's Q, K, V, pre-norm rows, O and lse
 // are already in the workspace (gqa_attn_forward_train), so nothing is recomputed.
 static int layer_backward(const gqa_bf16 *x, const gqa_bf16 *Wqkv, const gqa_bf16 *Wo, const gqa_bf16 *q_norm_w,
-                          const gqa_bf16 *k_norm_w, float rope_theta, float eps, int B, int S, int hidden, int Hq,
-                          int Hkv, int head_dim, int causal, const gqa_bf16 *dout, gqa_bf16 *dx, float *dWqkv,
-                          float *dWo, float *dq_norm_w, float *dk_norm_w, void *workspace, size_t workspace_bytes,
-                          void *stream, bool saved)
+                          const gqa_bf16 *k_norm_w, float rope_theta, float eps, int rd, int B, int S, int hidden,
+                          int Hq, int Hkv, int head_dim, int causal, const gqa_bf16 *dout, gqa_bf16 *dx,
+                          float *dWqkv, float *dWo, float *dq_norm_w, float *dk_norm_w, void *workspace,
+                          size_t workspace_bytes, void *stream, bool saved)
 {
     g_launches = 0;
     int rc = check_backward(B, S, hidden, Hq, Hkv, head_dim, q_norm_w, k_norm_w);
     if (rc) return rc;
+    if ((rc = check_rotary(rd, head_dim))) return rc;
     if (!x || !Wqkv || !Wo || !dout || !dx || !dWqkv || !dWo) return fail(GQA_ERR_ARG, "null tensor pointer");
     if (q_norm_w && (!dq_norm_w || !dk_norm_w))
         return fail(GQA_ERR_ARG, "dq_norm_w and dk_norm_w are required with QK-norm");
@@ -783,8 +785,8 @@ static int layer_backward(const gqa_bf16 *x, const gqa_bf16 *Wqkv, const gqa_bf1
     const gqa_bf16 *o = (const gqa_bf16 *)(aws + attn_bwd_layout(B, S, Hq, d).o);
     cudaStream_t s = (cudaStream_t)stream;
     // 1. the forward's Q, K, V (binary16) and pre-norm rows
-    if (!saved && (rc = run_qkv(*st, x, Wqkv, q_norm_w, k_norm_w, rope_theta, eps, d, B, S, hidden, Hq, Hkv, d, nullptr,
-                                S, S, S, 1, 1, q, k, v, s, 0, 1.0f, 1.0f, pre)))
+    if (!saved && (rc = run_qkv(*st, x, Wqkv, q_norm_w, k_norm_w, rope_theta, eps, rd, B, S, hidden, Hq, Hkv, d,
+                                nullptr, S, S, S, 1, 1, q, k, v, s, 0, 1.0f, 1.0f, pre)))
         return rc;
     // 2. dO = dout Wo, head-major binary16
     {
@@ -800,15 +802,15 @@ static int layer_backward(const gqa_bf16 *x, const gqa_bf16 *Wqkv, const gqa_bf1
     // 4. inverse RoPE and the QK-norm gradient -> dqkv
     {
         const float2 *rope = nullptr;
-        {
+        if (rd > 0) {
             std::lock_guard<std::mutex> lk(g_mu);
-            rc = rope_table(*st, (double)rope_theta, d, S, &rope);
+            rc = rope_table(*st, (double)rope_theta, rd, S, &rope);
         }
         if (rc) return rc;
         cudaError_t ce = cudaMemsetAsync(dqn, 0, d * sizeof(float), s);
         if (ce == cudaSuccess) ce = cudaMemsetAsync(dkn, 0, d * sizeof(float), s);
         if (ce != cudaSuccess) return cuda_fail(ce, "cudaMemsetAsync(norm-weight gradients)");
-        RopeNormBwd rp{dq, dk, dv, pre, rope, q_norm_w, k_norm_w, eps, dqkv, dqn, dkn, M, S, N, Hq, Hkv, d};
+        RopeNormBwd rp{dq, dk, dv, pre, rope, q_norm_w, k_norm_w, eps, dqkv, dqn, dkn, M, S, N, Hq, Hkv, d, rd};
         ce = launch_rope_norm_bwd(rp, s);
         if (ce != cudaSuccess) return cuda_fail(ce, "RoPE / QK-norm backward launch");
         ++g_launches;
@@ -842,14 +844,37 @@ static int layer_backward(const gqa_bf16 *x, const gqa_bf16 *Wqkv, const gqa_bf1
     return GQA_OK;
 }
 
+int gqa_attn_backward_rd(const gqa_bf16 *x, const gqa_bf16 *Wqkv, const gqa_bf16 *Wo, const gqa_bf16 *q_norm_w,
+                         const gqa_bf16 *k_norm_w, float rope_theta, float eps, int rotary_dim, int B, int S,
+                         int hidden, int Hq, int Hkv, int head_dim, int causal, const gqa_bf16 *dout, gqa_bf16 *dx,
+                         float *dWqkv, float *dWo, float *dq_norm_w, float *dk_norm_w, void *workspace,
+                         size_t workspace_bytes, void *stream)
+{
+    return layer_backward(x, Wqkv, Wo, q_norm_w, k_norm_w, rope_theta, eps, rotary_dim, B, S, hidden, Hq, Hkv,
+                          head_dim, causal, dout, dx, dWqkv, dWo, dq_norm_w, dk_norm_w, workspace, workspace_bytes,
+                          stream, false);
+}
+
 int gqa_attn_backward(const gqa_bf16 *x, const gqa_bf16 *Wqkv, const gqa_bf16 *Wo, const gqa_bf16 *q_norm_w,
                       const gqa_bf16 *k_norm_w, float rope_theta, float eps, int B, int S, int hidden, int Hq,
                       int Hkv, int head_dim, int causal, const gqa_bf16 *dout, gqa_bf16 *dx, float *dWqkv,
                       float *dWo, float *dq_norm_w, float *dk_norm_w, void *workspace, size_t workspace_bytes,
                       void *stream)
 {
-    return layer_backward(x, Wqkv, Wo, q_norm_w, k_norm_w, rope_theta, eps, B, S, hidden, Hq, Hkv, head_dim, causal,
-                          dout, dx, dWqkv, dWo, dq_norm_w, dk_norm_w, workspace, workspace_bytes, stream, false);
+    return layer_backward(x, Wqkv, Wo, q_norm_w, k_norm_w, rope_theta, eps, head_dim, B, S, hidden, Hq, Hkv, head_dim,
+                          causal, dout, dx, dWqkv, dWo, dq_norm_w, dk_norm_w, workspace, workspace_bytes, stream,
+                          false);
+}
+
+int gqa_attn_backward_saved_rd(const gqa_bf16 *x, const gqa_bf16 *Wqkv, const gqa_bf16 *Wo,
+                               const gqa_bf16 *q_norm_w, const gqa_bf16 *k_norm_w, float rope_theta, float eps,
+                               int rotary_dim, int B, int S, int hidden, int Hq, int Hkv, int head_dim, int causal,
+                               const gqa_bf16 *dout, gqa_bf16 *dx, float *dWqkv, float *dWo, float *dq_norm_w,
+                               float *dk_norm_w, void *workspace, size_t workspace_bytes, void *stream)
+{
+    return layer_backward(x, Wqkv, Wo, q_norm_w, k_norm_w, rope_theta, eps, rotary_dim, B, S, hidden, Hq, Hkv,
+                          head_dim, causal, dout, dx, dWqkv, dWo, dq_norm_w, dk_norm_w, workspace, workspace_bytes,
+                          stream, true);
 }
 
 int gqa_attn_backward_saved(const gqa_bf16 *x, const gqa_bf16 *Wqkv, const gqa_bf16 *Wo, const gqa_bf16 *q_norm_w,
@@ -858,8 +883,9 @@ int gqa_attn_backward_saved(const gqa_bf16 *x, const gqa_bf16 *Wqkv, const gqa_b
                             float *dWo, float *dq_norm_w, float *dk_norm_w, void *workspace, size_t workspace_bytes,
                             void *stream)
 {
-    return layer_backward(x, Wqkv, Wo, q_norm_w, k_norm_w, rope_theta, eps, B, S, hidden, Hq, Hkv, head_dim, causal,
-                          dout, dx, dWqkv, dWo, dq_norm_w, dk_norm_w, workspace, workspace_bytes, stream, true);
+    return layer_backward(x, Wqkv, Wo, q_norm_w, k_norm_w, rope_theta, eps, head_dim, B, S, hidden, Hq, Hkv, head_dim,
+                          causal, dout, dx, dWqkv, dWo, dq_norm_w, dk_norm_w, workspace, workspace_bytes, stream,
+                          true);
 }
 
 int gqa_attn_forward_train(const gqa_bf16 *x, const gqa_bf16 *Wqkv, const gqa_bf16 *Wo, const gqa_bf16 *q_norm_w,
@@ -867,9 +893,19 @@ int gqa_attn_forward_train(const gqa_bf16 *x, const gqa_bf16 *Wqkv, const gqa_bf
                            int Hkv, int head_dim, int causal, gqa_bf16 *out, void *workspace, size_t workspace_bytes,
                            void *stream)
 {
+    return gqa_attn_forward_train_rd(x, Wqkv, Wo, q_norm_w, k_norm_w, rope_theta, eps, head_dim, B, S, hidden, Hq, Hkv,
+                                     head_dim, causal, out, workspace, workspace_bytes, stream);
+}
+
+int gqa_attn_forward_train_rd(const gqa_bf16 *x, const gqa_bf16 *Wqkv, const gqa_bf16 *Wo, const gqa_bf16 *q_norm_w,
+                              const gqa_bf16 *k_norm_w, float rope_theta, float eps, int rotary_dim, int B, int S,
+                              int hidden, int Hq, int Hkv, int head_dim, int causal, gqa_bf16 *out, void *workspace,
+                              size_t workspace_bytes, void *stream)
+{
     g_launches = 0;
     int rc = check_backward(B, S, hidden, Hq, Hkv, head_dim, q_norm_w, k_norm_w);
     if (rc) return rc;
+    if ((rc = check_rotary(rotary_dim, head_dim))) return rc;
     if (!x || !Wqkv || !Wo || !out) return fail(GQA_ERR_ARG, "null tensor pointer");
     if (!aligned16(x) || !aligned16(Wqkv) || !aligned16(Wo) || !aligned16(out))
         return fail(GQA_ERR_ARG, "tensor pointers must be 16-byte aligned");
@@ -896,8 +932,8 @@ int gqa_attn_forward_train(const gqa_bf16 *x, const gqa_bf16 *Wqkv, const gqa_bf
     float *lse = (float *)(ws + L.attn + A.lse);
     cudaStream_t s = (cudaStream_t)stream;
     // the backward's inputs, written where gqa_attn_backward_saved reads them
-    if ((rc = run_qkv(*st, x, Wqkv, q_norm_w, k_norm_w, rope_theta, eps, d, B, S, hidden, Hq, Hkv, d, nullptr, S, S, S,
-                      1, 1, q, k, v, s, 0, 1.0f, 1.0f, pre)))
+    if ((rc = run_qkv(*st, x, Wqkv, q_norm_w, k_norm_w, rope_theta, eps, rotary_dim, B, S, hidden, Hq, Hkv, d, nullptr,
+                      S, S, S, 1, 1, q, k, v, s, 0, 1.0f, 1.0f, pre)))
         return rc;
     if ((rc = run_attention(*st, q, k, v, B, S, Hq, Hkv, d, causal, o, s, 0, nullptr, 0, lse, A.ld, 1))) return rc;
     return run_oproj(*st, o, Wo, x, B * S, hidden, Hq * d, out, s, 1);

@@ -1,5 +1,5 @@
 // attention_bwd.cu -- backward of the causal grouped-query attention on
-// tcgen05 (head_dim 64 and 128).
+// tcgen05 (head_dim 64, 80, 96 and 128).
 //
 // With P = softmax(s), s = <q, k> / sqrt(d), o = P v and dO the gradient of
 // the attention output (the derivatives of [T07] §4 step 6; K and V of a KV
@@ -23,7 +23,10 @@
 // tile is processed in two halves of 64 rows with separate TMEM buffers, one
 // warpgroup per half, so the tensor core computes one half while the other's
 // P and dS are formed.  Q, K, V and dO are binary16 (head-major), so P and dS
-// are binary16 as well.
+// are binary16 as well.  Head widths 80 and 96 are staged as 128-wide rows
+// whose columns past d the tensor copy fills with zeros: S and dP contract over
+// the d real columns, the accumulating products run 128 wide (the zero columns
+// give zero gradient columns) and only d columns are stored.
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -48,7 +51,8 @@ struct BwdParams {
 
 template <int D>
 struct BSmem {
-    static constexpr int NCH = D / 64;
+    static constexpr int NCH = (D + 63) / 64;     // 64-wide d chunks (80 and 96: two, the second part zero)
+    static constexpr int DP = NCH * 64;           // the staged width
     static constexpr int CH = kRows * 128;        // 128 rows x 64 16-bit values (16 KB)
     static constexpr int TILE = NCH * CH;          // one 128-row tile of d values
     // dkdv: K, V kept; Q, dO rings of 2; lse/D rings of 2 x 2 x 128 floats
@@ -180,8 +184,9 @@ DEVI void p_ds64(uint32_t tS, uint32_t tdP, float sl, const float *lse_c, const 
 // its own S / dP buffers in TMEM (columns [128h, 128h + 64) and
 // [128h + 64, 128h + 128)) and its own warpgroup for the elementwise step
 // (warps 2..5 for h = 0, 6..9 for h = 1), so the tensor core works on one half
-// while the other half's P and dS are formed.  Accumulators: dV, dK at
-// [256, 256 + D), [256 + D, 256 + 2D) (DKDV) or dQ at [256, 256 + D).
+// while the other half's P and dS are formed.  Accumulators (DP: d rounded up
+// to 64): dV, dK at [256, 256 + DP), [256 + DP, 256 + 2 DP) (DKDV) or dQ at
+// [256, 256 + DP).
 // MMA order per item i: acc(i, 0), S(i + 1, 0), acc(i, 1), S(i + 1, 1), where
 // S(i, h) is S and dP of half h and acc(i, h) the products that consume P and
 // dS of half h.  The MMAs of one CTA run in issue order, so S(i + 1, h) reuses
@@ -283,7 +288,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == 1) {
         if (lane == 0) {
             constexpr uint32_t idesc_s = idesc_f16_f32(kRows, kHalf, 0, 0);  // 128 kept rows x 64 streamed rows
-            constexpr uint32_t idesc_a = idesc_f16_f32(kRows, D, 0, 1);      // 128 x d, B MN-major (d contiguous)
+            constexpr uint32_t idesc_a = idesc_f16_f32(kRows, L::DP, 0, 1);  // 128 x DP, B MN-major (d contiguous)
             const uint32_t sA0 = smem_u32(smem + L::A0), sA1 = smem_u32(smem + L::A1);
             const uint32_t sRing = smem_u32(smem + L::RING);
             // S = A0 R0_h^T and dP = A1 R1_h^T for half h of item it: DKDV
@@ -294,6 +299,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int c = 0; c < NCH; ++c)
 #pragma unroll
                     for (int k = 0; k < 4; ++k) {
+                        if (c * 64 + k * 16 >= D) continue;  // d real columns, 16 per step
                         umma_f16_ss(tmem + 128 * h, sw128_desc(sA0 + c * L::CH + 32 * k, 16, 1024),
                                     sw128_desc(r0 + c * L::CH + 32 * k, 16, 1024), idesc_s, (c | k) != 0);
                         umma_f16_ss(tmem + 128 * h + 64, sw128_desc(sA1 + c * L::CH + 32 * k, 16, 1024),
@@ -310,7 +316,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (DKDV) {
                         umma_f16_ts(tmem + 256, tmem + 128 * h + 8 * k, sw128_desc(r1 + k * 16 * 128, L::CH, 1024),
                                     idesc_a, acc);  // dV += P^T dO
-                        umma_f16_ts(tmem + 256 + D, tmem + 128 * h + 64 + 8 * k,
+                        umma_f16_ts(tmem + 256 + L::DP, tmem + 128 * h + 64 + 8 * k,
                                     sw128_desc(r0 + k * 16 * 128, L::CH, 1024), idesc_a, acc);  // dK += dS^T Q
                     } else {
                         umma_f16_ts(tmem + 256, tmem + 128 * h + 8 * k, sw128_desc(r0 + k * 16 * 128, L::CH, 1024),
@@ -407,9 +413,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (ok && wait_all(acc_done, 0)) {
             tc_fence_after();
-            // DKDV: half 0 stores dV, half 1 dK; else each half stores d/2 columns of dQ.
-            // tcgen05.ld is warp-collective: every lane loads, only valid rows store.
-            constexpr int NC = DKDV ? D : D / 2;
+            // DKDV: half 0 stores dV, half 1 dK; else each half stores DP/2 columns of dQ
+            // (the d real ones of them).  tcgen05.ld is warp-collective: every lane loads,
+            // only valid rows store.
+            constexpr int NC = DKDV ? L::DP : L::DP / 2;
             const uint32_t tacc = tmem + lane_off + 256 + h * NC;
             float *dst;
             float sc;
@@ -423,16 +430,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                 sc = P.scale;
                 st_ok = row_ok;
             }
+            const int col0 = DKDV ? 0 : h * NC;  // d column of the first stored accumulator column
 #pragma unroll 1
             for (int c = 0; c < NC; c += 32) {
                 uint32_t a[32];
                 tmem_ld32(tacc + c, a);
+                const int nv = min(32, D - (col0 + c));  // real columns of this chunk (a multiple of 16)
                 if (st_ok) {
 #pragma unroll
                     for (int v = 0; v < 8; ++v)
-                        reinterpret_cast<float4 *>(dst + c)[v] =
-                            make_float4(__uint_as_float(a[4 * v]) * sc, __uint_as_float(a[4 * v + 1]) * sc,
-                                        __uint_as_float(a[4 * v + 2]) * sc, __uint_as_float(a[4 * v + 3]) * sc);
+                        if (4 * v < nv)
+                            reinterpret_cast<float4 *>(dst + c)[v] =
+                                make_float4(__uint_as_float(a[4 * v]) * sc, __uint_as_float(a[4 * v + 1]) * sc,
+                                            __uint_as_float(a[4 * v + 2]) * sc, __uint_as_float(a[4 * v + 3]) * sc);
                 }
             }
         }
@@ -505,6 +515,8 @@ cudaError_t launch_attention_backward(const AttnBwdProblem &p, unsigned *err, cu
     if (G <= 0 || p.Hq % p.Hkv || G > 32 || (G & (G - 1)) || p.ld % 4 || p.ld < p.S) return cudaErrorInvalidValue;
     if (p.d == 128) return run_bwd<128>(p, err, stream);
     if (p.d == 64) return run_bwd<64>(p, err, stream);
+    if (p.d == 80) return run_bwd<80>(p, err, stream);
+    if (p.d == 96) return run_bwd<96>(p, err, stream);
     return cudaErrorInvalidValue;
 }
 

@@ -293,6 +293,8 @@ DEVI void epilogue_f32(const GemmParams &P, uint32_t tcol, int m, int n0, bool r
 
 // binary16 head-major output: column n = j*d + c of row m = b*S + t goes to
 // out[((b*H + j)*S + t)*d + c] (clamped to binary16's range and flagged).
+// Stored 16 columns at a time: d is a multiple of 16 (64, 80, 96, 128), so a
+// 16-column piece never crosses a head, while a 32-column one would at d = 80.
 template <int BN>
 DEVI void epilogue_head16(const GemmParams &P, uint32_t tcol, int m, int n0, bool row_ok)
 {
@@ -306,11 +308,16 @@ DEVI void epilogue_head16(const GemmParams &P, uint32_t tcol, int m, int n0, boo
         uint32_t r[32];
         tmem_ld32(tcol + c, r);
         if (!row_ok) continue;
-        const int j = n / e.d, cc = n - j * e.d;
-        float v[32];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
-        storew<32>(e.out + ((size_t)(b * e.H + j) * e.S + t) * e.d + cc, v, true, clamped);
+        for (int h = 0; h < 2; ++h) {
+            const int nh = n + 16 * h;
+            if (nh >= P.N) break;
+            const int j = nh / e.d, cc = nh - j * e.d;
+            float v[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[16 * h + i]);
+            storew<16>(e.out + ((size_t)(b * e.H + j) * e.S + t) * e.d + cc, v, true, clamped);
+        }
     }
     if (clamped) atomicOr(P.err, kErrRange);
 }

@@ -135,12 +135,13 @@ cudaError_t launch_attention_backward(const AttnBwdProblem &p, unsigned *err, cu
 // pre-norm Q and K rows [M, (Hq + Hkv) d] fp32, or NULL without QK-norm.
 struct RopeNormBwd {
     const float *dq, *dk, *dv, *pre;
-    const float2 *rope;  // [S rows][d/2] (cos, sin)
+    const float2 *rope;  // [S rows][rd/2] (cos, sin) of the rotary width's angles; NULL when rd = 0
     const uint16_t *q_norm_w, *k_norm_w;
     float eps;
     uint16_t *dqkv;
     float *dq_norm_w, *dk_norm_w;
     int M, S, N, Hq, Hkv, d;
+    int rd;              // rotary width (RoPE on features [0, rd))
 };
 cudaError_t launch_rope_norm_bwd(const RopeNormBwd &p, cudaStream_t stream);
 // head_dim 256 (called by launch_attention)
