@@ -714,32 +714,56 @@ __global__ void __launch_bounds__(32 * (1 + CW), 1)
         consume_bf16<D, GM, CW>(P, smem, full, empty, red, scale_log2, n_items, err);
 }
 
-// One CTA per (b, head sub-group): merge the splits and write bf16 attn.
+// One CTA per (b, head sub-group): merge the splits and write bf16 attn.  The
+// splits' maxima and sums are read first (one round of independent loads),
+// each head's weights 2^(m_s - M) / sum_s 2^(m_s - M) l_s formed once in
+// shared memory, then every output element is one pass of independent loads
+// over the splits (a per-element max-then-sum would chain two dependent
+// memory reads per element).
+constexpr int kCombineThreads = 256;
+constexpr int kCombineMaxW = 16 * 256;  // weights: heads of a sub-group x splits
+
 template <int D>
-__global__ void __launch_bounds__(128) decode_combine_kernel(const DecodeAttentionProblem P)
+__global__ void __launch_bounds__(kCombineThreads) decode_combine_kernel(const DecodeAttentionProblem P)
 {
+    __shared__ float s_w[kCombineMaxW];  // [h][split]: m, then the normalised weight
+    __shared__ float s_l[kCombineMaxW];  // [h][split]: l
     const int Gv = P.Hq / P.Hkv / P.vsub;
     const int REC = Gv * (D + 2);
+    const int NS = P.splits;
     grid_dep_launch();
     grid_dep_wait();  // the split kernel's partial records
     const int bvg = blockIdx.x;
     const int nvg = P.Hkv * P.vsub;
     const int b = bvg / nvg, vg = bvg - b * nvg;
-    const float *recs = P.partials + (size_t)bvg * P.splits * REC;
-    for (int idx = threadIdx.x; idx < Gv * D; idx += blockDim.x) {
-        const int h = idx / D, c = idx - h * D;
+    const float *recs = P.partials + (size_t)bvg * NS * REC;
+    for (int i = threadIdx.x; i < Gv * NS; i += kCombineThreads) {
+        const int h = i / NS, s = i - h * NS;
+        const float *r = recs + (size_t)s * REC + h * (D + 2);
+        s_w[i] = r[D];
+        s_l[i] = r[D + 1];
+    }
+    __syncthreads();
+    for (int h = threadIdx.x; h < Gv; h += kCombineThreads) {
         float M = -INFINITY;
-        for (int s = 0; s < P.splits; ++s) M = fmaxf(M, recs[s * REC + h * (D + 2) + D]);
+        for (int s = 0; s < NS; ++s) M = fmaxf(M, s_w[h * NS + s]);
         const float Mu = (M == -INFINITY) ? 0.0f : M;
-        float acc = 0.0f, lsum = 0.0f;
-        for (int s = 0; s < P.splits; ++s) {
-            const float *r = recs + s * REC + h * (D + 2);
-            const float w = ex2(r[D] - Mu);
-            acc = fmaf(w, r[c], acc);
-            lsum = fmaf(w, r[D + 1], lsum);
+        float L = 0.0f;
+        for (int s = 0; s < NS; ++s) {
+            const float w = ex2(s_w[h * NS + s] - Mu);
+            s_w[h * NS + s] = w;
+            L = fmaf(w, s_l[h * NS + s], L);
         }
-        const float out = lsum > 0.0f ? acc / lsum * (P.fp8 ? P.v_scale : 1.0f) : 0.0f;
-        const __nv_bfloat16 ob = __float2bfloat16_rn(out);
+        const float inv = L > 0.0f ? (P.fp8 ? P.v_scale : 1.0f) / L : 0.0f;
+        for (int s = 0; s < NS; ++s) s_w[h * NS + s] *= inv;
+    }
+    __syncthreads();
+    for (int idx = threadIdx.x; idx < Gv * D; idx += kCombineThreads) {
+        const int h = idx / D, c = idx - h * D;
+        const float *r = recs + h * (D + 2) + c;
+        float acc = 0.0f;
+        for (int s = 0; s < NS; ++s) acc = fmaf(s_w[h * NS + s], r[(size_t)s * REC], acc);
+        const __nv_bfloat16 ob = __float2bfloat16_rn(acc);
         P.out[(size_t)b * P.Hq * D + (size_t)(vg * Gv + h) * D + c] = *reinterpret_cast<const uint16_t *>(&ob);
     }
 }
@@ -776,7 +800,8 @@ cudaError_t run_decode(const DecodeAttentionProblem &p0, unsigned *err, cudaStre
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     // the combine follows the split kernel as its programmatic dependent
-    LaunchCfg lc(dim3(p.B * p.Hkv * p.vsub), dim3(128), 0, stream, true);
+    if ((size_t)(p.Hq / p.Hkv / p.vsub) * p.splits > (size_t)kCombineMaxW) return cudaErrorInvalidValue;
+    LaunchCfg lc(dim3(p.B * p.Hkv * p.vsub), dim3(kCombineThreads), 0, stream, true);
     e = cudaLaunchKernelEx(&lc.cfg, decode_combine_kernel<D>, p);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
