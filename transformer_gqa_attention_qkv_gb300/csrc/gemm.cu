@@ -765,6 +765,188 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
+// Two-SM form for problems with many 256 x 256 output tiles (the prefill
+// projections).  A 2-CTA cluster computes one 256 x 256 tile with MMAs of
+// M = 256 over the CTA pair: each CTA stages its own 128 rows of A and its
+// own half (128 rows) of B, so per MMA each SM's tensor core reads 8 KB of
+// shared memory instead of 12 KB and each SM's copies bring 32 KB per K step
+// instead of 48 KB -- the single-SM 128 x 256 tile is bound by that traffic
+// -- and the lighter stages allow a 6-deep ring.  Each CTA's TMEM holds its
+// 128 accumulator rows, and its epilogue warps run the unchanged epilogue on
+// them.
+//   warp 0 (both CTAs)   TMA: A and B-half k-slices into the local ring; the
+//                        copies' byte counts complete on the even CTA's
+//                        `full` barrier, which only the even CTA arms
+//   warp 1 (even CTA)    MMA issue; each commit arrives on the barrier of
+//                        that offset in both CTAs (stage free, accumulator
+//                        full)
+//   warps 2..5 (both)    epilogue; the accumulator is released by arriving
+//                        on the even CTA's `tempty` (8 arrivals: both CTAs)
+template <int STAGES, int EPI, int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                     const GemmParams P)
+{
+    constexpr int BN = 256, BNH = 128;  // N of the pair's MMA; B rows staged by each CTA
+    constexpr int A_BYTES = BM * BK * 2, B_BYTES = BNH * BK * 2;
+    constexpr int ACC = 256;            // TMEM columns per accumulator
+    constexpr int RING = STAGES * (A_BYTES + B_BYTES);
+    constexpr int BARS = RING;
+    constexpr int TMEM_SLOT = BARS + (2 * STAGES + 5) * 8;
+    constexpr int NORM = (TMEM_SLOT + 16 + 15) & ~15;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t *sA = smem;
+    uint8_t *sB = smem + STAGES * A_BYTES;
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + BARS);
+    uint64_t *empty = full + STAGES;
+    uint64_t *tfull = empty + STAGES;
+    uint64_t *tempty = tfull + 2;
+    uint64_t *drain = tempty + 2;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + TMEM_SLOT);
+    float *s_norm = reinterpret_cast<float *>(smem + NORM);
+
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    unsigned *err = P.err;
+    grid_dep_launch();  // the next kernel may start its prologue meanwhile
+    const uint32_t rank = cluster_rank();  // 0: the CTA that issues the MMAs
+    const int tile0 = (int)(blockIdx.x / 2), tile_step = (int)(gridDim.x / 2);
+    const int kb0 = 0, kb1 = P.num_k;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(full + s, 1);   // armed by the even CTA's producer (both CTAs' bytes)
+            mbar_init(empty + s, 1);  // one multicast commit per fill
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(tfull + a, 1);
+            mbar_init(tempty + a, 8);  // the epilogue warps of both CTAs
+        }
+        mbar_init(drain, 1);
+        fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tmA);
+        tma_prefetch_desc(&tmB);
+    }
+    if (warp == 1) tmem_alloc_pair(tmem_slot, 2 * ACC);
+    if (EPI == EPI_QKV && warp >= 2 && P.qkv.q_norm_w) {
+        for (int i = threadIdx.x - 64; i < D; i += 128) {
+            s_norm[i] = __uint_as_float((uint32_t)P.qkv.q_norm_w[i] << 16);
+            s_norm[256 + i] = __uint_as_float((uint32_t)P.qkv.k_norm_w[i] << 16);
+        }
+    }
+    __syncthreads();
+    cluster_sync();  // both CTAs' barriers initialised before any copy or arrival reaches them
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const uint32_t full_lead = cluster_map(smem_u32(full), 0);      // the even CTA's full[0]
+    const uint32_t tempty_lead = cluster_map(smem_u32(tempty), 0);  // the even CTA's tempty[0]
+
+    if (warp == 0) {
+        if (lane == 0) {
+            auto load_a = [&](int s, int mb, int kb) {
+                tma_load_2d_pair(sA + s * A_BYTES, &tmA, kb * BK, mb * 2 * BM + (int)rank * BM, full_lead + 8 * s);
+            };
+            auto load_b = [&](int s, int nb, int kb) {
+                tma_load_2d_pair(sB + s * B_BYTES, &tmB, kb * BK, nb * BN + (int)rank * BNH, full_lead + 8 * s);
+            };
+            auto arm = [&](int s) {
+                if (rank == 0) mbar_arrive_expect_tx(full + s, 2 * (A_BYTES + B_BYTES));
+            };
+            // the weights (B) do not come from the previous kernel: the first ring
+            // fill's B tiles go out before waiting for it
+            int pre = 0;
+            if (tile0 < P.num_tiles) {
+                int mb, nb;
+                tile_coords(tile0, P.num_m, P.num_n, P.group_m, mb, nb);
+                for (int kb = kb0; kb < kb1 && pre < STAGES; ++kb, ++pre) {
+                    arm(pre);
+                    load_b(pre, nb, kb);
+                }
+            }
+            grid_dep_wait();
+            int it = 0;
+            bool ok = true;
+            for (int tile = tile0; ok && tile < P.num_tiles; tile += tile_step) {
+                int mb, nb;
+                tile_coords(tile, P.num_m, P.num_n, P.group_m, mb, nb);
+                for (int kb = kb0; kb < kb1; ++kb, ++it) {
+                    const int s = it % STAGES;
+                    if (it >= pre) {
+                        const uint32_t ph = (it / STAGES) & 1;
+                        if (!mbar_wait(empty + s, ph ^ 1, err)) {
+                            ok = false;
+                            break;
+                        }
+                        arm(s);
+                        load_b(s, nb, kb);
+                    }
+                    load_a(s, mb, kb);
+                }
+            }
+            // every fill has been consumed (so every copy has landed) before the CTA may exit
+            for (int j = max(0, it - STAGES); j < it; ++j) mbar_wait(empty + j % STAGES, (j / STAGES) & 1, err);
+        }
+    } else if (warp == 1) {
+        if (lane == 0 && rank == 0) {
+            constexpr uint32_t idesc = idesc_bf16_f32(2 * BM, BN, 0, 0);
+            int it = 0, use = 0;
+            bool ok = true;
+            for (int tile = tile0; ok && tile < P.num_tiles; tile += tile_step, ++use) {
+                const int acc = use & 1;
+                if (!mbar_wait<true>(tempty + acc, ((use >> 1) & 1) ^ 1, err)) break;
+                tc_fence_after();
+                const uint32_t d_tmem = tmem + acc * ACC;
+                for (int kb = kb0; kb < kb1; ++kb, ++it) {
+                    const int s = it % STAGES;
+                    if (!mbar_wait<true>(full + s, (it / STAGES) & 1, err)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a0 = smem_u32(sA + s * A_BYTES);
+                    const uint32_t b0 = smem_u32(sB + s * B_BYTES);
+#pragma unroll
+                    for (int k = 0; k < BK / 16; ++k)
+                        umma_f16_ss_pair(d_tmem, sw128_desc(a0 + 32 * k, 16, 1024), sw128_desc(b0 + 32 * k, 16, 1024),
+                                         idesc, (kb != kb0 || k != 0) ? 1u : 0u);
+                    umma_commit_pair(empty + s, 0x3);  // frees stage s in both CTAs
+                }
+                if (!ok) break;
+                umma_commit_pair(tfull + acc, 0x3);  // both CTAs' accumulator rows ready
+            }
+            umma_commit_pair(drain, 0x1);
+            mbar_wait(drain, 0, err);
+        }
+    } else {
+        const int quarter = warp & 3;  // TMEM lanes this warp may access
+        const int row = quarter * 32 + lane;
+        grid_dep_wait();  // the epilogue reads and writes what the previous kernel may touch
+        int use = 0;
+        for (int tile = tile0; tile < P.num_tiles; tile += tile_step, ++use) {
+            int mb, nb;
+            tile_coords(tile, P.num_m, P.num_n, P.group_m, mb, nb);
+            const int acc = use & 1;
+            const int m = mb * 2 * BM + (int)rank * BM + row;
+            epilogue_prefetch<BN, EPI, D>(P, m, nb * BN, m < P.M);
+            if (!mbar_wait<true>(tfull + acc, (use >> 1) & 1, err)) break;
+            tc_fence_after();
+            const uint32_t tcol = tmem + ((uint32_t)(quarter * 32) << 16) + acc * ACC;
+            epilogue_tile<BN, EPI, D>(P, tcol, m, nb * BN, m < P.M, s_norm);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(tempty_lead + 8 * acc);
+        }
+    }
+    __syncthreads();
+    cluster_sync();  // no CTA of the pair leaves while the other may still use its TMEM or barriers
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc_pair(tmem, 2 * ACC);
+    }
+}
+
 template <int BN, int STAGES, int EPI, int D, int MAJ = 0, int KS = 1>
 cudaError_t run(const GemmProblem &p, const GemmParams &params, int num_sms, cudaStream_t stream)
 {
@@ -850,6 +1032,45 @@ GemmParams make_params(const GemmProblem &p, int BN, unsigned *err)
     return g;
 }
 
+// The pair kernel over 256 x 256 tiles (tile rows of 256 = two CTAs' 128), as
+// many 2-CTA clusters as fit on the GPU at once; returns cudaErrorNotSupported
+// when the cluster shape cannot be placed (the caller then runs the single-SM
+// kernel).
+template <int STAGES, int EPI, int D>
+cudaError_t run_pair(const GemmProblem &p, GemmParams params, int group_m, cudaStream_t stream)
+{
+    constexpr int SMEM = STAGES * (BM * BK * 2 + 128 * BK * 2) + (2 * STAGES + 5) * 8 + 32 + 2 * 256 * 4 + 1024;
+    CUtensorMap ta, tb;
+    const uint64_t dA[2] = {(uint64_t)p.K, (uint64_t)p.M};
+    const uint64_t sA[1] = {(uint64_t)p.K * 2};
+    const uint64_t dB[2] = {(uint64_t)p.K, (uint64_t)p.N};
+    const uint64_t sB[1] = {(uint64_t)p.K * 2};
+    const uint32_t bA[2] = {(uint32_t)BK, (uint32_t)BM};
+    const uint32_t bB[2] = {(uint32_t)BK, 128u};
+    if (encode_tmap(&ta, p.A, 2, dA, sA, bA, true) != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    if (encode_tmap(&tb, p.B, 2, dB, sB, bB, true) != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    params.num_m = (p.M + 2 * BM - 1) / (2 * BM);  // pair-tile rows
+    params.num_n = (p.N + 255) / 256;
+    params.num_tiles = params.num_m * params.num_n;
+    params.group_m = group_m;
+    auto kern = gemm_pair_kernel<STAGES, EPI, D>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
+    if (e != cudaSuccess) return e;
+    int clusters = 0;
+    {
+        LaunchCfg probe(dim3(2), dim3(kThreads), SMEM, stream, false, 2);
+        if (cudaOccupancyMaxActiveClusters(&clusters, kern, &probe.cfg) != cudaSuccess || clusters < 1) {
+            cudaGetLastError();
+            return cudaErrorNotSupported;
+        }
+    }
+    const int n = params.num_tiles < clusters ? params.num_tiles : clusters;
+    LaunchCfg lc(dim3(2 * n), dim3(kThreads), SMEM, stream, p.pdl != 0, 2);
+    e = cudaLaunchKernelEx(&lc.cfg, kern, ta, tb, params);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+}
+
 }  // namespace
 
 cudaError_t launch_gemm_qkv(const GemmProblem &p, const QkvEpilogue &e, unsigned *err, int num_sms,
@@ -866,6 +1087,8 @@ cudaError_t launch_gemm_qkv(const GemmProblem &p, const QkvEpilogue &e, unsigned
         }
         GemmParams g = make_params(p, 256, err);
         g.qkv = e;
+        const cudaError_t pe = run_pair<6, EPI_QKV, 128>(p, g, 16, stream);
+        if (pe != cudaErrorNotSupported) return pe;
         return run<256, 4, EPI_QKV, 128>(p, g, num_sms, stream);
     }
     if (e.d == 256) {  // one 256-wide head per tile, also for decode-sized problems
@@ -881,6 +1104,8 @@ cudaError_t launch_gemm_qkv(const GemmProblem &p, const QkvEpilogue &e, unsigned
         }
         GemmParams g = make_params(p, 256, err);
         g.qkv = e;
+        const cudaError_t pe = run_pair<6, EPI_QKV, 64>(p, g, 16, stream);
+        if (pe != cudaErrorNotSupported) return pe;
         return run<256, 4, EPI_QKV, 64>(p, g, num_sms, stream);
     }
     // widths that do not divide 256: a tile of whole heads (3 x 80, 2 x 96)
@@ -907,7 +1132,10 @@ cudaError_t launch_gemm_residual(const GemmProblem &p, const ResidualEpilogue &e
     }
     GemmParams g = make_params(p, 256, err);
     g.res = e;
-    g.group_m = 16;  // o_proj's A panels are twice as long (K = Hq*d): half the group
+    // o_proj's A panels are twice as long (K = Hq*d): half the QKV projection's group
+    const cudaError_t pe = run_pair<6, EPI_RESIDUAL, 0>(p, g, 8, stream);
+    if (pe != cudaErrorNotSupported) return pe;
+    g.group_m = 16;
     return run<256, 4, EPI_RESIDUAL, 0>(p, g, num_sms, stream);
 }
 

@@ -59,29 +59,42 @@ DEVI void mbar_arrive(uint64_t *bar)
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
+// CLUSTER: acquire at cluster scope (the phase completes with arrivals from
+// another CTA of the cluster whose earlier writes must be visible).
+template <bool CLUSTER = false>
 DEVI bool mbar_try_wait(uint32_t bar, uint32_t parity)
 {
     uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
+    if constexpr (CLUSTER)
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}"
+            : "=r"(ok)
+            : "r"(bar), "r"(parity)
+            : "memory");
+    else
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}"
+            : "=r"(ok)
+            : "r"(bar), "r"(parity)
+            : "memory");
     return ok != 0;
 }
 
 // Wait until the phase with the given parity has completed.  Gives up after
 // limit_ns (recording kErrTimeout in *err) or as soon as another thread of the
 // grid has recorded a timeout.  Returns true when the phase completed.
+template <bool CLUSTER = false>
 DEVI bool mbar_wait(uint64_t *bar, uint32_t parity, unsigned *err, uint64_t limit_ns = kWaitLimitNs)
 {
     const uint32_t a = smem_u32(bar);
-    if (mbar_try_wait(a, parity)) return true;
+    if (mbar_try_wait<CLUSTER>(a, parity)) return true;
     const uint64_t t0 = globaltimer();
     for (uint32_t i = 1;; ++i) {
-        if (mbar_try_wait(a, parity)) return true;
+        if (mbar_try_wait<CLUSTER>(a, parity)) return true;
         if ((i & 63u) == 0) {
             if (*(volatile unsigned *)err & kErrTimeout) return false;
             if (globaltimer() - t0 > limit_ns) {
@@ -266,6 +279,68 @@ DEVI void umma_commit(uint64_t *bar)
 {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
                  : "memory");
+}
+
+// ------------------------------------------------ CTA pairs (.cta_group::2)
+// The two CTAs of a 2-CTA cluster share one MMA of M = 256: A rows 0-127 and
+// B rows 0 .. N/2-1 come from the even CTA's shared memory, A rows 128-255
+// and B rows N/2 .. N-1 from the odd CTA's (the same offsets in both), and
+// the accumulator rows sit in the two CTAs' TMEM (rows 0-127 in the even CTA,
+// 128-255 in the odd one), at the same address.  A kernel that uses these
+// uses no .cta_group::1 form.
+
+// One warp of EACH CTA of the pair: allocate ncols TMEM columns in both.
+DEVI void tmem_alloc_pair(uint32_t *dst, uint32_t ncols)
+{
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst)), "r"(ncols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+
+// One warp of EACH CTA of the pair.
+DEVI void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols)
+{
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+// One thread of the even CTA: D (+)= A * B^T over the pair.
+DEVI void umma_f16_ss_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// The issuing thread: when its pair MMAs so far have completed, arrive once on
+// the mbarrier at this offset in every CTA of cta_mask.
+DEVI void umma_commit_pair(uint64_t *bar, uint16_t cta_mask)
+{
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+            smem_u32(bar)),
+        "h"(cta_mask)
+        : "memory");
+}
+
+// Tensor copy into this CTA's shared memory whose completion (bytes) is
+// counted on the mbarrier at cluster address bar_cl, which may be the peer
+// CTA's.
+DEVI void tma_load_2d_pair(void *dst, const CUtensorMap *tm, int x, int y, uint32_t bar_cl)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.cta_group::2"
+        " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
+        "l"((uint64_t)tm), "r"(x), "r"(y), "r"(bar_cl)
+        : "memory");
+}
+
+// Arrive once on the mbarrier at cluster address bar_cl (this or another CTA).
+DEVI void mbar_arrive_cluster(uint32_t bar_cl)
+{
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cl) : "memory");
 }
 
 DEVI void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
