@@ -22,19 +22,21 @@
 //               group takes 16 keys of its group's chunks.  The query heads
 //               sharing each K/V row make it a genuine heads x d by d x keys
 //               product, computed with warp-level mma.sync m16n8k16:
-//     bf16 caches: heads in the MMA's 16 rows (up to GM = 16 heads per item),
-//               S = Q K^T with K fragments read by ldmatrix from the swizzled
-//               tile; the binary16 query is split into bf16 high and low parts
-//               (two MMAs) so no query precision is lost; online softmax in the
-//               S accumulator registers, whose layout is already the A
-//               fragment of O += P V (P also split into high and low parts),
-//               with V fragments from ldmatrix.trans;
-//     E4M3 caches: transposed products, S^T = K Q^T (16 keys in the rows, up
-//               to GM = 8 heads in the 8 columns) and O^T = V^T P^T (d in the
-//               rows): one MMA covers 16 keys x 8 heads, half the MMAs of the
-//               heads-in-rows form, and P^T reaches the B-fragment layout by
-//               an 8x8 transpose (movmatrix).  E4M3 widens exactly to binary16,
-//               so the MMAs are binary16 and the query needs no split.
+//     bf16 caches, groups of up to 8 heads (GM = 8): transposed products,
+//               S^T = K Q^T (16 keys in the MMA rows, the heads in its 8
+//               columns) and O^T = V^T P^T (d in the rows), K the A fragment
+//               straight from ldmatrix, V^T from ldmatrix.trans, P^T reaching
+//               the B-fragment layout by an 8x8 transpose (movmatrix); the
+//               binary16 query and P are split into bf16 high and low parts
+//               (two MMAs each) so no precision is lost;
+//     bf16 caches, 9 to 16 heads (GM = 16): heads in the MMA's 16 rows,
+//               S = Q K^T, online softmax in the S accumulator registers,
+//               whose layout is already the A fragment of O += P V (q and P
+//               split the same way), V fragments from ldmatrix.trans;
+//     E4M3 caches: the transposed products of the first form (up to GM = 8
+//               heads); E4M3 widens exactly to binary16, so the MMAs are
+//               binary16 and the query needs no split.
+//   Online softmax in the accumulator registers in every form.
 //   At the end of an item the warps' (max, sum, unnormalised output) are
 //   merged in shared memory into one fp32 partial record.
 // A group of more than GM query heads is taken as vsub sub-groups of G / vsub
