@@ -1130,7 +1130,7 @@ static int run_widen(DeviceState &st, const gqa_bf16 *k_cache, const gqa_bf16 *v
                      uint16_t *v16, const int *cache_len, int B, int S, int Hkv, int d, int Lmax, cudaStream_t stream,
                      int pdl)
 {
-    CacheWiden w{k_cache, v_cache, k16, v16, cache_len, B, S, Hkv, Lmax, d, d == 256 ? 64 : 128, pdl};
+    CacheWiden w{k_cache, v_cache, k16, v16, cache_len, B, S, Hkv, Lmax, d, 128, pdl};  // key tiles of 128
     cudaError_t ce = launch_cache_widen(w, st.err, stream);
     if (ce != cudaSuccess) return cuda_fail(ce, "cache widening launch");
     ++g_launches;

@@ -365,10 +365,347 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
+// ------------------------------------------------------------ CTA pairs
+// The same attention on 2-CTA clusters (.cta_group::2).  A pair takes two
+// consecutive query blocks of one (b, KV head); its MMAs have M = 256 (each
+// CTA's 128 packed rows) and read each B operand half from each CTA's shared
+// memory, so S tiles are 128 keys wide (N = 128, the tensor core's full rate;
+// 64-wide products run at ~60% of it) while each CTA still stages only 32 KB
+// per K or V tile:
+//   S(j) = Q K(j)^T   N = 128 keys: CTA r stages keys [64r, 64r + 64) of the
+//                     tile, all 256 d; each CTA's TMEM receives its rows x 128
+//   O += P(j) V(j)    N = 256 d: CTA r stages d [128r, 128r + 128) of all 128
+//                     keys (MN-major); A = P from each CTA's TMEM
+// The even CTA's thread issues every MMA once both CTAs' operands are in place:
+// the tensor copies of both CTAs count their bytes on the even CTA's full
+// barriers, both CTAs' softmax warps arrive on its P barriers, and each MMA
+// commit arrives on the barrier at the same offset in both CTAs.  The keys
+// walked are those of the pair's later block (the earlier block masks the
+// keys past its rows).
+//
+//   TMEM (each CTA)  S buffer 0 [0, 128), S buffer 1 [128, 256), O [256, 512)
+//   smem (each CTA)  Q 64 KB, a 3-stage K ring and a 2-stage V ring (32 KB
+//                    stages): 224 KB
+constexpr int kPKeys = 128;  // keys per tile of the pair
+constexpr int kPKst = 3;
+constexpr int kPVst = 2;
+
+struct SmemPair {
+    static constexpr int QCH = kRows * 128;            // 16 KB: 128 rows x 64 16-bit values
+    static constexpr int BOX = 64 * 128;               // 8 KB: 64 keys x 64 16-bit values
+    static constexpr int KST = kNch * BOX;             // 32 KB: this CTA's 64 keys x 256 d
+    static constexpr int VCH = kPKeys * 128;           // 16 KB: 128 keys x 64 d
+    static constexpr int VST = 2 * VCH;                // 32 KB: 128 keys x this CTA's 128 d
+    static constexpr int Q = 0;
+    static constexpr int K = Q + kNch * QCH;
+    static constexpr int V = K + kPKst * KST;
+    static constexpr int BARS = V + kPVst * VST;       // 224 KB of tiles
+    // q_full, k_full[3], k_empty[3], v_full[2], v_empty[2], s_full[2], p_full[2], pv_done, o_done, drain
+    static constexpr int NBARS = 1 + 2 * kPKst + 2 * kPVst + 2 + 2 + 3;
+    static constexpr int TMEM_SLOT = BARS + NBARS * 8;
+    static constexpr int TOTAL = TMEM_SLOT + 16;
+    static constexpr int ALLOC = TOTAL + 1024;
+};
+static_assert(SmemPair::ALLOC <= 232448, "shared memory per CTA");
+
+template <bool CACHED>
+__global__ void __launch_bounds__(kThreads, 1)
+    attn256_pair_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                        const __grid_constant__ CUtensorMap tmV, const Params256 P)
+{
+    using L = SmemPair;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::BARS);
+    uint64_t *q_full = bars;
+    uint64_t *k_full = q_full + 1;
+    uint64_t *k_empty = k_full + kPKst;
+    uint64_t *v_full = k_empty + kPKst;
+    uint64_t *v_empty = v_full + kPVst;
+    uint64_t *s_full = v_empty + kPVst;
+    uint64_t *p_full = s_full + 2;
+    uint64_t *pv_done = p_full + 2;
+    uint64_t *o_done = pv_done + 1;
+    uint64_t *drain = o_done + 1;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::TMEM_SLOT);
+
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    unsigned *err = P.err;
+    const uint32_t rank = cluster_rank();  // 0: the CTA that issues the MMAs
+
+    // heavy (late) query blocks first; the pair's blocks are consecutive
+    const int pair = (int)blockIdx.x / 2;
+    const int n_qp = (P.n_qblk + 1) / 2;
+    const int bh = pair % (P.B * P.Hkv);
+    const int qp = n_qp - 1 - pair / (P.B * P.Hkv);
+    const int b = bh / P.Hkv, g = bh % P.Hkv;
+    const int t0 = (2 * qp + (int)rank) * P.R;           // >= S for the odd CTA of a last odd block: no rows
+    const int t_last = min((2 * qp + 2) * P.R, P.S) - 1;  // the pair's last position
+    int p0 = 0;
+    bool bad = false;
+    if constexpr (CACHED) {
+        p0 = P.kv_start[b];
+        bad = p0 < 0 || p0 + P.S > P.kv_seq;
+        if (bad) {
+            if (threadIdx.x == 0 && rank == 0) atomicOr(P.err, kErrIndex);
+            p0 = 0;
+        }
+    }
+    const int n_kv = bad ? 0 : (P.causal ? ((p0 + t_last) / kPKeys + 1) : (p0 + P.S + kPKeys - 1) / kPKeys);
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < L::NBARS; ++i) mbar_init(bars + i, 1);
+        mbar_init(p_full, 8);  // the softmax warps of both CTAs
+        mbar_init(p_full + 1, 8);
+        fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tmQ);
+        tma_prefetch_desc(&tmK);
+        tma_prefetch_desc(&tmV);
+    }
+    if (warp == 1) tmem_alloc_pair(tmem_slot, 512);
+    __syncthreads();
+    cluster_sync();  // both CTAs' barriers initialised before any copy or arrival reaches them
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    auto lead = [&](uint64_t *bar) { return cluster_map(smem_u32(bar), 0); };  // the even CTA's barrier
+
+    if (warp == 0) {
+        if (lane == 0) {
+            bool ok = true;
+            auto arm = [&](uint64_t *bar, uint32_t bytes) {
+                if (rank == 0) mbar_arrive_expect_tx(bar, 2 * bytes);  // both CTAs' copies
+            };
+            auto load_k = [&](int j) {
+                const int s = j % kPKst;
+                if (!mbar_wait<true>(k_empty + s, ((j / kPKst) & 1) ^ 1, err)) return false;
+                arm(k_full + s, L::KST);
+                for (int c = 0; c < kNch; ++c)
+                    tma_load_3d_pair(smem + L::K + s * L::KST + c * L::BOX, &tmK, c * 64,
+                                     j * kPKeys + (int)rank * 64, b * P.Hkv + g, lead(k_full + s));
+                return true;
+            };
+            auto load_v = [&](int j) {
+                const int s = j % kPVst;
+                if (!mbar_wait<true>(v_empty + s, ((j / kPVst) & 1) ^ 1, err)) return false;
+                arm(v_full + s, L::VST);
+                for (int c = 0; c < 2; ++c)
+                    for (int h = 0; h < 2; ++h)
+                        tma_load_3d_pair(smem + L::V + s * L::VST + c * L::VCH + h * L::BOX, &tmV,
+                                         ((int)rank * 2 + c) * 64, j * kPKeys + h * 64, b * P.Hkv + g,
+                                         lead(v_full + s));
+                return true;
+            };
+            arm(q_full, kNch * 64 * 2 * P.R * P.G);
+            for (int c = 0; c < kNch; ++c)
+                tma_load_3d_pair(smem + L::Q + c * L::QCH, &tmQ, c * 64, t0, b * P.Hq + g * P.G, lead(q_full));
+            int nk = 0, nv = 0;  // tiles issued
+            if (n_kv > 0) {
+                ok = load_k(0);
+                if (ok) nk = 1;
+            }
+            for (int j = 1; ok && j < n_kv; ++j) {
+                ok = load_k(j);
+                if (ok) nk = j + 1;
+                if (ok) ok = load_v(j - 1);
+                if (ok) nv = j;
+            }
+            if (ok && n_kv > 0 && load_v(n_kv - 1)) nv = n_kv;
+            // every issued copy of both CTAs has landed before the pair may exit
+            // (the full barriers count both CTAs' bytes; the odd CTA waits for the
+            // even one at the final cluster barrier)
+            if (rank == 0) {
+                mbar_wait<true>(q_full, 0, err);
+                for (int j = max(0, nk - kPKst); j < nk; ++j)
+                    mbar_wait<true>(k_full + j % kPKst, (j / kPKst) & 1, err);
+                for (int j = max(0, nv - kPVst); j < nv; ++j)
+                    mbar_wait<true>(v_full + j % kPVst, (j / kPVst) & 1, err);
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0 && rank == 0) {
+            constexpr uint32_t idesc_s = idesc_f16_f32(2 * kRows, kPKeys, 0, 0);
+            constexpr uint32_t idesc_o = idesc_f16_f32(2 * kRows, kD, 0, 1);
+            constexpr uint16_t kBoth = 3;
+            const uint32_t sQ = smem_u32(smem + L::Q);
+            auto issue_s = [&](int buf, int j) {  // S(j) = Q K(j)^T into S buffer buf of both CTAs
+                const uint32_t sK = smem_u32(smem + L::K + (j % kPKst) * L::KST);
+#pragma unroll
+                for (int c = 0; c < kNch; ++c)
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        umma_f16_ss_pair(tmem + kPKeys * buf, sw128_desc(sQ + c * L::QCH + 32 * k, 16, 1024),
+                                         sw128_desc(sK + c * L::BOX + 32 * k, 16, 1024), idesc_s, (c | k) != 0);
+                umma_commit_pair(k_empty + j % kPKst, kBoth);
+                umma_commit_pair(s_full + buf, kBoth);
+            };
+            bool ok = (!CACHED || n_kv > 0) && mbar_wait<true>(q_full, 0, err) && mbar_wait<true>(k_full, 0, err);
+            if (ok) {
+                tc_fence_after();
+                issue_s(0, 0);
+                if (n_kv > 1) {
+                    ok = mbar_wait<true>(k_full + 1, 0, err);
+                    if (ok) {
+                        tc_fence_after();
+                        issue_s(1, 1);
+                    }
+                }
+            }
+            const uint32_t tO = tmem + 256;
+            for (int j = 0; ok && j < n_kv; ++j) {
+                const int buf = j & 1;
+                if (!mbar_wait<true>(p_full + buf, (j >> 1) & 1, err) ||
+                    !mbar_wait<true>(v_full + j % kPVst, (j / kPVst) & 1, err)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t sV = smem_u32(smem + L::V + (j % kPVst) * L::VST);
+#pragma unroll
+                for (int k = 0; k < kPKeys / 16; ++k)  // 16 keys = 8 packed TMEM columns of P
+                    umma_f16_ts_pair(tO, tmem + kPKeys * buf + 8 * k, sw128_desc(sV + k * 16 * 128, L::VCH, 1024),
+                                     idesc_o, (j | k) != 0);
+                umma_commit_pair(v_empty + j % kPVst, kBoth);
+                umma_commit_pair(pv_done, kBoth);
+                if (j + 2 < n_kv) {
+                    if (!mbar_wait<true>(k_full + (j + 2) % kPKst, ((j + 2) / kPKst) & 1, err)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    issue_s(buf, j + 2);
+                }
+            }
+            if (ok && n_kv > 0) umma_commit_pair(o_done, kBoth);
+            umma_commit_pair(drain, 1);
+            mbar_wait(drain, 0, err);
+        }
+    } else {
+        const int quarter = warp & 3;  // TMEM lanes this warp may access
+        const int r = quarter * 32 + lane;
+        const int hl = r / P.R, tl = r - hl * P.R;
+        const bool in_pack = hl < P.G;
+        const int t = t0 + tl;
+        const bool row_ok = in_pack && t < P.S;
+        const int lim = !in_pack ? -1 : (P.causal ? p0 + min(t, P.S - 1) : p0 + P.S - 1);
+        const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+        const uint32_t tO = tmem + lane_off + 256;
+        const float sl = P.scale_log2;
+        float m_i = -INFINITY, l_i = 0.0f;
+
+        for (int j = 0; j < n_kv; ++j) {
+            const int buf = j & 1;
+            if (!mbar_wait<true>(s_full + buf, (j >> 1) & 1, err)) break;
+            tc_fence_after();
+            const uint32_t tS = tmem + lane_off + kPKeys * buf;
+            const int u0 = j * kPKeys;
+            // the S row (two 64-column reducing loads) and its maximum
+            uint32_t va[64], vb[64];
+            float mxa, mxb;
+            tmem_ld64_max(tS, va, mxa);
+            tmem_ld64_max(tS + 64, vb, mxb);
+            float mx = fmaxf(mxa, mxb);
+            if (u0 + kPKeys - 1 > lim) {  // diagonal or ragged tile: mask keys past lim, max of the rest
+#pragma unroll
+                for (int e = 0; e < 64; ++e) {
+                    if (u0 + e > lim) va[e] = __float_as_uint(-INFINITY);
+                    if (u0 + 64 + e > lim) vb[e] = __float_as_uint(-INFINITY);
+                }
+                float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+                for (int e = 0; e < 64; e += 4)
+#pragma unroll
+                    for (int k = 0; k < 2; ++k) {
+                        mx4[k] = fmax3(mx4[k], __uint_as_float(va[e + 2 * k]), __uint_as_float(va[e + 2 * k + 1]));
+                        mx4[2 + k] =
+                            fmax3(mx4[2 + k], __uint_as_float(vb[e + 2 * k]), __uint_as_float(vb[e + 2 * k + 1]));
+                    }
+                mx = fmaxf(fmax3(mx4[0], mx4[1], mx4[2]), mx4[3]);
+            }
+            const float m_cand = fmaxf(m_i, mx * sl);
+            float m_new = m_i, alpha = 1.0f;
+            if (m_cand > m_i + kRescaleThreshold) {
+                m_new = m_cand;
+                alpha = ex2(m_i - m_new);  // 0 on the first tile
+            }
+            const float m_use = (m_new == -INFINITY) ? 0.0f : m_new;
+            const float2 sl2 = make_float2(sl, sl), nm2 = make_float2(-m_use, -m_use);
+            float2 rs2[2] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f)};
+#pragma unroll
+            for (int c = 0; c < kPKeys / 32; ++c) {
+                const uint32_t *v = c < 2 ? va + 32 * c : vb + 32 * (c - 2);
+                uint32_t pk[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                    const float2 x = __ffma2_rn(
+                        make_float2(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1])), sl2, nm2);
+                    const float2 p = make_float2(ex2(x.x), ex2(x.y));
+                    rs2[e & 1] = __fadd2_rn(rs2[e & 1], p);
+                    pk[e] = pack_f16(p.x, p.y);
+                }
+                tmem_st16_nowait(tS + 16 * c, pk);
+            }
+            tmem_st_wait();
+            const float rs = (rs2[0].x + rs2[0].y) + (rs2[1].x + rs2[1].y);
+            l_i = l_i * alpha + rs;
+            m_i = m_new;
+            // O holds PV(0..j-1) once PV(j-1) has completed (PV(j) waits for this P)
+            if (j > 0 && __any_sync(0xffffffffu, alpha != 1.0f)) {
+                if (!mbar_wait<true>(pv_done, (j - 1) & 1, err)) break;
+                tc_fence_after();
+#pragma unroll 1
+                for (int c = 0; c < kD; c += 32) {
+                    uint32_t o[32];
+                    tmem_ld32(tO + c, o);
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+                    tmem_st32(tO + c, o);
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(lead(p_full + buf));
+        }
+        if (CACHED && n_kv == 0) {  // rejected offset (reported): zero rows, nothing else ran
+            if (row_ok) {
+                uint4 *d4 = reinterpret_cast<uint4 *>(P.out + ((size_t)(b * P.S + t) * P.Hq + g * P.G + hl) * kD);
+                for (int c = 0; c < kD / 8; ++c) d4[c] = make_uint4(0, 0, 0, 0);
+            }
+        } else if (mbar_wait<true>(o_done, 0, err)) {
+            tc_fence_after();
+            const float inv_l = (l_i > 0.0f) ? 1.0f / l_i : 0.0f;
+            uint16_t *dst = P.out + ((size_t)(b * P.S + t) * P.Hq + g * P.G + hl) * kD;
+#pragma unroll 1
+            for (int c = 0; c < kD; c += 32) {
+                uint32_t o[32];
+                tmem_ld32(tO + c, o);
+                if (row_ok) {
+                    uint4 *d4 = reinterpret_cast<uint4 *>(dst + c);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        uint32_t w[4];
+#pragma unroll
+                        for (int k = 0; k < 4; ++k)
+                            w[k] = pack_bf16(__uint_as_float(o[8 * i + 2 * k]) * inv_l,
+                                             __uint_as_float(o[8 * i + 2 * k + 1]) * inv_l);
+                        d4[i] = make_uint4(w[0], w[1], w[2], w[3]);
+                    }
+                }
+            }
+        }
+    }
+    __syncthreads();
+    cluster_sync();  // no CTA leaves while the other's copies, MMAs or arrivals may still reach it
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc_pair(tmem, 512);
+    }
+}
+
 template <bool CACHED>
 cudaError_t run_attn256(const AttentionProblem &p, unsigned *err, cudaStream_t stream)
 {
-    using L = Smem256;
     const int G = p.Hq / p.Hkv;
     const int R = kRows / G;
     CUtensorMap tq, tk, tv;
@@ -397,10 +734,28 @@ cudaError_t run_attn256(const AttentionProblem &p, unsigned *err, cudaStream_t s
     a.scale_log2 = 1.4426950408889634f / 16.0f;  // log2(e) / sqrt(256)
     a.out = p.out;
     a.err = err;
+
+    // CTA pairs when the cluster shape can be placed, else one CTA per block
+    {
+        auto kern = attn256_pair_kernel<CACHED>;
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SmemPair::ALLOC);
+        if (e != cudaSuccess) return e;
+        int clusters = 0;
+        LaunchCfg probe(dim3(2), dim3(kThreads), SmemPair::ALLOC, stream, false, 2);
+        if (cudaOccupancyMaxActiveClusters(&clusters, kern, &probe.cfg) == cudaSuccess && clusters >= 1) {
+            const long long grid = 2LL * ((a.n_qblk + 1) / 2) * p.B * p.Hkv;
+            if (grid > 0x7fffffffLL) return cudaErrorInvalidValue;
+            LaunchCfg lc(dim3((unsigned)grid), dim3(kThreads), SmemPair::ALLOC, stream, false, 2);
+            e = cudaLaunchKernelEx(&lc.cfg, kern, tq, tk, tv, a);
+            if (e != cudaSuccess) return e;
+            return cudaGetLastError();
+        }
+        cudaGetLastError();
+    }
     auto kern = attn256_kernel<CACHED>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC);
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Smem256::ALLOC);
     if (e != cudaSuccess) return e;
-    kern<<<p.B * p.Hkv * a.n_qblk, kThreads, L::ALLOC, stream>>>(tq, tk, tv, a);
+    kern<<<p.B * p.Hkv * a.n_qblk, kThreads, Smem256::ALLOC, stream>>>(tq, tk, tv, a);
     return cudaGetLastError();
 }
 

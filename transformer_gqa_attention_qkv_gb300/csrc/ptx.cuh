@@ -337,6 +337,29 @@ DEVI void tma_load_2d_pair(void *dst, const CUtensorMap *tm, int x, int y, uint3
         : "memory");
 }
 
+// 3-D form of tma_load_2d_pair.
+DEVI void tma_load_3d_pair(void *dst, const CUtensorMap *tm, int x, int y, int z, uint32_t bar_cl)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.cta_group::2"
+        " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(dst)),
+        "l"((uint64_t)tm), "r"(x), "r"(y), "r"(z), "r"(bar_cl)
+        : "memory");
+}
+
+// One thread of the even CTA: D (+)= A * B over the pair, A from TMEM (each
+// CTA's 128 rows at the same TMEM address), B from shared memory as in
+// umma_f16_ss_pair.
+DEVI void umma_f16_ts_pair(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc, uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 // Arrive once on the mbarrier at cluster address bar_cl (this or another CTA).
 DEVI void mbar_arrive_cluster(uint32_t bar_cl)
 {
