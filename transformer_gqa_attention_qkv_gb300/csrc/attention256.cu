@@ -665,7 +665,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive_cluster(lead(p_full + buf));
+            // P (and any rescaled O) is in TMEM: the arrival carries no memory writes
+            if (lane == 0) mbar_arrive_cluster_relaxed(lead(p_full + buf));
         }
         if (CACHED && n_kv == 0) {  // rejected offset (reported): zero rows, nothing else ran
             if (row_ok) {
