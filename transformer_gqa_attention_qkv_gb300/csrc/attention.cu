@@ -382,7 +382,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(p_full + wg);
+            if (lane == 0) mbar_arrive_relaxed(p_full + wg);
         }
         const int head = g * P.G + hl;
         const size_t row = (size_t)(b * P.S + t) * P.Hq + head;  // output row, [B, S, Hq] order

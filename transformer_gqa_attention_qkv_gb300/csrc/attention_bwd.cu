@@ -409,7 +409,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(p_full + h);
+            if (lane == 0) mbar_arrive_relaxed(p_full + h);
         }
         if (ok && wait_all(acc_done, 0)) {
             tc_fence_after();

@@ -695,7 +695,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             epilogue_tile<BN, EPI, D>(P, tcol, m, nb * BN, m < P.M, s_norm);
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(tempty + acc);
+            if (lane == 0) mbar_arrive_relaxed(tempty + acc);
         }
     }
     if constexpr (KS > 1) {

@@ -59,6 +59,13 @@ DEVI void mbar_arrive(uint64_t *bar)
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
+// Arrive once without release semantics.  For hand-offs of TMEM contents
+// only (see mbar_arrive_cluster_relaxed).
+DEVI void mbar_arrive_relaxed(uint64_t *bar)
+{
+    asm volatile("mbarrier.arrive.relaxed.cta.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
 // CLUSTER: acquire at cluster scope (the phase completes with arrivals from
 // another CTA of the cluster whose earlier writes must be visible).
 template <bool CLUSTER = false>
