@@ -520,6 +520,16 @@ int gqa_selftest_bounded_wait(int limit_ms);
  * accounting in benchmarks). */
 int gqa_last_launch_count(void);
 
+/* Process-wide choice of kernel forms.  By default the prefill projections
+ * (head_dim 64 / 128 QKV and o_proj with more than 128 rows) and the
+ * head_dim 256 attention run on 2-CTA clusters (tcgen05 cta_group::2) whenever
+ * that cluster shape can be placed on the device; enable = 0 makes every
+ * later launch use the one-CTA kernels instead (same results up to rounding
+ * order), enable != 0 restores the default.  Returns the previous setting
+ * (1 or 0).  A diagnostic and tuning switch: it is read at each launch, so it
+ * should not be changed while another thread enqueues work. */
+int gqa_set_cta_pairs(int enable);
+
 #ifdef __cplusplus
 }
 #endif

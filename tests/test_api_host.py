@@ -27,11 +27,20 @@ def header_functions():
 
 def test_exports_match_header(L):
     names = header_functions()
-    assert len(names) == 40
+    assert len(names) == 41
     assert sorted(L.EXPORTS) == names
     lib = L.lib()
     for n in names:
         assert hasattr(lib, n), n
+
+
+def test_cta_pairs_switch_returns_previous_setting(L):
+    """gqa_set_cta_pairs is host state only (no device work): it returns the
+    previous setting, and the default is on."""
+    assert L.gqa_set_cta_pairs(False) is True
+    assert L.gqa_set_cta_pairs(False) is False
+    assert L.gqa_set_cta_pairs(True) is False
+    assert L.gqa_set_cta_pairs(True) is True
 
 
 def test_cost_matches_capacity_knob_counts(L):

@@ -3,7 +3,9 @@
 The [NeoX] page's Gemma-3 example ("Background": hidden 640, four query
 heads, an explicit head_dim of 256) needs 256-wide heads.  The QKV GEMM
 handles them with one head per 256-column tile; the attention has a kernel of
-its own (one query tile with two S buffers, 64-key tiles).  Checked: the
+its own (by default on 2-CTA clusters with 128-key S tiles; the one-CTA form,
+one query tile with two S buffers of 64 keys, is re-run under
+gqa_set_cta_pairs(0) in tests/test_one_cta_forms_gpu.py).  Checked: the
 attention stage over group sizes 1, 4, 8 and 16, ragged lengths and the
 unmasked case, with marker values for the head map; the cached-prefill
 attention; the QKV stage with full and partial rotary; the whole layer at

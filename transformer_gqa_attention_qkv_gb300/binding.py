@@ -30,7 +30,7 @@ EXPORTS = (
     "gqa_attention", "gqa_oproj_residual", "gqa_attn_decode_workspace_size", "gqa_attn_decode",
     "gqa_decode_qkv", "gqa_decode_attention_workspace_size", "gqa_decode_attention",
     "gqa_attn_cost", "gqa_last_error", "gqa_check_device_error", "gqa_selftest_bounded_wait",
-    "gqa_last_launch_count", "gqa_decode_attention_noalloc",
+    "gqa_last_launch_count", "gqa_set_cta_pairs", "gqa_decode_attention_noalloc",
     "gqa_attn_prefill_cached_workspace_size", "gqa_attn_prefill_cached", "gqa_attention_cached",
     "gqa_attention_cached_workspace_size",
     "gqa_attn_forward_rd", "gqa_qkv_proj_rd", "gqa_attn_prefill_cached_rd", "gqa_attn_decode_rd",
@@ -84,6 +84,7 @@ def lib():
         "gqa_check_device_error": (_I, []),
         "gqa_selftest_bounded_wait": (_I, [_I]),
         "gqa_last_launch_count": (_I, []),
+        "gqa_set_cta_pairs": (_I, [_I]),
         "gqa_decode_attention_noalloc": (_I, [_P] * 4 + [_I] * 5 + [_P, _P]),
         "gqa_attn_prefill_cached_workspace_size": (_Z, [_I] * 6),
         "gqa_attention_cached_workspace_size": (_Z, [_I] * 4),
@@ -391,6 +392,11 @@ def gqa_selftest_bounded_wait(limit_ms: int) -> int:
 
 def gqa_last_launch_count() -> int:
     return int(lib().gqa_last_launch_count())
+
+
+def gqa_set_cta_pairs(enable: bool) -> bool:
+    """Use (True, the default) or avoid the 2-CTA-cluster kernel forms; returns the previous setting."""
+    return bool(lib().gqa_set_cta_pairs(1 if enable else 0))
 
 
 # --------------------------------------------------------- tensor helpers

@@ -13,6 +13,8 @@
 #include <vector>
 
 #include "../../include/gqa_attn.h"
+#include <atomic>
+
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -357,6 +359,12 @@ static int run_decode_attn(DeviceState &st, const gqa_bf16 *q, const void *kc, c
 
 using namespace gqa;
 
+namespace gqa {
+static std::atomic<int> g_cta_pairs{1};
+bool cta_pairs_enabled() { return g_cta_pairs.load(std::memory_order_relaxed) != 0; }
+int set_cta_pairs(int enable) { return g_cta_pairs.exchange(enable ? 1 : 0); }
+}  // namespace gqa
+
 // =================================================================== C ABI
 
 extern "C" {
@@ -364,6 +372,8 @@ extern "C" {
 const char *gqa_last_error(void) { return g_msg; }
 
 int gqa_last_launch_count(void) { return g_launches; }
+
+int gqa_set_cta_pairs(int enable) { return set_cta_pairs(enable); }
 
 size_t gqa_attn_workspace_size(int B, int S, int hidden, int Hq, int Hkv, int head_dim)
 {

@@ -736,8 +736,8 @@ cudaError_t run_attn256(const AttentionProblem &p, unsigned *err, cudaStream_t s
     a.out = p.out;
     a.err = err;
 
-    // CTA pairs when the cluster shape can be placed, else one CTA per block
-    {
+    // CTA pairs when enabled and the cluster shape can be placed, else one CTA per block
+    if (cta_pairs_enabled()) {
         auto kern = attn256_pair_kernel<CACHED>;
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SmemPair::ALLOC);
         if (e != cudaSuccess) return e;

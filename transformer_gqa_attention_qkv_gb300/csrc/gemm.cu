@@ -1053,6 +1053,7 @@ cudaError_t run_pair(const GemmProblem &p, GemmParams params, int group_m, cudaS
     params.num_n = (p.N + 255) / 256;
     params.num_tiles = params.num_m * params.num_n;
     params.group_m = group_m;
+    if (!cta_pairs_enabled()) return cudaErrorNotSupported;
     auto kern = gemm_pair_kernel<STAGES, EPI, D>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
     if (e != cudaSuccess) return e;

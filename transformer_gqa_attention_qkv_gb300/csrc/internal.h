@@ -112,6 +112,10 @@ struct AttentionProblem {
     uint16_t *part_o = nullptr;
     float *part_lse = nullptr;
 };
+// Whether launchers may use their 2-CTA-cluster kernels (process-wide, default
+// on); off, every problem runs on the one-CTA kernels.
+bool cta_pairs_enabled();
+int set_cta_pairs(int enable);  // returns the previous setting
 cudaError_t launch_attention(const AttentionProblem &p, unsigned *err, int num_sms, cudaStream_t stream);
 // Backward of the attention (head_dim 64 / 128, Hq/Hkv <= 32).  q, k, v, dO
 // binary16 head-major ([B, H, S, d]); o the forward's bf16 output [B, S,
