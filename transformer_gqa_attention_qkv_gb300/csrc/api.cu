@@ -92,7 +92,7 @@ struct RopeTable {
     int d;
     int rows;
     float2 *dev;    // [rows][d/2]: position-major (a warp reads one position's pairs)
-    float2 *dev_t;  // [d/2][rows]: pair-major (a warp reads one pair at 32 consecutive positions)
+    float4 *dev_t;  // [d/4][rows]: quads of pairs 2k, 2k + 1 (a warp reads one quad at 32 consecutive positions)
 };
 
 struct DeviceState {
@@ -139,9 +139,13 @@ static int device_state(DeviceState **out)
 // the host and stored as fp32 (cos, sin) pairs.  Angles reach ~1.6e4 rad, where
 // an fp32 angle would already be off by ~1e-3 rad.
 // The (cos, sin) table of RoPE for (theta, width d) and at least `rows`
-// positions, in both layouts; *ld (if given) is the pair-major row length.
+// positions, in two layouts: position-major (cos, sin) pairs, and the quad
+// layout of the projection epilogue (entry [k][p] = (cos, cos, sin, sin) of
+// pairs 2k and 2k + 1 at position p, so a warp's consecutive positions read
+// one coalesced run and the epilogue rotates two pairs per packed fp32x2
+// operation); *ld (if given) is the quad layout's row length.
 static int rope_table(DeviceState &st, double theta, int d, int rows, const float2 **out,
-                      const float2 **out_t = nullptr, int *ld = nullptr)
+                      const float4 **out_t = nullptr, int *ld = nullptr)
 {
     for (const RopeTable &t : st.ropes)
         if (t.theta == theta && t.d == d && t.rows >= rows) {
@@ -152,21 +156,30 @@ static int rope_table(DeviceState &st, double theta, int d, int rows, const floa
         }
     int cap = 4096;
     while (cap < rows) cap *= 2;
-    const int H = d / 2;
-    std::vector<float2> host((size_t)cap * H), host_t((size_t)cap * H);
+    const int H = d / 2;  // even for every rotary width the kernels take
+    std::vector<float2> host((size_t)cap * H);
+    std::vector<float4> host_t((size_t)cap * (H / 2));
     for (int p = 0; p < cap; ++p)
         for (int i = 0; i < H; ++i) {
             const double f = (double)p * pow(theta, -2.0 * i / d);
             const float2 cs = make_float2((float)cos(f), (float)sin(f));
             host[(size_t)p * H + i] = cs;
-            host_t[(size_t)i * cap + p] = cs;
+            float4 &q = host_t[(size_t)(i / 2) * cap + p];
+            if (i % 2 == 0) {
+                q.x = cs.x;
+                q.z = cs.y;
+            } else {
+                q.y = cs.x;
+                q.w = cs.y;
+            }
         }
-    float2 *dev = nullptr, *dev_t = nullptr;
+    float2 *dev = nullptr;
+    float4 *dev_t = nullptr;
     cudaError_t e = cudaMalloc(&dev, host.size() * sizeof(float2));
-    if (e == cudaSuccess) e = cudaMalloc(&dev_t, host_t.size() * sizeof(float2));
+    if (e == cudaSuccess) e = cudaMalloc(&dev_t, host_t.size() * sizeof(float4));
     if (e != cudaSuccess) return cuda_fail(e, "cudaMalloc(rope table)");
     e = cudaMemcpy(dev, host.data(), host.size() * sizeof(float2), cudaMemcpyHostToDevice);
-    if (e == cudaSuccess) e = cudaMemcpy(dev_t, host_t.data(), host_t.size() * sizeof(float2), cudaMemcpyHostToDevice);
+    if (e == cudaSuccess) e = cudaMemcpy(dev_t, host_t.data(), host_t.size() * sizeof(float4), cudaMemcpyHostToDevice);
     if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpy(rope table)");
     st.ropes.push_back({theta, d, cap, dev, dev_t});
     *out = dev;
@@ -257,7 +270,8 @@ static int run_qkv(DeviceState &st, const gqa_bf16 *x, const gqa_bf16 *Wqkv, con
                    uint16_t *v_out, cudaStream_t stream, int kv_fp8 = 0, float k_scale = 1.0f, float v_scale = 1.0f,
                    float *pre_out = nullptr, int rows = -1, int m0 = 0)
 {
-    const float2 *rope = nullptr, *rope_t = nullptr;
+    const float2 *rope = nullptr;
+    const float4 *rope_t = nullptr;
     int rope_ld = 0;
     if (rd > 0) {
         int rc;

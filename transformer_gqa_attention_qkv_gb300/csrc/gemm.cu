@@ -12,10 +12,12 @@
 //   warp 0      TMA producer: A/B k-slices into a STAGES-deep shared ring
 //   warp 1      MMA issuer: tcgen05.mma 128 x BN x 16 into a TMEM accumulator;
 //               two accumulators so tile i's epilogue overlaps tile i+1's loop
-//   warps 2..5  epilogue: tcgen05.ld (one thread = one output row), fused
-//               math, 32-byte global stores where the row address allows;
-//               inputs it reads from memory (residual rows) are requested
-//               into L2 before the accumulator is ready
+//   warps 2..5  epilogue: tcgen05.ld gives a thread one output row; fused
+//               math on packed fp32 pairs, 32-byte global stores where the
+//               row address allows; residual rows are requested into L2
+//               before the accumulator is ready.  The QKV epilogue has a
+//               second warpgroup (warps 6..9, on the same TMEM lanes), and
+//               the two take alternate column chunks of each row
 //
 // Problems with a single M block (the decode step's projections: 64 rows, a
 // few dozen N tiles) would leave most SMs idle and stream the weights through
@@ -33,9 +35,16 @@ namespace {
 
 constexpr int BM = 128;
 constexpr int BK = 64;  // one 128-byte swizzle row of bf16
-constexpr int kThreads = 192;
-
 enum { EPI_QKV = 0, EPI_RESIDUAL = 1, EPI_F32 = 2, EPI_HEAD16 = 3 };
+
+// Epilogue warpgroups per CTA: two for the QKV epilogue (RMSNorm, RoPE and
+// head-major stores are its critical path on short-K problems), one for the
+// others (their epilogues hide behind the main loop; a second warpgroup made
+// the long-K o_proj 3-8% slower).  Warps 0 and 1 are the TMA and MMA warps.
+template <int EPI>
+__host__ __device__ constexpr int epi_groups() { return EPI == EPI_QKV ? 2 : 1; }
+template <int EPI>
+__host__ __device__ constexpr int kernel_threads() { return 64 + 128 * epi_groups<EPI>(); }
 
 // Operand storage: K-major (the contraction index contiguous: A [M, K], B
 // [N, K]) or MN-major (the row / column index contiguous: A stored [K, M],
@@ -117,6 +126,43 @@ DEVI void tmem_ldw(uint32_t taddr, uint32_t (&r)[W])
     }
 }
 
+// Barrier `id` over the first n threads that reach it (n a multiple of 32).
+DEVI void named_barrier_sync(int id, int n) { asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory"); }
+
+// Two TMEM loads of W columns each (the two halves of a RoPE pair chunk) and
+// one wait, in one statement (no use of a or b can be scheduled before the
+// data has arrived); W = 16 or 8, other widths take two waits.
+template <int W>
+DEVI void tmem_ldw2(uint32_t t1, uint32_t (&a)[W], uint32_t t2, uint32_t (&b)[W])
+{
+    if constexpr (W == 16) {
+        asm volatile(
+            "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+            "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%32];\n\t"
+            "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+            "{%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%33];\n\t"
+            "tcgen05.wait::ld.sync.aligned;"
+            : "=r"(a[0]), "=r"(a[1]), "=r"(a[2]), "=r"(a[3]), "=r"(a[4]), "=r"(a[5]), "=r"(a[6]), "=r"(a[7]),
+              "=r"(a[8]), "=r"(a[9]), "=r"(a[10]), "=r"(a[11]), "=r"(a[12]), "=r"(a[13]), "=r"(a[14]), "=r"(a[15]),
+              "=r"(b[0]), "=r"(b[1]), "=r"(b[2]), "=r"(b[3]), "=r"(b[4]), "=r"(b[5]), "=r"(b[6]), "=r"(b[7]),
+              "=r"(b[8]), "=r"(b[9]), "=r"(b[10]), "=r"(b[11]), "=r"(b[12]), "=r"(b[13]), "=r"(b[14]), "=r"(b[15])
+            : "r"(t1), "r"(t2)
+            : "memory");
+    } else if constexpr (W == 8) {
+        asm volatile(
+            "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%16];\n\t"
+            "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%8,%9,%10,%11,%12,%13,%14,%15}, [%17];\n\t"
+            "tcgen05.wait::ld.sync.aligned;"
+            : "=r"(a[0]), "=r"(a[1]), "=r"(a[2]), "=r"(a[3]), "=r"(a[4]), "=r"(a[5]), "=r"(a[6]), "=r"(a[7]),
+              "=r"(b[0]), "=r"(b[1]), "=r"(b[2]), "=r"(b[3]), "=r"(b[4]), "=r"(b[5]), "=r"(b[6]), "=r"(b[7])
+            : "r"(t1), "r"(t2)
+            : "memory");
+    } else {
+        tmem_ldw<W>(t1, a);
+        tmem_ldw<W>(t2, b);
+    }
+}
+
 // 32 bytes to global memory: one 256-bit store when p is 32-byte aligned
 // (the epilogues write one row per thread, so every store is its own
 // transaction and whole 32-byte sectors halve their count), else two
@@ -134,82 +180,82 @@ DEVI void st_global32(void *p, const uint32_t (&w)[8])
     }
 }
 
-// W values of one row -> 16-bit storage (bf16, or binary16 clamped to its
-// finite range; *clamped is set when a value had to be clamped).  dst is
-// aligned to 2W bytes (16 at most).
-template <int W>
-DEVI void storew(uint16_t *dst, const float *v, bool f16, bool &clamped)
+// N consecutive 32-bit words to dst (aligned to 4N bytes, 16 at most).
+template <int N>
+DEVI void st_words(void *dst, const uint32_t (&w)[N])
 {
-    uint32_t w[W / 2];
+    if constexpr (N >= 8) {
 #pragma unroll
-    for (int i = 0; i < W / 2; ++i) {
-        float a = v[2 * i], b = v[2 * i + 1];
-        if (f16) {
-            const float ca = fminf(fmaxf(a, -kHalfMax), kHalfMax), cb = fminf(fmaxf(b, -kHalfMax), kHalfMax);
-            clamped |= !(ca == a) || !(cb == b);
-            w[i] = pack_f16(ca, cb);
-        } else {
-            w[i] = pack_bf16(a, b);
-        }
-    }
-    if constexpr (W >= 16) {
-#pragma unroll
-        for (int i = 0; i < W / 16; ++i) {
+        for (int i = 0; i < N / 8; ++i) {
             const uint32_t w8[8] = {w[8 * i], w[8 * i + 1], w[8 * i + 2], w[8 * i + 3],
                                     w[8 * i + 4], w[8 * i + 5], w[8 * i + 6], w[8 * i + 7]};
-            st_global32(dst + 16 * i, w8);
+            st_global32(reinterpret_cast<uint32_t *>(dst) + 8 * i, w8);
         }
-    } else if constexpr (W == 8) {
+    } else if constexpr (N == 4) {
         *reinterpret_cast<uint4 *>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
-    } else if constexpr (W == 4) {
+    } else if constexpr (N == 2) {
         *reinterpret_cast<uint2 *>(dst) = make_uint2(w[0], w[1]);
     } else {
+        static_assert(N == 1, "store width");
         *reinterpret_cast<uint32_t *>(dst) = w[0];
     }
 }
 
-// Storage format of one projected head row: bf16, binary16 (clamped to its
+// Two floats -> packed binary16x2, rounded to nearest even and saturated at
+// the finite range (+-65504; NaN stays NaN), lo in the low half.
+DEVI uint32_t pack_f16_sat(float lo, float hi)
+{
+    uint32_t r;
+    asm("cvt.rn.satfinite.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// Storage format of one projected head row: bf16, binary16 (saturated at its
 // range and flagged), or E4M3 codes of value / scale (saturated and flagged).
 struct OutFmt {
     int mode;     // 0 bf16, 1 binary16, 2 E4M3
     float scale;  // E4M3 only
 };
 
-// Columns [c, c + W) of a head row whose first element is at dst.
-template <int W>
-DEVI void putw(void *dst, int c, const float *v, OutFmt f, bool &clamped)
+// Columns [c, c + N) (N even) of a head row whose first element is at dst,
+// from N/2 packed pairs.  binary16: *amax takes the largest magnitude stored
+// (the caller flags values past the finite range once per row); E4M3:
+// *clamped is set when a code saturated.
+template <int N>
+DEVI void putv(void *dst, int c, const float2 (&v)[N / 2], OutFmt f, float &amax, bool &clamped)
 {
     if (f.mode != 2) {
-        storew<W>(reinterpret_cast<uint16_t *>(dst) + c, v, f.mode == 1, clamped);
+        uint32_t w[N / 2];
+#pragma unroll
+        for (int i = 0; i < N / 2; ++i) {
+            if (f.mode == 1) {
+                w[i] = pack_f16_sat(v[i].x, v[i].y);
+                amax = fmax3(amax, fabsf(v[i].x), fabsf(v[i].y));
+            } else {
+                w[i] = pack_bf16(v[i].x, v[i].y);
+            }
+        }
+        st_words<N / 2>(reinterpret_cast<uint16_t *>(dst) + c, w);
         return;
     }
     uint8_t *d8 = reinterpret_cast<uint8_t *>(dst) + c;
-    if constexpr (W == 2) {
-        const float q0 = __fdiv_rn(v[0], f.scale), q1 = __fdiv_rn(v[1], f.scale);
+    if constexpr (N == 2) {
+        const float q0 = __fdiv_rn(v[0].x, f.scale), q1 = __fdiv_rn(v[0].y, f.scale);
         clamped |= !(fabsf(q0) <= 448.0f) || !(fabsf(q1) <= 448.0f);
         *reinterpret_cast<uint16_t *>(d8) = (uint16_t)f32x2_to_e4m3x2(q0, q1);
-        return;
-    }
-    constexpr int NW = W >= 4 ? W / 4 : 1;
-    uint32_t w[NW];
-#pragma unroll
-    for (int i = 0; i < W / 4; ++i) {
-        float q[4];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            q[k] = __fdiv_rn(v[4 * i + k], f.scale);
-            clamped |= !(fabsf(q[k]) <= 448.0f);
-        }
-        w[i] = f32x2_to_e4m3x2(q[0], q[1]) | (f32x2_to_e4m3x2(q[2], q[3]) << 16);
-    }
-    if constexpr (W >= 16) {
-#pragma unroll
-        for (int i = 0; i < W / 16; ++i)
-            reinterpret_cast<uint4 *>(d8)[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
-    } else if constexpr (W == 8) {
-        *reinterpret_cast<uint2 *>(d8) = make_uint2(w[0], w[1]);
     } else {
-        *reinterpret_cast<uint32_t *>(d8) = w[0];
+        uint32_t w[N / 4];
+#pragma unroll
+        for (int i = 0; i < N / 4; ++i) {
+            float q[4] = {v[2 * i].x, v[2 * i].y, v[2 * i + 1].x, v[2 * i + 1].y};
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                q[k] = __fdiv_rn(q[k], f.scale);
+                clamped |= !(fabsf(q[k]) <= 448.0f);
+            }
+            w[i] = f32x2_to_e4m3x2(q[0], q[1]) | (f32x2_to_e4m3x2(q[2], q[3]) << 16);
+        }
+        st_words<N / 4>(d8, w);
     }
 }
 
@@ -218,54 +264,95 @@ __host__ __device__ constexpr int chunk_width(int n)
 {
     return n % 32 == 0 ? 32 : n % 16 == 0 ? 16 : n % 8 == 0 ? 8 : n % 4 == 0 ? 4 : 2;
 }
+// The same, at most 16: the unit of the epilogue's RoPE and store passes, whose
+// chunks the two warpgroups take in turn.
+__host__ __device__ constexpr int chunk16(int n) { return n % 16 == 0 ? 16 : chunk_width(n); }
+
+DEVI float2 f2(uint32_t a, uint32_t b) { return make_float2(__uint_as_float(a), __uint_as_float(b)); }
+
+// The RoPE table of one row: rotary width RD, pairs (i, i + RD/2) taken W at a
+// time, a warpgroup's chunks every other one.  cs is the quad table at the
+// row's position: entry k * ld holds (cos, cos, sin, sin) of pairs 2k and
+// 2k + 1, so the 32 rows of a warp (consecutive positions of one sequence in a
+// prefill) read one coalesced 512-byte run per two pairs.  (Holding a row's
+// entries in registers across the tile's heads, which share them, needs 32
+// more registers than the epilogue warps have at 10 warps per CTA: 168.)
+template <int RD>
+struct RopeTab {
+    static constexpr int W = RD > 0 ? chunk16(RD / 2) : 2;
+    const float4 *cs;
+    int ld;
+};
+
+// Pairs [c, c + W) of a Q or K row: normalised (x * rinv * w), rotated
+// (rotate-half pairs (i, i + H), angle pos * theta^(-2i/RD)) and stored, on
+// packed fp32 pairs.
+template <int RD, bool NORM>
+DEVI void rope_chunk(uint32_t col, void *dst, int c, float2 rr, const float *w, const float4 (&t)[RopeTab<RD>::W / 2],
+                     bool row_ok, OutFmt fmt, float &amax, bool &clamped)
+{
+    constexpr int H = RD / 2, W = RopeTab<RD>::W;
+    uint32_t a[W], b[W];
+    tmem_ldw2<W>(col + c, a, col + c + H, b);
+    if constexpr (NORM) {  // a, b <- x * rinv * w (in place, as fp32 bits)
+#pragma unroll
+        for (int q = 0; q < W / 2; ++q) {
+            const float2 w1 = *reinterpret_cast<const float2 *>(w + c + 2 * q);
+            const float2 w2 = *reinterpret_cast<const float2 *>(w + c + H + 2 * q);
+            const float2 x1 = __fmul2_rn(f2(a[2 * q], a[2 * q + 1]), __fmul2_rn(rr, w1));
+            const float2 x2 = __fmul2_rn(f2(b[2 * q], b[2 * q + 1]), __fmul2_rn(rr, w2));
+            a[2 * q] = __float_as_uint(x1.x);
+            a[2 * q + 1] = __float_as_uint(x1.y);
+            b[2 * q] = __float_as_uint(x2.x);
+            b[2 * q + 1] = __float_as_uint(x2.y);
+        }
+    }
+    float2 y[W / 2];
+#pragma unroll
+    for (int q = 0; q < W / 2; ++q)  // first halves: x1 cos - x2 sin
+        y[q] = __ffma2_rn(f2(a[2 * q], a[2 * q + 1]), make_float2(t[q].x, t[q].y),
+                          __fmul2_rn(f2(b[2 * q], b[2 * q + 1]), make_float2(-t[q].z, -t[q].w)));
+    if (row_ok) putv<W>(dst, c, y, fmt, amax, clamped);
+#pragma unroll
+    for (int q = 0; q < W / 2; ++q)  // second halves: x2 cos + x1 sin
+        y[q] = __ffma2_rn(f2(b[2 * q], b[2 * q + 1]), make_float2(t[q].x, t[q].y),
+                          __fmul2_rn(f2(a[2 * q], a[2 * q + 1]), make_float2(t[q].z, t[q].w)));
+    if (row_ok) putv<W>(dst, c + H, y, fmt, amax, clamped);
+}
 
 // Normalised (x * rinv * w) head row of a Q or K head, rotated on its first
-// RD features (rotate-half pairs (i, i + RD/2), (cos, sin) of angle
-// pos * theta^(-2i/RD) from cs[i * ld], the pair-major table at this row's
-// position: the 32 rows of a warp are consecutive positions of one sequence in
-// a prefill, so each of these loads is one coalesced read) and stored; features [RD, D) are only
-// normalised.  The pairs are taken in chunks of W columns and the rest in
-// chunks of CW, the widest that tile RD/2 and D - RD, so that every TMEM load
-// starts at a multiple of its own width (head offsets are multiples of D).
-template <int D, int RD>
-DEVI void rope_store(uint32_t col, void *dst, float rinv, bool has_norm, const float *w, const float2 *cs,
-                     int ld, bool row_ok, OutFmt fmt, bool &clamped)
+// RD features and stored; features [RD, D) are only normalised.  Warpgroup wg
+// takes every other chunk.
+template <int D, int RD, bool NORM>
+DEVI void rope_store(uint32_t col, void *dst, float rinv, const float *w, const RopeTab<RD> &tab, bool row_ok,
+                     OutFmt fmt, int wg, float &amax, bool &clamped)
 {
-    auto nrm = [&](float x, int c) { return has_norm ? x * rinv * w[c] : x * rinv; };
+    const float2 rr = make_float2(rinv, rinv);
     if constexpr (RD > 0) {
-        constexpr int H = RD / 2, W = chunk_width(H);
+        constexpr int H = RD / 2, W = RopeTab<RD>::W;
+        static_assert(W % 2 == 0, "pairs are taken two at a time");
 #pragma unroll 1
-        for (int c = 0; c < H; c += W) {
-            uint32_t r1[W], r2[W];
-            tmem_ldw<W>(col + c, r1);
-            tmem_ldw<W>(col + c + H, r2);
-            float y1[W], y2[W];
-            float2 t[W];
+        for (int c = wg * W; c < H; c += 2 * W) {
+            float4 t[W / 2];
 #pragma unroll
-            for (int i = 0; i < W; ++i) t[i] = __ldg(cs + (size_t)(c + i) * ld);  // (cos, sin)
-#pragma unroll
-            for (int i = 0; i < W; ++i) {
-                const float x1 = nrm(__uint_as_float(r1[i]), c + i);
-                const float x2 = nrm(__uint_as_float(r2[i]), c + i + H);
-                y1[i] = x1 * t[i].x - x2 * t[i].y;
-                y2[i] = x2 * t[i].x + x1 * t[i].y;
-            }
-            if (row_ok) {
-                putw<W>(dst, c, y1, fmt, clamped);
-                putw<W>(dst, c + H, y2, fmt, clamped);
-            }
+            for (int q = 0; q < W / 2; ++q) t[q] = __ldg(tab.cs + (size_t)(c / 2 + q) * tab.ld);
+            rope_chunk<RD, NORM>(col, dst, c, rr, w, t, row_ok, fmt, amax, clamped);
         }
     }
     if constexpr (RD < D) {
-        constexpr int CW = chunk_width(D - RD);
+        constexpr int CW = chunk16(D - RD);
 #pragma unroll 1
-        for (int c = RD; c < D; c += CW) {  // features past the rotary width
+        for (int c = RD + wg * CW; c < D; c += 2 * CW) {  // features past the rotary width
             uint32_t r[CW];
             tmem_ldw<CW>(col + c, r);
-            float y[CW];
+            float2 y[CW / 2];
 #pragma unroll
-            for (int i = 0; i < CW; ++i) y[i] = nrm(__uint_as_float(r[i]), c + i);
-            if (row_ok) putw<CW>(dst, c, y, fmt, clamped);
+            for (int q = 0; q < CW / 2; ++q) {
+                y[q] = f2(r[2 * q], r[2 * q + 1]);
+                if constexpr (NORM)
+                    y[q] = __fmul2_rn(y[q], __fmul2_rn(rr, *reinterpret_cast<const float2 *>(w + c + 2 * q)));
+            }
+            if (row_ok) putv<CW>(dst, c, y, fmt, amax, clamped);
         }
     }
 }
@@ -292,7 +379,7 @@ DEVI void epilogue_f32(const GemmParams &P, uint32_t tcol, int m, int n0, bool r
 }
 
 // binary16 head-major output: column n = j*d + c of row m = b*S + t goes to
-// out[((b*H + j)*S + t)*d + c] (clamped to binary16's range and flagged).
+// out[((b*H + j)*S + t)*d + c] (saturated at binary16's range and flagged).
 // Stored 16 columns at a time: d is a multiple of 16 (64, 80, 96, 128), so a
 // 16-column piece never crosses a head, while a 32-column one would at d = 80.
 template <int BN>
@@ -300,7 +387,9 @@ DEVI void epilogue_head16(const GemmParams &P, uint32_t tcol, int m, int n0, boo
 {
     const HeadEpilogue &e = P.head;
     const int b = m / e.S, t = m - (m / e.S) * e.S;
-    bool clamped = false;
+    float amax = 0.0f;
+    bool unused = false;
+    const OutFmt f16{1, 1.0f};
 #pragma unroll 1
     for (int c = 0; c < BN; c += 32) {
         const int n = n0 + c;
@@ -313,43 +402,29 @@ DEVI void epilogue_head16(const GemmParams &P, uint32_t tcol, int m, int n0, boo
             const int nh = n + 16 * h;
             if (nh >= P.N) break;
             const int j = nh / e.d, cc = nh - j * e.d;
-            float v[16];
+            float2 v[8];
 #pragma unroll
-            for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[16 * h + i]);
-            storew<16>(e.out + ((size_t)(b * e.H + j) * e.S + t) * e.d + cc, v, true, clamped);
+            for (int i = 0; i < 8; ++i) v[i] = f2(r[16 * h + 2 * i], r[16 * h + 2 * i + 1]);
+            putv<16>(e.out + ((size_t)(b * e.H + j) * e.S + t) * e.d, cc, v, f16, amax, unused);
         }
     }
-    if (clamped) atomicOr(P.err, kErrRange);
+    if (amax > kHalfMax) atomicOr(P.err, kErrRange);
 }
 
-// Epilogue of one QKV tile row: BN columns = BN/D whole heads.
-template <int BN, int D>
-DEVI void epilogue_qkv(const GemmParams &P, uint32_t tcol, int m, int n0, bool row_ok, const float *s_norm)
+// The heads of one QKV tile row (BN columns = BN/D whole heads) at rotary
+// width RD.  Both warpgroups take the sum of squares of a Q or K row over all
+// its D columns (each loads the whole row from TMEM, so they never wait for
+// each other); each then rotates and stores its own chunks.
+template <int BN, int D, int RD>
+DEVI void qkv_heads(const GemmParams &P, uint32_t tcol, int m, int n0, bool row_ok, const float *s_norm, int wg,
+                    int b, int pos, int q_slot, int kv_slot, float &amax, bool &clamped)
 {
-    static_assert(BN % D == 0, "a tile holds whole heads");
-    constexpr int CWD = chunk_width(D);  // TMEM chunk that tiles a head row (32, or 16 for d = 80)
+    constexpr int CWN = chunk_width(D);  // norm pass: TMEM chunk that tiles a head row (32, or 16 for d = 80)
+    constexpr int CWV = chunk16(D);      // V rows: store chunk
     const QkvEpilogue &e = P.qkv;
     const int HqD = e.Hq * D, HkvD = e.Hkv * D;
-    int b = 0, pos = 0, q_slot = 0, kv_slot = 0;
-    if (row_ok) {
-        if (e.pos_dev) {  // new tokens after pos_dev[b] cached ones: position = slot = pos_dev[b] + t
-            b = m / e.S;
-            q_slot = m - b * e.S;
-            pos = e.pos_dev[b] + q_slot;
-            kv_slot = pos;
-        } else {
-            const int mg = e.m0 + m;  // row of the whole problem
-            b = mg / e.S;
-            pos = mg - b * e.S;
-            q_slot = kv_slot = pos;
-        }
-        if (pos < 0 || pos >= e.rope_rows || kv_slot >= e.kv_seq) {
-            atomicOr(P.err, kErrIndex);
-            row_ok = false;
-        }
-    }
     const bool has_norm = e.q_norm_w != nullptr;
-    bool clamped = false;
+    const RopeTab<RD> tab{RD > 0 ? e.rope + (row_ok ? pos : 0) : nullptr, e.rope_ld};
 #pragma unroll 1
     for (int h = 0; h < BN / D; ++h) {
         const int n = n0 + h * D;
@@ -386,61 +461,92 @@ DEVI void epilogue_qkv(const GemmParams &P, uint32_t tcol, int m, int n0, bool r
 
         if (kind == 2) {  // V: no norm, no rotation
 #pragma unroll 1
-            for (int c = 0; c < D; c += CWD) {
-                uint32_t r[CWD];
-                tmem_ldw<CWD>(col + c, r);
-                float v[CWD];
+            for (int c = wg * CWV; c < D; c += 2 * CWV) {
+                uint32_t r[CWV];
+                tmem_ldw<CWV>(col + c, r);
+                float2 v[CWV / 2];
 #pragma unroll
-                for (int i = 0; i < CWD; ++i) v[i] = __uint_as_float(r[i]);
-                if (row_ok) putw<CWD>(dst, c, v, fmt, clamped);
+                for (int i = 0; i < CWV / 2; ++i) v[i] = f2(r[2 * i], r[2 * i + 1]);
+                if (row_ok) putv<CWV>(dst, c, v, fmt, amax, clamped);
             }
             continue;
         }
         float rinv = 1.0f;
         if (has_norm) {
-            float ss = 0.0f;
+            float2 ss2 = make_float2(0.0f, 0.0f);
             // pre-norm Q/K rows for the backward's RMSNorm gradient: [M, (Hq+Hkv)*D] fp32
             float *pre = e.pre_out ? e.pre_out + (size_t)m * (e.Hq + e.Hkv) * D + (kind == 0 ? head : e.Hq + head) * D
                                    : nullptr;
 #pragma unroll 1
-            for (int c = 0; c < D; c += CWD) {
-                uint32_t r[CWD];
-                tmem_ldw<CWD>(col + c, r);
+            for (int c = 0; c < D; c += CWN) {
+                uint32_t r[CWN];
+                tmem_ldw<CWN>(col + c, r);
 #pragma unroll
-                for (int i = 0; i < CWD; ++i) {
-                    const float f = __uint_as_float(r[i]);
-                    ss = fmaf(f, f, ss);
+                for (int i = 0; i < CWN / 2; ++i) {
+                    const float2 f = f2(r[2 * i], r[2 * i + 1]);
+                    ss2 = __ffma2_rn(f, f, ss2);
                 }
-                if (pre && row_ok) {
+                if (pre && row_ok && ((c / CWN) & 1) == wg) {
                     float4 *d4 = reinterpret_cast<float4 *>(pre + c);
 #pragma unroll
-                    for (int i = 0; i < CWD / 4; ++i)
+                    for (int i = 0; i < CWN / 4; ++i)
                         d4[i] = make_float4(__uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1]),
                                             __uint_as_float(r[4 * i + 2]), __uint_as_float(r[4 * i + 3]));
                 }
             }
-            rinv = 1.0f / sqrtf(ss * (1.0f / D) + e.eps);
+            rinv = 1.0f / sqrtf((ss2.x + ss2.y) * (1.0f / D) + e.eps);
+            rope_store<D, RD, true>(col, dst, rinv, s_norm + (kind == 0 ? 0 : 256), tab, row_ok, fmt, wg, amax,
+                                    clamped);
+        } else {
+            rope_store<D, RD, false>(col, dst, rinv, s_norm, tab, row_ok, fmt, wg, amax, clamped);
         }
-        const float *w = s_norm + (kind == 0 ? 0 : 256);
-        const int p = row_ok ? pos : 0;
-        const float2 *cs = e.rope ? e.rope + p : nullptr;  // pair 0 at this position
-        if (e.rd == D)
-            rope_store<D, D>(col, dst, rinv, has_norm, w, cs, e.rope_ld, row_ok, fmt, clamped);
-        else if (e.rd == D / 2)
-            rope_store<D, D / 2>(col, dst, rinv, has_norm, w, cs, e.rope_ld, row_ok, fmt, clamped);
-        else if (e.rd == D / 4)
-            rope_store<D, D / 4>(col, dst, rinv, has_norm, w, cs, e.rope_ld, row_ok, fmt, clamped);
-        else
-            rope_store<D, 0>(col, dst, rinv, has_norm, w, nullptr, 0, row_ok, fmt, clamped);
     }
-    if (clamped) atomicOr(P.err, kErrRange);
 }
 
+// Epilogue of one QKV tile row: the row's position and output slots, then its
+// heads at the rotary width in use.
+template <int BN, int D>
+DEVI void epilogue_qkv(const GemmParams &P, uint32_t tcol, int m, int n0, bool row_ok, const float *s_norm, int wg)
+{
+    static_assert(BN % D == 0, "a tile holds whole heads");
+    const QkvEpilogue &e = P.qkv;
+    int b = 0, pos = 0, q_slot = 0, kv_slot = 0;
+    if (row_ok) {
+        if (e.pos_dev) {  // new tokens after pos_dev[b] cached ones: position = slot = pos_dev[b] + t
+            b = m / e.S;
+            q_slot = m - b * e.S;
+            pos = e.pos_dev[b] + q_slot;
+            kv_slot = pos;
+        } else {
+            const int mg = e.m0 + m;  // row of the whole problem
+            b = mg / e.S;
+            pos = mg - b * e.S;
+            q_slot = kv_slot = pos;
+        }
+        if (pos < 0 || pos >= e.rope_rows || kv_slot >= e.kv_seq) {
+            if (wg == 0) atomicOr(P.err, kErrIndex);
+            row_ok = false;
+        }
+    }
+    float amax = 0.0f;
+    bool clamped = false;
+    if (e.rd == D)
+        qkv_heads<BN, D, D>(P, tcol, m, n0, row_ok, s_norm, wg, b, pos, q_slot, kv_slot, amax, clamped);
+    else if (e.rd == D / 2)
+        qkv_heads<BN, D, D / 2>(P, tcol, m, n0, row_ok, s_norm, wg, b, pos, q_slot, kv_slot, amax, clamped);
+    else if (e.rd == D / 4)
+        qkv_heads<BN, D, D / 4>(P, tcol, m, n0, row_ok, s_norm, wg, b, pos, q_slot, kv_slot, amax, clamped);
+    else
+        qkv_heads<BN, D, 0>(P, tcol, m, n0, row_ok, s_norm, wg, b, pos, q_slot, kv_slot, amax, clamped);
+    if (amax > kHalfMax || clamped) atomicOr(P.err, kErrRange);
+}
+
+// out = acc + resid, bf16 rows; the residual of the next 32 columns is loaded
+// while this chunk is added.
 template <int BN>
 DEVI void epilogue_residual(const GemmParams &P, uint32_t tcol, int m, int n0, bool row_ok)
 {
     const ResidualEpilogue &e = P.res;
-    // the residual of the next 32 columns is loaded while this chunk is added
     auto load = [&](int c, uint4 (&x)[4]) {
         const int n = n0 + c;
         const uint4 *src = reinterpret_cast<const uint4 *>(e.resid + (size_t)m * P.N + n);
@@ -463,9 +569,11 @@ DEVI void epilogue_residual(const GemmParams &P, uint32_t tcol, int m, int n0, b
             for (int v = 0; v < 4; ++v) {
                 const uint32_t xs[4] = {cur[v].x, cur[v].y, cur[v].z, cur[v].w};
 #pragma unroll
-                for (int k = 0; k < 4; ++k)
-                    o[4 * v + k] = pack_bf16(__uint_as_float(r[8 * v + 2 * k]) + bf16lo(xs[k]),
-                                             __uint_as_float(r[8 * v + 2 * k + 1]) + bf16hi(xs[k]));
+                for (int q = 0; q < 4; ++q) {
+                    const float2 sum = __fadd2_rn(f2(r[8 * v + 2 * q], r[8 * v + 2 * q + 1]),
+                                                  make_float2(bf16lo(xs[q]), bf16hi(xs[q])));
+                    o[4 * v + q] = pack_bf16(sum.x, sum.y);
+                }
             }
             if (n + 32 <= P.N) {  // the whole chunk: two 32-byte stores
                 const uint32_t a[8] = {o[0], o[1], o[2], o[3], o[4], o[5], o[6], o[7]};
@@ -487,28 +595,29 @@ DEVI void epilogue_residual(const GemmParams &P, uint32_t tcol, int m, int n0, b
 // Before a tile's accumulator is ready, the residual rows its epilogue adds are
 // requested into L2 (one bulk prefetch per row segment), so the epilogue does
 // not wait on DRAM once per chunk; short-K problems are otherwise bound by it.
-// (The same for the RoPE table rows of the QKV epilogue measured slower.)
+// (Loading them into registers at that point, and the same prefetch for the
+// RoPE table rows of the QKV epilogue, measured slower.)
 DEVI void prefetch_l2(const void *p, uint32_t bytes)
 {
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
 }
 
-template <int BN, int EPI, int D>
+template <int BN, int EPI>
 DEVI void epilogue_prefetch(const GemmParams &P, int m, int n0, bool row_ok)
 {
-    if (!row_ok) return;
     if constexpr (EPI == EPI_RESIDUAL) {
         const int cols = min(BN, P.N - n0);  // a multiple of 8: whole 16-byte units
-        if (cols > 0) prefetch_l2(P.res.resid + (size_t)m * P.N + n0, (uint32_t)cols * 2);
+        if (row_ok && cols > 0) prefetch_l2(P.res.resid + (size_t)m * P.N + n0, (uint32_t)cols * 2);
     }
 }
 
-// The tile's epilogue, one thread per accumulator row.
+// The tile's epilogue: one thread per accumulator row; wg is the thread's
+// epilogue warpgroup (the QKV epilogue's two split the row's chunks).
 template <int BN, int EPI, int D>
-DEVI void epilogue_tile(const GemmParams &P, uint32_t tcol, int m, int n0, bool row_ok, const float *s_norm)
+DEVI void epilogue_tile(const GemmParams &P, uint32_t tcol, int m, int n0, bool row_ok, const float *s_norm, int wg)
 {
     if constexpr (EPI == EPI_QKV)
-        epilogue_qkv<BN, D>(P, tcol, m, n0, row_ok, s_norm);
+        epilogue_qkv<BN, D>(P, tcol, m, n0, row_ok, s_norm, wg);
     else if constexpr (EPI == EPI_RESIDUAL)
         epilogue_residual<BN>(P, tcol, m, n0, row_ok);
     else if constexpr (EPI == EPI_F32)
@@ -520,7 +629,7 @@ DEVI void epilogue_tile(const GemmParams &P, uint32_t tcol, int m, int n0, bool 
 // KS: CTAs of a cluster that split K for one tile (1: no split, persistent
 // over tiles).
 template <int BN, int STAGES, int EPI, int D, int MAJ, int KS>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kernel_threads<EPI>(), 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const GemmParams P)
 {
     constexpr bool AMN = MAJ & 1, BMN = (MAJ >> 1) & 1;
@@ -562,7 +671,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(tfull + a, 1);
-            mbar_init(tempty + a, 4);
+            mbar_init(tempty + a, 4 * epi_groups<EPI>());
         }
         mbar_init(drain, 1);
         fence_mbar_init();
@@ -574,7 +683,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool acc_ready = false;  // split K: this warp's accumulator rows are complete
     if (warp == 1) tmem_alloc(tmem_slot, 2 * ACC);
     if (EPI == EPI_QKV && warp >= 2 && P.qkv.q_norm_w) {
-        for (int i = threadIdx.x - 64; i < D; i += 128) {
+        for (int i = threadIdx.x - 64; i < D; i += kernel_threads<EPI>() - 64) {
             s_norm[i] = __uint_as_float((uint32_t)P.qkv.q_norm_w[i] << 16);
             s_norm[256 + i] = __uint_as_float((uint32_t)P.qkv.k_norm_w[i] << 16);
         }
@@ -674,7 +783,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_wait(drain, 0, err);
         }
     } else {
-        const int quarter = warp & 3;  // TMEM lanes this warp may access
+        const int quarter = warp & 3;    // TMEM lanes this warp may access
+        const int wg = (warp - 2) >> 2;  // epilogue warpgroup: which column chunks
         const int row = quarter * 32 + lane;
         grid_dep_wait();  // the epilogue reads and writes what the previous kernel may touch
         int use = 0;
@@ -682,17 +792,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             int mb, nb;
             tile_coords(tile, P.num_m, P.num_n, P.group_m, mb, nb);
             const int acc = use & 1;
-            epilogue_prefetch<BN, EPI, D>(P, mb * BM + row, nb * BN, mb * BM + row < P.M);
-            const bool ready = mbar_wait(tfull + acc, (use >> 1) & 1, err);
+            const int m = mb * BM + row;
             if constexpr (KS > 1) {  // the cluster sums the partials below
-                acc_ready = __all_sync(0xffffffffu, ready);
+                acc_ready = __all_sync(0xffffffffu, mbar_wait(tfull + acc, (use >> 1) & 1, err));
                 break;
             }
-            if (!ready) break;
+            epilogue_prefetch<BN, EPI>(P, m, nb * BN, m < P.M);
+            if (!mbar_wait(tfull + acc, (use >> 1) & 1, err)) break;
             tc_fence_after();
             const uint32_t tcol = tmem + ((uint32_t)(quarter * 32) << 16) + acc * ACC;
-            const int m = mb * BM + row;
-            epilogue_tile<BN, EPI, D>(P, tcol, m, nb * BN, m < P.M, s_norm);
+            epilogue_tile<BN, EPI, D>(P, tcol, m, nb * BN, m < P.M, s_norm, wg);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive_relaxed(tempty + acc);
@@ -703,20 +812,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         // gave up on a bounded wait, recorded in *err) and the first CTA's
         // operand ring is idle: the others add their partials into it.
         static_assert((KS - 1) * PART <= L::RING, "split-K partials fit in the operand ring");
-        __syncthreads();
+        // every epilogue warp of the CTA takes the same path below (they meet at a named barrier)
+        const bool all_ready = __syncthreads_and(warp < 2 || acc_ready);
         cluster_sync();
         const int quarter = warp & 3;
+        constexpr int NWG = epi_groups<EPI>();
+        const int wg = (warp - 2) >> 2;  // epilogue warpgroup (warps >= 2): every NWG-th 16 columns
         const int row = quarter * 32 + lane;
         const uint32_t tcol = tmem + ((uint32_t)(quarter * 32) << 16);
         int mb = 0, nb = 0;
         if (tile0 < P.num_tiles) tile_coords(tile0, P.num_m, P.num_n, P.group_m, mb, nb);
         const int m = mb * BM + row;
-        const bool active = warp >= 2 && tile0 < P.num_tiles && acc_ready;  // warp-uniform
+        const bool active = warp >= 2 && tile0 < P.num_tiles && all_ready;  // uniform over the epilogue warps
         if (active && crank != 0) {
             tc_fence_after();
             const uint32_t dst = cluster_map(smem_u32(smem), 0) + (uint32_t)(((crank - 1) * BM + row) * PART_LD * 4);
 #pragma unroll 1
-            for (int c = 0; c < BN; c += 16) {
+            for (int c = 16 * wg; c < BN; c += 16 * NWG) {
                 uint32_t r[16];
                 tmem_ld16(tcol + c, r);
                 if (m < P.M)
@@ -732,7 +844,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // only rows of the problem add partials
             const float *part = reinterpret_cast<const float *>(smem) + row * PART_LD;
 #pragma unroll 1
-            for (int c = 0; c < BN; c += 16) {
+            for (int c = 16 * wg; c < BN; c += 16 * NWG) {
                 uint32_t r[16];
                 tmem_ld16(tcol + c, r);
                 if (m < P.M) {
@@ -752,10 +864,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tmem_st16_nowait(tcol + c, r);
             }
             tmem_st_wait();
+            // every warpgroup's partial sums are in TMEM before another reads its columns
             tc_fence_before();
-            __syncwarp();
+            if constexpr (NWG > 1)
+                named_barrier_sync(1, NWG * 128);
+            else
+                __syncwarp();
             tc_fence_after();
-            epilogue_tile<BN, EPI, D>(P, tcol, m, nb * BN, m < P.M, s_norm);
+            epilogue_tile<BN, EPI, D>(P, tcol, m, nb * BN, m < P.M, s_norm, wg);
         }
     }
     __syncthreads();
@@ -780,10 +896,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 //   warp 1 (even CTA)    MMA issue; each commit arrives on the barrier of
 //                        that offset in both CTAs (stage free, accumulator
 //                        full)
-//   warps 2..5 (both)    epilogue; the accumulator is released by arriving
-//                        on the even CTA's `tempty` (8 arrivals: both CTAs)
+//   warps 2.. (both)     epilogue; the accumulator is released by arriving
+//                        on the even CTA's `tempty` (every epilogue warp of both CTAs)
 template <int STAGES, int EPI, int D>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kernel_threads<EPI>(), 1)
     gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                      const GemmParams P)
 {
@@ -820,7 +936,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(tfull + a, 1);
-            mbar_init(tempty + a, 8);  // the epilogue warps of both CTAs
+            mbar_init(tempty + a, 8 * epi_groups<EPI>());  // the epilogue warps of both CTAs
         }
         mbar_init(drain, 1);
         fence_mbar_init();
@@ -831,7 +947,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (warp == 1) tmem_alloc_pair(tmem_slot, 2 * ACC);
     if (EPI == EPI_QKV && warp >= 2 && P.qkv.q_norm_w) {
-        for (int i = threadIdx.x - 64; i < D; i += 128) {
+        for (int i = threadIdx.x - 64; i < D; i += kernel_threads<EPI>() - 64) {
             s_norm[i] = __uint_as_float((uint32_t)P.qkv.q_norm_w[i] << 16);
             s_norm[256 + i] = __uint_as_float((uint32_t)P.qkv.k_norm_w[i] << 16);
         }
@@ -920,7 +1036,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_wait(drain, 0, err);
         }
     } else {
-        const int quarter = warp & 3;  // TMEM lanes this warp may access
+        const int quarter = warp & 3;    // TMEM lanes this warp may access
+        const int wg = (warp - 2) >> 2;  // epilogue warpgroup: which column chunks
         const int row = quarter * 32 + lane;
         grid_dep_wait();  // the epilogue reads and writes what the previous kernel may touch
         int use = 0;
@@ -929,11 +1046,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             tile_coords(tile, P.num_m, P.num_n, P.group_m, mb, nb);
             const int acc = use & 1;
             const int m = mb * 2 * BM + (int)rank * BM + row;
-            epilogue_prefetch<BN, EPI, D>(P, m, nb * BN, m < P.M);
+            epilogue_prefetch<BN, EPI>(P, m, nb * BN, m < P.M);
             if (!mbar_wait<true>(tfull + acc, (use >> 1) & 1, err)) break;
             tc_fence_after();
             const uint32_t tcol = tmem + ((uint32_t)(quarter * 32) << 16) + acc * ACC;
-            epilogue_tile<BN, EPI, D>(P, tcol, m, nb * BN, m < P.M, s_norm);
+            epilogue_tile<BN, EPI, D>(P, tcol, m, nb * BN, m < P.M, s_norm, wg);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive_cluster(tempty_lead + 8 * acc);
@@ -967,7 +1084,7 @@ cudaError_t run(const GemmProblem &p, const GemmParams &params, int num_sms, cud
     if (e != cudaSuccess) return e;
     // split K: one tile per cluster of KS CTAs; otherwise persistent, one CTA per SM at most
     const int grid = KS > 1 ? params.num_tiles * KS : (params.num_tiles < num_sms ? params.num_tiles : num_sms);
-    LaunchCfg lc(dim3(grid), dim3(kThreads), L::ALLOC, stream, p.pdl != 0, KS);
+    LaunchCfg lc(dim3(grid), dim3(kernel_threads<EPI>()), L::ALLOC, stream, p.pdl != 0, KS);
     e = cudaLaunchKernelEx(&lc.cfg, kern, ta, tb, params);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
@@ -986,7 +1103,7 @@ int cluster_capacity()
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC) == cudaSuccess) {
         cudaLaunchConfig_t cfg{};
         cfg.gridDim = dim3(KS);
-        cfg.blockDim = dim3(kThreads);
+        cfg.blockDim = dim3(kernel_threads<EPI>());
         cfg.dynamicSmemBytes = L::ALLOC;
         cudaLaunchAttribute attr[1];
         attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -1059,14 +1176,14 @@ cudaError_t run_pair(const GemmProblem &p, GemmParams params, int group_m, cudaS
     if (e != cudaSuccess) return e;
     int clusters = 0;
     {
-        LaunchCfg probe(dim3(2), dim3(kThreads), SMEM, stream, false, 2);
+        LaunchCfg probe(dim3(2), dim3(kernel_threads<EPI>()), SMEM, stream, false, 2);
         if (cudaOccupancyMaxActiveClusters(&clusters, kern, &probe.cfg) != cudaSuccess || clusters < 1) {
             cudaGetLastError();
             return cudaErrorNotSupported;
         }
     }
     const int n = params.num_tiles < clusters ? params.num_tiles : clusters;
-    LaunchCfg lc(dim3(2 * n), dim3(kThreads), SMEM, stream, p.pdl != 0, 2);
+    LaunchCfg lc(dim3(2 * n), dim3(kernel_threads<EPI>()), SMEM, stream, p.pdl != 0, 2);
     e = cudaLaunchKernelEx(&lc.cfg, kern, ta, tb, params);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();

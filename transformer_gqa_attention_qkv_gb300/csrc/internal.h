@@ -26,8 +26,9 @@ struct QkvEpilogue {
     const uint16_t *q_norm_w, *k_norm_w;  // [d] bf16, or both NULL
     float eps;
     int rd;                // rotary width: d, d/2, d/4 or 0 (RoPE on features [0, rd))
-    const float2 *rope;    // [rd/2][rope_ld] (cos, sin of pos * theta^(-2i/rd)), pair-major; NULL when rd = 0
-    int rope_ld;           // positions per pair row of rope (>= rope_rows)
+    const float4 *rope;    // [rd/4][rope_ld] quads: (cos, cos, sin, sin) of pos * theta^(-2i/rd) for pairs
+                           // i = 2k, 2k + 1 at entry [k][pos]; NULL when rd = 0
+    int rope_ld;           // positions per quad row of rope (>= rope_rows)
     int rope_rows;         // positions the table covers
     int q_f16;             // 1: Q stored as binary16 (clamped, flagged); 0: bf16
     int kv_f16;            // 1: K and V stored as binary16 (clamped, flagged); 0: bf16
