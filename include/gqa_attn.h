@@ -42,8 +42,9 @@
  *     failing call on the calling thread.
  *   - Supported shapes: hidden a multiple of 8; Hq a multiple of Hkv;
  *     head_dim 64, 80, 96, 128 or 256 for the prefill paths (projection,
- *     attention, layer forward, prefill into a cache), 64 or 128 for decode
- *     and the backward.  Other head_dim values return GQA_ERR_UNSUPPORTED,
+ *     attention, layer forward, prefill into a cache) and for decode over
+ *     bf16 or E4M3 caches, 64, 80, 96 or 128 for the backward.  Other
+ *     head_dim values return GQA_ERR_UNSUPPORTED,
  *     naming the dimension ([Knob] "Where the invariance breaks": head_dim is
  *     a tile dimension of the fused kernels; 80 and 96 run in 128-wide tiles
  *     whose extra columns are zero).
@@ -320,9 +321,9 @@ int gqa_decode_attention_noalloc(const gqa_f16 *q, const gqa_bf16 *k_cache, cons
  * gqa_check_device_error() reports as GQA_ERR_RANGE.  Caches are
  * [B, Hkv, Lmax, head_dim] codes, half the bytes of bf16 caches; everything
  * else (arguments, workspace and its size, positions, statuses) is as for
- * the bf16 functions of the same name without _fp8.  head_dim must be 128
- * (else GQA_ERR_UNSUPPORTED); k_scale and v_scale must be finite and > 0
- * (else GQA_ERR_ARG). */
+ * the bf16 functions of the same name without _fp8.  head_dim must be 64,
+ * 80, 96, 128 or 256 (else GQA_ERR_UNSUPPORTED); k_scale and v_scale must be
+ * finite and > 0 (else GQA_ERR_ARG). */
 typedef uint8_t gqa_e4m3; /* one OCP FP8 E4M3 code */
 
 int gqa_attn_decode_fp8(const gqa_bf16 *x, const gqa_bf16 *Wqkv, const gqa_bf16 *Wo,

@@ -11,7 +11,11 @@ to agreement on all but near-tie elements and to E4M3's half-step bound.
 Checked: the attention stage over ragged lengths and every group size (slots
 past each sequence hold NaN codes, which must not leak), the projection and
 append stage, the whole step on a reduced and on the full Qwen3-8B-shaped
-workload, saturation reporting, and argument checks.
+workload, saturation reporting, and argument checks.  Head widths 64, 80 and
+96 (rows staged as 128 codes, the tensor copy filling codes past d with zeros)
+and 256 (rows of two 128-code boxes): the attention stage and the whole step
+at the widths' workloads ([Knob] "Where the invariance breaks"; [NeoX]
+"Background", Gemma-3's head_dim 256).
 """
 import numpy as np
 import pytest
@@ -71,6 +75,33 @@ def test_decode_attention_fp8_stage(B, Hq, Hkv, Lmax, lens):
     assert gq.gqa_check_device_error() == 0
     ref = oracle.decode_attention_stage_fp8(q, kc, vc, ks, vs, kl, B, Hq, Hkv, d, Lmax)
     assert_parity("fp8 decode attn", to64(out), ref)
+
+
+@pytest.mark.parametrize("d,B,Hq,Hkv,Lmax,lens", [
+    (64, 4, 16, 4, 700, [700, 1, 64, 333]),
+    (80, 3, 32, 8, 500, [500, 65, 2]),
+    (96, 2, 8, 8, 300, [300, 129]),
+    (256, 3, 4, 1, 600, [600, 1, 257]),  # the Gemma-3 head geometry
+    (256, 2, 16, 2, 200, [200, 99]),     # G = 8
+])
+def test_decode_attention_fp8_widths(d, B, Hq, Hkv, Lmax, lens):
+    ks, vs = 2.0 ** -5, 0.03
+    g = torch.Generator().manual_seed(1650 + d + Hq)
+    q = (torch.randn((B, Hq, d), generator=g) * 1.5).to(torch.float16)
+    kc = quantize(torch.randn((B, Hkv, Lmax, d), generator=g), ks)
+    vc = quantize(torch.randn((B, Hkv, Lmax, d), generator=g), vs)
+    for b, n in enumerate(lens):  # never-written slots: NaN codes
+        if n < Lmax:
+            kc[b, :, n:] = NAN_CODE
+            vc[b, :, n:] = NAN_CODE
+    kl = torch.tensor(lens, dtype=torch.int32)
+    out = torch.empty((B, Hq * d), dtype=torch.bfloat16, device=DEV)
+    ws = gq.new_workspace(gq.gqa_decode_attention_workspace_size(B, Hq, Hkv, d, Lmax))
+    gq.gqa_decode_attention_fp8(dev(q), dev(kc), dev(vc), ks, vs, dev(kl), B, Hq, Hkv, d, Lmax, out, ws)
+    torch.cuda.synchronize()
+    assert gq.gqa_check_device_error() == 0
+    ref = oracle.decode_attention_stage_fp8(q, kc, vc, ks, vs, kl, B, Hq, Hkv, d, Lmax)
+    assert_parity(f"fp8 decode attn d{d}", to64(out), ref)
 
 
 def _check_appended(name, codes_gpu, ref_vals, ref_codes, scale):
@@ -151,6 +182,25 @@ def test_decode_fp8_step(name, over):
     assert_parity("out", to64(out), ref["out"])
 
 
+@pytest.mark.parametrize("name,cfg", [
+    ("qwen3_0p6b_d64", DecodeConfig("t", 8, 700, 1024, 16, 8, 64, True, 1e6, Lmax=720)),
+    ("qwen3_4b_d80", DecodeConfig("t", 16, 2000, 2560, 32, 8, 80, True, 1e6, Lmax=2048)),
+    ("knob_d96", DecodeConfig("t", 8, 1000, 3072, 32, 8, 96, True, 1e6, Lmax=1024)),
+    ("gemma3_d256", DecodeConfig("t", 8, 3000, 640, 4, 1, 256, True, 1e6, Lmax=3072)),
+])
+def test_decode_fp8_step_widths(name, cfg):
+    ks, vs = 2.0 ** -5, 2.0 ** -5
+    t = make_decode_inputs(cfg, seed=1850 + cfg.head_dim)
+    cl = torch.tensor([(cfg.cache_len * (b + 1)) // cfg.B - b for b in range(cfg.B)], dtype=torch.int32)
+    kc8, vc8 = fp8_caches(cfg, t, ks, vs, lens=None)
+    out, attn = _run_step(cfg, t, kc8, vc8, ks, vs, cl)
+    assert gq.gqa_check_device_error() == 0
+    ref = oracle.decode_fp8(t["x"], t["Wqkv"], t["Wo"], t["q_norm_w"], t["k_norm_w"], cfg.rope_theta, cfg.eps,
+                            cfg.B, cfg.hidden, cfg.Hq, cfg.Hkv, cfg.head_dim, kc8, vc8, ks, vs, cl, cfg.lmax)
+    assert_parity(f"{name} fp8 attn", to64(attn), ref["attn"])
+    assert_parity(f"{name} fp8 out", to64(out), ref["out"])
+
+
 def test_fp8_saturation_is_reported():
     cfg = DECODE_CONFIGS["qwen3_8b_decode"].with_(B=2, cache_len=40, Lmax=64)
     t = make_decode_inputs(cfg, seed=1900)
@@ -162,13 +212,13 @@ def test_fp8_saturation_is_reported():
 
 
 def test_fp8_argument_checks():
-    q = torch.zeros((1, 8, 64), dtype=torch.float16, device=DEV)
-    c = torch.zeros((1, 1, 16, 64), dtype=torch.uint8, device=DEV)
+    q = torch.zeros((1, 8, 160), dtype=torch.float16, device=DEV)
+    c = torch.zeros((1, 1, 16, 160), dtype=torch.uint8, device=DEV)
     kl = torch.ones(1, dtype=torch.int32, device=DEV)
-    out = torch.empty((1, 8 * 64), dtype=torch.bfloat16, device=DEV)
+    out = torch.empty((1, 8 * 160), dtype=torch.bfloat16, device=DEV)
     ws = gq.new_workspace(1 << 20)
     with pytest.raises(gq.GqaError, match=f"status {gq.GQA_ERR_UNSUPPORTED}"):
-        gq.gqa_decode_attention_fp8(q, c, c, 1.0, 1.0, kl, 1, 8, 1, 64, 16, out, ws)
+        gq.gqa_decode_attention_fp8(q, c, c, 1.0, 1.0, kl, 1, 8, 1, 160, 16, out, ws)
     q = torch.zeros((1, 8, 128), dtype=torch.float16, device=DEV)
     c = torch.zeros((1, 1, 16, 128), dtype=torch.uint8, device=DEV)
     out = torch.empty((1, 8 * 128), dtype=torch.bfloat16, device=DEV)

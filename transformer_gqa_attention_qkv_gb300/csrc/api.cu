@@ -1233,7 +1233,9 @@ static int check_fp8(int d, float k_scale, float v_scale)
 {
     if (!(k_scale > 0.0f) || !(v_scale > 0.0f) || !isfinite(k_scale) || !isfinite(v_scale))
         return fail(GQA_ERR_ARG, "k_scale and v_scale must be finite and > 0");
-    if (d != 128) return fail(GQA_ERR_UNSUPPORTED, "E4M3 caches support head_dim 128 (got %d)", d);
+    if (d != 64 && d != 80 && d != 96 && d != 128 && d != 256)
+        return fail(GQA_ERR_UNSUPPORTED, "unsupported head_dim for E4M3 caches: %d (supported: 64, 80, 96, 128, 256)",
+                    d);
     return GQA_OK;
 }
 

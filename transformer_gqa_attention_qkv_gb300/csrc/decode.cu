@@ -64,12 +64,12 @@ constexpr int kGroup = 4;      // consumer warps per chunk, 16 keys each
 // GM: query heads per work item (rows of the per-warp partials).
 template <int D, int GM, bool F8 = false, int CW = kGroup>
 struct DSmem {
-    static constexpr int NCH = F8 ? 1 : (D + 63) / 64;  // 128-byte boxes per row: 64-wide d chunks, or 128 codes
+    static constexpr int NCH = F8 ? D / 128 : (D + 63) / 64;  // 128-byte boxes per row: 64-wide d chunks, or 128 codes
     static constexpr int BOX = kChunk * 128;       // one 64-key x 128-byte swizzled box (8 KB)
     static constexpr int CB = NCH * BOX;           // one K (or V) chunk
     // a multiple of the group count: stage s then always serves group s % (CW / kGroup),
     // so a group waiting for a stage's next fill has consumed its previous one
-    static constexpr int STAGES = F8 ? 12 : (NCH == 4 ? 3 : NCH == 2 ? 6 : 12);
+    static constexpr int STAGES = F8 ? (NCH == 2 ? 6 : 12) : (NCH == 4 ? 3 : NCH == 2 ? 6 : 12);
     static constexpr int K = 0;
     static constexpr int V = STAGES * CB;
     static constexpr int RED = 2 * STAGES * CB;    // [CW][GM][D + 2] floats
@@ -126,6 +126,13 @@ DEVI uint32_t swz(int key, int dcol)
 DEVI uint32_t swz8(int key, int byte)
 {
     return (uint32_t)(key * 128 + ((((byte >> 4) ^ (key & 7))) << 4) + (byte & 15));
+}
+
+// Byte offset of 16-byte block blk (codes 16 blk ..) of key `key` inside an
+// E4M3 chunk stored as 128-byte boxes (rows of 256 codes take two).
+DEVI uint32_t f8_off(int key, int blk)
+{
+    return (uint32_t)((blk >> 3) * (kChunk * 128)) + swz8(key, (blk & 7) * 16);
 }
 
 DEVI uint32_t bf16x2_bits(float lo, float hi) { return pack_bf16(lo, hi); }
@@ -187,11 +194,13 @@ DEVI void softmax_step(const float (&v)[4], float &m_run, float &l_run, float &a
 
 // Merge of the consumer warps' per-head (o, max, sum) rows in `red` into the
 // item's partial record: o = sum_w 2^(m_w - M) o_w, l likewise, M = max_w m_w.
-template <int D, int GM, int CW>
+// Records hold the DR real columns of each head (DR < D: rows staged wider,
+// with zero columns past DR).
+template <int D, int GM, int CW, int DR = D>
 DEVI void write_record(const float *red, float *rec, int Gv)
 {
-    for (int idx = threadIdx.x - 32; idx < Gv * D; idx += CW * 32) {
-        const int h = idx / D, c = idx - h * D;
+    for (int idx = threadIdx.x - 32; idx < Gv * DR; idx += CW * 32) {
+        const int h = idx / DR, c = idx - h * DR;
         float M = -INFINITY;
 #pragma unroll
         for (int w = 0; w < CW; ++w) M = fmaxf(M, red[(w * GM + h) * (D + 2) + D]);
@@ -204,10 +213,10 @@ DEVI void write_record(const float *red, float *rec, int Gv)
             acc = fmaf(f, rr[c], acc);
             lsum = fmaf(f, rr[D + 1], lsum);
         }
-        rec[h * (D + 2) + c] = acc;
+        rec[h * (DR + 2) + c] = acc;
         if (c == 0) {
-            rec[h * (D + 2) + D] = M;
-            rec[h * (D + 2) + D + 1] = lsum;
+            rec[h * (DR + 2) + DR] = M;
+            rec[h * (DR + 2) + DR + 1] = lsum;
         }
     }
 }
@@ -511,13 +520,14 @@ DEVI void consume_bf16_t(const DecodeAttentionProblem &P, uint8_t *smem, uint64_
 // holds d = 16b + 2grp and 16b + 2grp + 1) and are put back in order when
 // written to shared memory.  P stays <= 2^8 (lazy running max), exact in
 // binary16's range, so O is rescaled rarely.
-template <int D, int CW>
+template <int D, int CW, int DR = D>
 DEVI void consume_f8(const DecodeAttentionProblem &P, uint8_t *smem, uint64_t *full, uint64_t *empty, float *red,
                      float scale_log2, int n_items, unsigned *err)
 {
     constexpr int GM = 8;
     using L = DSmem<D, GM, true, CW>;
-    static_assert(D == 128, "E4M3 caches: 128-wide heads");
+    static_assert(D == 128 || D == 256, "E4M3 caches: rows of one or two 128-code boxes");
+    static_assert(DR <= D && DR % 16 == 0, "real head width");
     constexpr int NG = CW / kGroup;  // chunk it goes to group it % NG
     static_assert(L::STAGES % NG == 0, "each ring stage must belong to one group (phase parity)");
     constexpr int ST = L::STAGES;
@@ -538,11 +548,11 @@ DEVI void consume_f8(const DecodeAttentionProblem &P, uint8_t *smem, uint64_t *f
         const ItemRange r = item_range(P, item, err, false);
         // B fragments of Q^T, d in the order described above
         uint32_t qb[KS][2];
-        const uint16_t *qrow = P.q + (size_t)(r.b * P.Hq + r.vg * Gv + (head_valid ? grp : 0)) * D;
+        const uint16_t *qrow = P.q + (size_t)(r.b * P.Hq + r.vg * Gv + (head_valid ? grp : 0)) * DR;
 #pragma unroll
         for (int ks = 0; ks < KS; ++ks) {
-            uint2 v = make_uint2(0u, 0u);
-            if (head_valid) v = *reinterpret_cast<const uint2 *>(qrow + ks * 16 + 4 * tig);
+            uint2 v = make_uint2(0u, 0u);  // zero past the real width (the staged codes there are zero too)
+            if (head_valid && ks * 16 < DR) v = *reinterpret_cast<const uint2 *>(qrow + ks * 16 + 4 * tig);
             qb[ks][0] = v.x;
             qb[ks][1] = v.y;
         }
@@ -563,7 +573,7 @@ DEVI void consume_f8(const DecodeAttentionProblem &P, uint8_t *smem, uint64_t *f
 #pragma unroll
             for (int kp = 0; kp < KS / 2; ++kp) {
                 uint32_t rk[4];  // (keys 0-7, block 2kp), (8-15, 2kp), (0-7, 2kp+1), (8-15, 2kp+1)
-                ldsm_x4(kb + swz8(f8_key, (2 * kp + f8_blk) * 16), rk[0], rk[1], rk[2], rk[3]);
+                ldsm_x4(kb + f8_off(f8_key, 2 * kp + f8_blk), rk[0], rk[1], rk[2], rk[3]);
 #pragma unroll
                 for (int j = 0; j < 2; ++j) {
                     uint32_t lo0, hi0, lo1, hi1;
@@ -610,7 +620,7 @@ DEVI void consume_f8(const DecodeAttentionProblem &P, uint8_t *smem, uint64_t *f
 #pragma unroll
             for (int j2 = 0; j2 < D / 32; ++j2) {
                 uint32_t rv[4];  // (keys 0-7, block 2j2), (8-15, 2j2), (0-7, 2j2+1), (8-15, 2j2+1)
-                ldsm_x4_trans(vb + swz8(f8_key, (2 * j2 + f8_blk) * 16), rv[0], rv[1], rv[2], rv[3]);
+                ldsm_x4_trans(vb + f8_off(f8_key, 2 * j2 + f8_blk), rv[0], rv[1], rv[2], rv[3]);
 #pragma unroll
                 for (int x = 0; x < 2; ++x) {
                     // bytes (k c, k c+1, k+1 c, k+1 c+1) -> (k c, k+1 c | k c+1, k+1 c+1)
@@ -647,12 +657,12 @@ DEVI void consume_f8(const DecodeAttentionProblem &P, uint8_t *smem, uint64_t *f
             }
         }
         consumer_sync<CW>();
-        write_record<D, GM, CW>(red, P.partials + (size_t)r.rec * Gv * (D + 2), Gv);
+        write_record<D, GM, CW, DR>(red, P.partials + (size_t)r.rec * Gv * (DR + 2), Gv);
         consumer_sync<CW>();  // red is reused by the next item
     }
 }
 
-template <int D, int GM, bool F8, int CW>
+template <int D, int GM, bool F8, int CW, int DR>
 __global__ void __launch_bounds__(32 * (1 + CW), 1)
     decode_split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                         const DecodeAttentionProblem P, float scale_log2, int n_items, unsigned *err)
@@ -698,9 +708,10 @@ __global__ void __launch_bounds__(32 * (1 + CW), 1)
                     }
                     // whole boxes are transferred (rows past Lmax read as zero)
                     mbar_arrive_expect_tx(full + s, 2 * L::CB);
-                    for (int c = 0; c < L::NCH; ++c) {
-                        tma_load_3d(smem + L::K + s * L::CB + c * L::BOX, &tmK, c * 64, u0, z, full + s);
-                        tma_load_3d(smem + L::V + s * L::CB + c * L::BOX, &tmV, c * 64, u0, z, full + s);
+                    for (int c = 0; c < L::NCH; ++c) {  // 128-byte boxes: 64 bf16 values or 128 codes
+                        const int x = c * (F8 ? 128 : 64);
+                        tma_load_3d(smem + L::K + s * L::CB + c * L::BOX, &tmK, x, u0, z, full + s);
+                        tma_load_3d(smem + L::V + s * L::CB + c * L::BOX, &tmV, x, u0, z, full + s);
                     }
                 }
             }
@@ -709,7 +720,7 @@ __global__ void __launch_bounds__(32 * (1 + CW), 1)
         return;  // the producer takes no part in the consumer barriers below
     }
     if constexpr (F8)
-        consume_f8<D, CW>(P, smem, full, empty, red, scale_log2, n_items, err);
+        consume_f8<D, CW, DR>(P, smem, full, empty, red, scale_log2, n_items, err);
     else if constexpr (GM == 8)
         consume_bf16_t<D, CW>(P, smem, full, empty, red, scale_log2, n_items, err);
     else
@@ -770,14 +781,18 @@ __global__ void __launch_bounds__(kCombineThreads) decode_combine_kernel(const D
     }
 }
 
-template <int D, int GM, bool F8, int CW = (F8 ? 8 : 4)>
+// D: the staged row width; DR: the head's real width (E4M3 rows narrower than
+// 128 codes are staged 128 wide, the tensor copy filling codes past DR with
+// zeros).
+template <int D, int GM, bool F8, int CW = (F8 ? 8 : 4), int DR = D>
 cudaError_t run_decode(const DecodeAttentionProblem &p0, unsigned *err, cudaStream_t stream)
 {
+    static_assert(F8 || DR == D, "bf16 caches are staged at their own width");
     using L = DSmem<D, GM, F8, CW>;
     DecodeAttentionProblem p = p0;
     p.vsub = decode_head_subgroups(p.Hq / p.Hkv, GM);
     // E4M3 keys are code * k_scale: the scale joins the softmax scale
-    const float scale_log2 = 1.4426950408889634f / sqrtf((float)D) * (F8 ? p.k_scale : 1.0f);
+    const float scale_log2 = 1.4426950408889634f / sqrtf((float)DR) * (F8 ? p.k_scale : 1.0f);
     const int n_items = p.B * p.Hkv * p.vsub * p.splits;
     int dev = 0, sms = 148;
     cudaGetDevice(&dev);
@@ -785,12 +800,12 @@ cudaError_t run_decode(const DecodeAttentionProblem &p0, unsigned *err, cudaStre
     // caches viewed as [B*Hkv, Lmax, D]; box {128 bytes, 64 keys, 1}, 128-byte swizzle
     CUtensorMap tk, tv;
     const int eb = F8 ? 1 : 2;
-    const uint64_t dims[3] = {(uint64_t)D, (uint64_t)p.Lmax, (uint64_t)p.B * p.Hkv};
-    const uint64_t strides[2] = {(uint64_t)D * eb, (uint64_t)p.Lmax * D * eb};
+    const uint64_t dims[3] = {(uint64_t)DR, (uint64_t)p.Lmax, (uint64_t)p.B * p.Hkv};
+    const uint64_t strides[2] = {(uint64_t)DR * eb, (uint64_t)p.Lmax * DR * eb};
     const uint32_t box[3] = {(uint32_t)(128 / eb), (uint32_t)kChunk, 1};
     if (encode_tmap(&tk, p.k_cache, 3, dims, strides, box, true, eb) != CUDA_SUCCESS) return cudaErrorInvalidValue;
     if (encode_tmap(&tv, p.v_cache, 3, dims, strides, box, true, eb) != CUDA_SUCCESS) return cudaErrorInvalidValue;
-    auto kern = decode_split_kernel<D, GM, F8, CW>;
+    auto kern = decode_split_kernel<D, GM, F8, CW, DR>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC);
     if (e != cudaSuccess) return e;
     const int grid = n_items < sms ? n_items : sms;
@@ -804,7 +819,7 @@ cudaError_t run_decode(const DecodeAttentionProblem &p0, unsigned *err, cudaStre
     // the combine follows the split kernel as its programmatic dependent
     if ((size_t)(p.Hq / p.Hkv / p.vsub) * p.splits > (size_t)kCombineMaxW) return cudaErrorInvalidValue;
     LaunchCfg lc(dim3(p.B * p.Hkv * p.vsub), dim3(kCombineThreads), 0, stream, true);
-    e = cudaLaunchKernelEx(&lc.cfg, decode_combine_kernel<D>, p);
+    e = cudaLaunchKernelEx(&lc.cfg, decode_combine_kernel<DR>, p);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
@@ -851,7 +866,14 @@ cudaError_t launch_decode_attention(const DecodeAttentionProblem &p, unsigned *e
 {
     if (p.Hkv <= 0 || p.Hq % p.Hkv) return cudaErrorInvalidValue;
     const int G = p.Hq / p.Hkv;
-    if (p.fp8) return p.d == 128 ? run_decode<128, 8, true>(p, err, stream) : cudaErrorInvalidValue;
+    if (p.fp8) {
+        if (p.d == 128) return run_decode<128, 8, true>(p, err, stream);
+        if (p.d == 64) return run_decode<128, 8, true, 8, 64>(p, err, stream);
+        if (p.d == 80) return run_decode<128, 8, true, 8, 80>(p, err, stream);
+        if (p.d == 96) return run_decode<128, 8, true, 8, 96>(p, err, stream);
+        if (p.d == 256) return run_decode<256, 8, true, 4>(p, err, stream);  // one group: registers and partials
+        return cudaErrorInvalidValue;
+    }
     if (p.d == 128) return G <= 8 ? run_decode<128, 8, false>(p, err, stream) : run_decode<128, 16, false>(p, err, stream);
     if (p.d == 64) return G <= 8 ? run_decode<64, 8, false>(p, err, stream) : run_decode<64, 16, false>(p, err, stream);
     if (p.d == 80) return G <= 8 ? run_decode<80, 8, false>(p, err, stream) : run_decode<80, 16, false>(p, err, stream);
