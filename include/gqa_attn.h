@@ -161,7 +161,8 @@ int gqa_qkv_proj(const gqa_bf16 *x, const gqa_bf16 *Wqkv,
  * softmax and accumulation ([T07] §4 step 6; [NeoX] "Scaling and RoPE"):
  *   q [B, Hq, S, head_dim], k and v [B, Hkv, S, head_dim], binary16
  *   attn_out [B, S, Hq*head_dim], bf16 ([NeoX] "Attention output flattening").
- * Supported group sizes Hq/Hkv: powers of two up to 128. */
+ * Supported group sizes Hq/Hkv: up to 128 (a query tile packs floor(128/G)
+ * positions of each of the G heads). */
 int gqa_attention(const gqa_f16 *q, const gqa_f16 *k, const gqa_f16 *v,
                   int B, int S, int Hq, int Hkv, int head_dim, int causal,
                   gqa_bf16 *attn_out, void *stream);
@@ -407,7 +408,7 @@ int gqa_decode_qkv_rd(const gqa_bf16 *x, const gqa_bf16 *Wqkv,
  * The forward is recomputed (Q, K, V, the attention's per-row log-sum-exp);
  * the attention backward recomputes its probabilities from them.  Full
  * rotary (the *_rd forms below take a rotary width); head_dim 64, 80, 96 or
- * 128; Hq/Hkv a power of two up to 32, else GQA_ERR_UNSUPPORTED (head_dim
+ * 128; Hq/Hkv up to 32, else GQA_ERR_UNSUPPORTED (head_dim
  * 256: the dK and dV accumulators of a 128-key block would fill all 512 TMEM
  * columns).  dx must not overlap x or dout.  workspace: at least
  * gqa_attn_backward_workspace_size(...) bytes, 256-byte aligned.  Enqueued on

@@ -45,6 +45,14 @@ def f16_randn(shape, gen, std=1.0):
     (1, 260, 32, 1, 128, True),   # G = 32 (4 positions per query tile)
     (1, 256, 8, 2, 128, False),   # no mask, no ragged edge: every tile unmasked
     (2, 1024, 8, 1, 64, True),    # many tiles per CTA (both operand rings wrap often)
+    # group sizes that are not powers of two: R = floor(128/G) rounded down to a
+    # multiple of 4 positions per head, so a tile packs G*R < 128 query rows
+    (1, 300, 24, 8, 128, True),   # G = 3: 40 positions x 3 heads = 120 rows
+    (2, 257, 10, 2, 64, True),    # G = 5: 24 x 5 = 120
+    (1, 333, 40, 8, 128, True),   # G = 5 (Hq = 40, Hkv = 8)
+    (1, 200, 12, 2, 128, False),  # G = 6: 20 x 6 = 120, no mask
+    (1, 129, 7, 1, 64, True),     # G = 7: 16 x 7 = 112
+    (1, 150, 24, 1, 128, True),   # G = 24: 4 x 24 = 96
 ])
 def test_attention_backward_stage(B, S, Hq, Hkv, d, causal):
     g = torch.Generator().manual_seed(3000 + S)
@@ -83,6 +91,8 @@ def test_attention_backward_stage(B, S, Hq, Hkv, d, causal):
      True),
     ({"B": 1, "S": 200, "hidden": 384, "Hq": 8, "Hkv": 1, "head_dim": 128, "qk_norm": True, "rope_theta": 1e6},
      False),
+    ({"B": 1, "S": 260, "hidden": 640, "Hq": 10, "Hkv": 2, "head_dim": 64, "qk_norm": True, "rope_theta": 1e6},
+     True),  # G = 5
 ])
 def test_layer_backward(geom, causal):
     cfg = LayerConfig("t", **geom)

@@ -224,15 +224,6 @@ static int check_group(int Hq, int Hkv)
     return GQA_OK;
 }
 
-// The backward packs 128 / G positions per tile with power-of-two index masks.
-static int check_group_pow2(int Hq, int Hkv)
-{
-    const int G = Hq / Hkv;
-    if ((G & (G - 1)) || G > 128)
-        return fail(GQA_ERR_UNSUPPORTED, "unsupported group size Hq/Hkv=%d (a power of two up to 128)", G);
-    return GQA_OK;
-}
-
 // rotary_dim: even, in [0, head_dim]; the kernels implement d, d/2, d/4 and 0.
 static int check_rotary(int rd, int d)
 {
@@ -677,7 +668,6 @@ static int check_backward(int B, int S, int hidden, int Hq, int Hkv, int d, cons
 {
     int rc = check_layer(B, S, hidden, Hq, Hkv, d, qn, kn);
     if (rc) return rc;
-    if ((rc = check_group_pow2(Hq, Hkv))) return rc;
     if (d != 64 && d != 80 && d != 96 && d != 128)
         return fail(GQA_ERR_UNSUPPORTED, "the backward supports head_dim 64, 80, 96 and 128 (got %d)", d);
     if (Hq / Hkv > 32)

@@ -64,7 +64,8 @@ struct BSmem {
     static constexpr int BARS = ROWS + 2 * 2 * kRows * 4;
     static constexpr int NBARS = 10;
     static constexpr int TMEM_SLOT = BARS + NBARS * 8;
-    static constexpr int TOTAL = TMEM_SLOT + 16;
+    static constexpr int COLS = TMEM_SLOT + 16;   // dkdv: position of each packed query row in its tile, -1: none
+    static constexpr int TOTAL = COLS + kRows * 4;
     static constexpr int ALLOC = TOTAL + 1024;
 };
 
@@ -191,7 +192,9 @@ DEVI void p_ds64(uint32_t tS, uint32_t tdP, float sl, const float *lse_c, const 
 // S(i, h) is S and dP of half h and acc(i, h) the products that consume P and
 // dS of half h.  The MMAs of one CTA run in issue order, so S(i + 1, h) reuses
 // the columns acc(i, h) reads.
-template <int D, bool DKDV>
+// PACKED: G*R = 128 (G a power of two), every row of a query tile a real
+// query (the masks are index arithmetic); otherwise rows past G*R are padding.
+template <int D, bool DKDV, bool PACKED>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmG,
@@ -238,6 +241,30 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_prefetch_desc(&tmG);
     }
     if (warp == 1) tmem_alloc(tmem_slot, 512);
+    // A tile packs G heads x R positions = G*R <= 128 query rows.  dkdv: its
+    // query rows are the columns of S^T and dP^T and are summed over in dV and
+    // dK, so the ring's Q and dO rows and lse and D entries past G*R (never
+    // written by the tensor copies) are zeroed once (finite S, dP and D there,
+    // so P = 0 from the column table's mask gives dS = 0), and the column
+    // table marks them.
+    int *colpos = reinterpret_cast<int *>(smem + L::COLS);
+    if (DKDV && !PACKED) {
+        const int packed = P.G * P.R;
+        for (int i = threadIdx.x; i < kRows; i += kThreads) colpos[i] = i < packed ? i - (i / P.R) * P.R : -1;
+        const int pad = kRows - packed;
+        float *rows_all = reinterpret_cast<float *>(smem + L::ROWS);  // [stage][lse, D][128]
+        for (int idx = threadIdx.x; idx < 2 * 2 * pad; idx += kThreads)
+            rows_all[(idx / pad) * kRows + packed + idx % pad] = 0.0f;
+        for (int idx = threadIdx.x; idx < 2 * 2 * NCH * pad * 8; idx += kThreads) {
+            int rest = idx / 8;
+            const int unit = idx % 8, row = packed + rest % pad;
+            rest /= pad;
+            const int c = rest % NCH, tile = rest / NCH;  // tile: stage * 2 + (Q or dO)
+            *reinterpret_cast<uint4 *>(smem + L::RING + tile * L::TILE + c * L::CH + row * 128 + unit * 16) =
+                make_uint4(0u, 0u, 0u, 0u);
+        }
+        fence_proxy_async_smem();  // the tensor core reads these rows through the async proxy
+    }
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
@@ -245,7 +272,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp == 0) {
         if (lane == 0) {
-            mbar_arrive_expect_tx(fix_full, 2 * L::TILE + (DKDV ? 0 : 2 * kRows * 4));
+            // a query tile's copies bring its G*R packed rows (of Q, dO, lse and D) only
+            const uint32_t packed = (uint32_t)(P.G * P.R);
+            const uint32_t qtile = NCH * 128 * packed, qrows = 2 * packed * 4;
+            mbar_arrive_expect_tx(fix_full, DKDV ? 2 * L::TILE : 2 * qtile + qrows);
             for (int c = 0; c < NCH; ++c) {
                 if (DKDV) {
                     tma_load_3d(smem + L::A0 + c * L::CH, &tmK, c * 64, u0, kvhead, fix_full);
@@ -263,7 +293,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (; it < n_it; ++it) {
                 const int s = it & 1;
                 if (!mbar_wait(ring_empty + s, ((it >> 1) & 1) ^ 1, err)) break;
-                mbar_arrive_expect_tx(ring_full + s, 2 * L::TILE + (DKDV ? 2 * kRows * 4 : 0));
+                mbar_arrive_expect_tx(ring_full + s, DKDV ? 2 * qtile + qrows : 2 * L::TILE);
                 uint8_t *st = smem + L::RING + s * 2 * L::TILE;
                 if (DKDV) {
                     const int tt = (qt0 + it) * P.R;
@@ -356,10 +386,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
         const uint32_t tS = tmem + lane_off + 128 * h, tdP = tS + 64;
         const float sl = P.scale_log2;
-        const int rmask = P.R - 1;         // R = 128 / G is a power of two
         const int u = u0 + r;
-        const int hl = r / P.R, t = t0 + (r & rmask);
-        const bool row_ok = t < P.S;
+        const int hl = r / P.R, t = t0 + (PACKED ? (r & (P.R - 1)) : r - hl * P.R);
+        const bool row_ok = (PACKED || hl < P.G) && t < P.S;  // dq: a query row of the tile
         // a wait's outcome is made warp-uniform, so that a timeout never
         // leaves part of a warp before a warp-collective TMEM access
         auto wait_all = [&](uint64_t *bar, uint32_t parity) {
@@ -383,14 +412,24 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const float *rows = rows0 + s * 2 * kRows + kHalf * h;
                 // every (key, query) pair of the half visible: the whole block at
                 // or before the first position of the tile, no ragged edge
-                const bool full = (!P.causal || u0 + kRows - 1 <= tt) && tt + P.R <= P.S && u0 + kRows <= P.S;
+                const bool full = PACKED && (!P.causal || u0 + kRows - 1 <= tt) && tt + P.R <= P.S &&
+                                  u0 + kRows <= P.S;
                 if (full) {
                     p_ds64<true, false>(tS, tdP, sl, rows, rows + kRows, 0.0f, 0.0f, [](int) { return true; });
-                } else {
+                } else if (PACKED) {
                     // column i: packed query row 64h + i at position tt + ((64h + i) mod R)
+                    const int rmask = P.R - 1;  // R = 128 / G is a power of two
                     auto valid = [&](int i) {
                         const int tq = tt + ((kHalf * h + i) & rmask);
                         return tq < P.S && u < P.S && (!P.causal || u <= tq);
+                    };
+                    p_ds64<true, true>(tS, tdP, sl, rows, rows + kRows, 0.0f, 0.0f, valid);
+                } else {
+                    // column i: packed query row 64h + i at position tt + ((64h + i) mod R), if any
+                    auto valid = [&](int i) {
+                        const int po = colpos[kHalf * h + i];
+                        const int tq = tt + po;
+                        return po >= 0 && tq < P.S && u < P.S && (!P.causal || u <= tq);
                     };
                     p_ds64<true, true>(tS, tdP, sl, rows, rows + kRows, 0.0f, 0.0f, valid);
                 }
@@ -458,7 +497,10 @@ template <int D>
 cudaError_t run_bwd(const AttnBwdProblem &p, unsigned *err, cudaStream_t stream)
 {
     using L = BSmem<D>;
-    const int G = p.Hq / p.Hkv, R = kRows / G;
+    // R positions of each of the G heads per tile, a multiple of 4 so that every
+    // tile's first position is 16-byte aligned in the fp32 lse / D rows the
+    // tensor copies read (G <= 32: R >= 4)
+    const int G = p.Hq / p.Hkv, R = (kRows / G) & ~3;
     CUtensorMap tq, tg, tk, tv, tl, td;
     const uint64_t dq_[3] = {(uint64_t)D, (uint64_t)p.S, (uint64_t)p.B * p.Hq};
     const uint64_t sq_[2] = {(uint64_t)D * 2, (uint64_t)p.S * D * 2};
@@ -497,8 +539,9 @@ cudaError_t run_bwd(const AttnBwdProblem &p, unsigned *err, cudaStream_t stream)
     dsum_kernel<D><<<(unsigned)((rows + 7) / 8), 256, 0, stream>>>(p.dO, p.o, p.dsum, p.ld, p.B, p.S, p.Hq);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    auto k1 = attn_bwd_kernel<D, true>;
-    auto k2 = attn_bwd_kernel<D, false>;
+    const bool packed = G * R == kRows;
+    auto k1 = packed ? attn_bwd_kernel<D, true, true> : attn_bwd_kernel<D, true, false>;
+    auto k2 = packed ? attn_bwd_kernel<D, false, true> : attn_bwd_kernel<D, false, false>;
     if ((e = cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC)) != cudaSuccess) return e;
     if ((e = cudaFuncSetAttribute(k2, cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC)) != cudaSuccess) return e;
     k1<<<p.B * p.Hkv * a.n_kb, kThreads, L::ALLOC, stream>>>(tq, tk, tv, tg, tl, td, a);
@@ -512,7 +555,7 @@ cudaError_t run_bwd(const AttnBwdProblem &p, unsigned *err, cudaStream_t stream)
 cudaError_t launch_attention_backward(const AttnBwdProblem &p, unsigned *err, cudaStream_t stream)
 {
     const int G = p.Hkv > 0 ? p.Hq / p.Hkv : 0;
-    if (G <= 0 || p.Hq % p.Hkv || G > 32 || (G & (G - 1)) || p.ld % 4 || p.ld < p.S) return cudaErrorInvalidValue;
+    if (G <= 0 || p.Hq % p.Hkv || G > 32 || p.ld % 4 || p.ld < p.S) return cudaErrorInvalidValue;
     if (p.d == 128) return run_bwd<128>(p, err, stream);
     if (p.d == 64) return run_bwd<64>(p, err, stream);
     if (p.d == 80) return run_bwd<80>(p, err, stream);
