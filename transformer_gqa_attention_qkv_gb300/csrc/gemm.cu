@@ -898,12 +898,16 @@ __global__ void __launch_bounds__(kernel_threads<EPI>(), 1)
 //                        full)
 //   warps 2.. (both)     epilogue; the accumulator is released by arriving
 //                        on the even CTA's `tempty` (every epilogue warp of both CTAs)
-template <int STAGES, int EPI, int D>
+// BN: N of the pair's MMA, a tile of whole heads (256; 240 = 3 x 80 and
+// 192 = 2 x 96 for the head widths that do not divide 256), half of its B rows
+// staged by each CTA.
+template <int STAGES, int EPI, int D, int BN = 256>
 __global__ void __launch_bounds__(kernel_threads<EPI>(), 1)
     gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                      const GemmParams P)
 {
-    constexpr int BN = 256, BNH = 128;  // N of the pair's MMA; B rows staged by each CTA
+    constexpr int BNH = BN / 2;  // B rows staged by each CTA
+    static_assert(BN % 16 == 0 && BNH % 8 == 0 && BN <= 256, "pair MMA N; whole 8-row swizzle groups per CTA");
     constexpr int A_BYTES = BM * BK * 2, B_BYTES = BNH * BK * 2;
     constexpr int ACC = 256;            // TMEM columns per accumulator
     constexpr int RING = STAGES * (A_BYTES + B_BYTES);
@@ -1149,29 +1153,29 @@ GemmParams make_params(const GemmProblem &p, int BN, unsigned *err)
     return g;
 }
 
-// The pair kernel over 256 x 256 tiles (tile rows of 256 = two CTAs' 128), as
+// The pair kernel over 256 x BN tiles (tile rows of 256 = two CTAs' 128), as
 // many 2-CTA clusters as fit on the GPU at once; returns cudaErrorNotSupported
 // when the cluster shape cannot be placed (the caller then runs the single-SM
 // kernel).
-template <int STAGES, int EPI, int D>
+template <int STAGES, int EPI, int D, int BN = 256>
 cudaError_t run_pair(const GemmProblem &p, GemmParams params, int group_m, cudaStream_t stream)
 {
-    constexpr int SMEM = STAGES * (BM * BK * 2 + 128 * BK * 2) + (2 * STAGES + 5) * 8 + 32 + 2 * 256 * 4 + 1024;
+    constexpr int SMEM = STAGES * (BM * BK * 2 + BN / 2 * BK * 2) + (2 * STAGES + 5) * 8 + 32 + 2 * 256 * 4 + 1024;
     CUtensorMap ta, tb;
     const uint64_t dA[2] = {(uint64_t)p.K, (uint64_t)p.M};
     const uint64_t sA[1] = {(uint64_t)p.K * 2};
     const uint64_t dB[2] = {(uint64_t)p.K, (uint64_t)p.N};
     const uint64_t sB[1] = {(uint64_t)p.K * 2};
     const uint32_t bA[2] = {(uint32_t)BK, (uint32_t)BM};
-    const uint32_t bB[2] = {(uint32_t)BK, 128u};
+    const uint32_t bB[2] = {(uint32_t)BK, (uint32_t)(BN / 2)};
     if (encode_tmap(&ta, p.A, 2, dA, sA, bA, true) != CUDA_SUCCESS) return cudaErrorInvalidValue;
     if (encode_tmap(&tb, p.B, 2, dB, sB, bB, true) != CUDA_SUCCESS) return cudaErrorInvalidValue;
     params.num_m = (p.M + 2 * BM - 1) / (2 * BM);  // pair-tile rows
-    params.num_n = (p.N + 255) / 256;
+    params.num_n = (p.N + BN - 1) / BN;
     params.num_tiles = params.num_m * params.num_n;
     params.group_m = group_m;
     if (!cta_pairs_enabled()) return cudaErrorNotSupported;
-    auto kern = gemm_pair_kernel<STAGES, EPI, D>;
+    auto kern = gemm_pair_kernel<STAGES, EPI, D, BN>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
     if (e != cudaSuccess) return e;
     int clusters = 0;
@@ -1209,7 +1213,7 @@ cudaError_t launch_gemm_qkv(const GemmProblem &p, const QkvEpilogue &e, unsigned
         if (pe != cudaErrorNotSupported) return pe;
         return run<256, 4, EPI_QKV, 128>(p, g, num_sms, stream);
     }
-    if (e.d == 256) {  // one 256-wide head per tile, also for decode-sized problems
+    if (e.d == 256) {  // one 256-wide head per tile (its epilogue sets the pace: the pair form measured 9% slower)
         GemmParams g = make_params(p, 256, err);
         g.qkv = e;
         return run<256, 4, EPI_QKV, 256>(p, g, num_sms, stream);
@@ -1230,11 +1234,19 @@ cudaError_t launch_gemm_qkv(const GemmProblem &p, const QkvEpilogue &e, unsigned
     if (e.d == 80) {
         GemmParams g = make_params(p, 240, err);
         g.qkv = e;
+        if (!small_m) {
+            const cudaError_t pe = run_pair<6, EPI_QKV, 80, 240>(p, g, 16, stream);
+            if (pe != cudaErrorNotSupported) return pe;
+        }
         return run<240, 4, EPI_QKV, 80>(p, g, num_sms, stream);
     }
     if (e.d == 96) {
         GemmParams g = make_params(p, 192, err);
         g.qkv = e;
+        if (!small_m) {
+            const cudaError_t pe = run_pair<6, EPI_QKV, 96, 192>(p, g, 16, stream);
+            if (pe != cudaErrorNotSupported) return pe;
+        }
         return run<192, 4, EPI_QKV, 96>(p, g, num_sms, stream);
     }
     return cudaErrorInvalidValue;
