@@ -35,7 +35,11 @@
 //               split the same way), V fragments from ldmatrix.trans;
 //     E4M3 caches: the transposed products of the first form (up to GM = 8
 //               heads); E4M3 widens exactly to binary16, so the MMAs are
-//               binary16 and the query needs no split.
+//               binary16 and the query needs no split.  Rows of 64, 80 or 96
+//               codes are staged as 128 codes (the tensor copy fills the rest
+//               with zeros, the query is zero-padded alike, and the partial
+//               records keep the real width); rows of 256 codes are two
+//               128-byte boxes, taken by one group of consumer warps.
 //   Online softmax in the accumulator registers in every form.
 //   At the end of an item the warps' (max, sum, unnormalised output) are
 //   merged in shared memory into one fp32 partial record.

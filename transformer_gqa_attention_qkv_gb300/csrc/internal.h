@@ -118,7 +118,7 @@ struct AttentionProblem {
 bool cta_pairs_enabled();
 int set_cta_pairs(int enable);  // returns the previous setting
 cudaError_t launch_attention(const AttentionProblem &p, unsigned *err, int num_sms, cudaStream_t stream);
-// Backward of the attention (head_dim 64 / 128, Hq/Hkv <= 32).  q, k, v, dO
+// Backward of the attention (head_dim 64, 80, 96 or 128, Hq/Hkv <= 32).  q, k, v, dO
 // binary16 head-major ([B, H, S, d]); o the forward's bf16 output [B, S,
 // Hq*d]; lse the forward's log2-sum-exp and dsum a workspace, both fp32
 // [B*Hq, ld] with ld >= S, ld % 4 == 0; dq [B, Hq, S, d], dk/dv [B, Hkv, S, d]
