@@ -512,6 +512,14 @@ const char *gqa_last_error(void);
  * a device where only gqa_decode_attention_noalloc has run. */
 int gqa_check_device_error(void);
 
+/* The same check without synchronising the whole device: waits only for the
+ * work queued on `stream` (a cudaStream_t; NULL: the legacy default stream,
+ * which waits for every blocking stream), then reads and clears the current
+ * device's error words with copies ordered on that stream.  The words are per
+ * device, so an error recorded by another stream's kernel that has already
+ * run is reported here too (and cleared).  Returns as gqa_check_device_error. */
+int gqa_check_stream_error(void *stream);
+
 /* Watchdog self-test: launches one kernel whose mbarrier wait can never
  * complete, with a wait limit of limit_ms milliseconds (1..5000), waits for
  * it, and returns what the kernel reported: GQA_ERR_TIMEOUT when the bounded

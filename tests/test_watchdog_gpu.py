@@ -31,3 +31,30 @@ def test_bounded_wait_reports_timeout_and_device_survives():
 def test_selftest_rejects_bad_limit():
     assert gq.gqa_selftest_bounded_wait(0) == gq.GQA_ERR_ARG
     assert gq.gqa_selftest_bounded_wait(100000) == gq.GQA_ERR_ARG
+
+
+def test_stream_error_check_reports_and_clears():
+    """gqa_check_stream_error waits for one stream only: a projection whose Q/K/V
+    values pass binary16's range (saturated, flagged) on a private stream is
+    reported there, and the word is cleared by the check."""
+    assert gq.gqa_check_device_error() == gq.GQA_OK
+    s = torch.cuda.Stream()
+    B, S, h, Hq, Hkv, d = 1, 128, 64, 1, 1, 64
+    x = torch.full((B, S, h), 2000.0, device="cuda").to(torch.bfloat16)  # q = 2000 * 64 > 65504
+    W = torch.ones(((Hq + 2 * Hkv) * d, h), dtype=torch.bfloat16, device="cuda")
+    q = torch.empty((B, Hq, S, d), dtype=torch.float16, device="cuda")
+    k = torch.empty((B, Hkv, S, d), dtype=torch.float16, device="cuda")
+    v = torch.empty_like(k)
+    s.wait_stream(torch.cuda.current_stream())
+    gq.gqa_qkv_proj(x, W, None, None, 1e4, 1e-6, B, S, h, Hq, Hkv, d, q, k, v, s)
+    assert gq.gqa_check_stream_error(s) == gq.GQA_ERR_RANGE
+    assert "binary16 range" in gq.gqa_last_error()
+    assert gq.gqa_check_stream_error(s) == gq.GQA_OK
+    # saturated, not infinite
+    assert float(v.float().abs().max()) == 65504.0
+    # in range: nothing to report
+    x.fill_(0.5)
+    s.wait_stream(torch.cuda.current_stream())
+    gq.gqa_qkv_proj(x, W, None, None, 1e4, 1e-6, B, S, h, Hq, Hkv, d, q, k, v, s)
+    assert gq.gqa_check_stream_error(s) == gq.GQA_OK
+    assert gq.gqa_check_device_error() == gq.GQA_OK

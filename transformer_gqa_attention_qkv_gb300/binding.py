@@ -30,7 +30,7 @@ EXPORTS = (
     "gqa_attention", "gqa_oproj_residual", "gqa_attn_decode_workspace_size", "gqa_attn_decode",
     "gqa_decode_qkv", "gqa_decode_attention_workspace_size", "gqa_decode_attention",
     "gqa_attn_cost", "gqa_last_error", "gqa_check_device_error", "gqa_selftest_bounded_wait",
-    "gqa_last_launch_count", "gqa_set_cta_pairs", "gqa_decode_attention_noalloc",
+    "gqa_last_launch_count", "gqa_set_cta_pairs", "gqa_decode_attention_noalloc", "gqa_check_stream_error",
     "gqa_attn_prefill_cached_workspace_size", "gqa_attn_prefill_cached", "gqa_attention_cached",
     "gqa_attention_cached_workspace_size",
     "gqa_attn_forward_rd", "gqa_qkv_proj_rd", "gqa_attn_prefill_cached_rd", "gqa_attn_decode_rd",
@@ -82,6 +82,7 @@ def lib():
         "gqa_attn_cost": (_I, [_I] * 7 + [_LLP] * 4),
         "gqa_last_error": (ctypes.c_char_p, []),
         "gqa_check_device_error": (_I, []),
+        "gqa_check_stream_error": (_I, [_P]),
         "gqa_selftest_bounded_wait": (_I, [_I]),
         "gqa_last_launch_count": (_I, []),
         "gqa_set_cta_pairs": (_I, [_I]),
@@ -384,6 +385,11 @@ def gqa_last_error() -> str:
 
 def gqa_check_device_error() -> int:
     return int(lib().gqa_check_device_error())
+
+
+def gqa_check_stream_error(stream=None) -> int:
+    """The device error check, waiting only for `stream` (default: the current stream)."""
+    return int(lib().gqa_check_stream_error(_stream(stream)))
 
 
 def gqa_selftest_bounded_wait(limit_ms: int) -> int:

@@ -1380,6 +1380,16 @@ int gqa_attn_cost(int B, int S, int hidden, int Hq, int Hkv, int head_dim, int c
 
 // --------------------------------------------------------------- diagnostics
 
+// The status an error word reports (the worst of its bits first).
+static int error_word_status(unsigned word)
+{
+    if (word & kErrTimeout) return fail(GQA_ERR_TIMEOUT, "a bounded device wait gave up (error word 0x%x)", word);
+    if (word & kErrIndex) return fail(GQA_ERR_ARG, "a device-side index check failed (error word 0x%x)", word);
+    if (word & kErrRange)
+        return fail(GQA_ERR_RANGE, "a Q/K/V value beyond the binary16 range was clamped (error word 0x%x)", word);
+    return GQA_OK;
+}
+
 int gqa_check_device_error(void)
 {
     int dev = 0;
@@ -1407,11 +1417,33 @@ int gqa_check_device_error(void)
         }
     }
     word |= noalloc_take_error_word(dev);
-    if (word & kErrTimeout) return fail(GQA_ERR_TIMEOUT, "a bounded device wait gave up (error word 0x%x)", word);
-    if (word & kErrIndex) return fail(GQA_ERR_ARG, "a device-side index check failed (error word 0x%x)", word);
-    if (word & kErrRange)
-        return fail(GQA_ERR_RANGE, "a Q/K/V value beyond the binary16 range was clamped (error word 0x%x)", word);
-    return GQA_OK;
+    return error_word_status(word);
+}
+
+int gqa_check_stream_error(void *stream)
+{
+    const cudaStream_t s = (cudaStream_t)stream;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= 64) return fail(GQA_ERR_CUDA, "device index %d out of range", dev);
+    bool have_state;
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        have_state = g_dev[dev].init;
+    }
+    unsigned word = 0;
+    if (have_state) {
+        DeviceState &st = g_dev[dev];
+        // after the stream's queued work; the stream alone is waited for
+        if ((e = cudaMemcpyAsync(&word, st.err, sizeof word, cudaMemcpyDeviceToHost, s)) != cudaSuccess ||
+            (e = cudaStreamSynchronize(s)) != cudaSuccess)
+            return cuda_fail(e, "reading the error word on the stream");
+        if (word && (e = cudaMemsetAsync(st.err, 0, sizeof word, s)) != cudaSuccess)
+            return cuda_fail(e, "clearing the error word on the stream");
+    }
+    word |= noalloc_take_error_word(dev, s, true);
+    return error_word_status(word);
 }
 
 int gqa_selftest_bounded_wait(int limit_ms)

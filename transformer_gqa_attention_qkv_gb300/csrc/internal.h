@@ -186,9 +186,10 @@ void set_launch_count(int n);
 // cache size): GQA_OK or the status (with the message recorded) it returns.
 int check_decode_attention_args(int B, int Hq, int Hkv, int d, int Lmax);
 // Reads and clears the error word of gqa_decode_attention_noalloc on device
-// `dev` (0 if that entry point never ran there).  Host-synchronous: call with
-// the device idle.  Allocates nothing.
-unsigned noalloc_take_error_word(int dev);
+// `dev` (0 if that entry point never ran there).  Host-synchronous (call with
+// the device idle), or, on_stream, ordered on `stream` and waiting for it
+// alone.  Allocates nothing.
+unsigned noalloc_take_error_word(int dev, cudaStream_t stream = nullptr, bool on_stream = false);
 
 // Launch configuration for cudaLaunchKernelEx: optional thread-block cluster
 // (cluster > 1 CTAs along x) and optional programmatic dependent launch (pdl:

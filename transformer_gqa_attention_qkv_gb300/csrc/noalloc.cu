@@ -85,7 +85,7 @@ int noalloc_setup(NoAllocDevice **out)
 
 }  // namespace
 
-unsigned noalloc_take_error_word(int dev)
+unsigned noalloc_take_error_word(int dev, cudaStream_t stream, bool on_stream)
 {
     if (dev < 0 || dev >= 64) return 0;
     unsigned *err;
@@ -95,6 +95,13 @@ unsigned noalloc_take_error_word(int dev)
         err = g_noalloc_dev[dev].err;
     }
     unsigned word = 0;
+    if (on_stream) {  // ordered on the stream, which alone is waited for
+        if (cudaMemcpyAsync(&word, err, sizeof word, cudaMemcpyDeviceToHost, stream) != cudaSuccess ||
+            cudaStreamSynchronize(stream) != cudaSuccess)
+            return 0;
+        if (word) cudaMemsetAsync(err, 0, sizeof word, stream);
+        return word;
+    }
     if (cudaMemcpy(&word, err, sizeof word, cudaMemcpyDeviceToHost) != cudaSuccess) return 0;
     if (word) cudaMemset(err, 0, sizeof word);
     return word;
