@@ -158,3 +158,15 @@ def test_host_forward_and_training_pair_validate(L):
     assert saved(dout=0) == -1
     assert saved(d=160) == -2
     assert saved() == -5                             # 100 bytes of workspace
+
+
+def test_error_checks_without_a_device(L):
+    """The device error checks report a CUDA failure, not a crash, where no
+    device can be reached."""
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a device is present")
+    assert L.gqa_check_device_error() == L.GQA_ERR_CUDA
+    assert L.gqa_last_error()
+    assert L.lib().gqa_check_stream_error(ctypes.c_void_p(0)) == L.GQA_ERR_CUDA
+    assert L.gqa_last_error()
