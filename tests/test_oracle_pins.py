@@ -310,9 +310,11 @@ def _fwd(cfg, t, **kw):
 def test_forward_equals_library_composition():
     """The whole layer ([T07] §4 steps 1-7, residual as in [NeoX] "Qwen3-0.6B
     example") equals a float64 composition of torch library routines:
-    F.linear, F.rms_norm, complex-multiplication RoPE, scaled_dot_product_attention."""
-    for qk in (True, False):
-        cfg = _tiny(qk_norm=qk)
+    F.linear, F.rms_norm, complex-multiplication RoPE, scaled_dot_product_attention.
+    The last case has five query heads per KV head ([Part]: each KV head serves
+    Hq/Hkv contiguous query heads, a group size that is no power of two)."""
+    for qk, Hq, Hkv in ((True, 4, 2), (False, 4, 2), (True, 10, 2)):
+        cfg = _tiny(qk_norm=qk, Hq=Hq, Hkv=Hkv)
         t = make_layer_inputs(cfg, seed=11, w_std=0.3)
         B, S, h, Hq, Hkv, d = cfg.B, cfg.S, cfg.hidden, cfg.Hq, cfg.Hkv, cfg.head_dim
         x, W, Wo = f64(t["x"]), f64(t["Wqkv"]), f64(t["Wo"])
@@ -870,12 +872,13 @@ def _torch_layer(cfg, t, causal=True, keep=None, kv_round=None, rd=None):
     return leaves, x + F.linear(a, Wo)
 
 
-@pytest.mark.parametrize("qk,causal", [(True, True), (False, True), (True, False)])
-def test_backward_equals_library_autograd(qk, causal):
+@pytest.mark.parametrize("qk,causal,Hq", [(True, True, 4), (False, True, 4), (True, False, 4), (True, True, 10)])
+def test_backward_equals_library_autograd(qk, causal, Hq):
     """Every gradient of the layer (x, Wqkv, Wo, both norm weights, and the
     attention's inputs/outputs) equals torch's float64 autograd through the
-    library composition; K/V gradients include the sum over a group's heads."""
-    cfg = _tiny(qk_norm=qk)
+    library composition; K/V gradients include the sum over a group's heads
+    (two heads per group, and five in the last case)."""
+    cfg = _tiny(qk_norm=qk, Hq=Hq)
     t = make_layer_inputs(cfg, seed=51, w_std=0.3)
     dout = bf16(np.random.default_rng(51).standard_normal((cfg.B * cfg.S, cfg.hidden)))
     keep = {}
